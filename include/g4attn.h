@@ -1,0 +1,165 @@
+/*
+ * g4attn — batch-invariant hybrid decoder attention for Gemma-4-31B-class models on one
+ * NVIDIA GB300 (sm_103a). C ABI: plain pointers and sizes only.
+ *
+ * What it computes. The attention cores of the RL-Kernel RFC "[RFC][Gemma-4-31B-it]
+ * [CUDA/ROCm] WS1/WS2 kernel roadmap, ablation matrix and integration plan":
+ *   - section 2, "Checkpoint fingerprint" table: 32 query heads; sliding layers with 16 KV
+ *     heads of dim 256, window 1024, standard RoPE theta 1e4; global layers with 4 KV heads
+ *     of dim 512, K==V (attention_k_eq_v), proportional p-RoPE, partial factor 0.25,
+ *     theta 1e6; 262144 positions;
+ *   - section 5, work-item rows sliding_rope_d256, global_proportional_p_rope,
+ *     sliding_attention_core, global_attention_core, hybrid_kv_cache_contract and
+ *     global_k_eq_v_projection;
+ *   - section 4, "Numerical contract": fixed fp32 accumulation; a reduction order that does
+ *     not depend on batch size, batch position, packing, launch geometry, SM count or
+ *     occupancy; no dynamic split-KV and no cross-CTA atomics in the arithmetic; no TF32 or
+ *     fast-math; casts only at declared points; unsupported geometry fails closed; runtime
+ *     provenance.
+ *
+ * Arithmetic (fixed for every call):
+ *   q' = RoPE(q, pos), k' = RoPE(k, pos) on the leading R half-split pairs (element t pairs
+ *   with t + D/2; pair t turns by pos * theta^(-2t/D); R = D/2 on sliding layers, D/8 on
+ *   global ones; the other pairs pass unchanged). Query i sees keys j <= i, and on sliding
+ *   layers only i - j <= window - 1. o_i = sum_j softmax_j(scale * q'_i . k'_j) v_j, with
+ *   v_j = the stored V (sliding) or the stored un-rotated S (global, K==V).
+ *   Declared bf16 (round-to-nearest-even) casts: roped q, roped sliding K written to the
+ *   cache, roped global K columns, the softmax probabilities P before P.V, and the output.
+ *   Everything else accumulates in fp32.
+ *
+ * Memory. Every tensor is a device buffer owned by the caller. The library allocates no
+ * device memory: its only device-side state is static (the RoPE cos/sin tables, filled once
+ * per device on the first call, and one 32-bit error word). All calls are stream-ordered
+ * on `stream` (a cudaStream_t; NULL = the legacy default stream) and never synchronise,
+ * except g4attn_status_sync.
+ *
+ * Layouts (row-major, bf16 = IEEE bfloat16 in 2 bytes):
+ *   q, out         [T][n_q_heads][head_dim]           query rows / output rows
+ *   k, v           [T][n_kv_heads][head_dim]          new key / value rows of a prefill
+ *   k_new, v_new   [B][n_kv_heads][head_dim]          the decode token's key / value
+ *   cache->k       [num_pages][n_kv_heads][page_size][head_dim]  sliding K' (roped) or
+ *                                                    global S (un-rotated, K==V)
+ *   cache->v       same shape; sliding V; NULL on global layers
+ *   page_table     int32 [B][max_pages]: physical page of logical page i of sequence b
+ *                  (keys 16i .. 16i+15). Entries that no call needs may hold anything.
+ *   All pointers 16-byte aligned.
+ *
+ * Errors. Host-side checks run before any launch and return G4_ERR_INVALID (bad pointer,
+ * size or alignment) or G4_ERR_UNSUPPORTED (a geometry other than the two layer kinds
+ * below); nothing is launched then. Problems only the device can see (a page-table entry
+ * outside [0, num_pages), a position >= 262144 or beyond the page table, a bounded wait
+ * that ran out) set bits in a device error word and the affected work is skipped; read and
+ * clear the word with g4attn_status_sync. Kernels never trap.
+ */
+#ifndef G4ATTN_H
+#define G4ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  G4_OK = 0,
+  G4_ERR_INVALID = 1,      /* bad argument: NULL pointer, size, alignment, range */
+  G4_ERR_UNSUPPORTED = 2,  /* geometry or dtype outside the two supported layer kinds */
+  G4_ERR_CUDA = 3,         /* a CUDA runtime call failed (launch, table upload) */
+  G4_ERR_TIMEOUT = 4,      /* a bounded device wait ran out (device error word) */
+  G4_ERR_DEVICE = 5        /* device-detected bad data: page index or position (error word) */
+} g4_status;
+
+typedef enum { G4_SLIDING = 0, G4_GLOBAL = 1 } g4_kind;
+
+/* One attention layer. Supported (anything else: G4_ERR_UNSUPPORTED):
+ *   sliding: kind 0, n_q_heads 32, n_kv_heads 16, head_dim 256, 1 <= window <= 262144,
+ *            rope_theta 1e4, rope_partial 1.0, kv_shared 0;
+ *   global:  kind 1, n_q_heads 32, n_kv_heads 4, head_dim 512, window 0,
+ *            rope_theta 1e6, rope_partial 0.25, kv_shared 1.
+ * softmax_scale: any finite value > 0 (1/sqrt(head_dim) is the model's). */
+typedef struct {
+  int32_t kind;
+  int32_t n_q_heads;
+  int32_t n_kv_heads;
+  int32_t head_dim;
+  int32_t window;         /* keys seen including the query's own; 0 = unbounded */
+  float rope_theta;
+  float rope_partial;
+  float softmax_scale;
+  int32_t kv_shared;      /* 1: K==V, the cache holds one tensor S */
+} g4attn_layer;
+
+/* A paged bf16 KV cache of one layer (RFC section 5, hybrid_kv_cache_contract). */
+typedef struct {
+  void* k;                /* sliding: roped K'; global: the shared S */
+  void* v;                /* sliding: V; global: NULL */
+  int32_t num_pages;      /* physical pages in k (and v) */
+  int32_t page_size;      /* keys per page; must be 16 */
+} g4attn_cache;
+
+/* RoPE / p-RoPE of a [T][H][head_dim] bf16 tensor (RFC section 5, sliding_rope_d256 and
+ * global_proportional_p_rope). out[r][h] = bf16(RoPE(x[r][h], pos[r])). Pairs t >= R are
+ * copied bit for bit. x and out may be the same buffer. pos: int32 [T], device, each in
+ * [0, 262144) (others set G4_ERR_DEVICE and leave the row unwritten). T >= 0, H >= 1. */
+g4_status g4attn_rope_apply(const g4attn_layer* layer, const void* x, const int32_t* pos,
+                            int32_t T, int32_t H, void* out, void* stream);
+
+/* Prefill, or one chunk of a chunked prefill, for B sequences (RFC section 5,
+ * sliding_attention_core / global_attention_core). Sequence b owns rows
+ * q_start[b] .. q_start[b]+q_len[b]-1 of q, k, v and out; they are its positions
+ * ctx_start[b] .. ctx_start[b]+q_len[b]-1. Keys at positions < ctx_start[b] must already be
+ * in the cache. The call first writes the new rows' K'/V (sliding) or S (global) into the
+ * cache through page_table, then computes out for those rows. Rows of out that belong to no
+ * sequence are not written. q_start, q_len, ctx_start: int32 [B], device, read on the device
+ * (q_len 0 is allowed); sequences' row ranges must not overlap. T: rows in q/k/v/out.
+ * v: NULL on global layers (K==V). Launch geometry depends on T, B and the layer only. */
+g4_status g4attn_prefill(const g4attn_layer* layer, const void* q, const void* k, const void* v,
+                         int32_t T, const int32_t* q_start, const int32_t* q_len,
+                         const int32_t* ctx_start, int32_t B, const g4attn_cache* cache,
+                         const int32_t* page_table, int32_t max_pages, void* out, void* stream);
+
+/* Writes the K'/V (sliding) or S (global) rows of a prefill batch into the paged cache
+ * without computing attention: the first step of g4attn_prefill on its own (RFC section 5,
+ * hybrid_kv_cache_contract). Same row conventions and errors as g4attn_prefill; v NULL on
+ * global layers. */
+g4_status g4attn_kv_append(const g4attn_layer* layer, const void* k, const void* v, int32_t T,
+                           const int32_t* q_start, const int32_t* q_len, const int32_t* ctx_start,
+                           int32_t B, const g4attn_cache* cache, const int32_t* page_table,
+                           int32_t max_pages, void* stream);
+
+/* Bytes of device workspace g4attn_decode needs for B requests whose page table has
+ * max_pages columns (partial softmax states of the fixed key chunks). */
+size_t g4attn_decode_workspace_bytes(const g4attn_layer* layer, int32_t B, int32_t max_pages);
+
+/* One decode step for B requests. Request b's new token sits at position seq_len[b]-1
+ * (seq_len counts the new token); its key/value (k_new, v_new; v_new NULL on global layers)
+ * are first written into the cache at that position, then out[b] = attention of q[b] over
+ * positions 0 .. seq_len[b]-1 (the last `window` of them on sliding layers). Keys are split
+ * into fixed chunks aligned to absolute position 0 (256 keys on sliding layers, 1024 on
+ * global ones) and merged in ascending chunk order. seq_len: int32 [B], device, each in
+ * [1, min(262144, 16*max_pages)]. workspace: device, >= g4attn_decode_workspace_bytes,
+ * 16-byte aligned; its contents on entry do not matter. */
+g4_status g4attn_decode(const g4attn_layer* layer, const void* q, const void* k_new,
+                        const void* v_new, const int32_t* seq_len, int32_t B,
+                        const g4attn_cache* cache, const int32_t* page_table, int32_t max_pages,
+                        void* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Runtime provenance (RFC section 4, rule 8): writes a NUL-terminated one-line record
+ * (backend, kernel ids, schedule, split policy, accumulator, layer kind, device, dtype,
+ * fallback state) into buf. Returns the record's length without the NUL, or -1 when the
+ * layer is unsupported. Truncates to len-1 characters. */
+int32_t g4attn_provenance(const g4attn_layer* layer, char* buf, size_t len);
+
+/* Synchronises `stream`, then reads and clears the device error word of the current device:
+ * G4_OK, G4_ERR_TIMEOUT or G4_ERR_DEVICE (or G4_ERR_CUDA if a CUDA call failed). */
+g4_status g4attn_status_sync(void* stream);
+
+/* A static, human-readable name for a status code. */
+const char* g4attn_status_string(g4_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* G4ATTN_H */

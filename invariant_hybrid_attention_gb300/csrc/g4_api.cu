@@ -1,0 +1,217 @@
+// The C ABI of g4attn: argument validation (fail closed), dispatch to the kernels of the one
+// supported layer kind, runtime provenance and the device error word.
+//
+// Fail-closed rule and provenance follow section 4 ("Numerical contract", rules 7 and 8) of
+// the RL-Kernel RFC "[RFC][Gemma-4-31B-it] WS1/WS2 kernel roadmap": a geometry outside the
+// two supported layer kinds is refused before any launch, and there is no other code path to
+// fall back to.
+#include <math.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "g4_internal.h"
+#include "g4attn.h"
+
+using namespace g4;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+g4_status check_layer(const g4attn_layer* L, bool* global) {
+  if (!L) return G4_ERR_INVALID;
+  if (L->kind == G4_SLIDING) {
+    if (L->n_q_heads != kSlidingHq || L->n_kv_heads != kSlidingHkv || L->head_dim != kSlidingD ||
+        L->kv_shared != 0 || L->rope_theta != 1.0e4f || L->rope_partial != 1.0f)
+      return G4_ERR_UNSUPPORTED;
+    if (L->window < 1 || L->window > kMaxPos) return G4_ERR_UNSUPPORTED;
+    *global = false;
+  } else if (L->kind == G4_GLOBAL) {
+    if (L->n_q_heads != kGlobalHq || L->n_kv_heads != kGlobalHkv || L->head_dim != kGlobalD ||
+        L->kv_shared != 1 || L->rope_theta != 1.0e6f || L->rope_partial != 0.25f || L->window != 0)
+      return G4_ERR_UNSUPPORTED;
+    *global = true;
+  } else {
+    return G4_ERR_UNSUPPORTED;
+  }
+  if (!(L->softmax_scale > 0.f) || !isfinite(L->softmax_scale)) return G4_ERR_INVALID;
+  return G4_OK;
+}
+
+g4_status check_cache(const g4attn_cache* c, bool global, const int32_t* page_table, int32_t max_pages) {
+  if (!c || !c->k || !aligned16(c->k)) return G4_ERR_INVALID;
+  if (global) {
+    if (c->v != nullptr) return G4_ERR_INVALID;
+  } else if (!c->v || !aligned16(c->v)) {
+    return G4_ERR_INVALID;
+  }
+  if (c->page_size != kPage) return G4_ERR_UNSUPPORTED;
+  if (c->num_pages <= 0 || max_pages <= 0 || !page_table) return G4_ERR_INVALID;
+  return G4_OK;
+}
+
+float scale_log2(const g4attn_layer* L) { return (float)((double)L->softmax_scale * 1.4426950408889634); }
+
+g4_status from_cuda(cudaError_t e) { return e == cudaSuccess ? G4_OK : G4_ERR_CUDA; }
+
+PagedCache paged(const g4attn_cache* c, const int32_t* page_table, int32_t max_pages) {
+  PagedCache pc;
+  pc.k = c->k;
+  pc.v = c->v;
+  pc.num_pages = c->num_pages;
+  pc.page_table = page_table;
+  pc.max_pages = max_pages;
+  return pc;
+}
+
+g4_status check_rows(const void* q_or_k, int32_t T, const int32_t* q_start, const int32_t* q_len,
+                     const int32_t* ctx_start, int32_t B) {
+  if (T < 0 || B <= 0 || !q_start || !q_len || !ctx_start) return G4_ERR_INVALID;
+  if (T > 0 && (!q_or_k || !aligned16(q_or_k))) return G4_ERR_INVALID;
+  return G4_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* g4attn_status_string(g4_status s) {
+  switch (s) {
+    case G4_OK: return "ok";
+    case G4_ERR_INVALID: return "invalid argument";
+    case G4_ERR_UNSUPPORTED: return "unsupported geometry";
+    case G4_ERR_CUDA: return "CUDA runtime error";
+    case G4_ERR_TIMEOUT: return "bounded device wait timed out";
+    case G4_ERR_DEVICE: return "device-detected bad page index or position";
+  }
+  return "unknown status";
+}
+
+g4_status g4attn_rope_apply(const g4attn_layer* layer, const void* x, const int32_t* pos, int32_t T, int32_t H,
+                            void* out, void* stream) {
+  bool global = false;
+  g4_status s = check_layer(layer, &global);
+  if (s != G4_OK) return s;
+  if (T < 0 || H < 1) return G4_ERR_INVALID;
+  if (T == 0) return G4_OK;
+  if (!x || !out || !pos || !aligned16(x) || !aligned16(out)) return G4_ERR_INVALID;
+  DeviceState st;
+  if (device_state(&st) != cudaSuccess) return G4_ERR_CUDA;
+  return from_cuda(launch_rope_apply(global, x, pos, T, H, out, st, (cudaStream_t)stream));
+}
+
+g4_status g4attn_kv_append(const g4attn_layer* layer, const void* k, const void* v, int32_t T,
+                           const int32_t* q_start, const int32_t* q_len, const int32_t* ctx_start, int32_t B,
+                           const g4attn_cache* cache, const int32_t* page_table, int32_t max_pages, void* stream) {
+  bool global = false;
+  g4_status s = check_layer(layer, &global);
+  if (s != G4_OK) return s;
+  if ((s = check_rows(k, T, q_start, q_len, ctx_start, B)) != G4_OK) return s;
+  if ((s = check_cache(cache, global, page_table, max_pages)) != G4_OK) return s;
+  if (global ? v != nullptr : (T > 0 && (!v || !aligned16(v)))) return G4_ERR_INVALID;
+  if (T == 0) return G4_OK;
+  DeviceState st;
+  if (device_state(&st) != cudaSuccess) return G4_ERR_CUDA;
+  SeqRows rows{q_start, q_len, ctx_start, B, T};
+  return from_cuda(launch_append_prefill(global, k, v, rows, paged(cache, page_table, max_pages), st,
+                                         (cudaStream_t)stream));
+}
+
+g4_status g4attn_prefill(const g4attn_layer* layer, const void* q, const void* k, const void* v, int32_t T,
+                         const int32_t* q_start, const int32_t* q_len, const int32_t* ctx_start, int32_t B,
+                         const g4attn_cache* cache, const int32_t* page_table, int32_t max_pages, void* out,
+                         void* stream) {
+  bool global = false;
+  g4_status s = check_layer(layer, &global);
+  if (s != G4_OK) return s;
+  if ((s = check_rows(q, T, q_start, q_len, ctx_start, B)) != G4_OK) return s;
+  if ((s = check_cache(cache, global, page_table, max_pages)) != G4_OK) return s;
+  if (T > 0 && (!k || !aligned16(k) || !out || !aligned16(out))) return G4_ERR_INVALID;
+  if (global ? v != nullptr : (T > 0 && (!v || !aligned16(v)))) return G4_ERR_INVALID;
+  if (T == 0) return G4_OK;
+  DeviceState st;
+  if (device_state(&st) != cudaSuccess) return G4_ERR_CUDA;
+  const cudaStream_t cs = (cudaStream_t)stream;
+  const SeqRows rows{q_start, q_len, ctx_start, B, T};
+  const PagedCache pc = paged(cache, page_table, max_pages);
+  cudaError_t e = launch_append_prefill(global, k, v, rows, pc, st, cs);
+  if (e != cudaSuccess) return G4_ERR_CUDA;
+  return from_cuda(launch_prefill(global, q, rows, global ? 0 : layer->window, scale_log2(layer), pc, out, st, cs));
+}
+
+size_t g4attn_decode_workspace_bytes(const g4attn_layer* layer, int32_t B, int32_t max_pages) {
+  bool global = false;
+  if (check_layer(layer, &global) != G4_OK || B <= 0 || max_pages <= 0) return 0;
+  return decode_workspace_bytes(global, B, max_pages, global ? 0 : layer->window);
+}
+
+g4_status g4attn_decode(const g4attn_layer* layer, const void* q, const void* k_new, const void* v_new,
+                        const int32_t* seq_len, int32_t B, const g4attn_cache* cache, const int32_t* page_table,
+                        int32_t max_pages, void* out, void* workspace, size_t workspace_bytes, void* stream) {
+  bool global = false;
+  g4_status s = check_layer(layer, &global);
+  if (s != G4_OK) return s;
+  if (B <= 0 || !q || !k_new || !seq_len || !out || !workspace) return G4_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(out) || !aligned16(workspace)) return G4_ERR_INVALID;
+  if (global ? v_new != nullptr : (!v_new || !aligned16(v_new))) return G4_ERR_INVALID;
+  if ((s = check_cache(cache, global, page_table, max_pages)) != G4_OK) return s;
+  if (workspace_bytes < decode_workspace_bytes(global, B, max_pages, global ? 0 : layer->window))
+    return G4_ERR_INVALID;
+  DeviceState st;
+  if (device_state(&st) != cudaSuccess) return G4_ERR_CUDA;
+  const cudaStream_t cs = (cudaStream_t)stream;
+  const PagedCache pc = paged(cache, page_table, max_pages);
+  cudaError_t e = launch_append_decode(global, k_new, v_new, seq_len, B, pc, st, cs);
+  if (e != cudaSuccess) return G4_ERR_CUDA;
+  return from_cuda(launch_decode(global, q, seq_len, B, global ? 0 : layer->window, scale_log2(layer), pc, out,
+                                 workspace, st, cs));
+}
+
+int32_t g4attn_provenance(const g4attn_layer* layer, char* buf, size_t len) {
+  bool global = false;
+  if (check_layer(layer, &global) != G4_OK) return -1;
+  char dev[320] = "unknown";
+  int d = 0;
+  cudaDeviceProp prop;
+  if (cudaGetDevice(&d) == cudaSuccess && cudaGetDeviceProperties(&prop, d) == cudaSuccess)
+    snprintf(dev, sizeof(dev), "%s(sm_%d%d,%dSM)", prop.name, prop.major, prop.minor, prop.multiProcessorCount);
+  char rec[1536];
+  int n;
+  if (global)
+    n = snprintf(rec, sizeof(rec),
+                 "requested=g4attn;actual=g4attn-cuda-sm_103a;layer=global;kernels=append_shared_s,"
+                 "prefill_global_tcgen05,decode_global_mma_bf16,merge_ordered;schedule=qtile128@abs-pos,"
+                 "ktile64@abs-pos,ascending;split=decode-fixed-chunk-1024@abs-key0,4-warp-round-robin,ordered-merge;"
+                 "accumulator=fp32;casts=roped-q,roped-k,p,out:bf16-rne;device=%s;dtype=bf16;"
+                 "shape=Hq32,Hkv4,D512,k_eq_v,prope0.25,theta1e6,scale%.9g;fallback=none",
+                 dev, (double)layer->softmax_scale);
+  else
+    n = snprintf(rec, sizeof(rec),
+                 "requested=g4attn;actual=g4attn-cuda-sm_103a;layer=sliding;kernels=append_rope_kv,"
+                 "prefill_sliding_tcgen05,decode_sliding_cudacore,merge_ordered;schedule=qtile128@abs-pos,"
+                 "ktile64@abs-pos,ascending,window-skip;split=decode-fixed-chunk-256@abs-key0,4-warp-round-robin,"
+                 "ordered-merge;accumulator=fp32;casts=roped-q,roped-k,p,out:bf16-rne;device=%s;dtype=bf16;"
+                 "shape=Hq32,Hkv16,D256,W%d,theta1e4,scale%.9g;fallback=none",
+                 dev, layer->window, (double)layer->softmax_scale);
+  if (n < 0) return -1;
+  if (buf && len > 0) {
+    const size_t c = (size_t)n < len - 1 ? (size_t)n : len - 1;
+    memcpy(buf, rec, c);
+    buf[c] = '\0';
+  }
+  return n;
+}
+
+g4_status g4attn_status_sync(void* stream) {
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return G4_ERR_CUDA;
+  DeviceState st;
+  if (device_state(&st) != cudaSuccess) return G4_ERR_CUDA;
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, st.err, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return G4_ERR_CUDA;
+  if (word != 0 && cudaMemset(st.err, 0, sizeof(word)) != cudaSuccess) return G4_ERR_CUDA;
+  if (word & kErrTimeout) return G4_ERR_TIMEOUT;
+  if (word & (kErrPage | kErrPos)) return G4_ERR_DEVICE;
+  return G4_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,58 @@
+// Host-side interface between the g4attn translation units (not part of the public ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "g4_common.cuh"
+
+namespace g4 {
+
+// Static device state of the current device: the RoPE tables of both layer kinds and the
+// error word. Filled on the first call per device (a synchronous upload; make that first
+// call outside any stream capture).
+struct DeviceState {
+  RopeTables sliding;
+  RopeTables global;
+  uint32_t* err;
+};
+cudaError_t device_state(DeviceState* st);
+
+// Row-to-sequence description of a prefill batch (all device pointers, int32 [B]).
+struct SeqRows {
+  const int32_t* q_start;
+  const int32_t* q_len;
+  const int32_t* ctx_start;
+  int32_t B;
+  int32_t T;
+};
+
+struct PagedCache {
+  void* k;
+  void* v;
+  int32_t num_pages;
+  const int32_t* page_table;
+  int32_t max_pages;
+};
+
+cudaError_t launch_rope_apply(bool global, const void* x, const int32_t* pos, int T, int H, void* out,
+                              const DeviceState& st, cudaStream_t s);
+
+cudaError_t launch_append_prefill(bool global, const void* k, const void* v, const SeqRows& rows,
+                                  const PagedCache& cache, const DeviceState& st, cudaStream_t s);
+
+cudaError_t launch_append_decode(bool global, const void* k_new, const void* v_new, const int32_t* seq_len,
+                                 int B, const PagedCache& cache, const DeviceState& st, cudaStream_t s);
+
+// Decode partials + ordered merge. ws must hold decode_workspace_bytes(global, B, max_pages).
+size_t decode_workspace_bytes(bool global, int B, int max_pages, int window);
+cudaError_t launch_decode(bool global, const void* q, const int32_t* seq_len, int B, int window,
+                          float scale_log2, const PagedCache& cache, void* out, void* ws,
+                          const DeviceState& st, cudaStream_t s);
+
+cudaError_t launch_prefill(bool global, const void* q, const SeqRows& rows, int window, float scale_log2,
+                           const PagedCache& cache, void* out, const DeviceState& st, cudaStream_t s);
+
+}  // namespace g4

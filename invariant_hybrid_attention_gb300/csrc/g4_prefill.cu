@@ -1,0 +1,524 @@
+// Prefill attention on the 5th-generation tensor cores (tcgen05, accumulators in tensor memory).
+//
+// Work unit: (sequence, query tile of 128 positions aligned to absolute position, query head).
+// Key tiles of 64 keys are aligned to absolute key 0 and visited in ascending order, so the
+// arithmetic a row gets depends only on its own position, its sequence's keys and the window:
+// not on the batch, the row's place in it, padding, packing or the launch grid (RL-Kernel RFC
+// "[RFC][Gemma-4-31B-it] WS1/WS2 kernel roadmap", section 4 rules 2, 3 and 6).
+//
+// Sliding layer (RFC section 5, sliding_attention_core: causal local attention, window 1024,
+// 32 Q / 16 KV heads, D 256). Per CTA:
+//   warp 0  TMA producer: paged K and V boxes (16 keys x 64 dims, 128B swizzle) into a
+//           2-stage ring; pages outside the needed key range are zero-filled, never looked up;
+//   warp 1  MMA issuer: S = Q K^T with Q in tensor memory (A operand) and K in shared memory,
+//           O += P V with P and V in shared memory; one elected lane issues, commits signal;
+//   warps 2-5  one thread per query row: Q load + RoPE into tensor memory, then per key tile
+//           the mask, the online softmax (lazy rescale, threshold 2^8), P (bf16) into shared
+//           memory, the O correction when needed, and the epilogue O / l -> bf16.
+// Tensor memory (512 columns): O [0,256), Q [256,384) bf16 pairs, S double buffer [384,512).
+#include <math.h>
+
+#include "g4_internal.h"
+
+namespace g4 {
+
+namespace {
+
+constexpr int kBM = 128;                  // query rows per tile
+constexpr int kBN = 64;                   // keys per tile
+constexpr int kNS = 2;                    // K/V ring stages
+constexpr float kLazyRescale = 8.0f;
+
+// ---------------------------------------------------------------- sliding layer geometry
+constexpr int kSD = kSlidingD;            // 256
+constexpr int kSChunk = kBN * 128;        // one 64-dim chunk of a key tile: 64 rows x 128 B
+constexpr int kSKTile = (kSD / 64) * kSChunk;   // 32 KB
+constexpr int kPTile = kBM * 128;         // P: 128 rows x 64 keys bf16 (one 128B-swizzled chunk)
+
+constexpr uint32_t kTmO = 0, kTmQ = 256, kTmS = 384;   // column offsets
+constexpr uint32_t kIdescQK = idesc_bf16(kBM, kBN, false, false);
+constexpr uint32_t kIdescPV = idesc_bf16(kBM, kSD, false, true);
+
+struct SlidingSmem {
+  uint8_t k[kNS][kSKTile];
+  uint8_t v[kNS][kSKTile];
+  uint8_t p[2][kPTile];
+  uint64_t k_full[kNS], k_empty[kNS], v_full[kNS], v_empty[kNS];
+  uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];
+  uint64_t q_ready, teardown;
+  uint32_t tmem_base;
+  int abort_flag;
+  int unit_b, unit_t;
+};
+constexpr size_t kSlidingSmemBytes = sizeof(SlidingSmem) + 1024;
+
+struct PrefillParams {
+  const __nv_bfloat16* q;   // [T][32][D]
+  SeqRows rows;
+  int window;               // sliding W (0 on global layers)
+  float scale_log2;
+  int num_pages;
+  const int32_t* page_table;
+  int max_pages;
+  __nv_bfloat16* out;
+  RopeTables tb;
+  uint32_t* err;
+};
+
+// Finds this CTA's (sequence, query tile) among all sequences' tiles: slot s of sequence b
+// is its tile (last - s), so every sequence is walked from its most expensive tile down.
+// Warp-wide; returns b = -1 when the slot is past the last tile.
+__device__ __forceinline__ void find_unit(const SeqRows& rows, int slot, int& out_b, int& out_t) {
+  const int lane = threadIdx.x & 31;
+  int base = 0;
+  out_b = -1;
+  out_t = 0;
+  for (int b0 = 0; b0 < rows.B; b0 += 32) {
+    const int b = b0 + lane;
+    int cnt = 0, tl = 0;
+    if (b < rows.B) {
+      const int L = rows.q_len[b], cs = rows.ctx_start[b];
+      if (L > 0 && cs >= 0) {
+        tl = (cs + L - 1) / kBM;
+        cnt = tl - cs / kBM + 1;
+      }
+    }
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += n;
+    }
+    const int excl = incl - cnt;
+    const bool mine = cnt > 0 && slot >= base + excl && slot < base + incl;
+    const unsigned m = __ballot_sync(0xffffffffu, mine);
+    if (m) {
+      const int src = __ffs(m) - 1;
+      const int e = __shfl_sync(0xffffffffu, excl, src);
+      const int t_last = __shfl_sync(0xffffffffu, tl, src);
+      out_b = b0 + src;
+      out_t = t_last - (slot - base - e);
+      return;
+    }
+    base += __shfl_sync(0xffffffffu, incl, 31);
+  }
+}
+
+// Row of the cache's 2-D tensor map holding keys key0 .. key0+15 of KV head g, or -16
+// (entirely outside the map: the TMA fills zeros) when the page lies outside [k_lo, k_hi].
+__device__ __forceinline__ int page_row(int key0, int k_lo, int k_hi, const int32_t* pt, int num_pages, int hkv,
+                                        int g, uint32_t* err) {
+  if (key0 + kPage - 1 < k_lo || key0 > k_hi) return -kPage;
+  const int phys = pt[key0 >> 4];
+  if (phys < 0 || phys >= num_pages) {
+    set_error(err, kErrPage);
+    return -kPage;
+  }
+  return (phys * hkv + g) * kPage;
+}
+
+__device__ __forceinline__ uint32_t tmem_lane_base(int warp) { return (uint32_t)(32 * (warp & 3)) << 16; }
+
+__global__ void __launch_bounds__(192, 1)
+    prefill_sliding_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+                           PrefillParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  SlidingSmem& sm =
+      *reinterpret_cast<SlidingSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.x % kSlidingHq;
+  const int slot = blockIdx.x / kSlidingHq;
+  const int g = h / (kSlidingHq / kSlidingHkv);
+
+  if (warp == 0) {
+    int ub, ut;
+    find_unit(p.rows, slot, ub, ut);
+    if (lane == 0) {
+      sm.unit_b = ub;
+      sm.unit_t = ut;
+    }
+  }
+  __syncthreads();
+  const int b = sm.unit_b;
+  if (b < 0) return;
+  const int t = sm.unit_t;
+  const int cs = p.rows.ctx_start[b], L = p.rows.q_len[b], qs = p.rows.q_start[b];
+  const int p_lo = max(kBM * t, cs), p_hi = min(kBM * t + kBM - 1, cs + L - 1);
+  const int ctx_end = cs + L;
+  if (p_hi >= kMaxPos || (p_hi >> 4) >= p.max_pages) {
+    if (threadIdx.x == 0 && h == 0) set_error(p.err, kErrPos);
+    return;
+  }
+  const int W = p.window;
+  const int k_lo = W > 0 ? max(0, p_lo - W + 1) : 0;
+  const int k_hi = p_hi;
+  const int kt0 = k_lo / kBN;
+  const int n_tiles = k_hi / kBN - kt0 + 1;
+  const int q_row0 = qs + (kBM * t - cs);   // memory row of tile row 0 (may be negative)
+  const int32_t* pt = p.page_table + (size_t)b * p.max_pages;
+
+  if (threadIdx.x == 32) {
+    for (int s = 0; s < kNS; ++s) {
+      mbar_init(&sm.k_full[s], 1);
+      mbar_init(&sm.k_empty[s], 1);
+      mbar_init(&sm.v_full[s], 1);
+      mbar_init(&sm.v_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&sm.s_full[s], 1);
+      mbar_init(&sm.s_free[s], 128);
+      mbar_init(&sm.p_full[s], 128);
+      mbar_init(&sm.pv_done[s], 1);
+    }
+    mbar_init(&sm.q_ready, 128);
+    mbar_init(&sm.teardown, 1);
+    sm.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&sm.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tm = sm.tmem_base;
+  volatile int* abort_flag = &sm.abort_flag;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tmap(&tmap_k);
+      prefetch_tmap(&tmap_v);
+      int j = 0;
+      for (; j < n_tiles; ++j) {
+        const int s = j % kNS;
+        const int kb = (kt0 + j) * kBN;
+        if (j >= kNS && !mbar_wait(&sm.k_empty[s], ((j / kNS) - 1) & 1, abort_flag, p.err)) break;
+        mbar_arrive_expect_tx(&sm.k_full[s], kSKTile);
+        int rowv[4];
+#pragma unroll
+        for (int pp = 0; pp < 4; ++pp) {
+          rowv[pp] = page_row(kb + pp * kPage, k_lo, k_hi, pt, p.num_pages, kSlidingHkv, g, p.err);
+#pragma unroll
+          for (int c = 0; c < kSD / 64; ++c)
+            tma_load_2d(sm.k[s] + c * kSChunk + pp * 2048, &tmap_k, 64 * c, rowv[pp], &sm.k_full[s]);
+        }
+        if (j >= kNS && !mbar_wait(&sm.v_empty[s], ((j / kNS) - 1) & 1, abort_flag, p.err)) {
+          // K of tile j is in flight: account for it in the drain below.
+          ++j;
+          break;
+        }
+        mbar_arrive_expect_tx(&sm.v_full[s], kSKTile);
+#pragma unroll
+        for (int pp = 0; pp < 4; ++pp)
+#pragma unroll
+          for (int c = 0; c < kSD / 64; ++c)
+            tma_load_2d(sm.v[s] + c * kSChunk + pp * 2048, &tmap_v, 64 * c, rowv[pp], &sm.v_full[s]);
+      }
+      if (*abort_flag) {   // drain copies still in flight (bounded) before the CTA may exit
+        const unsigned long long t0 = globaltimer();
+        for (int i = max(0, j - kNS); i < j; ++i) {
+          while (!mbar_try_wait(smem_u32(&sm.k_full[i % kNS]), (i / kNS) & 1) && globaltimer() - t0 < kWaitLimitNs) {
+          }
+          while (!mbar_try_wait(smem_u32(&sm.v_full[i % kNS]), (i / kNS) & 1) && globaltimer() - t0 < kWaitLimitNs) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    auto pv = [&](int i) -> bool {
+      if (!mbar_wait(&sm.p_full[i & 1], (i >> 1) & 1, abort_flag, p.err)) return false;
+      if (!mbar_wait(&sm.v_full[i % kNS], (i / kNS) & 1, abort_flag, p.err)) return false;
+      const int kb = (kt0 + i) * kBN;
+      if (kb + kBN - 1 >= ctx_end) {
+        // Stale slots past the sequence's last key may hold anything (NaN): P = 0 there does
+        // not cancel NaN, so zero those V rows (whole 128-byte rows: the swizzle is irrelevant).
+        const int r0 = max(0, ctx_end - kb);
+        const int r1 = min(kBN, ((k_hi >> 4) + 1) * kPage - kb);
+        for (int idx = lane; idx < (r1 - r0) * (kSD / 64) * 8; idx += 32) {
+          const int r = r0 + idx / ((kSD / 64) * 8), rem = idx % ((kSD / 64) * 8);
+          *reinterpret_cast<uint4*>(sm.v[i % kNS] + (rem >> 3) * kSChunk + r * 128 + (rem & 7) * 16) =
+              make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async();
+        __syncwarp();
+      }
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t pa = smem_u32(sm.p[i & 1]);
+        const uint32_t va = smem_u32(sm.v[i % kNS]);
+#pragma unroll
+        for (int k = 0; k < kBN / 16; ++k)
+          mma_ss(tm + kTmO, desc_sw128(pa + k * 32, 16, 1024), desc_sw128(va + k * 2048, kSChunk, 1024), kIdescPV,
+                 (i > 0 || k > 0) ? 1u : 0u);
+        mma_commit(&sm.pv_done[i & 1]);
+        mma_commit(&sm.v_empty[i % kNS]);
+      }
+      __syncwarp();
+      return true;
+    };
+    bool ok = mbar_wait(&sm.q_ready, 0, abort_flag, p.err);
+    for (int j = 0; ok && j < n_tiles; ++j) {
+      const int s = j % kNS;
+      if (!mbar_wait(&sm.k_full[s], (j / kNS) & 1, abort_flag, p.err)) break;
+      if (j >= 2 && !mbar_wait(&sm.s_free[j & 1], ((j - 2) >> 1) & 1, abort_flag, p.err)) break;
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t ka = smem_u32(sm.k[s]);
+#pragma unroll
+        for (int k = 0; k < kSD / 16; ++k)
+          mma_ts(tm + kTmS + 64 * (j & 1), tm + kTmQ + 8 * k,
+                 desc_sw128(ka + (k >> 2) * kSChunk + (k & 3) * 32, 16, 1024), kIdescQK, k > 0 ? 1u : 0u);
+        mma_commit(&sm.s_full[j & 1]);
+        mma_commit(&sm.k_empty[s]);
+      }
+      __syncwarp();
+      if (j >= 1 && !pv(j - 1)) {
+        ok = false;
+        break;
+      }
+      if (j == n_tiles - 1 && !pv(j)) ok = false;
+    }
+  } else {
+    // ------------------------------------------------------------ softmax / epilogue warps
+    const int r = 32 * (warp & 3) + lane;   // query row = tensor-memory lane
+    const uint32_t tq = tm + tmem_lane_base(warp);
+    const int pos = kBM * t + r;
+    const bool row_ok = pos >= p_lo && pos <= p_hi;
+
+    // Q: load, RoPE (all 128 pairs), declared bf16 cast, into tensor memory as bf16 pairs.
+    {
+      const __nv_bfloat16* qrow = p.q + ((size_t)(q_row0 + r) * kSlidingHq + h) * kSD;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t lo[16], hi[16];
+        if (row_ok) {
+          uint4 a[4], bq[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            a[i] = *reinterpret_cast<const uint4*>(qrow + 32 * c + 8 * i);
+            bq[i] = *reinterpret_cast<const uint4*>(qrow + kSD / 2 + 32 * c + 8 * i);
+          }
+          const uint32_t* aw = reinterpret_cast<const uint32_t*>(a);
+          const uint32_t* bw = reinterpret_cast<const uint32_t*>(bq);
+#pragma unroll
+          for (int w = 0; w < 16; ++w) {
+            float x0 = bf16_lo(aw[w]), x1 = bf16_hi(aw[w]), y0 = bf16_lo(bw[w]), y1 = bf16_hi(bw[w]);
+            rope_pair(x0, y0, rope_cs(p.tb, 32 * c + 2 * w, pos));
+            rope_pair(x1, y1, rope_cs(p.tb, 32 * c + 2 * w + 1, pos));
+            lo[w] = pack_bf16(x0, x1);
+            hi[w] = pack_bf16(y0, y1);
+          }
+        } else {
+#pragma unroll
+          for (int w = 0; w < 16; ++w) lo[w] = hi[w] = 0u;
+        }
+        tmem_st16(tq + kTmQ + 16 * c, lo);
+        tmem_st16(tq + kTmQ + 64 + 16 * c, hi);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&sm.q_ready);
+    }
+
+    const float cl2 = p.scale_log2;
+    float m_used = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int kb = (kt0 + j) * kBN;
+      if (!mbar_wait(&sm.s_full[j & 1], (j >> 1) & 1, abort_flag, p.err)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sr[64];
+      tmem_ld32(tq + kTmS + 64 * (j & 1), *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+      tmem_ld32(tq + kTmS + 64 * (j & 1) + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&sm.s_free[j & 1]);
+
+      float s[64];
+#pragma unroll
+      for (int c = 0; c < 64; ++c) s[c] = __uint_as_float(sr[c]);
+      const bool full = row_ok && kb + kBN - 1 <= pos && (W == 0 || pos - kb <= W - 1);
+      if (!full) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          const int key = kb + c;
+          const bool vis = row_ok && key <= pos && (W == 0 || pos - key <= W - 1);
+          s[c] = vis ? s[c] : -INFINITY;
+        }
+      }
+      float mx[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        mx[i] = s[i];
+#pragma unroll
+        for (int c = 1; c < 8; ++c) mx[i] = fmaxf(mx[i], s[i + 8 * c]);
+      }
+      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * cl2;
+      float alpha = 1.f;
+      bool need_o = false;
+      if (mt > m_used + kLazyRescale) {
+        need_o = (m_used != -INFINITY);
+        alpha = exp2f(m_used - mt);
+        m_used = mt;
+      }
+      const float neg_m = (m_used == -INFINITY) ? 0.f : -m_used;
+      uint32_t pw[32];
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int w = 0; w < 32; ++w) {
+        const __nv_bfloat16 p0 = __float2bfloat16_rn(exp2f(fmaf(s[2 * w], cl2, neg_m)));
+        const __nv_bfloat16 p1 = __float2bfloat16_rn(exp2f(fmaf(s[2 * w + 1], cl2, neg_m)));
+        ls[w & 3] += __bfloat162float(p0) + __bfloat162float(p1);
+        pw[w] = (uint32_t)__bfloat16_as_ushort(p0) | ((uint32_t)__bfloat16_as_ushort(p1) << 16);
+      }
+      l_run = fmaf(l_run, alpha, (ls[0] + ls[1]) + (ls[2] + ls[3]));
+
+      // P_j into its shared-memory buffer once P_{j-2} has been consumed.
+      if (j >= 2 && !mbar_wait(&sm.pv_done[j & 1], ((j - 2) >> 1) & 1, abort_flag, p.err)) {
+        ok = false;
+        break;
+      }
+      uint8_t* prow = sm.p[j & 1] + r * 128;
+#pragma unroll
+      for (int k16 = 0; k16 < 8; ++k16)
+        *reinterpret_cast<uint4*>(prow + ((k16 ^ (r & 7)) * 16)) =
+            make_uint4(pw[4 * k16], pw[4 * k16 + 1], pw[4 * k16 + 2], pw[4 * k16 + 3]);
+      fence_proxy_async();
+
+      // O correction (rows whose max rose by more than 2^8), after P_{j-1} V_{j-1} landed.
+      if (__any_sync(0xffffffffu, need_o)) {
+        if (!mbar_wait(&sm.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, p.err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const float a = need_o ? alpha : 1.f;
+#pragma unroll 1
+        for (int cc = 0; cc < kSD / 32; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(tq + kTmO + 32 * cc, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * a);
+          tmem_st32(tq + kTmO + 32 * cc, o);
+        }
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      mbar_arrive(&sm.p_full[j & 1]);
+    }
+
+    // Epilogue: O / l -> bf16, rows of this sequence only.
+    if (ok && mbar_wait(&sm.pv_done[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1, abort_flag, p.err)) {
+      tc_fence_after();
+      const float inv = (l_run > 0.f) ? __frcp_rn(l_run) : 0.f;
+      __nv_bfloat16* orow = p.out + ((size_t)(q_row0 + r) * kSlidingHq + h) * kSD;
+#pragma unroll 1
+      for (int cc = 0; cc < kSD / 32; ++cc) {
+        uint32_t o[32];
+        tmem_ld32(tq + kTmO + 32 * cc, o);
+        tmem_ld_wait();
+        uint32_t w16[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          w16[c] = pack_bf16(__uint_as_float(o[2 * c]) * inv, __uint_as_float(o[2 * c + 1]) * inv);
+        if (row_ok) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * cc);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w16[4 * i], w16[4 * i + 1], w16[4 * i + 2], w16[4 * i + 3]);
+        }
+      }
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    if (sm.abort_flag) {   // let every issued MMA finish before the columns are freed
+      if (lane == 0) mma_commit(&sm.teardown);
+      __syncwarp();
+      const unsigned long long t0 = globaltimer();
+      while (!mbar_try_wait(smem_u32(&sm.teardown), 0) && globaltimer() - t0 < kWaitLimitNs) {
+      }
+    }
+    tmem_dealloc(tm, 512);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// 2-D map over a paged cache [num_pages][hkv][16][D] seen as rows of D bf16; box 64 x 16,
+// 128-byte swizzle, zero fill outside.
+bool cache_map(CUtensorMap* m, const void* base, int num_pages, int hkv, int D) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)num_pages * hkv * kPage};
+  cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)kPage};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(bool global, const void* q, const SeqRows& rows, int window, float scale_log2,
+                           const PagedCache& cache, void* out, const DeviceState& st, cudaStream_t s) {
+  if (global) return cudaErrorNotSupported;
+  PrefillParams p{};
+  p.q = (const __nv_bfloat16*)q;
+  p.rows = rows;
+  p.window = window;
+  p.scale_log2 = scale_log2;
+  p.num_pages = cache.num_pages;
+  p.page_table = cache.page_table;
+  p.max_pages = cache.max_pages;
+  p.out = (__nv_bfloat16*)out;
+  p.tb = st.sliding;
+  p.err = st.err;
+  CUtensorMap mk, mv;
+  if (!cache_map(&mk, cache.k, cache.num_pages, kSlidingHkv, kSD)) return cudaErrorInvalidValue;
+  if (!cache_map(&mv, cache.v, cache.num_pages, kSlidingHkv, kSD)) return cudaErrorInvalidValue;
+  static bool attr[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr[dev]) {
+    cudaError_t e =
+        cudaFuncSetAttribute(prefill_sliding_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSlidingSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr[dev] = true;
+  }
+  const long long slots = (long long)rows.T / kBM + 2LL * rows.B;
+  const long long blocks = slots * kSlidingHq;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+  prefill_sliding_kernel<<<(unsigned)blocks, 192, kSlidingSmemBytes, s>>>(mk, mv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace g4

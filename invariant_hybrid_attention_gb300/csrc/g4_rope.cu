@@ -1,0 +1,255 @@
+// RoPE / p-RoPE tables and the elementwise kernels: g4attn_rope_apply and the paged KV-cache
+// append of prefill and decode.
+//
+// RoPE as the RL-Kernel RFC "[RFC][Gemma-4-31B-it] WS1/WS2 kernel roadmap" lists it (section 2
+// fingerprint table; section 5 rows sliding_rope_d256 and global_proportional_p_rope):
+// standard RoPE with theta 1e4 on the 256-dim sliding heads; proportional p-RoPE with
+// partial factor 0.25 and theta 1e6 on the 512-dim global heads. Reading used here: element t
+// pairs with t + D/2, pair t turns by pos * theta^(-2t/D) (frequency denominator = full D),
+// and only pairs t < R turn (R = 128 sliding, 64 global); the rest are copied bit for bit.
+//
+// Angles: pos * f_t needs more than fp32 at large positions (about 0.016 rad of error at
+// pos 2^18), so the tables hold (cos, sin) of 256*c*f_t and of p*f_t, computed in fp64 on the
+// host, and a lookup combines them by the angle-addition formula in fp32. The tables are
+// static device arrays: the library allocates no device memory.
+#include <math.h>
+
+#include <mutex>
+#include <type_traits>
+#include <vector>
+
+#include "g4_internal.h"
+
+namespace g4 {
+
+static __device__ float2 g_rope_sliding_coarse[kSlidingR * kRopeCoarse];
+static __device__ float2 g_rope_sliding_fine[kSlidingR * kRopeFine];
+static __device__ float2 g_rope_global_coarse[kGlobalR * kRopeCoarse];
+static __device__ float2 g_rope_global_fine[kGlobalR * kRopeFine];
+static __device__ uint32_t g_error_word;
+
+namespace {
+
+void build_tables(int D, int R, double theta, std::vector<float2>& coarse, std::vector<float2>& fine) {
+  coarse.resize((size_t)R * kRopeCoarse);
+  fine.resize((size_t)R * kRopeFine);
+  for (int t = 0; t < R; ++t) {
+    const double f = pow(theta, -2.0 * t / (double)D);
+    for (int c = 0; c < kRopeCoarse; ++c) {
+      const double a = (256.0 * c) * f;
+      coarse[(size_t)t * kRopeCoarse + c] = make_float2((float)cos(a), (float)sin(a));
+    }
+    for (int p = 0; p < kRopeFine; ++p) {
+      const double a = (double)p * f;
+      fine[(size_t)t * kRopeFine + p] = make_float2((float)cos(a), (float)sin(a));
+    }
+  }
+}
+
+constexpr int kMaxDevices = 64;
+std::mutex g_state_mutex;
+bool g_state_ready[kMaxDevices];
+DeviceState g_state[kMaxDevices];
+
+}  // namespace
+
+cudaError_t device_state(DeviceState* st) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_state_mutex);
+  if (!g_state_ready[dev]) {
+    static std::vector<float2> sc, sf, gc, gf;
+    if (sc.empty()) {
+      build_tables(kSlidingD, kSlidingR, 1.0e4, sc, sf);
+      build_tables(kGlobalD, kGlobalR, 1.0e6, gc, gf);
+    }
+    DeviceState s{};
+    void* p = nullptr;
+    if ((e = cudaMemcpyToSymbol(g_rope_sliding_coarse, sc.data(), sc.size() * sizeof(float2))) != cudaSuccess) return e;
+    if ((e = cudaMemcpyToSymbol(g_rope_sliding_fine, sf.data(), sf.size() * sizeof(float2))) != cudaSuccess) return e;
+    if ((e = cudaMemcpyToSymbol(g_rope_global_coarse, gc.data(), gc.size() * sizeof(float2))) != cudaSuccess) return e;
+    if ((e = cudaMemcpyToSymbol(g_rope_global_fine, gf.data(), gf.size() * sizeof(float2))) != cudaSuccess) return e;
+    const uint32_t zero = 0;
+    if ((e = cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero))) != cudaSuccess) return e;
+    if ((e = cudaGetSymbolAddress(&p, g_rope_sliding_coarse)) != cudaSuccess) return e;
+    s.sliding.coarse = (const float2*)p;
+    if ((e = cudaGetSymbolAddress(&p, g_rope_sliding_fine)) != cudaSuccess) return e;
+    s.sliding.fine = (const float2*)p;
+    if ((e = cudaGetSymbolAddress(&p, g_rope_global_coarse)) != cudaSuccess) return e;
+    s.global.coarse = (const float2*)p;
+    if ((e = cudaGetSymbolAddress(&p, g_rope_global_fine)) != cudaSuccess) return e;
+    s.global.fine = (const float2*)p;
+    if ((e = cudaGetSymbolAddress(&p, g_error_word)) != cudaSuccess) return e;
+    s.err = (uint32_t*)p;
+    g_state[dev] = s;
+    g_state_ready[dev] = true;
+  }
+  *st = g_state[dev];
+  return cudaSuccess;
+}
+
+// ---- one D-vector per warp ----------------------------------------------------------------------
+// Lane l owns pairs t = l*P .. l*P+P-1 (P = D/64), i.e. P contiguous elements of each half.
+template <int D, int R>
+__device__ __forceinline__ void rope_vec_warp(const __nv_bfloat16* __restrict__ src, __nv_bfloat16* dst, int pos,
+                                              const RopeTables& tb) {
+  constexpr int P = D / 64;                    // 4 (D=256) or 8 (D=512)
+  constexpr int half = D / 2;
+  const int lane = threadIdx.x & 31;
+  const int t0 = lane * P;
+  using Vec = typename std::conditional<P == 8, uint4, uint2>::type;
+  Vec lo = *reinterpret_cast<const Vec*>(src + t0);
+  Vec hi = *reinterpret_cast<const Vec*>(src + half + t0);
+  if (t0 < R) {                                 // R is a multiple of P: whole lanes turn or not
+    uint32_t* lw = reinterpret_cast<uint32_t*>(&lo);
+    uint32_t* hw = reinterpret_cast<uint32_t*>(&hi);
+#pragma unroll
+    for (int w = 0; w < P / 2; ++w) {
+      float a0 = bf16_lo(lw[w]), a1 = bf16_hi(lw[w]);
+      float b0 = bf16_lo(hw[w]), b1 = bf16_hi(hw[w]);
+      rope_pair(a0, b0, rope_cs(tb, t0 + 2 * w, pos));
+      rope_pair(a1, b1, rope_cs(tb, t0 + 2 * w + 1, pos));
+      lw[w] = pack_bf16(a0, a1);
+      hw[w] = pack_bf16(b0, b1);
+    }
+  }
+  *reinterpret_cast<Vec*>(dst + t0) = lo;
+  *reinterpret_cast<Vec*>(dst + half + t0) = hi;
+}
+
+template <int D>
+__device__ __forceinline__ void copy_vec_warp(const __nv_bfloat16* __restrict__ src, __nv_bfloat16* dst) {
+  constexpr int E = D / 32;                    // elements per lane: 8 or 16
+  const int lane = threadIdx.x & 31;
+  const uint4* s = reinterpret_cast<const uint4*>(src + lane * 8);
+  uint4* d = reinterpret_cast<uint4*>(dst + lane * 8);
+#pragma unroll
+  for (int i = 0; i < E / 8; ++i) d[i * 32] = s[i * 32];
+}
+
+template <int D, int R>
+__global__ void __launch_bounds__(256) rope_apply_kernel(const __nv_bfloat16* __restrict__ x,
+                                                         const int32_t* __restrict__ pos, int T, int H,
+                                                         __nv_bfloat16* out, RopeTables tb, uint32_t* err) {
+  const long long vec = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (vec >= (long long)T * H) return;
+  const int row = (int)(vec / H);
+  const int p = pos[row];
+  if (p < 0 || p >= kMaxPos) {
+    if ((threadIdx.x & 31) == 0) set_error(err, kErrPos);
+    return;
+  }
+  rope_vec_warp<D, R>(x + vec * D, out + vec * D, p, tb);
+}
+
+cudaError_t launch_rope_apply(bool global, const void* x, const int32_t* pos, int T, int H, void* out,
+                              const DeviceState& st, cudaStream_t s) {
+  const long long vecs = (long long)T * H;
+  if (vecs == 0) return cudaSuccess;
+  const unsigned blocks = (unsigned)((vecs + 7) / 8);
+  if (global)
+    rope_apply_kernel<kGlobalD, kGlobalR><<<blocks, 256, 0, s>>>((const __nv_bfloat16*)x, pos, T, H,
+                                                                  (__nv_bfloat16*)out, st.global, st.err);
+  else
+    rope_apply_kernel<kSlidingD, kSlidingR><<<blocks, 256, 0, s>>>((const __nv_bfloat16*)x, pos, T, H,
+                                                                    (__nv_bfloat16*)out, st.sliding, st.err);
+  return cudaGetLastError();
+}
+
+// ---- paged KV append ----------------------------------------------------------------------------
+// Writes one token's Hkv vectors into its page slot: sliding K' = bf16(RoPE(k)) and V as given;
+// global S as given (K==V: the one stored projection, rotated only where it is read as K).
+template <int D, int R, int HKV, bool SHARED>
+__device__ __forceinline__ void append_token(const __nv_bfloat16* k_row, const __nv_bfloat16* v_row, int b, int pos,
+                                             const PagedCache& c, const RopeTables& tb, uint32_t* err) {
+  const int lane = threadIdx.x & 31;
+  if (pos < 0 || pos >= kMaxPos || (pos >> 4) >= c.max_pages) {
+    if (lane == 0) set_error(err, kErrPos);
+    return;
+  }
+  const int phys = c.page_table[(size_t)b * c.max_pages + (pos >> 4)];
+  if (phys < 0 || phys >= c.num_pages) {
+    if (lane == 0) set_error(err, kErrPage);
+    return;
+  }
+  const size_t slot = ((size_t)phys * HKV * kPage + (pos & 15)) * D;   // + g * kPage * D
+  __nv_bfloat16* ck = (__nv_bfloat16*)c.k;
+  for (int g = 0; g < HKV; ++g) {
+    const size_t dst = slot + (size_t)g * kPage * D;
+    if (SHARED) {
+      copy_vec_warp<D>(k_row + (size_t)g * D, ck + dst);
+    } else {
+      rope_vec_warp<D, R>(k_row + (size_t)g * D, ck + dst, pos, tb);
+      copy_vec_warp<D>(v_row + (size_t)g * D, (__nv_bfloat16*)c.v + dst);
+    }
+  }
+}
+
+// One warp per row of the prefill batch; the owning sequence is found by a scan over B.
+template <int D, int R, int HKV, bool SHARED>
+__global__ void __launch_bounds__(256) append_prefill_kernel(const __nv_bfloat16* __restrict__ k,
+                                                             const __nv_bfloat16* __restrict__ v, SeqRows rows,
+                                                             PagedCache cache, RopeTables tb, uint32_t* err) {
+  const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= rows.T) return;
+  int owner = -1;
+  for (int b0 = 0; b0 < rows.B; b0 += 32) {
+    const int b = b0 + lane;
+    bool mine = false;
+    if (b < rows.B) {
+      const int s = rows.q_start[b], L = rows.q_len[b];
+      mine = (L > 0 && r >= s && r - s < L);
+    }
+    const unsigned m = __ballot_sync(0xffffffffu, mine);
+    if (m) {
+      owner = b0 + __ffs(m) - 1;
+      break;
+    }
+  }
+  if (owner < 0) return;
+  const int pos = rows.ctx_start[owner] + (r - rows.q_start[owner]);
+  append_token<D, R, HKV, SHARED>(k + (size_t)r * HKV * D, SHARED ? nullptr : v + (size_t)r * HKV * D, owner, pos,
+                                  cache, tb, err);
+}
+
+template <int D, int R, int HKV, bool SHARED>
+__global__ void __launch_bounds__(256) append_decode_kernel(const __nv_bfloat16* __restrict__ k,
+                                                            const __nv_bfloat16* __restrict__ v,
+                                                            const int32_t* __restrict__ seq_len, int B,
+                                                            PagedCache cache, RopeTables tb, uint32_t* err) {
+  const int b = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (b >= B) return;
+  append_token<D, R, HKV, SHARED>(k + (size_t)b * HKV * D, SHARED ? nullptr : v + (size_t)b * HKV * D, b,
+                                  seq_len[b] - 1, cache, tb, err);
+}
+
+cudaError_t launch_append_prefill(bool global, const void* k, const void* v, const SeqRows& rows,
+                                  const PagedCache& cache, const DeviceState& st, cudaStream_t s) {
+  if (rows.T <= 0 || rows.B <= 0) return cudaSuccess;
+  const unsigned blocks = (unsigned)((rows.T + 7) / 8);
+  if (global)
+    append_prefill_kernel<kGlobalD, kGlobalR, kGlobalHkv, true><<<blocks, 256, 0, s>>>(
+        (const __nv_bfloat16*)k, nullptr, rows, cache, st.global, st.err);
+  else
+    append_prefill_kernel<kSlidingD, kSlidingR, kSlidingHkv, false><<<blocks, 256, 0, s>>>(
+        (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, rows, cache, st.sliding, st.err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_append_decode(bool global, const void* k_new, const void* v_new, const int32_t* seq_len,
+                                 int B, const PagedCache& cache, const DeviceState& st, cudaStream_t s) {
+  if (B <= 0) return cudaSuccess;
+  const unsigned blocks = (unsigned)((B + 7) / 8);
+  if (global)
+    append_decode_kernel<kGlobalD, kGlobalR, kGlobalHkv, true><<<blocks, 256, 0, s>>>(
+        (const __nv_bfloat16*)k_new, nullptr, seq_len, B, cache, st.global, st.err);
+  else
+    append_decode_kernel<kSlidingD, kSlidingR, kSlidingHkv, false><<<blocks, 256, 0, s>>>(
+        (const __nv_bfloat16*)k_new, (const __nv_bfloat16*)v_new, seq_len, B, cache, st.sliding, st.err);
+  return cudaGetLastError();
+}
+
+}  // namespace g4

@@ -1,0 +1,120 @@
+"""CPU checks of the C ABI: the library builds, loads without a GPU, exports every symbol the
+header declares, and refuses bad arguments on the host before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import invariant_hybrid_attention_gb300 as g4
+from invariant_hybrid_attention_gb300 import build as g4build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    g4build.build()
+    return g4.load()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "g4attn.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(g4attn_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("g4attn_prefill", "g4attn_decode", "g4attn_rope_apply"):
+        assert n in names
+    assert set(names) == set(g4.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    syms = os.popen(f"nm -D {g4.LIB_PATH}").read()
+    for name in declared_functions():
+        assert re.search(rf"\sT\s{name}$", syms, flags=re.M), name
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert len(g4.status_string(s)) > 0
+    assert g4.status_string(g4.G4_ERR_UNSUPPORTED) == "unsupported geometry"
+
+
+def test_unsupported_geometry_fails_closed(lib):
+    bad = g4.sliding_layer()
+    bad.head_dim = 128
+    assert lib.g4attn_provenance(ctypes.byref(bad), None, 0) == -1
+    cache = g4.g4attn_cache(16, 32, 4, 16)
+    st = lib.g4attn_prefill(ctypes.byref(bad), 16, 16, 16, 8, 16, 16, 16, 1, ctypes.byref(cache), 16, 1, 16, None)
+    assert st == g4.G4_ERR_UNSUPPORTED
+    glob = g4.global_layer()
+    glob.rope_partial = 0.5
+    assert lib.g4attn_rope_apply(ctypes.byref(glob), 16, 16, 4, 1, 16, None) == g4.G4_ERR_UNSUPPORTED
+    win = g4.global_layer()
+    win.window = 1024          # a window on a global layer is not a supported geometry
+    assert lib.g4attn_decode_workspace_bytes(ctypes.byref(win), 4, 4) == 0
+    s = g4.sliding_layer()
+    s.window = 0
+    assert lib.g4attn_rope_apply(ctypes.byref(s), 16, 16, 4, 1, 16, None) == g4.G4_ERR_UNSUPPORTED
+
+
+def test_invalid_arguments_refused_on_host(lib):
+    s = g4.sliding_layer()
+    cache = g4.g4attn_cache(16, 32, 4, 16)
+    # NULL q
+    assert lib.g4attn_prefill(ctypes.byref(s), None, 16, 16, 8, 16, 16, 16, 1, ctypes.byref(cache), 16, 1, 16,
+                              None) == g4.G4_ERR_INVALID
+    # misaligned q
+    assert lib.g4attn_prefill(ctypes.byref(s), 18, 16, 16, 8, 16, 16, 16, 1, ctypes.byref(cache), 16, 1, 16,
+                              None) == g4.G4_ERR_INVALID
+    # B = 0
+    assert lib.g4attn_prefill(ctypes.byref(s), 16, 16, 16, 8, 16, 16, 16, 0, ctypes.byref(cache), 16, 1, 16,
+                              None) == g4.G4_ERR_INVALID
+    # page size other than 16
+    c8 = g4.g4attn_cache(16, 32, 4, 8)
+    assert lib.g4attn_prefill(ctypes.byref(s), 16, 16, 16, 8, 16, 16, 16, 1, ctypes.byref(c8), 16, 1, 16,
+                              None) == g4.G4_ERR_UNSUPPORTED
+    # a global layer given a V tensor (K==V takes none)
+    gl = g4.global_layer()
+    cg = g4.g4attn_cache(16, 32, 4, 16)
+    assert lib.g4attn_prefill(ctypes.byref(gl), 16, 16, 16, 8, 16, 16, 16, 1, ctypes.byref(cg), 16, 1, 16,
+                              None) == g4.G4_ERR_INVALID
+    # scale must be finite and positive
+    s2 = g4.sliding_layer(softmax_scale=-1.0)
+    assert lib.g4attn_rope_apply(ctypes.byref(s2), 16, 16, 4, 1, 16, None) == g4.G4_ERR_INVALID
+    # too small a decode workspace
+    ws_need = lib.g4attn_decode_workspace_bytes(ctypes.byref(s), 4, 100)
+    assert ws_need > 0
+    assert lib.g4attn_decode(ctypes.byref(s), 16, 16, 16, 16, 4, ctypes.byref(cache), 16, 100, 16, 16,
+                             ws_need - 1, None) == g4.G4_ERR_INVALID
+
+
+def test_workspace_sizes(lib):
+    s, gl = g4.sliding_layer(), g4.global_layer()
+    # sliding: a 1024-key window touches at most 5 chunks of 256 keys; partial = (m, l) + 256 floats
+    n = lib.g4attn_decode_workspace_bytes(ctypes.byref(s), 64, 2048)
+    assert n >= 64 * 32 * 5 * (256 + 2) * 4
+    # global: 32768 keys = 32 chunks of 1024
+    n = lib.g4attn_decode_workspace_bytes(ctypes.byref(gl), 64, 2048)
+    assert n >= 64 * 32 * 32 * (512 + 2) * 4
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    monkeypatch.setattr(g4, "_lib", None)
+    with pytest.raises(RuntimeError, match="not found"):
+        g4.load(str(tmp_path / "nope.so"))
+
+
+def test_product_path_never_imports_the_oracle():
+    pkg = os.path.join(ROOT, "invariant_hybrid_attention_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", text, flags=re.M), f
+                assert "oracle/" not in text and "oracle." not in text, f

@@ -1,0 +1,176 @@
+"""GPU parity: every CUDA entry point against the fp64 oracle on the same seeded inputs.
+
+Bars: max-abs 2e-2 and mean-abs 2e-3 on bf16 outputs (fp32 accumulation); bit-exact where the
+operation is a copy (p-RoPE's untouched pairs, V and S written into the cache).
+"""
+import numpy as np
+import pytest
+import torch
+
+import invariant_hybrid_attention_gb300 as g4
+import oracle
+from invariant_hybrid_attention_gb300 import inputs as gi
+from invariant_hybrid_attention_gb300.paged import device_int32
+
+from gpu_cases import GEOM, Batch, DecodeBatch, assert_close, f64, layers
+
+pytestmark = pytest.mark.gpu
+
+
+def bf16_round_bound(ref: np.ndarray) -> np.ndarray:
+    """Half a bf16 ulp of |ref| plus a small fp32 slack: the bound on one RNE cast."""
+    a = np.abs(ref)
+    e = np.floor(np.log2(np.maximum(a, 1e-30)))
+    return np.where(a > 0, 2.0 ** (e - 8), 0) + 1e-6 * (1 + a)
+
+
+# ---------------------------------------------------------------- RoPE / p-RoPE
+
+@pytest.mark.parametrize("kind", ["sliding", "global"])
+def test_rope_apply_matches_oracle(kind):
+    layer, olayer = layers(kind)
+    D = GEOM[kind]["d"]
+    T, H = 300, 7
+    x = gi.bf16_normal((T, H, D), 3, 2.0)
+    pos = torch.tensor(gi.uniform_ints(T, 0, oracle.MAX_POSITIONS - 1, 4), dtype=torch.int32)
+    pos[:4] = torch.tensor([0, 1, 255, oracle.MAX_POSITIONS - 1], dtype=torch.int32)
+    out = g4.g4attn_rope_apply(layer, x.cuda(), pos.cuda(), out=torch.empty((T, H, D), dtype=torch.bfloat16,
+                                                                            device="cuda"))
+    torch.cuda.synchronize()
+    want = oracle.rope(x.double().numpy(), pos.numpy()[:, None], olayer.rope_theta, olayer.rope_partial)
+    got = f64(out)
+    assert (np.abs(got - want) <= bf16_round_bound(want) + 2e-6 * np.abs(want) + 1e-6).all()
+    R = oracle.rope_rotated_pairs(D, olayer.rope_partial)
+    keep = np.r_[R:D // 2, D // 2 + R:D]
+    assert torch.equal(out.cpu()[:, :, keep], x[:, :, keep])          # untouched pairs: bit for bit
+    # in place gives the same bits
+    xi = x.cuda()
+    g4.g4attn_rope_apply(layer, xi, pos.cuda())
+    torch.cuda.synchronize()
+    assert torch.equal(xi.cpu(), out.cpu())
+
+
+# ---------------------------------------------------------------- cache append
+
+@pytest.mark.parametrize("kind", ["sliding", "global"])
+def test_kv_append_writes_the_contract_layout(kind):
+    layer, olayer = layers(kind)
+    bt = Batch(kind, [37, 5, 70], ctx_starts=[0, 20, 3], seed=5)
+    cache = bt.device_cache()
+    table = bt.plan.table.cuda()
+    bt.append_history(layer, cache, table)
+    g4.g4attn_kv_append(layer, bt.k_rows.cuda(), None if bt.v_rows is None else bt.v_rows.cuda(),
+                        device_int32(bt.layout.q_start), device_int32(bt.layout.q_len),
+                        device_int32(bt.layout.ctx_start), cache.desc, table)
+    torch.cuda.synchronize()
+    assert g4.g4attn_status_sync() == g4.G4_OK
+    kc = cache.k.cpu()
+    vc = None if cache.v is None else cache.v.cpu()
+    for b, L in enumerate(bt.ctx_lens):
+        for pos in range(L):
+            page = int(bt.plan.table[b, pos // 16])
+            stored = kc[page, :, pos % 16, :]
+            raw = bt.hist_k[b][pos]
+            if kind == "global":
+                assert torch.equal(stored, raw)                          # S stored un-rotated
+            else:
+                want = oracle.rope(raw.double().numpy(), pos, olayer.rope_theta, olayer.rope_partial)
+                got = stored.double().numpy()
+                assert (np.abs(got - want) <= bf16_round_bound(want) + 1e-6).all()
+                assert torch.equal(vc[page, :, pos % 16, :], bt.hist_v[b][pos])
+
+
+# ---------------------------------------------------------------- decode
+
+DECODE_CASES = {
+    "sliding-w1024": ("sliding", 1024, [1, 2, 17, 255, 256, 257, 1023, 1024, 1025, 3000, 4097]),
+    "sliding-w64": ("sliding", 64, [1, 16, 63, 64, 65, 200, 513]),
+    "global": ("global", 0, [1, 15, 16, 17, 1023, 1024, 1025, 2049, 5000]),
+}
+
+
+@pytest.mark.parametrize("case", list(DECODE_CASES))
+def test_decode_matches_oracle(case):
+    kind, window, lens = DECODE_CASES[case]
+    layer, olayer = layers(kind, window if window else 1024)
+    db = DecodeBatch(kind, lens, seed=11, window=window, sliding_window_only=(kind == "sliding"))
+    out, _ = db.run(layer)
+    got = f64(out)
+    for b in range(len(lens)):
+        assert_close(got[b], db.oracle_row(olayer, b), f"{case} request {b} (len {lens[b]})")
+
+
+@pytest.mark.parametrize("kind", ["sliding", "global"])
+def test_decode_is_batch_invariant(kind):
+    """The same request (same data, same pages) alone and inside a larger ragged batch at a
+    different index gives the same bits."""
+    layer, _ = layers(kind)
+    target_len = 2500
+    alone = DecodeBatch(kind, [target_len], seed=21)
+    out_a, _ = alone.run(layer)
+    mixed_lens = [700, 3, target_len, 1500, 4000]
+    mixed = DecodeBatch(kind, mixed_lens, seed=21)
+    # give index 2 the target's data
+    mixed.hist_k[2] = alone.hist_k[0]
+    if kind == "sliding":
+        mixed.hist_v[2] = alone.hist_v[0]
+    mixed.q[2] = alone.q[0]
+    out_m, _ = mixed.run(layer)
+    assert torch.equal(out_a[0].cpu(), out_m[2].cpu())
+
+
+# ---------------------------------------------------------------- sliding prefill
+
+def check_prefill(bt: Batch, kind, window, sample=None):
+    layer, olayer = layers(kind, window)
+    out, _ = bt.run(layer)
+    got = f64(out)
+    covered = np.zeros(bt.layout.T, dtype=bool)
+    for b, L in enumerate(bt.q_lens):
+        s = bt.layout.q_start[b]
+        covered[s:s + L] = True
+        if L == 0:
+            continue
+        rows = None if sample is None or L <= sample else np.unique(
+            np.r_[0, L - 1, np.random.default_rng(b).choice(L, sample, replace=False)])
+        want = bt.oracle_rows(olayer, b, rows)
+        idx = np.arange(L) if rows is None else rows
+        assert_close(got[s + idx], want, f"sequence {b} (len {L}, ctx {bt.ctx_starts[b]})")
+    # rows outside every sequence are never written
+    assert np.isnan(got[~covered]).all()
+    return out
+
+
+def test_prefill_sliding_tiny_oracle_case():
+    """Two causal sequences of 96 and 200 tokens, window shrunk to 64, N(0,1) inputs, seed 0."""
+    check_prefill(Batch("sliding", [96, 200], seed=0), "sliding", 64)
+
+
+@pytest.mark.parametrize("window", [1024, 64, 1])
+@pytest.mark.parametrize("padded", [False, True], ids=["packed", "padded"])
+def test_prefill_sliding_ragged(window, padded):
+    bt = Batch("sliding", [1, 5, 127, 128, 129, 700, 1300], padded=padded, seed=3, scale=0.5)
+    check_prefill(bt, "sliding", window, sample=96)
+
+
+def test_prefill_sliding_chunked_with_history():
+    """Chunks that start mid-sequence read earlier keys from the cache (written by kv_append)."""
+    bt = Batch("sliding", [300, 64, 1, 200], ctx_starts=[1000, 77, 4000, 129], seed=4, scale=0.5)
+    check_prefill(bt, "sliding", 1024, sample=96)
+
+
+def test_prefill_sliding_batch_invariance():
+    """A target sequence alone, packed among others and padded at another index: same bits."""
+    layer, _ = layers("sliding", 1024)
+    L = 1500
+    alone = Batch("sliding", [L], seed=9, scale=0.5)
+    out_a, _ = alone.run(layer)
+    for lens, padded, at in [([200, L, 33], False, 1), ([L, 900], True, 0), ([5, 77, 1030, L], True, 3)]:
+        bt = Batch("sliding", lens, padded=padded, seed=9 + len(lens), scale=0.5)
+        bt.hist_k[at], bt.hist_v[at] = alone.hist_k[0], alone.hist_v[0]
+        s = bt.layout.q_start[at]
+        bt.q[s:s + L] = alone.q[:L]
+        bt.k_rows = gi.rows_of(bt.hist_k, bt.layout)
+        bt.v_rows = gi.rows_of(bt.hist_v, bt.layout)
+        out_b, _ = bt.run(layer)
+        assert torch.equal(out_a[:L].cpu(), out_b[s:s + L].cpu()), (lens, padded, at)
