@@ -37,9 +37,11 @@
  *   q, out         [T][n_q_heads][head_dim]           query rows / output rows
  *   k, v           [T][n_kv_heads][head_dim]          new key / value rows of a prefill
  *   k_new, v_new   [B][n_kv_heads][head_dim]          the decode token's key / value
- *   cache->k       [num_pages][n_kv_heads][page_size][head_dim]  sliding K' (roped) or
- *                                                    global S (un-rotated, K==V)
- *   cache->v       same shape; sliding V; NULL on global layers
+ *   cache->k       [num_pages][n_kv_heads][2][head_dim/8][8][8]: one page-head block of
+ *                  16 keys x head_dim dims stored as 8x8 core matrices, key j and dim d at
+ *                  [j/8][d/8][j%8][d%8] (16*head_dim contiguous bf16 per page and head);
+ *                  sliding K' (roped) or global S (un-rotated, K==V)
+ *   cache->v       same layout; sliding V; NULL on global layers
  *   page_table     int32 [B][max_pages]: physical page of logical page i of sequence b
  *                  (keys 16i .. 16i+15). Entries that no call needs may hold anything.
  *   All pointers 16-byte aligned.

@@ -134,9 +134,11 @@ g4_status g4attn_prefill(const g4attn_layer* layer, const void* q, const void* k
   const cudaStream_t cs = (cudaStream_t)stream;
   const SeqRows rows{q_start, q_len, ctx_start, B, T};
   const PagedCache pc = paged(cache, page_table, max_pages);
-  cudaError_t e = launch_append_prefill(global, k, v, rows, pc, st, cs);
+  // Launch 1: cache append, and the roped queries staged in `out` (each sequence row of `out`
+  // holds its roped query until launch 2 overwrites it with the attention output).
+  cudaError_t e = launch_append_prefill(global, k, v, rows, pc, st, cs, q, out);
   if (e != cudaSuccess) return G4_ERR_CUDA;
-  return from_cuda(launch_prefill(global, q, rows, global ? 0 : layer->window, scale_log2(layer), pc, out, st, cs));
+  return from_cuda(launch_prefill(global, rows, global ? 0 : layer->window, scale_log2(layer), pc, out, st, cs));
 }
 
 size_t g4attn_decode_workspace_bytes(const g4attn_layer* layer, int32_t B, int32_t max_pages) {

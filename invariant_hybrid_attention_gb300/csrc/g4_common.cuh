@@ -16,8 +16,9 @@ namespace g4 {
 // ---- constants fixed by the two supported layer kinds ------------------------------------
 constexpr int kPage = 16;                 // keys per cache page
 constexpr int kMaxPos = 262144;           // positions 0 .. 262143
-constexpr int kRopeCoarse = kMaxPos / 256;  // coarse table rows: angle of 256*c
-constexpr int kRopeFine = 256;              // fine table rows: angle of p, 0 <= p < 256
+constexpr int kRopeCoarse = kMaxPos / 256;  // coarse table: angle of 256*c, 0 <= c < 1024
+constexpr int kRopeMid = 16;                // mid table: angle of 16*a, 0 <= a < 16
+constexpr int kRopeFine = 16;               // fine table: angle of b, 0 <= b < 16
 
 constexpr int kSlidingHq = 32, kSlidingHkv = 16, kSlidingD = 256, kSlidingR = 128;
 constexpr int kGlobalHq = 32, kGlobalHkv = 4, kGlobalD = 512, kGlobalR = 64;
@@ -31,10 +32,23 @@ enum : uint32_t { kErrTimeout = 1u, kErrPage = 2u, kErrPos = 4u };
 // Bounded waits give up after this long; nothing legitimate waits anywhere near it.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
-// RoPE cos/sin tables for one layer kind: coarse[t][c] = (cos, sin)(256*c*f_t) and
-// fine[t][p] = (cos, sin)(p*f_t), built in fp64 on the host and stored as fp32.
+// Cache page layout. One page of one KV head holds 16 keys x D dims as core matrices of
+// 8 keys x 8 dims (128 contiguous bytes): key j, dim d sits at element
+//   ((j / 8) * (D / 8) + d / 8) * 64 + (j % 8) * 8 + d % 8
+// of the page-head block, whose 16*D elements are contiguous at
+//   cache + (page * Hkv + head) * 16 * D.
+// One contiguous copy of a block lands in shared memory as an operand the tensor cores read
+// directly (K-major for K, MN-major for V), and every 8x8 block is one ldmatrix tile.
+__host__ __device__ constexpr int tiled_offset(int j, int d, int D) {
+  return ((j >> 3) * (D >> 3) + (d >> 3)) * 64 + (j & 7) * 8 + (d & 7);
+}
+
+// RoPE cos/sin tables for one layer kind, built in fp64 on the host and stored as fp32:
+// coarse[t][c] = (cos, sin)(256*c*f_t), mid[t][a] = (cos, sin)(16*a*f_t) and
+// fine[t][b] = (cos, sin)(b*f_t). The mid and fine tables are small enough to stay in L1.
 struct RopeTables {
   const float2* coarse;   // [R][kRopeCoarse]
+  const float2* mid;      // [R][kRopeMid]
   const float2* fine;     // [R][kRopeFine]
 };
 
@@ -64,13 +78,28 @@ G4_DEV uint32_t pack_bf16(float lo, float hi) {
 }
 G4_DEV float round_bf16(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
 
-// (cos, sin)(pos * f_t) from the two-level table by the angle-addition formula.
+// Complex product (cos a, sin a) * (cos b, sin b) = (cos, sin)(a + b), fp32.
+G4_DEV float2 cmul(float2 a, float2 b) {
+  return make_float2(fmaf(a.x, b.x, -(a.y * b.y)), fmaf(a.y, b.x, a.x * b.y));
+}
+
+// (cos, sin)(pos * f_t) from the three-level table by the angle-addition formula:
+// pos = 256*c + 16*a + b, combined as (coarse * mid) * fine.
 G4_DEV float2 rope_cs(const RopeTables& tb, int t, int pos) {
-  const float2 a = __ldg(tb.coarse + (size_t)t * kRopeCoarse + (pos >> 8));
-  const float2 b = __ldg(tb.fine + (size_t)t * kRopeFine + (pos & 255));
-  float c = fmaf(a.x, b.x, -(a.y * b.y));
-  float s = fmaf(a.y, b.x, a.x * b.y);
-  return make_float2(c, s);
+  const float2 c = __ldg(tb.coarse + (size_t)t * kRopeCoarse + (pos >> 8));
+  const float2 m = __ldg(tb.mid + t * kRopeMid + ((pos >> 4) & 15));
+  const float2 f = __ldg(tb.fine + t * kRopeFine + (pos & 15));
+  return cmul(cmul(c, m), f);
+}
+
+// 2^x on the multi-function unit (PTX ex2.approx.ftz.f32; 2^-inf = +0). Results below 2^-126
+// flush to zero: in the softmax they are weights under 2^-126 next to a row maximum of 1, far
+// below what an fp32 accumulator or the bf16 output resolves. The non-flushing form costs
+// about three times as much issue time here.
+G4_DEV float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // The rotation of one half-split pair, fp32 (the same expression everywhere in the library).
@@ -120,6 +149,19 @@ G4_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, uint3
       return false;
     }
   }
+}
+
+// Named barrier over `count` threads that also ANDs a predicate across them. Every thread of
+// the group must reach it; the waits before it are bounded, so it is reached in bounded time.
+G4_DEV bool named_barrier_and(uint32_t id, uint32_t count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
 }
 
 // ---- bulk copies (TMA) -------------------------------------------------------------------------
@@ -179,6 +221,18 @@ G4_DEV uint64_t desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
   d |= (uint64_t)1 << 46;
   d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// Shared-memory matrix descriptor, no swizzle (core matrices of 8 rows x 16 bytes stored as
+// 128 contiguous bytes). lbo = byte distance between core matrices adjacent along K,
+// sbo = along M/N (both for K-major and MN-major operands).
+G4_DEV uint64_t desc_tiled(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
   return d;
 }
 

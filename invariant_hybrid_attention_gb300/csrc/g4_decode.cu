@@ -116,12 +116,12 @@ __global__ void __launch_bounds__(128) decode_sliding_kernel(DecodeParams p) {
   const __nv_bfloat16* kc = (const __nv_bfloat16*)p.cache.k;
   const __nv_bfloat16* vc = (const __nv_bfloat16*)p.cache.v;
   for (int pg = pg0 + warp; pg <= pg1; pg += 4) {
-    const size_t base = (((size_t)pt[pg] * kSlidingHkv + g) * kPage) * kSD + lane * 8;
+    const size_t base = (((size_t)pt[pg] * kSlidingHkv + g) * kPage) * kSD;   // page-head block
     uint4 kr[16], vr[16];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) kr[j] = ldg_nc(kc + base + (size_t)j * kSD);
+    for (int j = 0; j < 16; ++j) kr[j] = ldg_nc(kc + base + tiled_offset(j, lane * 8, kSD));
 #pragma unroll
-    for (int j = 0; j < 16; ++j) vr[j] = ldg_nc(vc + base + (size_t)j * kSD);
+    for (int j = 0; j < 16; ++j) vr[j] = ldg_nc(vc + base + tiled_offset(j, lane * 8, kSD));
 
     // Partial dot products over this lane's 8 dims: index 2*key + head.
     float part[32];
@@ -236,8 +236,8 @@ __global__ void __launch_bounds__(128) decode_sliding_kernel(DecodeParams p) {
 constexpr int kGD = kGlobalD;
 constexpr int kGWarps = 4;
 constexpr int kGStages = 3;                      // pages in flight per warp
-constexpr int kGRow = kGD * 2 + 16;              // padded smem row: ldmatrix rows hit distinct banks
-constexpr int kGStageBytes = kPage * kGRow;      // 16640
+constexpr int kGStageBytes = kPage * kGD * 2;    // one tiled page-head block: 16 KB
+constexpr int kGRow = kGD * 2 + 16;              // padded query row: ldmatrix rows hit distinct banks
 constexpr int kGQBytes = 8 * kGRow;              // the 8 roped query heads
 constexpr int kGPRow = 48;                       // P^T staging row (8 heads x 16 keys bf16, padded)
 constexpr int kGSmem = kGWarps * kGStages * kGStageBytes + kGQBytes + kGWarps * 8 * kGPRow + 256;
@@ -296,9 +296,8 @@ __global__ void __launch_bounds__(128, 1) decode_global_kernel(DecodeParams p) {
     const __nv_bfloat16* src = sc + (((size_t)pt[pg] * kGlobalHkv + g) * kPage) * kGD;
     uint8_t* dst = my_stages + (i % kGStages) * kGStageBytes;
     uint64_t* bar = &my_bars[i % kGStages];
-    mbar_arrive_expect_tx(bar, kPage * kGD * 2);
-#pragma unroll 1
-    for (int r = 0; r < kPage; ++r) bulk_g2s(dst + r * kGRow, src + (size_t)r * kGD, kGD * 2, bar);
+    mbar_arrive_expect_tx(bar, kGStageBytes);
+    bulk_g2s(dst, src, kGStageBytes, bar);
   };
   int n_issued = 0, n_done = 0;   // lane 0's view of this warp's copies
   if (lane == 0)
@@ -325,11 +324,12 @@ __global__ void __launch_bounds__(128, 1) decode_global_kernel(DecodeParams p) {
   for (int mt = 0; mt < 32; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
   float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
 
-  // ldmatrix lane addressing (byte offsets inside a page stage / the query block).
-  const int a_row = (lane & 7) + ((lane >> 3) & 1) * 8;   // K as A (non-transposed)
-  const int a_col = (lane >> 4) * 8;
-  const int v_row = (lane & 7) + ((lane >> 4) & 1) * 8;   // V^T as A (transposed load)
-  const int v_col = ((lane >> 3) & 1) * 8;
+  // ldmatrix lane addressing. A page stage is tiled (8 keys x 8 dims core matrices of 128 B,
+  // key group kg and dim group dg at (kg * 64 + dg) * 128): each 8x8 ldmatrix tile is one
+  // core matrix. K as A (non-transposed): tiles (keys 0-7 | 8-15) x (dims +0 | +8);
+  // V^T as A (transposed): tiles (dims +0 | +8) x (keys 0-7 | 8-15).
+  const uint32_t a_lane = (((lane >> 3) & 1) * 64 + (lane >> 4)) * 128 + (lane & 7) * 16;
+  const uint32_t v_lane = (((lane >> 4) & 1) * 64 + ((lane >> 3) & 1)) * 128 + (lane & 7) * 16;
   const uint32_t q_lane = q_addr + (lane & 7) * kGRow + (lane >> 3) * 16;
 
   for (int i = 0; i < n_mine; ++i) {
@@ -340,8 +340,9 @@ __global__ void __launch_bounds__(128, 1) decode_global_kernel(DecodeParams p) {
     const int key0 = (pg0 + warp + kGWarps * i) * kPage;
     if (key0 + kPage - 1 > k_end) {   // zero stale rows (NaN-safe V), then make them visible
       for (int idx = lane; idx < kPage * (kGD / 8); idx += 32) {
-        const int r = idx / (kGD / 8), col = idx % (kGD / 8);
-        if (key0 + r > k_end) *reinterpret_cast<uint4*>(page + r * kGRow + col * 16) = make_uint4(0, 0, 0, 0);
+        const int r = idx / (kGD / 8), dg = idx % (kGD / 8);
+        if (key0 + r > k_end)
+          *reinterpret_cast<uint4*>(page + ((r >> 3) * (kGD / 8) + dg) * 128 + (r & 7) * 16) = make_uint4(0, 0, 0, 0);
       }
       __syncwarp();
     }
@@ -352,8 +353,8 @@ __global__ void __launch_bounds__(128, 1) decode_global_kernel(DecodeParams p) {
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks) {   // rotated k-steps: dims 16ks.. with partners +256
       uint32_t a[4], h[4], bq0, bq1, bh0, bh1;
-      ldsm_x4(pa + a_row * kGRow + (ks * 16 + a_col) * 2, a[0], a[1], a[2], a[3]);
-      ldsm_x4(pa + a_row * kGRow + ((ks + 16) * 16 + a_col) * 2, h[0], h[1], h[2], h[3]);
+      ldsm_x4(pa + a_lane + (2 * ks) * 128, a[0], a[1], a[2], a[3]);
+      ldsm_x4(pa + a_lane + (2 * (ks + 16)) * 128, h[0], h[1], h[2], h[3]);
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
         const int key = key0 + gq + 8 * (r & 1);
@@ -374,8 +375,8 @@ __global__ void __launch_bounds__(128, 1) decode_global_kernel(DecodeParams p) {
     for (int kp = 0; kp < 32; kp += 2) {   // plain k-steps, two at a time
       if ((kp >= 0 && kp < 4) || (kp >= 16 && kp < 20)) continue;
       uint32_t a[4], a2[4], b0, b1, b2, b3;
-      ldsm_x4(pa + a_row * kGRow + (kp * 16 + a_col) * 2, a[0], a[1], a[2], a[3]);
-      ldsm_x4(pa + a_row * kGRow + ((kp + 1) * 16 + a_col) * 2, a2[0], a2[1], a2[2], a2[3]);
+      ldsm_x4(pa + a_lane + (2 * kp) * 128, a[0], a[1], a[2], a[3]);
+      ldsm_x4(pa + a_lane + (2 * (kp + 1)) * 128, a2[0], a2[1], a2[2], a2[3]);
       ldsm_x4(q_lane + kp * 32, b0, b1, b2, b3);
       mma16816(s0, a[0], a[1], a[2], a[3], b0, b1);
       mma16816(s1, a2[0], a2[1], a2[2], a2[3], b2, b3);
@@ -427,7 +428,7 @@ __global__ void __launch_bounds__(128, 1) decode_global_kernel(DecodeParams p) {
 #pragma unroll
     for (int mt = 0; mt < 32; ++mt) {
       uint32_t a0, a1, a2, a3;
-      ldsm_x4_t(pa + v_row * kGRow + (mt * 16 + v_col) * 2, a0, a1, a2, a3);
+      ldsm_x4_t(pa + v_lane + (2 * mt) * 128, a0, a1, a2, a3);
       mma16816(o[mt], a0, a1, a2, a3, pb0, pb1);
     }
     __syncwarp();

@@ -40,8 +40,11 @@ struct PagedCache {
 cudaError_t launch_rope_apply(bool global, const void* x, const int32_t* pos, int T, int H, void* out,
                               const DeviceState& st, cudaStream_t s);
 
+// Writes the rows' K'/V (or S) into the cache; with q_out set, also the rows' roped queries
+// (bf16) into q_out, the staging the prefill attention kernel reads its queries from.
 cudaError_t launch_append_prefill(bool global, const void* k, const void* v, const SeqRows& rows,
-                                  const PagedCache& cache, const DeviceState& st, cudaStream_t s);
+                                  const PagedCache& cache, const DeviceState& st, cudaStream_t s,
+                                  const void* q = nullptr, void* q_out = nullptr);
 
 cudaError_t launch_append_decode(bool global, const void* k_new, const void* v_new, const int32_t* seq_len,
                                  int B, const PagedCache& cache, const DeviceState& st, cudaStream_t s);
@@ -52,7 +55,9 @@ cudaError_t launch_decode(bool global, const void* q, const int32_t* seq_len, in
                           float scale_log2, const PagedCache& cache, void* out, void* ws,
                           const DeviceState& st, cudaStream_t s);
 
-cudaError_t launch_prefill(bool global, const void* q, const SeqRows& rows, int window, float scale_log2,
-                           const PagedCache& cache, void* out, const DeviceState& st, cudaStream_t s);
+// Attention over roped queries staged in `out` (by launch_append_prefill); writes the output
+// rows over them.
+cudaError_t launch_prefill(bool global, const SeqRows& rows, int window, float scale_log2, const PagedCache& cache,
+                           void* out, const DeviceState& st, cudaStream_t s);
 
 }  // namespace g4

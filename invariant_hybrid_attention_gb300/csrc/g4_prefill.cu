@@ -8,14 +8,19 @@
 //
 // Sliding layer (RFC section 5, sliding_attention_core: causal local attention, window 1024,
 // 32 Q / 16 KV heads, D 256). Per CTA:
-//   warp 0  TMA producer: paged K and V boxes (16 keys x 64 dims, 128B swizzle) into a
-//           2-stage ring; pages outside the needed key range are zero-filled, never looked up;
-//   warp 1  MMA issuer: S = Q K^T with Q in tensor memory (A operand) and K in shared memory,
-//           O += P V with P and V in shared memory; one elected lane issues, commits signal;
-//   warps 2-5  one thread per query row: Q load + RoPE into tensor memory, then per key tile
-//           the mask, the online softmax (lazy rescale, threshold 2^8), P (bf16) into shared
-//           memory, the O correction when needed, and the epilogue O / l -> bf16.
-// Tensor memory (512 columns): O [0,256), Q [256,384) bf16 pairs, S double buffer [384,512).
+//   warp 0  copy producer: one bulk copy per tiled page-head block (8 KB: 16 keys x 256 dims as
+//           8x8 core matrices) into a 2-stage ring; pages outside the needed key range are
+//           never looked up nor copied;
+//   warp 1  MMA issuer: S = Q K^T with Q (128B swizzle) and K (K-major, no swizzle) in shared
+//           memory, O += P V with P (128B swizzle) and V (MN-major, no swizzle) in shared
+//           memory; one elected lane issues, commits signal;
+//   warps 2-5  one thread per query row: per key tile the mask, the online softmax (lazy
+//           rescale, threshold 2^8), P (bf16) into shared memory, the O correction when
+//           needed, and the epilogue O / l -> bf16.
+// The queries arrive already roped: the cache-append pass before this kernel wrote
+// bf16(RoPE(q)) into the sequence rows of `out`; the producer's TMA loads the tile from there,
+// and the epilogue later overwrites exactly those rows (each row belongs to one CTA).
+// Tensor memory (512 columns): O [0,256), S double buffer [256,384).
 #include <math.h>
 
 #include "g4_internal.h"
@@ -28,14 +33,18 @@ constexpr int kBM = 128;                  // query rows per tile
 constexpr int kBN = 64;                   // keys per tile
 constexpr int kNS = 2;                    // K/V ring stages
 constexpr float kLazyRescale = 8.0f;
+constexpr int kSoftmaxThreads = 128;      // one thread per query row
+constexpr int kSlidingThreads = 64 + kSoftmaxThreads;
+constexpr int kQChunk = kBM * 128;         // roped Q tile: 128 rows x 64 dims per chunk, 128B swizzle
 
 // ---------------------------------------------------------------- sliding layer geometry
 constexpr int kSD = kSlidingD;            // 256
-constexpr int kSChunk = kBN * 128;        // one 64-dim chunk of a key tile: 64 rows x 128 B
-constexpr int kSKTile = (kSD / 64) * kSChunk;   // 32 KB
+constexpr int kPageBytes = kPage * kSD * 2;       // one tiled page-head block: 8 KB
+constexpr int kKeyGroupBytes = 8 * kSD * 2;       // 8 keys x all dims: 4 KB
+constexpr int kSKTile = (kBN / kPage) * kPageBytes;   // 32 KB: 4 pages, key groups 0..7
 constexpr int kPTile = kBM * 128;         // P: 128 rows x 64 keys bf16 (one 128B-swizzled chunk)
 
-constexpr uint32_t kTmO = 0, kTmQ = 256, kTmS = 384;   // column offsets
+constexpr uint32_t kTmO = 0, kTmS = 256;   // column offsets: O, then the S double buffer
 constexpr uint32_t kIdescQK = idesc_bf16(kBM, kBN, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16(kBM, kSD, false, true);
 
@@ -43,20 +52,23 @@ struct SlidingSmem {
   uint8_t k[kNS][kSKTile];
   uint8_t v[kNS][kSKTile];
   uint8_t p[2][kPTile];
+  uint8_t q[(kSlidingD / 64) * kQChunk];
   uint64_t k_full[kNS], k_empty[kNS], v_full[kNS], v_empty[kNS];
   uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];
-  uint64_t q_ready, teardown;
+  uint64_t q_full, teardown;
   uint32_t tmem_base;
   int abort_flag;
   int unit_b, unit_t;
 };
 constexpr size_t kSlidingSmemBytes = sizeof(SlidingSmem) + 1024;
+static_assert(kSlidingSmemBytes <= 232448, "sliding prefill exceeds the 227 KB shared-memory limit");
 
 struct PrefillParams {
-  const __nv_bfloat16* q;   // [T][32][D]
   SeqRows rows;
   int window;               // sliding W (0 on global layers)
   float scale_log2;
+  const void* k_cache;
+  const void* v_cache;
   int num_pages;
   const int32_t* page_table;
   int max_pages;
@@ -104,24 +116,23 @@ __device__ __forceinline__ void find_unit(const SeqRows& rows, int slot, int& ou
   }
 }
 
-// Row of the cache's 2-D tensor map holding keys key0 .. key0+15 of KV head g, or -16
-// (entirely outside the map: the TMA fills zeros) when the page lies outside [k_lo, k_hi].
-__device__ __forceinline__ int page_row(int key0, int k_lo, int k_hi, const int32_t* pt, int num_pages, int hkv,
-                                        int g, uint32_t* err) {
-  if (key0 + kPage - 1 < k_lo || key0 > k_hi) return -kPage;
+// Page-head block (physical page * hkv + g) holding keys key0 .. key0+15 of KV head g, or -1
+// when the page lies outside [k_lo, k_hi]: such pages are never looked up nor copied.
+__device__ __forceinline__ int page_block(int key0, int k_lo, int k_hi, const int32_t* pt, int num_pages, int hkv,
+                                          int g, uint32_t* err) {
+  if (key0 + kPage - 1 < k_lo || key0 > k_hi) return -1;
   const int phys = pt[key0 >> 4];
   if (phys < 0 || phys >= num_pages) {
     set_error(err, kErrPage);
-    return -kPage;
+    return -1;
   }
-  return (phys * hkv + g) * kPage;
+  return phys * hkv + g;
 }
 
 __device__ __forceinline__ uint32_t tmem_lane_base(int warp) { return (uint32_t)(32 * (warp & 3)) << 16; }
 
-__global__ void __launch_bounds__(192, 1)
-    prefill_sliding_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
-                           PrefillParams p) {
+__global__ void __launch_bounds__(kSlidingThreads, 1)
+    prefill_sliding_kernel(const __grid_constant__ CUtensorMap tmap_q, PrefillParams p) {
   extern __shared__ uint8_t smem_raw[];
   SlidingSmem& sm =
       *reinterpret_cast<SlidingSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -166,11 +177,11 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&sm.s_full[s], 1);
-      mbar_init(&sm.s_free[s], 128);
-      mbar_init(&sm.p_full[s], 128);
+      mbar_init(&sm.s_free[s], kSoftmaxThreads);
+      mbar_init(&sm.p_full[s], kSoftmaxThreads);
       mbar_init(&sm.pv_done[s], 1);
     }
-    mbar_init(&sm.q_ready, 128);
+    mbar_init(&sm.q_full, 1);
     mbar_init(&sm.teardown, 1);
     sm.abort_flag = 0;
     fence_mbar_init();
@@ -186,43 +197,58 @@ __global__ void __launch_bounds__(192, 1)
   volatile int* abort_flag = &sm.abort_flag;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      prefetch_tmap(&tmap_k);
-      prefetch_tmap(&tmap_v);
-      int j = 0;
-      for (; j < n_tiles; ++j) {
-        const int s = j % kNS;
-        const int kb = (kt0 + j) * kBN;
-        if (j >= kNS && !mbar_wait(&sm.k_empty[s], ((j / kNS) - 1) & 1, abort_flag, p.err)) break;
-        mbar_arrive_expect_tx(&sm.k_full[s], kSKTile);
-        int rowv[4];
+    // ------------------------------------------------------------ copy producer
+    // One bulk copy per 8 KB tiled page-head block, lanes 0-3 one page each. Block indices come
+    // from the page table ahead of use: lane l holds page (l & 3) of tile (l >> 2) of the
+    // current group of 8 tiles, and the next group is looked up one group early.
+    auto load_blocks = [&](int j0) -> int {
+      const int jt = j0 + (lane >> 2);
+      if (jt >= n_tiles) return -1;
+      return page_block((kt0 + jt) * kBN + (lane & 3) * kPage, k_lo, k_hi, pt, p.num_pages, kSlidingHkv, g, p.err);
+    };
+    if (lane == 0) {   // the roped Q tile: 4 boxes of 64 dims x 128 rows (rows outside T read as 0)
+      prefetch_tmap(&tmap_q);
+      mbar_arrive_expect_tx(&sm.q_full, (kSlidingD / 64) * kQChunk);
 #pragma unroll
-        for (int pp = 0; pp < 4; ++pp) {
-          rowv[pp] = page_row(kb + pp * kPage, k_lo, k_hi, pt, p.num_pages, kSlidingHkv, g, p.err);
-#pragma unroll
-          for (int c = 0; c < kSD / 64; ++c)
-            tma_load_2d(sm.k[s] + c * kSChunk + pp * 2048, &tmap_k, 64 * c, rowv[pp], &sm.k_full[s]);
-        }
-        if (j >= kNS && !mbar_wait(&sm.v_empty[s], ((j / kNS) - 1) & 1, abort_flag, p.err)) {
-          // K of tile j is in flight: account for it in the drain below.
-          ++j;
-          break;
-        }
-        mbar_arrive_expect_tx(&sm.v_full[s], kSKTile);
-#pragma unroll
-        for (int pp = 0; pp < 4; ++pp)
-#pragma unroll
-          for (int c = 0; c < kSD / 64; ++c)
-            tma_load_2d(sm.v[s] + c * kSChunk + pp * 2048, &tmap_v, 64 * c, rowv[pp], &sm.v_full[s]);
+      for (int c = 0; c < kSlidingD / 64; ++c) tma_load_3d(sm.q + c * kQChunk, &tmap_q, 64 * c, h, q_row0, &sm.q_full);
+    }
+    int blk_cur = load_blocks(0), blk_next = load_blocks(8);
+    const __nv_bfloat16* kc = (const __nv_bfloat16*)p.k_cache;
+    const __nv_bfloat16* vc = (const __nv_bfloat16*)p.v_cache;
+    int j = 0;
+    for (; j < n_tiles; ++j) {
+      const int s = j % kNS;
+      if (j > 0 && (j & 7) == 0) {
+        blk_cur = blk_next;
+        blk_next = load_blocks(j + 8);
       }
-      if (*abort_flag) {   // drain copies still in flight (bounded) before the CTA may exit
-        const unsigned long long t0 = globaltimer();
-        for (int i = max(0, j - kNS); i < j; ++i) {
-          while (!mbar_try_wait(smem_u32(&sm.k_full[i % kNS]), (i / kNS) & 1) && globaltimer() - t0 < kWaitLimitNs) {
-          }
-          while (!mbar_try_wait(smem_u32(&sm.v_full[i % kNS]), (i / kNS) & 1) && globaltimer() - t0 < kWaitLimitNs) {
-          }
+      const int my_blk = __shfl_sync(0xffffffffu, blk_cur, (j & 7) * 4 + (lane & 3));
+      const unsigned live = __ballot_sync(0xffffffffu, lane < 4 && my_blk >= 0);
+      const uint32_t bytes = __popc(live) * kPageBytes;
+      bool ok = (j < kNS) || lane != 0 || mbar_wait(&sm.k_empty[s], ((j / kNS) - 1) & 1, abort_flag, p.err);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      if (lane == 0) mbar_arrive_expect_tx(&sm.k_full[s], bytes);
+      __syncwarp();
+      if (lane < 4 && my_blk >= 0)
+        bulk_g2s(sm.k[s] + lane * kPageBytes, kc + (size_t)my_blk * kPage * kSD, kPageBytes, &sm.k_full[s]);
+      ok = (j < kNS) || lane != 0 || mbar_wait(&sm.v_empty[s], ((j / kNS) - 1) & 1, abort_flag, p.err);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) {
+        ++j;   // K of tile j is in flight: the drain below accounts for it
+        break;
+      }
+      if (lane == 0) mbar_arrive_expect_tx(&sm.v_full[s], bytes);
+      __syncwarp();
+      if (lane < 4 && my_blk >= 0)
+        bulk_g2s(sm.v[s] + lane * kPageBytes, vc + (size_t)my_blk * kPage * kSD, kPageBytes, &sm.v_full[s]);
+    }
+    if (lane == 0 && *abort_flag) {   // drain copies still in flight (bounded) before the CTA may exit
+      const unsigned long long t0 = globaltimer();
+      while (!mbar_try_wait(smem_u32(&sm.q_full), 0) && globaltimer() - t0 < kWaitLimitNs) {
+      }
+      for (int i = max(0, j - kNS); i < j; ++i) {
+        while (!mbar_try_wait(smem_u32(&sm.k_full[i % kNS]), (i / kNS) & 1) && globaltimer() - t0 < kWaitLimitNs) {
+        }
+        while (!mbar_try_wait(smem_u32(&sm.v_full[i % kNS]), (i / kNS) & 1) && globaltimer() - t0 < kWaitLimitNs) {
         }
       }
     }
@@ -232,15 +258,16 @@ __global__ void __launch_bounds__(192, 1)
       if (!mbar_wait(&sm.p_full[i & 1], (i >> 1) & 1, abort_flag, p.err)) return false;
       if (!mbar_wait(&sm.v_full[i % kNS], (i / kNS) & 1, abort_flag, p.err)) return false;
       const int kb = (kt0 + i) * kBN;
-      if (kb + kBN - 1 >= ctx_end) {
-        // Stale slots past the sequence's last key may hold anything (NaN): P = 0 there does
-        // not cancel NaN, so zero those V rows (whole 128-byte rows: the swizzle is irrelevant).
-        const int r0 = max(0, ctx_end - kb);
-        const int r1 = min(kBN, ((k_hi >> 4) + 1) * kPage - kb);
-        for (int idx = lane; idx < (r1 - r0) * (kSD / 64) * 8; idx += 32) {
-          const int r = r0 + idx / ((kSD / 64) * 8), rem = idx % ((kSD / 64) * 8);
-          *reinterpret_cast<uint4*>(sm.v[i % kNS] + (rem >> 3) * kSChunk + r * 128 + (rem & 7) * 16) =
-              make_uint4(0, 0, 0, 0);
+      // V rows of keys that hold no data of this sequence are zeroed before P.V: pages that
+      // were not copied (outside the needed key range) keep an older tile, and slots past the
+      // sequence's last key may hold anything (NaN); P = 0 there does not cancel NaN.
+      const int v0 = max(kb, (k_lo >> 4) * kPage), v1 = min(min(kb + kBN, ((k_hi >> 4) + 1) * kPage), ctx_end);
+      if (v0 > kb || v1 < kb + kBN) {
+        for (int idx = lane; idx < kBN * (kSD / 8); idx += 32) {
+          const int r = idx / (kSD / 8), dg = idx % (kSD / 8);
+          if (kb + r < v0 || kb + r >= v1)
+            *reinterpret_cast<uint4*>(sm.v[i % kNS] + ((r >> 3) * (kSD / 8) + dg) * 128 + (r & 7) * 16) =
+                make_uint4(0, 0, 0, 0);
         }
         fence_proxy_async();
         __syncwarp();
@@ -251,15 +278,15 @@ __global__ void __launch_bounds__(192, 1)
         const uint32_t va = smem_u32(sm.v[i % kNS]);
 #pragma unroll
         for (int k = 0; k < kBN / 16; ++k)
-          mma_ss(tm + kTmO, desc_sw128(pa + k * 32, 16, 1024), desc_sw128(va + k * 2048, kSChunk, 1024), kIdescPV,
-                 (i > 0 || k > 0) ? 1u : 0u);
+          mma_ss(tm + kTmO, desc_sw128(pa + k * 32, 16, 1024), desc_tiled(va + k * 2 * kKeyGroupBytes,
+                 kKeyGroupBytes, 128), kIdescPV, (i > 0 || k > 0) ? 1u : 0u);
         mma_commit(&sm.pv_done[i & 1]);
         mma_commit(&sm.v_empty[i % kNS]);
       }
       __syncwarp();
       return true;
     };
-    bool ok = mbar_wait(&sm.q_ready, 0, abort_flag, p.err);
+    bool ok = mbar_wait(&sm.q_full, 0, abort_flag, p.err);
     for (int j = 0; ok && j < n_tiles; ++j) {
       const int s = j % kNS;
       if (!mbar_wait(&sm.k_full[s], (j / kNS) & 1, abort_flag, p.err)) break;
@@ -267,10 +294,11 @@ __global__ void __launch_bounds__(192, 1)
       tc_fence_after();
       if (lane == 0) {
         const uint32_t ka = smem_u32(sm.k[s]);
+        const uint32_t qa = smem_u32(sm.q);
 #pragma unroll
         for (int k = 0; k < kSD / 16; ++k)
-          mma_ts(tm + kTmS + 64 * (j & 1), tm + kTmQ + 8 * k,
-                 desc_sw128(ka + (k >> 2) * kSChunk + (k & 3) * 32, 16, 1024), kIdescQK, k > 0 ? 1u : 0u);
+          mma_ss(tm + kTmS + 64 * (j & 1), desc_sw128(qa + (k >> 2) * kQChunk + (k & 3) * 32, 16, 1024),
+                 desc_tiled(ka + k * 256, 128, kKeyGroupBytes), kIdescQK, k > 0 ? 1u : 0u);
         mma_commit(&sm.s_full[j & 1]);
         mma_commit(&sm.k_empty[s]);
       }
@@ -287,41 +315,6 @@ __global__ void __launch_bounds__(192, 1)
     const uint32_t tq = tm + tmem_lane_base(warp);
     const int pos = kBM * t + r;
     const bool row_ok = pos >= p_lo && pos <= p_hi;
-
-    // Q: load, RoPE (all 128 pairs), declared bf16 cast, into tensor memory as bf16 pairs.
-    {
-      const __nv_bfloat16* qrow = p.q + ((size_t)(q_row0 + r) * kSlidingHq + h) * kSD;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t lo[16], hi[16];
-        if (row_ok) {
-          uint4 a[4], bq[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            a[i] = *reinterpret_cast<const uint4*>(qrow + 32 * c + 8 * i);
-            bq[i] = *reinterpret_cast<const uint4*>(qrow + kSD / 2 + 32 * c + 8 * i);
-          }
-          const uint32_t* aw = reinterpret_cast<const uint32_t*>(a);
-          const uint32_t* bw = reinterpret_cast<const uint32_t*>(bq);
-#pragma unroll
-          for (int w = 0; w < 16; ++w) {
-            float x0 = bf16_lo(aw[w]), x1 = bf16_hi(aw[w]), y0 = bf16_lo(bw[w]), y1 = bf16_hi(bw[w]);
-            rope_pair(x0, y0, rope_cs(p.tb, 32 * c + 2 * w, pos));
-            rope_pair(x1, y1, rope_cs(p.tb, 32 * c + 2 * w + 1, pos));
-            lo[w] = pack_bf16(x0, x1);
-            hi[w] = pack_bf16(y0, y1);
-          }
-        } else {
-#pragma unroll
-          for (int w = 0; w < 16; ++w) lo[w] = hi[w] = 0u;
-        }
-        tmem_st16(tq + kTmQ + 16 * c, lo);
-        tmem_st16(tq + kTmQ + 64 + 16 * c, hi);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&sm.q_ready);
-    }
 
     const float cl2 = p.scale_log2;
     float m_used = -INFINITY, l_run = 0.f;
@@ -365,7 +358,7 @@ __global__ void __launch_bounds__(192, 1)
       bool need_o = false;
       if (mt > m_used + kLazyRescale) {
         need_o = (m_used != -INFINITY);
-        alpha = exp2f(m_used - mt);
+        alpha = ex2(m_used - mt);
         m_used = mt;
       }
       const float neg_m = (m_used == -INFINITY) ? 0.f : -m_used;
@@ -373,10 +366,11 @@ __global__ void __launch_bounds__(192, 1)
       float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int w = 0; w < 32; ++w) {
-        const __nv_bfloat16 p0 = __float2bfloat16_rn(exp2f(fmaf(s[2 * w], cl2, neg_m)));
-        const __nv_bfloat16 p1 = __float2bfloat16_rn(exp2f(fmaf(s[2 * w + 1], cl2, neg_m)));
-        ls[w & 3] += __bfloat162float(p0) + __bfloat162float(p1);
-        pw[w] = (uint32_t)__bfloat16_as_ushort(p0) | ((uint32_t)__bfloat16_as_ushort(p1) << 16);
+        const float e0 = ex2(fmaf(s[2 * w], cl2, neg_m));
+        const float e1 = ex2(fmaf(s[2 * w + 1], cl2, neg_m));
+        ls[w & 3] += e0;
+        ls[w & 3] += e1;
+        pw[w] = pack_bf16(e0, e1);   // declared cast: P in bf16 for P.V
       }
       l_run = fmaf(l_run, alpha, (ls[0] + ls[1]) + (ls[2] + ls[3]));
 
@@ -472,27 +466,26 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D map over a paged cache [num_pages][hkv][16][D] seen as rows of D bf16; box 64 x 16,
+// 3-D map over q [T][Hq][D] (dims innermost first: D, Hq, T); box 64 dims x 1 head x 128 rows,
 // 128-byte swizzle, zero fill outside.
-bool cache_map(CUtensorMap* m, const void* base, int num_pages, int hkv, int D) {
+bool q_map(CUtensorMap* m, const void* q, int T, int hq, int D) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)num_pages * hkv * kPage};
-  cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)kPage};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)hq, (cuuint64_t)T};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)hq * D * 2};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)kBM};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
 
-cudaError_t launch_prefill(bool global, const void* q, const SeqRows& rows, int window, float scale_log2,
-                           const PagedCache& cache, void* out, const DeviceState& st, cudaStream_t s) {
+cudaError_t launch_prefill(bool global, const SeqRows& rows, int window, float scale_log2, const PagedCache& cache,
+                           void* out, const DeviceState& st, cudaStream_t s) {
   if (global) return cudaErrorNotSupported;
   PrefillParams p{};
-  p.q = (const __nv_bfloat16*)q;
   p.rows = rows;
   p.window = window;
   p.scale_log2 = scale_log2;
@@ -502,9 +495,10 @@ cudaError_t launch_prefill(bool global, const void* q, const SeqRows& rows, int 
   p.out = (__nv_bfloat16*)out;
   p.tb = st.sliding;
   p.err = st.err;
-  CUtensorMap mk, mv;
-  if (!cache_map(&mk, cache.k, cache.num_pages, kSlidingHkv, kSD)) return cudaErrorInvalidValue;
-  if (!cache_map(&mv, cache.v, cache.num_pages, kSlidingHkv, kSD)) return cudaErrorInvalidValue;
+  p.k_cache = cache.k;
+  p.v_cache = cache.v;
+  CUtensorMap mq;
+  if (!q_map(&mq, out, rows.T, kSlidingHq, kSD)) return cudaErrorInvalidValue;
   static bool attr[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -517,7 +511,7 @@ cudaError_t launch_prefill(bool global, const void* q, const SeqRows& rows, int 
   const long long slots = (long long)rows.T / kBM + 2LL * rows.B;
   const long long blocks = slots * kSlidingHq;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-  prefill_sliding_kernel<<<(unsigned)blocks, 192, kSlidingSmemBytes, s>>>(mk, mv, p);
+  prefill_sliding_kernel<<<(unsigned)blocks, kSlidingThreads, kSlidingSmemBytes, s>>>(mq, p);
   return cudaGetLastError();
 }
 

@@ -9,9 +9,9 @@
 // and only pairs t < R turn (R = 128 sliding, 64 global); the rest are copied bit for bit.
 //
 // Angles: pos * f_t needs more than fp32 at large positions (about 0.016 rad of error at
-// pos 2^18), so the tables hold (cos, sin) of 256*c*f_t and of p*f_t, computed in fp64 on the
-// host, and a lookup combines them by the angle-addition formula in fp32. The tables are
-// static device arrays: the library allocates no device memory.
+// pos 2^18), so the tables hold (cos, sin) of 256*c*f_t, 16*a*f_t and b*f_t, computed in fp64
+// on the host, and a lookup combines them by the angle-addition formula in fp32. The tables
+// are static device arrays: the library allocates no device memory.
 #include <math.h>
 
 #include <mutex>
@@ -23,26 +23,29 @@
 namespace g4 {
 
 static __device__ float2 g_rope_sliding_coarse[kSlidingR * kRopeCoarse];
+static __device__ float2 g_rope_sliding_mid[kSlidingR * kRopeMid];
 static __device__ float2 g_rope_sliding_fine[kSlidingR * kRopeFine];
 static __device__ float2 g_rope_global_coarse[kGlobalR * kRopeCoarse];
+static __device__ float2 g_rope_global_mid[kGlobalR * kRopeMid];
 static __device__ float2 g_rope_global_fine[kGlobalR * kRopeFine];
 static __device__ uint32_t g_error_word;
 
 namespace {
 
-void build_tables(int D, int R, double theta, std::vector<float2>& coarse, std::vector<float2>& fine) {
-  coarse.resize((size_t)R * kRopeCoarse);
-  fine.resize((size_t)R * kRopeFine);
+struct HostTables {
+  std::vector<float2> coarse, mid, fine;
+};
+
+void build_tables(int D, int R, double theta, HostTables& h) {
+  h.coarse.resize((size_t)R * kRopeCoarse);
+  h.mid.resize((size_t)R * kRopeMid);
+  h.fine.resize((size_t)R * kRopeFine);
+  auto cs = [](double a) { return make_float2((float)cos(a), (float)sin(a)); };
   for (int t = 0; t < R; ++t) {
     const double f = pow(theta, -2.0 * t / (double)D);
-    for (int c = 0; c < kRopeCoarse; ++c) {
-      const double a = (256.0 * c) * f;
-      coarse[(size_t)t * kRopeCoarse + c] = make_float2((float)cos(a), (float)sin(a));
-    }
-    for (int p = 0; p < kRopeFine; ++p) {
-      const double a = (double)p * f;
-      fine[(size_t)t * kRopeFine + p] = make_float2((float)cos(a), (float)sin(a));
-    }
+    for (int c = 0; c < kRopeCoarse; ++c) h.coarse[(size_t)t * kRopeCoarse + c] = cs((256.0 * c) * f);
+    for (int a = 0; a < kRopeMid; ++a) h.mid[(size_t)t * kRopeMid + a] = cs((16.0 * a) * f);
+    for (int b = 0; b < kRopeFine; ++b) h.fine[(size_t)t * kRopeFine + b] = cs((double)b * f);
   }
 }
 
@@ -60,27 +63,34 @@ cudaError_t device_state(DeviceState* st) {
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_state_mutex);
   if (!g_state_ready[dev]) {
-    static std::vector<float2> sc, sf, gc, gf;
-    if (sc.empty()) {
-      build_tables(kSlidingD, kSlidingR, 1.0e4, sc, sf);
-      build_tables(kGlobalD, kGlobalR, 1.0e6, gc, gf);
+    static HostTables hs, hg;
+    if (hs.coarse.empty()) {
+      build_tables(kSlidingD, kSlidingR, 1.0e4, hs);
+      build_tables(kGlobalD, kGlobalR, 1.0e6, hg);
     }
     DeviceState s{};
     void* p = nullptr;
-    if ((e = cudaMemcpyToSymbol(g_rope_sliding_coarse, sc.data(), sc.size() * sizeof(float2))) != cudaSuccess) return e;
-    if ((e = cudaMemcpyToSymbol(g_rope_sliding_fine, sf.data(), sf.size() * sizeof(float2))) != cudaSuccess) return e;
-    if ((e = cudaMemcpyToSymbol(g_rope_global_coarse, gc.data(), gc.size() * sizeof(float2))) != cudaSuccess) return e;
-    if ((e = cudaMemcpyToSymbol(g_rope_global_fine, gf.data(), gf.size() * sizeof(float2))) != cudaSuccess) return e;
+#define G4_UPLOAD(sym, vec)                                                                   \
+  if ((e = cudaMemcpyToSymbol(sym, (vec).data(), (vec).size() * sizeof(float2))) != cudaSuccess) return e
+#define G4_ADDR(sym, dst)                                                   \
+  if ((e = cudaGetSymbolAddress(&p, sym)) != cudaSuccess) return e;         \
+  dst = (const float2*)p
+    G4_UPLOAD(g_rope_sliding_coarse, hs.coarse);
+    G4_UPLOAD(g_rope_sliding_mid, hs.mid);
+    G4_UPLOAD(g_rope_sliding_fine, hs.fine);
+    G4_UPLOAD(g_rope_global_coarse, hg.coarse);
+    G4_UPLOAD(g_rope_global_mid, hg.mid);
+    G4_UPLOAD(g_rope_global_fine, hg.fine);
+    G4_ADDR(g_rope_sliding_coarse, s.sliding.coarse);
+    G4_ADDR(g_rope_sliding_mid, s.sliding.mid);
+    G4_ADDR(g_rope_sliding_fine, s.sliding.fine);
+    G4_ADDR(g_rope_global_coarse, s.global.coarse);
+    G4_ADDR(g_rope_global_mid, s.global.mid);
+    G4_ADDR(g_rope_global_fine, s.global.fine);
+#undef G4_UPLOAD
+#undef G4_ADDR
     const uint32_t zero = 0;
     if ((e = cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero))) != cudaSuccess) return e;
-    if ((e = cudaGetSymbolAddress(&p, g_rope_sliding_coarse)) != cudaSuccess) return e;
-    s.sliding.coarse = (const float2*)p;
-    if ((e = cudaGetSymbolAddress(&p, g_rope_sliding_fine)) != cudaSuccess) return e;
-    s.sliding.fine = (const float2*)p;
-    if ((e = cudaGetSymbolAddress(&p, g_rope_global_coarse)) != cudaSuccess) return e;
-    s.global.coarse = (const float2*)p;
-    if ((e = cudaGetSymbolAddress(&p, g_rope_global_fine)) != cudaSuccess) return e;
-    s.global.fine = (const float2*)p;
     if ((e = cudaGetSymbolAddress(&p, g_error_word)) != cudaSuccess) return e;
     s.err = (uint32_t*)p;
     g_state[dev] = s;
@@ -92,8 +102,20 @@ cudaError_t device_state(DeviceState* st) {
 
 // ---- one D-vector per warp ----------------------------------------------------------------------
 // Lane l owns pairs t = l*P .. l*P+P-1 (P = D/64), i.e. P contiguous elements of each half.
-template <int D, int R>
-__device__ __forceinline__ void rope_vec_warp(const __nv_bfloat16* __restrict__ src, __nv_bfloat16* dst, int pos,
+// `Dst` maps a dim to its place: contiguous rows (rope_apply) or a key row of a tiled page.
+struct RowDst {
+  __nv_bfloat16* p;
+  __device__ __forceinline__ __nv_bfloat16* at(int d) const { return p + d; }
+};
+template <int D>
+struct PageDst {   // key slot j of a page-head block (see tiled_offset)
+  __nv_bfloat16* block;
+  int j;
+  __device__ __forceinline__ __nv_bfloat16* at(int d) const { return block + tiled_offset(j, d, D); }
+};
+
+template <int D, int R, class Dst>
+__device__ __forceinline__ void rope_vec_warp(const __nv_bfloat16* __restrict__ src, const Dst& dst, int pos,
                                               const RopeTables& tb) {
   constexpr int P = D / 64;                    // 4 (D=256) or 8 (D=512)
   constexpr int half = D / 2;
@@ -115,18 +137,20 @@ __device__ __forceinline__ void rope_vec_warp(const __nv_bfloat16* __restrict__ 
       hw[w] = pack_bf16(b0, b1);
     }
   }
-  *reinterpret_cast<Vec*>(dst + t0) = lo;
-  *reinterpret_cast<Vec*>(dst + half + t0) = hi;
+  // P elements never cross an 8-dim group, so each half is one contiguous store either way.
+  *reinterpret_cast<Vec*>(dst.at(t0)) = lo;
+  *reinterpret_cast<Vec*>(dst.at(half + t0)) = hi;
 }
 
-template <int D>
-__device__ __forceinline__ void copy_vec_warp(const __nv_bfloat16* __restrict__ src, __nv_bfloat16* dst) {
+template <int D, class Dst>
+__device__ __forceinline__ void copy_vec_warp(const __nv_bfloat16* __restrict__ src, const Dst& dst) {
   constexpr int E = D / 32;                    // elements per lane: 8 or 16
   const int lane = threadIdx.x & 31;
-  const uint4* s = reinterpret_cast<const uint4*>(src + lane * 8);
-  uint4* d = reinterpret_cast<uint4*>(dst + lane * 8);
 #pragma unroll
-  for (int i = 0; i < E / 8; ++i) d[i * 32] = s[i * 32];
+  for (int i = 0; i < E / 8; ++i) {
+    const int d = (i * 32 + lane) * 8;
+    *reinterpret_cast<uint4*>(dst.at(d)) = *reinterpret_cast<const uint4*>(src + d);
+  }
 }
 
 template <int D, int R>
@@ -141,7 +165,7 @@ __global__ void __launch_bounds__(256) rope_apply_kernel(const __nv_bfloat16* __
     if ((threadIdx.x & 31) == 0) set_error(err, kErrPos);
     return;
   }
-  rope_vec_warp<D, R>(x + vec * D, out + vec * D, p, tb);
+  rope_vec_warp<D, R>(x + vec * D, RowDst{out + vec * D}, p, tb);
 }
 
 cudaError_t launch_rope_apply(bool global, const void* x, const int32_t* pos, int T, int H, void* out,
@@ -174,24 +198,27 @@ __device__ __forceinline__ void append_token(const __nv_bfloat16* k_row, const _
     if (lane == 0) set_error(err, kErrPage);
     return;
   }
-  const size_t slot = ((size_t)phys * HKV * kPage + (pos & 15)) * D;   // + g * kPage * D
-  __nv_bfloat16* ck = (__nv_bfloat16*)c.k;
+  const int j = pos & 15;
   for (int g = 0; g < HKV; ++g) {
-    const size_t dst = slot + (size_t)g * kPage * D;
+    const size_t blk = ((size_t)phys * HKV + g) * kPage * D;   // page-head block
     if (SHARED) {
-      copy_vec_warp<D>(k_row + (size_t)g * D, ck + dst);
+      copy_vec_warp<D>(k_row + (size_t)g * D, PageDst<D>{(__nv_bfloat16*)c.k + blk, j});
     } else {
-      rope_vec_warp<D, R>(k_row + (size_t)g * D, ck + dst, pos, tb);
-      copy_vec_warp<D>(v_row + (size_t)g * D, (__nv_bfloat16*)c.v + dst);
+      rope_vec_warp<D, R>(k_row + (size_t)g * D, PageDst<D>{(__nv_bfloat16*)c.k + blk, j}, pos, tb);
+      copy_vec_warp<D>(v_row + (size_t)g * D, PageDst<D>{(__nv_bfloat16*)c.v + blk, j});
     }
   }
 }
 
 // One warp per row of the prefill batch; the owning sequence is found by a scan over B.
-template <int D, int R, int HKV, bool SHARED>
+// With q_out set, the row's query heads are also roped (declared bf16 cast) into q_out: the
+// attention kernel that follows reads its queries already rotated.
+template <int D, int R, int HKV, int HQ, bool SHARED>
 __global__ void __launch_bounds__(256) append_prefill_kernel(const __nv_bfloat16* __restrict__ k,
-                                                             const __nv_bfloat16* __restrict__ v, SeqRows rows,
-                                                             PagedCache cache, RopeTables tb, uint32_t* err) {
+                                                             const __nv_bfloat16* __restrict__ v,
+                                                             const __nv_bfloat16* __restrict__ q,
+                                                             __nv_bfloat16* q_out, SeqRows rows, PagedCache cache,
+                                                             RopeTables tb, uint32_t* err) {
   const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (r >= rows.T) return;
@@ -211,6 +238,11 @@ __global__ void __launch_bounds__(256) append_prefill_kernel(const __nv_bfloat16
   }
   if (owner < 0) return;
   const int pos = rows.ctx_start[owner] + (r - rows.q_start[owner]);
+  if (q_out != nullptr && pos >= 0 && pos < kMaxPos) {
+#pragma unroll 1
+    for (int h = 0; h < HQ; ++h)
+      rope_vec_warp<D, R>(q + ((size_t)r * HQ + h) * D, RowDst{q_out + ((size_t)r * HQ + h) * D}, pos, tb);
+  }
   append_token<D, R, HKV, SHARED>(k + (size_t)r * HKV * D, SHARED ? nullptr : v + (size_t)r * HKV * D, owner, pos,
                                   cache, tb, err);
 }
@@ -227,15 +259,18 @@ __global__ void __launch_bounds__(256) append_decode_kernel(const __nv_bfloat16*
 }
 
 cudaError_t launch_append_prefill(bool global, const void* k, const void* v, const SeqRows& rows,
-                                  const PagedCache& cache, const DeviceState& st, cudaStream_t s) {
+                                  const PagedCache& cache, const DeviceState& st, cudaStream_t s, const void* q,
+                                  void* q_out) {
   if (rows.T <= 0 || rows.B <= 0) return cudaSuccess;
   const unsigned blocks = (unsigned)((rows.T + 7) / 8);
   if (global)
-    append_prefill_kernel<kGlobalD, kGlobalR, kGlobalHkv, true><<<blocks, 256, 0, s>>>(
-        (const __nv_bfloat16*)k, nullptr, rows, cache, st.global, st.err);
+    append_prefill_kernel<kGlobalD, kGlobalR, kGlobalHkv, kGlobalHq, true><<<blocks, 256, 0, s>>>(
+        (const __nv_bfloat16*)k, nullptr, (const __nv_bfloat16*)q, (__nv_bfloat16*)q_out, rows, cache, st.global,
+        st.err);
   else
-    append_prefill_kernel<kSlidingD, kSlidingR, kSlidingHkv, false><<<blocks, 256, 0, s>>>(
-        (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, rows, cache, st.sliding, st.err);
+    append_prefill_kernel<kSlidingD, kSlidingR, kSlidingHkv, kSlidingHq, false><<<blocks, 256, 0, s>>>(
+        (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, (const __nv_bfloat16*)q, (__nv_bfloat16*)q_out, rows,
+        cache, st.sliding, st.err);
   return cudaGetLastError();
 }
 

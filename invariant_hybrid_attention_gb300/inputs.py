@@ -31,6 +31,17 @@ def bf16_normal(shape: Sequence[int], seed: int, scale: float = 1.0) -> torch.Te
     return x.to(torch.bfloat16)
 
 
+def bf16_normal_device(shape: Sequence[int], seed: int, scale: float = 1.0, device="cuda") -> torch.Tensor:
+    """Same recipe as `bf16_normal`, drawn on the device from a seeded CUDA generator (used for
+    the benchmark's multi-GB tensors; the values differ from the CPU generator's)."""
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    x = torch.randn(*shape, generator=g, dtype=torch.float32, device=device)
+    if scale != 1.0:
+        x.mul_(scale)
+    return x.to(torch.bfloat16)
+
+
 def uniform_ints(n: int, lo: int, hi: int, seed: int) -> List[int]:
     """`n` integers uniform in [lo, hi] (both ends included)."""
     g = torch.Generator(device="cpu")

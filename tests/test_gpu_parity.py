@@ -10,7 +10,7 @@ import torch
 import invariant_hybrid_attention_gb300 as g4
 import oracle
 from invariant_hybrid_attention_gb300 import inputs as gi
-from invariant_hybrid_attention_gb300.paged import device_int32
+from invariant_hybrid_attention_gb300.paged import device_int32, untile
 
 from gpu_cases import GEOM, Batch, DecodeBatch, assert_close, f64, layers
 
@@ -64,8 +64,8 @@ def test_kv_append_writes_the_contract_layout(kind):
                         device_int32(bt.layout.ctx_start), cache.desc, table)
     torch.cuda.synchronize()
     assert g4.g4attn_status_sync() == g4.G4_OK
-    kc = cache.k.cpu()
-    vc = None if cache.v is None else cache.v.cpu()
+    kc = untile(cache.k.cpu())
+    vc = None if cache.v is None else untile(cache.v.cpu())
     for b, L in enumerate(bt.ctx_lens):
         for pos in range(L):
             page = int(bt.plan.table[b, pos // 16])
