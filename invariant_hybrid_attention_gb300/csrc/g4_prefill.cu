@@ -8,19 +8,23 @@
 //
 // Sliding layer (RFC section 5, sliding_attention_core: causal local attention, window 1024,
 // 32 Q / 16 KV heads, D 256). Per CTA:
-//   warp 0  copy producer: one bulk copy per tiled page-head block (8 KB: 16 keys x 256 dims as
-//           8x8 core matrices) into a 2-stage ring; pages outside the needed key range are
-//           never looked up nor copied;
-//   warp 1  MMA issuer: S = Q K^T with Q (128B swizzle) and K (K-major, no swizzle) in shared
-//           memory, O += P V with P (128B swizzle) and V (MN-major, no swizzle) in shared
+//   warps 0, 6  copy producers (Q and K; V): the roped Q tile by TMA, then one bulk copy per
+//           tiled page-head block (8 KB: 16 keys x 256 dims as 8x8 core matrices) into a
+//           3-stage ring; pages outside the needed key range are never looked up nor copied;
+//   warp 1  MMA issuer: S = Q K^T with Q in tensor memory and K (K-major, no swizzle) in shared
+//           memory, O += P V with P in tensor memory and V (MN-major, no swizzle) in shared
 //           memory; one elected lane issues, commits signal;
 //   warps 2-5  one thread per query row: per key tile the mask, the online softmax (lazy
-//           rescale, threshold 2^8), P (bf16) into shared memory, the O correction when
-//           needed, and the epilogue O / l -> bf16.
+//           rescale, threshold 2^8), P (bf16) written over the tile's own S columns, the O
+//           correction when needed, and the epilogue O / l -> bf16.
 // The queries arrive already roped: the cache-append pass before this kernel wrote
-// bf16(RoPE(q)) into the sequence rows of `out`; the producer's TMA loads the tile from there,
-// and the epilogue later overwrites exactly those rows (each row belongs to one CTA).
-// Tensor memory (512 columns): O [0,256), S double buffer [256,384).
+// bf16(RoPE(q)) into the sequence rows of `out`; the producer's TMA loads the tile from there
+// (into ring stage 2, which the softmax threads then empty into tensor memory), and the
+// epilogue later overwrites exactly those rows (each row belongs to one CTA).
+// Tensor memory (512 columns): O [0,256), Q dims 0-127 [256,320) as bf16 pairs, three S buffers
+// [320,512) whose first 32 columns take P once the softmax has read S (three, so that QK^T of
+// tile j+1 never waits on P.V of tile j-1). Shared memory: the 3-stage K/V ring and Q dims
+// 128-255.
 #include <math.h>
 
 #include "g4_internal.h"
@@ -31,10 +35,10 @@ namespace {
 
 constexpr int kBM = 128;                  // query rows per tile
 constexpr int kBN = 64;                   // keys per tile
-constexpr int kNS = 2;                    // K/V ring stages
+constexpr int kNS = 3;                    // K/V ring stages (stage 2 first holds the Q tile)
 constexpr float kLazyRescale = 8.0f;
 constexpr int kSoftmaxThreads = 128;      // one thread per query row
-constexpr int kSlidingThreads = 64 + kSoftmaxThreads;
+constexpr int kSlidingThreads = 64 + kSoftmaxThreads + 32;   // + the V producer warp (warp 6)
 constexpr int kQChunk = kBM * 128;         // roped Q tile: 128 rows x 64 dims per chunk, 128B swizzle
 
 // ---------------------------------------------------------------- sliding layer geometry
@@ -42,24 +46,23 @@ constexpr int kSD = kSlidingD;            // 256
 constexpr int kPageBytes = kPage * kSD * 2;       // one tiled page-head block: 8 KB
 constexpr int kKeyGroupBytes = 8 * kSD * 2;       // 8 keys x all dims: 4 KB
 constexpr int kSKTile = (kBN / kPage) * kPageBytes;   // 32 KB: 4 pages, key groups 0..7
-constexpr int kPTile = kBM * 128;         // P: 128 rows x 64 keys bf16 (one 128B-swizzled chunk)
 
-constexpr uint32_t kTmO = 0, kTmS = 256;   // column offsets: O, then the S double buffer
+constexpr int kNSP = 3;                   // S/P buffers in tensor memory
+constexpr uint32_t kTmO = 0, kTmQ = 256, kTmS = 320;   // column offsets: O, Q dims 0-127, S/P x3
 constexpr uint32_t kIdescQK = idesc_bf16(kBM, kBN, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16(kBM, kSD, false, true);
 
 struct SlidingSmem {
-  uint8_t k[kNS][kSKTile];
-  uint8_t v[kNS][kSKTile];
-  uint8_t p[2][kPTile];
-  uint8_t q[(kSlidingD / 64) * kQChunk];
+  uint8_t st[kNS][2 * kSKTile];   // ring stage s: K tile, then V tile; st[2] first holds Q dims 0-127
+  uint8_t qhi[2 * kQChunk];       // Q dims 128-255 (128B swizzle), the shared-memory A operand
   uint64_t k_full[kNS], k_empty[kNS], v_full[kNS], v_empty[kNS];
-  uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];
-  uint64_t q_full, teardown;
+  uint64_t s_full[kNSP], p_full[kNSP], pv_done[kNSP];
+  uint64_t q_full, q_ready, teardown;
   uint32_t tmem_base;
   int abort_flag;
   int unit_b, unit_t;
 };
+static_assert(2 * kQChunk <= 2 * kSKTile, "Q dims 0-127 must fit in one ring stage");
 constexpr size_t kSlidingSmemBytes = sizeof(SlidingSmem) + 1024;
 static_assert(kSlidingSmemBytes <= 232448, "sliding prefill exceeds the 227 KB shared-memory limit");
 
@@ -175,13 +178,13 @@ __global__ void __launch_bounds__(kSlidingThreads, 1)
       mbar_init(&sm.v_full[s], 1);
       mbar_init(&sm.v_empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kNSP; ++s) {
       mbar_init(&sm.s_full[s], 1);
-      mbar_init(&sm.s_free[s], kSoftmaxThreads);
       mbar_init(&sm.p_full[s], kSoftmaxThreads);
       mbar_init(&sm.pv_done[s], 1);
     }
     mbar_init(&sm.q_full, 1);
+    mbar_init(&sm.q_ready, kSoftmaxThreads);
     mbar_init(&sm.teardown, 1);
     sm.abort_flag = 0;
     fence_mbar_init();
@@ -196,25 +199,31 @@ __global__ void __launch_bounds__(kSlidingThreads, 1)
   const uint32_t tm = sm.tmem_base;
   volatile int* abort_flag = &sm.abort_flag;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ copy producer
-    // One bulk copy per 8 KB tiled page-head block, lanes 0-3 one page each. Block indices come
-    // from the page table ahead of use: lane l holds page (l & 3) of tile (l >> 2) of the
-    // current group of 8 tiles, and the next group is looked up one group early.
+  if (warp == 0 || warp == 6) {
+    // ------------------------------------------------------------ copy producers
+    // Warp 0 loads the roped Q tile by TMA, then the K tiles; warp 6 loads the V tiles. Split
+    // so that K, needed a tile earlier, never queues behind the release of a V stage. One bulk
+    // copy per 8 KB tiled page-head block, lanes 0-3 one page each. Block indices come from the
+    // page table ahead of use: lane l holds page (l & 3) of tile (l >> 2) of the current group
+    // of 8 tiles, and the next group is looked up one group early.
+    const bool is_v = (warp == 6);
     auto load_blocks = [&](int j0) -> int {
       const int jt = j0 + (lane >> 2);
       if (jt >= n_tiles) return -1;
       return page_block((kt0 + jt) * kBN + (lane & 3) * kPage, k_lo, k_hi, pt, p.num_pages, kSlidingHkv, g, p.err);
     };
-    if (lane == 0) {   // the roped Q tile: 4 boxes of 64 dims x 128 rows (rows outside T read as 0)
+    if (!is_v && lane == 0) {   // the roped Q tile: 4 boxes of 64 dims x 128 rows (rows outside T read as 0)
       prefetch_tmap(&tmap_q);
       mbar_arrive_expect_tx(&sm.q_full, (kSlidingD / 64) * kQChunk);
 #pragma unroll
-      for (int c = 0; c < kSlidingD / 64; ++c) tma_load_3d(sm.q + c * kQChunk, &tmap_q, 64 * c, h, q_row0, &sm.q_full);
+      for (int c = 0; c < kSlidingD / 64; ++c)
+        tma_load_3d((c < 2 ? sm.st[2] : sm.qhi - 2 * kQChunk) + c * kQChunk, &tmap_q, 64 * c, h, q_row0, &sm.q_full);
     }
     int blk_cur = load_blocks(0), blk_next = load_blocks(8);
-    const __nv_bfloat16* kc = (const __nv_bfloat16*)p.k_cache;
-    const __nv_bfloat16* vc = (const __nv_bfloat16*)p.v_cache;
+    const __nv_bfloat16* src = (const __nv_bfloat16*)(is_v ? p.v_cache : p.k_cache);
+    uint64_t* full = is_v ? sm.v_full : sm.k_full;
+    uint64_t* empty = is_v ? sm.v_empty : sm.k_empty;
+    const int half = is_v ? kSKTile : 0;
     int j = 0;
     for (; j < n_tiles; ++j) {
       const int s = j % kNS;
@@ -225,37 +234,29 @@ __global__ void __launch_bounds__(kSlidingThreads, 1)
       const int my_blk = __shfl_sync(0xffffffffu, blk_cur, (j & 7) * 4 + (lane & 3));
       const unsigned live = __ballot_sync(0xffffffffu, lane < 4 && my_blk >= 0);
       const uint32_t bytes = __popc(live) * kPageBytes;
-      bool ok = (j < kNS) || lane != 0 || mbar_wait(&sm.k_empty[s], ((j / kNS) - 1) & 1, abort_flag, p.err);
+      bool ok = (j < kNS) || lane != 0 || mbar_wait(&empty[s], ((j / kNS) - 1) & 1, abort_flag, p.err);
+      if (j == 2 && lane == 0) ok = ok && mbar_wait(&sm.q_ready, 0, abort_flag, p.err);   // Q left stage 2
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      if (lane == 0) mbar_arrive_expect_tx(&sm.k_full[s], bytes);
+      if (lane == 0) mbar_arrive_expect_tx(&full[s], bytes);
       __syncwarp();
       if (lane < 4 && my_blk >= 0)
-        bulk_g2s(sm.k[s] + lane * kPageBytes, kc + (size_t)my_blk * kPage * kSD, kPageBytes, &sm.k_full[s]);
-      ok = (j < kNS) || lane != 0 || mbar_wait(&sm.v_empty[s], ((j / kNS) - 1) & 1, abort_flag, p.err);
-      if (!__shfl_sync(0xffffffffu, ok, 0)) {
-        ++j;   // K of tile j is in flight: the drain below accounts for it
-        break;
-      }
-      if (lane == 0) mbar_arrive_expect_tx(&sm.v_full[s], bytes);
-      __syncwarp();
-      if (lane < 4 && my_blk >= 0)
-        bulk_g2s(sm.v[s] + lane * kPageBytes, vc + (size_t)my_blk * kPage * kSD, kPageBytes, &sm.v_full[s]);
+        bulk_g2s(sm.st[s] + half + lane * kPageBytes, src + (size_t)my_blk * kPage * kSD, kPageBytes, &full[s]);
     }
     if (lane == 0 && *abort_flag) {   // drain copies still in flight (bounded) before the CTA may exit
       const unsigned long long t0 = globaltimer();
-      while (!mbar_try_wait(smem_u32(&sm.q_full), 0) && globaltimer() - t0 < kWaitLimitNs) {
+      if (!is_v) {
+        while (!mbar_try_wait(smem_u32(&sm.q_full), 0) && globaltimer() - t0 < kWaitLimitNs) {
+        }
       }
       for (int i = max(0, j - kNS); i < j; ++i) {
-        while (!mbar_try_wait(smem_u32(&sm.k_full[i % kNS]), (i / kNS) & 1) && globaltimer() - t0 < kWaitLimitNs) {
-        }
-        while (!mbar_try_wait(smem_u32(&sm.v_full[i % kNS]), (i / kNS) & 1) && globaltimer() - t0 < kWaitLimitNs) {
+        while (!mbar_try_wait(smem_u32(&full[i % kNS]), (i / kNS) & 1) && globaltimer() - t0 < kWaitLimitNs) {
         }
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     auto pv = [&](int i) -> bool {
-      if (!mbar_wait(&sm.p_full[i & 1], (i >> 1) & 1, abort_flag, p.err)) return false;
+      if (!mbar_wait(&sm.p_full[i % kNSP], (i / kNSP) & 1, abort_flag, p.err)) return false;
       if (!mbar_wait(&sm.v_full[i % kNS], (i / kNS) & 1, abort_flag, p.err)) return false;
       const int kb = (kt0 + i) * kBN;
       // V rows of keys that hold no data of this sequence are zeroed before P.V: pages that
@@ -266,7 +267,7 @@ __global__ void __launch_bounds__(kSlidingThreads, 1)
         for (int idx = lane; idx < kBN * (kSD / 8); idx += 32) {
           const int r = idx / (kSD / 8), dg = idx % (kSD / 8);
           if (kb + r < v0 || kb + r >= v1)
-            *reinterpret_cast<uint4*>(sm.v[i % kNS] + ((r >> 3) * (kSD / 8) + dg) * 128 + (r & 7) * 16) =
+            *reinterpret_cast<uint4*>(sm.st[i % kNS] + kSKTile + ((r >> 3) * (kSD / 8) + dg) * 128 + (r & 7) * 16) =
                 make_uint4(0, 0, 0, 0);
         }
         fence_proxy_async();
@@ -274,32 +275,37 @@ __global__ void __launch_bounds__(kSlidingThreads, 1)
       }
       tc_fence_after();
       if (lane == 0) {
-        const uint32_t pa = smem_u32(sm.p[i & 1]);
-        const uint32_t va = smem_u32(sm.v[i % kNS]);
+        const uint32_t va = smem_u32(sm.st[i % kNS] + kSKTile);
 #pragma unroll
         for (int k = 0; k < kBN / 16; ++k)
-          mma_ss(tm + kTmO, desc_sw128(pa + k * 32, 16, 1024), desc_tiled(va + k * 2 * kKeyGroupBytes,
-                 kKeyGroupBytes, 128), kIdescPV, (i > 0 || k > 0) ? 1u : 0u);
-        mma_commit(&sm.pv_done[i & 1]);
+          mma_ts(tm + kTmO, tm + kTmS + 64 * (i % kNSP) + 8 * k,
+                 desc_tiled(va + k * 2 * kKeyGroupBytes, kKeyGroupBytes, 128), kIdescPV, (i > 0 || k > 0) ? 1u : 0u);
+        mma_commit(&sm.pv_done[i % kNSP]);
         mma_commit(&sm.v_empty[i % kNS]);
       }
       __syncwarp();
       return true;
     };
-    bool ok = mbar_wait(&sm.q_full, 0, abort_flag, p.err);
+    bool ok = mbar_wait(&sm.q_ready, 0, abort_flag, p.err);
     for (int j = 0; ok && j < n_tiles; ++j) {
       const int s = j % kNS;
       if (!mbar_wait(&sm.k_full[s], (j / kNS) & 1, abort_flag, p.err)) break;
-      if (j >= 2 && !mbar_wait(&sm.s_free[j & 1], ((j - 2) >> 1) & 1, abort_flag, p.err)) break;
+      // S buffer j % 3 last held P_{j-3}: reuse it once P_{j-3} V_{j-3} has completed (issued two
+      // MMA groups earlier, so this wait does not drain the tensor pipe).
+      if (j >= kNSP && !mbar_wait(&sm.pv_done[j % kNSP], ((j - kNSP) / kNSP) & 1, abort_flag, p.err)) break;
       tc_fence_after();
       if (lane == 0) {
-        const uint32_t ka = smem_u32(sm.k[s]);
-        const uint32_t qa = smem_u32(sm.q);
+        const uint32_t ka = smem_u32(sm.st[s]);
+        const uint32_t qh = smem_u32(sm.qhi);
+        const uint32_t sd = tm + kTmS + 64 * (j % kNSP);
 #pragma unroll
-        for (int k = 0; k < kSD / 16; ++k)
-          mma_ss(tm + kTmS + 64 * (j & 1), desc_sw128(qa + (k >> 2) * kQChunk + (k & 3) * 32, 16, 1024),
-                 desc_tiled(ka + k * 256, 128, kKeyGroupBytes), kIdescQK, k > 0 ? 1u : 0u);
-        mma_commit(&sm.s_full[j & 1]);
+        for (int k = 0; k < 8; ++k)   // dims 0-127: Q from tensor memory
+          mma_ts(sd, tm + kTmQ + 8 * k, desc_tiled(ka + k * 256, 128, kKeyGroupBytes), kIdescQK, k > 0 ? 1u : 0u);
+#pragma unroll
+        for (int k = 8; k < 16; ++k)  // dims 128-255: Q from shared memory
+          mma_ss(sd, desc_sw128(qh + ((k - 8) >> 2) * kQChunk + (k & 3) * 32, 16, 1024),
+                 desc_tiled(ka + k * 256, 128, kKeyGroupBytes), kIdescQK, 1u);
+        mma_commit(&sm.s_full[j % kNSP]);
         mma_commit(&sm.k_empty[s]);
       }
       __syncwarp();
@@ -309,29 +315,54 @@ __global__ void __launch_bounds__(kSlidingThreads, 1)
       }
       if (j == n_tiles - 1 && !pv(j)) ok = false;
     }
-  } else {
+  } else if (warp >= 2 && warp <= 5) {
     // ------------------------------------------------------------ softmax / epilogue warps
     const int r = 32 * (warp & 3) + lane;   // query row = tensor-memory lane
     const uint32_t tq = tm + tmem_lane_base(warp);
     const int pos = kBM * t + r;
     const bool row_ok = pos >= p_lo && pos <= p_hi;
 
+    // Q: the producer's TMA brought the roped tile in (4 chunks of 64 dims, 128B swizzle);
+    // dims 0-127 sit in ring stage 2 and each thread moves its row of them into tensor memory
+    // (an A operand in bf16 pairs), which frees stage 2 for keys and values. Dims 128-255 stay
+    // in shared memory as the A operand of the other half of the QK^T k-steps.
+    {
+      const bool okq = mbar_wait(&sm.q_full, 0, abort_flag, p.err);
+      const uint8_t* qrow = sm.st[2] + r * 128;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t w[32];
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+          const uint4 v = okq ? *reinterpret_cast<const uint4*>(qrow + c * kQChunk + ((g ^ (r & 7)) * 16))
+                              : make_uint4(0, 0, 0, 0);
+          w[4 * g] = v.x;
+          w[4 * g + 1] = v.y;
+          w[4 * g + 2] = v.z;
+          w[4 * g + 3] = v.w;
+        }
+        tmem_st32(tq + kTmQ + 32 * c, w);   // dims 64c .. 64c+63 -> columns 32c .. 32c+31
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&sm.q_ready);
+    }
+
     const float cl2 = p.scale_log2;
     float m_used = -INFINITY, l_run = 0.f;
     bool ok = true;
     for (int j = 0; j < n_tiles; ++j) {
       const int kb = (kt0 + j) * kBN;
-      if (!mbar_wait(&sm.s_full[j & 1], (j >> 1) & 1, abort_flag, p.err)) {
+      const int sb = j % kNSP;
+      if (!mbar_wait(&sm.s_full[sb], (j / kNSP) & 1, abort_flag, p.err)) {
         ok = false;
         break;
       }
       tc_fence_after();
       uint32_t sr[64];
-      tmem_ld32(tq + kTmS + 64 * (j & 1), *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-      tmem_ld32(tq + kTmS + 64 * (j & 1) + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+      tmem_ld32(tq + kTmS + 64 * sb, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+      tmem_ld32(tq + kTmS + 64 * sb + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
       tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(&sm.s_free[j & 1]);
 
       float s[64];
 #pragma unroll
@@ -374,21 +405,12 @@ __global__ void __launch_bounds__(kSlidingThreads, 1)
       }
       l_run = fmaf(l_run, alpha, (ls[0] + ls[1]) + (ls[2] + ls[3]));
 
-      // P_j into its shared-memory buffer once P_{j-2} has been consumed.
-      if (j >= 2 && !mbar_wait(&sm.pv_done[j & 1], ((j - 2) >> 1) & 1, abort_flag, p.err)) {
-        ok = false;
-        break;
-      }
-      uint8_t* prow = sm.p[j & 1] + r * 128;
-#pragma unroll
-      for (int k16 = 0; k16 < 8; ++k16)
-        *reinterpret_cast<uint4*>(prow + ((k16 ^ (r & 7)) * 16)) =
-            make_uint4(pw[4 * k16], pw[4 * k16 + 1], pw[4 * k16 + 2], pw[4 * k16 + 3]);
-      fence_proxy_async();
+      // P_j (bf16 key pairs) over the first 32 columns of its own S buffer: the A operand of P.V.
+      tmem_st32(tq + kTmS + 64 * sb, pw);
 
       // O correction (rows whose max rose by more than 2^8), after P_{j-1} V_{j-1} landed.
       if (__any_sync(0xffffffffu, need_o)) {
-        if (!mbar_wait(&sm.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, p.err)) {
+        if (!mbar_wait(&sm.pv_done[(j - 1) % kNSP], ((j - 1) / kNSP) & 1, abort_flag, p.err)) {
           ok = false;
           break;
         }
@@ -405,12 +427,13 @@ __global__ void __launch_bounds__(kSlidingThreads, 1)
         }
         tmem_st_wait();
       }
+      tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&sm.p_full[j & 1]);
+      mbar_arrive(&sm.p_full[sb]);
     }
 
     // Epilogue: O / l -> bf16, rows of this sequence only.
-    if (ok && mbar_wait(&sm.pv_done[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1, abort_flag, p.err)) {
+    if (ok && mbar_wait(&sm.pv_done[(n_tiles - 1) % kNSP], ((n_tiles - 1) / kNSP) & 1, abort_flag, p.err)) {
       tc_fence_after();
       const float inv = (l_run > 0.f) ? __frcp_rn(l_run) : 0.f;
       __nv_bfloat16* orow = p.out + ((size_t)(q_row0 + r) * kSlidingHq + h) * kSD;
