@@ -37,11 +37,18 @@
  *   q, out         [T][n_q_heads][head_dim]           query rows / output rows
  *   k, v           [T][n_kv_heads][head_dim]          new key / value rows of a prefill
  *   k_new, v_new   [B][n_kv_heads][head_dim]          the decode token's key / value
- *   cache->k       [num_pages][n_kv_heads][2][head_dim/8][8][8]: one page-head block of
- *                  16 keys x head_dim dims stored as 8x8 core matrices, key j and dim d at
- *                  [j/8][d/8][j%8][d%8] (16*head_dim contiguous bf16 per page and head);
+ *   cache->k       one page-head block of 16 keys x head_dim dims per (page, KV head),
+ *                  16*head_dim contiguous bf16 at k + (page*n_kv_heads + head)*16*head_dim,
+ *                  stored as 8x8 core matrices (key j, dim d):
+ *                    sliding (D 256): [j/8][d/8][j%8][d%8]            = [2][32][8][8]
+ *                    global  (D 512): [d/256][j/8][(d%256)/8][j%8][d%8] = [2][2][32][8][8]
  *                  sliding K' (roped) or global S (un-rotated, K==V)
- *   cache->v       same layout; sliding V; NULL on global layers
+ *   cache->v       sliding: V, same layout as k; global: NULL
+ *   cache->k_rot   global only (NULL on sliding layers): p-RoPE(S) on the 128 rotated
+ *                  columns d in [0,64) U [256,320), 2048 bf16 per (page, KV head) at
+ *                  k_rot + (page*4 + head)*2048, as [d/256][j/8][(d%64)/8][j%8][d%8].
+ *                  Written by the library with S; it spares the prefill kernels from
+ *                  rotating every key tile again for every query tile and head.
  *   page_table     int32 [B][max_pages]: physical page of logical page i of sequence b
  *                  (keys 16i .. 16i+15). Entries that no call needs may hold anything.
  *   All pointers 16-byte aligned.
@@ -96,7 +103,8 @@ typedef struct {
 typedef struct {
   void* k;                /* sliding: roped K'; global: the shared S */
   void* v;                /* sliding: V; global: NULL */
-  int32_t num_pages;      /* physical pages in k (and v) */
+  void* k_rot;            /* global: roped rotated columns of S; sliding: NULL */
+  int32_t num_pages;      /* physical pages in k (and v, k_rot) */
   int32_t page_size;      /* keys per page; must be 16 */
 } g4attn_cache;
 

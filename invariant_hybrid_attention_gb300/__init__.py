@@ -32,8 +32,8 @@ class g4attn_layer(ctypes.Structure):
 
 
 class g4attn_cache(ctypes.Structure):
-    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("num_pages", ctypes.c_int32),
-                ("page_size", ctypes.c_int32)]
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("k_rot", ctypes.c_void_p),
+                ("num_pages", ctypes.c_int32), ("page_size", ctypes.c_int32)]
 
 
 class G4Error(RuntimeError):
@@ -90,8 +90,8 @@ def global_layer(softmax_scale: Optional[float] = None) -> g4attn_layer:
                         1.0 / math.sqrt(512) if softmax_scale is None else float(softmax_scale), 1)
 
 
-def make_cache(k, v, num_pages: int) -> g4attn_cache:
-    return g4attn_cache(_ptr(k), _ptr(v), int(num_pages), PAGE_SIZE)
+def make_cache(k, v, num_pages: int, k_rot=None) -> g4attn_cache:
+    return g4attn_cache(_ptr(k), _ptr(v), _ptr(k_rot), int(num_pages), PAGE_SIZE)
 
 
 def _ptr(t) -> Optional[int]:

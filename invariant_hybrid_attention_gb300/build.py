@@ -17,8 +17,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libg4attn.so")
-SOURCES = ["g4_api.cu", "g4_rope.cu", "g4_decode.cu", "g4_prefill.cu"]
-HEADERS = ["g4_common.cuh", "g4_internal.h"]
+SOURCES = ["g4_api.cu", "g4_rope.cu", "g4_decode.cu", "g4_prefill.cu", "g4_prefill_global.cu"]
+HEADERS = ["g4_common.cuh", "g4_internal.h", "g4_prefill_common.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", os.path.join(ROOT, "include"), "-I", CSRC]

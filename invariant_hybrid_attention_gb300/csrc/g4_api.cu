@@ -41,8 +41,8 @@ g4_status check_layer(const g4attn_layer* L, bool* global) {
 g4_status check_cache(const g4attn_cache* c, bool global, const int32_t* page_table, int32_t max_pages) {
   if (!c || !c->k || !aligned16(c->k)) return G4_ERR_INVALID;
   if (global) {
-    if (c->v != nullptr) return G4_ERR_INVALID;
-  } else if (!c->v || !aligned16(c->v)) {
+    if (c->v != nullptr || !c->k_rot || !aligned16(c->k_rot)) return G4_ERR_INVALID;
+  } else if (!c->v || !aligned16(c->v) || c->k_rot != nullptr) {
     return G4_ERR_INVALID;
   }
   if (c->page_size != kPage) return G4_ERR_UNSUPPORTED;
@@ -58,6 +58,7 @@ PagedCache paged(const g4attn_cache* c, const int32_t* page_table, int32_t max_p
   PagedCache pc;
   pc.k = c->k;
   pc.v = c->v;
+  pc.krot = c->k_rot;
   pc.num_pages = c->num_pages;
   pc.page_table = page_table;
   pc.max_pages = max_pages;

@@ -33,14 +33,28 @@ enum : uint32_t { kErrTimeout = 1u, kErrPage = 2u, kErrPos = 4u };
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
 // Cache page layout. One page of one KV head holds 16 keys x D dims as core matrices of
-// 8 keys x 8 dims (128 contiguous bytes): key j, dim d sits at element
-//   ((j / 8) * (D / 8) + d / 8) * 64 + (j % 8) * 8 + d % 8
+// 8 keys x 8 dims (128 contiguous bytes). Sliding pages (D = 256): key j, dim d sits at element
+//   ((j / 8) * 32 + d / 8) * 64 + (j % 8) * 8 + d % 8
 // of the page-head block, whose 16*D elements are contiguous at
 //   cache + (page * Hkv + head) * 16 * D.
-// One contiguous copy of a block lands in shared memory as an operand the tensor cores read
-// directly (K-major for K, MN-major for V), and every 8x8 block is one ldmatrix tile.
+// Global pages (D = 512) are two such 256-dim halves one after the other, so that each half
+// (8 KB) is contiguous: key j, dim d at
+//   (((d / 256) * 2 + j / 8) * 32 + (d % 256) / 8) * 64 + (j % 8) * 8 + d % 8.
+// One contiguous copy of a block (or half-block) lands in shared memory as an operand the
+// tensor cores read directly (K-major for K, MN-major for V), and every 8x8 block is one
+// ldmatrix tile.
 __host__ __device__ constexpr int tiled_offset(int j, int d, int D) {
-  return ((j >> 3) * (D >> 3) + (d >> 3)) * 64 + (j & 7) * 8 + (d & 7);
+  return D == 512 ? ((((d >> 8) * 2 + (j >> 3)) * 32 + ((d & 255) >> 3)) * 64 + (j & 7) * 8 + (d & 7))
+                  : (((j >> 3) * (D >> 3) + (d >> 3)) * 64 + (j & 7) * 8 + (d & 7));
+}
+
+// Rotated-column side pages of a global (K==V) cache: p-RoPE(S) on the 128 rotated dims
+// d in [0, 64) U [256, 320), the only columns where K differs from the stored S. Key j, dim d
+// sits at element (((d / 256) * 2 + j / 8) * 8 + (d % 64) / 8) * 64 + (j % 8) * 8 + d % 8 of a
+// 2048-element page-head block at k_rot + (page * Hkv + head) * 2048.
+constexpr int kRotPageElems = kPage * 2 * kGlobalR;   // 2048
+__host__ __device__ constexpr int rot_offset(int j, int d) {
+  return ((((d >> 8) * 2 + (j >> 3)) * 8 + ((d & 63) >> 3)) * 64 + (j & 7) * 8 + (d & 7));
 }
 
 // RoPE cos/sin tables for one layer kind, built in fp64 on the host and stored as fp32:
@@ -162,6 +176,57 @@ G4_DEV bool named_barrier_and(uint32_t id, uint32_t count, bool pred) {
       : "r"((uint32_t)pred), "r"(id), "r"(count)
       : "memory");
   return r != 0;
+}
+
+// ---- thread-block clusters (distributed shared memory between the two CTAs of a pair) ---------
+G4_DEV uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Address in CTA `rank`'s shared memory of the variable at local shared address `saddr`.
+G4_DEV uint32_t map_peer(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+G4_DEV void st_peer_v4(uint32_t addr, float a, float b, float c, float d) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+G4_DEV void st_peer_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+// Arrive on an mbarrier of another CTA of the cluster, releasing this thread's prior writes.
+G4_DEV void mbar_arrive_peer(uint32_t peer_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(peer_bar) : "memory");
+}
+G4_DEV bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// mbar_wait for barriers completed by the other CTA of the cluster (acquires its writes).
+G4_DEV bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort, uint32_t* err) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait_cluster(a, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  while (true) {
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait_cluster(a, parity)) return true;
+    if (abort && *abort) return false;
+    if (globaltimer() - t0 > kWaitLimitNs) {
+      if (abort) *abort = 1;
+      set_error(err, kErrTimeout);
+      return false;
+    }
+  }
 }
 
 // ---- bulk copies (TMA) -------------------------------------------------------------------------

@@ -324,12 +324,15 @@ __global__ void __launch_bounds__(128, 1) decode_global_kernel(DecodeParams p) {
   for (int mt = 0; mt < 32; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
   float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
 
-  // ldmatrix lane addressing. A page stage is tiled (8 keys x 8 dims core matrices of 128 B,
-  // key group kg and dim group dg at (kg * 64 + dg) * 128): each 8x8 ldmatrix tile is one
-  // core matrix. K as A (non-transposed): tiles (keys 0-7 | 8-15) x (dims +0 | +8);
+  // ldmatrix lane addressing. A page stage is a tiled global page: two halves of 256 dims,
+  // each [key group kg][dim group dg][8 keys][8 dims] (core matrices of 128 B at
+  // ((half * 2 + kg) * 32 + dg) * 128): each 8x8 ldmatrix tile is one core matrix.
+  // K as A (non-transposed): tiles (keys 0-7 | 8-15) x (dims +0 | +8);
   // V^T as A (transposed): tiles (dims +0 | +8) x (keys 0-7 | 8-15).
-  const uint32_t a_lane = (((lane >> 3) & 1) * 64 + (lane >> 4)) * 128 + (lane & 7) * 16;
-  const uint32_t v_lane = (((lane >> 4) & 1) * 64 + ((lane >> 3) & 1)) * 128 + (lane & 7) * 16;
+  // A 16-dim step s starts at byte (s / 16) * 8192 + (s % 16) * 256 of the stage.
+  const uint32_t a_lane = (((lane >> 3) & 1) * 32 + (lane >> 4)) * 128 + (lane & 7) * 16;
+  const uint32_t v_lane = (((lane >> 4) & 1) * 32 + ((lane >> 3) & 1)) * 128 + (lane & 7) * 16;
+  auto step_off = [](int s16) -> uint32_t { return (uint32_t)((s16 >> 4) * 8192 + (s16 & 15) * 256); };
   const uint32_t q_lane = q_addr + (lane & 7) * kGRow + (lane >> 3) * 16;
 
   for (int i = 0; i < n_mine; ++i) {
@@ -342,7 +345,8 @@ __global__ void __launch_bounds__(128, 1) decode_global_kernel(DecodeParams p) {
       for (int idx = lane; idx < kPage * (kGD / 8); idx += 32) {
         const int r = idx / (kGD / 8), dg = idx % (kGD / 8);
         if (key0 + r > k_end)
-          *reinterpret_cast<uint4*>(page + ((r >> 3) * (kGD / 8) + dg) * 128 + (r & 7) * 16) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(page + (((dg >> 5) * 2 + (r >> 3)) * 32 + (dg & 31)) * 128 + (r & 7) * 16) =
+              make_uint4(0, 0, 0, 0);
       }
       __syncwarp();
     }
@@ -353,8 +357,8 @@ __global__ void __launch_bounds__(128, 1) decode_global_kernel(DecodeParams p) {
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks) {   // rotated k-steps: dims 16ks.. with partners +256
       uint32_t a[4], h[4], bq0, bq1, bh0, bh1;
-      ldsm_x4(pa + a_lane + (2 * ks) * 128, a[0], a[1], a[2], a[3]);
-      ldsm_x4(pa + a_lane + (2 * (ks + 16)) * 128, h[0], h[1], h[2], h[3]);
+      ldsm_x4(pa + a_lane + step_off(ks), a[0], a[1], a[2], a[3]);
+      ldsm_x4(pa + a_lane + step_off(ks + 16), h[0], h[1], h[2], h[3]);
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
         const int key = key0 + gq + 8 * (r & 1);
@@ -375,8 +379,8 @@ __global__ void __launch_bounds__(128, 1) decode_global_kernel(DecodeParams p) {
     for (int kp = 0; kp < 32; kp += 2) {   // plain k-steps, two at a time
       if ((kp >= 0 && kp < 4) || (kp >= 16 && kp < 20)) continue;
       uint32_t a[4], a2[4], b0, b1, b2, b3;
-      ldsm_x4(pa + a_lane + (2 * kp) * 128, a[0], a[1], a[2], a[3]);
-      ldsm_x4(pa + a_lane + (2 * (kp + 1)) * 128, a2[0], a2[1], a2[2], a2[3]);
+      ldsm_x4(pa + a_lane + step_off(kp), a[0], a[1], a[2], a[3]);
+      ldsm_x4(pa + a_lane + step_off(kp + 1), a2[0], a2[1], a2[2], a2[3]);
       ldsm_x4(q_lane + kp * 32, b0, b1, b2, b3);
       mma16816(s0, a[0], a[1], a[2], a[3], b0, b1);
       mma16816(s1, a2[0], a2[1], a2[2], a2[3], b2, b3);
@@ -428,7 +432,7 @@ __global__ void __launch_bounds__(128, 1) decode_global_kernel(DecodeParams p) {
 #pragma unroll
     for (int mt = 0; mt < 32; ++mt) {
       uint32_t a0, a1, a2, a3;
-      ldsm_x4_t(pa + v_lane + (2 * mt) * 128, a0, a1, a2, a3);
+      ldsm_x4_t(pa + v_lane + step_off(mt), a0, a1, a2, a3);
       mma16816(o[mt], a0, a1, a2, a3, pb0, pb1);
     }
     __syncwarp();

@@ -32,6 +32,7 @@ struct SeqRows {
 struct PagedCache {
   void* k;
   void* v;
+  void* krot;   // global layers: p-RoPE(S) on the rotated columns (rot_offset layout)
   int32_t num_pages;
   const int32_t* page_table;
   int32_t max_pages;
@@ -59,5 +60,7 @@ cudaError_t launch_decode(bool global, const void* q, const int32_t* seq_len, in
 // rows over them.
 cudaError_t launch_prefill(bool global, const SeqRows& rows, int window, float scale_log2, const PagedCache& cache,
                            void* out, const DeviceState& st, cudaStream_t s);
+cudaError_t launch_prefill_global(const SeqRows& rows, float scale_log2, const PagedCache& cache, void* out,
+                                  const DeviceState& st, cudaStream_t s);
 
 }  // namespace g4

@@ -27,19 +27,16 @@
 // 128-255.
 #include <math.h>
 
-#include "g4_internal.h"
+#include "g4_prefill_common.cuh"
 
 namespace g4 {
 
 namespace {
 
-constexpr int kBM = 128;                  // query rows per tile
-constexpr int kBN = 64;                   // keys per tile
+using namespace pf;
+
 constexpr int kNS = 3;                    // K/V ring stages (stage 2 first holds the Q tile)
-constexpr float kLazyRescale = 8.0f;
-constexpr int kSoftmaxThreads = 128;      // one thread per query row
 constexpr int kSlidingThreads = 64 + kSoftmaxThreads + 32;   // + the V producer warp (warp 6)
-constexpr int kQChunk = kBM * 128;         // roped Q tile: 128 rows x 64 dims per chunk, 128B swizzle
 
 // ---------------------------------------------------------------- sliding layer geometry
 constexpr int kSD = kSlidingD;            // 256
@@ -65,74 +62,6 @@ struct SlidingSmem {
 static_assert(2 * kQChunk <= 2 * kSKTile, "Q dims 0-127 must fit in one ring stage");
 constexpr size_t kSlidingSmemBytes = sizeof(SlidingSmem) + 1024;
 static_assert(kSlidingSmemBytes <= 232448, "sliding prefill exceeds the 227 KB shared-memory limit");
-
-struct PrefillParams {
-  SeqRows rows;
-  int window;               // sliding W (0 on global layers)
-  float scale_log2;
-  const void* k_cache;
-  const void* v_cache;
-  int num_pages;
-  const int32_t* page_table;
-  int max_pages;
-  __nv_bfloat16* out;
-  RopeTables tb;
-  uint32_t* err;
-};
-
-// Finds this CTA's (sequence, query tile) among all sequences' tiles: slot s of sequence b
-// is its tile (last - s), so every sequence is walked from its most expensive tile down.
-// Warp-wide; returns b = -1 when the slot is past the last tile.
-__device__ __forceinline__ void find_unit(const SeqRows& rows, int slot, int& out_b, int& out_t) {
-  const int lane = threadIdx.x & 31;
-  int base = 0;
-  out_b = -1;
-  out_t = 0;
-  for (int b0 = 0; b0 < rows.B; b0 += 32) {
-    const int b = b0 + lane;
-    int cnt = 0, tl = 0;
-    if (b < rows.B) {
-      const int L = rows.q_len[b], cs = rows.ctx_start[b];
-      if (L > 0 && cs >= 0) {
-        tl = (cs + L - 1) / kBM;
-        cnt = tl - cs / kBM + 1;
-      }
-    }
-    int incl = cnt;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int n = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += n;
-    }
-    const int excl = incl - cnt;
-    const bool mine = cnt > 0 && slot >= base + excl && slot < base + incl;
-    const unsigned m = __ballot_sync(0xffffffffu, mine);
-    if (m) {
-      const int src = __ffs(m) - 1;
-      const int e = __shfl_sync(0xffffffffu, excl, src);
-      const int t_last = __shfl_sync(0xffffffffu, tl, src);
-      out_b = b0 + src;
-      out_t = t_last - (slot - base - e);
-      return;
-    }
-    base += __shfl_sync(0xffffffffu, incl, 31);
-  }
-}
-
-// Page-head block (physical page * hkv + g) holding keys key0 .. key0+15 of KV head g, or -1
-// when the page lies outside [k_lo, k_hi]: such pages are never looked up nor copied.
-__device__ __forceinline__ int page_block(int key0, int k_lo, int k_hi, const int32_t* pt, int num_pages, int hkv,
-                                          int g, uint32_t* err) {
-  if (key0 + kPage - 1 < k_lo || key0 > k_hi) return -1;
-  const int phys = pt[key0 >> 4];
-  if (phys < 0 || phys >= num_pages) {
-    set_error(err, kErrPage);
-    return -1;
-  }
-  return phys * hkv + g;
-}
-
-__device__ __forceinline__ uint32_t tmem_lane_base(int warp) { return (uint32_t)(32 * (warp & 3)) << 16; }
 
 __global__ void __launch_bounds__(kSlidingThreads, 1)
     prefill_sliding_kernel(const __grid_constant__ CUtensorMap tmap_q, PrefillParams p) {
@@ -217,7 +146,7 @@ __global__ void __launch_bounds__(kSlidingThreads, 1)
       mbar_arrive_expect_tx(&sm.q_full, (kSlidingD / 64) * kQChunk);
 #pragma unroll
       for (int c = 0; c < kSlidingD / 64; ++c)
-        tma_load_3d((c < 2 ? sm.st[2] : sm.qhi - 2 * kQChunk) + c * kQChunk, &tmap_q, 64 * c, h, q_row0, &sm.q_full);
+        tma_load_3d(c < 2 ? sm.st[2] + c * kQChunk : sm.qhi + (c - 2) * kQChunk, &tmap_q, 64 * c, h, q_row0, &sm.q_full);
     }
     int blk_cur = load_blocks(0), blk_next = load_blocks(8);
     const __nv_bfloat16* src = (const __nv_bfloat16*)(is_v ? p.v_cache : p.k_cache);
@@ -471,43 +400,11 @@ __global__ void __launch_bounds__(kSlidingThreads, 1)
   }
 }
 
-// ---------------------------------------------------------------- host side
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  }
-  return fn;
-}
-
-// 3-D map over q [T][Hq][D] (dims innermost first: D, Hq, T); box 64 dims x 1 head x 128 rows,
-// 128-byte swizzle, zero fill outside.
-bool q_map(CUtensorMap* m, const void* q, int T, int hq, int D) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)hq, (cuuint64_t)T};
-  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)hq * D * 2};
-  cuuint32_t box[3] = {64, 1, (cuuint32_t)kBM};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace
 
 cudaError_t launch_prefill(bool global, const SeqRows& rows, int window, float scale_log2, const PagedCache& cache,
                            void* out, const DeviceState& st, cudaStream_t s) {
-  if (global) return cudaErrorNotSupported;
+  if (global) return launch_prefill_global(rows, scale_log2, cache, out, st, s);
   PrefillParams p{};
   p.rows = rows;
   p.window = window;

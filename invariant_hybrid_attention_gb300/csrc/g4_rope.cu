@@ -114,6 +114,21 @@ struct PageDst {   // key slot j of a page-head block (see tiled_offset)
   __device__ __forceinline__ __nv_bfloat16* at(int d) const { return block + tiled_offset(j, d, D); }
 };
 
+struct RotDst {   // key slot j of a rotated-column side page (see rot_offset); other dims dropped
+  __nv_bfloat16* block;
+  int j;
+  __device__ __forceinline__ __nv_bfloat16* at(int d) const { return block + rot_offset(j, d); }
+};
+
+template <class Dst>
+struct RotatedOnly {
+  static constexpr bool value = false;
+};
+template <>
+struct RotatedOnly<RotDst> {
+  static constexpr bool value = true;
+};
+
 template <int D, int R, class Dst>
 __device__ __forceinline__ void rope_vec_warp(const __nv_bfloat16* __restrict__ src, const Dst& dst, int pos,
                                               const RopeTables& tb) {
@@ -138,6 +153,7 @@ __device__ __forceinline__ void rope_vec_warp(const __nv_bfloat16* __restrict__ 
     }
   }
   // P elements never cross an 8-dim group, so each half is one contiguous store either way.
+  if (RotatedOnly<Dst>::value && t0 >= R) return;
   *reinterpret_cast<Vec*>(dst.at(t0)) = lo;
   *reinterpret_cast<Vec*>(dst.at(half + t0)) = hi;
 }
@@ -203,6 +219,9 @@ __device__ __forceinline__ void append_token(const __nv_bfloat16* k_row, const _
     const size_t blk = ((size_t)phys * HKV + g) * kPage * D;   // page-head block
     if (SHARED) {
       copy_vec_warp<D>(k_row + (size_t)g * D, PageDst<D>{(__nv_bfloat16*)c.k + blk, j});
+      // The rotated columns once more, roped (the K side of K==V where it differs from S).
+      rope_vec_warp<D, R>(k_row + (size_t)g * D,
+                          RotDst{(__nv_bfloat16*)c.krot + ((size_t)phys * HKV + g) * kRotPageElems, j}, pos, tb);
     } else {
       rope_vec_warp<D, R>(k_row + (size_t)g * D, PageDst<D>{(__nv_bfloat16*)c.k + blk, j}, pos, tb);
       copy_vec_warp<D>(v_row + (size_t)g * D, PageDst<D>{(__nv_bfloat16*)c.v + blk, j});

@@ -49,7 +49,7 @@ def test_unsupported_geometry_fails_closed(lib):
     bad = g4.sliding_layer()
     bad.head_dim = 128
     assert lib.g4attn_provenance(ctypes.byref(bad), None, 0) == -1
-    cache = g4.g4attn_cache(16, 32, 4, 16)
+    cache = g4.g4attn_cache(16, 32, None, 4, 16)
     st = lib.g4attn_prefill(ctypes.byref(bad), 16, 16, 16, 8, 16, 16, 16, 1, ctypes.byref(cache), 16, 1, 16, None)
     assert st == g4.G4_ERR_UNSUPPORTED
     glob = g4.global_layer()
@@ -65,7 +65,7 @@ def test_unsupported_geometry_fails_closed(lib):
 
 def test_invalid_arguments_refused_on_host(lib):
     s = g4.sliding_layer()
-    cache = g4.g4attn_cache(16, 32, 4, 16)
+    cache = g4.g4attn_cache(16, 32, None, 4, 16)
     # NULL q
     assert lib.g4attn_prefill(ctypes.byref(s), None, 16, 16, 8, 16, 16, 16, 1, ctypes.byref(cache), 16, 1, 16,
                               None) == g4.G4_ERR_INVALID
@@ -76,12 +76,15 @@ def test_invalid_arguments_refused_on_host(lib):
     assert lib.g4attn_prefill(ctypes.byref(s), 16, 16, 16, 8, 16, 16, 16, 0, ctypes.byref(cache), 16, 1, 16,
                               None) == g4.G4_ERR_INVALID
     # page size other than 16
-    c8 = g4.g4attn_cache(16, 32, 4, 8)
+    c8 = g4.g4attn_cache(16, 32, None, 4, 8)
     assert lib.g4attn_prefill(ctypes.byref(s), 16, 16, 16, 8, 16, 16, 16, 1, ctypes.byref(c8), 16, 1, 16,
                               None) == g4.G4_ERR_UNSUPPORTED
-    # a global layer given a V tensor (K==V takes none)
+    # a global layer given a V tensor (K==V takes none), or without its rotated-column pages
     gl = g4.global_layer()
-    cg = g4.g4attn_cache(16, 32, 4, 16)
+    cg = g4.g4attn_cache(16, 32, 48, 4, 16)
+    assert lib.g4attn_prefill(ctypes.byref(gl), 16, 16, None, 8, 16, 16, 16, 1,
+                              ctypes.byref(g4.g4attn_cache(16, None, None, 4, 16)), 16, 1, 16,
+                              None) == g4.G4_ERR_INVALID
     assert lib.g4attn_prefill(ctypes.byref(gl), 16, 16, 16, 8, 16, 16, 16, 1, ctypes.byref(cg), 16, 1, 16,
                               None) == g4.G4_ERR_INVALID
     # scale must be finite and positive

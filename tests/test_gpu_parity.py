@@ -10,7 +10,7 @@ import torch
 import invariant_hybrid_attention_gb300 as g4
 import oracle
 from invariant_hybrid_attention_gb300 import inputs as gi
-from invariant_hybrid_attention_gb300.paged import device_int32, untile
+from invariant_hybrid_attention_gb300.paged import device_int32, untile, untile_rot
 
 from gpu_cases import GEOM, Batch, DecodeBatch, assert_close, f64, layers
 
@@ -66,6 +66,9 @@ def test_kv_append_writes_the_contract_layout(kind):
     assert g4.g4attn_status_sync() == g4.G4_OK
     kc = untile(cache.k.cpu())
     vc = None if cache.v is None else untile(cache.v.cpu())
+    rc = None if cache.k_rot is None else untile_rot(cache.k_rot.cpu())
+    R = oracle.rope_rotated_pairs(olayer.head_dim, olayer.rope_partial)
+    rot_dims = np.r_[0:R, olayer.head_dim // 2:olayer.head_dim // 2 + R]
     for b, L in enumerate(bt.ctx_lens):
         for pos in range(L):
             page = int(bt.plan.table[b, pos // 16])
@@ -73,6 +76,10 @@ def test_kv_append_writes_the_contract_layout(kind):
             raw = bt.hist_k[b][pos]
             if kind == "global":
                 assert torch.equal(stored, raw)                          # S stored un-rotated
+                # k_rot: p-RoPE(S) on the rotated dims, one bf16 rounding from the exact value
+                want = oracle.rope(raw.double().numpy(), pos, olayer.rope_theta, olayer.rope_partial)[:, rot_dims]
+                got = rc[page, :, pos % 16, :].double().numpy()
+                assert (np.abs(got - want) <= bf16_round_bound(want) + 1e-6).all(), (b, pos)
             else:
                 want = oracle.rope(raw.double().numpy(), pos, olayer.rope_theta, olayer.rope_partial)
                 got = stored.double().numpy()
@@ -172,5 +179,40 @@ def test_prefill_sliding_batch_invariance():
         bt.q[s:s + L] = alone.q[:L]
         bt.k_rows = gi.rows_of(bt.hist_k, bt.layout)
         bt.v_rows = gi.rows_of(bt.hist_v, bt.layout)
+        out_b, _ = bt.run(layer)
+        assert torch.equal(out_a[:L].cpu(), out_b[s:s + L].cpu()), (lens, padded, at)
+
+
+# ---------------------------------------------------------------- global (K==V) prefill
+
+def test_prefill_global_tiny_oracle_case():
+    """Two causal sequences of 96 and 200 tokens on the K==V layer, N(0,1) inputs, seed 0."""
+    check_prefill(Batch("global", [96, 200], seed=0), "global", 0)
+
+
+@pytest.mark.parametrize("padded", [False, True], ids=["packed", "padded"])
+def test_prefill_global_ragged(padded):
+    bt = Batch("global", [1, 5, 127, 128, 129, 700], padded=padded, seed=3, scale=0.5)
+    check_prefill(bt, "global", 0, sample=64)
+
+
+def test_prefill_global_chunked_with_history():
+    """Chunks that start mid-sequence read earlier S and k_rot pages written by kv_append."""
+    bt = Batch("global", [300, 64, 1, 200], ctx_starts=[1000, 77, 2500, 129], seed=4, scale=0.5)
+    check_prefill(bt, "global", 0, sample=64)
+
+
+def test_prefill_global_batch_invariance():
+    """A target sequence alone, packed among others and padded at another index: same bits."""
+    layer, _ = layers("global")
+    L = 900
+    alone = Batch("global", [L], seed=9, scale=0.5)
+    out_a, _ = alone.run(layer)
+    for lens, padded, at in [([200, L, 33], False, 1), ([L, 300], True, 0), ([5, 77, 530, L], True, 3)]:
+        bt = Batch("global", lens, padded=padded, seed=9 + len(lens), scale=0.5)
+        bt.hist_k[at] = alone.hist_k[0]
+        s = bt.layout.q_start[at]
+        bt.q[s:s + L] = alone.q[:L]
+        bt.k_rows = gi.rows_of(bt.hist_k, bt.layout)
         out_b, _ = bt.run(layer)
         assert torch.equal(out_a[:L].cpu(), out_b[s:s + L].cpu()), (lens, padded, at)

@@ -1,7 +1,7 @@
 """CPU checks of the tiled cache-page layout helpers (8x8 core matrices per page and head)."""
 import torch
 
-from invariant_hybrid_attention_gb300.paged import tile, untile
+from invariant_hybrid_attention_gb300.paged import tile, untile, untile_rot
 
 
 def test_tile_untile_roundtrip():
@@ -13,3 +13,30 @@ def test_tile_untile_roundtrip():
     for j, d in [(0, 0), (5, 9), (8, 7), (15, 255), (9, 130)]:
         assert flat[1, 1, ((j // 8) * 32 + d // 8) * 64 + (j % 8) * 8 + d % 8] == x[1, 1, j, d]
     assert torch.equal(untile(t), x)
+
+
+def test_global_half_layout_roundtrip():
+    x = torch.arange(2 * 3 * 16 * 512, dtype=torch.float32).view(2, 3, 16, 512)
+    t = tile(x)
+    assert t.shape == (2, 3, 2, 2, 32, 8, 8)
+    flat = t.reshape(2, 3, -1)
+    # key j, dim d at (((d // 256) * 2 + j // 8) * 32 + (d % 256) // 8) * 64 + (j % 8) * 8 + d % 8
+    for j, d in [(0, 0), (5, 9), (8, 263), (15, 511), (9, 300), (3, 255)]:
+        off = (((d // 256) * 2 + j // 8) * 32 + (d % 256) // 8) * 64 + (j % 8) * 8 + d % 8
+        assert flat[1, 2, off] == x[1, 2, j, d]
+    assert torch.equal(untile(t), x)
+    # each 256-dim half of a page-head is one contiguous 4096-element block
+    assert torch.equal(flat[0, 0, 4096:8192].sort().values, x[0, 0, :, 256:].reshape(-1).sort().values)
+
+
+def test_rotated_side_layout():
+    # element of key j, rotated dim d (d in [0,64) or [256,320)):
+    #   (((d // 256) * 2 + j // 8) * 8 + (d % 64) // 8) * 64 + (j % 8) * 8 + d % 8
+    t = torch.arange(2 * 4 * 2048, dtype=torch.float32).view(2, 4, 2, 2, 8, 8, 8)
+    rows = untile_rot(t)
+    assert rows.shape == (2, 4, 16, 128)
+    flat = t.reshape(2, 4, -1)
+    for j, d in [(0, 0), (7, 63), (8, 256), (15, 319), (10, 300)]:
+        col = d if d < 64 else d - 256 + 64
+        off = (((d // 256) * 2 + j // 8) * 8 + (d % 64) // 8) * 64 + (j % 8) * 8 + d % 8
+        assert rows[1, 3, j, col] == flat[1, 3, off]
