@@ -529,10 +529,12 @@ __global__ void __launch_bounds__(D / 4) decode_merge_kernel(const float* __rest
   *reinterpret_cast<uint2*>(dst) = pk;
 }
 
+// Chunks a request can span: positions stop below kMaxPos, so a longer page table adds none.
 int decode_chunks(bool global, int max_pages, int window) {
-  if (global) return (max_pages * kPage + kDecodeChunkGlobal - 1) / kDecodeChunkGlobal;
+  const long long keys = (long long)max_pages * kPage < kMaxPos ? (long long)max_pages * kPage : kMaxPos;
+  if (global) return (int)((keys + kDecodeChunkGlobal - 1) / kDecodeChunkGlobal);
   const int by_window = (window - 1) / kDecodeChunkSliding + 2;
-  const int by_table = (max_pages * kPage + kDecodeChunkSliding - 1) / kDecodeChunkSliding;
+  const int by_table = (int)((keys + kDecodeChunkSliding - 1) / kDecodeChunkSliding);
   return by_window < by_table ? by_window : by_table;
 }
 

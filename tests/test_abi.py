@@ -105,6 +105,12 @@ def test_workspace_sizes(lib):
     # global: 32768 keys = 32 chunks of 1024
     n = lib.g4attn_decode_workspace_bytes(ctypes.byref(gl), 64, 2048)
     assert n >= 64 * 32 * 32 * (512 + 2) * 4
+    # a page table longer than the 262144-position limit needs no more chunks (and no int overflow)
+    at_limit = lib.g4attn_decode_workspace_bytes(ctypes.byref(gl), 2, 262144 // 16)
+    assert at_limit >= 2 * 32 * 256 * (512 + 2) * 4
+    assert lib.g4attn_decode_workspace_bytes(ctypes.byref(gl), 2, 2**31 - 1) == at_limit
+    assert lib.g4attn_decode_workspace_bytes(ctypes.byref(s), 2, 2**31 - 1) == \
+        lib.g4attn_decode_workspace_bytes(ctypes.byref(s), 2, 2048)
 
 
 def test_missing_library_fails_loudly(tmp_path, monkeypatch):
