@@ -29,7 +29,8 @@
  *
  * Memory. Every tensor is a device buffer owned by the caller. The library allocates no
  * device memory: its only device-side state is static (the RoPE cos/sin tables, filled once
- * per device on the first call, and one 32-bit error word). All calls are stream-ordered
+ * per device on the first call, one 32-bit error word, and the scratch buffer of
+ * g4attn_decode_static). All calls are stream-ordered
  * on `stream` (a cudaStream_t; NULL = the legacy default stream) and never synchronise,
  * except g4attn_status_sync.
  *
@@ -76,8 +77,12 @@ typedef enum {
   G4_ERR_UNSUPPORTED = 2,  /* geometry or dtype outside the two supported layer kinds */
   G4_ERR_CUDA = 3,         /* a CUDA runtime call failed (launch, table upload) */
   G4_ERR_TIMEOUT = 4,      /* a bounded device wait ran out (device error word) */
-  G4_ERR_DEVICE = 5        /* device-detected bad data: page index or position (error word) */
+  G4_ERR_DEVICE = 5,       /* device-detected bad data: page index or position (error word) */
+  G4_ERR_SCRATCH = 6       /* g4attn_decode_static: the step needs more than the static scratch */
 } g4_status;
+
+/* Size of the static device scratch buffer behind g4attn_decode_static (per device). */
+#define G4ATTN_DECODE_STATIC_SCRATCH_BYTES ((size_t)32 << 20)
 
 typedef enum { G4_SLIDING = 0, G4_GLOBAL = 1 } g4_kind;
 
@@ -154,6 +159,33 @@ g4_status g4attn_decode(const g4attn_layer* layer, const void* q, const void* k_
                         const void* v_new, const int32_t* seq_len, int32_t B,
                         const g4attn_cache* cache, const int32_t* page_table, int32_t max_pages,
                         void* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/* g4attn_decode without a caller workspace. The RFC this library follows has no counterpart
+ * of this call; it exists for callers that cannot allocate device memory when they decode:
+ * a plain C host program with no device allocator of its own, or a serving process whose
+ * device memory is reserved up front by its pooling allocator, where one more allocation
+ * would fail or stall the step.
+ *
+ * The partial softmax states live in a static device buffer of the library,
+ * G4ATTN_DECODE_STATIC_SCRATCH_BYTES (32 MiB) per device, and this call allocates nothing.
+ * A step fits when g4attn_decode_workspace_bytes(layer, B, max_pages) is at most that size:
+ * for example a sliding step (window 1024) of up to 203 requests, or a global step of up to
+ * 15 requests with page tables of 2048 pages (32768 positions). A larger step returns
+ * G4_ERR_SCRATCH and launches nothing; use g4attn_decode with a workspace for it.
+ *
+ * Arguments, layouts, arithmetic, results and other errors are those of g4attn_decode (the
+ * same kernels run). Nothing in the scratch needs to start at zero: each call writes every
+ * scratch entry it later reads.
+ *
+ * All calls on one device share the one buffer. Calls whose kernels may run at the same time
+ * on the GPU (different streams with no ordering between them) race on it and give wrong
+ * results; calls ordered on one stream do not. The first call on each device looks up the
+ * buffer's address (and, like every first call, uploads the RoPE tables) with that device
+ * current; make that first call before any stream capture. */
+g4_status g4attn_decode_static(const g4attn_layer* layer, const void* q, const void* k_new,
+                               const void* v_new, const int32_t* seq_len, int32_t B,
+                               const g4attn_cache* cache, const int32_t* page_table,
+                               int32_t max_pages, void* out, void* stream);
 
 /* Runtime provenance (RFC section 4, rule 8): writes a NUL-terminated one-line record
  * (backend, kernel ids, schedule, split policy, accumulator, layer kind, device, dtype,

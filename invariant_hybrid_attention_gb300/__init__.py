@@ -17,12 +17,13 @@ from typing import Optional
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libg4attn.so")
 
-G4_OK, G4_ERR_INVALID, G4_ERR_UNSUPPORTED, G4_ERR_CUDA, G4_ERR_TIMEOUT, G4_ERR_DEVICE = range(6)
+G4_OK, G4_ERR_INVALID, G4_ERR_UNSUPPORTED, G4_ERR_CUDA, G4_ERR_TIMEOUT, G4_ERR_DEVICE, G4_ERR_SCRATCH = range(7)
 G4_SLIDING, G4_GLOBAL = 0, 1
 PAGE_SIZE = 16
+DECODE_STATIC_SCRATCH_BYTES = 32 << 20   # the static scratch of g4attn_decode_static, per device
 
 EXPORTS = ("g4attn_rope_apply", "g4attn_prefill", "g4attn_kv_append", "g4attn_decode_workspace_bytes",
-           "g4attn_decode", "g4attn_provenance", "g4attn_status_sync", "g4attn_status_string")
+           "g4attn_decode", "g4attn_decode_static", "g4attn_provenance", "g4attn_status_sync", "g4attn_status_string")
 
 
 class g4attn_layer(ctypes.Structure):
@@ -62,6 +63,7 @@ def load(path: Optional[str] = None):
         "g4attn_kv_append": (I32, [L, P, P, I32, P, P, P, I32, C, P, I32, P]),
         "g4attn_decode_workspace_bytes": (SZ, [L, I32, I32]),
         "g4attn_decode": (I32, [L, P, P, P, P, I32, C, P, I32, P, P, SZ, P]),
+        "g4attn_decode_static": (I32, [L, P, P, P, P, I32, C, P, I32, P, P]),
         "g4attn_provenance": (I32, [L, ctypes.c_char_p, SZ]),
         "g4attn_status_sync": (I32, [P]),
         "g4attn_status_string": (ctypes.c_char_p, [I32]),
@@ -148,6 +150,18 @@ def g4attn_decode(layer, q, k_new, v_new, seq_len, cache: g4attn_cache, page_tab
     _check(load().g4attn_decode(ctypes.byref(layer), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(seq_len), B,
                                 ctypes.byref(cache), _ptr(page_table), int(page_table.shape[1]), _ptr(out),
                                 _ptr(workspace), nbytes, _stream(stream)), "g4attn_decode")
+    return out
+
+
+def g4attn_decode_static(layer, q, k_new, v_new, seq_len, cache: g4attn_cache, page_table, out, stream=None):
+    """g4attn_decode with the library's static scratch instead of a workspace: for callers that
+    cannot allocate device memory at decode time. Allocates nothing (this wrapper included).
+    Raises G4Error(G4_ERR_SCRATCH) when the step needs more than DECODE_STATIC_SCRATCH_BYTES.
+    Calls that may overlap on the GPU (unordered streams) share the scratch and race."""
+    B = int(q.shape[0])
+    _check(load().g4attn_decode_static(ctypes.byref(layer), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(seq_len), B,
+                                       ctypes.byref(cache), _ptr(page_table), int(page_table.shape[1]), _ptr(out),
+                                       _stream(stream)), "g4attn_decode_static")
     return out
 
 

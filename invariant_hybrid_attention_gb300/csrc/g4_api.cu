@@ -9,6 +9,8 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "g4_internal.h"
 #include "g4attn.h"
 
@@ -72,6 +74,30 @@ g4_status check_rows(const void* q_or_k, int32_t T, const int32_t* q_start, cons
   return G4_OK;
 }
 
+// Scratch of g4attn_decode_static: the partial softmax states of one decode step, in a
+// file-scope device array so that the call needs no allocation. One copy per device; its
+// address is looked up once per device and cached.
+static __device__ __align__(256) uint8_t g_decode_scratch[G4ATTN_DECODE_STATIC_SCRATCH_BYTES];
+
+constexpr int kScratchDevices = 64;
+std::mutex g_scratch_mutex;
+void* g_scratch_ptr[kScratchDevices];
+
+cudaError_t decode_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kScratchDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    if ((e = cudaGetSymbolAddress(&p, g_decode_scratch)) != cudaSuccess) return e;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return cudaSuccess;
+}
+
 }  // namespace
 
 extern "C" {
@@ -82,6 +108,7 @@ const char* g4attn_status_string(g4_status s) {
     case G4_ERR_INVALID: return "invalid argument";
     case G4_ERR_UNSUPPORTED: return "unsupported geometry";
     case G4_ERR_CUDA: return "CUDA runtime error";
+    case G4_ERR_SCRATCH: return "decode step larger than the static scratch buffer";
     case G4_ERR_TIMEOUT: return "bounded device wait timed out";
     case G4_ERR_DEVICE: return "device-detected bad page index or position";
   }
@@ -168,6 +195,21 @@ g4_status g4attn_decode(const g4attn_layer* layer, const void* q, const void* k_
   if (e != cudaSuccess) return G4_ERR_CUDA;
   return from_cuda(launch_decode(global, q, seq_len, B, global ? 0 : layer->window, scale_log2(layer), pc, out,
                                  workspace, st, cs));
+}
+
+g4_status g4attn_decode_static(const g4attn_layer* layer, const void* q, const void* k_new, const void* v_new,
+                               const int32_t* seq_len, int32_t B, const g4attn_cache* cache,
+                               const int32_t* page_table, int32_t max_pages, void* out, void* stream) {
+  bool global = false;
+  g4_status s = check_layer(layer, &global);
+  if (s != G4_OK) return s;
+  if (B <= 0 || max_pages <= 0) return G4_ERR_INVALID;
+  const size_t need = decode_workspace_bytes(global, B, max_pages, global ? 0 : layer->window);
+  if (need > G4ATTN_DECODE_STATIC_SCRATCH_BYTES) return G4_ERR_SCRATCH;
+  void* ws = nullptr;
+  if (decode_scratch(&ws) != cudaSuccess) return G4_ERR_CUDA;
+  return g4attn_decode(layer, q, k_new, v_new, seq_len, B, cache, page_table, max_pages, out, ws,
+                       G4ATTN_DECODE_STATIC_SCRATCH_BYTES, stream);
 }
 
 int32_t g4attn_provenance(const g4attn_layer* layer, char* buf, size_t len) {

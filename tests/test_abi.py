@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for s in range(6):
+    for s in range(7):
         assert len(g4.status_string(s)) > 0
     assert g4.status_string(g4.G4_ERR_UNSUPPORTED) == "unsupported geometry"
 
@@ -127,3 +127,25 @@ def test_product_path_never_imports_the_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(import|from)\s+oracle\b", text, flags=re.M), f
                 assert "oracle/" not in text and "oracle." not in text, f
+
+
+def test_decode_static_scratch_limit(lib):
+    """The static-scratch decode refuses, on the host and before any CUDA call, a step whose
+    workspace would exceed the static buffer; the documented examples sit at the boundary."""
+    hdr = open(os.path.join(ROOT, "include", "g4attn.h")).read()
+    assert "#define G4ATTN_DECODE_STATIC_SCRATCH_BYTES ((size_t)32 << 20)" in hdr
+    cap = g4.DECODE_STATIC_SCRATCH_BYTES
+    s, gl = g4.sliding_layer(1024), g4.global_layer()
+    ws = lambda layer, B, mp: lib.g4attn_decode_workspace_bytes(ctypes.byref(layer), B, mp)
+    assert ws(s, 203, 2048) <= cap < ws(s, 204, 2048)
+    assert ws(gl, 15, 2048) <= cap < ws(gl, 16, 2048)
+    cache = g4.g4attn_cache(16, None, 16, 4, 16)
+    st = lib.g4attn_decode_static(ctypes.byref(gl), 16, 16, None, 16, 16, ctypes.byref(cache), 16, 2048, 16, None)
+    assert st == g4.G4_ERR_SCRATCH
+    assert "static scratch" in g4.status_string(g4.G4_ERR_SCRATCH)
+    assert lib.g4attn_decode_static(ctypes.byref(gl), 16, 16, None, 16, 0, ctypes.byref(cache), 16, 2048, 16,
+                                    None) == g4.G4_ERR_INVALID
+    bad = g4.global_layer()
+    bad.head_dim = 256
+    assert lib.g4attn_decode_static(ctypes.byref(bad), 16, 16, None, 16, 1, ctypes.byref(cache), 16, 8, 16,
+                                    None) == g4.G4_ERR_UNSUPPORTED
