@@ -194,6 +194,14 @@ G4_DEV void st_peer_v4(uint32_t addr, float a, float b, float c, float d) {
   asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
                : "memory");
 }
+// Asynchronous store of 16 bytes into another CTA's shared memory; its completion counts the
+// bytes on that CTA's mbarrier `peer_bar` (complete_tx), as a bulk copy does. No fence needed:
+// the receiver sees the data once it observes the barrier phase complete.
+G4_DEV void st_async_peer_v4(uint32_t addr, float a, float b, float c, float d, uint32_t peer_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(addr),
+               "f"(a), "f"(b), "f"(c), "f"(d), "r"(peer_bar)
+               : "memory");
+}
 G4_DEV void st_peer_u32(uint32_t addr, uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }

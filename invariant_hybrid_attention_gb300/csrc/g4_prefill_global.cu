@@ -114,8 +114,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&sm.pv_done[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&sm.xfull[s], kSoftmaxThreads);   // arrivals come from the peer's softmax threads
-      mbar_init(&sm.xfree[s], kSoftmaxThreads);
+      mbar_init(&sm.xfull[s], 1);   // one local arrive with the expected bytes; the peer's stores complete them
+      mbar_init(&sm.xfree[s], kSoftmaxThreads / 32);   // one arrive per peer softmax warp
     }
     mbar_init(&sm.q_full, 1);
     mbar_init(&sm.q_ready, kSoftmaxThreads);
@@ -276,6 +276,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
 
     const uint32_t peer_xbuf = map_peer(smem_u32(&sm.xbuf[0][r][0]), peer);
+    const uint32_t peer_xfull = map_peer(smem_u32(&sm.xfull[0]), peer);
+    const uint32_t peer_xfree = map_peer(smem_u32(&sm.xfree[0]), peer);
+    constexpr uint32_t kXBytes = kBM * kBN * 4;   // one partial score tile
+    if (threadIdx.x == 64) {   // expect the peer's first two tiles
+      mbar_arrive_expect_tx(&sm.xfull[0], kXBytes);
+      if (n_tiles > 1) mbar_arrive_expect_tx(&sm.xfull[1], kXBytes);
+    }
     const float cl2 = p.scale_log2;
     float m_used = -INFINITY, l_run = 0.f;
     bool ok = true;
@@ -301,13 +308,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         ok = false;
         break;
       }
-      const uint32_t dst = peer_xbuf + par * (kBM * kBN * 4);
+      const uint32_t dst = peer_xbuf + par * kXBytes;
+      const uint32_t dbar = peer_xfull + par * 8;
 #pragma unroll
       for (int c = 0; c < 16; ++c)
-        st_peer_v4(dst + ((c ^ rsw) << 4), __uint_as_float(sr[4 * c]), __uint_as_float(sr[4 * c + 1]),
-                   __uint_as_float(sr[4 * c + 2]), __uint_as_float(sr[4 * c + 3]));
-      mbar_arrive_peer(map_peer(smem_u32(&sm.xfull[par]), peer));
-      if (!__all_sync(0xffffffffu, mbar_wait_cluster(&sm.xfull[par], (j >> 1) & 1, abort_flag, p.err))) {
+        st_async_peer_v4(dst + ((c ^ rsw) << 4), __uint_as_float(sr[4 * c]), __uint_as_float(sr[4 * c + 1]),
+                         __uint_as_float(sr[4 * c + 2]), __uint_as_float(sr[4 * c + 3]), dbar);
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.xfull[par], (j >> 1) & 1, abort_flag, p.err))) {
         ok = false;
         break;
       }
@@ -321,7 +328,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         s[4 * c + 2] = __uint_as_float(sr[4 * c + 2]) + o.z;
         s[4 * c + 3] = __uint_as_float(sr[4 * c + 3]) + o.w;
       }
-      if (j + 2 < n_tiles) mbar_arrive_peer(map_peer(smem_u32(&sm.xfree[par]), peer));
+      if (j + 2 < n_tiles) {   // buffer `par` is read: expect the peer's tile j+2 there, and tell the peer
+        __syncwarp();
+        if (threadIdx.x == 64) mbar_arrive_expect_tx(&sm.xfull[par], kXBytes);
+        if (lane == 0) mbar_arrive_peer(peer_xfree + par * 8);
+      }
 
       if (!(row_ok && kb + kBN - 1 <= pos)) {   // causal mask (and rows outside the sequence)
 #pragma unroll
