@@ -202,6 +202,14 @@ G4_DEV void st_async_peer_v4(uint32_t addr, float a, float b, float c, float d, 
                "f"(a), "f"(b), "f"(c), "f"(d), "r"(peer_bar)
                : "memory");
 }
+// Bulk copy of `bytes` from this CTA's shared memory into another CTA's (addresses 16-byte
+// aligned, size a multiple of 16); completion counts the bytes on the receiver's mbarrier.
+G4_DEV void bulk_s2peer(uint32_t dst_cluster, const void* src, uint32_t bytes, uint32_t peer_bar) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   dst_cluster),
+               "r"(smem_u32(src)), "r"(bytes), "r"(peer_bar)
+               : "memory");
+}
 G4_DEV void st_peer_u32(uint32_t addr, uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }

@@ -7,8 +7,9 @@
 // runs on a cluster of two CTAs, each owning half of the head dims (rank r: dims 256r ..
 // 256r+255):
 //   - S_r = Q[:, half r] . K[:, half r]^T on the CTA's tensor cores; the two partial score
-//     tiles are exchanged through distributed shared memory and both CTAs add them (IEEE
-//     addition commutes, so both hold the same S bits) and run the same softmax;
+//     tiles are exchanged through distributed shared memory (each warp stages its 32 rows and
+//     one bulk copy carries them to the peer) and both CTAs add them (IEEE addition commutes,
+//     so both hold the same S bits) and run the same softmax;
 //   - O[:, half r] += P . V[:, half r], V being the CTA's half of the un-rotated S tile: one
 //     copy of each stored half-page serves V and the un-rotated 3/4 of K;
 //   - the rotated quarter of K comes from the cache's k_rot side pages (p-RoPE(S), written
@@ -50,10 +51,11 @@ struct GlobalSmem {
   uint8_t st[kNS][kStage];          // S half tile (V; K outside the rotated columns), rotated tile;
                                     // st[2] first holds Q dims 0-127 of the half
   uint8_t qhi[2 * kQChunk];         // Q dims 128-255 of the half (128B swizzle): an A operand
-  float xbuf[2][kBM][kBN];          // the peer's partial scores, by tile parity
+  float xbuf[2][kBM][kBN];          // partial scores: the peer's tile j lands in xbuf[j & 1]; this
+                                    // CTA's own tile j is staged in xbuf[(j + 1) & 1] for the copy out
   uint64_t full[kNS], empty[kNS];
   uint64_t s_full[kNSP], p_full[kNSP], pv_done[kNSP];
-  uint64_t xfull[2], xfree[2];
+  uint64_t xfull[2];
   uint64_t q_full, q_ready, peer_done, teardown;
   uint32_t tmem_base;
   int abort_flag;
@@ -113,10 +115,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&sm.p_full[s], kSoftmaxThreads);
       mbar_init(&sm.pv_done[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&sm.xfull[s], 1);   // one local arrive with the expected bytes; the peer's stores complete them
-      mbar_init(&sm.xfree[s], kSoftmaxThreads / 32);   // one arrive per peer softmax warp
-    }
+    for (int s = 0; s < 2; ++s) mbar_init(&sm.xfull[s], 1);   // one local arrive with the expected bytes
     mbar_init(&sm.q_full, 1);
     mbar_init(&sm.q_ready, kSoftmaxThreads);
     mbar_init(&sm.peer_done, 1);
@@ -275,10 +274,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_arrive(&sm.q_ready);
     }
 
-    const uint32_t peer_xbuf = map_peer(smem_u32(&sm.xbuf[0][r][0]), peer);
-    const uint32_t peer_xfull = map_peer(smem_u32(&sm.xfull[0]), peer);
-    const uint32_t peer_xfree = map_peer(smem_u32(&sm.xfree[0]), peer);
     constexpr uint32_t kXBytes = kBM * kBN * 4;   // one partial score tile
+    constexpr uint32_t kXWarpBytes = 32 * kBN * 4;   // the 32 rows of one warp
+    const uint32_t xrows = (uint32_t)(warp & 3) * kXWarpBytes;
+    const uint32_t peer_xbuf = map_peer(smem_u32(&sm.xbuf[0][0][0]), peer) + xrows;
+    const uint32_t peer_xfull = map_peer(smem_u32(&sm.xfull[0]), peer);
     if (threadIdx.x == 64) {   // expect the peer's first two tiles
       mbar_arrive_expect_tx(&sm.xfull[0], kXBytes);
       if (n_tiles > 1) mbar_arrive_expect_tx(&sm.xfull[1], kXBytes);
@@ -302,18 +302,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tmem_ld_wait();
 
       // Partial scores over this CTA's 256 dims go to the peer; the peer's come back. Both
-      // CTAs then hold own + peer, the same sum in either order.
-      if (j >= 2 &&
-          !__all_sync(0xffffffffu, mbar_wait_cluster(&sm.xfree[par], ((j >> 1) - 1) & 1, abort_flag, p.err))) {
-        ok = false;
-        break;
-      }
-      const uint32_t dst = peer_xbuf + par * kXBytes;
-      const uint32_t dbar = peer_xfull + par * 8;
+      // CTAs then hold own + peer, the same sum in either order. The own tile is staged in
+      // xbuf[par ^ 1]: this CTA read the peer's tile j-1 from there last iteration, and the
+      // peer's tile j+1 cannot land there before this copy has completed (the peer sends it
+      // only after it has received all of tile j).
+      {
+        float4* stg = reinterpret_cast<float4*>(&sm.xbuf[par ^ 1][r][0]);
 #pragma unroll
-      for (int c = 0; c < 16; ++c)
-        st_async_peer_v4(dst + ((c ^ rsw) << 4), __uint_as_float(sr[4 * c]), __uint_as_float(sr[4 * c + 1]),
-                         __uint_as_float(sr[4 * c + 2]), __uint_as_float(sr[4 * c + 3]), dbar);
+        for (int c = 0; c < 16; ++c)
+          stg[c ^ rsw] = make_float4(__uint_as_float(sr[4 * c]), __uint_as_float(sr[4 * c + 1]),
+                                     __uint_as_float(sr[4 * c + 2]), __uint_as_float(sr[4 * c + 3]));
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0)
+          bulk_s2peer(peer_xbuf + par * kXBytes, reinterpret_cast<const uint8_t*>(&sm.xbuf[par ^ 1][0][0]) + xrows,
+                      kXWarpBytes, peer_xfull + par * 8);
+      }
       if (!__all_sync(0xffffffffu, mbar_wait(&sm.xfull[par], (j >> 1) & 1, abort_flag, p.err))) {
         ok = false;
         break;
@@ -328,11 +332,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         s[4 * c + 2] = __uint_as_float(sr[4 * c + 2]) + o.z;
         s[4 * c + 3] = __uint_as_float(sr[4 * c + 3]) + o.w;
       }
-      if (j + 2 < n_tiles) {   // buffer `par` is read: expect the peer's tile j+2 there, and tell the peer
-        __syncwarp();
-        if (threadIdx.x == 64) mbar_arrive_expect_tx(&sm.xfull[par], kXBytes);
-        if (lane == 0) mbar_arrive_peer(peer_xfree + par * 8);
-      }
+      if (j + 2 < n_tiles && threadIdx.x == 64) mbar_arrive_expect_tx(&sm.xfull[par], kXBytes);   // the peer's tile j+2
 
       if (!(row_ok && kb + kBN - 1 <= pos)) {   // causal mask (and rows outside the sequence)
 #pragma unroll
