@@ -67,9 +67,11 @@ def prefill_flops(D: int, Hq: int, lens, W: int) -> float:
 # ---------------------------------------------------------------- clocks sampling
 
 class Clocks:
+    """nvidia-smi sampler (50 ms) started before the warm-up; summary() keeps the samples whose
+    timestamps fall inside the timed region [t0, t1] (host wall clock)."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,timestamp")
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
@@ -81,7 +83,7 @@ class Clocks:
         os.close(fd)
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
@@ -95,14 +97,24 @@ class Clocks:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
-    def summary(self):
+    @staticmethod
+    def _when(stamp: str):
+        import datetime
+        try:
+            return datetime.datetime.strptime(stamp.strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
+
+    def summary(self, t0: float, t1: float):
         rows = []
         if self.path and os.path.exists(self.path):
             for line in open(self.path):
                 f = [x.strip() for x in line.split(",")]
-                if len(f) >= 9:
+                if len(f) >= 10:
                     rows.append(f)
             os.unlink(self.path)
+        inside = [r for r in rows if (self._when(r[9]) or 0.0) >= t0 and (self._when(r[9]) or 0.0) <= t1]
+        rows = inside
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
 
@@ -117,7 +129,7 @@ class Clocks:
         reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.strip().lower() == "active"})
         loaded = [s for s in sm if mx and s >= 0.5 * max(mx)] or sm
         return {"sm_mhz": statistics.median(loaded) if loaded else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows),
+                "reasons": reasons, "samples": len(rows), "window_s": round(t1 - t0, 3),
                 "power_w_max": max((num(r[3]) or 0.0) for r in rows)}
 
 
@@ -335,11 +347,13 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="g4attn", choices=["g4attn", "reference"])
     ap.add_argument("--parts", default="sliding,global,decode")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--decode-batch", type=int, default=64,
+                    help="requests in the decode mix (64 is the measured workload; smaller only for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -377,7 +391,7 @@ def main():
         parts.append(SlidingPrefill(g4, gi, PagedKV, device_int32))
     if "global" in want:
         parts.append(GlobalPrefill(g4, gi, PagedKV, device_int32))
-    dec = DecodeMix(g4, gi, PagedKV, device_int32) if "decode" in want else None
+    dec = DecodeMix(g4, gi, PagedKV, device_int32, B=args.decode_batch) if "decode" in want else None
     flush_buf = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device="cuda")
 
     def flush():
@@ -394,6 +408,7 @@ def main():
         return out
 
     sp = step_parts()
+    clk = Clocks(local).__enter__()   # sampling from before the warm-up; summarised over the timed region
     for _ in range(args.warmup):
         for _, fn in sp:
             fn()
@@ -407,23 +422,25 @@ def main():
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
-    with Clocks(local) as clk:
-        for _ in range(args.steps):
-            evs = []
-            for n, fn in sp:
-                flush()
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record()
-                fn()
-                b.record()
-                evs.append((n, a, b))
-            torch.cuda.synchronize()
-            for n, a, b in evs:
-                times[n].append(a.elapsed_time(b))
+    t_start = time.time()
+    for _ in range(args.steps):
+        evs = []
+        for n, fn in sp:
+            flush()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            evs.append((n, a, b))
+        torch.cuda.synchronize()
+        for n, a, b in evs:
+            times[n].append(a.elapsed_time(b))
     torch.cuda.synchronize()
+    t_end = time.time()
+    clk.__exit__(None, None, None)
     if dist is not None:
         dist.barrier()
-    clocks = clk.summary()
+    clocks = clk.summary(t_start, t_end)
     st = g4.g4attn_status_sync()
     if st != g4.G4_OK:
         raise SystemExit(f"device error in the timed region: {g4.status_string(st)}")
@@ -520,7 +537,7 @@ def main():
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic: seeded N(0,1) bf16 values (device generator), random page permutations",
-            "config": {"workload": WORKLOAD, "parts": [n for n, _ in sp],
+            "config": {"workload": WORKLOAD, "parts": [n for n, _ in sp], "decode_batch": args.decode_batch,
                        "l2": "flushed before every part (512 MB write); inputs also exceed L2",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "roofline": roofline, "prefill": res, "decode": decode, "cpu_baseline": cpu, "e2e": e2e,
