@@ -213,6 +213,7 @@ class DecodeMix:
         gplan = gi.make_page_plan(self.lens, seed=length_seed * 31 + 99)
         self.g_cache = PagedKV(gplan.num_pages, 4, 512, shared=True, fill=None)
         self.g_cache.k.copy_(gi.bf16_normal_device(tuple(self.g_cache.k.shape), value_seed * 1000 + 99))
+        self.g_cache.k_rot.copy_(gi.bf16_normal_device(tuple(self.g_cache.k_rot.shape), value_seed * 1000 + 98))
         self.g_table = gplan.table.cuda()
         self.q_s = gi.bf16_normal_device((B, 32, 256), value_seed * 7 + 1)
         self.k_s = gi.bf16_normal_device((B, 16, 256), value_seed * 7 + 2)
@@ -228,7 +229,7 @@ class DecodeMix:
         qo_s = B * 32 * 256 * 2 * 2
         qo_g = B * 32 * 512 * 2 * 2
         self.bytes_sliding = sum(min(L, W) for L in self.lens) * 16 * 256 * 2 * 2 + qo_s
-        self.bytes_global = sum(self.lens) * 4 * 512 * 2 + qo_g
+        self.bytes_global = sum(self.lens) * 4 * 512 * 2 + qo_g   # credited: S once (the k_rot reads are not)
         self.n_sliding = n_sliding
         self.bytes = n_sliding * self.bytes_sliding + self.bytes_global
         self.launches = 3 * (n_sliding + 1)

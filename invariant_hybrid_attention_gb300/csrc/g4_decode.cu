@@ -8,9 +8,10 @@
 // Every number a request gets depends only on its own position, window and data.
 //
 // Sliding layers (2 query heads per KV head, 2 flop per byte) run on CUDA cores. Global layers
-// (8 query heads per KV head, K==V, 16 flop per byte) run on warp-level bf16 MMA: S^T = K q^T
-// with K = p-RoPE(S) rotated in registers (pairs t < 64: dims t and t+256), then
-// O^T += S^T' P^T with the same un-rotated S rows as V: one read of the cache for both.
+// (8 query heads per KV head, K==V, 16 flop per byte) run on warp-level bf16 MMA: S^T = K q^T,
+// where K is the stored S except on the 128 rotated dims (pairs t < 64: dims t and t+256),
+// which come from the cache's k_rot side pages (p-RoPE(S), written with S by the append pass);
+// then O^T += S^T' P^T with the un-rotated S rows as V.
 #include <math.h>
 
 #include "g4_internal.h"
@@ -235,8 +236,10 @@ __global__ void __launch_bounds__(128) decode_sliding_kernel(DecodeParams p) {
 // ---------------------------------------------------------------- global: D 512, Hkv 4, G 8, K==V
 constexpr int kGD = kGlobalD;
 constexpr int kGWarps = 4;
-constexpr int kGStages = 3;                      // pages in flight per warp
-constexpr int kGStageBytes = kPage * kGD * 2;    // one tiled page-head block: 16 KB
+constexpr int kGStages = 2;                      // pages in flight per warp
+constexpr int kGSBytes = kPage * kGD * 2;        // one tiled page-head block of S: 16 KB
+constexpr int kGRotBytes = kRotPageElems * 2;    // its k_rot block: 4 KB
+constexpr int kGStageBytes = kGSBytes + kGRotBytes;
 constexpr int kGRow = kGD * 2 + 16;              // padded query row: ldmatrix rows hit distinct banks
 constexpr int kGQBytes = 8 * kGRow;              // the 8 roped query heads
 constexpr int kGPRow = 48;                       // P^T staging row (8 heads x 16 keys bf16, padded)
@@ -291,13 +294,15 @@ __global__ void __launch_bounds__(128, 1) decode_global_kernel(DecodeParams p) {
   uint8_t* my_stages = stage_base + warp * kGStages * kGStageBytes;
   uint64_t* my_bars = bars + warp * kGStages;
   const __nv_bfloat16* sc = (const __nv_bfloat16*)p.cache.k;
+  const __nv_bfloat16* rc = (const __nv_bfloat16*)p.cache.krot;
   auto issue = [&](int i) {   // lane 0 only
     const int pg = pg0 + warp + kGWarps * i;
-    const __nv_bfloat16* src = sc + (((size_t)pt[pg] * kGlobalHkv + g) * kPage) * kGD;
+    const size_t blk = (size_t)pt[pg] * kGlobalHkv + g;
     uint8_t* dst = my_stages + (i % kGStages) * kGStageBytes;
     uint64_t* bar = &my_bars[i % kGStages];
     mbar_arrive_expect_tx(bar, kGStageBytes);
-    bulk_g2s(dst, src, kGStageBytes, bar);
+    bulk_g2s(dst, sc + blk * kPage * kGD, kGSBytes, bar);
+    bulk_g2s(dst + kGSBytes, rc + blk * kRotPageElems, kGRotBytes, bar);
   };
   int n_issued = 0, n_done = 0;   // lane 0's view of this warp's copies
   if (lane == 0)
@@ -330,7 +335,10 @@ __global__ void __launch_bounds__(128, 1) decode_global_kernel(DecodeParams p) {
   // K as A (non-transposed): tiles (keys 0-7 | 8-15) x (dims +0 | +8);
   // V^T as A (transposed): tiles (dims +0 | +8) x (keys 0-7 | 8-15).
   // A 16-dim step s starts at byte (s / 16) * 8192 + (s % 16) * 256 of the stage.
+  // The k_rot block after it holds the rotated dims as [half][kg][dg 0-7][8][8]: rotated step
+  // s (s % 16 < 4) starts at byte 16384 + (s / 16) * 2048 + (s % 16) * 256, key groups 1 KB apart.
   const uint32_t a_lane = (((lane >> 3) & 1) * 32 + (lane >> 4)) * 128 + (lane & 7) * 16;
+  const uint32_t r_lane = kGSBytes + (((lane >> 3) & 1) * 8 + (lane >> 4)) * 128 + (lane & 7) * 16;
   const uint32_t v_lane = (((lane >> 4) & 1) * 32 + ((lane >> 3) & 1)) * 128 + (lane & 7) * 16;
   auto step_off = [](int s16) -> uint32_t { return (uint32_t)((s16 >> 4) * 8192 + (s16 & 15) * 256); };
   const uint32_t q_lane = q_addr + (lane & 7) * kGRow + (lane >> 3) * 16;
@@ -355,20 +363,10 @@ __global__ void __launch_bounds__(128, 1) decode_global_kernel(DecodeParams p) {
     // ---- S^T = K q^T (16 keys x 8 heads), two accumulation chains
     float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {   // rotated k-steps: dims 16ks.. with partners +256
+    for (int ks = 0; ks < 4; ++ks) {   // rotated k-steps: dims 16ks.. and their partners +256
       uint32_t a[4], h[4], bq0, bq1, bh0, bh1;
-      ldsm_x4(pa + a_lane + step_off(ks), a[0], a[1], a[2], a[3]);
-      ldsm_x4(pa + a_lane + step_off(ks + 16), h[0], h[1], h[2], h[3]);
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int key = key0 + gq + 8 * (r & 1);
-        const int t = ks * 16 + 2 * cq + 8 * (r >> 1);
-        float x0 = bf16_lo(a[r]), x1 = bf16_hi(a[r]), y0 = bf16_lo(h[r]), y1 = bf16_hi(h[r]);
-        rope_pair(x0, y0, rope_cs(p.tb, t, key));
-        rope_pair(x1, y1, rope_cs(p.tb, t + 1, key));
-        a[r] = pack_bf16(x0, x1);   // declared cast: roped K in bf16
-        h[r] = pack_bf16(y0, y1);
-      }
+      ldsm_x4(pa + r_lane + ks * 256, a[0], a[1], a[2], a[3]);
+      ldsm_x4(pa + r_lane + 2048 + ks * 256, h[0], h[1], h[2], h[3]);
       uint32_t t0, t1;
       ldsm_x4(q_lane + ks * 32, bq0, bq1, t0, t1);          // k-step ks (and ks+1, unused)
       ldsm_x4(q_lane + (ks + 16) * 32, bh0, bh1, t0, t1);   // k-step ks+16
