@@ -7,8 +7,8 @@
 // inside a chunk the pages go round-robin to four warps whose states merge in warp order.
 // Every number a request gets depends only on its own position, window and data.
 //
-// Sliding layers (2 query heads per KV head, 2 flop per byte) run on CUDA cores. Global layers
-// (8 query heads per KV head, K==V, 16 flop per byte) run on warp-level bf16 MMA: S^T = K q^T,
+// Both layer kinds run on warp-level bf16 MMA (m16n8k16) over bulk-copied page blocks. Global
+// layers (8 query heads per KV head, K==V, 16 flop per byte): S^T = K q^T,
 // where K is the stored S except on the 128 rotated dims (pairs t < 64: dims t and t+256),
 // which come from the cache's k_rot side pages (p-RoPE(S), written with S by the append pass);
 // then O^T += S^T' P^T with the un-rotated S rows as V.
@@ -36,22 +36,36 @@ struct DecodeParams {
   uint32_t* err;
 };
 
-__device__ __forceinline__ uint4 ldg_nc(const void* p) {
-  uint4 r;
-  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
-  return r;
-}
-
 // ---------------------------------------------------------------- sliding: D 256, Hkv 16, G 2
+// One CTA per (fixed 256-key chunk, KV head, request); its pages (16 keys each) go round-robin
+// to 4 warps. Pages arrive by bulk copy (8 KB of K' and 8 KB of V per page-head block) into a
+// 6-stage ring shared by the warps: page i sits in stage i % 6, and the warp that consumed
+// page i refills that stage with page i + 6. A per-stage count of issued pages lets the
+// consumer of page i wait until page i has been issued before it tests the barrier: from then
+// on the barrier is in phase i / 6 or the one after, which a parity wait tells apart (a
+// parity wait cannot tell phases two apart, and the consumer of page i never saw page i - 6). Scores S^T = K q^T and O^T += V^T P^T run on
+// warp-level bf16 MMA (m16n8k16) from ldmatrix on the tiled blocks; the two query heads of
+// the KV head are columns 0-1 of the 8-wide N dimension (the other columns carry q = 0 and
+// are never read out).
 constexpr int kSD = kSlidingD;
+constexpr int kSStages = 6;
+constexpr int kSPageBytes = kPage * kSD * 2;      // one tiled page-head block (K' or V): 8 KB
+constexpr int kSStageBytes = 2 * kSPageBytes;     // K' then V
+constexpr int kSPRow = 48;                        // P^T staging row (8 heads x 16 keys bf16, padded)
+constexpr int kSSmem = kSStages * kSStageBytes + 4 * 8 * kSPRow + kSStages * 8;
 
-__global__ void __launch_bounds__(128) decode_sliding_kernel(DecodeParams p) {
+__global__ void __launch_bounds__(128, 2) decode_sliding_kernel(DecodeParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* ring = smem;
+  uint8_t* p_s_all = smem + kSStages * kSStageBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(p_s_all + 4 * 8 * kSPRow);
+  __shared__ int abort_flag;
+  __shared__ int issued[kSStages];   // pages issued into each stage so far
+  __shared__ float red_m[4][2], red_l[4][2];
+
   const int cr = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __shared__ float red_m[4][2], red_l[4][2];
-  __shared__ float red_o[4][2][kSD];
+  const int gq = lane >> 2, cq = lane & 3;   // mma fragment coordinates
 
   const int pos = p.seq_len[b] - 1;
   if (pos < 0 || pos >= kMaxPos || (pos >> 4) >= p.cache.max_pages) {
@@ -65,12 +79,19 @@ __global__ void __launch_bounds__(128) decode_sliding_kernel(DecodeParams p) {
   if (k_begin > k_end) return;                                                       // unused slot
 
   const int pg0 = k_begin >> 4, pg1 = k_end >> 4;
+  const int n_pages = pg1 - pg0 + 1;
   const int32_t* pt = p.cache.page_table + (size_t)b * p.cache.max_pages;
   bool bad = false;
   for (int i = pg0 + (int)threadIdx.x; i <= pg1; i += 128) {
     const int ph = pt[i];
     bad |= (ph < 0 || ph >= p.cache.num_pages);
   }
+  if (threadIdx.x == 0) abort_flag = 0;
+  if (threadIdx.x < kSStages) {
+    mbar_init(&full[threadIdx.x], 1);
+    issued[threadIdx.x] = 0;
+  }
+  fence_mbar_init();
   const size_t slot = (((size_t)b * kSlidingHq + 2 * g) * p.NC + cr);
   if (__syncthreads_or(bad)) {
     if (threadIdx.x == 0) {
@@ -83,132 +104,184 @@ __global__ void __launch_bounds__(128) decode_sliding_kernel(DecodeParams p) {
     return;
   }
 
-  // Roped query of both heads; lane owns dims 8*lane .. 8*lane+7 (pair t = 8*(lane%16) + i).
-  float q0[8], q1[8];
-  {
-    const int t0 = (lane & 15) * 8;
-    const bool hi = lane >= 16;
-    const __nv_bfloat16* qb = p.q + ((size_t)b * kSlidingHq + 2 * g) * kSD;
-    float2 cs[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) cs[i] = rope_cs(p.tb, t0 + i, pos);
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      const uint4 a4 = *reinterpret_cast<const uint4*>(qb + hh * kSD + t0);
-      const uint4 b4 = *reinterpret_cast<const uint4*>(qb + hh * kSD + kSD / 2 + t0);
-      const uint32_t* aw = reinterpret_cast<const uint32_t*>(&a4);
-      const uint32_t* bw = reinterpret_cast<const uint32_t*>(&b4);
-      float* qd = hh ? q1 : q0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        float x = (i & 1) ? bf16_hi(aw[i >> 1]) : bf16_lo(aw[i >> 1]);
-        float y = (i & 1) ? bf16_hi(bw[i >> 1]) : bf16_lo(bw[i >> 1]);
-        rope_pair(x, y, cs[i]);
-        qd[i] = round_bf16(hi ? y : x);   // declared cast: roped q in bf16
-      }
-    }
-  }
-
-  float m_run0 = -INFINITY, m_run1 = -INFINITY, l_run0 = 0.f, l_run1 = 0.f;
-  float o0[8], o1[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) o0[i] = o1[i] = 0.f;
-
   const __nv_bfloat16* kc = (const __nv_bfloat16*)p.cache.k;
   const __nv_bfloat16* vc = (const __nv_bfloat16*)p.cache.v;
-  for (int pg = pg0 + warp; pg <= pg1; pg += 4) {
-    const size_t base = (((size_t)pt[pg] * kSlidingHkv + g) * kPage) * kSD;   // page-head block
-    uint4 kr[16], vr[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) kr[j] = ldg_nc(kc + base + tiled_offset(j, lane * 8, kSD));
-#pragma unroll
-    for (int j = 0; j < 16; ++j) vr[j] = ldg_nc(vc + base + tiled_offset(j, lane * 8, kSD));
+  auto issue = [&](int i) {   // one thread
+    const int st = i % kSStages;
+    const size_t blk = (size_t)pt[pg0 + i] * kSlidingHkv + g;
+    uint8_t* dst = ring + st * kSStageBytes;
+    mbar_arrive_expect_tx(&full[st], kSStageBytes);
+    bulk_g2s(dst, kc + blk * kPage * kSD, kSPageBytes, &full[st]);
+    bulk_g2s(dst + kSPageBytes, vc + blk * kPage * kSD, kSPageBytes, &full[st]);
+    __threadfence_block();
+    *reinterpret_cast<volatile int*>(&issued[st]) = i / kSStages + 1;
+  };
+  if (threadIdx.x == 0)
+    for (int i = 0; i < min(kSStages, n_pages); ++i) issue(i);
 
-    // Partial dot products over this lane's 8 dims: index 2*key + head.
-    float part[32];
+  // Roped query as B fragments: b0/b1 of k-step ks hold q[gq][16ks + 2cq (+8) .. +1] for
+  // heads gq = 0, 1 (zero for the other columns). Pair t and t + 128 sit in k-steps ks and
+  // ks + 8 of the same lane.
+  uint32_t qb[16][2];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const uint32_t* w = reinterpret_cast<const uint32_t*>(&kr[j]);
-      float s0 = 0.f, s1 = 0.f;
+  for (int ks = 0; ks < 16; ++ks) qb[ks][0] = qb[ks][1] = 0u;
+  if (gq < 2) {
+    const __nv_bfloat16* qr = p.q + ((size_t)b * kSlidingHq + 2 * g + gq) * kSD;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float kv = (i & 1) ? bf16_hi(w[i >> 1]) : bf16_lo(w[i >> 1]);
-        s0 = fmaf(q0[i], kv, s0);
-        s1 = fmaf(q1[i], kv, s1);
+    for (int ks = 0; ks < 8; ++ks) {
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const int t = 16 * ks + 8 * hf + 2 * cq;
+        const uint32_t xw = *reinterpret_cast<const uint32_t*>(qr + t);
+        const uint32_t yw = *reinterpret_cast<const uint32_t*>(qr + t + kSD / 2);
+        float x0 = bf16_lo(xw), x1 = bf16_hi(xw), y0 = bf16_lo(yw), y1 = bf16_hi(yw);
+        rope_pair(x0, y0, rope_cs(p.tb, t, pos));
+        rope_pair(x1, y1, rope_cs(p.tb, t + 1, pos));
+        qb[ks][hf] = pack_bf16(x0, x1);   // declared cast: roped q in bf16
+        qb[ks + 8][hf] = pack_bf16(y0, y1);
       }
-      part[2 * j] = s0;
-      part[2 * j + 1] = s1;
     }
-    // Transposing reduction: afterwards lane l holds the full dot of index l.
-#pragma unroll
-    for (int m = 16, n = 32; m >= 1; m >>= 1, n >>= 1) {
-      const bool upper = (lane & m) != 0;
-#pragma unroll
-      for (int i = 0; i < n / 2; ++i) {
-        const float send = upper ? part[i] : part[i + n / 2];
-        const float keep = upper ? part[i + n / 2] : part[i];
-        part[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
-      }
-    }
-    const int key = pg * kPage + (lane >> 1);
-    const bool valid = key >= k_begin && key <= k_end;
-    const float x = valid ? part[0] * p.scale_log2 : -INFINITY;
+  }
 
-    float mt = x;
+  uint8_t* p_s = p_s_all + warp * 8 * kSPRow;
+  const uint32_t p_addr = smem_u32(p_s);
+  float o[16][4];
 #pragma unroll
-    for (int m = 2; m <= 16; m <<= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, m));
-    const float mt_o = __shfl_xor_sync(0xffffffffu, mt, 1);
-    const float mt0 = (lane & 1) ? mt_o : mt, mt1 = (lane & 1) ? mt : mt_o;
-    const float mn0 = fmaxf(m_run0, mt0), mn1 = fmaxf(m_run1, mt1);
-    if (mn0 > m_run0 + kLazyRescale) {
-      const float a = exp2f(m_run0 - mn0);
-      m_run0 = mn0;
-      l_run0 *= a;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) o0[i] *= a;
-    }
-    if (mn1 > m_run1 + kLazyRescale) {
-      const float a = exp2f(m_run1 - mn1);
-      m_run1 = mn1;
-      l_run1 *= a;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) o1[i] *= a;
-    }
-    const float pv = valid ? exp2f(x - ((lane & 1) ? m_run1 : m_run0)) : 0.f;
-    float ls = pv;
-#pragma unroll
-    for (int m = 2; m <= 16; m <<= 1) ls += __shfl_xor_sync(0xffffffffu, ls, m);
-    const float ls_o = __shfl_xor_sync(0xffffffffu, ls, 1);
-    l_run0 += (lane & 1) ? ls_o : ls;
-    l_run1 += (lane & 1) ? ls : ls_o;
+  for (int mt = 0; mt < 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+  // ldmatrix lane addresses in a tiled block [key group kg][dim group dg][8 keys][8 dims]
+  // (core matrices of 128 B at (kg * 32 + dg) * 128): K as A takes tiles (keys 0-7 | 8-15) x
+  // (dims +0 | +8); V^T as A (transposed) takes tiles (dims +0 | +8) x (keys 0-7 | 8-15).
+  const uint32_t a_lane = (((lane >> 3) & 1) * 32 + (lane >> 4)) * 128 + (lane & 7) * 16;
+  const uint32_t v_lane = (((lane >> 4) & 1) * 32 + ((lane >> 3) & 1)) * 128 + (lane & 7) * 16;
 
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const float p0 = __shfl_sync(0xffffffffu, pv, 2 * j);
-      const float p1 = __shfl_sync(0xffffffffu, pv, 2 * j + 1);
-      const int kj = pg * kPage + j;
-      if (kj >= k_begin && kj <= k_end) {   // stale slots may hold NaN: never multiply them
-        const uint32_t* w = reinterpret_cast<const uint32_t*>(&vr[j]);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float vv = (i & 1) ? bf16_hi(w[i >> 1]) : bf16_lo(w[i >> 1]);
-          o0[i] = fmaf(p0, vv, o0[i]);
-          o1[i] = fmaf(p1, vv, o1[i]);
+  for (int i = warp; i < n_pages; i += 4) {
+    const int st = i % kSStages, ph = i / kSStages;
+    if (ph > 0) {   // page i issued yet? (bounded)
+      bool ok = true;
+      const unsigned long long t0 = globaltimer();
+      while (*reinterpret_cast<volatile int*>(&issued[st]) <= ph) {
+        if (*reinterpret_cast<volatile int*>(&abort_flag)) {
+          ok = false;
+          break;
+        }
+        if (globaltimer() - t0 > kWaitLimitNs) {
+          abort_flag = 1;
+          set_error(p.err, kErrTimeout);
+          ok = false;
+          break;
         }
       }
+      if (!__all_sync(0xffffffffu, ok)) break;
+      __threadfence_block();
+    }
+    if (!mbar_wait(&full[st], ph & 1, &abort_flag, p.err)) break;
+    uint8_t* kp = ring + st * kSStageBytes;
+    uint8_t* vp = kp + kSPageBytes;
+    const int key0 = (pg0 + i) * kPage;
+    if (key0 < k_begin || key0 + kPage - 1 > k_end) {   // V rows of keys outside the chunk: zero
+      for (int idx = lane; idx < kPage * (kSD / 8); idx += 32) {
+        const int r = idx / (kSD / 8), dg = idx % (kSD / 8);
+        if (key0 + r < k_begin || key0 + r > k_end)
+          *reinterpret_cast<uint4*>(vp + ((r >> 3) * 32 + dg) * 128 + (r & 7) * 16) = make_uint4(0, 0, 0, 0);
+      }
+      __syncwarp();
+    }
+    const uint32_t ka = smem_u32(kp), va = smem_u32(vp);
+
+    // ---- S^T = K q^T (16 keys x 8 columns), two accumulation chains
+    float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ks = 0; ks < 16; ks += 2) {
+      uint32_t a[4], a2[4];
+      ldsm_x4(ka + a_lane + ks * 256, a[0], a[1], a[2], a[3]);
+      ldsm_x4(ka + a_lane + (ks + 1) * 256, a2[0], a2[1], a2[2], a2[3]);
+      mma16816(s0, a[0], a[1], a[2], a[3], qb[ks][0], qb[ks][1]);
+      mma16816(s1, a2[0], a2[1], a2[2], a2[3], qb[ks + 1][0], qb[ks + 1][1]);
+    }
+
+    // ---- online softmax per column (heads 2cq, 2cq+1; keys gq, gq+8)
+    float x[4];
+    const bool v_lo = key0 + gq >= k_begin && key0 + gq <= k_end;
+    const bool v_hi = key0 + gq + 8 >= k_begin && key0 + gq + 8 <= k_end;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const float sv = s0[r] + s1[r];
+      x[r] = ((r < 2) ? v_lo : v_hi) ? sv * p.scale_log2 : -INFINITY;
+    }
+    float pb[4];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      float mt = fmaxf(x[j], x[2 + j]);
+#pragma unroll
+      for (int m = 4; m <= 16; m <<= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, m));
+      const float mn = fmaxf(m_run[j], mt);
+      if (mn > m_run[j] + kLazyRescale) {
+        const float al = exp2f(m_run[j] - mn);
+        m_run[j] = mn;
+        l_run[j] *= al;
+#pragma unroll
+        for (int mt2 = 0; mt2 < 16; ++mt2) {
+          o[mt2][j] *= al;
+          o[mt2][2 + j] *= al;
+        }
+      }
+      pb[j] = (x[j] == -INFINITY) ? 0.f : round_bf16(exp2f(x[j] - m_run[j]));
+      pb[2 + j] = (x[2 + j] == -INFINITY) ? 0.f : round_bf16(exp2f(x[2 + j] - m_run[j]));
+      float ls = pb[j] + pb[2 + j];
+#pragma unroll
+      for (int m = 4; m <= 16; m <<= 1) ls += __shfl_xor_sync(0xffffffffu, ls, m);
+      l_run[j] += ls;
+    }
+    // P^T into the B-fragment layout through a per-warp staging block [column][key].
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      *reinterpret_cast<__nv_bfloat16*>(p_s + (2 * cq + j) * kSPRow + gq * 2) = __float2bfloat16_rn(pb[j]);
+      *reinterpret_cast<__nv_bfloat16*>(p_s + (2 * cq + j) * kSPRow + (gq + 8) * 2) = __float2bfloat16_rn(pb[2 + j]);
+    }
+    __syncwarp();
+    uint32_t pb0, pb1;
+    ldsm_x2(p_addr + (lane & 7) * kSPRow + ((lane >> 3) & 1) * 16, pb0, pb1);
+
+    // ---- O^T += V^T P^T over the 16 dim tiles
+#pragma unroll
+    for (int mt = 0; mt < 16; ++mt) {
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4_t(va + v_lane + mt * 256, a0, a1, a2, a3);
+      mma16816(o[mt], a0, a1, a2, a3, pb0, pb1);
+    }
+    __syncwarp();
+    if (lane == 0 && i + kSStages < n_pages) {   // refill this stage with page i + 6
+      fence_proxy_async();
+      issue(i + kSStages);
     }
   }
-
-  if (lane == 0) {
-    red_m[warp][0] = m_run0;
-    red_m[warp][1] = m_run1;
-    red_l[warp][0] = l_run0;
-    red_l[warp][1] = l_run1;
+  __syncthreads();
+  if (abort_flag && threadIdx.x == 0) {   // after a timeout: wait (bounded) for copies in flight
+    const unsigned long long t0 = globaltimer();
+    for (int st = 0; st < kSStages; ++st)
+      if (issued[st] > 0)
+        while (!mbar_try_wait(smem_u32(&full[st]), (issued[st] - 1) & 1) && globaltimer() - t0 < kWaitLimitNs) {
+        }
   }
+  __syncthreads();   // all stages consumed: reuse the ring for the warp merge
+
+  float* red_o = reinterpret_cast<float*>(ring);   // [warps][2 heads][256]
+  if (lane == 0) {
+    red_m[warp][0] = m_run[0];
+    red_m[warp][1] = m_run[1];
+    red_l[warp][0] = l_run[0];
+    red_l[warp][1] = l_run[1];
+  }
+  if (cq == 0) {
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    red_o[warp][0][lane * 8 + i] = o0[i];
-    red_o[warp][1][lane * 8 + i] = o1[i];
+    for (int mt = 0; mt < 16; ++mt) {
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int d = mt * 16 + gq + 8 * (r >> 1), hh = r & 1;
+        red_o[(warp * 2 + hh) * kSD + d] = o[mt][r];
+      }
+    }
   }
   __syncthreads();
   // Merge the four warps in warp order; thread t writes 4 of the 2 x 256 outputs.
@@ -222,7 +295,7 @@ __global__ void __launch_bounds__(128) decode_sliding_kernel(DecodeParams p) {
     for (int w = 0; w < 4; ++w) {
       const float sc = (M == -INFINITY) ? 0.f : exp2f(red_m[w][hh] - M);
       L = fmaf(red_l[w][hh], sc, L);
-      O = fmaf(red_o[w][hh][d], sc, O);
+      O = fmaf(red_o[(w * 2 + hh) * kSD + d], sc, O);
     }
     const size_t s = slot + (size_t)hh * p.NC;
     p.ws_o[s * kSD + d] = O;
@@ -577,7 +650,15 @@ cudaError_t launch_decode(bool global, const void* q, const int32_t* seq_len, in
                                                                     kDecodeChunkGlobal, (__nv_bfloat16*)out);
   } else {
     p.tb = st.sliding;
-    decode_sliding_kernel<<<dim3(p.NC, kSlidingHkv, B), 128, 0, s>>>(p);
+    static bool attr_set_s[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !attr_set_s[dev]) {
+      cudaError_t e = cudaFuncSetAttribute(decode_sliding_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSSmem);
+      if (e != cudaSuccess) return e;
+      attr_set_s[dev] = true;
+    }
+    decode_sliding_kernel<<<dim3(p.NC, kSlidingHkv, B), 128, kSSmem, s>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     decode_merge_kernel<kSD><<<dim3(kSlidingHq, B), kSD / 4, 0, s>>>(p.ws_ml, p.ws_o, seq_len, p.NC, window,
