@@ -309,22 +309,28 @@ __global__ void __launch_bounds__(128, 2) decode_sliding_kernel(DecodeParams p) 
 // ---------------------------------------------------------------- global: D 512, Hkv 4, G 8, K==V
 constexpr int kGD = kGlobalD;
 constexpr int kGWarps = 4;
-constexpr int kGStages = 2;                      // pages in flight per warp
+constexpr int kGStages = 5;                      // ring of page stages shared by the 4 warps
 constexpr int kGSBytes = kPage * kGD * 2;        // one tiled page-head block of S: 16 KB
 constexpr int kGRotBytes = kRotPageElems * 2;    // its k_rot block: 4 KB
 constexpr int kGStageBytes = kGSBytes + kGRotBytes;
 constexpr int kGRow = kGD * 2 + 16;              // padded query row: ldmatrix rows hit distinct banks
 constexpr int kGQBytes = 8 * kGRow;              // the 8 roped query heads
 constexpr int kGPRow = 48;                       // P^T staging row (8 heads x 16 keys bf16, padded)
-constexpr int kGSmem = kGWarps * kGStages * kGStageBytes + kGQBytes + kGWarps * 8 * kGPRow + 256;
+constexpr int kGSmem = kGStages * kGStageBytes + kGQBytes + kGWarps * 8 * kGPRow + kGStages * 8;
+static_assert(kGStages * kGStageBytes >= kGWarps * 8 * kGD * 4, "the warp merge reuses the ring");
 
-__global__ void __launch_bounds__(128, 1) decode_global_kernel(DecodeParams p) {
+// Page i of the chunk goes to warp i % 4 and sits in ring stage i % 5; the warp that consumed
+// page i refills the stage with page i + 5. As in the sliding kernel, the consumer of page i
+// first waits until page i has been issued (per-stage counts), so that a parity wait names
+// the right phase. Two CTAs fit per SM.
+__global__ void __launch_bounds__(128, 2) decode_global_kernel(DecodeParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* stage_base = smem;
-  uint8_t* q_s = smem + kGWarps * kGStages * kGStageBytes;
+  uint8_t* q_s = smem + kGStages * kGStageBytes;
   uint8_t* p_s_all = q_s + kGQBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(p_s_all + kGWarps * 8 * kGPRow);   // [warps][stages]
+  uint64_t* full = reinterpret_cast<uint64_t*>(p_s_all + kGWarps * 8 * kGPRow);
   __shared__ int abort_flag;
+  __shared__ int issued[kGStages];   // pages issued into each stage so far
   __shared__ float red_m[kGWarps][8], red_l[kGWarps][8];
 
   const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
@@ -349,7 +355,10 @@ __global__ void __launch_bounds__(128, 1) decode_global_kernel(DecodeParams p) {
     bad |= (ph < 0 || ph >= p.cache.num_pages);
   }
   if (threadIdx.x == 0) abort_flag = 0;
-  if (threadIdx.x < kGWarps * kGStages) mbar_init(&bars[threadIdx.x], 1);
+  if (threadIdx.x < kGStages) {
+    mbar_init(&full[threadIdx.x], 1);
+    issued[threadIdx.x] = 0;
+  }
   fence_mbar_init();
   if (__syncthreads_or(bad)) {
     if (threadIdx.x == 0) {
@@ -362,24 +371,21 @@ __global__ void __launch_bounds__(128, 1) decode_global_kernel(DecodeParams p) {
     return;
   }
 
-  // This warp's pages: pg0 + warp + 4*i.
-  const int n_mine = (pg1 - pg0 - warp) >= 0 ? (pg1 - pg0 - warp) / kGWarps + 1 : 0;
-  uint8_t* my_stages = stage_base + warp * kGStages * kGStageBytes;
-  uint64_t* my_bars = bars + warp * kGStages;
+  const int n_pages = pg1 - pg0 + 1;
   const __nv_bfloat16* sc = (const __nv_bfloat16*)p.cache.k;
   const __nv_bfloat16* rc = (const __nv_bfloat16*)p.cache.krot;
-  auto issue = [&](int i) {   // lane 0 only
-    const int pg = pg0 + warp + kGWarps * i;
-    const size_t blk = (size_t)pt[pg] * kGlobalHkv + g;
-    uint8_t* dst = my_stages + (i % kGStages) * kGStageBytes;
-    uint64_t* bar = &my_bars[i % kGStages];
-    mbar_arrive_expect_tx(bar, kGStageBytes);
-    bulk_g2s(dst, sc + blk * kPage * kGD, kGSBytes, bar);
-    bulk_g2s(dst + kGSBytes, rc + blk * kRotPageElems, kGRotBytes, bar);
+  auto issue = [&](int i) {   // one thread
+    const int st = i % kGStages;
+    const size_t blk = (size_t)pt[pg0 + i] * kGlobalHkv + g;
+    uint8_t* dst = stage_base + st * kGStageBytes;
+    mbar_arrive_expect_tx(&full[st], kGStageBytes);
+    bulk_g2s(dst, sc + blk * kPage * kGD, kGSBytes, &full[st]);
+    bulk_g2s(dst + kGSBytes, rc + blk * kRotPageElems, kGRotBytes, &full[st]);
+    __threadfence_block();
+    *reinterpret_cast<volatile int*>(&issued[st]) = i / kGStages + 1;
   };
-  int n_issued = 0, n_done = 0;   // lane 0's view of this warp's copies
-  if (lane == 0)
-    for (; n_issued < min(kGStages, n_mine); ++n_issued) issue(n_issued);
+  if (threadIdx.x == 0)
+    for (int i = 0; i < min(kGStages, n_pages); ++i) issue(i);
 
   // Stage the 8 roped query heads (bf16) while the first pages are in flight.
   {
@@ -416,12 +422,29 @@ __global__ void __launch_bounds__(128, 1) decode_global_kernel(DecodeParams p) {
   auto step_off = [](int s16) -> uint32_t { return (uint32_t)((s16 >> 4) * 8192 + (s16 & 15) * 256); };
   const uint32_t q_lane = q_addr + (lane & 7) * kGRow + (lane >> 3) * 16;
 
-  for (int i = 0; i < n_mine; ++i) {
-    const int st = i % kGStages;
-    if (!mbar_wait(&my_bars[st], (i / kGStages) & 1, &abort_flag, p.err)) break;
-    n_done = i + 1;
-    uint8_t* page = my_stages + st * kGStageBytes;
-    const int key0 = (pg0 + warp + kGWarps * i) * kPage;
+  for (int i = warp; i < n_pages; i += kGWarps) {
+    const int st = i % kGStages, ph = i / kGStages;
+    if (ph > 0) {   // page i issued yet? (bounded)
+      bool ok = true;
+      const unsigned long long t0 = globaltimer();
+      while (*reinterpret_cast<volatile int*>(&issued[st]) <= ph) {
+        if (*reinterpret_cast<volatile int*>(&abort_flag)) {
+          ok = false;
+          break;
+        }
+        if (globaltimer() - t0 > kWaitLimitNs) {
+          abort_flag = 1;
+          set_error(p.err, kErrTimeout);
+          ok = false;
+          break;
+        }
+      }
+      if (!__all_sync(0xffffffffu, ok)) break;
+      __threadfence_block();
+    }
+    if (!mbar_wait(&full[st], ph & 1, &abort_flag, p.err)) break;
+    uint8_t* page = stage_base + st * kGStageBytes;
+    const int key0 = (pg0 + i) * kPage;
     if (key0 + kPage - 1 > k_end) {   // zero stale rows (NaN-safe V), then make them visible
       for (int idx = lane; idx < kPage * (kGD / 8); idx += 32) {
         const int r = idx / (kGD / 8), dg = idx % (kGD / 8);
@@ -507,20 +530,18 @@ __global__ void __launch_bounds__(128, 1) decode_global_kernel(DecodeParams p) {
       mma16816(o[mt], a0, a1, a2, a3, pb0, pb1);
     }
     __syncwarp();
-    if (lane == 0 && i + kGStages < n_mine) {
+    if (lane == 0 && i + kGStages < n_pages) {   // refill this stage with page i + 5
       fence_proxy_async();
       issue(i + kGStages);
-      n_issued = i + kGStages + 1;
     }
   }
-  // After a timeout, wait (bounded) for this warp's copies still in flight before leaving.
-  if (abort_flag && lane == 0) {
+  __syncthreads();
+  if (abort_flag && threadIdx.x == 0) {   // after a timeout: wait (bounded) for copies in flight
     const unsigned long long t0 = globaltimer();
-    for (int i = n_done; i < n_issued; ++i) {
-      while (!mbar_try_wait(smem_u32(&my_bars[i % kGStages]), (i / kGStages) & 1) &&
-             globaltimer() - t0 < kWaitLimitNs) {
-      }
-    }
+    for (int st = 0; st < kGStages; ++st)
+      if (issued[st] > 0)
+        while (!mbar_try_wait(smem_u32(&full[st]), (issued[st] - 1) & 1) && globaltimer() - t0 < kWaitLimitNs) {
+        }
   }
   __syncthreads();   // all stages consumed: reuse them for the warp merge
 
