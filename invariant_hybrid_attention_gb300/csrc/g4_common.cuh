@@ -190,18 +190,6 @@ G4_DEV uint32_t map_peer(uint32_t saddr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
   return r;
 }
-G4_DEV void st_peer_v4(uint32_t addr, float a, float b, float c, float d) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
-               : "memory");
-}
-// Asynchronous store of 16 bytes into another CTA's shared memory; its completion counts the
-// bytes on that CTA's mbarrier `peer_bar` (complete_tx), as a bulk copy does. No fence needed:
-// the receiver sees the data once it observes the barrier phase complete.
-G4_DEV void st_async_peer_v4(uint32_t addr, float a, float b, float c, float d, uint32_t peer_bar) {
-  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(addr),
-               "f"(a), "f"(b), "f"(c), "f"(d), "r"(peer_bar)
-               : "memory");
-}
 // Bulk copy of `bytes` from this CTA's shared memory into another CTA's (addresses 16-byte
 // aligned, size a multiple of 16); completion counts the bytes on the receiver's mbarrier.
 G4_DEV void bulk_s2peer(uint32_t dst_cluster, const void* src, uint32_t bytes, uint32_t peer_bar) {
@@ -228,23 +216,6 @@ G4_DEV bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// mbar_wait for barriers completed by the other CTA of the cluster (acquires its writes).
-G4_DEV bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort, uint32_t* err) {
-  const uint32_t a = smem_u32(bar);
-  if (mbar_try_wait_cluster(a, parity)) return true;
-  const unsigned long long t0 = globaltimer();
-  while (true) {
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait_cluster(a, parity)) return true;
-    if (abort && *abort) return false;
-    if (globaltimer() - t0 > kWaitLimitNs) {
-      if (abort) *abort = 1;
-      set_error(err, kErrTimeout);
-      return false;
-    }
-  }
-}
-
 // ---- bulk copies (TMA) -------------------------------------------------------------------------
 G4_DEV void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
@@ -254,14 +225,6 @@ G4_DEV void bulk_g2s(void* smem, const void* gmem, uint32_t bytes, uint64_t* bar
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
           smem_u32(smem)),
       "l"(gmem), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-
-G4_DEV void tma_load_2d(void* smem, const CUtensorMap* map, int x, int y, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
-      "[%4];" ::"r"(smem_u32(smem)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
 }
 

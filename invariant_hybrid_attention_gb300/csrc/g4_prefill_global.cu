@@ -65,10 +65,6 @@ static_assert(2 * kQChunk <= kStage, "Q dims 0-127 must fit in one ring stage");
 constexpr size_t kGlobalSmemBytes = sizeof(GlobalSmem) + 1024;
 static_assert(kGlobalSmemBytes <= 232448, "global prefill exceeds the 227 KB shared-memory limit");
 
-G4_DEV void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     prefill_global_kernel(const __grid_constant__ CUtensorMap tmap_q, PrefillParams p) {
   extern __shared__ uint8_t smem_raw[];
