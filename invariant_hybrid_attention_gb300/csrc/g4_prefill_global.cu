@@ -210,11 +210,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       __syncwarp();
       return true;
     };
-    bool ok = mbar_wait(&sm.q_ready, 0, abort_flag, p.err);
-    for (int j = 0; ok && j < n_tiles; ++j) {
+    // QK^T runs two tiles ahead of P.V: the softmax sends tile j+1's partial scores while it
+    // works on tile j, so S_{j+1} must be ready when tile j's softmax starts.
+    auto qk = [&](int j) -> bool {
       const int s = j % kNS;
-      if (!mbar_wait(&sm.full[s], (j / kNS) & 1, abort_flag, p.err)) break;
-      if (j >= kNSP && !mbar_wait(&sm.pv_done[j % kNSP], ((j - kNSP) / kNSP) & 1, abort_flag, p.err)) break;
+      if (!mbar_wait(&sm.full[s], (j / kNS) & 1, abort_flag, p.err)) return false;
+      // S buffer j % 3 last held P_{j-3}: reuse it once P_{j-3} V_{j-3} has completed.
+      if (j >= kNSP && !mbar_wait(&sm.pv_done[j % kNSP], ((j - kNSP) / kNSP) & 1, abort_flag, p.err)) return false;
       tc_fence_after();
       if (lane == 0) {
         const uint32_t sa = smem_u32(sm.st[s]);
@@ -234,11 +236,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mma_commit(&sm.s_full[j % kNSP]);
       }
       __syncwarp();
-      if (j >= 1 && !pv(j - 1)) {
-        ok = false;
-        break;
-      }
-      if (j == n_tiles - 1 && !pv(j)) ok = false;
+      return true;
+    };
+    bool ok = mbar_wait(&sm.q_ready, 0, abort_flag, p.err);
+    for (int j = 0; ok && j < 2 && j < n_tiles; ++j) ok = qk(j);
+    for (int i = 0; ok && i < n_tiles; ++i) {
+      if (!pv(i) || (i + 2 < n_tiles && !qk(i + 2))) ok = false;
     }
   } else {
     // ------------------------------------------------------------ softmax / epilogue warps
@@ -279,56 +282,73 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_arrive_expect_tx(&sm.xfull[0], kXBytes);
       if (n_tiles > 1) mbar_arrive_expect_tx(&sm.xfull[1], kXBytes);
     }
+    // Exchange of partial scores, one tile ahead of the softmax. The peer's tile j lands in
+    // xbuf[j & 1]; this CTA's own tile j is staged in xbuf[(j + 1) & 1] and sent from there.
+    // Iteration j: wait for the peer's tile j, read this warp's rows of it into registers,
+    // stage and send own tile j+1 from the buffer just read, then run tile j's softmax while
+    // that copy is in flight. Reuse is safe without a separate free signal: the peer sends its
+    // tile j+2 into xbuf[j & 1] only after it has received all of this CTA's tile j+1, whose
+    // copy read that buffer, and this CTA read the peer's tile j from it before staging.
+    auto send_own = [&](int jt) -> bool {   // stage own tile jt and copy it into the peer
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.s_full[jt % kNSP], (jt / kNSP) & 1, abort_flag, p.err)))
+        return false;
+      tc_fence_after();
+      uint32_t sr[64];
+      tmem_ld32(tq + kTmS + 64 * (jt % kNSP), *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+      tmem_ld32(tq + kTmS + 64 * (jt % kNSP) + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+      tmem_ld_wait();
+      const int sp = (jt + 1) & 1;
+      float4* stg = reinterpret_cast<float4*>(&sm.xbuf[sp][r][0]);
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        stg[c ^ rsw] = make_float4(__uint_as_float(sr[4 * c]), __uint_as_float(sr[4 * c + 1]),
+                                   __uint_as_float(sr[4 * c + 2]), __uint_as_float(sr[4 * c + 3]));
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0)
+        bulk_s2peer(peer_xbuf + (jt & 1) * kXBytes, reinterpret_cast<const uint8_t*>(&sm.xbuf[sp][0][0]) + xrows,
+                    kXWarpBytes, peer_xfull + (jt & 1) * 8);
+      return true;
+    };
+
     const float cl2 = p.scale_log2;
     float m_used = -INFINITY, l_run = 0.f;
-    bool ok = true;
-    for (int j = 0; j < n_tiles; ++j) {
+    bool ok = n_tiles > 0 && send_own(0);
+    for (int j = 0; ok && j < n_tiles; ++j) {
       const int kb = j * kBN;
       const int sb = j % kNSP;
       const int par = j & 1;
       // Waits are made warp-uniform so that every lane leaves the loop together on an abort.
-      if (!__all_sync(0xffffffffu, mbar_wait(&sm.s_full[sb], (j / kNSP) & 1, abort_flag, p.err))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      uint32_t sr[64];
-      tmem_ld32(tq + kTmS + 64 * sb, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-      tmem_ld32(tq + kTmS + 64 * sb + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-      tmem_ld_wait();
-
-      // Partial scores over this CTA's 256 dims go to the peer; the peer's come back. Both
-      // CTAs then hold own + peer, the same sum in either order. The own tile is staged in
-      // xbuf[par ^ 1]: this CTA read the peer's tile j-1 from there last iteration, and the
-      // peer's tile j+1 cannot land there before this copy has completed (the peer sends it
-      // only after it has received all of tile j).
-      {
-        float4* stg = reinterpret_cast<float4*>(&sm.xbuf[par ^ 1][r][0]);
-#pragma unroll
-        for (int c = 0; c < 16; ++c)
-          stg[c ^ rsw] = make_float4(__uint_as_float(sr[4 * c]), __uint_as_float(sr[4 * c + 1]),
-                                     __uint_as_float(sr[4 * c + 2]), __uint_as_float(sr[4 * c + 3]));
-        fence_proxy_async();
-        __syncwarp();
-        if (lane == 0)
-          bulk_s2peer(peer_xbuf + par * kXBytes, reinterpret_cast<const uint8_t*>(&sm.xbuf[par ^ 1][0][0]) + xrows,
-                      kXWarpBytes, peer_xfull + par * 8);
-      }
       if (!__all_sync(0xffffffffu, mbar_wait(&sm.xfull[par], (j >> 1) & 1, abort_flag, p.err))) {
         ok = false;
         break;
       }
-      float s[64];
-      const float4* xr = reinterpret_cast<const float4*>(&sm.xbuf[par][r][0]);
-#pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const float4 o = xr[c ^ rsw];
-        s[4 * c] = __uint_as_float(sr[4 * c]) + o.x;
-        s[4 * c + 1] = __uint_as_float(sr[4 * c + 1]) + o.y;
-        s[4 * c + 2] = __uint_as_float(sr[4 * c + 2]) + o.z;
-        s[4 * c + 3] = __uint_as_float(sr[4 * c + 3]) + o.w;
-      }
       if (j + 2 < n_tiles && threadIdx.x == 64) mbar_arrive_expect_tx(&sm.xfull[par], kXBytes);   // the peer's tile j+2
+      float pe[64];
+      {
+        const float4* xr = reinterpret_cast<const float4*>(&sm.xbuf[par][r][0]);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const float4 o = xr[c ^ rsw];
+          pe[4 * c] = o.x;
+          pe[4 * c + 1] = o.y;
+          pe[4 * c + 2] = o.z;
+          pe[4 * c + 3] = o.w;
+        }
+      }
+      if (j + 1 < n_tiles && !send_own(j + 1)) {
+        ok = false;
+        break;
+      }
+      // S of tile j: own partial (still in its tensor-memory buffer) + the peer's, the same sum
+      // in either CTA.
+      uint32_t sr[64];
+      tmem_ld32(tq + kTmS + 64 * sb, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+      tmem_ld32(tq + kTmS + 64 * sb + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+      tmem_ld_wait();
+      float s[64];
+#pragma unroll
+      for (int c = 0; c < 64; ++c) s[c] = __uint_as_float(sr[c]) + pe[c];
 
       if (!(row_ok && kb + kBN - 1 <= pos)) {   // causal mask (and rows outside the sequence)
 #pragma unroll
