@@ -7,9 +7,10 @@
 // runs on a cluster of two CTAs, each owning half of the head dims (rank r: dims 256r ..
 // 256r+255):
 //   - S_r = Q[:, half r] . K[:, half r]^T on the CTA's tensor cores; the two partial score
-//     tiles are exchanged through distributed shared memory (each warp stages its 32 rows and
-//     one bulk copy carries them to the peer) and both CTAs add them (IEEE addition commutes,
-//     so both hold the same S bits) and run the same softmax;
+//     tiles are exchanged through distributed shared memory in 32-key halves (each warp stages
+//     its 32 rows of a half and one bulk copy carries them to the peer), one half ahead of the
+//     softmax, and both CTAs add them (IEEE addition commutes, so both hold the same S bits)
+//     and run the same softmax;
 //   - O[:, half r] += P . V[:, half r], V being the CTA's half of the un-rotated S tile: one
 //     copy of each stored half-page serves V and the un-rotated 3/4 of K;
 //   - the rotated quarter of K comes from the cache's k_rot side pages (p-RoPE(S), written
@@ -18,7 +19,7 @@
 // tiles are aligned to absolute position (section 4 rules 2, 3 and 6).
 //
 // Per CTA: warp 0 copies (roped Q tile by TMA; per key tile one 8 KB S half-page and one 2 KB
-// rotated half-page per page, 3-stage ring), warp 1 issues the MMAs, warps 2-5 run the
+// rotated half-page per page, 4-stage ring), warp 1 issues the MMAs, warps 2-5 run the
 // exchange, mask, online softmax, P (bf16, into tensor memory) and the epilogue.
 // Tensor memory: O half [0,256), Q dims 0-127 of the half [256,320), three S/P buffers [320,512).
 #include <math.h>
@@ -33,7 +34,8 @@ using namespace pf;
 
 constexpr int kGD = kGlobalD;                          // 512
 constexpr int kHalf = kGD / 2;                         // dims per CTA
-constexpr int kNS = 3;                                 // key-tile ring stages
+constexpr int kNS = 4;                                 // key-tile ring stages
+constexpr int kXCols = kBN / 2;                        // partial scores cross the pair in 32-key halves
 constexpr int kNSP = 3;                                // S/P buffers
 constexpr int kHalfPageBytes = kPage * kHalf * 2;      // 8 KB
 constexpr int kRotHalfPageBytes = kPage * kGlobalR * 2;   // 2 KB
@@ -51,8 +53,8 @@ struct GlobalSmem {
   uint8_t st[kNS][kStage];          // S half tile (V; K outside the rotated columns), rotated tile;
                                     // st[2] first holds Q dims 0-127 of the half
   uint8_t qhi[2 * kQChunk];         // Q dims 128-255 of the half (128B swizzle): an A operand
-  float xbuf[2][kBM][kBN];          // partial scores: the peer's tile j lands in xbuf[j & 1]; this
-                                    // CTA's own tile j is staged in xbuf[(j + 1) & 1] for the copy out
+  float xbuf[2][kBM][kXCols];       // partial scores by 32-key half h: the peer's half h lands in
+                                    // xbuf[h & 1]; this CTA's own half h is staged in xbuf[(h + 1) & 1]
   uint64_t full[kNS], empty[kNS];
   uint64_t s_full[kNSP], p_full[kNSP], pv_done[kNSP];
   uint64_t xfull[2];
@@ -273,116 +275,136 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_arrive(&sm.q_ready);
     }
 
-    constexpr uint32_t kXBytes = kBM * kBN * 4;   // one partial score tile
-    constexpr uint32_t kXWarpBytes = 32 * kBN * 4;   // the 32 rows of one warp
+    constexpr uint32_t kXBytes = kBM * kXCols * 4;      // one 32-key half of a partial score tile
+    constexpr uint32_t kXWarpBytes = 32 * kXCols * 4;   // the 32 rows of one warp
     const uint32_t xrows = (uint32_t)(warp & 3) * kXWarpBytes;
     const uint32_t peer_xbuf = map_peer(smem_u32(&sm.xbuf[0][0][0]), peer) + xrows;
     const uint32_t peer_xfull = map_peer(smem_u32(&sm.xfull[0]), peer);
-    if (threadIdx.x == 64) {   // expect the peer's first two tiles
+    const int n_halves = 2 * n_tiles;
+    if (threadIdx.x == 64) {   // expect the peer's first two halves
       mbar_arrive_expect_tx(&sm.xfull[0], kXBytes);
-      if (n_tiles > 1) mbar_arrive_expect_tx(&sm.xfull[1], kXBytes);
+      mbar_arrive_expect_tx(&sm.xfull[1], kXBytes);
     }
-    // Exchange of partial scores, one tile ahead of the softmax. The peer's tile j lands in
-    // xbuf[j & 1]; this CTA's own tile j is staged in xbuf[(j + 1) & 1] and sent from there.
-    // Iteration j: wait for the peer's tile j, read this warp's rows of it into registers,
-    // stage and send own tile j+1 from the buffer just read, then run tile j's softmax while
-    // that copy is in flight. Reuse is safe without a separate free signal: the peer sends its
-    // tile j+2 into xbuf[j & 1] only after it has received all of this CTA's tile j+1, whose
-    // copy read that buffer, and this CTA read the peer's tile j from it before staging.
-    auto send_own = [&](int jt) -> bool {   // stage own tile jt and copy it into the peer
-      if (!__all_sync(0xffffffffu, mbar_wait(&sm.s_full[jt % kNSP], (jt / kNSP) & 1, abort_flag, p.err)))
+    // Exchange of partial scores in 32-key halves h = 2j + e (tile j, columns 32e..32e+31), one
+    // half ahead of the softmax. The peer's half h lands in xbuf[h & 1]; this CTA's own half h is
+    // staged in xbuf[(h + 1) & 1] and sent from there. Step h: wait for the peer's half h, read
+    // this warp's rows of it into registers, stage and send own half h+1 from the buffer just
+    // read, then run half h's softmax while that copy is in flight. Reuse is safe without a
+    // separate free signal: the peer sends its half h+2 into xbuf[h & 1] only after it has
+    // received all of this CTA's half h+1, whose copy read that buffer, and this CTA read the
+    // peer's half h from it before staging.
+    auto send_half = [&](int hh) -> bool {   // stage own half hh and copy it into the peer
+      const int jt = hh >> 1, eh = hh & 1;
+      if (eh == 0 &&
+          !__all_sync(0xffffffffu, mbar_wait(&sm.s_full[jt % kNSP], (jt / kNSP) & 1, abort_flag, p.err)))
         return false;
       tc_fence_after();
-      uint32_t sr[64];
-      tmem_ld32(tq + kTmS + 64 * (jt % kNSP), *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-      tmem_ld32(tq + kTmS + 64 * (jt % kNSP) + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+      uint32_t sr[32];
+      tmem_ld32(tq + kTmS + 64 * (jt % kNSP) + kXCols * eh, sr);
       tmem_ld_wait();
-      const int sp = (jt + 1) & 1;
+      const int sp = (hh + 1) & 1;
       float4* stg = reinterpret_cast<float4*>(&sm.xbuf[sp][r][0]);
 #pragma unroll
-      for (int c = 0; c < 16; ++c)
+      for (int c = 0; c < kXCols / 4; ++c)
         stg[c ^ rsw] = make_float4(__uint_as_float(sr[4 * c]), __uint_as_float(sr[4 * c + 1]),
                                    __uint_as_float(sr[4 * c + 2]), __uint_as_float(sr[4 * c + 3]));
       fence_proxy_async();
       __syncwarp();
       if (lane == 0)
-        bulk_s2peer(peer_xbuf + (jt & 1) * kXBytes, reinterpret_cast<const uint8_t*>(&sm.xbuf[sp][0][0]) + xrows,
-                    kXWarpBytes, peer_xfull + (jt & 1) * 8);
+        bulk_s2peer(peer_xbuf + (hh & 1) * kXBytes, reinterpret_cast<const uint8_t*>(&sm.xbuf[sp][0][0]) + xrows,
+                    kXWarpBytes, peer_xfull + (hh & 1) * 8);
       return true;
     };
 
     const float cl2 = p.scale_log2;
     float m_used = -INFINITY, l_run = 0.f;
-    bool ok = n_tiles > 0 && send_own(0);
+    bool ok = n_tiles > 0 && send_half(0);
     for (int j = 0; ok && j < n_tiles; ++j) {
-      const int kb = j * kBN;
       const int sb = j % kNSP;
-      const int par = j & 1;
-      // Waits are made warp-uniform so that every lane leaves the loop together on an abort.
-      if (!__all_sync(0xffffffffu, mbar_wait(&sm.xfull[par], (j >> 1) & 1, abort_flag, p.err))) {
-        ok = false;
-        break;
-      }
-      if (j + 2 < n_tiles && threadIdx.x == 64) mbar_arrive_expect_tx(&sm.xfull[par], kXBytes);   // the peer's tile j+2
-      float pe[64];
-      {
-        const float4* xr = reinterpret_cast<const float4*>(&sm.xbuf[par][r][0]);
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const float4 o = xr[c ^ rsw];
-          pe[4 * c] = o.x;
-          pe[4 * c + 1] = o.y;
-          pe[4 * c + 2] = o.z;
-          pe[4 * c + 3] = o.w;
-        }
-      }
-      if (j + 1 < n_tiles && !send_own(j + 1)) {
-        ok = false;
-        break;
-      }
-      // S of tile j: own partial (still in its tensor-memory buffer) + the peer's, the same sum
-      // in either CTA.
-      uint32_t sr[64];
-      tmem_ld32(tq + kTmS + 64 * sb, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-      tmem_ld32(tq + kTmS + 64 * sb + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-      tmem_ld_wait();
-      float s[64];
-#pragma unroll
-      for (int c = 0; c < 64; ++c) s[c] = __uint_as_float(sr[c]) + pe[c];
-
-      if (!(row_ok && kb + kBN - 1 <= pos)) {   // causal mask (and rows outside the sequence)
-#pragma unroll
-        for (int c = 0; c < 64; ++c) s[c] = (row_ok && kb + c <= pos) ? s[c] : -INFINITY;
-      }
-      float mx[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        mx[i] = s[i];
-#pragma unroll
-        for (int c = 1; c < 8; ++c) mx[i] = fmaxf(mx[i], s[i + 8 * c]);
-      }
-      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * cl2;
-      float alpha = 1.f;
+      float alpha_t = 1.f;   // O rescale owed for this tile (product over its halves)
       bool need_o = false;
-      if (mt > m_used + kLazyRescale) {
-        need_o = (m_used != -INFINITY);
-        alpha = ex2(m_used - mt);
-        m_used = mt;
-      }
-      const float neg_m = (m_used == -INFINITY) ? 0.f : -m_used;
-      uint32_t pw[32];
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+      for (int e = 0; e < 2; ++e) {
+        const int hh = 2 * j + e;
+        const int par = hh & 1;
+        const int kb = j * kBN + kXCols * e;   // first key of this half
+        // Waits are made warp-uniform so that every lane leaves the loop together on an abort.
+        if (!__all_sync(0xffffffffu, mbar_wait(&sm.xfull[par], (hh >> 1) & 1, abort_flag, p.err))) {
+          ok = false;
+          break;
+        }
+        if (hh + 2 < n_halves && threadIdx.x == 64) mbar_arrive_expect_tx(&sm.xfull[par], kXBytes);   // half h+2
+        float pe[kXCols];
+        {
+          const float4* xr = reinterpret_cast<const float4*>(&sm.xbuf[par][r][0]);
 #pragma unroll
-      for (int w = 0; w < 32; ++w) {
-        const float e0 = ex2(fmaf(s[2 * w], cl2, neg_m));
-        const float e1 = ex2(fmaf(s[2 * w + 1], cl2, neg_m));
-        ls[w & 3] += e0;
-        ls[w & 3] += e1;
-        pw[w] = pack_bf16(e0, e1);   // declared cast: P in bf16 for P.V
+          for (int c = 0; c < kXCols / 4; ++c) {
+            const float4 o = xr[c ^ rsw];
+            pe[4 * c] = o.x;
+            pe[4 * c + 1] = o.y;
+            pe[4 * c + 2] = o.z;
+            pe[4 * c + 3] = o.w;
+          }
+        }
+        if (hh + 1 < n_halves && !send_half(hh + 1)) {
+          ok = false;
+          break;
+        }
+        // S of this half: own partial (still in its tensor-memory buffer) + the peer's, the same
+        // sum in either CTA.
+        uint32_t sr[kXCols];
+        tmem_ld32(tq + kTmS + 64 * sb + kXCols * e, sr);
+        tmem_ld_wait();
+        float s[kXCols];
+#pragma unroll
+        for (int c = 0; c < kXCols; ++c) s[c] = __uint_as_float(sr[c]) + pe[c];
+        if (!(row_ok && kb + kXCols - 1 <= pos)) {   // causal mask (and rows outside the sequence)
+#pragma unroll
+          for (int c = 0; c < kXCols; ++c) s[c] = (row_ok && kb + c <= pos) ? s[c] : -INFINITY;
+        }
+        float mx[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = fmaxf(fmaxf(s[i], s[i + 8]), fmaxf(s[i + 16], s[i + 24]));
+        const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * cl2;
+        float alpha = 1.f;
+        bool raised = false;
+        if (mt > m_used + kLazyRescale) {
+          need_o = need_o || (m_used != -INFINITY);
+          alpha = ex2(m_used - mt);
+          m_used = mt;
+          raised = true;
+        }
+        // The tile's first half of P was written against the old reference: rescale it too, so
+        // that P_j V_j sees one reference per row.
+        if (e == 1 && __any_sync(0xffffffffu, raised)) {
+          uint32_t pw0[16];
+          tmem_st_wait();   // the first half's own store has landed
+          tmem_ld16(tq + kTmS + 64 * sb, pw0);
+          tmem_ld_wait();
+          const float a = raised ? alpha : 1.f;
+#pragma unroll
+          for (int w = 0; w < 16; ++w) pw0[w] = pack_bf16(bf16_lo(pw0[w]) * a, bf16_hi(pw0[w]) * a);
+          tmem_st16(tq + kTmS + 64 * sb, pw0);
+        }
+        const float neg_m = (m_used == -INFINITY) ? 0.f : -m_used;
+        uint32_t pw[16];
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int w = 0; w < 16; ++w) {
+          const float e0 = ex2(fmaf(s[2 * w], cl2, neg_m));
+          const float e1 = ex2(fmaf(s[2 * w + 1], cl2, neg_m));
+          ls[w & 3] += e0;
+          ls[w & 3] += e1;
+          pw[w] = pack_bf16(e0, e1);   // declared cast: P in bf16 for P.V
+        }
+        l_run = fmaf(l_run, alpha, (ls[0] + ls[1]) + (ls[2] + ls[3]));
+        alpha_t *= alpha;
+        // P of this half (bf16 key pairs) over columns 16e.. of the tile's S buffer, whose S
+        // values there are already consumed: the A operand of P.V.
+        tmem_st16(tq + kTmS + 64 * sb + 16 * e, pw);
       }
-      l_run = fmaf(l_run, alpha, (ls[0] + ls[1]) + (ls[2] + ls[3]));
-      tmem_st32(tq + kTmS + 64 * sb, pw);
+      if (!ok) break;
 
       if (__any_sync(0xffffffffu, need_o)) {   // O correction after P_{j-1} V_{j-1} landed
         if (!__all_sync(0xffffffffu, mbar_wait(&sm.pv_done[(j - 1) % kNSP], ((j - 1) / kNSP) & 1, abort_flag, p.err))) {
@@ -390,7 +412,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        const float a = need_o ? alpha : 1.f;
+        const float a = need_o ? alpha_t : 1.f;
 #pragma unroll 1
         for (int cc = 0; cc < kHalf / 32; ++cc) {
           uint32_t o[32];
