@@ -44,7 +44,10 @@
  *                    sliding (D 256): [j/8][d/8][j%8][d%8]            = [2][32][8][8]
  *                    global  (D 512): [d/256][j/8][(d%256)/8][j%8][d%8] = [2][2][32][8][8]
  *                  sliding K' (roped) or global S (un-rotated, K==V)
- *   cache->v       sliding: V, same layout as k; global: NULL
+ *   cache->v       sliding: V, 16 keys x 256 dims per (page, KV head) at the same place as k's
+ *                  block, stored as two contiguous 128-dim halves of 8x8 core matrices:
+ *                    [d/128][j/8][(d%128)/8][j%8][d%8]                 = [2][2][16][8][8]
+ *                  global: NULL
  *   cache->k_rot   global only (NULL on sliding layers): p-RoPE(S) on the 128 rotated
  *                  columns d in [0,64) U [256,320), 2048 bf16 per (page, KV head) at
  *                  k_rot + (page*4 + head)*2048, as [d/256][j/8][(d%64)/8][j%8][d%8].

@@ -48,6 +48,14 @@ __host__ __device__ constexpr int tiled_offset(int j, int d, int D) {
                   : (((j >> 3) * (D >> 3) + (d >> 3)) * 64 + (j & 7) * 8 + (d & 7));
 }
 
+// Sliding V pages are stored as two contiguous 128-dim halves (4 KB each) of the same 8x8 core
+// matrices, so that each CTA of a prefill pair (one per half of the head dims) copies its half
+// of a page with one bulk copy: key j, dim d at
+//   (((d / 128) * 2 + j / 8) * 16 + (d % 128) / 8) * 64 + (j % 8) * 8 + d % 8.
+__host__ __device__ constexpr int tiled_offset_v256(int j, int d) {
+  return ((((d >> 7) * 2 + (j >> 3)) * 16 + ((d & 127) >> 3)) * 64 + (j & 7) * 8 + (d & 7));
+}
+
 // Rotated-column side pages of a global (K==V) cache: p-RoPE(S) on the 128 rotated dims
 // d in [0, 64) U [256, 320), the only columns where K differs from the stored S. Key j, dim d
 // sits at element (((d / 256) * 2 + j / 8) * 8 + (d % 64) / 8) * 64 + (j % 8) * 8 + d % 8 of a
@@ -205,6 +213,14 @@ G4_DEV void st_peer_u32(uint32_t addr, uint32_t v) {
 G4_DEV void mbar_arrive_peer(uint32_t peer_bar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(peer_bar) : "memory");
 }
+// Arrive on an mbarrier of another CTA of the cluster with the default (CTA-scope) release. About
+// four times faster than the cluster-scope release above; for signals whose data is already
+// complete when the arrive issues: registers read back (tcgen05.wait::ld), tensor-memory stores
+// finished (tcgen05.wait::st), generic writes fenced to the async proxy, or copies observed
+// complete. The waiter acquires at cluster scope.
+G4_DEV void mbar_arrive_remote(uint32_t peer_bar) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(peer_bar) : "memory");
+}
 G4_DEV bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -216,6 +232,24 @@ G4_DEV bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// mbar_wait for barriers that the other CTA of the cluster arrives on: acquires their writes at
+// cluster scope. Bounded like mbar_wait.
+G4_DEV bool mbar_wait_cl(uint64_t* bar, uint32_t parity, volatile int* abort, uint32_t* err) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait_cluster(a, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  while (true) {
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait_cluster(a, parity)) return true;
+    if (abort && *abort) return false;
+    if (globaltimer() - t0 > kWaitLimitNs) {
+      if (abort) *abort = 1;
+      set_error(err, kErrTimeout);
+      return false;
+    }
+  }
+}
+
 // ---- bulk copies (TMA) -------------------------------------------------------------------------
 G4_DEV void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
@@ -311,6 +345,42 @@ G4_DEV void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t i
 G4_DEV void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    smem_u32(bar))
+               : "memory");
+}
+
+// ---- 2-SM forms: the two CTAs of a cluster pair act as one MMA unit ----------------------------
+// Allocation, relinquish and deallocation with cta_group::2 are collective: one warp of each CTA
+// issues them and both CTAs get the same columns. An MMA is issued by the even CTA only: A and D
+// are split by rows (each CTA holds its 128 rows of an M = 256 tile), B by columns (each CTA
+// holds N/2 of the N columns, at the same shared-memory offset); the instruction descriptor
+// carries M = 256 and the full N.
+G4_DEV void tmem_alloc2(uint32_t* dst_smem, uint32_t ncols) {   // whole warp, in both CTAs
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+}
+G4_DEV void tmem_relinquish2() { asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory"); }
+G4_DEV void tmem_dealloc2(uint32_t taddr, uint32_t ncols) {   // whole warp, in both CTAs
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+G4_DEV void mma2_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
+}
+G4_DEV void mma2_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate));
+}
+// Commit of the pair's MMAs issued so far by this thread: arrives on the mbarrier at `bar`'s
+// offset in every CTA of `cta_mask`.
+G4_DEV void mma2_commit_mc(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                   smem_u32(bar)),
+               "h"(cta_mask)
                : "memory");
 }
 

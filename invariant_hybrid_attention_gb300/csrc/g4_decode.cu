@@ -149,11 +149,13 @@ __global__ void __launch_bounds__(128, 2) decode_sliding_kernel(DecodeParams p) 
 #pragma unroll
   for (int mt = 0; mt < 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
   float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-  // ldmatrix lane addresses in a tiled block [key group kg][dim group dg][8 keys][8 dims]
-  // (core matrices of 128 B at (kg * 32 + dg) * 128): K as A takes tiles (keys 0-7 | 8-15) x
-  // (dims +0 | +8); V^T as A (transposed) takes tiles (dims +0 | +8) x (keys 0-7 | 8-15).
+  // ldmatrix lane addresses. K block [key group kg][dim group dg][8 keys][8 dims] (core matrices
+  // of 128 B at (kg * 32 + dg) * 128): K as A takes tiles (keys 0-7 | 8-15) x (dims +0 | +8).
+  // V block in 128-dim halves [half][kg][dg 0-15][8][8] (core matrix (kg, dg) at
+  // ((dg / 16 * 2 + kg) * 16 + dg % 16) * 128): V^T as A (transposed) takes tiles (dims +0 | +8) x
+  // (keys 0-7 | 8-15); dim tile mt starts at (mt / 8) * 4096 + (mt % 8) * 256.
   const uint32_t a_lane = (((lane >> 3) & 1) * 32 + (lane >> 4)) * 128 + (lane & 7) * 16;
-  const uint32_t v_lane = (((lane >> 4) & 1) * 32 + ((lane >> 3) & 1)) * 128 + (lane & 7) * 16;
+  const uint32_t v_lane = (((lane >> 4) & 1) * 16 + ((lane >> 3) & 1)) * 128 + (lane & 7) * 16;
 
   for (int i = warp; i < n_pages; i += 4) {
     const int st = i % kSStages, ph = i / kSStages;
@@ -183,7 +185,8 @@ __global__ void __launch_bounds__(128, 2) decode_sliding_kernel(DecodeParams p) 
       for (int idx = lane; idx < kPage * (kSD / 8); idx += 32) {
         const int r = idx / (kSD / 8), dg = idx % (kSD / 8);
         if (key0 + r < k_begin || key0 + r > k_end)
-          *reinterpret_cast<uint4*>(vp + ((r >> 3) * 32 + dg) * 128 + (r & 7) * 16) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(vp + (((dg >> 4) * 2 + (r >> 3)) * 16 + (dg & 15)) * 128 + (r & 7) * 16) =
+              make_uint4(0, 0, 0, 0);
       }
       __syncwarp();
     }
@@ -247,7 +250,7 @@ __global__ void __launch_bounds__(128, 2) decode_sliding_kernel(DecodeParams p) 
 #pragma unroll
     for (int mt = 0; mt < 16; ++mt) {
       uint32_t a0, a1, a2, a3;
-      ldsm_x4_t(va + v_lane + mt * 256, a0, a1, a2, a3);
+      ldsm_x4_t(va + v_lane + (mt >> 3) * 4096 + (mt & 7) * 256, a0, a1, a2, a3);
       mma16816(o[mt], a0, a1, a2, a3, pb0, pb1);
     }
     __syncwarp();

@@ -1,30 +1,40 @@
-// Prefill attention on the 5th-generation tensor cores (tcgen05, accumulators in tensor memory).
+// Sliding-layer prefill on the 5th-generation tensor cores (tcgen05, accumulators in tensor
+// memory), one 2-SM MMA unit per pair of query heads.
 //
-// Work unit: (sequence, query tile of 128 positions aligned to absolute position, query head).
-// Key tiles of 64 keys are aligned to absolute key 0 and visited in ascending order, so the
-// arithmetic a row gets depends only on its own position, its sequence's keys and the window:
-// not on the batch, the row's place in it, padding, packing or the launch grid (RL-Kernel RFC
-// "[RFC][Gemma-4-31B-it] WS1/WS2 kernel roadmap", section 4 rules 2, 3 and 6).
+// Sliding layer (RL-Kernel RFC "[RFC][Gemma-4-31B-it] WS1/WS2 kernel roadmap", section 5,
+// sliding_attention_core: causal local attention, window 1024, 32 Q / 16 KV heads, D 256).
+// Work unit: (sequence, query tile of 128 positions aligned to absolute position, KV head g)
+// on a cluster of two CTAs; CTA rank r owns query head 2g + r, i.e. the two query heads that
+// share K and V. Key tiles of 128 keys are aligned to absolute key 0 and visited in ascending
+// order, so the arithmetic a row gets depends only on its own position, its sequence's keys and
+// the window: not on the batch, the row's place in it, padding, packing or the launch grid. A
+// key tile that holds no visible key for a row adds exact zeros to it (RFC section 4 rules 2,
+// 3 and 6).
 //
-// Sliding layer (RFC section 5, sliding_attention_core: causal local attention, window 1024,
-// 32 Q / 16 KV heads, D 256). Per CTA:
-//   warps 0, 6  copy producers (Q and K; V): the roped Q tile by TMA, then one bulk copy per
-//           tiled page-head block (8 KB: 16 keys x 256 dims as 8x8 core matrices) into a
-//           3-stage ring; pages outside the needed key range are never looked up nor copied;
-//   warp 1  MMA issuer: S = Q K^T with Q in tensor memory and K (K-major, no swizzle) in shared
-//           memory, O += P V with P in tensor memory and V (MN-major, no swizzle) in shared
-//           memory; one elected lane issues, commits signal;
-//   warps 2-5  one thread per query row: per key tile the mask, the online softmax (lazy
-//           rescale, threshold 2^8), P (bf16) written over the tile's own S columns, the O
-//           correction when needed, and the epilogue O / l -> bf16.
+// Every tcgen05 MMA is one 2-SM operation (M = 256: the two heads' 128 rows each) issued by
+// the even CTA. A (queries, P) and D (S, O) are split by rows, so each CTA keeps its own head's
+// rows in its own tensor memory; B (K, V) is split by columns, so each CTA stages only half of
+// every key tile: keys 64r .. 64r+63 of K (all dims) and dims 128r .. 128r+127 of V (all 128
+// keys), 64 KB per tile instead of 128 KB. QK^T runs at N = 128 keys, P.V at N = 256 dims.
+// Per CTA:
+//   warp 0     the roped Q tile by TMA, then this CTA's K half of each key tile (four 8 KB
+//              page-head blocks) into a 3-stage ring;
+//   warp 6     this CTA's V half of each key tile (eight 4 KB copies: sliding V pages store each
+//              128-dim half of a page-head block contiguously) into a 3-stage ring;
+//   warp 1     even CTA: issues S = Q K^T and O += P V for the pair. Odd CTA: tells the even
+//              CTA when its K half of a tile has landed;
+//   warp 7     zeroes value rows of this CTA's V half that hold no key of the sequence, then
+//              tells the even CTA that the V half is ready;
+//   warps 2-5  one thread per query row of this CTA's head: mask, online softmax (lazy
+//              rescale, threshold 2^8), P (bf16), the O correction when needed, and the
+//              epilogue O / l -> bf16.
 // The queries arrive already roped: the cache-append pass before this kernel wrote
-// bf16(RoPE(q)) into the sequence rows of `out`; the producer's TMA loads the tile from there
-// (into ring stage 2, which the softmax threads then empty into tensor memory), and the
-// epilogue later overwrites exactly those rows (each row belongs to one CTA).
-// Tensor memory (512 columns): O [0,256), Q dims 0-127 [256,320) as bf16 pairs, three S buffers
-// [320,512) whose first 32 columns take P once the softmax has read S (three, so that QK^T of
-// tile j+1 never waits on P.V of tile j-1). Shared memory: the 3-stage K/V ring and Q dims
-// 128-255.
+// bf16(RoPE(q)) into the sequence rows of `out`; the epilogue later overwrites exactly those
+// rows (each row belongs to one CTA).
+// Tensor memory (512 columns, allocated jointly by the pair): O [0,256), Q dims 0-127 [256,320)
+// as bf16 pairs, P [320,384) as bf16 key pairs, S [384,512). With one S buffer, QK^T of tile
+// j+1 is issued as soon as both CTAs' softmax threads have read S_j into registers, so it runs
+// while they exponentiate; P has its own buffer, so it never waits for S to be consumed.
 #include <math.h>
 
 #include "g4_prefill_common.cuh"
@@ -35,43 +45,52 @@ namespace {
 
 using namespace pf;
 
-constexpr int kNS = 3;                    // K/V ring stages (stage 2 first holds the Q tile)
-constexpr int kSlidingThreads = 64 + kSoftmaxThreads + 32;   // + the V producer warp (warp 6)
-
-// ---------------------------------------------------------------- sliding layer geometry
-constexpr int kSD = kSlidingD;            // 256
+constexpr int kSD = kSlidingD;                    // 256
+constexpr int kSN = 128;                          // keys per tile
+constexpr int kNK = 3, kNV = 3;                   // K and V ring stages
+constexpr int kQStage = 2;                        // K stage that first holds Q dims 0-127
 constexpr int kPageBytes = kPage * kSD * 2;       // one tiled page-head block: 8 KB
-constexpr int kKeyGroupBytes = 8 * kSD * 2;       // 8 keys x all dims: 4 KB
-constexpr int kSKTile = (kBN / kPage) * kPageBytes;   // 32 KB: 4 pages, key groups 0..7
-
-constexpr int kNSP = 3;                   // S/P buffers in tensor memory
-constexpr uint32_t kTmO = 0, kTmQ = 256, kTmS = 320;   // column offsets: O, Q dims 0-127, S/P x3
-constexpr uint32_t kIdescQK = idesc_bf16(kBM, kBN, false, false);
-constexpr uint32_t kIdescPV = idesc_bf16(kBM, kSD, false, true);
+constexpr int kKeyGroupBytes = 8 * kSD * 2;       // K: 8 keys x 256 dims, 4 KB
+constexpr int kVGroupBytes = 8 * (kSD / 2) * 2;   // V half: 8 keys x 128 dims, 2 KB
+constexpr int kVHalfPageBytes = 2 * kVGroupBytes; // V half of one page-head block: 4 KB
+constexpr int kKStage = (kSN / 2 / kPage) * kPageBytes;   // 4 pages: 32 KB
+constexpr int kVStage = (kSN / 8) * kVGroupBytes;         // 16 key groups: 32 KB
+constexpr int kThreads = 256;
+constexpr uint32_t kTmO = 0, kTmQ = 256, kTmP = 320, kTmS = 384;
+constexpr uint32_t kIdescQK = idesc_bf16(2 * kBM, kSN, false, false);   // M 256 over the pair, N 128 keys
+constexpr uint32_t kIdescPV = idesc_bf16(2 * kBM, kSD, false, true);    // M 256, N 256 dims
+constexpr uint16_t kBoth = 0x3;
+constexpr uint32_t kPairWarps = 8;                // softmax warps of both CTAs
 
 struct SlidingSmem {
-  uint8_t st[kNS][2 * kSKTile];   // ring stage s: K tile, then V tile; st[2] first holds Q dims 0-127
-  uint8_t qhi[2 * kQChunk];       // Q dims 128-255 (128B swizzle), the shared-memory A operand
-  uint64_t k_full[kNS], k_empty[kNS], v_full[kNS], v_empty[kNS];
-  uint64_t s_full[kNSP], p_full[kNSP], pv_done[kNSP];
-  uint64_t q_full, q_ready, teardown;
+  uint8_t k[kNK][kKStage];          // K halves [8 key groups][32 dim groups][8][8]; k[2] first holds Q dims 0-127
+  uint8_t v[kNV][kVStage];          // V halves [16 key groups][16 dim groups][8][8]
+  uint8_t qhi[2 * kQChunk];         // Q dims 128-255 (128B swizzle), the shared-memory A operand
+  uint64_t k_full[kNK], k_empty[kNK], k_peer[kNK];
+  uint64_t v_full[kNV], v_empty[kNV], v_ready[kNV];
+  uint64_t s_full, s_free, p_full, pv_done;
+  uint64_t q_full, q_local, q_pair, teardown;
   uint32_t tmem_base;
   int abort_flag;
   int unit_b, unit_t;
 };
-static_assert(2 * kQChunk <= 2 * kSKTile, "Q dims 0-127 must fit in one ring stage");
+static_assert(2 * kQChunk <= kKStage, "Q dims 0-127 must fit in one K stage");
 constexpr size_t kSlidingSmemBytes = sizeof(SlidingSmem) + 1024;
 static_assert(kSlidingSmemBytes <= 232448, "sliding prefill exceeds the 227 KB shared-memory limit");
 
-__global__ void __launch_bounds__(kSlidingThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     prefill_sliding_kernel(const __grid_constant__ CUtensorMap tmap_q, PrefillParams p) {
   extern __shared__ uint8_t smem_raw[];
   SlidingSmem& sm =
       *reinterpret_cast<SlidingSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = blockIdx.x % kSlidingHq;
-  const int slot = blockIdx.x / kSlidingHq;
-  const int g = h / (kSlidingHq / kSlidingHkv);
+  const uint32_t rank = cluster_rank();   // which query head of the KV head's pair
+  const uint32_t peer = rank ^ 1u;
+  const bool leader = rank == 0;
+  const int unit = blockIdx.x >> 1;
+  const int g = unit % kSlidingHkv;
+  const int slot = unit / kSlidingHkv;
+  const int h = 2 * g + (int)rank;
 
   if (warp == 0) {
     int ub, ut;
@@ -82,167 +101,207 @@ __global__ void __launch_bounds__(kSlidingThreads, 1)
     }
   }
   __syncthreads();
-  const int b = sm.unit_b;
+  const int b = sm.unit_b;   // both CTAs of the pair find the same unit
   if (b < 0) return;
   const int t = sm.unit_t;
   const int cs = p.rows.ctx_start[b], L = p.rows.q_len[b], qs = p.rows.q_start[b];
   const int p_lo = max(kBM * t, cs), p_hi = min(kBM * t + kBM - 1, cs + L - 1);
   const int ctx_end = cs + L;
   if (p_hi >= kMaxPos || (p_hi >> 4) >= p.max_pages) {
-    if (threadIdx.x == 0 && h == 0) set_error(p.err, kErrPos);
+    if (threadIdx.x == 0 && g == 0 && leader) set_error(p.err, kErrPos);
     return;
   }
   const int W = p.window;
   const int k_lo = W > 0 ? max(0, p_lo - W + 1) : 0;
   const int k_hi = p_hi;
-  const int kt0 = k_lo / kBN;
-  const int n_tiles = k_hi / kBN - kt0 + 1;
+  const int kt0 = k_lo / kSN;
+  const int n_tiles = k_hi / kSN - kt0 + 1;
   const int q_row0 = qs + (kBM * t - cs);   // memory row of tile row 0 (may be negative)
   const int32_t* pt = p.page_table + (size_t)b * p.max_pages;
 
   if (threadIdx.x == 32) {
-    for (int s = 0; s < kNS; ++s) {
+    for (int s = 0; s < kNK; ++s) {
       mbar_init(&sm.k_full[s], 1);
-      mbar_init(&sm.k_empty[s], 1);
+      mbar_init(&sm.k_empty[s], 1);   // the even CTA's commits arrive in both CTAs
+      mbar_init(&sm.k_peer[s], 1);    // even CTA: the odd CTA's K half has landed
+    }
+    for (int s = 0; s < kNV; ++s) {
       mbar_init(&sm.v_full[s], 1);
       mbar_init(&sm.v_empty[s], 1);
+      mbar_init(&sm.v_ready[s], 2);   // even CTA: both V halves landed and checked
     }
-    for (int s = 0; s < kNSP; ++s) {
-      mbar_init(&sm.s_full[s], 1);
-      mbar_init(&sm.p_full[s], kSoftmaxThreads);
-      mbar_init(&sm.pv_done[s], 1);
-    }
+    mbar_init(&sm.s_full, 1);
+    mbar_init(&sm.s_free, kPairWarps);   // even CTA: both CTAs' softmax warps have read S
+    mbar_init(&sm.p_full, kPairWarps);   // even CTA: both CTAs' P is in tensor memory
+    mbar_init(&sm.pv_done, 1);
     mbar_init(&sm.q_full, 1);
-    mbar_init(&sm.q_ready, kSoftmaxThreads);
+    mbar_init(&sm.q_local, kSoftmaxThreads / 32);   // this CTA's Q dims 0-127 left the K stage
+    mbar_init(&sm.q_pair, kPairWarps);              // even CTA: both CTAs' Q is in tensor memory
     mbar_init(&sm.teardown, 1);
     sm.abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(&sm.tmem_base, 512);
-    tmem_relinquish();
+    tmem_alloc2(&sm.tmem_base, 512);
+    tmem_relinquish2();
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();   // both CTAs' barriers and tensor memory exist before any cross-CTA signal
   tc_fence_after();
   const uint32_t tm = sm.tmem_base;
   volatile int* abort_flag = &sm.abort_flag;
+  // Arrive on one of the even CTA's barriers: locally there, remotely from the odd CTA.
+  auto arrive_leader = [&](uint64_t* bar) {
+    if (leader)
+      mbar_arrive(bar);
+    else
+      mbar_arrive_remote(map_peer(smem_u32(bar), 0u));
+  };
 
   if (warp == 0 || warp == 6) {
     // ------------------------------------------------------------ copy producers
-    // Warp 0 loads the roped Q tile by TMA, then the K tiles; warp 6 loads the V tiles. Split
-    // so that K, needed a tile earlier, never queues behind the release of a V stage. One bulk
-    // copy per 8 KB tiled page-head block, lanes 0-3 one page each. Block indices come from the
-    // page table ahead of use: lane l holds page (l & 3) of tile (l >> 2) of the current group
-    // of 8 tiles, and the next group is looked up one group early.
+    // Block indices come from the page table ahead of use: lane l holds page (l & 7) of tile
+    // (l >> 3) of the current group of 4 tiles; the next group is looked up one group early.
+    // Warp 0 copies this CTA's K pages (4r .. 4r+3 of the tile's 8), lanes 0-3 one page each;
+    // warp 6 the dims half r of every page of the tile, lanes 0-7 one page each.
+    // Pages outside [k_lo, k_hi] are neither looked up nor copied.
     const bool is_v = (warp == 6);
     auto load_blocks = [&](int j0) -> int {
-      const int jt = j0 + (lane >> 2);
+      const int jt = j0 + (lane >> 3);
       if (jt >= n_tiles) return -1;
-      return page_block((kt0 + jt) * kBN + (lane & 3) * kPage, k_lo, k_hi, pt, p.num_pages, kSlidingHkv, g, p.err);
+      return page_block((kt0 + jt) * kSN + (lane & 7) * kPage, k_lo, k_hi, pt, p.num_pages, kSlidingHkv, g, p.err);
     };
     if (!is_v && lane == 0) {   // the roped Q tile: 4 boxes of 64 dims x 128 rows (rows outside T read as 0)
       prefetch_tmap(&tmap_q);
-      mbar_arrive_expect_tx(&sm.q_full, (kSlidingD / 64) * kQChunk);
+      mbar_arrive_expect_tx(&sm.q_full, (kSD / 64) * kQChunk);
 #pragma unroll
-      for (int c = 0; c < kSlidingD / 64; ++c)
-        tma_load_3d(c < 2 ? sm.st[2] + c * kQChunk : sm.qhi + (c - 2) * kQChunk, &tmap_q, 64 * c, h, q_row0, &sm.q_full);
+      for (int c = 0; c < kSD / 64; ++c)
+        tma_load_3d(c < 2 ? sm.k[kQStage] + c * kQChunk : sm.qhi + (c - 2) * kQChunk, &tmap_q, 64 * c, h, q_row0,
+                    &sm.q_full);
     }
-    int blk_cur = load_blocks(0), blk_next = load_blocks(8);
-    const __nv_bfloat16* src = (const __nv_bfloat16*)(is_v ? p.v_cache : p.k_cache);
+    int blk_cur = load_blocks(0), blk_next = load_blocks(4);
     uint64_t* full = is_v ? sm.v_full : sm.k_full;
     uint64_t* empty = is_v ? sm.v_empty : sm.k_empty;
-    const int half = is_v ? kSKTile : 0;
+    const int n_st = is_v ? kNV : kNK;
+    const bool mine = is_v ? lane < 8 : lane < 4;
+    const int pg = is_v ? (lane & 7) : (int)(4 * rank) + (lane & 3);   // page of the tile this lane copies
     int j = 0;
     for (; j < n_tiles; ++j) {
-      const int s = j % kNS;
-      if (j > 0 && (j & 7) == 0) {
+      const int s = j % n_st;
+      if (j > 0 && (j & 3) == 0) {
         blk_cur = blk_next;
-        blk_next = load_blocks(j + 8);
+        blk_next = load_blocks(j + 4);
       }
-      const int my_blk = __shfl_sync(0xffffffffu, blk_cur, (j & 7) * 4 + (lane & 3));
-      const unsigned live = __ballot_sync(0xffffffffu, lane < 4 && my_blk >= 0);
-      const uint32_t bytes = __popc(live) * kPageBytes;
-      bool ok = (j < kNS) || lane != 0 || mbar_wait(&empty[s], ((j / kNS) - 1) & 1, abort_flag, p.err);
-      if (j == 2 && lane == 0) ok = ok && mbar_wait(&sm.q_ready, 0, abort_flag, p.err);   // Q left stage 2
+      const int my_blk = __shfl_sync(0xffffffffu, blk_cur, (j & 3) * 8 + (pg & 7));
+      const unsigned live = __ballot_sync(0xffffffffu, mine && my_blk >= 0);
+      const uint32_t bytes = __popc(live) * (is_v ? kVHalfPageBytes : kPageBytes);
+      bool ok = true;
+      if (lane == 0) {
+        if (!is_v && j == kQStage) ok = mbar_wait(&sm.q_local, 0, abort_flag, p.err);   // Q left the stage
+        if (ok && j >= n_st) ok = mbar_wait(&empty[s], ((j / n_st) - 1) & 1, abort_flag, p.err);
+      }
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
       if (lane == 0) mbar_arrive_expect_tx(&full[s], bytes);
       __syncwarp();
-      if (lane < 4 && my_blk >= 0)
-        bulk_g2s(sm.st[s] + half + lane * kPageBytes, src + (size_t)my_blk * kPage * kSD, kPageBytes, &full[s]);
+      if (mine && my_blk >= 0) {
+        if (is_v)   // dims 128r .. 128r+127 of page pg: key groups 2pg, 2pg+1
+          bulk_g2s(sm.v[s] + pg * kVHalfPageBytes,
+                   (const __nv_bfloat16*)p.v_cache + (size_t)my_blk * kPage * kSD + rank * (kVHalfPageBytes / 2),
+                   kVHalfPageBytes, &full[s]);
+        else
+          bulk_g2s(sm.k[s] + (lane & 3) * kPageBytes, (const __nv_bfloat16*)p.k_cache + (size_t)my_blk * kPage * kSD,
+                   kPageBytes, &full[s]);
+      }
     }
     if (lane == 0 && *abort_flag) {   // drain copies still in flight (bounded) before the CTA may exit
-      const unsigned long long t0 = globaltimer();
+      const unsigned long long w0 = globaltimer();
       if (!is_v) {
-        while (!mbar_try_wait(smem_u32(&sm.q_full), 0) && globaltimer() - t0 < kWaitLimitNs) {
+        while (!mbar_try_wait(smem_u32(&sm.q_full), 0) && globaltimer() - w0 < kWaitLimitNs) {
         }
       }
-      for (int i = max(0, j - kNS); i < j; ++i) {
-        while (!mbar_try_wait(smem_u32(&full[i % kNS]), (i / kNS) & 1) && globaltimer() - t0 < kWaitLimitNs) {
+      for (int i = max(0, j - n_st); i < j; ++i) {
+        while (!mbar_try_wait(smem_u32(&full[i % n_st]), (i / n_st) & 1) && globaltimer() - w0 < kWaitLimitNs) {
         }
+      }
+    }
+  } else if (warp == 7) {
+    // ------------------------------------------------------------ V check (both CTAs)
+    // Value rows of this CTA's V half for keys that hold no data of this sequence are zeroed
+    // before P.V: pages outside the key range were not copied and keep an older tile, and slots
+    // past the sequence's last key may hold anything (NaN); P = 0 there does not cancel NaN.
+    for (int j = 0; j < n_tiles; ++j) {
+      const int s = j % kNV;
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.v_full[s], (j / kNV) & 1, abort_flag, p.err))) break;
+      const int kb = (kt0 + j) * kSN;
+      const int v0 = max(kb, (k_lo >> 4) * kPage), v1 = min(min(kb + kSN, ((k_hi >> 4) + 1) * kPage), ctx_end);
+      if (v0 > kb || v1 < kb + kSN) {
+        for (int idx = lane; idx < kSN * 16; idx += 32) {
+          const int r = idx >> 4, dg = idx & 15;
+          if (kb + r < v0 || kb + r >= v1)
+            *reinterpret_cast<uint4*>(sm.v[s] + ((r >> 3) * 16 + dg) * 128 + (r & 7) * 16) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async();
+      }
+      __syncwarp();
+      if (lane == 0) arrive_leader(&sm.v_ready[s]);
+    }
+  } else if (warp == 1 && !leader) {
+    // ------------------------------------------------------------ K relay (odd CTA)
+    if (lane == 0) {
+      for (int j = 0; j < n_tiles; ++j) {
+        const int s = j % kNK;
+        if (!mbar_wait(&sm.k_full[s], (j / kNK) & 1, abort_flag, p.err)) break;
+        mbar_arrive_remote(map_peer(smem_u32(&sm.k_peer[s]), peer));
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    auto pv = [&](int i) -> bool {
-      if (!mbar_wait(&sm.p_full[i % kNSP], (i / kNSP) & 1, abort_flag, p.err)) return false;
-      if (!mbar_wait(&sm.v_full[i % kNS], (i / kNS) & 1, abort_flag, p.err)) return false;
-      const int kb = (kt0 + i) * kBN;
-      // V rows of keys that hold no data of this sequence are zeroed before P.V: pages that
-      // were not copied (outside the needed key range) keep an older tile, and slots past the
-      // sequence's last key may hold anything (NaN); P = 0 there does not cancel NaN.
-      const int v0 = max(kb, (k_lo >> 4) * kPage), v1 = min(min(kb + kBN, ((k_hi >> 4) + 1) * kPage), ctx_end);
-      if (v0 > kb || v1 < kb + kBN) {
-        for (int idx = lane; idx < kBN * (kSD / 8); idx += 32) {
-          const int r = idx / (kSD / 8), dg = idx % (kSD / 8);
-          if (kb + r < v0 || kb + r >= v1)
-            *reinterpret_cast<uint4*>(sm.st[i % kNS] + kSKTile + ((r >> 3) * (kSD / 8) + dg) * 128 + (r & 7) * 16) =
-                make_uint4(0, 0, 0, 0);
-        }
-        fence_proxy_async();
-        __syncwarp();
-      }
+    // ------------------------------------------------------------ MMA issuer (even CTA)
+    auto qk = [&](int j) -> bool {
+      const int s = j % kNK;
+      if (!mbar_wait(&sm.k_full[s], (j / kNK) & 1, abort_flag, p.err)) return false;
+      if (!mbar_wait_cl(&sm.k_peer[s], (j / kNK) & 1, abort_flag, p.err)) return false;
+      // The single S buffer: both CTAs' softmax threads have read S_{j-1} into registers.
+      if (j > 0 && !mbar_wait_cl(&sm.s_free, (j - 1) & 1, abort_flag, p.err)) return false;
       tc_fence_after();
       if (lane == 0) {
-        const uint32_t va = smem_u32(sm.st[i % kNS] + kSKTile);
+        const uint32_t ka = smem_u32(sm.k[s]);
+        const uint32_t qh = smem_u32(sm.qhi);
 #pragma unroll
-        for (int k = 0; k < kBN / 16; ++k)
-          mma_ts(tm + kTmO, tm + kTmS + 64 * (i % kNSP) + 8 * k,
-                 desc_tiled(va + k * 2 * kKeyGroupBytes, kKeyGroupBytes, 128), kIdescPV, (i > 0 || k > 0) ? 1u : 0u);
-        mma_commit(&sm.pv_done[i % kNSP]);
-        mma_commit(&sm.v_empty[i % kNS]);
+        for (int k = 0; k < 8; ++k)   // dims 0-127: Q from tensor memory
+          mma2_ts(tm + kTmS, tm + kTmQ + 8 * k, desc_tiled(ka + k * 256, 128, kKeyGroupBytes), kIdescQK, k > 0 ? 1u : 0u);
+#pragma unroll
+        for (int k = 8; k < 16; ++k)  // dims 128-255: Q from shared memory
+          mma2_ss(tm + kTmS, desc_sw128(qh + ((k - 8) >> 2) * kQChunk + (k & 3) * 32, 16, 1024),
+                  desc_tiled(ka + k * 256, 128, kKeyGroupBytes), kIdescQK, 1u);
+        mma2_commit_mc(&sm.s_full, kBoth);
+        mma2_commit_mc(&sm.k_empty[s], kBoth);
       }
       __syncwarp();
       return true;
     };
-    bool ok = mbar_wait(&sm.q_ready, 0, abort_flag, p.err);
-    for (int j = 0; ok && j < n_tiles; ++j) {
-      const int s = j % kNS;
-      if (!mbar_wait(&sm.k_full[s], (j / kNS) & 1, abort_flag, p.err)) break;
-      // S buffer j % 3 last held P_{j-3}: reuse it once P_{j-3} V_{j-3} has completed (issued two
-      // MMA groups earlier, so this wait does not drain the tensor pipe).
-      if (j >= kNSP && !mbar_wait(&sm.pv_done[j % kNSP], ((j - kNSP) / kNSP) & 1, abort_flag, p.err)) break;
+    auto pv = [&](int i) -> bool {
+      const int s = i % kNV;
+      if (!mbar_wait_cl(&sm.p_full, i & 1, abort_flag, p.err)) return false;
+      if (!mbar_wait_cl(&sm.v_ready[s], (i / kNV) & 1, abort_flag, p.err)) return false;
       tc_fence_after();
       if (lane == 0) {
-        const uint32_t ka = smem_u32(sm.st[s]);
-        const uint32_t qh = smem_u32(sm.qhi);
-        const uint32_t sd = tm + kTmS + 64 * (j % kNSP);
+        const uint32_t va = smem_u32(sm.v[s]);
 #pragma unroll
-        for (int k = 0; k < 8; ++k)   // dims 0-127: Q from tensor memory
-          mma_ts(sd, tm + kTmQ + 8 * k, desc_tiled(ka + k * 256, 128, kKeyGroupBytes), kIdescQK, k > 0 ? 1u : 0u);
-#pragma unroll
-        for (int k = 8; k < 16; ++k)  // dims 128-255: Q from shared memory
-          mma_ss(sd, desc_sw128(qh + ((k - 8) >> 2) * kQChunk + (k & 3) * 32, 16, 1024),
-                 desc_tiled(ka + k * 256, 128, kKeyGroupBytes), kIdescQK, 1u);
-        mma_commit(&sm.s_full[j % kNSP]);
-        mma_commit(&sm.k_empty[s]);
+        for (int k = 0; k < kSN / 16; ++k)   // 16 keys (two key groups) per step
+          mma2_ts(tm + kTmO, tm + kTmP + 8 * k, desc_tiled(va + k * 2 * kVGroupBytes, kVGroupBytes, 128), kIdescPV,
+                  (i > 0 || k > 0) ? 1u : 0u);
+        mma2_commit_mc(&sm.pv_done, kBoth);
+        mma2_commit_mc(&sm.v_empty[s], kBoth);
       }
       __syncwarp();
-      if (j >= 1 && !pv(j - 1)) {
-        ok = false;
-        break;
-      }
-      if (j == n_tiles - 1 && !pv(j)) ok = false;
+      return true;
+    };
+    // QK^T of tile j+1 goes in as soon as S_j has been read, ahead of P_j V_j, which waits for
+    // the softmax to finish tile j.
+    bool ok = mbar_wait_cl(&sm.q_pair, 0, abort_flag, p.err) && qk(0);
+    for (int j = 1; ok && j <= n_tiles; ++j) {
+      if (j < n_tiles && !qk(j)) ok = false;
+      if (ok && !pv(j - 1)) ok = false;
     }
   } else if (warp >= 2 && warp <= 5) {
     // ------------------------------------------------------------ softmax / epilogue warps
@@ -252,65 +311,72 @@ __global__ void __launch_bounds__(kSlidingThreads, 1)
     const bool row_ok = pos >= p_lo && pos <= p_hi;
 
     // Q: the producer's TMA brought the roped tile in (4 chunks of 64 dims, 128B swizzle);
-    // dims 0-127 sit in ring stage 2 and each thread moves its row of them into tensor memory
-    // (an A operand in bf16 pairs), which frees stage 2 for keys and values. Dims 128-255 stay
-    // in shared memory as the A operand of the other half of the QK^T k-steps.
+    // dims 0-127 sit in K stage 2 and each thread moves its row of them into tensor memory (an A
+    // operand in bf16 pairs), which frees the stage for keys. Dims 128-255 stay in shared memory
+    // as the A operand of the other half of the QK^T k-steps.
     {
       const bool okq = mbar_wait(&sm.q_full, 0, abort_flag, p.err);
-      const uint8_t* qrow = sm.st[2] + r * 128;
+      const uint8_t* qrow = sm.k[kQStage] + r * 128;
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t w[32];
 #pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          const uint4 v = okq ? *reinterpret_cast<const uint4*>(qrow + c * kQChunk + ((g ^ (r & 7)) * 16))
+        for (int q8 = 0; q8 < 8; ++q8) {
+          const uint4 v = okq ? *reinterpret_cast<const uint4*>(qrow + c * kQChunk + ((q8 ^ (r & 7)) * 16))
                               : make_uint4(0, 0, 0, 0);
-          w[4 * g] = v.x;
-          w[4 * g + 1] = v.y;
-          w[4 * g + 2] = v.z;
-          w[4 * g + 3] = v.w;
+          w[4 * q8] = v.x;
+          w[4 * q8 + 1] = v.y;
+          w[4 * q8 + 2] = v.z;
+          w[4 * q8 + 3] = v.w;
         }
         tmem_st32(tq + kTmQ + 32 * c, w);   // dims 64c .. 64c+63 -> columns 32c .. 32c+31
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&sm.q_ready);
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&sm.q_local);
+        arrive_leader(&sm.q_pair);
+      }
     }
 
     const float cl2 = p.scale_log2;
     float m_used = -INFINITY, l_run = 0.f;
     bool ok = true;
     for (int j = 0; j < n_tiles; ++j) {
-      const int kb = (kt0 + j) * kBN;
-      const int sb = j % kNSP;
-      if (!mbar_wait(&sm.s_full[sb], (j / kNSP) & 1, abort_flag, p.err)) {
+      const int kb = (kt0 + j) * kSN;
+      // Waits are made warp-uniform so that every lane leaves the loop together on an abort.
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.s_full, j & 1, abort_flag, p.err))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      uint32_t sr[64];
-      tmem_ld32(tq + kTmS + 64 * sb, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-      tmem_ld32(tq + kTmS + 64 * sb + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+      uint32_t sr[kSN];
+#pragma unroll
+      for (int c = 0; c < kSN / 32; ++c) tmem_ld32(tq + kTmS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
       tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) arrive_leader(&sm.s_free);   // S may now be overwritten by QK^T of tile j+1
 
-      float s[64];
+      float s[kSN];
 #pragma unroll
-      for (int c = 0; c < 64; ++c) s[c] = __uint_as_float(sr[c]);
-      const bool full = row_ok && kb + kBN - 1 <= pos && (W == 0 || pos - kb <= W - 1);
-      if (!full) {
+      for (int c = 0; c < kSN; ++c) s[c] = __uint_as_float(sr[c]);
+      const bool full = row_ok && kb + kSN - 1 <= pos && (W == 0 || pos - kb <= W - 1);
+      if (!full) {   // the row's visible keys in this tile are one run of columns [lo, hi]
+        int lo = W > 0 ? max(0, pos - W + 1 - kb) : 0;
+        int hi = row_ok ? min(kSN - 1, pos - kb) : -1;
+        if (hi < lo) lo = hi = 1 << 20;   // none
+        const unsigned span = (unsigned)(hi - lo);
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const int key = kb + c;
-          const bool vis = row_ok && key <= pos && (W == 0 || pos - key <= W - 1);
-          s[c] = vis ? s[c] : -INFINITY;
-        }
+        for (int c = 0; c < kSN; ++c) s[c] = ((unsigned)(c - lo) <= span) ? s[c] : -INFINITY;
       }
       float mx[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         mx[i] = s[i];
 #pragma unroll
-        for (int c = 1; c < 8; ++c) mx[i] = fmaxf(mx[i], s[i + 8 * c]);
+        for (int c = 1; c < kSN / 8; ++c) mx[i] = fmaxf(mx[i], s[i + 8 * c]);
       }
       const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                              fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * cl2;
@@ -322,10 +388,10 @@ __global__ void __launch_bounds__(kSlidingThreads, 1)
         m_used = mt;
       }
       const float neg_m = (m_used == -INFINITY) ? 0.f : -m_used;
-      uint32_t pw[32];
+      uint32_t pw[kSN / 2];
       float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int w = 0; w < 32; ++w) {
+      for (int w = 0; w < kSN / 2; ++w) {
         const float e0 = ex2(fmaf(s[2 * w], cl2, neg_m));
         const float e1 = ex2(fmaf(s[2 * w + 1], cl2, neg_m));
         ls[w & 3] += e0;
@@ -334,16 +400,14 @@ __global__ void __launch_bounds__(kSlidingThreads, 1)
       }
       l_run = fmaf(l_run, alpha, (ls[0] + ls[1]) + (ls[2] + ls[3]));
 
-      // P_j (bf16 key pairs) over the first 32 columns of its own S buffer: the A operand of P.V.
-      tmem_st32(tq + kTmS + 64 * sb, pw);
-
-      // O correction (rows whose max rose by more than 2^8), after P_{j-1} V_{j-1} landed.
-      if (__any_sync(0xffffffffu, need_o)) {
-        if (!mbar_wait(&sm.pv_done[(j - 1) % kNSP], ((j - 1) / kNSP) & 1, abort_flag, p.err)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
+      // P_{j-1} V_{j-1} has completed: the P buffer is free and O holds every earlier tile.
+      if (j > 0 &&
+          !__all_sync(0xffffffffu, mbar_wait(&sm.pv_done, (j - 1) & 1, abort_flag, p.err))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (__any_sync(0xffffffffu, need_o)) {   // O correction (rows whose max rose by more than 2^8)
         const float a = need_o ? alpha : 1.f;
 #pragma unroll 1
         for (int cc = 0; cc < kSD / 32; ++cc) {
@@ -354,15 +418,18 @@ __global__ void __launch_bounds__(kSlidingThreads, 1)
           for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * a);
           tmem_st32(tq + kTmO + 32 * cc, o);
         }
-        tmem_st_wait();
       }
+      // P_j (bf16 key pairs): the A operand of P.V.
+      tmem_st32(tq + kTmP, *reinterpret_cast<const uint32_t(*)[32]>(&pw[0]));
+      tmem_st32(tq + kTmP + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pw[32]));
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&sm.p_full[sb]);
+      __syncwarp();
+      if (lane == 0) arrive_leader(&sm.p_full);
     }
 
     // Epilogue: O / l -> bf16, rows of this sequence only.
-    if (ok && mbar_wait(&sm.pv_done[(n_tiles - 1) % kNSP], ((n_tiles - 1) / kNSP) & 1, abort_flag, p.err)) {
+    if (ok && __all_sync(0xffffffffu, mbar_wait(&sm.pv_done, (n_tiles - 1) & 1, abort_flag, p.err))) {
       tc_fence_after();
       const float inv = (l_run > 0.f) ? __frcp_rn(l_run) : 0.f;
       __nv_bfloat16* orow = p.out + ((size_t)(q_row0 + r) * kSlidingHq + h) * kSD;
@@ -385,18 +452,43 @@ __global__ void __launch_bounds__(kSlidingThreads, 1)
   }
 
   // ------------------------------------------------------------ teardown
+  // Neither CTA may free its tensor memory or leave while the pair's MMAs or signals into it
+  // are in flight: each waits (bounded) for the last stage releases it was sent, an abort is
+  // passed to the peer so that its waits end early, and a cluster barrier closes the pair.
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) {
+    if (*abort_flag) {
+      st_peer_u32(map_peer(smem_u32(&sm.abort_flag), peer), 1u);
+    } else {
+      const unsigned long long w0 = globaltimer();
+      for (int s = 0; s < kNK && s < n_tiles; ++s) {
+        const int j_last = s + kNK * ((n_tiles - 1 - s) / kNK);
+        while (!mbar_try_wait(smem_u32(&sm.k_empty[s]), (uint32_t)(j_last / kNK) & 1u) &&
+               globaltimer() - w0 < kWaitLimitNs) {
+        }
+      }
+      for (int s = 0; s < kNV && s < n_tiles; ++s) {
+        const int j_last = s + kNV * ((n_tiles - 1 - s) / kNV);
+        while (!mbar_try_wait(smem_u32(&sm.v_empty[s]), (uint32_t)(j_last / kNV) & 1u) &&
+               globaltimer() - w0 < kWaitLimitNs) {
+        }
+      }
+    }
+  }
+  __syncthreads();
+  tc_fence_before();
+  cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
     if (sm.abort_flag) {   // let every issued MMA finish before the columns are freed
-      if (lane == 0) mma_commit(&sm.teardown);
+      if (leader && lane == 0) mma2_commit_mc(&sm.teardown, kBoth);
       __syncwarp();
-      const unsigned long long t0 = globaltimer();
-      while (!mbar_try_wait(smem_u32(&sm.teardown), 0) && globaltimer() - t0 < kWaitLimitNs) {
+      const unsigned long long w0 = globaltimer();
+      while (!mbar_try_wait(smem_u32(&sm.teardown), 0) && globaltimer() - w0 < kWaitLimitNs) {
       }
     }
-    tmem_dealloc(tm, 512);
+    tmem_dealloc2(tm, 512);
   }
 }
 
@@ -429,9 +521,9 @@ cudaError_t launch_prefill(bool global, const SeqRows& rows, int window, float s
     attr[dev] = true;
   }
   const long long slots = (long long)rows.T / kBM + 2LL * rows.B;
-  const long long blocks = slots * kSlidingHq;
+  const long long blocks = slots * kSlidingHkv * 2;   // a pair of CTAs (two query heads) per (query tile, KV head)
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-  prefill_sliding_kernel<<<(unsigned)blocks, kSlidingThreads, kSlidingSmemBytes, s>>>(mq, p);
+  prefill_sliding_kernel<<<(unsigned)blocks, kThreads, kSlidingSmemBytes, s>>>(mq, p);
   return cudaGetLastError();
 }
 

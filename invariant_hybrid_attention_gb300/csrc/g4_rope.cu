@@ -114,6 +114,12 @@ struct PageDst {   // key slot j of a page-head block (see tiled_offset)
   __device__ __forceinline__ __nv_bfloat16* at(int d) const { return block + tiled_offset(j, d, D); }
 };
 
+struct VDst {   // key slot j of a sliding V page-head block (see tiled_offset_v256)
+  __nv_bfloat16* block;
+  int j;
+  __device__ __forceinline__ __nv_bfloat16* at(int d) const { return block + tiled_offset_v256(j, d); }
+};
+
 struct RotDst {   // key slot j of a rotated-column side page (see rot_offset); other dims dropped
   __nv_bfloat16* block;
   int j;
@@ -224,7 +230,7 @@ __device__ __forceinline__ void append_token(const __nv_bfloat16* k_row, const _
                           RotDst{(__nv_bfloat16*)c.krot + ((size_t)phys * HKV + g) * kRotPageElems, j}, pos, tb);
     } else {
       rope_vec_warp<D, R>(k_row + (size_t)g * D, PageDst<D>{(__nv_bfloat16*)c.k + blk, j}, pos, tb);
-      copy_vec_warp<D>(v_row + (size_t)g * D, PageDst<D>{(__nv_bfloat16*)c.v + blk, j});
+      copy_vec_warp<D>(v_row + (size_t)g * D, VDst{(__nv_bfloat16*)c.v + blk, j});
     }
   }
 }

@@ -37,6 +37,21 @@ def tile(rows: torch.Tensor) -> torch.Tensor:
     return r.permute(0, 1, 4, 2, 5, 3, 6).contiguous().reshape(P, H, 2, 2, 32, 8, 8)
 
 
+def untile_v256(t: torch.Tensor) -> torch.Tensor:
+    """A sliding V tensor [pages][heads][2][2][16][8][8] (two 128-dim halves per page-head block)
+    as plain rows [pages][heads][16][256]."""
+    P, H = t.shape[0], t.shape[1]
+    r = t.reshape(P, H, 2, 2, 16, 8, 8).permute(0, 1, 3, 5, 2, 4, 6)   # [P][H][kg][j8][half][dg][d8]
+    return r.reshape(P, H, PAGE_SIZE, 256)
+
+
+def tile_v256(rows: torch.Tensor) -> torch.Tensor:
+    """Plain rows [pages][heads][16][256] in the sliding V layout (inverse of `untile_v256`)."""
+    P, H = rows.shape[0], rows.shape[1]
+    r = rows.reshape(P, H, 2, 8, 2, 16, 8)          # [P][H][kg][j8][half][dg][d8]
+    return r.permute(0, 1, 4, 2, 5, 3, 6).contiguous().reshape(P, H, 2, 2, 16, 8, 8)
+
+
 def untile_rot(t: torch.Tensor) -> torch.Tensor:
     """A global k_rot tensor [pages][4][2][2][8][8][8] as rows [pages][4][16][128] holding dims
     0-63 then 256-319."""
@@ -56,7 +71,9 @@ class PagedKV:
         else:
             shape = (int(num_pages), int(n_kv_heads), 2, 2, 32, 8, 8)
         self.k = torch.empty(shape, dtype=torch.bfloat16, device=device)
-        self.v = None if shared else torch.empty(shape, dtype=torch.bfloat16, device=device)
+        # sliding V: two contiguous 128-dim halves per page-head block (see untile_v256)
+        self.v = None if shared else torch.empty((int(num_pages), int(n_kv_heads), 2, 2, 16, 8, 8),
+                                                 dtype=torch.bfloat16, device=device)
         self.k_rot = (torch.empty((int(num_pages), int(n_kv_heads), 2, 2, 8, 8, 8), dtype=torch.bfloat16,
                                   device=device) if shared else None)
         if fill is not None:

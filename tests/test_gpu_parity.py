@@ -10,7 +10,7 @@ import torch
 import invariant_hybrid_attention_gb300 as g4
 import oracle
 from invariant_hybrid_attention_gb300 import inputs as gi
-from invariant_hybrid_attention_gb300.paged import device_int32, untile, untile_rot
+from invariant_hybrid_attention_gb300.paged import device_int32, untile, untile_rot, untile_v256
 
 from gpu_cases import GEOM, Batch, DecodeBatch, assert_close, f64, layers
 
@@ -65,7 +65,7 @@ def test_kv_append_writes_the_contract_layout(kind):
     torch.cuda.synchronize()
     assert g4.g4attn_status_sync() == g4.G4_OK
     kc = untile(cache.k.cpu())
-    vc = None if cache.v is None else untile(cache.v.cpu())
+    vc = None if cache.v is None else untile_v256(cache.v.cpu())
     rc = None if cache.k_rot is None else untile_rot(cache.k_rot.cpu())
     R = oracle.rope_rotated_pairs(olayer.head_dim, olayer.rope_partial)
     rot_dims = np.r_[0:R, olayer.head_dim // 2:olayer.head_dim // 2 + R]

@@ -1,7 +1,7 @@
 """CPU checks of the tiled cache-page layout helpers (8x8 core matrices per page and head)."""
 import torch
 
-from invariant_hybrid_attention_gb300.paged import tile, untile, untile_rot
+from invariant_hybrid_attention_gb300.paged import tile, tile_v256, untile, untile_rot, untile_v256
 
 
 def test_tile_untile_roundtrip():
@@ -40,3 +40,17 @@ def test_rotated_side_layout():
         col = d if d < 64 else d - 256 + 64
         off = (((d // 256) * 2 + j // 8) * 8 + (d % 64) // 8) * 64 + (j % 8) * 8 + d % 8
         assert rows[1, 3, j, col] == flat[1, 3, off]
+
+
+def test_sliding_v_half_layout_roundtrip():
+    # sliding V: key j, dim d at (((d // 128) * 2 + j // 8) * 16 + (d % 128) // 8) * 64 + (j % 8) * 8 + d % 8
+    x = torch.arange(3 * 2 * 16 * 256, dtype=torch.float32).view(3, 2, 16, 256)
+    t = tile_v256(x)
+    assert t.shape == (3, 2, 2, 2, 16, 8, 8)
+    flat = t.reshape(3, 2, -1)
+    for j, d in [(0, 0), (5, 9), (8, 127), (15, 255), (9, 130), (3, 128)]:
+        off = (((d // 128) * 2 + j // 8) * 16 + (d % 128) // 8) * 64 + (j % 8) * 8 + d % 8
+        assert flat[2, 1, off] == x[2, 1, j, d]
+    assert torch.equal(untile_v256(t), x)
+    # each 128-dim half of a page-head block is one contiguous 2048-element (4 KB) block
+    assert torch.equal(flat[0, 0, 2048:].sort().values, x[0, 0, :, 128:].reshape(-1).sort().values)
