@@ -21,10 +21,11 @@
 //              page-head blocks) into a 3-stage ring;
 //   warp 6     this CTA's V half of each key tile (eight 4 KB copies: sliding V pages store each
 //              128-dim half of a page-head block contiguously) into a 3-stage ring;
-//   warp 1     even CTA: issues S = Q K^T and O += P V for the pair. Odd CTA: tells the even
-//              CTA when its K half of a tile has landed;
-//   warp 7     zeroes value rows of this CTA's V half that hold no key of the sequence, then
-//              tells the even CTA that the V half is ready;
+//   warp 1     even CTA: issues S = Q K^T for the pair. Odd CTA: tells the even CTA when its K
+//              half of a tile has landed;
+//   warp 7     zeroes value rows of this CTA's V half that hold no key of the sequence; then
+//              the even CTA's issues O += P V for the pair, the odd CTA's tells the even CTA
+//              that its V half is ready;
 //   warps 2-5  one thread per query row of this CTA's head: mask, online softmax (lazy
 //              rescale, threshold 2^8), P (bf16), the O correction when needed, and the
 //              epilogue O / l -> bf16.
@@ -128,7 +129,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kNV; ++s) {
       mbar_init(&sm.v_full[s], 1);
       mbar_init(&sm.v_empty[s], 1);
-      mbar_init(&sm.v_ready[s], 2);   // even CTA: both V halves landed and checked
+      mbar_init(&sm.v_ready[s], 1);   // even CTA: the odd CTA's V half landed and was checked
     }
     mbar_init(&sm.s_full, 1);
     mbar_init(&sm.s_free, kPairWarps);   // even CTA: both CTAs' softmax warps have read S
@@ -137,7 +138,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(&sm.q_full, 1);
     mbar_init(&sm.q_local, kSoftmaxThreads / 32);   // this CTA's Q dims 0-127 left the K stage
     mbar_init(&sm.q_pair, kPairWarps);              // even CTA: both CTAs' Q is in tensor memory
-    mbar_init(&sm.teardown, 1);
+    mbar_init(&sm.teardown, 2);   // on an abort both issuers commit
     sm.abort_flag = 0;
     fence_mbar_init();
   }
@@ -224,27 +225,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp == 7) {
-    // ------------------------------------------------------------ V check (both CTAs)
-    // Value rows of this CTA's V half for keys that hold no data of this sequence are zeroed
-    // before P.V: pages outside the key range were not copied and keep an older tile, and slots
-    // past the sequence's last key may hold anything (NaN); P = 0 there does not cancel NaN.
-    for (int j = 0; j < n_tiles; ++j) {
-      const int s = j % kNV;
-      if (!__all_sync(0xffffffffu, mbar_wait(&sm.v_full[s], (j / kNV) & 1, abort_flag, p.err))) break;
-      const int kb = (kt0 + j) * kSN;
-      const int v0 = max(kb, (k_lo >> 4) * kPage), v1 = min(min(kb + kSN, ((k_hi >> 4) + 1) * kPage), ctx_end);
-      if (v0 > kb || v1 < kb + kSN) {
-        for (int idx = lane; idx < kSN * 16; idx += 32) {
-          const int r = idx >> 4, dg = idx & 15;
-          if (kb + r < v0 || kb + r >= v1)
-            *reinterpret_cast<uint4*>(sm.v[s] + ((r >> 3) * 16 + dg) * 128 + (r & 7) * 16) = make_uint4(0, 0, 0, 0);
-        }
-        fence_proxy_async();
-      }
-      __syncwarp();
-      if (lane == 0) arrive_leader(&sm.v_ready[s]);
-    }
   } else if (warp == 1 && !leader) {
     // ------------------------------------------------------------ K relay (odd CTA)
     if (lane == 0) {
@@ -255,13 +235,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer (even CTA)
-    auto qk = [&](int j) -> bool {
+    // ------------------------------------------------------------ QK^T issuer (even CTA)
+    // Issuing a group of MMAs blocks for about as long as they run, so QK^T and P.V have one
+    // issuer each: neither waits for its operands while the tensor pipe idles. Each commit
+    // tracks its own thread's MMAs only.
+    // Waits are made warp-uniform so that every lane leaves the loop together on an abort.
+    bool ok = __all_sync(0xffffffffu, mbar_wait_cl(&sm.q_pair, 0, abort_flag, p.err));
+    for (int j = 0; ok && j < n_tiles; ++j) {
       const int s = j % kNK;
-      if (!mbar_wait(&sm.k_full[s], (j / kNK) & 1, abort_flag, p.err)) return false;
-      if (!mbar_wait_cl(&sm.k_peer[s], (j / kNK) & 1, abort_flag, p.err)) return false;
-      // The single S buffer: both CTAs' softmax threads have read S_{j-1} into registers.
-      if (j > 0 && !mbar_wait_cl(&sm.s_free, (j - 1) & 1, abort_flag, p.err)) return false;
+      ok = __all_sync(0xffffffffu, mbar_wait(&sm.k_full[s], (j / kNK) & 1, abort_flag, p.err) &&
+                                       mbar_wait_cl(&sm.k_peer[s], (j / kNK) & 1, abort_flag, p.err) &&
+                                       // the single S buffer: both CTAs' softmax threads have read
+                                       // S_{j-1} into registers
+                                       (j == 0 || mbar_wait_cl(&sm.s_free, (j - 1) & 1, abort_flag, p.err)));
+      if (!ok) break;
       tc_fence_after();
       if (lane == 0) {
         const uint32_t ka = smem_u32(sm.k[s]);
@@ -277,12 +264,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mma2_commit_mc(&sm.k_empty[s], kBoth);
       }
       __syncwarp();
-      return true;
-    };
-    auto pv = [&](int i) -> bool {
+    }
+  } else if (warp == 7) {
+    // ------------------------------------------------------------ V check (both CTAs), P.V issuer (even CTA)
+    // Value rows of this CTA's V half for keys that hold no data of this sequence are zeroed
+    // before P.V: pages outside the key range were not copied and keep an older tile, and slots
+    // past the sequence's last key may hold anything (NaN); P = 0 there does not cancel NaN.
+    for (int i = 0; i < n_tiles; ++i) {
       const int s = i % kNV;
-      if (!mbar_wait_cl(&sm.p_full, i & 1, abort_flag, p.err)) return false;
-      if (!mbar_wait_cl(&sm.v_ready[s], (i / kNV) & 1, abort_flag, p.err)) return false;
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.v_full[s], (i / kNV) & 1, abort_flag, p.err))) break;
+      const int kb = (kt0 + i) * kSN;
+      const int v0 = max(kb, (k_lo >> 4) * kPage), v1 = min(min(kb + kSN, ((k_hi >> 4) + 1) * kPage), ctx_end);
+      if (v0 > kb || v1 < kb + kSN) {
+        for (int idx = lane; idx < kSN * 16; idx += 32) {
+          const int r = idx >> 4, dg = idx & 15;
+          if (kb + r < v0 || kb + r >= v1)
+            *reinterpret_cast<uint4*>(sm.v[s] + ((r >> 3) * 16 + dg) * 128 + (r & 7) * 16) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async();
+      }
+      __syncwarp();
+      if (!leader) {
+        if (lane == 0) mbar_arrive_remote(map_peer(smem_u32(&sm.v_ready[s]), peer));
+        continue;
+      }
+      if (!__all_sync(0xffffffffu, mbar_wait_cl(&sm.p_full, i & 1, abort_flag, p.err) &&
+                                       mbar_wait_cl(&sm.v_ready[s], (i / kNV) & 1, abort_flag, p.err)))
+        break;
       tc_fence_after();
       if (lane == 0) {
         const uint32_t va = smem_u32(sm.v[s]);
@@ -294,14 +302,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mma2_commit_mc(&sm.v_empty[s], kBoth);
       }
       __syncwarp();
-      return true;
-    };
-    // QK^T of tile j+1 goes in as soon as S_j has been read, ahead of P_j V_j, which waits for
-    // the softmax to finish tile j.
-    bool ok = mbar_wait_cl(&sm.q_pair, 0, abort_flag, p.err) && qk(0);
-    for (int j = 1; ok && j <= n_tiles; ++j) {
-      if (j < n_tiles && !qk(j)) ok = false;
-      if (ok && !pv(j - 1)) ok = false;
     }
   } else if (warp >= 2 && warp <= 5) {
     // ------------------------------------------------------------ softmax / epilogue warps
@@ -479,16 +479,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_before();
   cluster_sync_all();
-  if (warp == 1) {
+  if (warp == 1 || warp == 7) {
     tc_fence_after();
     if (sm.abort_flag) {   // let every issued MMA finish before the columns are freed
-      if (leader && lane == 0) mma2_commit_mc(&sm.teardown, kBoth);
+      if (leader && lane == 0) mma2_commit_mc(&sm.teardown, kBoth);   // both issuers
       __syncwarp();
-      const unsigned long long w0 = globaltimer();
-      while (!mbar_try_wait(smem_u32(&sm.teardown), 0) && globaltimer() - w0 < kWaitLimitNs) {
+      if (warp == 1) {
+        const unsigned long long w0 = globaltimer();
+        while (!mbar_try_wait(smem_u32(&sm.teardown), 0) && globaltimer() - w0 < kWaitLimitNs) {
+        }
       }
     }
-    tmem_dealloc2(tm, 512);
+    if (warp == 1) tmem_dealloc2(tm, 512);
   }
 }
 
