@@ -239,8 +239,10 @@ G4_DEV bool mbar_wait_cl(uint64_t* bar, uint32_t parity, volatile int* abort, ui
   if (mbar_try_wait_cluster(a, parity)) return true;
   const unsigned long long t0 = globaltimer();
   while (true) {
-    for (int i = 0; i < 32; ++i)
+    for (int i = 0; i < 32; ++i) {
       if (mbar_try_wait_cluster(a, parity)) return true;
+      __nanosleep(32);   // a cluster-scope poll does not suspend: leave issue slots to the other warps
+    }
     if (abort && *abort) return false;
     if (globaltimer() - t0 > kWaitLimitNs) {
       if (abort) *abort = 1;
@@ -269,6 +271,18 @@ G4_DEV void tma_load_3d(void* smem, const CUtensorMap* map, int x, int y, int z,
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
       : "memory");
 }
+
+// Tiled shared -> global store through a tensor map (bulk async-group completion). The
+// innermost coordinate must keep the copy 16-byte aligned; no coordinate may be negative.
+G4_DEV void tma_store_3d(const CUtensorMap* map, const void* smem, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(smem)), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+G4_DEV void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Waits until every committed bulk store of this thread has finished reading shared memory.
+G4_DEV void bulk_wait_group_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
 G4_DEV void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

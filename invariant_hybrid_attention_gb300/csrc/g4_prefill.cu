@@ -225,6 +225,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
     }
+    __syncwarp();
   } else if (warp == 1 && !leader) {
     // ------------------------------------------------------------ K relay (odd CTA)
     if (lane == 0) {
@@ -234,6 +235,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_arrive_remote(map_peer(smem_u32(&sm.k_peer[s]), peer));
       }
     }
+    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ QK^T issuer (even CTA)
     // Issuing a group of MMAs blocks for about as long as they run, so QK^T and P.V have one
@@ -428,11 +430,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (lane == 0) arrive_leader(&sm.p_full);
     }
 
-    // Epilogue: O / l -> bf16, rows of this sequence only.
-    if (ok && __all_sync(0xffffffffu, mbar_wait(&sm.pv_done, (n_tiles - 1) & 1, abort_flag, p.err))) {
+    // Epilogue: O / l -> bf16, rows of this sequence only. A tile whose 128 rows all belong to
+    // this sequence is staged in shared memory (the K ring, free by now) in the 128B-swizzled
+    // layout of the query tensor map and written by four TMA stores; any other tile is written
+    // row by row, so that rows of other sequences or padding are never touched.
+    const bool tile_full = p_lo == kBM * t && p_hi == kBM * t + kBM - 1;
+    const bool ep_ok = ok && __all_sync(0xffffffffu, mbar_wait(&sm.pv_done, (n_tiles - 1) & 1, abort_flag, p.err));
+    if (ep_ok) {
       tc_fence_after();
       const float inv = (l_run > 0.f) ? __frcp_rn(l_run) : 0.f;
       __nv_bfloat16* orow = p.out + ((size_t)(q_row0 + r) * kSlidingHq + h) * kSD;
+      uint8_t* stage = sm.k[0];   // 4 boxes of 128 rows x 64 dims (16 KB each)
 #pragma unroll 1
       for (int cc = 0; cc < kSD / 32; ++cc) {
         uint32_t o[32];
@@ -442,12 +450,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 16; ++c)
           w16[c] = pack_bf16(__uint_as_float(o[2 * c]) * inv, __uint_as_float(o[2 * c + 1]) * inv);
-        if (row_ok) {
+        if (tile_full) {
+          uint8_t* box = stage + (cc >> 1) * kQChunk + r * 128;
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            *reinterpret_cast<uint4*>(box + ((((cc & 1) * 4 + i) ^ (r & 7)) * 16)) =
+                make_uint4(w16[4 * i], w16[4 * i + 1], w16[4 * i + 2], w16[4 * i + 3]);
+        } else if (row_ok) {
           uint4* dst = reinterpret_cast<uint4*>(orow + 32 * cc);
 #pragma unroll
           for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w16[4 * i], w16[4 * i + 1], w16[4 * i + 2], w16[4 * i + 3]);
         }
       }
+    }
+    if (tile_full) {   // every softmax thread gets here, so the named barrier cannot hang
+      fence_proxy_async();
+      if (named_barrier_and(1, kSoftmaxThreads, ep_ok) && threadIdx.x == 64) {
+#pragma unroll
+        for (int c = 0; c < kSD / 64; ++c) tma_store_3d(&tmap_q, sm.k[0] + c * kQChunk, 64 * c, h, q_row0);
+        bulk_commit_group();
+        bulk_wait_group_read0();
+      }
+      __syncwarp();
     }
   }
 
@@ -455,6 +479,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // Neither CTA may free its tensor memory or leave while the pair's MMAs or signals into it
   // are in flight: each waits (bounded) for the last stage releases it was sent, an abort is
   // passed to the peer so that its waits end early, and a cluster barrier closes the pair.
+  // Aligned CTA barriers count whole warps: every warp arrives converged.
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -476,6 +502,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
     }
   }
+  __syncwarp();
   __syncthreads();
   tc_fence_before();
   cluster_sync_all();
