@@ -252,6 +252,17 @@ G4_DEV bool mbar_wait_cl(uint64_t* bar, uint32_t parity, volatile int* abort, ui
   }
 }
 
+// Out-of-line copies of the two waits, for kernels that wait in many places (one copy of each
+// polling loop keeps their hot loops small enough for the instruction caches; a kernel whose
+// inner loop waits on every step keeps the inlined form).
+static __device__ __noinline__ bool mbar_wait_ool(uint64_t* bar, uint32_t parity, volatile int* abort, uint32_t* err) {
+  return mbar_wait(bar, parity, abort, err);
+}
+static __device__ __noinline__ bool mbar_wait_cl_ool(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                                     uint32_t* err) {
+  return mbar_wait_cl(bar, parity, abort, err);
+}
+
 // ---- bulk copies (TMA) -------------------------------------------------------------------------
 G4_DEV void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
@@ -283,6 +294,14 @@ G4_DEV void tma_store_3d(const CUtensorMap* map, const void* smem, int x, int y,
 G4_DEV void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Waits until every committed bulk store of this thread has finished reading shared memory.
 G4_DEV void bulk_wait_group_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
+// Prefetch of a tensor-map tile into L2 (no shared memory, no completion to wait for).
+G4_DEV void tma_prefetch_l2_3d(const CUtensorMap* map, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
 
 G4_DEV void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

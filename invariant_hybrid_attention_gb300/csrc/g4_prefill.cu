@@ -1,41 +1,51 @@
 // Sliding-layer prefill on the 5th-generation tensor cores (tcgen05, accumulators in tensor
-// memory), one 2-SM MMA unit per pair of query heads.
+// memory): a persistent kernel of 2-SM MMA units, one unit per pair of query heads.
 //
 // Sliding layer (RL-Kernel RFC "[RFC][Gemma-4-31B-it] WS1/WS2 kernel roadmap", section 5,
 // sliding_attention_core: causal local attention, window 1024, 32 Q / 16 KV heads, D 256).
-// Work unit: (sequence, query tile of 128 positions aligned to absolute position, KV head g)
-// on a cluster of two CTAs; CTA rank r owns query head 2g + r, i.e. the two query heads that
-// share K and V. Key tiles of 128 keys are aligned to absolute key 0 and visited in ascending
-// order, so the arithmetic a row gets depends only on its own position, its sequence's keys and
-// the window: not on the batch, the row's place in it, padding, packing or the launch grid. A
-// key tile that holds no visible key for a row adds exact zeros to it (RFC section 4 rules 2,
-// 3 and 6).
+// Work unit: (sequence, query tile of 128 positions aligned to absolute position, KV head g),
+// computed by a cluster of two CTAs; CTA rank r owns query head 2g + r, i.e. the two query
+// heads that share K and V. Key tiles of 128 keys are aligned to absolute key 0 and visited in
+// ascending order, so the arithmetic a row gets depends only on its own position, its
+// sequence's keys and the window: not on the batch, the row's place in it, padding, packing, the
+// launch grid or which cluster runs the unit. A key tile that holds no visible key for a row
+// adds exact zeros to it (RFC section 4 rules 2, 3 and 6).
 //
 // Every tcgen05 MMA is one 2-SM operation (M = 256: the two heads' 128 rows each) issued by
 // the even CTA. A (queries, P) and D (S, O) are split by rows, so each CTA keeps its own head's
 // rows in its own tensor memory; B (K, V) is split by columns, so each CTA stages only half of
 // every key tile: keys 64r .. 64r+63 of K (all dims) and dims 128r .. 128r+127 of V (all 128
 // keys), 64 KB per tile instead of 128 KB. QK^T runs at N = 128 keys, P.V at N = 256 dims.
+//
+// The grid holds as many clusters as can be resident at once; cluster c computes units
+// c, c + C, c + 2C, ... (a fixed assignment: no work queue, no atomics). The K and V rings and
+// every barrier run on counters that continue across units, so the next unit's keys stream in
+// while the current one finishes, and its roped Q tile (prefetched into L2 one unit ahead) is
+// loaded as soon as the last QK^T of the current unit has read the previous one.
 // Per CTA:
-//   warp 0     the roped Q tile by TMA, then this CTA's K half of each key tile (four 8 KB
-//              page-head blocks) into a 3-stage ring;
+//   warp 0     per unit: K tiles 0 and 1, then the roped Q tile (dims 0-127 into the next K
+//              ring slot, dims 128-255 into their own buffer, once the previous unit's QK^T
+//              is done), then the remaining K tiles: this CTA's K half of each key tile is four
+//              8 KB page-head blocks, into a 3-stage ring;
 //   warp 6     this CTA's V half of each key tile (eight 4 KB copies: sliding V pages store each
 //              128-dim half of a page-head block contiguously) into a 3-stage ring;
-//   warp 1     even CTA: issues S = Q K^T for the pair. Odd CTA: tells the even CTA when its K
-//              half of a tile has landed;
+//   warp 1     even CTA: issues S = Q K^T for the pair. Odd CTA: tells the even CTA when each
+//              of its K ring slots has landed;
 //   warp 7     zeroes value rows of this CTA's V half that hold no key of the sequence; then
 //              the even CTA's issues O += P V for the pair, the odd CTA's tells the even CTA
 //              that its V half is ready;
-//   warps 2-5  one thread per query row of this CTA's head: mask, online softmax (lazy
-//              rescale, threshold 2^8), P (bf16), the O correction when needed, and the
-//              epilogue O / l -> bf16.
+//   warps 2-5  one thread per query row of this CTA's head: Q dims 0-127 into tensor memory,
+//              mask, online softmax (lazy rescale, threshold 2^8), P (bf16), the O correction
+//              when needed, and the epilogue O / l -> bf16.
 // The queries arrive already roped: the cache-append pass before this kernel wrote
 // bf16(RoPE(q)) into the sequence rows of `out`; the epilogue later overwrites exactly those
-// rows (each row belongs to one CTA).
+// rows (each row belongs to one unit).
 // Tensor memory (512 columns, allocated jointly by the pair): O [0,256), Q dims 0-127 [256,320)
 // as bf16 pairs, P [320,384) as bf16 key pairs, S [384,512). With one S buffer, QK^T of tile
 // j+1 is issued as soon as both CTAs' softmax threads have read S_j into registers, so it runs
 // while they exponentiate; P has its own buffer, so it never waits for S to be consumed.
+// An mbarrier parity wait cannot tell phases two apart, so every role that waits on a ring
+// barrier waits on each of its phases in order, including phases it has no use for.
 #include <math.h>
 
 #include "g4_prefill_common.cuh"
@@ -49,7 +59,7 @@ using namespace pf;
 constexpr int kSD = kSlidingD;                    // 256
 constexpr int kSN = 128;                          // keys per tile
 constexpr int kNK = 3, kNV = 3;                   // K and V ring stages
-constexpr int kQStage = 2;                        // K stage that first holds Q dims 0-127
+constexpr int kQAfter = 2;                        // a unit's Q takes the K ring slot after its first two tiles
 constexpr int kPageBytes = kPage * kSD * 2;       // one tiled page-head block: 8 KB
 constexpr int kKeyGroupBytes = 8 * kSD * 2;       // K: 8 keys x 256 dims, 4 KB
 constexpr int kVGroupBytes = 8 * (kSD / 2) * 2;   // V half: 8 keys x 128 dims, 2 KB
@@ -64,20 +74,56 @@ constexpr uint16_t kBoth = 0x3;
 constexpr uint32_t kPairWarps = 8;                // softmax warps of both CTAs
 
 struct SlidingSmem {
-  uint8_t k[kNK][kKStage];          // K halves [8 key groups][32 dim groups][8][8]; k[2] first holds Q dims 0-127
+  uint8_t k[kNK][kKStage];          // K halves [8 key groups][32 dim groups][8][8], or a unit's Q dims 0-127
   uint8_t v[kNV][kVStage];          // V halves [16 key groups][16 dim groups][8][8]
   uint8_t qhi[2 * kQChunk];         // Q dims 128-255 (128B swizzle), the shared-memory A operand
   uint64_t k_full[kNK], k_empty[kNK], k_peer[kNK];
   uint64_t v_full[kNV], v_empty[kNV], v_ready[kNV];
   uint64_t s_full, s_free, p_full, pv_done;
-  uint64_t q_full, q_local, q_pair, teardown;
+  uint64_t q_full, q_pair, q_free, o_free, q_read, teardown;
   uint32_t tmem_base;
   int abort_flag;
-  int unit_b, unit_t;
 };
 static_assert(2 * kQChunk <= kKStage, "Q dims 0-127 must fit in one K stage");
 constexpr size_t kSlidingSmemBytes = sizeof(SlidingSmem) + 1024;
 static_assert(kSlidingSmemBytes <= 232448, "sliding prefill exceeds the 227 KB shared-memory limit");
+
+// One unit as one CTA of its pair sees it.
+struct Unit {
+  int g, h, t, p_lo, p_hi, ctx_end, k_lo, k_hi, kt0, n_tiles, q_row0, qpos;
+  const int32_t* pt;
+  // K ring slot of key tile j, counting from the unit's first slot (its Q takes slot qpos)
+  __device__ int kslot(int j) const { return j + (j >= qpos ? 1 : 0); }
+};
+
+// Warp-wide. False when unit u holds no rows (its slot is past the last query tile) or its
+// positions are out of range (then the error word is set); every role skips such units alike.
+// Not inlined: six roles call it, once per unit.
+__device__ __noinline__ bool sliding_unit(const PrefillParams& p, int u, uint32_t rank, Unit& o) {
+  o.g = u % kSlidingHkv;
+  o.h = 2 * o.g + (int)rank;
+  int b, t;
+  find_unit(p.rows, u / kSlidingHkv, b, t);
+  if (b < 0) return false;
+  const int cs = p.rows.ctx_start[b], L = p.rows.q_len[b], qs = p.rows.q_start[b];
+  o.t = t;
+  o.p_lo = max(kBM * t, cs);
+  o.p_hi = min(kBM * t + kBM - 1, cs + L - 1);
+  o.ctx_end = cs + L;
+  if (o.p_hi >= kMaxPos || (o.p_hi >> 4) >= p.max_pages) {
+    if ((threadIdx.x & 31) == 0) set_error(p.err, kErrPos);
+    return false;
+  }
+  const int W = p.window;
+  o.k_lo = W > 0 ? max(0, o.p_lo - W + 1) : 0;
+  o.k_hi = o.p_hi;
+  o.kt0 = o.k_lo / kSN;
+  o.n_tiles = o.k_hi / kSN - o.kt0 + 1;
+  o.q_row0 = qs + (kBM * t - cs);   // memory row of tile row 0 (may be negative)
+  o.pt = p.page_table + (size_t)b * p.max_pages;
+  o.qpos = min(kQAfter, o.n_tiles);
+  return true;
+}
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     prefill_sliding_kernel(const __grid_constant__ CUtensorMap tmap_q, PrefillParams p) {
@@ -88,43 +134,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t rank = cluster_rank();   // which query head of the KV head's pair
   const uint32_t peer = rank ^ 1u;
   const bool leader = rank == 0;
-  const int unit = blockIdx.x >> 1;
-  const int g = unit % kSlidingHkv;
-  const int slot = unit / kSlidingHkv;
-  const int h = 2 * g + (int)rank;
-
-  if (warp == 0) {
-    int ub, ut;
-    find_unit(p.rows, slot, ub, ut);
-    if (lane == 0) {
-      sm.unit_b = ub;
-      sm.unit_t = ut;
-    }
-  }
-  __syncthreads();
-  const int b = sm.unit_b;   // both CTAs of the pair find the same unit
-  if (b < 0) return;
-  const int t = sm.unit_t;
-  const int cs = p.rows.ctx_start[b], L = p.rows.q_len[b], qs = p.rows.q_start[b];
-  const int p_lo = max(kBM * t, cs), p_hi = min(kBM * t + kBM - 1, cs + L - 1);
-  const int ctx_end = cs + L;
-  if (p_hi >= kMaxPos || (p_hi >> 4) >= p.max_pages) {
-    if (threadIdx.x == 0 && g == 0 && leader) set_error(p.err, kErrPos);
-    return;
-  }
+  const int cluster = blockIdx.x >> 1, n_clusters = gridDim.x >> 1;
   const int W = p.window;
-  const int k_lo = W > 0 ? max(0, p_lo - W + 1) : 0;
-  const int k_hi = p_hi;
-  const int kt0 = k_lo / kSN;
-  const int n_tiles = k_hi / kSN - kt0 + 1;
-  const int q_row0 = qs + (kBM * t - cs);   // memory row of tile row 0 (may be negative)
-  const int32_t* pt = p.page_table + (size_t)b * p.max_pages;
 
   if (threadIdx.x == 32) {
     for (int s = 0; s < kNK; ++s) {
       mbar_init(&sm.k_full[s], 1);
-      mbar_init(&sm.k_empty[s], 1);   // the even CTA's commits arrive in both CTAs
-      mbar_init(&sm.k_peer[s], 1);    // even CTA: the odd CTA's K half has landed
+      mbar_init(&sm.k_empty[s], 1);   // QK^T commits (both CTAs), or the local Q move
+      mbar_init(&sm.k_peer[s], 1);    // even CTA: the odd CTA's slot has landed
     }
     for (int s = 0; s < kNV; ++s) {
       mbar_init(&sm.v_full[s], 1);
@@ -135,10 +152,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(&sm.s_free, kPairWarps);   // even CTA: both CTAs' softmax warps have read S
     mbar_init(&sm.p_full, kPairWarps);   // even CTA: both CTAs' P is in tensor memory
     mbar_init(&sm.pv_done, 1);
-    mbar_init(&sm.q_full, 1);
-    mbar_init(&sm.q_local, kSoftmaxThreads / 32);   // this CTA's Q dims 0-127 left the K stage
-    mbar_init(&sm.q_pair, kPairWarps);              // even CTA: both CTAs' Q is in tensor memory
-    mbar_init(&sm.teardown, 2);   // on an abort both issuers commit
+    mbar_init(&sm.q_full, 1);            // Q dims 128-255 landed
+    mbar_init(&sm.q_pair, kPairWarps);   // even CTA: both CTAs' Q is in place
+    mbar_init(&sm.q_free, 1);            // the unit's last QK^T is done: Q may be replaced
+    mbar_init(&sm.o_free, kPairWarps);   // even CTA: both CTAs have read O out
+    mbar_init(&sm.q_read, kSoftmaxThreads / 32);   // this CTA's softmax warps have read the Q slot
+    mbar_init(&sm.teardown, 2);          // on an abort both issuers commit
     sm.abort_flag = 0;
     fence_mbar_init();
   }
@@ -158,174 +177,253 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     else
       mbar_arrive_remote(map_peer(smem_u32(bar), 0u));
   };
+  uint32_t k_slots = 0, v_slots = 0;   // ring slots used (warp 0 keeps both for the teardown)
 
   if (warp == 0 || warp == 6) {
     // ------------------------------------------------------------ copy producers
     // Block indices come from the page table ahead of use: lane l holds page (l & 7) of tile
     // (l >> 3) of the current group of 4 tiles; the next group is looked up one group early.
-    // Warp 0 copies this CTA's K pages (4r .. 4r+3 of the tile's 8), lanes 0-3 one page each;
-    // warp 6 the dims half r of every page of the tile, lanes 0-7 one page each.
-    // Pages outside [k_lo, k_hi] are neither looked up nor copied.
+    // Warp 0 copies this CTA's K pages (4r .. 4r+3 of the tile's 8), lanes 0-3 one page each,
+    // and each unit's roped Q tile; warp 6 the dims half r of every page of the tile, lanes
+    // 0-7 one page each. Pages outside [k_lo, k_hi] are neither looked up nor copied.
     const bool is_v = (warp == 6);
-    auto load_blocks = [&](int j0) -> int {
-      const int jt = j0 + (lane >> 3);
-      if (jt >= n_tiles) return -1;
-      return page_block((kt0 + jt) * kSN + (lane & 7) * kPage, k_lo, k_hi, pt, p.num_pages, kSlidingHkv, g, p.err);
-    };
-    if (!is_v && lane == 0) {   // the roped Q tile: 4 boxes of 64 dims x 128 rows (rows outside T read as 0)
-      prefetch_tmap(&tmap_q);
-      mbar_arrive_expect_tx(&sm.q_full, (kSD / 64) * kQChunk);
-#pragma unroll
-      for (int c = 0; c < kSD / 64; ++c)
-        tma_load_3d(c < 2 ? sm.k[kQStage] + c * kQChunk : sm.qhi + (c - 2) * kQChunk, &tmap_q, 64 * c, h, q_row0,
-                    &sm.q_full);
-    }
-    int blk_cur = load_blocks(0), blk_next = load_blocks(4);
     uint64_t* full = is_v ? sm.v_full : sm.k_full;
     uint64_t* empty = is_v ? sm.v_empty : sm.k_empty;
     const int n_st = is_v ? kNV : kNK;
     const bool mine = is_v ? lane < 8 : lane < 4;
     const int pg = is_v ? (lane & 7) : (int)(4 * rank) + (lane & 3);   // page of the tile this lane copies
-    int j = 0;
-    for (; j < n_tiles; ++j) {
-      const int s = j % n_st;
-      if (j > 0 && (j & 3) == 0) {
-        blk_cur = blk_next;
-        blk_next = load_blocks(j + 4);
+    uint32_t c = 0, vt = 0, q_issued = 0;
+    int uq = 0;
+    bool ok = true;
+    if (!is_v && lane == 0) prefetch_tmap(&tmap_q);
+    for (int u = cluster; ok && u < p.n_units; u += n_clusters) {
+      Unit un;
+      if (!sliding_unit(p, u, rank, un)) continue;
+      if (!is_v) {   // the next unit's roped Q tile into L2, a unit ahead of its load
+        Unit nx;
+        if (u + n_clusters < p.n_units && sliding_unit(p, u + n_clusters, rank, nx) && lane == 0) {
+#pragma unroll
+          for (int c2 = 0; c2 < kSD / 64; ++c2) tma_prefetch_l2_3d(&tmap_q, 64 * c2, nx.h, max(nx.q_row0, 0));
+        }
       }
-      const int my_blk = __shfl_sync(0xffffffffu, blk_cur, (j & 3) * 8 + (pg & 7));
-      const unsigned live = __ballot_sync(0xffffffffu, mine && my_blk >= 0);
-      const uint32_t bytes = __popc(live) * (is_v ? kVHalfPageBytes : kPageBytes);
-      bool ok = true;
-      if (lane == 0) {
-        if (!is_v && j == kQStage) ok = mbar_wait(&sm.q_local, 0, abort_flag, p.err);   // Q left the stage
-        if (ok && j >= n_st) ok = mbar_wait(&empty[s], ((j / n_st) - 1) & 1, abort_flag, p.err);
+      auto load_blocks = [&](int j0) -> int {
+        const int jt = j0 + (lane >> 3);
+        if (jt >= un.n_tiles) return -1;
+        return page_block((un.kt0 + jt) * kSN + (lane & 7) * kPage, un.k_lo, un.k_hi, un.pt, p.num_pages,
+                          kSlidingHkv, un.g, p.err);
+      };
+      int blk_cur = load_blocks(0), blk_next = load_blocks(4);
+      const int n_slots = is_v ? un.n_tiles : un.n_tiles + 1;
+      for (int idx = 0; idx < n_slots; ++idx, ++c) {
+        const int s = c % n_st;
+        const bool is_q = !is_v && idx == un.qpos;
+        const int j = (is_v || idx < un.qpos) ? idx : idx - 1;   // key tile of a K/V slot
+        int my_blk = -1;
+        if (!is_q) {
+          if (j > 0 && (j & 3) == 0) {
+            blk_cur = blk_next;
+            blk_next = load_blocks(j + 4);
+          }
+          my_blk = __shfl_sync(0xffffffffu, blk_cur, (j & 3) * 8 + (pg & 7));
+        }
+        const unsigned live = __ballot_sync(0xffffffffu, !is_q && mine && my_blk >= 0);
+        bool okw = true;
+        if (lane == 0) {
+          if (c >= (uint32_t)n_st) okw = mbar_wait_ool(&empty[s], ((c / n_st) - 1) & 1, abort_flag, p.err);
+          // the unit's Q replaces the previous unit's only once that unit's last QK^T is done
+          if (okw && is_q && uq > 0) okw = mbar_wait_ool(&sm.q_free, (uq - 1) & 1, abort_flag, p.err);
+        }
+        if (!__shfl_sync(0xffffffffu, okw, 0)) {
+          ok = false;
+          break;
+        }
+        if (is_q) {
+          if (lane == 0) {   // 4 boxes of 64 dims x 128 rows (rows outside T read as 0)
+            mbar_arrive_expect_tx(&full[s], 2 * kQChunk);
+            mbar_arrive_expect_tx(&sm.q_full, 2 * kQChunk);
+#pragma unroll
+            for (int c2 = 0; c2 < kSD / 64; ++c2)
+              tma_load_3d(c2 < 2 ? sm.k[s] + c2 * kQChunk : sm.qhi + (c2 - 2) * kQChunk, &tmap_q, 64 * c2, un.h,
+                          un.q_row0, c2 < 2 ? &full[s] : &sm.q_full);
+          }
+          ++q_issued;
+        } else {
+          if (lane == 0) mbar_arrive_expect_tx(&full[s], __popc(live) * (is_v ? kVHalfPageBytes : kPageBytes));
+          __syncwarp();
+          if (mine && my_blk >= 0) {
+            if (is_v)   // dims 128r .. 128r+127 of page pg: key groups 2pg, 2pg+1
+              bulk_g2s(sm.v[s] + pg * kVHalfPageBytes,
+                       (const __nv_bfloat16*)p.v_cache + (size_t)my_blk * kPage * kSD + rank * (kVHalfPageBytes / 2),
+                       kVHalfPageBytes, &full[s]);
+            else
+              bulk_g2s(sm.k[s] + (lane & 3) * kPageBytes,
+                       (const __nv_bfloat16*)p.k_cache + (size_t)my_blk * kPage * kSD, kPageBytes, &full[s]);
+          }
+        }
+        __syncwarp();
       }
-      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      if (lane == 0) mbar_arrive_expect_tx(&full[s], bytes);
-      __syncwarp();
-      if (mine && my_blk >= 0) {
-        if (is_v)   // dims 128r .. 128r+127 of page pg: key groups 2pg, 2pg+1
-          bulk_g2s(sm.v[s] + pg * kVHalfPageBytes,
-                   (const __nv_bfloat16*)p.v_cache + (size_t)my_blk * kPage * kSD + rank * (kVHalfPageBytes / 2),
-                   kVHalfPageBytes, &full[s]);
-        else
-          bulk_g2s(sm.k[s] + (lane & 3) * kPageBytes, (const __nv_bfloat16*)p.k_cache + (size_t)my_blk * kPage * kSD,
-                   kPageBytes, &full[s]);
-      }
+      if (!is_v) vt += un.n_tiles;
+      ++uq;
     }
     if (lane == 0 && *abort_flag) {   // drain copies still in flight (bounded) before the CTA may exit
       const unsigned long long w0 = globaltimer();
-      if (!is_v) {
-        while (!mbar_try_wait(smem_u32(&sm.q_full), 0) && globaltimer() - w0 < kWaitLimitNs) {
+      if (q_issued > 0) {
+        while (!mbar_try_wait(smem_u32(&sm.q_full), (q_issued - 1) & 1) && globaltimer() - w0 < kWaitLimitNs) {
         }
       }
-      for (int i = max(0, j - n_st); i < j; ++i) {
+      for (uint32_t i = c > (uint32_t)n_st ? c - n_st : 0; i < c; ++i) {
         while (!mbar_try_wait(smem_u32(&full[i % n_st]), (i / n_st) & 1) && globaltimer() - w0 < kWaitLimitNs) {
         }
       }
     }
     __syncwarp();
+    k_slots = c;
+    v_slots = vt;
   } else if (warp == 1 && !leader) {
     // ------------------------------------------------------------ K relay (odd CTA)
-    if (lane == 0) {
-      for (int j = 0; j < n_tiles; ++j) {
-        const int s = j % kNK;
-        if (!mbar_wait(&sm.k_full[s], (j / kNK) & 1, abort_flag, p.err)) break;
-        mbar_arrive_remote(map_peer(smem_u32(&sm.k_peer[s]), peer));
+    uint32_t c = 0;
+    bool ok = true;
+    for (int u = cluster; ok && u < p.n_units; u += n_clusters) {
+      Unit un;
+      if (!sliding_unit(p, u, rank, un)) continue;
+      for (int idx = 0; idx <= un.n_tiles; ++idx, ++c) {   // every slot, the unit's Q included
+        const int s = c % kNK;
+        ok = __all_sync(0xffffffffu, mbar_wait_ool(&sm.k_full[s], (c / kNK) & 1, abort_flag, p.err));
+        if (!ok) break;
+        if (lane == 0) mbar_arrive_remote(map_peer(smem_u32(&sm.k_peer[s]), peer));
+        __syncwarp();
       }
     }
-    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ QK^T issuer (even CTA)
     // Issuing a group of MMAs blocks for about as long as they run, so QK^T and P.V have one
     // issuer each: neither waits for its operands while the tensor pipe idles. Each commit
-    // tracks its own thread's MMAs only.
-    // Waits are made warp-uniform so that every lane leaves the loop together on an abort.
-    bool ok = __all_sync(0xffffffffu, mbar_wait_cl(&sm.q_pair, 0, abort_flag, p.err));
-    for (int j = 0; ok && j < n_tiles; ++j) {
-      const int s = j % kNK;
-      ok = __all_sync(0xffffffffu, mbar_wait(&sm.k_full[s], (j / kNK) & 1, abort_flag, p.err) &&
-                                       mbar_wait_cl(&sm.k_peer[s], (j / kNK) & 1, abort_flag, p.err) &&
-                                       // the single S buffer: both CTAs' softmax threads have read
-                                       // S_{j-1} into registers
-                                       (j == 0 || mbar_wait_cl(&sm.s_free, (j - 1) & 1, abort_flag, p.err)));
-      if (!ok) break;
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t ka = smem_u32(sm.k[s]);
-        const uint32_t qh = smem_u32(sm.qhi);
+    // tracks its own thread's MMAs only. Waits are warp-uniform, so that every lane leaves the
+    // loops together on an abort.
+    auto slot_ready = [&](uint32_t c) -> bool {   // K ring slot c has landed in both CTAs
+      return mbar_wait_ool(&sm.k_full[c % kNK], (c / kNK) & 1, abort_flag, p.err) &&
+             mbar_wait_cl_ool(&sm.k_peer[c % kNK], (c / kNK) & 1, abort_flag, p.err);
+    };
+    uint32_t c0 = 0, jt = 0;
+    int uq = 0;
+    bool ok = true;
+    for (int u = cluster; ok && u < p.n_units; u += n_clusters) {
+      Unit un;
+      if (!sliding_unit(p, u, rank, un)) continue;
+      // the unit's Q: its slot has landed, and both CTAs' softmax warps have moved dims 0-127
+      ok = __all_sync(0xffffffffu, slot_ready(c0 + un.qpos) && mbar_wait_cl_ool(&sm.q_pair, uq & 1, abort_flag, p.err));
+      for (int j = 0; ok && j < un.n_tiles; ++j, ++jt) {
+        const uint32_t c = c0 + un.kslot(j);
+        const int s = c % kNK;
+        // the single S buffer: both CTAs' softmax threads have read the previous S into registers
+        ok = __all_sync(0xffffffffu,
+                        slot_ready(c) && (jt == 0 || mbar_wait_cl_ool(&sm.s_free, (jt - 1) & 1, abort_flag, p.err)));
+        if (!ok) break;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t ka = smem_u32(sm.k[s]);
+          const uint32_t qh = smem_u32(sm.qhi);
 #pragma unroll
-        for (int k = 0; k < 8; ++k)   // dims 0-127: Q from tensor memory
-          mma2_ts(tm + kTmS, tm + kTmQ + 8 * k, desc_tiled(ka + k * 256, 128, kKeyGroupBytes), kIdescQK, k > 0 ? 1u : 0u);
+          for (int k = 0; k < 8; ++k)   // dims 0-127: Q from tensor memory
+            mma2_ts(tm + kTmS, tm + kTmQ + 8 * k, desc_tiled(ka + k * 256, 128, kKeyGroupBytes), kIdescQK,
+                    k > 0 ? 1u : 0u);
 #pragma unroll
-        for (int k = 8; k < 16; ++k)  // dims 128-255: Q from shared memory
-          mma2_ss(tm + kTmS, desc_sw128(qh + ((k - 8) >> 2) * kQChunk + (k & 3) * 32, 16, 1024),
-                  desc_tiled(ka + k * 256, 128, kKeyGroupBytes), kIdescQK, 1u);
-        mma2_commit_mc(&sm.s_full, kBoth);
-        mma2_commit_mc(&sm.k_empty[s], kBoth);
+          for (int k = 8; k < 16; ++k)  // dims 128-255: Q from shared memory
+            mma2_ss(tm + kTmS, desc_sw128(qh + ((k - 8) >> 2) * kQChunk + (k & 3) * 32, 16, 1024),
+                    desc_tiled(ka + k * 256, 128, kKeyGroupBytes), kIdescQK, 1u);
+          mma2_commit_mc(&sm.s_full, kBoth);
+          mma2_commit_mc(&sm.k_empty[s], kBoth);
+        }
+        __syncwarp();
       }
+      if (!ok) break;
+      if (lane == 0) mma2_commit_mc(&sm.q_free, kBoth);   // done with this unit's Q once these QK^T are
       __syncwarp();
+      c0 += un.n_tiles + 1;
+      ++uq;
     }
   } else if (warp == 7) {
     // ------------------------------------------------------------ V check (both CTAs), P.V issuer (even CTA)
     // Value rows of this CTA's V half for keys that hold no data of this sequence are zeroed
     // before P.V: pages outside the key range were not copied and keep an older tile, and slots
     // past the sequence's last key may hold anything (NaN); P = 0 there does not cancel NaN.
-    for (int i = 0; i < n_tiles; ++i) {
-      const int s = i % kNV;
-      if (!__all_sync(0xffffffffu, mbar_wait(&sm.v_full[s], (i / kNV) & 1, abort_flag, p.err))) break;
-      const int kb = (kt0 + i) * kSN;
-      const int v0 = max(kb, (k_lo >> 4) * kPage), v1 = min(min(kb + kSN, ((k_hi >> 4) + 1) * kPage), ctx_end);
-      if (v0 > kb || v1 < kb + kSN) {
-        for (int idx = lane; idx < kSN * 16; idx += 32) {
-          const int r = idx >> 4, dg = idx & 15;
-          if (kb + r < v0 || kb + r >= v1)
-            *reinterpret_cast<uint4*>(sm.v[s] + ((r >> 3) * 16 + dg) * 128 + (r & 7) * 16) = make_uint4(0, 0, 0, 0);
+    uint32_t cv = 0, jt = 0;
+    int uq = 0;
+    bool ok = true;
+    for (int u = cluster; ok && u < p.n_units; u += n_clusters) {
+      Unit un;
+      if (!sliding_unit(p, u, rank, un)) continue;
+      for (int i = 0; i < un.n_tiles; ++i, ++cv, ++jt) {
+        const int s = cv % kNV;
+        ok = __all_sync(0xffffffffu, mbar_wait_ool(&sm.v_full[s], (cv / kNV) & 1, abort_flag, p.err));
+        if (!ok) break;
+        const int kb = (un.kt0 + i) * kSN;
+        const int v0 = max(kb, (un.k_lo >> 4) * kPage);
+        const int v1 = min(min(kb + kSN, ((un.k_hi >> 4) + 1) * kPage), un.ctx_end);
+        if (v0 > kb || v1 < kb + kSN) {
+          for (int idx = lane; idx < kSN * 16; idx += 32) {
+            const int r = idx >> 4, dg = idx & 15;
+            if (kb + r < v0 || kb + r >= v1)
+              *reinterpret_cast<uint4*>(sm.v[s] + ((r >> 3) * 16 + dg) * 128 + (r & 7) * 16) = make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async();
         }
-        fence_proxy_async();
-      }
-      __syncwarp();
-      if (!leader) {
-        if (lane == 0) mbar_arrive_remote(map_peer(smem_u32(&sm.v_ready[s]), peer));
-        continue;
-      }
-      if (!__all_sync(0xffffffffu, mbar_wait_cl(&sm.p_full, i & 1, abort_flag, p.err) &&
-                                       mbar_wait_cl(&sm.v_ready[s], (i / kNV) & 1, abort_flag, p.err)))
-        break;
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t va = smem_u32(sm.v[s]);
+        __syncwarp();
+        if (!leader) {
+          if (lane == 0) mbar_arrive_remote(map_peer(smem_u32(&sm.v_ready[s]), peer));
+          __syncwarp();
+          continue;
+        }
+        // P_i is in place in both CTAs, the odd CTA's V half is ready, and (first tile of a
+        // unit) the previous unit's O has been read out before this P.V overwrites it
+        ok = __all_sync(0xffffffffu, mbar_wait_cl_ool(&sm.p_full, jt & 1, abort_flag, p.err) &&
+                                         mbar_wait_cl_ool(&sm.v_ready[s], (cv / kNV) & 1, abort_flag, p.err) &&
+                                         (i > 0 || uq == 0 || mbar_wait_cl_ool(&sm.o_free, (uq - 1) & 1, abort_flag, p.err)));
+        if (!ok) break;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t va = smem_u32(sm.v[s]);
 #pragma unroll
-        for (int k = 0; k < kSN / 16; ++k)   // 16 keys (two key groups) per step
-          mma2_ts(tm + kTmO, tm + kTmP + 8 * k, desc_tiled(va + k * 2 * kVGroupBytes, kVGroupBytes, 128), kIdescPV,
-                  (i > 0 || k > 0) ? 1u : 0u);
-        mma2_commit_mc(&sm.pv_done, kBoth);
-        mma2_commit_mc(&sm.v_empty[s], kBoth);
+          for (int k = 0; k < kSN / 16; ++k)   // 16 keys (two key groups) per step
+            mma2_ts(tm + kTmO, tm + kTmP + 8 * k, desc_tiled(va + k * 2 * kVGroupBytes, kVGroupBytes, 128), kIdescPV,
+                    (i > 0 || k > 0) ? 1u : 0u);
+          mma2_commit_mc(&sm.pv_done, kBoth);
+          mma2_commit_mc(&sm.v_empty[s], kBoth);
+        }
+        __syncwarp();
       }
-      __syncwarp();
+      ++uq;
     }
-  } else if (warp >= 2 && warp <= 5) {
+  } else {
     // ------------------------------------------------------------ softmax / epilogue warps
     const int r = 32 * (warp & 3) + lane;   // query row = tensor-memory lane
     const uint32_t tq = tm + tmem_lane_base(warp);
-    const int pos = kBM * t + r;
-    const bool row_ok = pos >= p_lo && pos <= p_hi;
-
-    // Q: the producer's TMA brought the roped tile in (4 chunks of 64 dims, 128B swizzle);
-    // dims 0-127 sit in K stage 2 and each thread moves its row of them into tensor memory (an A
-    // operand in bf16 pairs), which frees the stage for keys. Dims 128-255 stay in shared memory
-    // as the A operand of the other half of the QK^T k-steps.
-    {
-      const bool okq = mbar_wait(&sm.q_full, 0, abort_flag, p.err);
-      const uint8_t* qrow = sm.k[kQStage] + r * 128;
+    const float cl2 = p.scale_log2;
+    uint32_t c0 = 0, jt = 0;
+    int uq = 0, u = cluster - n_clusters;
+    bool ok = true;
+    auto next_unit = [&](Unit& o) -> bool {   // this cluster's next unit with rows (warp-wide)
+      for (u += n_clusters; u < p.n_units; u += n_clusters)
+        if (sliding_unit(p, u, rank, o)) return true;
+      return false;
+    };
+    // Q dims 0-127 of unit o (the roped tile the producer put in K ring slot c0o + qpos, 128B
+    // swizzle) into tensor memory as bf16 pairs: the A operand of half of the QK^T k-steps. The
+    // load was issued only after the previous unit's last QK^T, so the columns are free. Once
+    // all four warps have read the slot, one thread releases it.
+    auto move_q = [&](const Unit& o, uint32_t c0o, int uqo) -> bool {
+      const uint32_t cq = c0o + o.qpos;
+      const int s = cq % kNK;
+      if (!__all_sync(0xffffffffu, mbar_wait_ool(&sm.k_full[s], (cq / kNK) & 1, abort_flag, p.err) &&
+                                       mbar_wait_ool(&sm.q_full, uqo & 1, abort_flag, p.err)))
+        return false;
+      const uint8_t* qrow = sm.k[s] + r * 128;
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t w[32];
 #pragma unroll
         for (int q8 = 0; q8 < 8; ++q8) {
-          const uint4 v = okq ? *reinterpret_cast<const uint4*>(qrow + c * kQChunk + ((q8 ^ (r & 7)) * 16))
-                              : make_uint4(0, 0, 0, 0);
+          const uint4 v = *reinterpret_cast<const uint4*>(qrow + c * kQChunk + ((q8 ^ (r & 7)) * 16));
           w[4 * q8] = v.x;
           w[4 * q8 + 1] = v.y;
           w[4 * q8 + 2] = v.z;
@@ -337,149 +435,161 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(&sm.q_local);
         arrive_leader(&sm.q_pair);
+        mbar_arrive(&sm.q_read);
       }
-    }
+      bool okr = true;
+      if (threadIdx.x == 64) {
+        okr = mbar_wait_ool(&sm.q_read, uqo & 1, abort_flag, p.err);
+        if (okr) mbar_arrive(&sm.k_empty[s]);
+      }
+      return __shfl_sync(0xffffffffu, okr, 0);
+    };
 
-    const float cl2 = p.scale_log2;
-    float m_used = -INFINITY, l_run = 0.f;
-    bool ok = true;
-    for (int j = 0; j < n_tiles; ++j) {
-      const int kb = (kt0 + j) * kSN;
-      // Waits are made warp-uniform so that every lane leaves the loop together on an abort.
-      if (!__all_sync(0xffffffffu, mbar_wait(&sm.s_full, j & 1, abort_flag, p.err))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      uint32_t sr[kSN];
-#pragma unroll
-      for (int c = 0; c < kSN / 32; ++c) tmem_ld32(tq + kTmS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) arrive_leader(&sm.s_free);   // S may now be overwritten by QK^T of tile j+1
-
-      float s[kSN];
-#pragma unroll
-      for (int c = 0; c < kSN; ++c) s[c] = __uint_as_float(sr[c]);
-      const bool full = row_ok && kb + kSN - 1 <= pos && (W == 0 || pos - kb <= W - 1);
-      if (!full) {   // the row's visible keys in this tile are one run of columns [lo, hi]
-        int lo = W > 0 ? max(0, pos - W + 1 - kb) : 0;
-        int hi = row_ok ? min(kSN - 1, pos - kb) : -1;
-        if (hi < lo) lo = hi = 1 << 20;   // none
-        const unsigned span = (unsigned)(hi - lo);
-#pragma unroll
-        for (int c = 0; c < kSN; ++c) s[c] = ((unsigned)(c - lo) <= span) ? s[c] : -INFINITY;
-      }
-      float mx[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        mx[i] = s[i];
-#pragma unroll
-        for (int c = 1; c < kSN / 8; ++c) mx[i] = fmaxf(mx[i], s[i + 8 * c]);
-      }
-      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * cl2;
-      float alpha = 1.f;
-      bool need_o = false;
-      if (mt > m_used + kLazyRescale) {
-        need_o = (m_used != -INFINITY);
-        alpha = ex2(m_used - mt);
-        m_used = mt;
-      }
-      const float neg_m = (m_used == -INFINITY) ? 0.f : -m_used;
-      uint32_t pw[kSN / 2];
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int w = 0; w < kSN / 2; ++w) {
-        const float e0 = ex2(fmaf(s[2 * w], cl2, neg_m));
-        const float e1 = ex2(fmaf(s[2 * w + 1], cl2, neg_m));
-        ls[w & 3] += e0;
-        ls[w & 3] += e1;
-        pw[w] = pack_bf16(e0, e1);   // declared cast: P in bf16 for P.V
-      }
-      l_run = fmaf(l_run, alpha, (ls[0] + ls[1]) + (ls[2] + ls[3]));
-
-      // P_{j-1} V_{j-1} has completed: the P buffer is free and O holds every earlier tile.
-      if (j > 0 &&
-          !__all_sync(0xffffffffu, mbar_wait(&sm.pv_done, (j - 1) & 1, abort_flag, p.err))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      if (__any_sync(0xffffffffu, need_o)) {   // O correction (rows whose max rose by more than 2^8)
-        const float a = need_o ? alpha : 1.f;
-#pragma unroll 1
-        for (int cc = 0; cc < kSD / 32; ++cc) {
-          uint32_t o[32];
-          tmem_ld32(tq + kTmO + 32 * cc, o);
-          tmem_ld_wait();
-#pragma unroll
-          for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * a);
-          tmem_st32(tq + kTmO + 32 * cc, o);
+    Unit cur;
+    bool have = next_unit(cur);
+    if (have) ok = move_q(cur, c0, uq);
+    while (ok && have) {
+      const int pos = kBM * cur.t + r;
+      const bool row_ok = pos >= cur.p_lo && pos <= cur.p_hi;
+      float m_used = -INFINITY, l_run = 0.f;
+      for (int j = 0; j < cur.n_tiles; ++j, ++jt) {
+        const int kb = (cur.kt0 + j) * kSN;
+        // Waits are made warp-uniform so that every lane leaves the loop together on an abort.
+        if (!__all_sync(0xffffffffu, mbar_wait_ool(&sm.s_full, jt & 1, abort_flag, p.err))) {
+          ok = false;
+          break;
         }
-      }
-      // P_j (bf16 key pairs): the A operand of P.V.
-      tmem_st32(tq + kTmP, *reinterpret_cast<const uint32_t(*)[32]>(&pw[0]));
-      tmem_st32(tq + kTmP + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pw[32]));
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) arrive_leader(&sm.p_full);
-    }
+        tc_fence_after();
+        uint32_t sr[kSN];
+#pragma unroll
+        for (int c = 0; c < kSN / 32; ++c)
+          tmem_ld32(tq + kTmS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) arrive_leader(&sm.s_free);   // S may now be overwritten by the next QK^T
 
-    // Epilogue: O / l -> bf16, rows of this sequence only. A tile whose 128 rows all belong to
-    // this sequence is staged in shared memory (the K ring, free by now) in the 128B-swizzled
-    // layout of the query tensor map and written by four TMA stores; any other tile is written
-    // row by row, so that rows of other sequences or padding are never touched.
-    const bool tile_full = p_lo == kBM * t && p_hi == kBM * t + kBM - 1;
-    const bool ep_ok = ok && __all_sync(0xffffffffu, mbar_wait(&sm.pv_done, (n_tiles - 1) & 1, abort_flag, p.err));
-    if (ep_ok) {
+        float s[kSN];
+#pragma unroll
+        for (int c = 0; c < kSN; ++c) s[c] = __uint_as_float(sr[c]);
+        const bool full = row_ok && kb + kSN - 1 <= pos && (W == 0 || pos - kb <= W - 1);
+        if (!full) {   // the row's visible keys in this tile are one run of columns [lo, hi]
+          int lo = W > 0 ? max(0, pos - W + 1 - kb) : 0;
+          int hi = row_ok ? min(kSN - 1, pos - kb) : -1;
+          if (hi < lo) lo = hi = 1 << 20;   // none
+          const unsigned span = (unsigned)(hi - lo);
+#pragma unroll
+          for (int c = 0; c < kSN; ++c) s[c] = ((unsigned)(c - lo) <= span) ? s[c] : -INFINITY;
+        }
+        float mx[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          mx[i] = s[i];
+#pragma unroll
+          for (int c = 1; c < kSN / 8; ++c) mx[i] = fmaxf(mx[i], s[i + 8 * c]);
+        }
+        const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * cl2;
+        float alpha = 1.f;
+        bool need_o = false;
+        if (mt > m_used + kLazyRescale) {
+          need_o = (m_used != -INFINITY);
+          alpha = ex2(m_used - mt);
+          m_used = mt;
+        }
+        const float neg_m = (m_used == -INFINITY) ? 0.f : -m_used;
+        uint32_t pw[kSN / 2];
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int w = 0; w < kSN / 2; ++w) {
+          const float e0 = ex2(fmaf(s[2 * w], cl2, neg_m));
+          const float e1 = ex2(fmaf(s[2 * w + 1], cl2, neg_m));
+          ls[w & 3] += e0;
+          ls[w & 3] += e1;
+          pw[w] = pack_bf16(e0, e1);   // declared cast: P in bf16 for P.V
+        }
+        l_run = fmaf(l_run, alpha, (ls[0] + ls[1]) + (ls[2] + ls[3]));
+
+        // The previous P.V has completed: the P buffer is free and O holds every earlier tile.
+        if (jt > 0 && !__all_sync(0xffffffffu, mbar_wait_ool(&sm.pv_done, (jt - 1) & 1, abort_flag, p.err))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, need_o)) {   // O correction (rows whose max rose by more than 2^8)
+          const float a = need_o ? alpha : 1.f;
+#pragma unroll 1
+          for (int cc = 0; cc < kSD / 32; ++cc) {
+            uint32_t o[32];
+            tmem_ld32(tq + kTmO + 32 * cc, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * a);
+            tmem_st32(tq + kTmO + 32 * cc, o);
+          }
+        }
+        // P_j (bf16 key pairs): the A operand of P.V.
+        tmem_st32(tq + kTmP, *reinterpret_cast<const uint32_t(*)[32]>(&pw[0]));
+        tmem_st32(tq + kTmP + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pw[32]));
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) arrive_leader(&sm.p_full);
+      }
+      if (!ok) break;
+
+      // The next unit's Q goes into tensor memory now (this unit's QK^T are all done), so that
+      // its first QK^T runs while this unit's O is written out.
+      Unit nxt;
+      const bool have_n = next_unit(nxt);
+      const uint32_t c0n = c0 + cur.n_tiles + 1;
+      if (have_n && !move_q(nxt, c0n, uq + 1)) {
+        ok = false;
+        break;
+      }
+
+      // Epilogue: O / l -> bf16, rows of this sequence only. Once O is in registers the even
+      // CTA may start the next unit's P.V, which overwrites it.
+      if (!__all_sync(0xffffffffu, mbar_wait_ool(&sm.pv_done, (jt - 1) & 1, abort_flag, p.err))) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
       const float inv = (l_run > 0.f) ? __frcp_rn(l_run) : 0.f;
-      __nv_bfloat16* orow = p.out + ((size_t)(q_row0 + r) * kSlidingHq + h) * kSD;
-      uint8_t* stage = sm.k[0];   // 4 boxes of 128 rows x 64 dims (16 KB each)
+      __nv_bfloat16* orow = p.out + ((size_t)(cur.q_row0 + r) * kSlidingHq + cur.h) * kSD;
 #pragma unroll 1
       for (int cc = 0; cc < kSD / 32; ++cc) {
         uint32_t o[32];
         tmem_ld32(tq + kTmO + 32 * cc, o);
         tmem_ld_wait();
+        if (cc == kSD / 32 - 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) arrive_leader(&sm.o_free);
+        }
         uint32_t w16[16];
 #pragma unroll
         for (int c = 0; c < 16; ++c)
           w16[c] = pack_bf16(__uint_as_float(o[2 * c]) * inv, __uint_as_float(o[2 * c + 1]) * inv);
-        if (tile_full) {
-          uint8_t* box = stage + (cc >> 1) * kQChunk + r * 128;
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            *reinterpret_cast<uint4*>(box + ((((cc & 1) * 4 + i) ^ (r & 7)) * 16)) =
-                make_uint4(w16[4 * i], w16[4 * i + 1], w16[4 * i + 2], w16[4 * i + 3]);
-        } else if (row_ok) {
+        if (row_ok) {
           uint4* dst = reinterpret_cast<uint4*>(orow + 32 * cc);
 #pragma unroll
           for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w16[4 * i], w16[4 * i + 1], w16[4 * i + 2], w16[4 * i + 3]);
         }
       }
-    }
-    if (tile_full) {   // every softmax thread gets here, so the named barrier cannot hang
-      fence_proxy_async();
-      if (named_barrier_and(1, kSoftmaxThreads, ep_ok) && threadIdx.x == 64) {
-#pragma unroll
-        for (int c = 0; c < kSD / 64; ++c) tma_store_3d(&tmap_q, sm.k[0] + c * kQChunk, 64 * c, h, q_row0);
-        bulk_commit_group();
-        bulk_wait_group_read0();
-      }
-      __syncwarp();
+      c0 = c0n;
+      ++uq;
+      cur = nxt;
+      have = have_n;
     }
   }
 
   // ------------------------------------------------------------ teardown
   // Neither CTA may free its tensor memory or leave while the pair's MMAs or signals into it
-  // are in flight: each waits (bounded) for the last stage releases it was sent, an abort is
-  // passed to the peer so that its waits end early, and a cluster barrier closes the pair.
-  // Aligned CTA barriers count whole warps: every warp arrives converged.
+  // are in flight: each waits (bounded) for the last stage releases and the last Q release it
+  // was sent, an abort is passed to the peer so that its waits end early, and a cluster barrier
+  // closes the pair. Aligned CTA barriers count whole warps: every warp arrives converged.
   __syncwarp();
   tc_fence_before();
   __syncthreads();
@@ -488,16 +598,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       st_peer_u32(map_peer(smem_u32(&sm.abort_flag), peer), 1u);
     } else {
       const unsigned long long w0 = globaltimer();
-      for (int s = 0; s < kNK && s < n_tiles; ++s) {
-        const int j_last = s + kNK * ((n_tiles - 1 - s) / kNK);
-        while (!mbar_try_wait(smem_u32(&sm.k_empty[s]), (uint32_t)(j_last / kNK) & 1u) &&
-               globaltimer() - w0 < kWaitLimitNs) {
+      for (uint32_t s = 0; s < (uint32_t)kNK && s < k_slots; ++s) {
+        const uint32_t last = s + kNK * ((k_slots - 1 - s) / kNK);
+        while (!mbar_try_wait(smem_u32(&sm.k_empty[s]), (last / kNK) & 1u) && globaltimer() - w0 < kWaitLimitNs) {
         }
       }
-      for (int s = 0; s < kNV && s < n_tiles; ++s) {
-        const int j_last = s + kNV * ((n_tiles - 1 - s) / kNV);
-        while (!mbar_try_wait(smem_u32(&sm.v_empty[s]), (uint32_t)(j_last / kNV) & 1u) &&
-               globaltimer() - w0 < kWaitLimitNs) {
+      for (uint32_t s = 0; s < (uint32_t)kNV && s < v_slots; ++s) {
+        const uint32_t last = s + kNV * ((v_slots - 1 - s) / kNV);
+        while (!mbar_try_wait(smem_u32(&sm.v_empty[s]), (last / kNV) & 1u) && globaltimer() - w0 < kWaitLimitNs) {
+        }
+      }
+      const uint32_t units = k_slots - v_slots;   // each unit takes one K ring slot more than V
+      if (units > 0) {
+        while (!mbar_try_wait(smem_u32(&sm.q_free), (units - 1) & 1u) && globaltimer() - w0 < kWaitLimitNs) {
         }
       }
     }
@@ -541,18 +654,38 @@ cudaError_t launch_prefill(bool global, const SeqRows& rows, int window, float s
   CUtensorMap mq;
   if (!q_map(&mq, out, rows.T, kSlidingHq, kSD)) return cudaErrorInvalidValue;
   static bool attr[64] = {};
+  static int max_clusters[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr[dev]) {
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr[dev]) {
     cudaError_t e =
         cudaFuncSetAttribute(prefill_sliding_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSlidingSmemBytes);
     if (e != cudaSuccess) return e;
+    // clusters that fit on the device at once: the persistent grid
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSlidingSmemBytes;
+    cudaLaunchAttribute la[1];
+    la[0].id = cudaLaunchAttributeClusterDimension;
+    la[0].val.clusterDim.x = 2;
+    la[0].val.clusterDim.y = 1;
+    la[0].val.clusterDim.z = 1;
+    cfg.attrs = la;
+    cfg.numAttrs = 1;
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, prefill_sliding_kernel, &cfg);
+    if (e != cudaSuccess) return e;
+    max_clusters[dev] = n > 0 ? n : 1;
     attr[dev] = true;
   }
   const long long slots = (long long)rows.T / kBM + 2LL * rows.B;
-  const long long blocks = slots * kSlidingHkv * 2;   // a pair of CTAs (two query heads) per (query tile, KV head)
-  if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-  prefill_sliding_kernel<<<(unsigned)blocks, kThreads, kSlidingSmemBytes, s>>>(mq, p);
+  const long long n_units = slots * kSlidingHkv;   // (query tile, KV head) units, one per cluster at a time
+  if (n_units <= 0 || n_units > 0x3fffffffLL) return cudaErrorInvalidValue;
+  p.n_units = (int)n_units;
+  const int n_clusters = (int)(n_units < max_clusters[dev] ? n_units : max_clusters[dev]);
+  prefill_sliding_kernel<<<2u * (unsigned)n_clusters, kThreads, kSlidingSmemBytes, s>>>(mq, p);
   return cudaGetLastError();
 }
 

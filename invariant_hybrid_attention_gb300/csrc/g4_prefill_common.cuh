@@ -26,6 +26,7 @@ struct PrefillParams {
   __nv_bfloat16* out;
   RopeTables tb;
   uint32_t* err;
+  int n_units;              // persistent sliding kernel: (query tile, KV head) units of the batch
 };
 
 // Finds this CTA's (sequence, query tile) among all sequences' tiles: slot s of sequence b
