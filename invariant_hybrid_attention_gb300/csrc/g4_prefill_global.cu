@@ -3,25 +3,36 @@
 // global_attention_core and global_k_eq_v_projection; section 2: proportional p-RoPE, partial
 // factor 0.25, theta 1e6).
 //
-// A 128 x 512 fp32 output tile fills all of one SM's tensor memory, so each (query tile, head)
-// runs on a cluster of two CTAs, each owning half of the head dims (rank r: dims 256r ..
-// 256r+255):
-//   - S_r = Q[:, half r] . K[:, half r]^T on the CTA's tensor cores; the two partial score
-//     tiles are exchanged through distributed shared memory in 32-key halves (each warp stages
-//     its 32 rows of a half and one bulk copy carries them to the peer), one half ahead of the
-//     softmax, and both CTAs add them (IEEE addition commutes, so both hold the same S bits)
-//     and run the same softmax;
-//   - O[:, half r] += P . V[:, half r], V being the CTA's half of the un-rotated S tile: one
-//     copy of each stored half-page serves V and the un-rotated 3/4 of K;
-//   - the rotated quarter of K comes from the cache's k_rot side pages (p-RoPE(S), written
-//     with S by the append pass), so no CTA re-rotates key tiles.
-// Key tiles of 64 keys are aligned to absolute key 0 and visited in ascending order, query
-// tiles are aligned to absolute position (section 4 rules 2, 3 and 6).
+// A 128 x 512 fp32 output tile fills all 512 tensor-memory columns of one SM, so no SM can hold
+// both the output of its rows and their scores. The work of one unit, (sequence, 128-row query
+// tile, pair of query heads 2i, 2i+1 of one KV head), is therefore split over a cluster of four
+// CTAs forming two 2-SM MMA pairs:
+//   - the score pair (ranks 0, 1; rank r owns head 2i + r): S = Q K^T as one cta_group::2 MMA
+//     over both heads (M = 256, N = 128 keys, K = 512 dims; each CTA stages 64 keys of every
+//     key tile, all dims), then the online softmax of its head's rows. Each CTA sends its bf16 P
+//     tile and per-row (alpha, l) to the output CTA of its head by bulk copies into that CTA's
+//     shared memory;
+//   - the output pair (ranks 2, 3; rank 2 + r owns head 2i + r): O += P V as one cta_group::2
+//     MMA (M = 256, N = 256 dims per instruction, two instructions per 16-key step), V being the
+//     stored un-rotated S (each CTA stages its 256-dim half of every key). Its warps apply the
+//     lazy O rescale that alpha asks for and write the output.
+// The rotated quarter of K comes from the cache's k_rot side pages (p-RoPE(S), written with S by
+// the append pass); the un-rotated dims of K and all of V come from the same stored S pages.
+// Key tiles of 128 keys are aligned to absolute key 0 and visited in ascending order, query
+// tiles to absolute position; every row's arithmetic depends only on its own position and its
+// sequence's keys (section 4 rules 2, 3 and 6).
 //
-// Per CTA: warp 0 copies (roped Q tile by TMA; per key tile one 8 KB S half-page and one 2 KB
-// rotated half-page per page, 4-stage ring), warp 1 issues the MMAs, warps 2-5 run the
-// exchange, mask, online softmax, P (bf16, into tensor memory) and the epilogue.
-// Tensor memory: O half [0,256), Q dims 0-127 of the half [256,320), three S/P buffers [320,512).
+// Score CTA warps: 0 copies the roped Q tile (TMA) and this CTA's K half of each key tile into a
+// 3-stage ring; 1 issues QK^T (rank 0) or tells rank 0 that its ring slot has landed (rank 1);
+// 2-5 move Q into tensor memory, then run mask, online softmax and P (one thread per row).
+// Output CTA warps: 0 copies this CTA's V half of each 64-key half tile into a 4-stage ring;
+// 1 zeroes value rows that hold no key of the sequence, then issues P.V (rank 2) or tells rank
+// 2 that its half is ready (rank 3); 2-5 check alpha, rescale O when asked, and write the
+// output; 6 hands P slots back to the score CTA once P.V has read them.
+// Tensor memory, score CTAs: Q [0,256) as bf16 pairs, two S buffers [256,384), [384,512).
+// Output CTAs: O [0,512), where column c holds dim c for c < 128 or c >= 384, dim c + 128 for
+// 128 <= c < 256 and dim c - 128 for 256 <= c < 384 (each instruction's N = 256 columns are
+// 128 dims of rank 2's half followed by the same 128 dims of rank 3's half).
 #include <math.h>
 
 #include "g4_prefill_common.cuh"
@@ -32,366 +43,334 @@ namespace {
 
 using namespace pf;
 
-constexpr int kGD = kGlobalD;                          // 512
-constexpr int kHalf = kGD / 2;                         // dims per CTA
-constexpr int kNS = 4;                                 // key-tile ring stages
-constexpr int kXCols = kBN / 2;                        // partial scores cross the pair in 32-key halves
-constexpr int kNSP = 3;                                // S/P buffers
-constexpr int kHalfPageBytes = kPage * kHalf * 2;      // 8 KB
-constexpr int kRotHalfPageBytes = kPage * kGlobalR * 2;   // 2 KB
-constexpr int kKG = 8 * kHalf * 2;                     // S half tile: bytes per key group (4 KB)
-constexpr int kRotKG = 8 * kGlobalR * 2;               // rotated tile: bytes per key group (1 KB)
-constexpr int kSTile = (kBN / kPage) * kHalfPageBytes;       // 32 KB
-constexpr int kRotTile = (kBN / kPage) * kRotHalfPageBytes;  // 8 KB
-constexpr int kStage = kSTile + kRotTile;              // 40 KB
-constexpr int kThreads = 64 + kSoftmaxThreads;
-constexpr uint32_t kTmO = 0, kTmQ = 256, kTmS = 320;
-constexpr uint32_t kIdescQK = idesc_bf16(kBM, kBN, false, false);
-constexpr uint32_t kIdescPV = idesc_bf16(kBM, kHalf, false, true);
+constexpr int kGD = kGlobalD;       // 512
+constexpr int kHalf = kGD / 2;      // 256
+constexpr int kTN = 128;            // keys per tile: N of QK^T over the score pair
+constexpr int kVN = 64;             // keys per V stage
+constexpr int kNK = 3;              // K ring stages (score CTAs)
+constexpr int kNV = 4;              // V ring stages (output CTAs)
+constexpr int kNP = 2;              // S buffers (score CTAs) and P slots (output CTAs)
+constexpr int kThreads = 224;
+constexpr uint16_t kScorePair = 0x3, kOutPair = 0xC;
 
-struct GlobalSmem {
-  uint8_t st[kNS][kStage];          // S half tile (V; K outside the rotated columns), rotated tile;
-                                    // st[2] first holds Q dims 0-127 of the half
-  uint8_t qhi[2 * kQChunk];         // Q dims 128-255 of the half (128B swizzle): an A operand
-  float xbuf[2][kBM][kXCols];       // partial scores by 32-key half h: the peer's half h lands in
-                                    // xbuf[h & 1]; this CTA's own half h is staged in xbuf[(h + 1) & 1]
-  uint64_t full[kNS], empty[kNS];
-  uint64_t s_full[kNSP], p_full[kNSP], pv_done[kNSP];
-  uint64_t xfull[2];
-  uint64_t q_full, q_ready, peer_done, teardown;
+// Score-CTA K stage: this CTA's 64 keys of a tile, all 512 dims, per dim half h:
+//   dims 64..255 of the half (from S): [key group (8)][dim group 8..31 (24)][8][8] at h * kUnrotHalf,
+//   dims 0..63 of the half (from k_rot): [key group (8)][dim group (8)][8][8] at kRotOff + h * kRotHalf.
+constexpr int kUnrotKG = 24 * 128;               // 3 KB
+constexpr int kUnrotHalf = 8 * kUnrotKG;         // 24 KB
+constexpr int kRotKG = 8 * 128;                  // 1 KB
+constexpr int kRotHalf = 8 * kRotKG;             // 8 KB
+constexpr int kRotOff = 2 * kUnrotHalf;          // 48 KB
+constexpr int kKStage = kRotOff + 2 * kRotHalf;  // 64 KB
+constexpr int kKPageBytes = kKStage / 4;         // 16 KB: one page's share of a stage
+constexpr int kQOff = kKStage;                   // roped Q, 8 boxes of 64 dims x 128 rows: K stages 1-2
+// P tile of one head: [row group (16)][key group (16)][8 rows][8 keys] bf16; aux: (alpha, l) per row.
+constexpr int kPBytes = kBM * kTN * 2;           // 32 KB
+constexpr int kPWarpBytes = kPBytes / 4;         // 8 KB: the rows of one softmax warp
+constexpr int kAuxBytes = kBM * 8;               // 1 KB
+constexpr int kAuxWarpBytes = kAuxBytes / 4;     // 256 B
+constexpr int kPSlot = kPBytes + kAuxBytes;      // 33 KB
+constexpr uint32_t kPSendBytes = kPSlot;         // bytes one tile's copies deliver into a P slot
+// Output-CTA V stage: 64 keys x this CTA's 256 dims: [key group (8)][dim group (32)][8][8].
+constexpr int kVKG = 32 * 128;                   // 4 KB
+constexpr int kVStage = 8 * kVKG;                // 32 KB
+constexpr int kVPageBytes = 2 * kVKG;            // 8 KB: one page's half-block
+// Byte offsets in the data area. Score CTAs: K ring [0, 192K), P staging, aux staging.
+// Output CTAs: V ring [0, 128K), two P slots.
+constexpr int kSOffStage = kNK * kKStage;
+constexpr int kSOffAux = kSOffStage + kPBytes;
+constexpr int kOOffP = kNV * kVStage;
+constexpr int kDataBytes = kSOffAux + kAuxBytes;   // 225 KB
+static_assert(kOOffP + kNP * kPSlot <= kDataBytes, "output CTA layout exceeds the data area");
+static_assert(kQOff + 8 * kQChunk <= kNK * kKStage, "Q must fit in K stages 1-2");
+
+constexpr uint32_t kTmQ = 0, kTmS = 256, kTmO = 0;
+constexpr uint32_t kIdescQK = idesc_bf16(2 * kBM, kTN, false, false);   // M 256 over the pair, N 128 keys
+constexpr uint32_t kIdescPV = idesc_bf16(2 * kBM, 256, false, true);    // M 256, N 256 dims
+
+struct Bars {
+  // score CTAs
+  uint64_t k_full[kNK], k_empty[kNK], k_peer[kNK];
+  uint64_t s_full[kNP], s_free[kNP], p_free[kNP];
+  uint64_t q_full, q_moved, q_pair, stg_free;
+  // output CTAs
+  uint64_t v_full[kNV], v_empty[kNV], v_ready[kNV];
+  uint64_t p_full[kNP], o_ready[kNP], pv_done[kNP];
+  uint64_t teardown;
   uint32_t tmem_base;
   int abort_flag;
   int unit_b, unit_t;
+  int p_seen[kNP];   // output CTAs: phases of each P slot consumed (for the abort drain)
 };
-static_assert(2 * kQChunk <= kStage, "Q dims 0-127 must fit in one ring stage");
+
+struct GlobalSmem {
+  uint8_t data[kDataBytes];
+  Bars bar;
+};
 constexpr size_t kGlobalSmemBytes = sizeof(GlobalSmem) + 1024;
 static_assert(kGlobalSmemBytes <= 232448, "global prefill exceeds the 227 KB shared-memory limit");
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+// Output-CTA tensor-memory column -> head dim (see the header).
+__device__ __forceinline__ int o_dim(int col) {
+  return (col < 128 || col >= 384) ? col : (col < 256 ? col + 128 : col - 128);
+}
+
+__global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
     prefill_global_kernel(const __grid_constant__ CUtensorMap tmap_q, PrefillParams p) {
   extern __shared__ uint8_t smem_raw[];
   GlobalSmem& sm = *reinterpret_cast<GlobalSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* const base = sm.data;
+  Bars& bar = sm.bar;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_rank();   // which half of the head dims
-  const uint32_t peer = rank ^ 1u;
-  const int unit = blockIdx.x >> 1;
-  const int h = unit % kGlobalHq;
-  const int slot = unit / kGlobalHq;
-  const int g = h / (kGlobalHq / kGlobalHkv);
+  const uint32_t rank = cluster_rank();
+  const bool is_out = rank >= 2;
+  const uint32_t pr = rank & 1u;             // which head of the pair
+  const uint32_t pair_peer = rank ^ 1u;      // the other CTA of this MMA pair
+  const uint32_t partner = rank ^ 2u;        // score CTA r <-> output CTA r + 2 (same head)
+  const bool leader = pr == 0;               // issues the pair's MMAs
+  const int unit = blockIdx.x >> 2;
+  const int hp = unit % (kGlobalHq / 2);
+  const int slot = unit / (kGlobalHq / 2);
+  const int h = 2 * hp + (int)pr;
+  const int g = h / (kGlobalHq / kGlobalHkv);   // both heads of the pair share KV head g
 
   if (warp == 0) {
     int ub, ut;
     find_unit(p.rows, slot, ub, ut);
     if (lane == 0) {
-      sm.unit_b = ub;
-      sm.unit_t = ut;
+      bar.unit_b = ub;
+      bar.unit_t = ut;
     }
   }
   __syncthreads();
-  const int b = sm.unit_b;   // both CTAs of the pair find the same unit
+  const int b = bar.unit_b;   // all four CTAs find the same unit
   if (b < 0) return;
-  const int t = sm.unit_t;
+  const int t = bar.unit_t;
   const int cs = p.rows.ctx_start[b], L = p.rows.q_len[b], qs = p.rows.q_start[b];
   const int p_lo = max(kBM * t, cs), p_hi = min(kBM * t + kBM - 1, cs + L - 1);
   const int ctx_end = cs + L;
   if (p_hi >= kMaxPos || (p_hi >> 4) >= p.max_pages) {
-    if (threadIdx.x == 0 && h == 0 && rank == 0) set_error(p.err, kErrPos);
+    if (threadIdx.x == 0 && rank == 0 && hp == 0) set_error(p.err, kErrPos);
     return;
   }
-  const int k_lo = 0, k_hi = p_hi;
-  const int n_tiles = k_hi / kBN + 1;
+  const int k_hi = p_hi;
+  const int n_tiles = k_hi / kTN + 1;
   const int q_row0 = qs + (kBM * t - cs);
   const int32_t* pt = p.page_table + (size_t)b * p.max_pages;
 
   if (threadIdx.x == 32) {
-    for (int s = 0; s < kNS; ++s) {
-      mbar_init(&sm.full[s], 1);
-      mbar_init(&sm.empty[s], 1);
+    for (int s = 0; s < kNK; ++s) {
+      mbar_init(&bar.k_full[s], 1);
+      mbar_init(&bar.k_empty[s], 1);
+      mbar_init(&bar.k_peer[s], 1);
     }
-    for (int s = 0; s < kNSP; ++s) {
-      mbar_init(&sm.s_full[s], 1);
-      mbar_init(&sm.p_full[s], kSoftmaxThreads);
-      mbar_init(&sm.pv_done[s], 1);
+    for (int s = 0; s < kNP; ++s) {
+      mbar_init(&bar.s_full[s], 1);
+      mbar_init(&bar.s_free[s], 8);    // rank 0: both score CTAs' softmax warps have read S
+      mbar_init(&bar.p_free[s], 1);    // the output CTA's P.V has read this P slot
+      mbar_init(&bar.p_full[s], 1);    // one local expect-tx arrive, then the score CTA's bytes
+      mbar_init(&bar.o_ready[s], 8);   // rank 2: both output CTAs have checked alpha (and rescaled O)
+      mbar_init(&bar.pv_done[s], 1);   // P.V of tiles of this parity
+      bar.p_seen[s] = 0;
     }
-    for (int s = 0; s < 2; ++s) mbar_init(&sm.xfull[s], 1);   // one local arrive with the expected bytes
-    mbar_init(&sm.q_full, 1);
-    mbar_init(&sm.q_ready, kSoftmaxThreads);
-    mbar_init(&sm.peer_done, 1);
-    mbar_init(&sm.teardown, 1);
-    sm.abort_flag = 0;
+    mbar_init(&bar.q_full, 1);
+    mbar_init(&bar.q_moved, kSoftmaxThreads / 32);
+    mbar_init(&bar.q_pair, 8);
+    mbar_init(&bar.stg_free, 1);
+    for (int s = 0; s < kNV; ++s) {
+      mbar_init(&bar.v_full[s], 1);
+      mbar_init(&bar.v_empty[s], 1);
+      mbar_init(&bar.v_ready[s], 1);
+    }
+    mbar_init(&bar.teardown, 1);
+    bar.abort_flag = 0;
+    if (is_out) {   // the first two tiles' P may arrive as soon as the cluster is up
+      for (int s = 0; s < kNP && s < n_tiles; ++s) mbar_arrive_expect_tx(&bar.p_full[s], kPSendBytes);
+    }
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(&sm.tmem_base, 512);
-    tmem_relinquish();
+    tmem_alloc2(&bar.tmem_base, 512);
+    tmem_relinquish2();
   }
   tc_fence_before();
-  cluster_sync_all();   // the peer's barriers are initialised before any remote arrive
+  cluster_sync_all();   // every CTA's barriers and tensor memory exist before any cross-CTA signal
   tc_fence_after();
-  const uint32_t tm = sm.tmem_base;
-  volatile int* abort_flag = &sm.abort_flag;
+  const uint32_t tm = bar.tmem_base;
+  volatile int* abort_flag = &bar.abort_flag;
+  auto arrive_leader = [&](uint64_t* br) {   // arrive on the pair leader's copy of a barrier
+    if (leader)
+      mbar_arrive(br);
+    else
+      mbar_arrive_remote(map_peer(smem_u32(br), pair_peer));
+  };
+  int k_issued = 0, v_issued = 0;   // copies in flight at an abort (producer warps)
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ copy producer
-    auto load_blocks = [&](int j0) -> int {
-      const int jt = j0 + (lane >> 2);
-      if (jt >= n_tiles) return -1;
-      return page_block(jt * kBN + (lane & 3) * kPage, k_lo, k_hi, pt, p.num_pages, kGlobalHkv, g, p.err);
-    };
-    if (lane == 0) {   // roped Q dims 256r .. 256r+255: chunks 0-1 into stage 2, chunks 2-3 stay
-      prefetch_tmap(&tmap_q);
-      mbar_arrive_expect_tx(&sm.q_full, 4 * kQChunk);
+  if (!is_out) {
+    // ================================================================ score CTAs
+    if (warp == 0) {
+      // ------------------------------------------------------------ Q and K copies
+      const __nv_bfloat16* sc = (const __nv_bfloat16*)p.k_cache;
+      const __nv_bfloat16* rc = (const __nv_bfloat16*)p.krot_cache;
+      if (lane == 0) {   // roped Q of head h: 8 boxes of 64 dims x 128 rows (rows outside T read as 0)
+        prefetch_tmap(&tmap_q);
+        mbar_arrive_expect_tx(&bar.q_full, 8 * kQChunk);
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-        tma_load_3d((c < 2 ? sm.st[2] + c * kQChunk : sm.qhi + (c - 2) * kQChunk), &tmap_q, kHalf * rank + 64 * c,
-                    h, q_row0, &sm.q_full);
-    }
-    int blk_cur = load_blocks(0), blk_next = load_blocks(8);
-    const __nv_bfloat16* sc = (const __nv_bfloat16*)p.k_cache;
-    const __nv_bfloat16* rc = (const __nv_bfloat16*)p.krot_cache;
-    int j = 0;
-    for (; j < n_tiles; ++j) {
-      const int s = j % kNS;
-      if (j > 0 && (j & 7) == 0) {
-        blk_cur = blk_next;
-        blk_next = load_blocks(j + 8);
+        for (int c = 0; c < 8; ++c) tma_load_3d(base + kQOff + c * kQChunk, &tmap_q, 64 * c, h, q_row0, &bar.q_full);
       }
-      const int my_blk = __shfl_sync(0xffffffffu, blk_cur, (j & 7) * 4 + (lane & 3));
-      const unsigned live = __ballot_sync(0xffffffffu, lane < 4 && my_blk >= 0);
-      const uint32_t bytes = __popc(live) * (kHalfPageBytes + kRotHalfPageBytes);
-      bool ok = (j < kNS) || lane != 0 || mbar_wait(&sm.empty[s], ((j / kNS) - 1) & 1, abort_flag, p.err);
-      if (j == 2 && lane == 0) ok = ok && mbar_wait(&sm.q_ready, 0, abort_flag, p.err);   // Q left stage 2
-      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      if (lane == 0) mbar_arrive_expect_tx(&sm.full[s], bytes);
-      __syncwarp();
-      if (lane < 4 && my_blk >= 0) {
-        bulk_g2s(sm.st[s] + lane * kHalfPageBytes, sc + (size_t)my_blk * kPage * kGD + rank * (kPage * kHalf),
-                 kHalfPageBytes, &sm.full[s]);
-        bulk_g2s(sm.st[s] + kSTile + lane * kRotHalfPageBytes,
-                 rc + (size_t)my_blk * kRotPageElems + rank * (kPage * kGlobalR), kRotHalfPageBytes, &sm.full[s]);
-      }
-    }
-    if (lane == 0 && *abort_flag) {   // drain copies still in flight (bounded) before the CTA may exit
-      const unsigned long long t0 = globaltimer();
-      while (!mbar_try_wait(smem_u32(&sm.q_full), 0) && globaltimer() - t0 < kWaitLimitNs) {
-      }
-      for (int i = max(0, j - kNS); i < j; ++i) {
-        while (!mbar_try_wait(smem_u32(&sm.full[i % kNS]), (i / kNS) & 1) && globaltimer() - t0 < kWaitLimitNs) {
+      // Lane l < 24 copies part (l % 6) of page (l / 6) of this CTA's 64 keys: parts 0-3 are the
+      // un-rotated dims of half (part >> 1), key group (part & 1); parts 4-5 the k_rot block of
+      // half (part - 4). Pages outside [0, k_hi] are neither looked up nor copied.
+      const int pl = lane / 6, part = lane % 6;
+      int j = 0;
+      for (; j < n_tiles; ++j) {
+        const int s = j % kNK;
+        const int key0 = j * kTN + 64 * (int)pr;
+        const int bl = lane < 4 ? page_block(key0 + kPage * lane, 0, k_hi, pt, p.num_pages, kGlobalHkv, g, p.err) : -1;
+        const unsigned live = __ballot_sync(0xffffffffu, bl >= 0);
+        const int blk = __shfl_sync(0xffffffffu, bl, pl & 3);
+        bool okw = true;
+        if (lane == 0) {
+          if (j == 1 || j == 2)   // stages 1-2 held Q until the softmax warps moved it
+            okw = mbar_wait(&bar.q_moved, 0, abort_flag, p.err);
+          else if (j >= kNK)
+            okw = mbar_wait(&bar.k_empty[s], ((j / kNK) - 1) & 1, abort_flag, p.err);
         }
-      }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    auto pv = [&](int i) -> bool {
-      if (!mbar_wait(&sm.p_full[i % kNSP], (i / kNSP) & 1, abort_flag, p.err)) return false;
-      const int kb = i * kBN;
-      uint8_t* vt = sm.st[i % kNS];
-      // V rows of keys that hold no data of this sequence are zeroed before P.V (pages past the
-      // last needed one keep an older tile, slots past the last key may hold NaN). QK^T of this
-      // tile has completed (the softmax read its S before arriving on p_full).
-      const int v1 = min(min(kb + kBN, ((k_hi >> 4) + 1) * kPage), ctx_end);
-      if (v1 < kb + kBN) {
-        for (int idx = lane; idx < kBN * (kHalf / 8); idx += 32) {
-          const int r = idx / (kHalf / 8), dg = idx % (kHalf / 8);
-          if (kb + r >= v1)
-            *reinterpret_cast<uint4*>(vt + (r >> 3) * kKG + dg * 128 + (r & 7) * 16) = make_uint4(0, 0, 0, 0);
-        }
-        fence_proxy_async();
+        if (!__shfl_sync(0xffffffffu, okw, 0)) break;
+        if (lane == 0) mbar_arrive_expect_tx(&bar.k_full[s], __popc(live) * kKPageBytes);
         __syncwarp();
-      }
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t va = smem_u32(vt);
-#pragma unroll
-        for (int k = 0; k < kBN / 16; ++k)   // V = the S half tile, MN-major: 16 keys (2 key groups) per step
-          mma_ts(tm + kTmO, tm + kTmS + 64 * (i % kNSP) + 8 * k, desc_tiled(va + k * 2 * kKG, kKG, 128), kIdescPV,
-                 (i > 0 || k > 0) ? 1u : 0u);
-        mma_commit(&sm.pv_done[i % kNSP]);
-        mma_commit(&sm.empty[i % kNS]);
-      }
-      __syncwarp();
-      return true;
-    };
-    // QK^T runs two tiles ahead of P.V: the softmax sends tile j+1's partial scores while it
-    // works on tile j, so S_{j+1} must be ready when tile j's softmax starts.
-    auto qk = [&](int j) -> bool {
-      const int s = j % kNS;
-      if (!mbar_wait(&sm.full[s], (j / kNS) & 1, abort_flag, p.err)) return false;
-      // S buffer j % 3 last held P_{j-3}: reuse it once P_{j-3} V_{j-3} has completed.
-      if (j >= kNSP && !mbar_wait(&sm.pv_done[j % kNSP], ((j - kNSP) / kNSP) & 1, abort_flag, p.err)) return false;
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t sa = smem_u32(sm.st[s]);
-        const uint32_t ra = sa + kSTile;
-        const uint32_t qh = smem_u32(sm.qhi);
-        const uint32_t sd = tm + kTmS + 64 * (j % kNSP);
-#pragma unroll
-        for (int k = 0; k < 4; ++k)    // dims 0-63 of the half (the rotated ones): K from k_rot
-          mma_ts(sd, tm + kTmQ + 8 * k, desc_tiled(ra + k * 256, 128, kRotKG), kIdescQK, k > 0 ? 1u : 0u);
-#pragma unroll
-        for (int k = 4; k < 8; ++k)    // dims 64-127: K = S
-          mma_ts(sd, tm + kTmQ + 8 * k, desc_tiled(sa + k * 256, 128, kKG), kIdescQK, 1u);
-#pragma unroll
-        for (int k = 8; k < 16; ++k)   // dims 128-255: Q from shared memory, K = S
-          mma_ss(sd, desc_sw128(qh + ((k - 8) >> 2) * kQChunk + (k & 3) * 32, 16, 1024),
-                 desc_tiled(sa + k * 256, 128, kKG), kIdescQK, 1u);
-        mma_commit(&sm.s_full[j % kNSP]);
-      }
-      __syncwarp();
-      return true;
-    };
-    bool ok = mbar_wait(&sm.q_ready, 0, abort_flag, p.err);
-    for (int j = 0; ok && j < 2 && j < n_tiles; ++j) ok = qk(j);
-    for (int i = 0; ok && i < n_tiles; ++i) {
-      if (!pv(i) || (i + 2 < n_tiles && !qk(i + 2))) ok = false;
-    }
-  } else {
-    // ------------------------------------------------------------ softmax / epilogue warps
-    const int r = 32 * (warp & 3) + lane;   // query row = tensor-memory lane
-    const uint32_t tq = tm + tmem_lane_base(warp);
-    const int pos = kBM * t + r;
-    const bool row_ok = pos >= p_lo && pos <= p_hi;
-    const uint32_t rsw = (uint32_t)(r & 7);   // 16-byte chunk swizzle of the exchange rows
-
-    {   // Q dims 0-127 of the half: ring stage 2 -> tensor memory (bf16 pairs)
-      const bool okq = mbar_wait(&sm.q_full, 0, abort_flag, p.err);
-      const uint8_t* qrow = sm.st[2] + r * 128;
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t w[32];
-#pragma unroll
-        for (int q8 = 0; q8 < 8; ++q8) {
-          const uint4 v = okq ? *reinterpret_cast<const uint4*>(qrow + c * kQChunk + ((q8 ^ (r & 7)) * 16))
-                              : make_uint4(0, 0, 0, 0);
-          w[4 * q8] = v.x;
-          w[4 * q8 + 1] = v.y;
-          w[4 * q8 + 2] = v.z;
-          w[4 * q8 + 3] = v.w;
-        }
-        tmem_st32(tq + kTmQ + 32 * c, w);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&sm.q_ready);
-    }
-
-    constexpr uint32_t kXBytes = kBM * kXCols * 4;      // one 32-key half of a partial score tile
-    constexpr uint32_t kXWarpBytes = 32 * kXCols * 4;   // the 32 rows of one warp
-    const uint32_t xrows = (uint32_t)(warp & 3) * kXWarpBytes;
-    const uint32_t peer_xbuf = map_peer(smem_u32(&sm.xbuf[0][0][0]), peer) + xrows;
-    const uint32_t peer_xfull = map_peer(smem_u32(&sm.xfull[0]), peer);
-    const int n_halves = 2 * n_tiles;
-    if (threadIdx.x == 64) {   // expect the peer's first two halves
-      mbar_arrive_expect_tx(&sm.xfull[0], kXBytes);
-      mbar_arrive_expect_tx(&sm.xfull[1], kXBytes);
-    }
-    // Exchange of partial scores in 32-key halves h = 2j + e (tile j, columns 32e..32e+31), one
-    // half ahead of the softmax. The peer's half h lands in xbuf[h & 1]; this CTA's own half h is
-    // staged in xbuf[(h + 1) & 1] and sent from there. Step h: wait for the peer's half h, read
-    // this warp's rows of it into registers, stage and send own half h+1 from the buffer just
-    // read, then run half h's softmax while that copy is in flight. Reuse is safe without a
-    // separate free signal: the peer sends its half h+2 into xbuf[h & 1] only after it has
-    // received all of this CTA's half h+1, whose copy read that buffer, and this CTA read the
-    // peer's half h from it before staging.
-    auto send_half = [&](int hh) -> bool {   // stage own half hh and copy it into the peer
-      const int jt = hh >> 1, eh = hh & 1;
-      if (eh == 0 &&
-          !__all_sync(0xffffffffu, mbar_wait(&sm.s_full[jt % kNSP], (jt / kNSP) & 1, abort_flag, p.err)))
-        return false;
-      tc_fence_after();
-      uint32_t sr[32];
-      tmem_ld32(tq + kTmS + 64 * (jt % kNSP) + kXCols * eh, sr);
-      tmem_ld_wait();
-      const int sp = (hh + 1) & 1;
-      float4* stg = reinterpret_cast<float4*>(&sm.xbuf[sp][r][0]);
-#pragma unroll
-      for (int c = 0; c < kXCols / 4; ++c)
-        stg[c ^ rsw] = make_float4(__uint_as_float(sr[4 * c]), __uint_as_float(sr[4 * c + 1]),
-                                   __uint_as_float(sr[4 * c + 2]), __uint_as_float(sr[4 * c + 3]));
-      fence_proxy_async();
-      __syncwarp();
-      if (lane == 0)
-        bulk_s2peer(peer_xbuf + (hh & 1) * kXBytes, reinterpret_cast<const uint8_t*>(&sm.xbuf[sp][0][0]) + xrows,
-                    kXWarpBytes, peer_xfull + (hh & 1) * 8);
-      return true;
-    };
-
-    const float cl2 = p.scale_log2;
-    float m_used = -INFINITY, l_run = 0.f;
-    bool ok = n_tiles > 0 && send_half(0);
-    for (int j = 0; ok && j < n_tiles; ++j) {
-      const int sb = j % kNSP;
-      float alpha_t = 1.f;   // O rescale owed for this tile (product over its halves)
-      bool need_o = false;
-#pragma unroll 1
-      for (int e = 0; e < 2; ++e) {
-        const int hh = 2 * j + e;
-        const int par = hh & 1;
-        const int kb = j * kBN + kXCols * e;   // first key of this half
-        // Waits are made warp-uniform so that every lane leaves the loop together on an abort.
-        if (!__all_sync(0xffffffffu, mbar_wait(&sm.xfull[par], (hh >> 1) & 1, abort_flag, p.err))) {
-          ok = false;
-          break;
-        }
-        if (hh + 2 < n_halves && threadIdx.x == 64) mbar_arrive_expect_tx(&sm.xfull[par], kXBytes);   // half h+2
-        float pe[kXCols];
-        {
-          const float4* xr = reinterpret_cast<const float4*>(&sm.xbuf[par][r][0]);
-#pragma unroll
-          for (int c = 0; c < kXCols / 4; ++c) {
-            const float4 o = xr[c ^ rsw];
-            pe[4 * c] = o.x;
-            pe[4 * c + 1] = o.y;
-            pe[4 * c + 2] = o.z;
-            pe[4 * c + 3] = o.w;
+        if (lane < 24 && blk >= 0) {
+          uint8_t* st = base + s * kKStage;
+          if (part < 4) {
+            const int hh = part >> 1, kg = part & 1;
+            bulk_g2s(st + hh * kUnrotHalf + (2 * pl + kg) * kUnrotKG,
+                     sc + (size_t)blk * (kPage * kGD) + hh * (kPage * kHalf) + kg * (8 * kHalf) + 8 * 64, kUnrotKG,
+                     &bar.k_full[s]);
+          } else {
+            const int hh = part - 4;
+            bulk_g2s(st + kRotOff + hh * kRotHalf + pl * 2 * kRotKG,
+                     rc + (size_t)blk * kRotPageElems + hh * (kPage * kGlobalR), 2 * kRotKG, &bar.k_full[s]);
           }
         }
-        if (hh + 1 < n_halves && !send_half(hh + 1)) {
+        __syncwarp();
+      }
+      k_issued = j;
+    } else if (warp == 1 && !leader) {
+      // ------------------------------------------------------------ K relay (rank 1)
+      for (int j = 0; j < n_tiles; ++j) {
+        const int s = j % kNK;
+        if (!__all_sync(0xffffffffu, mbar_wait(&bar.k_full[s], (j / kNK) & 1, abort_flag, p.err))) break;
+        if (lane == 0) mbar_arrive_remote(map_peer(smem_u32(&bar.k_peer[s]), pair_peer));
+        __syncwarp();
+      }
+    } else if (warp == 1) {
+      // ------------------------------------------------------------ QK^T issuer (rank 0)
+      bool ok = __all_sync(0xffffffffu, mbar_wait_cl(&bar.q_pair, 0, abort_flag, p.err));
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        const int s = j % kNK, sb = j % kNP;
+        // both CTAs' halves of the tile have landed; S buffer sb was read by tile j-2's softmax
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar.k_full[s], (j / kNK) & 1, abort_flag, p.err) &&
+                                         mbar_wait_cl(&bar.k_peer[s], (j / kNK) & 1, abort_flag, p.err) &&
+                                         (j < kNP || mbar_wait_cl(&bar.s_free[sb], ((j - kNP) / kNP) & 1, abort_flag, p.err)));
+        if (!ok) break;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t st = smem_u32(base + s * kKStage);
+          const uint32_t sd = tm + kTmS + kTN * sb;
+#pragma unroll
+          for (int ks = 0; ks < kGD / 16; ++ks) {   // dims 16ks .. 16ks+15
+            const int hh = ks >> 4, kk = ks & 15;
+            const uint64_t bd = kk < 4 ? desc_tiled(st + kRotOff + hh * kRotHalf + kk * 256, 128, kRotKG)
+                                       : desc_tiled(st + hh * kUnrotHalf + (kk - 4) * 256, 128, kUnrotKG);
+            mma2_ts(sd, tm + kTmQ + 8 * ks, bd, kIdescQK, ks > 0 ? 1u : 0u);
+          }
+          mma2_commit_mc(&bar.s_full[sb], kScorePair);
+          mma2_commit_mc(&bar.k_empty[s], kScorePair);
+        }
+        __syncwarp();
+      }
+    } else if (warp >= 2 && warp <= 5) {
+      // ------------------------------------------------------------ Q move, softmax, P
+      const int r = 32 * (warp & 3) + lane;   // query row = tensor-memory lane
+      const int wq = warp & 3;
+      const uint32_t tq = tm + tmem_lane_base(warp);
+      const int pos = kBM * t + r;
+      const bool row_ok = pos >= p_lo && pos <= p_hi;
+      bool ok = __all_sync(0xffffffffu, mbar_wait(&bar.q_full, 0, abort_flag, p.err));
+      if (ok) {   // Q (128B-swizzled boxes in K stages 1-2) -> tensor memory, bf16 pairs
+        const uint8_t* qrow = base + kQOff + r * 128;
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          uint32_t w[32];
+#pragma unroll
+          for (int q8 = 0; q8 < 8; ++q8) {
+            const uint4 v = *reinterpret_cast<const uint4*>(qrow + c * kQChunk + ((q8 ^ (r & 7)) * 16));
+            w[4 * q8] = v.x;
+            w[4 * q8 + 1] = v.y;
+            w[4 * q8 + 2] = v.z;
+            w[4 * q8 + 3] = v.w;
+          }
+          tmem_st32(tq + kTmQ + 32 * c, w);   // dims 64c .. 64c+63 -> columns 32c .. 32c+31
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&bar.q_moved);
+          arrive_leader(&bar.q_pair);
+        }
+      }
+      const uint32_t p_dst = map_peer(smem_u32(base + kOOffP), partner);
+      const uint32_t pfull_dst = map_peer(smem_u32(&bar.p_full[0]), partner);
+      uint8_t* stg = base + kSOffStage;
+      float2* aux = reinterpret_cast<float2*>(base + kSOffAux);
+      const float cl2 = p.scale_log2;
+      float m_used = -INFINITY, l_run = 0.f;
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        const int sb = j % kNP;
+        const int kb = j * kTN;
+        // Waits are made warp-uniform so that every lane leaves the loop together on an abort.
+        if (!__all_sync(0xffffffffu, mbar_wait(&bar.s_full[sb], (j / kNP) & 1, abort_flag, p.err))) {
           ok = false;
           break;
         }
-        // S of this half: own partial (still in its tensor-memory buffer) + the peer's, the same
-        // sum in either CTA.
-        uint32_t sr[kXCols];
-        tmem_ld32(tq + kTmS + 64 * sb + kXCols * e, sr);
+        tc_fence_after();
+        uint32_t sr[kTN];
+#pragma unroll
+        for (int c = 0; c < kTN / 32; ++c)
+          tmem_ld32(tq + kTmS + kTN * sb + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
         tmem_ld_wait();
-        float s[kXCols];
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) arrive_leader(&bar.s_free[sb]);   // buffer sb may take QK^T of tile j+2
+
+        float s[kTN];
 #pragma unroll
-        for (int c = 0; c < kXCols; ++c) s[c] = __uint_as_float(sr[c]) + pe[c];
-        if (!(row_ok && kb + kXCols - 1 <= pos)) {   // causal mask (and rows outside the sequence)
+        for (int c = 0; c < kTN; ++c) s[c] = __uint_as_float(sr[c]);
+        if (!(row_ok && kb + kTN - 1 <= pos)) {   // causal mask (and rows outside the sequence)
+          const int hi = row_ok ? pos - kb : -1;
 #pragma unroll
-          for (int c = 0; c < kXCols; ++c) s[c] = (row_ok && kb + c <= pos) ? s[c] : -INFINITY;
+          for (int c = 0; c < kTN; ++c) s[c] = (c <= hi) ? s[c] : -INFINITY;
         }
         float mx[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) mx[i] = fmaxf(fmaxf(s[i], s[i + 8]), fmaxf(s[i + 16], s[i + 24]));
+        for (int i = 0; i < 8; ++i) {
+          mx[i] = s[i];
+#pragma unroll
+          for (int c = 1; c < kTN / 8; ++c) mx[i] = fmaxf(mx[i], s[i + 8 * c]);
+        }
         const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * cl2;
-        float alpha = 1.f;
-        bool raised = false;
+        float alpha = 1.f;   // O rescale owed before P_j V_j (1 unless the reference rose by > 2^8)
         if (mt > m_used + kLazyRescale) {
-          need_o = need_o || (m_used != -INFINITY);
-          alpha = ex2(m_used - mt);
+          if (m_used != -INFINITY) alpha = ex2(m_used - mt);
           m_used = mt;
-          raised = true;
-        }
-        // The tile's first half of P was written against the old reference: rescale it too, so
-        // that P_j V_j sees one reference per row.
-        if (e == 1 && __any_sync(0xffffffffu, raised)) {
-          uint32_t pw0[16];
-          tmem_st_wait();   // the first half's own store has landed
-          tmem_ld16(tq + kTmS + 64 * sb, pw0);
-          tmem_ld_wait();
-          const float a = raised ? alpha : 1.f;
-#pragma unroll
-          for (int w = 0; w < 16; ++w) pw0[w] = pack_bf16(bf16_lo(pw0[w]) * a, bf16_hi(pw0[w]) * a);
-          tmem_st16(tq + kTmS + 64 * sb, pw0);
         }
         const float neg_m = (m_used == -INFINITY) ? 0.f : -m_used;
-        uint32_t pw[16];
+        uint32_t pw[kTN / 2];
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int w = 0; w < 16; ++w) {
+        for (int w = 0; w < kTN / 2; ++w) {
           const float e0 = ex2(fmaf(s[2 * w], cl2, neg_m));
           const float e1 = ex2(fmaf(s[2 * w + 1], cl2, neg_m));
           ls[w & 3] += e0;
@@ -399,88 +378,240 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           pw[w] = pack_bf16(e0, e1);   // declared cast: P in bf16 for P.V
         }
         l_run = fmaf(l_run, alpha, (ls[0] + ls[1]) + (ls[2] + ls[3]));
-        alpha_t *= alpha;
-        // P of this half (bf16 key pairs) over columns 16e.. of the tile's S buffer, whose S
-        // values there are already consumed: the A operand of P.V.
-        tmem_st16(tq + kTmS + 64 * sb + 16 * e, pw);
-      }
-      if (!ok) break;
 
-      if (__any_sync(0xffffffffu, need_o)) {   // O correction after P_{j-1} V_{j-1} landed
-        if (!__all_sync(0xffffffffu, mbar_wait(&sm.pv_done[(j - 1) % kNSP], ((j - 1) / kNSP) & 1, abort_flag, p.err))) {
+        // The staging area is free once the previous tile's copies have landed.
+        if (j > 0 && !__all_sync(0xffffffffu, mbar_wait_cl(&bar.stg_free, (j - 1) & 1, abort_flag, p.err))) {
           ok = false;
           break;
         }
+        uint8_t* prow = stg + (r >> 3) * 2048 + (r & 7) * 16;
+#pragma unroll
+        for (int kg = 0; kg < kTN / 8; ++kg)   // keys 8kg .. 8kg+7 of row r: one core-matrix row
+          *reinterpret_cast<uint4*>(prow + kg * 128) = make_uint4(pw[4 * kg], pw[4 * kg + 1], pw[4 * kg + 2], pw[4 * kg + 3]);
+        aux[r] = make_float2(alpha, l_run);
+        fence_proxy_async();   // the bulk copies read what the generic stores wrote
+        __syncwarp();
+        bool okp = true;
+        if (lane == 0) {
+          // P slot sb of the output CTA was last read by P.V of tile j-2
+          okp = j < kNP || mbar_wait_cl(&bar.p_free[sb], ((j - kNP) / kNP) & 1, abort_flag, p.err);
+          if (okp) {
+            bulk_s2peer(p_dst + sb * kPSlot + wq * kPWarpBytes, stg + wq * kPWarpBytes, kPWarpBytes, pfull_dst + sb * 8);
+            bulk_s2peer(p_dst + sb * kPSlot + kPBytes + wq * kAuxWarpBytes,
+                        reinterpret_cast<const uint8_t*>(aux) + wq * kAuxWarpBytes, kAuxWarpBytes, pfull_dst + sb * 8);
+          }
+        }
+        if (!__shfl_sync(0xffffffffu, okp, 0)) ok = false;
+      }
+    }
+  } else {
+    // ================================================================ output CTAs
+    const int hv = (int)pr;   // this CTA stages dims 256 hv .. 256 hv + 255 of V
+    if (warp == 0) {
+      // ------------------------------------------------------------ V copies
+      const __nv_bfloat16* sc = (const __nv_bfloat16*)p.k_cache;
+      const int n_st = 2 * n_tiles;
+      int c = 0;
+      for (; c < n_st; ++c) {
+        const int s = c % kNV;
+        const int bl =
+            lane < 4 ? page_block(c * kVN + kPage * lane, 0, k_hi, pt, p.num_pages, kGlobalHkv, g, p.err) : -1;
+        const unsigned live = __ballot_sync(0xffffffffu, bl >= 0);
+        bool okw = true;
+        if (lane == 0 && c >= kNV) okw = mbar_wait(&bar.v_empty[s], ((c / kNV) - 1) & 1, abort_flag, p.err);
+        if (!__shfl_sync(0xffffffffu, okw, 0)) break;
+        if (lane == 0) mbar_arrive_expect_tx(&bar.v_full[s], __popc(live) * kVPageBytes);
+        __syncwarp();
+        if (bl >= 0)
+          bulk_g2s(base + s * kVStage + lane * kVPageBytes, sc + (size_t)bl * (kPage * kGD) + hv * (kPage * kHalf),
+                   kVPageBytes, &bar.v_full[s]);
+        __syncwarp();
+      }
+      v_issued = c;
+    } else if (warp == 1) {
+      // ------------------------------------------------------------ V check; P.V issuer (rank 2) or relay (rank 3)
+      // Value rows of keys that hold no data of this sequence are zeroed before P.V: pages past
+      // the last needed one were not copied and keep an older tile, and slots past the
+      // sequence's last key may hold anything (NaN); P = 0 there does not cancel NaN.
+      bool ok = true;
+      const int n_st = 2 * n_tiles;
+      for (int c = 0; ok && c < n_st; ++c) {
+        const int s = c % kNV, j = c >> 1, e = c & 1;
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar.v_full[s], (c / kNV) & 1, abort_flag, p.err));
+        if (!ok) break;
+        const int kb = c * kVN;
+        const int v1 = min(min(kb + kVN, ((k_hi >> 4) + 1) * kPage), ctx_end);
+        if (v1 < kb + kVN) {
+          uint8_t* vt = base + s * kVStage;
+          for (int idx = lane; idx < kVN * 32; idx += 32) {
+            const int rr = idx >> 5, dg = idx & 31;
+            if (kb + rr >= v1)
+              *reinterpret_cast<uint4*>(vt + (rr >> 3) * kVKG + dg * 128 + (rr & 7) * 16) = make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async();
+        }
+        __syncwarp();
+        if (!leader) {
+          if (lane == 0) mbar_arrive_remote(map_peer(smem_u32(&bar.v_ready[s]), pair_peer));
+          __syncwarp();
+          continue;
+        }
+        // rank 3's half is ready; at a tile's first half, both CTAs have P_j and have applied alpha
+        ok = __all_sync(0xffffffffu, mbar_wait_cl(&bar.v_ready[s], (c / kNV) & 1, abort_flag, p.err) &&
+                                         (e == 1 || mbar_wait_cl(&bar.o_ready[j % kNP], (j / kNP) & 1, abort_flag, p.err)));
+        if (!ok) break;
         tc_fence_after();
-        const float a = need_o ? alpha_t : 1.f;
+        if (lane == 0) {
+          const uint32_t va = smem_u32(base + s * kVStage);
+          const uint32_t pa = smem_u32(base + kOOffP + (j % kNP) * kPSlot);
+#pragma unroll
+          for (int k = 0; k < kVN / 16; ++k) {   // 16 keys (two key groups) per step
+            const uint32_t acc = (j > 0 || e > 0 || k > 0) ? 1u : 0u;
+            const uint64_t ad = desc_tiled(pa + (4 * e + k) * 256, 128, 2048);
+            mma2_ss(tm + kTmO, ad, desc_tiled(va + k * 2 * kVKG, kVKG, 128), kIdescPV, acc);
+            mma2_ss(tm + kTmO + 256, ad, desc_tiled(va + k * 2 * kVKG + 2048, kVKG, 128), kIdescPV, acc);
+          }
+          mma2_commit_mc(&bar.v_empty[s], kOutPair);
+          if (e == 1) mma2_commit_mc(&bar.pv_done[j % kNP], kOutPair);
+        }
+        __syncwarp();
+      }
+    } else if (warp >= 2 && warp <= 5) {
+      // ------------------------------------------------------------ alpha, O rescale, epilogue
+      const int r = 32 * (warp & 3) + lane;
+      const uint32_t tq = tm + tmem_lane_base(warp);
+      const int pos = kBM * t + r;
+      const bool row_ok = pos >= p_lo && pos <= p_hi;
+      const uint32_t stg_free_dst = map_peer(smem_u32(&bar.stg_free), partner);
+      float l_last = 0.f;
+      bool ok = true;
+      for (int j = 0; j < n_tiles; ++j) {
+        const int sb = j % kNP;
+        if (!__all_sync(0xffffffffu, mbar_wait_cl(&bar.p_full[sb], (j / kNP) & 1, abort_flag, p.err))) {
+          ok = false;
+          break;
+        }
+        const float2 ax = reinterpret_cast<const float2*>(base + kOOffP + sb * kPSlot + kPBytes)[r];
+        if (threadIdx.x == 64) {
+          bar.p_seen[sb] = j / kNP + 1;
+          if (j + 1 < n_tiles) mbar_arrive_remote(stg_free_dst);   // the score CTA may refill its staging
+        }
+        l_last = ax.y;
+        const bool need = j > 0 && ax.x != 1.f;
+        if (__any_sync(0xffffffffu, need)) {   // O correction, after P_{j-1} V_{j-1} has landed
+          const int jp = j - 1;
+          if (!__all_sync(0xffffffffu, mbar_wait(&bar.pv_done[jp % kNP], (jp / kNP) & 1, abort_flag, p.err))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const float a = need ? ax.x : 1.f;
 #pragma unroll 1
-        for (int cc = 0; cc < kHalf / 32; ++cc) {
+          for (int cc = 0; cc < kGD / 32; ++cc) {
+            uint32_t o[32];
+            tmem_ld32(tq + kTmO + 32 * cc, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * a);
+            tmem_st32(tq + kTmO + 32 * cc, o);
+          }
+          tmem_st_wait();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) arrive_leader(&bar.o_ready[sb]);
+      }
+      // Epilogue: O / l -> bf16, rows of this sequence only.
+      const int jl = n_tiles - 1;
+      if (ok && __all_sync(0xffffffffu, mbar_wait(&bar.pv_done[jl % kNP], (jl / kNP) & 1, abort_flag, p.err))) {
+        tc_fence_after();
+        const float inv = (l_last > 0.f) ? __frcp_rn(l_last) : 0.f;
+        __nv_bfloat16* orow = p.out + ((size_t)(q_row0 + r) * kGlobalHq + h) * kGD;
+#pragma unroll 1
+        for (int cc = 0; cc < kGD / 32; ++cc) {
           uint32_t o[32];
           tmem_ld32(tq + kTmO + 32 * cc, o);
           tmem_ld_wait();
+          uint32_t w16[16];
 #pragma unroll
-          for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * a);
-          tmem_st32(tq + kTmO + 32 * cc, o);
-        }
-        tmem_st_wait();
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&sm.p_full[sb]);
-    }
-
-    // Epilogue: this CTA's 256 dims of O / l -> bf16, rows of this sequence only.
-    if (ok && mbar_wait(&sm.pv_done[(n_tiles - 1) % kNSP], ((n_tiles - 1) / kNSP) & 1, abort_flag, p.err)) {
-      tc_fence_after();
-      const float inv = (l_run > 0.f) ? __frcp_rn(l_run) : 0.f;
-      __nv_bfloat16* orow = p.out + ((size_t)(q_row0 + r) * kGlobalHq + h) * kGD + kHalf * rank;
-#pragma unroll 1
-      for (int cc = 0; cc < kHalf / 32; ++cc) {
-        uint32_t o[32];
-        tmem_ld32(tq + kTmO + 32 * cc, o);
-        tmem_ld_wait();
-        uint32_t w16[16];
+          for (int c = 0; c < 16; ++c)
+            w16[c] = pack_bf16(__uint_as_float(o[2 * c]) * inv, __uint_as_float(o[2 * c + 1]) * inv);
+          if (row_ok) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + o_dim(32 * cc));
 #pragma unroll
-        for (int c = 0; c < 16; ++c)
-          w16[c] = pack_bf16(__uint_as_float(o[2 * c]) * inv, __uint_as_float(o[2 * c + 1]) * inv);
-        if (row_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * cc);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w16[4 * i], w16[4 * i + 1], w16[4 * i + 2], w16[4 * i + 3]);
+            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w16[4 * i], w16[4 * i + 1], w16[4 * i + 2], w16[4 * i + 3]);
+          }
         }
       }
+    } else if (warp == 6) {
+      // ------------------------------------------------------------ P slot hand-back
+      // Once P.V of tile j has completed, its P slot takes tile j+2: post the bytes that tile's
+      // copies will deliver, then tell the score CTA (posting first keeps the count ahead).
+      if (lane == 0) {
+        const uint32_t pfree_dst = map_peer(smem_u32(&bar.p_free[0]), partner);
+        for (int j = 0; j < n_tiles; ++j) {
+          if (!mbar_wait(&bar.pv_done[j % kNP], (j / kNP) & 1, abort_flag, p.err)) break;
+          if (j + kNP < n_tiles) {
+            mbar_arrive_expect_tx(&bar.p_full[j % kNP], kPSendBytes);
+            mbar_arrive_remote(pfree_dst + (j % kNP) * 8);
+          }
+        }
+      }
+      __syncwarp();
     }
   }
 
   // ------------------------------------------------------------ teardown
+  // No CTA may free its tensor memory or leave while MMAs, copies or signals into it are in
+  // flight. On an abort the flag is passed to the other three CTAs (their waits then end
+  // early), copies this CTA issued are drained (bounded), and a cluster barrier closes the unit.
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    if (sm.abort_flag) {   // let every issued MMA finish before the columns are freed
-      if (lane == 0) mma_commit(&sm.teardown);
-      __syncwarp();
-      const unsigned long long t0 = globaltimer();
-      while (!mbar_try_wait(smem_u32(&sm.teardown), 0) && globaltimer() - t0 < kWaitLimitNs) {
+  if (!*abort_flag && threadIdx.x == 0) {   // the last stage releases (MMA commits) have arrived
+    const unsigned long long w0 = globaltimer();
+    const int n_st = is_out ? 2 * n_tiles : n_tiles, ring = is_out ? kNV : kNK;
+    uint64_t* empty = is_out ? bar.v_empty : bar.k_empty;
+    for (int s = 0; s < ring && s < n_st; ++s) {
+      const int last = s + ring * ((n_st - 1 - s) / ring);
+      while (!mbar_try_wait(smem_u32(&empty[s]), (last / ring) & 1) && globaltimer() - w0 < kWaitLimitNs) {
       }
     }
-    tmem_dealloc(tm, 512);
   }
-  // Neither CTA leaves while the other may still write into its shared memory: an abort is
-  // passed on (so the peer's waits end early), then each side tells the other it is done.
-  if (threadIdx.x == 0) {
-    if (sm.abort_flag) st_peer_u32(map_peer(smem_u32(&sm.abort_flag), peer), 1u);
-    mbar_arrive_peer(map_peer(smem_u32(&sm.peer_done), peer));
-    const uint32_t a = smem_u32(&sm.peer_done);
-    const unsigned long long t0 = globaltimer();
-    while (!mbar_try_wait_cluster(a, 0)) {
-      if (globaltimer() - t0 > 2 * kWaitLimitNs) {
-        set_error(p.err, kErrTimeout);
-        break;
+  if (*abort_flag) {
+    if (threadIdx.x == 0) {
+      for (uint32_t q = 0; q < 4; ++q)
+        if (q != rank) st_peer_u32(map_peer(smem_u32(&bar.abort_flag), q), 1u);
+    }
+    if (threadIdx.x == 0) {   // copies into this CTA's shared memory that may still be in flight
+      const unsigned long long w0 = globaltimer();
+      auto drain = [&](uint64_t* br, uint32_t par) {
+        while (!mbar_try_wait_cluster(smem_u32(br), par) && globaltimer() - w0 < kWaitLimitNs) {
+        }
+      };
+      if (!is_out) {
+        drain(&bar.q_full, 0);
+        for (int i = max(0, k_issued - kNK); i < k_issued; ++i) drain(&bar.k_full[i % kNK], (i / kNK) & 1);
+      } else {
+        for (int i = max(0, v_issued - kNV); i < v_issued; ++i) drain(&bar.v_full[i % kNV], (i / kNV) & 1);
+        for (int s = 0; s < kNP; ++s) drain(&bar.p_full[s], bar.p_seen[s] & 1);
       }
     }
   }
   __syncthreads();
+  tc_fence_before();
+  cluster_sync_all();
+  if (warp == 1) {
+    tc_fence_after();
+    if (bar.abort_flag) {   // let every MMA the pair issued finish before the columns are freed
+      if (leader && lane == 0) mma2_commit_mc(&bar.teardown, is_out ? kOutPair : kScorePair);
+      __syncwarp();
+      const unsigned long long w0 = globaltimer();
+      while (!mbar_try_wait(smem_u32(&bar.teardown), 0) && globaltimer() - w0 < kWaitLimitNs) {
+      }
+    }
+    tmem_dealloc2(tm, 512);
+  }
 }
 
 }  // namespace
@@ -505,15 +636,16 @@ cudaError_t launch_prefill_global(const SeqRows& rows, float scale_log2, const P
   static bool attr[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr[dev]) {
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr[dev]) {
     cudaError_t e =
         cudaFuncSetAttribute(prefill_global_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGlobalSmemBytes);
     if (e != cudaSuccess) return e;
     attr[dev] = true;
   }
   const long long slots = (long long)rows.T / kBM + 2LL * rows.B;
-  const long long blocks = slots * kGlobalHq * 2;   // a pair of CTAs per (query tile, head)
-  if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+  const long long blocks = slots * (kGlobalHq / 2) * 4;   // a cluster of four CTAs per (query tile, head pair)
+  if (blocks <= 0 || blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
   prefill_global_kernel<<<(unsigned)blocks, kThreads, kGlobalSmemBytes, s>>>(mq, p);
   return cudaGetLastError();
 }
