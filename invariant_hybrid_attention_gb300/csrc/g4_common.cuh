@@ -283,6 +283,14 @@ G4_DEV void tma_load_3d(void* smem, const CUtensorMap* map, int x, int y, int z,
       : "memory");
 }
 
+G4_DEV void tma_load_5d(void* smem, const CUtensorMap* map, int c0, int c1, int c2, int c3, int c4, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
+      "%5, %6}], [%7];" ::"r"(smem_u32(smem)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // Tiled shared -> global store through a tensor map (bulk async-group completion). The
 // innermost coordinate must keep the copy 16-byte aligned; no coordinate may be negative.
 G4_DEV void tma_store_3d(const CUtensorMap* map, const void* smem, int x, int y, int z) {

@@ -53,36 +53,44 @@ constexpr int kNP = 2;              // S buffers (score CTAs) and P slots (outpu
 constexpr int kThreads = 224;
 constexpr uint16_t kScorePair = 0x3, kOutPair = 0xC;
 
-// Score-CTA K stage: this CTA's 64 keys of a tile, all 512 dims, per dim half h:
-//   dims 64..255 of the half (from S): [key group (8)][dim group 8..31 (24)][8][8] at h * kUnrotHalf,
-//   dims 0..63 of the half (from k_rot): [key group (8)][dim group (8)][8][8] at kRotOff + h * kRotHalf.
-constexpr int kUnrotKG = 24 * 128;               // 3 KB
-constexpr int kUnrotHalf = 8 * kUnrotKG;         // 24 KB
-constexpr int kRotKG = 8 * 128;                  // 1 KB
-constexpr int kRotHalf = 8 * kRotKG;             // 8 KB
-constexpr int kRotOff = 2 * kUnrotHalf;          // 48 KB
-constexpr int kKStage = kRotOff + 2 * kRotHalf;  // 64 KB
-constexpr int kKPageBytes = kKStage / 4;         // 16 KB: one page's share of a stage
-constexpr int kQOff = kKStage;                   // roped Q, 8 boxes of 64 dims x 128 rows: K stages 1-2
-// P tile of one head: [row group (16)][key group (16)][8 rows][8 keys] bf16; aux: (alpha, l) per row.
-constexpr int kPBytes = kBM * kTN * 2;           // 32 KB
-constexpr int kPWarpBytes = kPBytes / 4;         // 8 KB: the rows of one softmax warp
-constexpr int kAuxBytes = kBM * 8;               // 1 KB
-constexpr int kAuxWarpBytes = kAuxBytes / 4;     // 256 B
-constexpr int kPSlot = kPBytes + kAuxBytes;      // 33 KB
+// Score-CTA K stage: this CTA's 64 keys of a tile (4 pages), all 512 dims. Each page arrives as
+// two tensor copies whose boxes put the key group outside the dim half, so that for either half
+// the 8 key groups of the stage sit at one fixed stride (the matrix descriptor's SBO):
+//   dims 64..255 of each half (from S): [page (4)][key group (2)][half (2)][dim group 8..31 (24)][8][8]
+//   at 0, key-group stride 6 KB;
+//   dims 0..63 of each half (from k_rot): [page (4)][key group (2)][half (2)][dim group (8)][8][8]
+//   at kRotOff, key-group stride 2 KB.
+constexpr int kUnrotCM = 24 * 128;               // 3 KB: 24 core matrices of one (key group, half)
+constexpr int kUnrotKG = 2 * kUnrotCM;           // 6 KB
+constexpr int kUnrotPage = 2 * kUnrotKG;         // 12 KB
+constexpr int kRotCM = 8 * 128;                  // 1 KB
+constexpr int kRotKG = 2 * kRotCM;               // 2 KB
+constexpr int kRotPage = 2 * kRotKG;             // 4 KB
+constexpr int kRotOff = 4 * kUnrotPage;          // 48 KB
+constexpr int kKStage = kRotOff + 4 * kRotPage;  // 64 KB
+constexpr int kKPageBytes = kUnrotPage + kRotPage;   // 16 KB: one page's share of a stage
+// The roped Q tile (8 boxes of 64 dims x 128 rows, 128B swizzle) lands at the first 1024-byte
+// boundary at or after K stage 1; it may reach up to 1008 bytes into the P staging area, which is
+// first written after every softmax warp of both score CTAs has moved Q into tensor memory.
+// P tile of one head: [row group (16)][key group (17)][8 rows][8 keys] bf16. Key groups 0-15 are
+// P (the A operand of P.V, row-group stride kPRowGroup); key group 16 carries the row's softmax
+// state instead: alpha (fp32) in bytes 0-3 and l (fp32) in bytes 4-7 of its 16-byte row. The
+// rows of one softmax warp (4 row groups) are contiguous, so one bulk copy per warp carries them.
+constexpr int kPRowGroup = 17 * 128;             // 2176 B
+constexpr int kPSlot = 16 * kPRowGroup;          // 34 KB
+constexpr int kPWarpBytes = kPSlot / 4;          // 8.5 KB
 constexpr uint32_t kPSendBytes = kPSlot;         // bytes one tile's copies deliver into a P slot
 // Output-CTA V stage: 64 keys x this CTA's 256 dims: [key group (8)][dim group (32)][8][8].
 constexpr int kVKG = 32 * 128;                   // 4 KB
 constexpr int kVStage = 8 * kVKG;                // 32 KB
 constexpr int kVPageBytes = 2 * kVKG;            // 8 KB: one page's half-block
-// Byte offsets in the data area. Score CTAs: K ring [0, 192K), P staging, aux staging.
-// Output CTAs: V ring [0, 128K), two P slots.
+// Byte offsets in the data area. Score CTAs: K ring [0, 192K), P staging [192K, 226K).
+// Output CTAs: V ring [0, 128K), two P slots [128K, 196K).
 constexpr int kSOffStage = kNK * kKStage;
-constexpr int kSOffAux = kSOffStage + kPBytes;
 constexpr int kOOffP = kNV * kVStage;
-constexpr int kDataBytes = kSOffAux + kAuxBytes;   // 225 KB
+constexpr int kDataBytes = kSOffStage + kPSlot;   // 226 KB
 static_assert(kOOffP + kNP * kPSlot <= kDataBytes, "output CTA layout exceeds the data area");
-static_assert(kQOff + 8 * kQChunk <= kNK * kKStage, "Q must fit in K stages 1-2");
+static_assert(kKStage + 1023 + 8 * kQChunk <= kDataBytes, "Q must fit between K stage 1 and the end");
 
 constexpr uint32_t kTmQ = 0, kTmS = 256, kTmO = 0;
 constexpr uint32_t kIdescQK = idesc_bf16(2 * kBM, kTN, false, false);   // M 256 over the pair, N 128 keys
@@ -107,7 +115,9 @@ struct GlobalSmem {
   uint8_t data[kDataBytes];
   Bars bar;
 };
-constexpr size_t kGlobalSmemBytes = sizeof(GlobalSmem) + 1024;
+// The data area needs 128-byte alignment only (bulk copies, matrix descriptors); the Q staging
+// finds its own 1024-byte boundary.
+constexpr size_t kGlobalSmemBytes = sizeof(GlobalSmem) + 128;
 static_assert(kGlobalSmemBytes <= 232448, "global prefill exceeds the 227 KB shared-memory limit");
 
 // Output-CTA tensor-memory column -> head dim (see the header).
@@ -116,10 +126,12 @@ __device__ __forceinline__ int o_dim(int col) {
 }
 
 __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
-    prefill_global_kernel(const __grid_constant__ CUtensorMap tmap_q, PrefillParams p) {
+    prefill_global_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_s,
+                          const __grid_constant__ CUtensorMap tmap_rot, PrefillParams p) {
   extern __shared__ uint8_t smem_raw[];
-  GlobalSmem& sm = *reinterpret_cast<GlobalSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  GlobalSmem& sm = *reinterpret_cast<GlobalSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   uint8_t* const base = sm.data;
+  uint8_t* const q_stage = base + kKStage + ((1024u - (smem_u32(base + kKStage) & 1023u)) & 1023u);
   Bars& bar = sm.bar;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
@@ -210,25 +222,38 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
     // ================================================================ score CTAs
     if (warp == 0) {
       // ------------------------------------------------------------ Q and K copies
-      const __nv_bfloat16* sc = (const __nv_bfloat16*)p.k_cache;
-      const __nv_bfloat16* rc = (const __nv_bfloat16*)p.krot_cache;
       if (lane == 0) {   // roped Q of head h: 8 boxes of 64 dims x 128 rows (rows outside T read as 0)
         prefetch_tmap(&tmap_q);
         mbar_arrive_expect_tx(&bar.q_full, 8 * kQChunk);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) tma_load_3d(base + kQOff + c * kQChunk, &tmap_q, 64 * c, h, q_row0, &bar.q_full);
+        for (int c = 0; c < 8; ++c) tma_load_3d(q_stage + c * kQChunk, &tmap_q, 64 * c, h, q_row0, &bar.q_full);
       }
-      // Lane l < 24 copies part (l % 6) of page (l / 6) of this CTA's 64 keys: parts 0-3 are the
-      // un-rotated dims of half (part >> 1), key group (part & 1); parts 4-5 the k_rot block of
-      // half (part - 4). Pages outside [0, k_hi] are neither looked up nor copied.
-      const int pl = lane / 6, part = lane % 6;
+      // Lanes 0-3 copy the un-rotated dims of page `lane` of this CTA's 64 keys, lanes 4-7 its
+      // k_rot block. Pages outside [0, k_hi] are neither looked up nor copied. Block indices come
+      // from the page table ahead of use: lane l holds page (l & 3) of tile (l >> 2) of the
+      // current group of 8 tiles, and the next group is looked up one group early.
+      if (lane == 0) {
+        prefetch_tmap(&tmap_s);
+        prefetch_tmap(&tmap_rot);
+      }
+      const int pl = lane & 3;
+      auto load_blocks = [&](int j0) -> int {
+        const int jt = j0 + (lane >> 2);
+        if (jt >= n_tiles) return -1;
+        return page_block(jt * kTN + 64 * (int)pr + kPage * (lane & 3), 0, k_hi, pt, p.num_pages, kGlobalHkv, g,
+                          p.err);
+      };
+      int blk_cur = load_blocks(0), blk_next = load_blocks(8);
       int j = 0;
       for (; j < n_tiles; ++j) {
         const int s = j % kNK;
-        const int key0 = j * kTN + 64 * (int)pr;
-        const int bl = lane < 4 ? page_block(key0 + kPage * lane, 0, k_hi, pt, p.num_pages, kGlobalHkv, g, p.err) : -1;
-        const unsigned live = __ballot_sync(0xffffffffu, bl >= 0);
-        const int blk = __shfl_sync(0xffffffffu, bl, pl & 3);
+        if (j > 0 && (j & 7) == 0) {
+          blk_cur = blk_next;
+          blk_next = load_blocks(j + 8);
+        }
+        const int bl = __shfl_sync(0xffffffffu, blk_cur, (j & 7) * 4 + (lane & 3));
+        const unsigned live = __ballot_sync(0xffffffffu, lane < 4 && bl >= 0);
+        const int blk = __shfl_sync(0xffffffffu, bl, pl);
         bool okw = true;
         if (lane == 0) {
           if (j == 1 || j == 2)   // stages 1-2 held Q until the softmax warps moved it
@@ -239,18 +264,12 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         if (!__shfl_sync(0xffffffffu, okw, 0)) break;
         if (lane == 0) mbar_arrive_expect_tx(&bar.k_full[s], __popc(live) * kKPageBytes);
         __syncwarp();
-        if (lane < 24 && blk >= 0) {
+        if (lane < 8 && blk >= 0) {
           uint8_t* st = base + s * kKStage;
-          if (part < 4) {
-            const int hh = part >> 1, kg = part & 1;
-            bulk_g2s(st + hh * kUnrotHalf + (2 * pl + kg) * kUnrotKG,
-                     sc + (size_t)blk * (kPage * kGD) + hh * (kPage * kHalf) + kg * (8 * kHalf) + 8 * 64, kUnrotKG,
-                     &bar.k_full[s]);
-          } else {
-            const int hh = part - 4;
-            bulk_g2s(st + kRotOff + hh * kRotHalf + pl * 2 * kRotKG,
-                     rc + (size_t)blk * kRotPageElems + hh * (kPage * kGlobalR), 2 * kRotKG, &bar.k_full[s]);
-          }
+          if (lane < 4)   // box {64, 24 dim groups from 8, 2 halves, 2 key groups, 1 block}
+            tma_load_5d(st + pl * kUnrotPage, &tmap_s, 0, 8, 0, 0, blk, &bar.k_full[s]);
+          else            // box {64, 8 dim groups, 2 halves, 2 key groups, 1 block}
+            tma_load_5d(st + kRotOff + pl * kRotPage, &tmap_rot, 0, 0, 0, 0, blk, &bar.k_full[s]);
         }
         __syncwarp();
       }
@@ -280,8 +299,8 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int ks = 0; ks < kGD / 16; ++ks) {   // dims 16ks .. 16ks+15
             const int hh = ks >> 4, kk = ks & 15;
-            const uint64_t bd = kk < 4 ? desc_tiled(st + kRotOff + hh * kRotHalf + kk * 256, 128, kRotKG)
-                                       : desc_tiled(st + hh * kUnrotHalf + (kk - 4) * 256, 128, kUnrotKG);
+            const uint64_t bd = kk < 4 ? desc_tiled(st + kRotOff + hh * kRotCM + kk * 256, 128, kRotKG)
+                                       : desc_tiled(st + hh * kUnrotCM + (kk - 4) * 256, 128, kUnrotKG);
             mma2_ts(sd, tm + kTmQ + 8 * ks, bd, kIdescQK, ks > 0 ? 1u : 0u);
           }
           mma2_commit_mc(&bar.s_full[sb], kScorePair);
@@ -298,7 +317,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
       const bool row_ok = pos >= p_lo && pos <= p_hi;
       bool ok = __all_sync(0xffffffffu, mbar_wait(&bar.q_full, 0, abort_flag, p.err));
       if (ok) {   // Q (128B-swizzled boxes in K stages 1-2) -> tensor memory, bf16 pairs
-        const uint8_t* qrow = base + kQOff + r * 128;
+        const uint8_t* qrow = q_stage + r * 128;
 #pragma unroll 1
         for (int c = 0; c < 8; ++c) {
           uint32_t w[32];
@@ -323,7 +342,6 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t p_dst = map_peer(smem_u32(base + kOOffP), partner);
       const uint32_t pfull_dst = map_peer(smem_u32(&bar.p_full[0]), partner);
       uint8_t* stg = base + kSOffStage;
-      float2* aux = reinterpret_cast<float2*>(base + kSOffAux);
       const float cl2 = p.scale_log2;
       float m_used = -INFINITY, l_run = 0.f;
       for (int j = 0; ok && j < n_tiles; ++j) {
@@ -384,11 +402,11 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        uint8_t* prow = stg + (r >> 3) * 2048 + (r & 7) * 16;
+        uint8_t* prow = stg + (r >> 3) * kPRowGroup + (r & 7) * 16;
 #pragma unroll
         for (int kg = 0; kg < kTN / 8; ++kg)   // keys 8kg .. 8kg+7 of row r: one core-matrix row
           *reinterpret_cast<uint4*>(prow + kg * 128) = make_uint4(pw[4 * kg], pw[4 * kg + 1], pw[4 * kg + 2], pw[4 * kg + 3]);
-        aux[r] = make_float2(alpha, l_run);
+        *reinterpret_cast<uint4*>(prow + 16 * 128) = make_uint4(__float_as_uint(alpha), __float_as_uint(l_run), 0u, 0u);
         fence_proxy_async();   // the bulk copies read what the generic stores wrote
         __syncwarp();
         bool okp = true;
@@ -397,8 +415,6 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
           okp = j < kNP || mbar_wait_cl(&bar.p_free[sb], ((j - kNP) / kNP) & 1, abort_flag, p.err);
           if (okp) {
             bulk_s2peer(p_dst + sb * kPSlot + wq * kPWarpBytes, stg + wq * kPWarpBytes, kPWarpBytes, pfull_dst + sb * 8);
-            bulk_s2peer(p_dst + sb * kPSlot + kPBytes + wq * kAuxWarpBytes,
-                        reinterpret_cast<const uint8_t*>(aux) + wq * kAuxWarpBytes, kAuxWarpBytes, pfull_dst + sb * 8);
           }
         }
         if (!__shfl_sync(0xffffffffu, okp, 0)) ok = false;
@@ -410,12 +426,24 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
     if (warp == 0) {
       // ------------------------------------------------------------ V copies
       const __nv_bfloat16* sc = (const __nv_bfloat16*)p.k_cache;
+      // Block indices ahead of use: lane l holds page (l & 3) of stage (l >> 2) of the current
+      // group of 8 stages; the next group is looked up one group early.
       const int n_st = 2 * n_tiles;
+      auto load_blocks = [&](int c0) -> int {
+        const int cs2 = c0 + (lane >> 2);
+        if (cs2 >= n_st) return -1;
+        return page_block(cs2 * kVN + kPage * (lane & 3), 0, k_hi, pt, p.num_pages, kGlobalHkv, g, p.err);
+      };
+      int blk_cur = load_blocks(0), blk_next = load_blocks(8);
       int c = 0;
       for (; c < n_st; ++c) {
         const int s = c % kNV;
-        const int bl =
-            lane < 4 ? page_block(c * kVN + kPage * lane, 0, k_hi, pt, p.num_pages, kGlobalHkv, g, p.err) : -1;
+        if (c > 0 && (c & 7) == 0) {
+          blk_cur = blk_next;
+          blk_next = load_blocks(c + 8);
+        }
+        const int bl0 = __shfl_sync(0xffffffffu, blk_cur, (c & 7) * 4 + (lane & 3));
+        const int bl = lane < 4 ? bl0 : -1;
         const unsigned live = __ballot_sync(0xffffffffu, bl >= 0);
         bool okw = true;
         if (lane == 0 && c >= kNV) okw = mbar_wait(&bar.v_empty[s], ((c / kNV) - 1) & 1, abort_flag, p.err);
@@ -467,7 +495,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < kVN / 16; ++k) {   // 16 keys (two key groups) per step
             const uint32_t acc = (j > 0 || e > 0 || k > 0) ? 1u : 0u;
-            const uint64_t ad = desc_tiled(pa + (4 * e + k) * 256, 128, 2048);
+            const uint64_t ad = desc_tiled(pa + (4 * e + k) * 256, 128, kPRowGroup);
             mma2_ss(tm + kTmO, ad, desc_tiled(va + k * 2 * kVKG, kVKG, 128), kIdescPV, acc);
             mma2_ss(tm + kTmO + 256, ad, desc_tiled(va + k * 2 * kVKG + 2048, kVKG, 128), kIdescPV, acc);
           }
@@ -491,7 +519,8 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        const float2 ax = reinterpret_cast<const float2*>(base + kOOffP + sb * kPSlot + kPBytes)[r];
+        const float2 ax = *reinterpret_cast<const float2*>(base + kOOffP + sb * kPSlot + (r >> 3) * kPRowGroup +
+                                                          16 * 128 + (r & 7) * 16);
         if (threadIdx.x == 64) {
           bar.p_seen[sb] = j / kNP + 1;
           if (j + 1 < n_tiles) mbar_arrive_remote(stg_free_dst);   // the score CTA may refill its staging
@@ -614,6 +643,37 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
   }
 }
 
+// Tensor maps over the global cache's page-head blocks, as 5-D tensors (innermost first):
+// 64 elements of a core matrix, dim group, dim half, key group, block (page * 4 + KV head). The
+// dim half comes before the key group although its stride is larger, so that a box lands with the
+// key group outermost (see the K stage layout). S: 32 dim groups per half, box from dim group 8;
+// k_rot: 8 dim groups per half.
+bool page_maps(CUtensorMap* ms, CUtensorMap* mr, const void* s_cache, const void* rot_cache, int num_pages) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t blocks = (cuuint64_t)num_pages * kGlobalHkv;
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  {
+    const cuuint64_t dims[5] = {64, 32, 2, 2, blocks};
+    const cuuint64_t strides[4] = {128, 2 * 32 * 128, 32 * 128, (cuuint64_t)kPage * kGD * 2};
+    const cuuint32_t box[5] = {64, 24, 2, 2, 1};
+    if (fn(ms, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(s_cache), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
+  {
+    const cuuint64_t dims[5] = {64, 8, 2, 2, blocks};
+    const cuuint64_t strides[4] = {128, 2 * 8 * 128, 8 * 128, (cuuint64_t)kRotPageElems * 2};
+    const cuuint32_t box[5] = {64, 8, 2, 2, 1};
+    if (fn(mr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(rot_cache), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
+  return true;
+}
+
 }  // namespace
 
 cudaError_t launch_prefill_global(const SeqRows& rows, float scale_log2, const PagedCache& cache, void* out,
@@ -631,8 +691,9 @@ cudaError_t launch_prefill_global(const SeqRows& rows, float scale_log2, const P
   p.out = (__nv_bfloat16*)out;
   p.tb = st.global;
   p.err = st.err;
-  CUtensorMap mq;
+  CUtensorMap mq, ms, mr;
   if (!q_map(&mq, out, rows.T, kGlobalHq, kGD)) return cudaErrorInvalidValue;
+  if (!page_maps(&ms, &mr, cache.k, cache.krot, cache.num_pages)) return cudaErrorInvalidValue;
   static bool attr[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -646,7 +707,7 @@ cudaError_t launch_prefill_global(const SeqRows& rows, float scale_log2, const P
   const long long slots = (long long)rows.T / kBM + 2LL * rows.B;
   const long long blocks = slots * (kGlobalHq / 2) * 4;   // a cluster of four CTAs per (query tile, head pair)
   if (blocks <= 0 || blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-  prefill_global_kernel<<<(unsigned)blocks, kThreads, kGlobalSmemBytes, s>>>(mq, p);
+  prefill_global_kernel<<<(unsigned)blocks, kThreads, kGlobalSmemBytes, s>>>(mq, ms, mr, p);
   return cudaGetLastError();
 }
 
