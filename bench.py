@@ -7,7 +7,9 @@ One step runs the whole path once over seeded synthetic inputs already resident 
   2. global K==V prefill, 2 x 8192 (Q 32x512, 4 shared K=V heads x 512, p-RoPE 0.25, theta 1e6);
   3. one decode pass of the 5 sliding : 1 global mix: 64 requests, one query each, contexts
      uniform in [1024, 32768] (seed 7), pages scattered by random permutation.
-Each part is timed with CUDA events on the launching stream after an L2 flush (a 512 MB write).
+Each part is timed with CUDA events on the launching stream after an L2 flush (a 512 MB write); a
+prefill part runs its two launches through g4attn_prefill_stage and g4attn_prefill_attend (exactly
+g4attn_prefill) with an event between them, so the attention kernel is timed on its own.
 
 Headline value: prefill TFLOP/s (credited FLOPs of parts 1+2 over their time); the decode part
 reports KV GB/s. Both also as fractions of the measured GB300 peaks.
@@ -159,8 +161,12 @@ class SlidingPrefill:
         self.g4.g4attn_prefill(self.layer, self.q, self.k, self.v, self.qs, self.ql, self.cs, self.cache.desc,
                                self.table, self.out)
 
-    def run_append(self):
-        self.g4.g4attn_kv_append(self.layer, self.k, self.v, self.qs, self.ql, self.cs, self.cache.desc, self.table)
+    def run_stage(self):   # launch 1 of g4attn_prefill: cache append + roped-q staging
+        self.g4.g4attn_prefill_stage(self.layer, self.q, self.k, self.v, self.qs, self.ql, self.cs, self.cache.desc,
+                                     self.table, self.out)
+
+    def run_attend(self):  # launch 2: the attention kernel
+        self.g4.g4attn_prefill_attend(self.layer, self.qs, self.ql, self.cs, self.cache.desc, self.table, self.out)
 
     def host_io(self):
         return [self.q, self.k, self.v], [self.out]
@@ -252,21 +258,6 @@ class DecodeMix:
 
 
 # ---------------------------------------------------------------- timing helpers
-
-def timed(fn, reps, flush):
-    """Median over `reps` of one call of fn, each after an L2 flush; CUDA events on torch's stream."""
-    import torch
-    ts = []
-    for _ in range(reps):
-        flush()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        fn()
-        b.record()
-        b.synchronize()
-        ts.append(a.elapsed_time(b))
-    return statistics.median(ts)
-
 
 def traffic_record(kernel: str):
     """dram bytes per launch from the committed ncu summary, if it was taken on the current source."""
@@ -401,7 +392,7 @@ def main():
     def step_parts():
         out = []
         for p in parts:
-            out.append((p.name, p.run))
+            out.append((p.name, (p.run_stage, p.run_attend)))
         if dec is not None:
             for i in range(dec.n_sliding):
                 out.append((f"decode_sliding_{i}", lambda i=i: dec.run_sliding(i)))
@@ -410,9 +401,16 @@ def main():
 
     sp = step_parts()
     clk = Clocks(local).__enter__()   # sampling from before the warm-up; summarised over the timed region
+    def call(fn):
+        if isinstance(fn, tuple):
+            for f in fn:
+                f()
+        else:
+            fn()
+
     for _ in range(args.warmup):
         for _, fn in sp:
-            fn()
+            call(fn)
     torch.cuda.synchronize()
     st = g4.g4attn_status_sync()
     if st != g4.G4_OK:
@@ -420,6 +418,7 @@ def main():
 
     # ---- timed region: K steps, per-part CUDA events, L2 flushed before each part
     times = {n: [] for n, _ in sp}
+    kern_times = {p.name: [] for p in parts}   # the attention launch of each prefill part
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
@@ -429,13 +428,22 @@ def main():
         for n, fn in sp:
             flush()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            m = None
             a.record()
-            fn()
+            if isinstance(fn, tuple):   # prefill: stage, event, attend
+                fn[0]()
+                m = torch.cuda.Event(enable_timing=True)
+                m.record()
+                fn[1]()
+            else:
+                fn()
             b.record()
-            evs.append((n, a, b))
+            evs.append((n, a, m, b))
         torch.cuda.synchronize()
-        for n, a, b in evs:
+        for n, a, m, b in evs:
             times[n].append(a.elapsed_time(b))
+            if m is not None:
+                kern_times[n].append(m.elapsed_time(b))
     torch.cuda.synchronize()
     t_end = time.time()
     clk.__exit__(None, None, None)
@@ -447,10 +455,14 @@ def main():
         raise SystemExit(f"device error in the timed region: {g4.status_string(st)}")
 
     tot = {n: sum(v) for n, v in times.items()}          # ms over K steps
+    ktot = {n: sum(v) for n, v in kern_times.items()}
     if dist is not None:
-        t = torch.tensor([tot[n] for n, _ in sp], dtype=torch.float64, device="cuda")
+        names = [n for n, _ in sp] + [f"kernel:{n}" for n in ktot]
+        t = torch.tensor([tot[n] for n, _ in sp] + [ktot[n] for n in ktot], dtype=torch.float64, device="cuda")
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        tot = {n: float(x) for (n, _), x in zip(sp, t.tolist())}
+        vals = dict(zip(names, t.tolist()))
+        tot = {n: float(vals[n]) for n, _ in sp}
+        ktot = {n: float(vals[f"kernel:{n}"]) for n in ktot}
     K = args.steps
     pk = peaks()
     res = {}
@@ -458,14 +470,13 @@ def main():
     pre_ms = sum(tot[p.name] for p in parts)
     value = pre_flops / (pre_ms * 1e-3) / 1e12 if pre_ms > 0 else None
 
-    # kernel-only prefill times: the prefill call minus its cache append, timed alone
+    # the attention kernel of each prefill part, timed on its own (event between the two launches)
     roofs = []
     for p in parts:
-        app = timed(p.run_append, 5, flush)
         call = tot[p.name] / K
-        kern = max(call - app, 1e-6)
+        kern = ktot[p.name] / K
         ach = p.flops / (kern * 1e-3) / 1e12
-        res[p.name] = {"ms": call, "append_ms": app, "attention_kernel_ms": kern,
+        res[p.name] = {"ms": call, "stage_ms": call - kern, "attention_kernel_ms": kern,
                        "tflops_call": p.flops / (call * 1e-3) / 1e12, "tflops_kernel": ach,
                        "frac_of_measured_burst": ach / pk["bf16_tflops"],
                        "frac_of_measured_sustained": ach / pk["bf16_tflops_sustained"],

@@ -137,6 +137,27 @@ g4_status g4attn_prefill(const g4attn_layer* layer, const void* q, const void* k
                          const int32_t* ctx_start, int32_t B, const g4attn_cache* cache,
                          const int32_t* page_table, int32_t max_pages, void* out, void* stream);
 
+/* The two steps of g4attn_prefill, for callers that schedule or time them apart; the pair gives
+ * the same bits as g4attn_prefill, which is exactly g4attn_prefill_stage followed by
+ * g4attn_prefill_attend on one stream.
+ * g4attn_prefill_stage: the cache append of the new rows (RFC section 5,
+ * hybrid_kv_cache_contract) and the declared bf16 cast of the roped queries, which it writes
+ * into the sequences' rows of `out` (sliding_rope_d256 / global_proportional_p_rope). Arguments
+ * and errors as g4attn_prefill.
+ * g4attn_prefill_attend: the attention step (sliding_attention_core / global_attention_core)
+ * over queries that g4attn_prefill_stage staged in `out` with the same rows, cache and page
+ * table; it overwrites those rows with the output and writes no other row. Arguments as
+ * g4attn_prefill without q, k and v; out must be 16-byte aligned when T > 0. Calling it on rows
+ * that were not staged gives meaningless (but bounded, fault-free) output. */
+g4_status g4attn_prefill_stage(const g4attn_layer* layer, const void* q, const void* k, const void* v,
+                               int32_t T, const int32_t* q_start, const int32_t* q_len,
+                               const int32_t* ctx_start, int32_t B, const g4attn_cache* cache,
+                               const int32_t* page_table, int32_t max_pages, void* out, void* stream);
+g4_status g4attn_prefill_attend(const g4attn_layer* layer, int32_t T, const int32_t* q_start,
+                                const int32_t* q_len, const int32_t* ctx_start, int32_t B,
+                                const g4attn_cache* cache, const int32_t* page_table, int32_t max_pages,
+                                void* out, void* stream);
+
 /* Writes the K'/V (sliding) or S (global) rows of a prefill batch into the paged cache
  * without computing attention: the first step of g4attn_prefill on its own (RFC section 5,
  * hybrid_kv_cache_contract). Same row conventions and errors as g4attn_prefill; v NULL on

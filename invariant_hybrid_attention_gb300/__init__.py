@@ -22,7 +22,8 @@ G4_SLIDING, G4_GLOBAL = 0, 1
 PAGE_SIZE = 16
 DECODE_STATIC_SCRATCH_BYTES = 32 << 20   # the static scratch of g4attn_decode_static, per device
 
-EXPORTS = ("g4attn_rope_apply", "g4attn_prefill", "g4attn_kv_append", "g4attn_decode_workspace_bytes",
+EXPORTS = ("g4attn_rope_apply", "g4attn_prefill", "g4attn_prefill_stage", "g4attn_prefill_attend",
+           "g4attn_kv_append", "g4attn_decode_workspace_bytes",
            "g4attn_decode", "g4attn_decode_static", "g4attn_provenance", "g4attn_status_sync", "g4attn_status_string")
 
 
@@ -60,6 +61,8 @@ def load(path: Optional[str] = None):
     sigs = {
         "g4attn_rope_apply": (I32, [L, P, P, I32, I32, P, P]),
         "g4attn_prefill": (I32, [L, P, P, P, I32, P, P, P, I32, C, P, I32, P, P]),
+        "g4attn_prefill_stage": (I32, [L, P, P, P, I32, P, P, P, I32, C, P, I32, P, P]),
+        "g4attn_prefill_attend": (I32, [L, I32, P, P, P, I32, C, P, I32, P, P]),
         "g4attn_kv_append": (I32, [L, P, P, I32, P, P, P, I32, C, P, I32, P]),
         "g4attn_decode_workspace_bytes": (SZ, [L, I32, I32]),
         "g4attn_decode": (I32, [L, P, P, P, P, I32, C, P, I32, P, P, SZ, P]),
@@ -137,6 +140,23 @@ def g4attn_prefill(layer, q, k, v, q_start, q_len, ctx_start, cache: g4attn_cach
     _check(load().g4attn_prefill(ctypes.byref(layer), _ptr(q), _ptr(k), _ptr(v), T, _ptr(q_start), _ptr(q_len),
                                  _ptr(ctx_start), B, ctypes.byref(cache), _ptr(page_table), int(page_table.shape[1]),
                                  _ptr(out), _stream(stream)), "g4attn_prefill")
+    return out
+
+
+def g4attn_prefill_stage(layer, q, k, v, q_start, q_len, ctx_start, cache: g4attn_cache, page_table, out,
+                         stream=None):
+    T, B = int(q.shape[0]), int(q_start.shape[0])
+    _check(load().g4attn_prefill_stage(ctypes.byref(layer), _ptr(q), _ptr(k), _ptr(v), T, _ptr(q_start),
+                                       _ptr(q_len), _ptr(ctx_start), B, ctypes.byref(cache), _ptr(page_table),
+                                       int(page_table.shape[1]), _ptr(out), _stream(stream)), "g4attn_prefill_stage")
+    return out
+
+
+def g4attn_prefill_attend(layer, q_start, q_len, ctx_start, cache: g4attn_cache, page_table, out, stream=None):
+    T, B = int(out.shape[0]), int(q_start.shape[0])
+    _check(load().g4attn_prefill_attend(ctypes.byref(layer), T, _ptr(q_start), _ptr(q_len), _ptr(ctx_start), B,
+                                        ctypes.byref(cache), _ptr(page_table), int(page_table.shape[1]),
+                                        _ptr(out), _stream(stream)), "g4attn_prefill_attend")
     return out
 
 

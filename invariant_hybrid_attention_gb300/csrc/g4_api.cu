@@ -145,10 +145,10 @@ g4_status g4attn_kv_append(const g4attn_layer* layer, const void* k, const void*
                                          (cudaStream_t)stream));
 }
 
-g4_status g4attn_prefill(const g4attn_layer* layer, const void* q, const void* k, const void* v, int32_t T,
-                         const int32_t* q_start, const int32_t* q_len, const int32_t* ctx_start, int32_t B,
-                         const g4attn_cache* cache, const int32_t* page_table, int32_t max_pages, void* out,
-                         void* stream) {
+g4_status g4attn_prefill_stage(const g4attn_layer* layer, const void* q, const void* k, const void* v, int32_t T,
+                               const int32_t* q_start, const int32_t* q_len, const int32_t* ctx_start, int32_t B,
+                               const g4attn_cache* cache, const int32_t* page_table, int32_t max_pages, void* out,
+                               void* stream) {
   bool global = false;
   g4_status s = check_layer(layer, &global);
   if (s != G4_OK) return s;
@@ -159,14 +159,37 @@ g4_status g4attn_prefill(const g4attn_layer* layer, const void* q, const void* k
   if (T == 0) return G4_OK;
   DeviceState st;
   if (device_state(&st) != cudaSuccess) return G4_ERR_CUDA;
-  const cudaStream_t cs = (cudaStream_t)stream;
+  // Cache append, and the roped queries staged in `out`: each sequence row of `out` holds its
+  // roped query until g4attn_prefill_attend overwrites it with the attention output.
   const SeqRows rows{q_start, q_len, ctx_start, B, T};
-  const PagedCache pc = paged(cache, page_table, max_pages);
-  // Launch 1: cache append, and the roped queries staged in `out` (each sequence row of `out`
-  // holds its roped query until launch 2 overwrites it with the attention output).
-  cudaError_t e = launch_append_prefill(global, k, v, rows, pc, st, cs, q, out);
-  if (e != cudaSuccess) return G4_ERR_CUDA;
-  return from_cuda(launch_prefill(global, rows, global ? 0 : layer->window, scale_log2(layer), pc, out, st, cs));
+  return from_cuda(launch_append_prefill(global, k, v, rows, paged(cache, page_table, max_pages), st,
+                                         (cudaStream_t)stream, q, out));
+}
+
+g4_status g4attn_prefill_attend(const g4attn_layer* layer, int32_t T, const int32_t* q_start, const int32_t* q_len,
+                                const int32_t* ctx_start, int32_t B, const g4attn_cache* cache,
+                                const int32_t* page_table, int32_t max_pages, void* out, void* stream) {
+  bool global = false;
+  g4_status s = check_layer(layer, &global);
+  if (s != G4_OK) return s;
+  if ((s = check_rows(out, T, q_start, q_len, ctx_start, B)) != G4_OK) return s;
+  if ((s = check_cache(cache, global, page_table, max_pages)) != G4_OK) return s;
+  if (T == 0) return G4_OK;
+  DeviceState st;
+  if (device_state(&st) != cudaSuccess) return G4_ERR_CUDA;
+  const SeqRows rows{q_start, q_len, ctx_start, B, T};
+  return from_cuda(launch_prefill(global, rows, global ? 0 : layer->window, scale_log2(layer),
+                                  paged(cache, page_table, max_pages), out, st, (cudaStream_t)stream));
+}
+
+g4_status g4attn_prefill(const g4attn_layer* layer, const void* q, const void* k, const void* v, int32_t T,
+                         const int32_t* q_start, const int32_t* q_len, const int32_t* ctx_start, int32_t B,
+                         const g4attn_cache* cache, const int32_t* page_table, int32_t max_pages, void* out,
+                         void* stream) {
+  g4_status s = g4attn_prefill_stage(layer, q, k, v, T, q_start, q_len, ctx_start, B, cache, page_table,
+                                     max_pages, out, stream);
+  if (s != G4_OK) return s;
+  return g4attn_prefill_attend(layer, T, q_start, q_len, ctx_start, B, cache, page_table, max_pages, out, stream);
 }
 
 size_t g4attn_decode_workspace_bytes(const g4attn_layer* layer, int32_t B, int32_t max_pages) {

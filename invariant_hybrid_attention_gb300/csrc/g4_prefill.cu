@@ -102,10 +102,10 @@ struct Unit {
 __device__ __noinline__ bool sliding_unit(const PrefillParams& p, int u, uint32_t rank, Unit& o) {
   o.g = u % kSlidingHkv;
   o.h = 2 * o.g + (int)rank;
-  int b, t;
-  find_unit(p.rows, u / kSlidingHkv, b, t);
+  int b, t, f[3];
+  find_unit(p.rows, u / kSlidingHkv, b, t, f);
   if (b < 0) return false;
-  const int cs = p.rows.ctx_start[b], L = p.rows.q_len[b], qs = p.rows.q_start[b];
+  const int cs = f[0], L = f[1], qs = f[2];
   o.t = t;
   o.p_lo = max(kBM * t, cs);
   o.p_hi = min(kBM * t + kBM - 1, cs + L - 1);
@@ -196,23 +196,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     int uq = 0;
     bool ok = true;
     if (!is_v && lane == 0) prefetch_tmap(&tmap_q);
-    for (int u = cluster; ok && u < p.n_units; u += n_clusters) {
-      Unit un;
-      if (!sliding_unit(p, u, rank, un)) continue;
-      if (!is_v) {   // the next unit's roped Q tile into L2, a unit ahead of its load
-        Unit nx;
-        if (u + n_clusters < p.n_units && sliding_unit(p, u + n_clusters, rank, nx) && lane == 0) {
-#pragma unroll
-          for (int c2 = 0; c2 < kSD / 64; ++c2) tma_prefetch_l2_3d(&tmap_q, 64 * c2, nx.h, max(nx.q_row0, 0));
-        }
-      }
+    auto next_valid = [&](int& uu, Unit& o) -> bool {   // this cluster's first unit >= uu with rows
+      for (; uu < p.n_units; uu += n_clusters)
+        if (sliding_unit(p, uu, rank, o)) return true;
+      return false;
+    };
+    auto raw_blocks = [&](const Unit& o, int j0) -> int {   // raw table entry of this lane's page
+      const int jt = j0 + (lane >> 3);
+      if (jt >= o.n_tiles) return kNoPage;
+      return page_raw((o.kt0 + jt) * kSN + (lane & 7) * kPage, o.k_lo, o.k_hi, o.pt);
+    };
+    // The next unit is looked up, and the page-table entries of its first two groups of tiles
+    // loaded, once the current unit's first slot is issued: at the unit boundary nothing waits
+    // for memory, and the lookup does not delay the first copy.
+    int u = cluster;
+    Unit un;
+    bool have = next_valid(u, un);
+    int raw0 = have ? raw_blocks(un, 0) : kNoPage, raw1 = have ? raw_blocks(un, 4) : kNoPage;
+    while (ok && have) {
+      int u2 = u + n_clusters;
+      Unit nx;
+      bool have_n = false;
+      int nraw0 = kNoPage, nraw1 = kNoPage;
       auto load_blocks = [&](int j0) -> int {
-        const int jt = j0 + (lane >> 3);
-        if (jt >= un.n_tiles) return -1;
-        return page_block((un.kt0 + jt) * kSN + (lane & 7) * kPage, un.k_lo, un.k_hi, un.pt, p.num_pages,
-                          kSlidingHkv, un.g, p.err);
+        return page_check(raw_blocks(un, j0), p.num_pages, kSlidingHkv, un.g, p.err);
       };
-      int blk_cur = load_blocks(0), blk_next = load_blocks(4);
+      int blk_cur = page_check(raw0, p.num_pages, kSlidingHkv, un.g, p.err);
+      int blk_next = page_check(raw1, p.num_pages, kSlidingHkv, un.g, p.err);
       const int n_slots = is_v ? un.n_tiles : un.n_tiles + 1;
       for (int idx = 0; idx < n_slots; ++idx, ++c) {
         const int s = c % n_st;
@@ -261,9 +271,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
         __syncwarp();
+        if (idx == 0) {
+          have_n = next_valid(u2, nx);
+          if (!is_v && have_n && lane == 0) {   // the next unit's roped Q tile into L2, a unit ahead of its load
+#pragma unroll
+            for (int c2 = 0; c2 < kSD / 64; ++c2) tma_prefetch_l2_3d(&tmap_q, 64 * c2, nx.h, max(nx.q_row0, 0));
+          }
+          if (have_n) {
+            nraw0 = raw_blocks(nx, 0);
+            nraw1 = raw_blocks(nx, 4);
+          }
+        }
       }
       if (!is_v) vt += un.n_tiles;
       ++uq;
+      un = nx;
+      u = u2;
+      have = have_n;
+      raw0 = nraw0;
+      raw1 = nraw1;
     }
     if (lane == 0 && *abort_flag) {   // drain copies still in flight (bounded) before the CTA may exit
       const unsigned long long w0 = globaltimer();
@@ -446,9 +472,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       return __shfl_sync(0xffffffffu, okr, 0);
     };
 
-    Unit cur;
+    // The unit after the current one is looked up at the start of the current one, while the
+    // softmax waits for its first scores, so that moving its Q never waits for the lookup.
+    Unit cur, nxt;
     bool have = next_unit(cur);
     if (have) ok = move_q(cur, c0, uq);
+    bool have_n = have && next_unit(nxt);
     while (ok && have) {
       const int pos = kBM * cur.t + r;
       const bool row_ok = pos >= cur.p_lo && pos <= cur.p_hi;
@@ -541,8 +570,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
       // The next unit's Q goes into tensor memory now (this unit's QK^T are all done), so that
       // its first QK^T runs while this unit's O is written out.
-      Unit nxt;
-      const bool have_n = next_unit(nxt);
       const uint32_t c0n = c0 + cur.n_tiles + 1;
       if (have_n && !move_q(nxt, c0n, uq + 1)) {
         ok = false;
@@ -582,6 +609,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ++uq;
       cur = nxt;
       have = have_n;
+      if (have) have_n = next_unit(nxt);
     }
   }
 

@@ -31,17 +31,23 @@ struct PrefillParams {
 
 // Finds this CTA's (sequence, query tile) among all sequences' tiles: slot s of sequence b
 // is its tile (last - s), so every sequence is walked from its most expensive tile down.
-// Warp-wide; returns b = -1 when the slot is past the last tile.
-inline __device__ void find_unit(const SeqRows& rows, int slot, int& out_b, int& out_t) {
+// Warp-wide; returns b = -1 when the slot is past the last tile. The per-sequence arrays are
+// read through the read-only path: a CTA reads them again for every unit it computes, and they
+// then come from L1 instead of costing an L2 round trip each time.
+// With `fields` set, the sequence's ctx_start, q_len and q_start come back in fields[0..2], read
+// in the same round trip as the search.
+inline __device__ void find_unit(const SeqRows& rows, int slot, int& out_b, int& out_t, int* fields = nullptr) {
   const int lane = threadIdx.x & 31;
   int base = 0;
   out_b = -1;
   out_t = 0;
   for (int b0 = 0; b0 < rows.B; b0 += 32) {
     const int b = b0 + lane;
-    int cnt = 0, tl = 0;
+    int cnt = 0, tl = 0, L = 0, cs = 0, qs = 0;
     if (b < rows.B) {
-      const int L = rows.q_len[b], cs = rows.ctx_start[b];
+      L = __ldg(rows.q_len + b);
+      cs = __ldg(rows.ctx_start + b);
+      if (fields) qs = __ldg(rows.q_start + b);
       if (L > 0 && cs >= 0) {
         tl = (cs + L - 1) / kBM;
         cnt = tl - cs / kBM + 1;
@@ -62,6 +68,11 @@ inline __device__ void find_unit(const SeqRows& rows, int slot, int& out_b, int&
       const int t_last = __shfl_sync(0xffffffffu, tl, src);
       out_b = b0 + src;
       out_t = t_last - (slot - base - e);
+      if (fields) {
+        fields[0] = __shfl_sync(0xffffffffu, cs, src);
+        fields[1] = __shfl_sync(0xffffffffu, L, src);
+        fields[2] = __shfl_sync(0xffffffffu, qs, src);
+      }
       return;
     }
     base += __shfl_sync(0xffffffffu, incl, 31);
@@ -79,6 +90,25 @@ inline __device__ int page_block(int key0, int k_lo, int k_hi, const int32_t* pt
     return -1;
   }
   return phys * hkv + g;
+}
+
+// The same lookup in two steps, so that the page-table load can be issued a unit ahead of its
+// use: page_raw returns the table entry of the page holding keys key0 .. key0+15 (kNoPage when
+// the page lies outside [k_lo, k_hi]), page_check turns it into a page-head block index or -1
+// (setting the error word for an entry outside the pool).
+constexpr int kNoPage = -2147483647 - 1;
+inline __device__ int page_raw(int key0, int k_lo, int k_hi, const int32_t* pt) {
+  if (key0 + kPage - 1 < k_lo || key0 > k_hi) return kNoPage;
+  const int v = __ldg(pt + (key0 >> 4));
+  return v == kNoPage ? -1 : v;
+}
+inline __device__ int page_check(int raw, int num_pages, int hkv, int g, uint32_t* err) {
+  if (raw == kNoPage) return -1;
+  if (raw < 0 || raw >= num_pages) {
+    set_error(err, kErrPage);
+    return -1;
+  }
+  return raw * hkv + g;
 }
 
 inline __device__ uint32_t tmem_lane_base(int warp) { return (uint32_t)(32 * (warp & 3)) << 16; }

@@ -74,7 +74,8 @@ class Batch:
         g4.g4attn_kv_append(layer, k, v, device_int32(lay.q_start), device_int32(lay.q_len),
                             device_int32([0] * len(lens)), cache.desc, table)
 
-    def run(self, layer, out_fill=float("nan")):
+    def run(self, layer, out_fill=float("nan"), split=False):
+        """One prefill of the batch: g4attn_prefill, or (split) its two steps called apart."""
         cache = self.device_cache()
         table = self.plan.table.cuda()
         self.append_history(layer, cache, table)
@@ -82,8 +83,12 @@ class Batch:
         k = self.k_rows.cuda()
         v = None if self.v_rows is None else self.v_rows.cuda()
         out = torch.full_like(q, out_fill)
-        g4.g4attn_prefill(layer, q, k, v, device_int32(self.layout.q_start), device_int32(self.layout.q_len),
-                          device_int32(self.layout.ctx_start), cache.desc, table, out)
+        rows = (device_int32(self.layout.q_start), device_int32(self.layout.q_len), device_int32(self.layout.ctx_start))
+        if split:
+            g4.g4attn_prefill_stage(layer, q, k, v, *rows, cache.desc, table, out)
+            g4.g4attn_prefill_attend(layer, *rows, cache.desc, table, out)
+        else:
+            g4.g4attn_prefill(layer, q, k, v, *rows, cache.desc, table, out)
         torch.cuda.synchronize()
         st = g4.g4attn_status_sync()
         assert st == g4.G4_OK, g4.status_string(st)

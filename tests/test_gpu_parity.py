@@ -216,3 +216,15 @@ def test_prefill_global_batch_invariance():
         bt.k_rows = gi.rows_of(bt.hist_k, bt.layout)
         out_b, _ = bt.run(layer)
         assert torch.equal(out_a[:L].cpu(), out_b[s:s + L].cpu()), (lens, padded, at)
+
+
+@pytest.mark.parametrize("kind", ["sliding", "global"])
+def test_prefill_split_steps_equal_prefill(kind):
+    """g4attn_prefill_stage then g4attn_prefill_attend give exactly g4attn_prefill's bits."""
+    layer, _ = layers(kind, 1024)
+    lens, starts = [300, 1, 129, 700], [0, 40, 256, 1000]
+    whole, cache_a = Batch(kind, lens, ctx_starts=starts, seed=21, scale=0.5).run(layer)
+    split, cache_b = Batch(kind, lens, ctx_starts=starts, seed=21, scale=0.5).run(layer, split=True)
+    # bit patterns: rows outside every sequence and unwritten cache slots hold NaN in both
+    assert torch.equal(whole.cpu().view(torch.int16), split.cpu().view(torch.int16))
+    assert torch.equal(cache_a.k.cpu().view(torch.int16), cache_b.k.cpu().view(torch.int16))
