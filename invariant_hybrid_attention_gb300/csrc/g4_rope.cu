@@ -135,9 +135,21 @@ struct RotatedOnly<RotDst> {
   static constexpr bool value = true;
 };
 
+// (cos, sin) of this lane's P pairs at position pos (lanes whose pairs do not turn skip it). One
+// row's vectors all turn by the same angles, so a row computes them once for all its heads.
+template <int D, int R>
+__device__ __forceinline__ void rope_cs_lane(const RopeTables& tb, int pos, float2 (&cs)[D / 64]) {
+  constexpr int P = D / 64;
+  const int t0 = (threadIdx.x & 31) * P;
+  if (t0 < R) {
+#pragma unroll
+    for (int i = 0; i < P; ++i) cs[i] = rope_cs(tb, t0 + i, pos);
+  }
+}
+
 template <int D, int R, class Dst>
-__device__ __forceinline__ void rope_vec_warp(const __nv_bfloat16* __restrict__ src, const Dst& dst, int pos,
-                                              const RopeTables& tb) {
+__device__ __forceinline__ void rope_vec_warp_cs(const __nv_bfloat16* __restrict__ src, const Dst& dst,
+                                                 const float2 (&cs)[D / 64]) {
   constexpr int P = D / 64;                    // 4 (D=256) or 8 (D=512)
   constexpr int half = D / 2;
   const int lane = threadIdx.x & 31;
@@ -152,8 +164,8 @@ __device__ __forceinline__ void rope_vec_warp(const __nv_bfloat16* __restrict__ 
     for (int w = 0; w < P / 2; ++w) {
       float a0 = bf16_lo(lw[w]), a1 = bf16_hi(lw[w]);
       float b0 = bf16_lo(hw[w]), b1 = bf16_hi(hw[w]);
-      rope_pair(a0, b0, rope_cs(tb, t0 + 2 * w, pos));
-      rope_pair(a1, b1, rope_cs(tb, t0 + 2 * w + 1, pos));
+      rope_pair(a0, b0, cs[2 * w]);
+      rope_pair(a1, b1, cs[2 * w + 1]);
       lw[w] = pack_bf16(a0, a1);
       hw[w] = pack_bf16(b0, b1);
     }
@@ -162,6 +174,51 @@ __device__ __forceinline__ void rope_vec_warp(const __nv_bfloat16* __restrict__ 
   if (RotatedOnly<Dst>::value && t0 >= R) return;
   *reinterpret_cast<Vec*>(dst.at(t0)) = lo;
   *reinterpret_cast<Vec*>(dst.at(half + t0)) = hi;
+}
+
+template <int D, int R, class Dst>
+__device__ __forceinline__ void rope_vec_warp(const __nv_bfloat16* __restrict__ src, const Dst& dst, int pos,
+                                              const RopeTables& tb) {
+  float2 cs[D / 64];
+  rope_cs_lane<D, R>(tb, pos, cs);
+  rope_vec_warp_cs<D, R>(src, dst, cs);
+}
+
+// The same rotation with 8 pairs per lane, so that every load and store is 16 bytes, one
+// core-matrix row of a tiled page: D/16 lanes per vector, 32/(D/16) vectors per warp (two when
+// D = 256). Lane l handles pairs (l % (D/16)) * 8 .. + 7 of vector l / (D/16); the caller passes
+// that vector's source and destination. cs comes from rope_cs_lane8.
+template <int D, int R>
+__device__ __forceinline__ void rope_cs_lane8(const RopeTables& tb, int pos, float2 (&cs)[8]) {
+  const int t0 = ((threadIdx.x & 31) % (D / 16)) * 8;
+  if (t0 < R) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) cs[i] = rope_cs(tb, t0 + i, pos);
+  }
+}
+template <int D, int R, class Dst>
+__device__ __forceinline__ void rope_vec8_cs(const __nv_bfloat16* __restrict__ src, const Dst& dst,
+                                             const float2 (&cs)[8]) {
+  constexpr int half = D / 2;
+  const int t0 = ((threadIdx.x & 31) % (D / 16)) * 8;
+  uint4 lo = *reinterpret_cast<const uint4*>(src + t0);
+  uint4 hi = *reinterpret_cast<const uint4*>(src + half + t0);
+  if (t0 < R) {
+    uint32_t* lw = reinterpret_cast<uint32_t*>(&lo);
+    uint32_t* hw = reinterpret_cast<uint32_t*>(&hi);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      float a0 = bf16_lo(lw[w]), a1 = bf16_hi(lw[w]);
+      float b0 = bf16_lo(hw[w]), b1 = bf16_hi(hw[w]);
+      rope_pair(a0, b0, cs[2 * w]);
+      rope_pair(a1, b1, cs[2 * w + 1]);
+      lw[w] = pack_bf16(a0, a1);
+      hw[w] = pack_bf16(b0, b1);
+    }
+  }
+  if (RotatedOnly<Dst>::value && t0 >= R) return;
+  *reinterpret_cast<uint4*>(dst.at(t0)) = lo;
+  *reinterpret_cast<uint4*>(dst.at(half + t0)) = hi;
 }
 
 template <int D, class Dst>
@@ -207,6 +264,40 @@ cudaError_t launch_rope_apply(bool global, const void* x, const int32_t* pos, in
 // ---- paged KV append ----------------------------------------------------------------------------
 // Writes one token's Hkv vectors into its page slot: sliding K' = bf16(RoPE(k)) and V as given;
 // global S as given (K==V: the one stored projection, rotated only where it is read as K).
+// cs: the lane's (cos, sin) at the token's position (rope_cs_lane); pos is in range.
+template <int D, int R, int HKV, bool SHARED>
+__device__ __forceinline__ void append_token_cs(const __nv_bfloat16* k_row, const __nv_bfloat16* v_row, int b, int pos,
+                                                const PagedCache& c, const float2 (&cs)[8], uint32_t* err) {
+  constexpr int VPW = 32 / (D / 16);   // vectors per warp instruction of rope_vec8_cs
+  const int lane = threadIdx.x & 31;
+  const int phys = c.page_table[(size_t)b * c.max_pages + (pos >> 4)];
+  if (phys < 0 || phys >= c.num_pages) {
+    if (lane == 0) set_error(err, kErrPage);
+    return;
+  }
+  const int j = pos & 15;
+#pragma unroll 2
+  for (int g0 = 0; g0 < HKV; g0 += VPW) {
+    const int g = g0 + lane / (D / 16);   // this lane's KV head for the rotation
+    const size_t blk = ((size_t)phys * HKV + g) * kPage * D;   // page-head block
+    if (SHARED) {
+      // The rotated columns once more, roped (the K side of K==V where it differs from S).
+      rope_vec8_cs<D, R>(k_row + (size_t)g * D,
+                         RotDst{(__nv_bfloat16*)c.krot + ((size_t)phys * HKV + g) * kRotPageElems, j}, cs);
+    } else {
+      rope_vec8_cs<D, R>(k_row + (size_t)g * D, PageDst<D>{(__nv_bfloat16*)c.k + blk, j}, cs);
+    }
+#pragma unroll
+    for (int gv = g0; gv < g0 + VPW; ++gv) {   // S (global) or V (sliding) as given, a warp per vector
+      const size_t blkv = ((size_t)phys * HKV + gv) * kPage * D;
+      if (SHARED)
+        copy_vec_warp<D>(k_row + (size_t)gv * D, PageDst<D>{(__nv_bfloat16*)c.k + blkv, j});
+      else
+        copy_vec_warp<D>(v_row + (size_t)gv * D, VDst{(__nv_bfloat16*)c.v + blkv, j});
+    }
+  }
+}
+
 template <int D, int R, int HKV, bool SHARED>
 __device__ __forceinline__ void append_token(const __nv_bfloat16* k_row, const __nv_bfloat16* v_row, int b, int pos,
                                              const PagedCache& c, const RopeTables& tb, uint32_t* err) {
@@ -215,24 +306,9 @@ __device__ __forceinline__ void append_token(const __nv_bfloat16* k_row, const _
     if (lane == 0) set_error(err, kErrPos);
     return;
   }
-  const int phys = c.page_table[(size_t)b * c.max_pages + (pos >> 4)];
-  if (phys < 0 || phys >= c.num_pages) {
-    if (lane == 0) set_error(err, kErrPage);
-    return;
-  }
-  const int j = pos & 15;
-  for (int g = 0; g < HKV; ++g) {
-    const size_t blk = ((size_t)phys * HKV + g) * kPage * D;   // page-head block
-    if (SHARED) {
-      copy_vec_warp<D>(k_row + (size_t)g * D, PageDst<D>{(__nv_bfloat16*)c.k + blk, j});
-      // The rotated columns once more, roped (the K side of K==V where it differs from S).
-      rope_vec_warp<D, R>(k_row + (size_t)g * D,
-                          RotDst{(__nv_bfloat16*)c.krot + ((size_t)phys * HKV + g) * kRotPageElems, j}, pos, tb);
-    } else {
-      rope_vec_warp<D, R>(k_row + (size_t)g * D, PageDst<D>{(__nv_bfloat16*)c.k + blk, j}, pos, tb);
-      copy_vec_warp<D>(v_row + (size_t)g * D, VDst{(__nv_bfloat16*)c.v + blk, j});
-    }
-  }
+  float2 cs[8];
+  rope_cs_lane8<D, R>(tb, pos, cs);
+  append_token_cs<D, R, HKV, SHARED>(k_row, v_row, b, pos, c, cs, err);
 }
 
 // One warp per row of the prefill batch; the owning sequence is found by a scan over B.
@@ -263,13 +339,22 @@ __global__ void __launch_bounds__(256) append_prefill_kernel(const __nv_bfloat16
   }
   if (owner < 0) return;
   const int pos = rows.ctx_start[owner] + (r - rows.q_start[owner]);
-  if (q_out != nullptr && pos >= 0 && pos < kMaxPos) {
-#pragma unroll 1
-    for (int h = 0; h < HQ; ++h)
-      rope_vec_warp<D, R>(q + ((size_t)r * HQ + h) * D, RowDst{q_out + ((size_t)r * HQ + h) * D}, pos, tb);
+  if (pos < 0 || pos >= kMaxPos || (pos >> 4) >= cache.max_pages) {
+    if (lane == 0) set_error(err, kErrPos);
+    return;
   }
-  append_token<D, R, HKV, SHARED>(k + (size_t)r * HKV * D, SHARED ? nullptr : v + (size_t)r * HKV * D, owner, pos,
-                                  cache, tb, err);
+  float2 cs[8];   // the row's angles, shared by its query heads and its key heads
+  rope_cs_lane8<D, R>(tb, pos, cs);
+  if (q_out != nullptr) {
+    constexpr int VPW = 32 / (D / 16);
+#pragma unroll 4
+    for (int h0 = 0; h0 < HQ; h0 += VPW) {
+      const size_t v = (size_t)r * HQ + h0 + lane / (D / 16);
+      rope_vec8_cs<D, R>(q + v * D, RowDst{q_out + v * D}, cs);
+    }
+  }
+  append_token_cs<D, R, HKV, SHARED>(k + (size_t)r * HKV * D, SHARED ? nullptr : v + (size_t)r * HKV * D, owner, pos,
+                                     cache, cs, err);
 }
 
 template <int D, int R, int HKV, bool SHARED>
