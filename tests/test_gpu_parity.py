@@ -228,3 +228,30 @@ def test_prefill_split_steps_equal_prefill(kind):
     # bit patterns: rows outside every sequence and unwritten cache slots hold NaN in both
     assert torch.equal(whole.cpu().view(torch.int16), split.cpu().view(torch.int16))
     assert torch.equal(cache_a.k.cpu().view(torch.int16), cache_b.k.cpu().view(torch.int16))
+
+
+@pytest.mark.parametrize("kind", ["sliding", "global"])
+def test_chunked_prefill_is_bit_identical_to_one_prefill(kind):
+    """A sequence prefilled in chunks (each chunk reading the earlier keys from the cache) gives the
+    same bits as one prefill of the whole sequence. Query tiles are aligned to absolute position
+    and a key tile with no visible key adds exact zeros, so a row's arithmetic does not depend on
+    where its chunk starts. Cuts fall mid-tile, on tile edges and one row from them; the last
+    pattern ends in one-row chunks, i.e. decode steps run through g4attn_prefill."""
+    layer, _ = layers(kind, 1024)
+    L = 1500
+    full = Batch(kind, [L], seed=31, scale=0.5)
+    out_full, _ = full.run(layer)
+    ref = out_full[:L].cpu().view(torch.int16)
+    for cuts in ([700], [333, 1029], [1, 127, 128, 1281], [1497, 1498, 1499]):
+        edges = [0] + cuts + [L]
+        for a, b in zip(edges[:-1], edges[1:]):
+            ch = Batch(kind, [b - a], ctx_starts=[a], seed=7 + a, scale=0.5)
+            ch.hist_k = [full.hist_k[0][:b]]
+            if full.hist_v is not None:
+                ch.hist_v = [full.hist_v[0][:b]]
+            ch.q[:b - a] = full.q[a:b]
+            ch.k_rows = gi.rows_of(ch.hist_k, ch.layout)
+            ch.v_rows = None if ch.hist_v is None else gi.rows_of(ch.hist_v, ch.layout)
+            out_c, _ = ch.run(layer)
+            got = out_c[:b - a].cpu().view(torch.int16)
+            assert torch.equal(got, ref[a:b]), (kind, cuts, a, b)
