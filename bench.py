@@ -298,6 +298,20 @@ def oracle_sample(budget_s: float, seed: int = 1):
     return done_flops / dt / 1e12, rows, dt
 
 
+def max_over_ranks(ms: dict, dist, device) -> dict:
+    """Each named time (ms) as the maximum over all ranks: the job is as slow as its slowest rank."""
+    import torch
+    names = sorted(ms)
+    t = torch.tensor([float(ms[n]) for n in names], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return dict(zip(names, (float(x) for x in t.tolist())))
+
+
+def job_tflops(flops_per_step: float, steps: int, world: int, ms: float):
+    """Whole-job throughput: the work of all ranks (replicas) over the max-over-ranks time."""
+    return flops_per_step * steps * world / (ms * 1e-3) / 1e12 if ms > 0 else None
+
+
 def cpu_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -457,18 +471,12 @@ def main():
     tot = {n: sum(v) for n, v in times.items()}          # ms over K steps
     ktot = {n: sum(v) for n, v in kern_times.items()}
     if dist is not None:
-        names = [n for n, _ in sp] + [f"kernel:{n}" for n in ktot]
-        t = torch.tensor([tot[n] for n, _ in sp] + [ktot[n] for n in ktot], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        vals = dict(zip(names, t.tolist()))
-        tot = {n: float(vals[n]) for n, _ in sp}
-        ktot = {n: float(vals[f"kernel:{n}"]) for n in ktot}
+        tot = max_over_ranks(tot, dist, "cuda")
+        ktot = max_over_ranks(ktot, dist, "cuda")
     K = args.steps
     pk = peaks()
     res = {}
-    pre_flops = sum(p.flops for p in parts) * K * world
-    pre_ms = sum(tot[p.name] for p in parts)
-    value = pre_flops / (pre_ms * 1e-3) / 1e12 if pre_ms > 0 else None
+    value = job_tflops(sum(p.flops for p in parts), K, world, sum(tot[p.name] for p in parts))
 
     # the attention kernel of each prefill part, timed on its own (event between the two launches)
     roofs = []
