@@ -33,6 +33,11 @@ Readings of points the pages leave open (each is listed in the design notes):
   are capped, RFC §2).
 * Positions are the index within the sequence: 0 .. L-1; a decode query sits at L-1.
 * GQA: KV head g serves query heads g*G .. g*G+G-1 with G = Hq / Hkv.
+* Per-head norms (RFC §5 row ``qk_rmsnorm_d256_d512``; TensorFold's ``tf_qk_rows_once``, which
+  "can norm v by a unit RMS norm"), optional and applied to the raw projections before RoPE:
+  n(x) = x / sqrt(mean(x^2 over the head dim) + eps). q -> w_q * n(q) and k -> w_k * n(k) with
+  per-dim weights; v -> n(v) (unit, no weight). On a K==V layer the one projection S gives
+  K = w_k * n(S) and V = n(S). The pages do not give eps; it is a parameter (1e-6 by default).
 
 Parity pins for every function here live in ``tests/test_oracle.py``.
 """
@@ -75,6 +80,43 @@ MAX_POSITIONS = 262144
 def with_window(layer: Layer, window: int) -> Layer:
     return Layer(layer.kind, layer.n_q_heads, layer.n_kv_heads, layer.head_dim, int(window),
                  layer.rope_theta, layer.rope_partial, layer.kv_shared, layer.softmax_scale)
+
+
+# ---- per-head RMS norms (RFC §5 qk_rmsnorm_d256_d512) -------------------------------------
+
+@dataclass(frozen=True)
+class Norms:
+    q_weight: Optional[np.ndarray] = None   # [D] multiplier of the query norm; None: q is not normed
+    k_weight: Optional[np.ndarray] = None   # [D] multiplier of the key norm; None: k is not normed
+    v_norm: bool = False                    # values (V, or S read as V) get a unit RMS norm
+    eps: float = 1e-6
+
+
+def rms_norm(x: np.ndarray, weight: Optional[np.ndarray], eps: float) -> np.ndarray:
+    """x / sqrt(mean(x^2) + eps) over the last axis, times `weight` per element when given."""
+    x = np.asarray(x, dtype=np.float64)
+    y = x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + float(eps))
+    return y if weight is None else y * np.asarray(weight, dtype=np.float64)
+
+
+def normed_q(norms: Optional[Norms], q: np.ndarray) -> np.ndarray:
+    q = np.asarray(q, np.float64)
+    if norms is None or norms.q_weight is None:
+        return q
+    return rms_norm(q, norms.q_weight, norms.eps)
+
+
+def normed_kv(layer: "Layer", norms: Optional[Norms], k: np.ndarray, v: Optional[np.ndarray]):
+    """The key source and the values after the norms, before RoPE. K==V: both come from S."""
+    k = np.asarray(k, np.float64)
+    if layer.kv_shared:
+        kk = k if norms is None or norms.k_weight is None else rms_norm(k, norms.k_weight, norms.eps)
+        vv = k if norms is None or not norms.v_norm else rms_norm(k, None, norms.eps)
+        return kk, vv
+    v = np.asarray(v, np.float64)
+    kk = k if norms is None or norms.k_weight is None else rms_norm(k, norms.k_weight, norms.eps)
+    vv = v if norms is None or not norms.v_norm else rms_norm(v, None, norms.eps)
+    return kk, vv
 
 
 # ---- RoPE / p-RoPE (RFC §5 rows sliding_rope_d256 and global_proportional_p_rope) ----------
@@ -141,7 +183,8 @@ def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, q_pos, k_pos, window:
     return (p @ np.asarray(v, np.float64)) / p.sum(axis=1, keepdims=True)
 
 
-def keys_values(layer: Layer, k_hist: np.ndarray, v_hist: Optional[np.ndarray], pos_offset: int = 0):
+def keys_values(layer: Layer, k_hist: np.ndarray, v_hist: Optional[np.ndarray], pos_offset: int = 0,
+                norms: Optional[Norms] = None):
     """The rotated keys and the values of one sequence's history.
 
     k_hist: [L, Hkv, D] raw key projections (the shared S for a K==V layer);
@@ -151,28 +194,26 @@ def keys_values(layer: Layer, k_hist: np.ndarray, v_hist: Optional[np.ndarray], 
     k_hist = np.asarray(k_hist, np.float64)
     L = k_hist.shape[0]
     pos = np.arange(L, dtype=np.int64) + pos_offset
-    k_rot = rope(k_hist, pos[:, None], layer.rope_theta, layer.rope_partial)
     if layer.kv_shared:
         if v_hist is not None:
             raise ValueError("a K==V layer takes no separate V")
-        v = k_hist.copy()                  # V is the stored projection, un-rotated
-    else:
-        if v_hist is None:
-            raise ValueError("a sliding layer needs V")
-        v = np.asarray(v_hist, np.float64)
+    elif v_hist is None:
+        raise ValueError("a sliding layer needs V")
+    k_src, v = normed_kv(layer, norms, k_hist, v_hist)   # K==V without norms: V is S, un-rotated
+    k_rot = rope(k_src, pos[:, None], layer.rope_theta, layer.rope_partial)
     return k_rot, v
 
 
 def layer_rows(layer: Layer, q_rows: np.ndarray, q_pos: Sequence[int], k_hist: np.ndarray,
-               v_hist: Optional[np.ndarray], pos_offset: int = 0) -> np.ndarray:
+               v_hist: Optional[np.ndarray], pos_offset: int = 0, norms: Optional[Norms] = None) -> np.ndarray:
     """Attention output of one sequence's query rows.
 
     q_rows: [n, Hq, D] raw query projections at positions q_pos (each < L, measured from the
     first key); k_hist / v_hist as in `keys_values`. Returns [n, Hq, D] fp64.
     """
-    q_rows = np.asarray(q_rows, np.float64)
+    q_rows = normed_q(norms, q_rows)
     q_pos = np.asarray(q_pos, dtype=np.int64)
-    k_rot, v = keys_values(layer, k_hist, v_hist, pos_offset)
+    k_rot, v = keys_values(layer, k_hist, v_hist, pos_offset, norms)
     L = k_rot.shape[0]
     k_pos = np.arange(L, dtype=np.int64) + pos_offset
     qp = q_pos + pos_offset
@@ -186,7 +227,7 @@ def layer_rows(layer: Layer, q_rows: np.ndarray, q_pos: Sequence[int], k_hist: n
 
 
 def prefill(layer: Layer, q: np.ndarray, k_hist: Sequence[np.ndarray], v_hist, q_start: Sequence[int],
-            q_len: Sequence[int], ctx_start: Sequence[int]) -> np.ndarray:
+            q_len: Sequence[int], ctx_start: Sequence[int], norms: Optional[Norms] = None) -> np.ndarray:
     """Batched prefill: rows q_start[b] .. +q_len[b] of q [T, Hq, D] are sequence b's positions
     ctx_start[b] .. ctx_start[b]+q_len[b]-1; k_hist[b] holds that sequence's keys at positions
     0 .. ctx_start[b]+q_len[b]-1. Rows of q outside every sequence come back as NaN."""
@@ -197,15 +238,16 @@ def prefill(layer: Layer, q: np.ndarray, k_hist: Sequence[np.ndarray], v_hist, q
         if L == 0:
             continue
         vb = None if v_hist is None else v_hist[b][:c + L]
-        out[s:s + L] = layer_rows(layer, q[s:s + L], np.arange(c, c + L), k_hist[b][:c + L], vb)
+        out[s:s + L] = layer_rows(layer, q[s:s + L], np.arange(c, c + L), k_hist[b][:c + L], vb, 0, norms)
     return out
 
 
-def decode_row(layer: Layer, q_new: np.ndarray, k_hist: np.ndarray, v_hist: Optional[np.ndarray]) -> np.ndarray:
+def decode_row(layer: Layer, q_new: np.ndarray, k_hist: np.ndarray, v_hist: Optional[np.ndarray],
+               norms: Optional[Norms] = None) -> np.ndarray:
     """One decode step: the query [Hq, D] sits at position L-1 where L = len(k_hist), and the
     history already holds the new token's key/value at L-1. Written head by head, key by key."""
-    q_new = np.asarray(q_new, np.float64)
-    k_rot, v = keys_values(layer, k_hist, v_hist)
+    q_new = normed_q(norms, q_new)
+    k_rot, v = keys_values(layer, k_hist, v_hist, 0, norms)
     L = k_rot.shape[0]
     p = L - 1
     qr = rope(q_new, np.full((layer.n_q_heads,), p), layer.rope_theta, layer.rope_partial)

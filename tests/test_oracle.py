@@ -168,7 +168,119 @@ def check_outside_perturbation(o, layer, L=90, seed=5):
     assert np.abs(o.layer_rows(layer, q[[i]], [i], k3, v) - base).max() > 1e-6
 
 
+def check_rms_norm_closed_form(o, seed=11):
+    """The unit norm keeps each vector's direction and gives mean(y^2) = ms / (ms + eps), where
+    ms is the input's mean square."""
+    r = rng(seed)
+    x = r.standard_normal((5, 3, 64)) * 3.0
+    eps = 0.25
+    y = o.rms_norm(x, None, eps)
+    ms = (x * x).mean(axis=-1)
+    assert np.allclose((y * y).mean(axis=-1), ms / (ms + eps), rtol=1e-12, atol=0)
+    c = y / x
+    assert (c > 0).all() and np.allclose(c, c[..., :1], rtol=1e-12, atol=0)
+
+
+def check_rms_norm_vs_torch(o, seed=12):
+    r = rng(seed)
+    for D in (256, 512):
+        x = r.standard_normal((4, 2, D)) * 2.0
+        w = r.standard_normal(D)
+        for weight in (w, None):
+            ref = F.rms_norm(torch.from_numpy(x), (D,), weight=None if weight is None else torch.from_numpy(w),
+                             eps=1e-6).numpy()
+            assert np.abs(o.rms_norm(x, weight, 1e-6) - ref).max() < 1e-12
+
+
+def normed_inputs(layer, L, seed, k_weight=True, q_weight=True, v_norm=True, eps=1e-6):
+    r = rng(seed)
+    D = layer.head_dim
+    q = r.standard_normal((L, layer.n_q_heads, D)) * 1.7
+    k = r.standard_normal((L, layer.n_kv_heads, D)) * 0.6
+    v = None if layer.kv_shared else r.standard_normal((L, layer.n_kv_heads, D)) * 2.2
+    norms = oracle.Norms(q_weight=r.uniform(0.5, 1.5, D) if q_weight else None,
+                         k_weight=r.uniform(0.5, 1.5, D) if k_weight else None, v_norm=v_norm, eps=eps)
+    return q, k, v, norms
+
+
+def check_normed_layer_vs_torch(o, layer, L=24, seed=14, **kw):
+    """A normed layer against torch: F.rms_norm on the raw projections (K==V: K = w_k n(S), V = n(S)),
+    the oracle's own pinned rope, and SDPA with the GQA heads repeated by torch."""
+    q, k, v, norms = normed_inputs(layer, L, seed, **kw)
+    got = o.layer_rows(layer, q, np.arange(L), k, v, 0, norms)
+    D = layer.head_dim
+
+    def tn(x, w):
+        return F.rms_norm(torch.from_numpy(x), (D,), weight=None if w is None else torch.from_numpy(w),
+                          eps=norms.eps).numpy()
+    qn = q if norms.q_weight is None else tn(q, norms.q_weight)
+    kn = k if norms.k_weight is None else tn(k, norms.k_weight)
+    vsrc = k if layer.kv_shared else v
+    vn = tn(vsrc, None) if norms.v_norm else vsrc
+    pos = np.arange(L)[:, None]
+    qr = oracle.rope(qn, pos, layer.rope_theta, layer.rope_partial)
+    kr = oracle.rope(kn, pos, layer.rope_theta, layer.rope_partial)
+    tq = torch.from_numpy(qr).permute(1, 0, 2)[None]
+    tk = torch.from_numpy(kr).permute(1, 0, 2).repeat_interleave(layer.group, dim=0)[None]
+    tv = torch.from_numpy(vn).permute(1, 0, 2).repeat_interleave(layer.group, dim=0)[None]
+    ones = torch.ones(L, L, dtype=torch.bool)
+    mask = torch.tril(ones)
+    if layer.window > 0:
+        mask &= torch.triu(ones, diagonal=-(layer.window - 1))
+    ref = F.scaled_dot_product_attention(tq, tk, tv, attn_mask=mask,
+                                         scale=1.0 / math.sqrt(D))[0].permute(1, 0, 2).numpy()
+    assert np.abs(got - ref).max() < 1e-11
+
+
+def check_norm_scale_invariance(o, layer, L=30, seed=13):
+    """With q, k and v normed (eps far below the inputs' mean square), scaling any raw q, k or v
+    vector by a positive factor leaves every output unchanged; without the norms it does not."""
+    q, k, v, norms = normed_inputs(layer, L, seed, eps=1e-14)
+    r = rng(seed + 1)
+    cq = r.uniform(0.1, 10.0, (L, layer.n_q_heads, 1))
+    ck = r.uniform(0.1, 10.0, (L, layer.n_kv_heads, 1))
+    v2 = None if v is None else v * r.uniform(0.1, 10.0, (L, layer.n_kv_heads, 1))
+    base = o.layer_rows(layer, q, np.arange(L), k, v, 0, norms)
+    got = o.layer_rows(layer, q * cq, np.arange(L), k * ck, v2, 0, norms)
+    assert np.abs(got - base).max() < 1e-9
+    raw = o.layer_rows(layer, q * cq, np.arange(L), k * ck, v2) - o.layer_rows(layer, q, np.arange(L), k, v)
+    assert np.abs(raw).max() > 1e-3
+
+
 # ---------------------------------------------------------------- the pins
+
+
+def test_rms_norm_closed_form():
+    check_rms_norm_closed_form(oracle)
+
+
+def test_rms_norm_matches_torch():
+    check_rms_norm_vs_torch(oracle)
+
+
+@pytest.mark.parametrize("layer,kw", [
+    (oracle.with_window(oracle.SLIDING, 8), {}),
+    (oracle.with_window(oracle.SLIDING, 8), dict(k_weight=False, v_norm=False)),
+    (oracle.with_window(oracle.SLIDING, 8), dict(q_weight=False)),
+    (oracle.GLOBAL, {}),
+    (oracle.GLOBAL, dict(k_weight=False, v_norm=False)),
+], ids=["sliding-all", "sliding-q-only", "sliding-kv-only", "global-all", "global-q-only"])
+def test_normed_layer_matches_torch(layer, kw):
+    check_normed_layer_vs_torch(oracle, layer, **kw)
+
+
+@pytest.mark.parametrize("layer", [oracle.with_window(oracle.SLIDING, 8), oracle.GLOBAL], ids=["sliding", "global"])
+def test_normed_outputs_do_not_depend_on_input_scale(layer):
+    check_norm_scale_invariance(oracle, layer)
+
+
+def test_normed_decode_row_equals_prefill_row():
+    for layer in (oracle.with_window(oracle.SLIDING, 16), oracle.GLOBAL):
+        q, k, v, norms = normed_inputs(layer, 40, 15)
+        rows = oracle.layer_rows(layer, q, np.arange(40), k, v, 0, norms)
+        for p in (0, 17, 39):
+            d = oracle.decode_row(layer, q[p], k[:p + 1], None if v is None else v[:p + 1], norms)
+            assert np.abs(d - rows[p]).max() < 1e-12
 
 def test_geometry_matches_checkpoint_fingerprint():
     check_geometry(oracle)
@@ -378,8 +490,8 @@ def test_control_frequency_denominator(monkeypatch):
 def test_control_values_rotated(monkeypatch):
     good = oa.keys_values
 
-    def rotated_v(layer, k_hist, v_hist, pos_offset=0):
-        k_rot, v = good(layer, k_hist, v_hist, pos_offset)
+    def rotated_v(layer, k_hist, v_hist, pos_offset=0, norms=None):
+        k_rot, v = good(layer, k_hist, v_hist, pos_offset, norms)
         return k_rot, (k_rot.copy() if layer.kv_shared else v)
     monkeypatch.setattr(oa, "keys_values", rotated_v)
     assert _fails(check_q_zero_mean, oa, oracle.GLOBAL)
@@ -407,3 +519,28 @@ def test_control_gqa_mapping(monkeypatch):
         return out
     monkeypatch.setattr(oa, "layer_rows", modulo_rows)
     assert _fails(check_layer_vs_sdpa, oa, oracle.GLOBAL)
+
+
+def test_control_norm_weight_inside(monkeypatch):
+    # The weight applied before the normalisation instead of after it.
+    good = oa.rms_norm
+    monkeypatch.setattr(oa, "rms_norm", lambda x, w, eps: good(np.asarray(x) * (1.0 if w is None else w), None, eps))
+    assert _fails(check_normed_layer_vs_torch, oa, oracle.with_window(oracle.SLIDING, 8))
+    assert _fails(check_normed_layer_vs_torch, oa, oracle.GLOBAL)
+
+
+def test_control_k_eq_v_values_take_the_key_weight(monkeypatch):
+    # K==V with V normed by the key's weighted norm instead of the unit norm.
+    good = oa.normed_kv
+
+    def wrong(layer, norms, k, v):
+        kk, vv = good(layer, norms, k, v)
+        return kk, (kk.copy() if layer.kv_shared and norms is not None and norms.k_weight is not None else vv)
+    monkeypatch.setattr(oa, "normed_kv", wrong)
+    assert _fails(check_normed_layer_vs_torch, oa, oracle.GLOBAL)
+
+
+def test_control_norm_missing_on_queries(monkeypatch):
+    monkeypatch.setattr(oa, "normed_q", lambda norms, q: np.asarray(q, np.float64))
+    assert _fails(check_normed_layer_vs_torch, oa, oracle.GLOBAL)
+    assert _fails(check_norm_scale_invariance, oa, oracle.with_window(oracle.SLIDING, 8))
