@@ -107,6 +107,28 @@ typedef struct {
   int32_t kv_shared;      /* 1: K==V, the cache holds one tensor S */
 } g4attn_layer;
 
+/* Optional per-head RMS norms of the raw projections, applied before RoPE (RFC section 5, work
+ * item qk_rmsnorm_d256_d512; TensorFold "cuda gemma4: images on the 31B", tf_qk_rows_once, which
+ * can also norm v by a unit RMS norm). For a head vector x of head_dim elements:
+ *   n(x) = x / sqrt(mean(x^2) + eps), computed in fp32 before the rotation and the declared cast;
+ *   q -> q_weight * n(q)   when q_weight is set,
+ *   k -> k_weight * n(k)   when k_weight is set,
+ *   v -> n(v)              when v_norm is 1 (a unit norm, no weight).
+ * On a K==V (global) layer the one projection S gives K = k_weight * n(S) and V = n(S): the
+ * cache stores n(S) once, the k_rot pages hold RoPE(k_weight * n(S)), and the library carries
+ * k_weight into the queries' un-rotated dims, where the attention reads K from the stored S.
+ * There k_weight and v_norm must come together (both or neither; G4_ERR_UNSUPPORTED otherwise).
+ * The weights are whatever multiplies the normalised vector: for a checkpoint that stores a
+ * zero-centred Gemma weight g, pass 1 + g. Decode queries are normed (and, on K==V layers,
+ * multiplied by k_weight on their un-rotated dims) into `out` first, with a bf16 cast there,
+ * one declared cast more than prefill has. */
+typedef struct {
+  const void* q_weight;   /* bf16 [head_dim], device, 16-byte aligned, or NULL: queries not normed */
+  const void* k_weight;   /* bf16 [head_dim], device, 16-byte aligned, or NULL: keys not normed */
+  int32_t v_norm;         /* 1: values get the unit RMS norm; 0: they do not */
+  float eps;              /* added to the mean square; finite and > 0 (Gemma uses 1e-6) */
+} g4attn_norms;
+
 /* A paged bf16 KV cache of one layer (RFC section 5, hybrid_kv_cache_contract). */
 typedef struct {
   void* k;                /* sliding: roped K'; global: the shared S */
@@ -157,6 +179,25 @@ g4_status g4attn_prefill_attend(const g4attn_layer* layer, int32_t T, const int3
                                 const int32_t* q_len, const int32_t* ctx_start, int32_t B,
                                 const g4attn_cache* cache, const int32_t* page_table, int32_t max_pages,
                                 void* out, void* stream);
+
+/* g4attn_prefill, g4attn_kv_append and g4attn_decode with the per-head norms of g4attn_norms
+ * applied to the raw q, k and v they are given (norms NULL: exactly the plain calls). A
+ * sequence's history must have been appended with the same norms. Errors as the plain calls,
+ * plus G4_ERR_INVALID for a bad eps, v_norm or weight alignment, and G4_ERR_UNSUPPORTED for a
+ * K==V layer whose key norm and value norm do not come together. */
+g4_status g4attn_prefill_normed(const g4attn_layer* layer, const g4attn_norms* norms, const void* q,
+                                const void* k, const void* v, int32_t T, const int32_t* q_start,
+                                const int32_t* q_len, const int32_t* ctx_start, int32_t B,
+                                const g4attn_cache* cache, const int32_t* page_table, int32_t max_pages,
+                                void* out, void* stream);
+g4_status g4attn_kv_append_normed(const g4attn_layer* layer, const g4attn_norms* norms, const void* k,
+                                  const void* v, int32_t T, const int32_t* q_start, const int32_t* q_len,
+                                  const int32_t* ctx_start, int32_t B, const g4attn_cache* cache,
+                                  const int32_t* page_table, int32_t max_pages, void* stream);
+g4_status g4attn_decode_normed(const g4attn_layer* layer, const g4attn_norms* norms, const void* q,
+                               const void* k_new, const void* v_new, const int32_t* seq_len, int32_t B,
+                               const g4attn_cache* cache, const int32_t* page_table, int32_t max_pages,
+                               void* out, void* workspace, size_t workspace_bytes, void* stream);
 
 /* Writes the K'/V (sliding) or S (global) rows of a prefill batch into the paged cache
  * without computing attention: the first step of g4attn_prefill on its own (RFC section 5,

@@ -23,6 +23,7 @@ PAGE_SIZE = 16
 DECODE_STATIC_SCRATCH_BYTES = 32 << 20   # the static scratch of g4attn_decode_static, per device
 
 EXPORTS = ("g4attn_rope_apply", "g4attn_prefill", "g4attn_prefill_stage", "g4attn_prefill_attend",
+           "g4attn_prefill_normed", "g4attn_kv_append_normed", "g4attn_decode_normed",
            "g4attn_kv_append", "g4attn_decode_workspace_bytes",
            "g4attn_decode", "g4attn_decode_static", "g4attn_provenance", "g4attn_status_sync", "g4attn_status_string")
 
@@ -31,6 +32,11 @@ class g4attn_layer(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int32), ("n_q_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("window", ctypes.c_int32), ("rope_theta", ctypes.c_float),
                 ("rope_partial", ctypes.c_float), ("softmax_scale", ctypes.c_float), ("kv_shared", ctypes.c_int32)]
+
+
+class g4attn_norms(ctypes.Structure):
+    _fields_ = [("q_weight", ctypes.c_void_p), ("k_weight", ctypes.c_void_p), ("v_norm", ctypes.c_int32),
+                ("eps", ctypes.c_float)]
 
 
 class g4attn_cache(ctypes.Structure):
@@ -58,11 +64,15 @@ def load(path: Optional[str] = None):
     lib = ctypes.CDLL(p)
     P, I32, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
     L, C = ctypes.POINTER(g4attn_layer), ctypes.POINTER(g4attn_cache)
+    N = ctypes.POINTER(g4attn_norms)
     sigs = {
         "g4attn_rope_apply": (I32, [L, P, P, I32, I32, P, P]),
         "g4attn_prefill": (I32, [L, P, P, P, I32, P, P, P, I32, C, P, I32, P, P]),
         "g4attn_prefill_stage": (I32, [L, P, P, P, I32, P, P, P, I32, C, P, I32, P, P]),
         "g4attn_prefill_attend": (I32, [L, I32, P, P, P, I32, C, P, I32, P, P]),
+        "g4attn_prefill_normed": (I32, [L, N, P, P, P, I32, P, P, P, I32, C, P, I32, P, P]),
+        "g4attn_kv_append_normed": (I32, [L, N, P, P, I32, P, P, P, I32, C, P, I32, P]),
+        "g4attn_decode_normed": (I32, [L, N, P, P, P, P, I32, C, P, I32, P, P, SZ, P]),
         "g4attn_kv_append": (I32, [L, P, P, I32, P, P, P, I32, C, P, I32, P]),
         "g4attn_decode_workspace_bytes": (SZ, [L, I32, I32]),
         "g4attn_decode": (I32, [L, P, P, P, P, I32, C, P, I32, P, P, SZ, P]),
@@ -195,3 +205,38 @@ def g4attn_provenance(layer) -> str:
 
 def g4attn_status_sync(stream=None) -> int:
     return int(load().g4attn_status_sync(_stream(stream)))
+
+
+def make_norms(q_weight=None, k_weight=None, v_norm: bool = False, eps: float = 1e-6) -> g4attn_norms:
+    """Per-head norm arguments: q_weight / k_weight are bf16 [head_dim] device tensors or None."""
+    return g4attn_norms(_ptr(q_weight), _ptr(k_weight), 1 if v_norm else 0, float(eps))
+
+
+def g4attn_prefill_normed(layer, norms: g4attn_norms, q, k, v, q_start, q_len, ctx_start, cache: g4attn_cache,
+                          page_table, out, stream=None):
+    T, B = int(q.shape[0]), int(q_start.shape[0])
+    _check(load().g4attn_prefill_normed(ctypes.byref(layer), ctypes.byref(norms), _ptr(q), _ptr(k), _ptr(v), T,
+                                        _ptr(q_start), _ptr(q_len), _ptr(ctx_start), B, ctypes.byref(cache),
+                                        _ptr(page_table), int(page_table.shape[1]), _ptr(out), _stream(stream)),
+           "g4attn_prefill_normed")
+    return out
+
+
+def g4attn_kv_append_normed(layer, norms: g4attn_norms, k, v, q_start, q_len, ctx_start, cache: g4attn_cache,
+                            page_table, stream=None):
+    T, B = int(k.shape[0]), int(q_start.shape[0])
+    _check(load().g4attn_kv_append_normed(ctypes.byref(layer), ctypes.byref(norms), _ptr(k), _ptr(v), T,
+                                          _ptr(q_start), _ptr(q_len), _ptr(ctx_start), B, ctypes.byref(cache),
+                                          _ptr(page_table), int(page_table.shape[1]), _stream(stream)),
+           "g4attn_kv_append_normed")
+
+
+def g4attn_decode_normed(layer, norms: g4attn_norms, q, k_new, v_new, seq_len, cache: g4attn_cache, page_table,
+                         out, workspace, stream=None):
+    B = int(q.shape[0])
+    _check(load().g4attn_decode_normed(ctypes.byref(layer), ctypes.byref(norms), _ptr(q), _ptr(k_new), _ptr(v_new),
+                                       _ptr(seq_len), B, ctypes.byref(cache), _ptr(page_table),
+                                       int(page_table.shape[1]), _ptr(out), _ptr(workspace),
+                                       int(workspace.numel() * workspace.element_size()), _stream(stream)),
+           "g4attn_decode_normed")
+    return out

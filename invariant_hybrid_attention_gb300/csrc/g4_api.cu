@@ -74,6 +74,23 @@ g4_status check_rows(const void* q_or_k, int32_t T, const int32_t* q_start, cons
   return G4_OK;
 }
 
+// Norm arguments, checked on the host before any launch. On a K==V layer the stored S serves as V,
+// and the key norm's weight reaches K only through the queries' un-rotated dims, so the key norm
+// and the unit value norm come together there (or neither does).
+g4_status check_norms(const g4attn_norms* n, bool global, NormArgs* out) {
+  *out = NormArgs{};
+  if (!n) return G4_OK;
+  if (!(n->eps > 0.f) || !isfinite(n->eps)) return G4_ERR_INVALID;
+  if (n->v_norm != 0 && n->v_norm != 1) return G4_ERR_INVALID;
+  if ((n->q_weight && !aligned16(n->q_weight)) || (n->k_weight && !aligned16(n->k_weight))) return G4_ERR_INVALID;
+  if (global && (n->v_norm != 0) != (n->k_weight != nullptr)) return G4_ERR_UNSUPPORTED;
+  out->wq = (const __nv_bfloat16*)n->q_weight;
+  out->wk = (const __nv_bfloat16*)n->k_weight;
+  out->v_norm = n->v_norm;
+  out->eps = n->eps;
+  return G4_OK;
+}
+
 // Scratch of g4attn_decode_static: the partial softmax states of one decode step, in a
 // file-scope device array so that the call needs no allocation. One copy per device; its
 // address is looked up once per device and cached.
@@ -128,12 +145,15 @@ g4_status g4attn_rope_apply(const g4attn_layer* layer, const void* x, const int3
   return from_cuda(launch_rope_apply(global, x, pos, T, H, out, st, (cudaStream_t)stream));
 }
 
-g4_status g4attn_kv_append(const g4attn_layer* layer, const void* k, const void* v, int32_t T,
-                           const int32_t* q_start, const int32_t* q_len, const int32_t* ctx_start, int32_t B,
-                           const g4attn_cache* cache, const int32_t* page_table, int32_t max_pages, void* stream) {
+g4_status g4attn_kv_append_normed(const g4attn_layer* layer, const g4attn_norms* norms, const void* k,
+                                  const void* v, int32_t T, const int32_t* q_start, const int32_t* q_len,
+                                  const int32_t* ctx_start, int32_t B, const g4attn_cache* cache,
+                                  const int32_t* page_table, int32_t max_pages, void* stream) {
   bool global = false;
   g4_status s = check_layer(layer, &global);
   if (s != G4_OK) return s;
+  NormArgs nm;
+  if ((s = check_norms(norms, global, &nm)) != G4_OK) return s;
   if ((s = check_rows(k, T, q_start, q_len, ctx_start, B)) != G4_OK) return s;
   if ((s = check_cache(cache, global, page_table, max_pages)) != G4_OK) return s;
   if (global ? v != nullptr : (T > 0 && (!v || !aligned16(v)))) return G4_ERR_INVALID;
@@ -142,16 +162,25 @@ g4_status g4attn_kv_append(const g4attn_layer* layer, const void* k, const void*
   if (device_state(&st) != cudaSuccess) return G4_ERR_CUDA;
   SeqRows rows{q_start, q_len, ctx_start, B, T};
   return from_cuda(launch_append_prefill(global, k, v, rows, paged(cache, page_table, max_pages), st,
-                                         (cudaStream_t)stream));
+                                         (cudaStream_t)stream, nullptr, nullptr, nm));
 }
 
-g4_status g4attn_prefill_stage(const g4attn_layer* layer, const void* q, const void* k, const void* v, int32_t T,
-                               const int32_t* q_start, const int32_t* q_len, const int32_t* ctx_start, int32_t B,
-                               const g4attn_cache* cache, const int32_t* page_table, int32_t max_pages, void* out,
-                               void* stream) {
+g4_status g4attn_kv_append(const g4attn_layer* layer, const void* k, const void* v, int32_t T,
+                           const int32_t* q_start, const int32_t* q_len, const int32_t* ctx_start, int32_t B,
+                           const g4attn_cache* cache, const int32_t* page_table, int32_t max_pages, void* stream) {
+  return g4attn_kv_append_normed(layer, nullptr, k, v, T, q_start, q_len, ctx_start, B, cache, page_table, max_pages,
+                                 stream);
+}
+
+static g4_status prefill_stage(const g4attn_layer* layer, const g4attn_norms* norms, const void* q, const void* k,
+                               const void* v, int32_t T, const int32_t* q_start, const int32_t* q_len,
+                               const int32_t* ctx_start, int32_t B, const g4attn_cache* cache,
+                               const int32_t* page_table, int32_t max_pages, void* out, void* stream) {
   bool global = false;
   g4_status s = check_layer(layer, &global);
   if (s != G4_OK) return s;
+  NormArgs nm;
+  if ((s = check_norms(norms, global, &nm)) != G4_OK) return s;
   if ((s = check_rows(q, T, q_start, q_len, ctx_start, B)) != G4_OK) return s;
   if ((s = check_cache(cache, global, page_table, max_pages)) != G4_OK) return s;
   if (T > 0 && (!k || !aligned16(k) || !out || !aligned16(out))) return G4_ERR_INVALID;
@@ -163,7 +192,15 @@ g4_status g4attn_prefill_stage(const g4attn_layer* layer, const void* q, const v
   // roped query until g4attn_prefill_attend overwrites it with the attention output.
   const SeqRows rows{q_start, q_len, ctx_start, B, T};
   return from_cuda(launch_append_prefill(global, k, v, rows, paged(cache, page_table, max_pages), st,
-                                         (cudaStream_t)stream, q, out));
+                                         (cudaStream_t)stream, q, out, nm));
+}
+
+g4_status g4attn_prefill_stage(const g4attn_layer* layer, const void* q, const void* k, const void* v, int32_t T,
+                               const int32_t* q_start, const int32_t* q_len, const int32_t* ctx_start, int32_t B,
+                               const g4attn_cache* cache, const int32_t* page_table, int32_t max_pages, void* out,
+                               void* stream) {
+  return prefill_stage(layer, nullptr, q, k, v, T, q_start, q_len, ctx_start, B, cache, page_table, max_pages, out,
+                       stream);
 }
 
 g4_status g4attn_prefill_attend(const g4attn_layer* layer, int32_t T, const int32_t* q_start, const int32_t* q_len,
@@ -182,14 +219,22 @@ g4_status g4attn_prefill_attend(const g4attn_layer* layer, int32_t T, const int3
                                   paged(cache, page_table, max_pages), out, st, (cudaStream_t)stream));
 }
 
+g4_status g4attn_prefill_normed(const g4attn_layer* layer, const g4attn_norms* norms, const void* q, const void* k,
+                                const void* v, int32_t T, const int32_t* q_start, const int32_t* q_len,
+                                const int32_t* ctx_start, int32_t B, const g4attn_cache* cache,
+                                const int32_t* page_table, int32_t max_pages, void* out, void* stream) {
+  g4_status s = prefill_stage(layer, norms, q, k, v, T, q_start, q_len, ctx_start, B, cache, page_table, max_pages,
+                              out, stream);
+  if (s != G4_OK) return s;
+  return g4attn_prefill_attend(layer, T, q_start, q_len, ctx_start, B, cache, page_table, max_pages, out, stream);
+}
+
 g4_status g4attn_prefill(const g4attn_layer* layer, const void* q, const void* k, const void* v, int32_t T,
                          const int32_t* q_start, const int32_t* q_len, const int32_t* ctx_start, int32_t B,
                          const g4attn_cache* cache, const int32_t* page_table, int32_t max_pages, void* out,
                          void* stream) {
-  g4_status s = g4attn_prefill_stage(layer, q, k, v, T, q_start, q_len, ctx_start, B, cache, page_table,
-                                     max_pages, out, stream);
-  if (s != G4_OK) return s;
-  return g4attn_prefill_attend(layer, T, q_start, q_len, ctx_start, B, cache, page_table, max_pages, out, stream);
+  return g4attn_prefill_normed(layer, nullptr, q, k, v, T, q_start, q_len, ctx_start, B, cache, page_table, max_pages,
+                               out, stream);
 }
 
 size_t g4attn_decode_workspace_bytes(const g4attn_layer* layer, int32_t B, int32_t max_pages) {
@@ -198,12 +243,15 @@ size_t g4attn_decode_workspace_bytes(const g4attn_layer* layer, int32_t B, int32
   return decode_workspace_bytes(global, B, max_pages, global ? 0 : layer->window);
 }
 
-g4_status g4attn_decode(const g4attn_layer* layer, const void* q, const void* k_new, const void* v_new,
-                        const int32_t* seq_len, int32_t B, const g4attn_cache* cache, const int32_t* page_table,
-                        int32_t max_pages, void* out, void* workspace, size_t workspace_bytes, void* stream) {
+g4_status g4attn_decode_normed(const g4attn_layer* layer, const g4attn_norms* norms, const void* q,
+                               const void* k_new, const void* v_new, const int32_t* seq_len, int32_t B,
+                               const g4attn_cache* cache, const int32_t* page_table, int32_t max_pages, void* out,
+                               void* workspace, size_t workspace_bytes, void* stream) {
   bool global = false;
   g4_status s = check_layer(layer, &global);
   if (s != G4_OK) return s;
+  NormArgs nm;
+  if ((s = check_norms(norms, global, &nm)) != G4_OK) return s;
   if (B <= 0 || !q || !k_new || !seq_len || !out || !workspace) return G4_ERR_INVALID;
   if (!aligned16(q) || !aligned16(k_new) || !aligned16(out) || !aligned16(workspace)) return G4_ERR_INVALID;
   if (global ? v_new != nullptr : (!v_new || !aligned16(v_new))) return G4_ERR_INVALID;
@@ -214,10 +262,24 @@ g4_status g4attn_decode(const g4attn_layer* layer, const void* q, const void* k_
   if (device_state(&st) != cudaSuccess) return G4_ERR_CUDA;
   const cudaStream_t cs = (cudaStream_t)stream;
   const PagedCache pc = paged(cache, page_table, max_pages);
-  cudaError_t e = launch_append_decode(global, k_new, v_new, seq_len, B, pc, st, cs);
+  // Normed queries go through `out`: the decode kernel reads them there before the merge writes
+  // the output rows.
+  const void* q_eff = q;
+  if (nm.wq != nullptr || (global && nm.wk != nullptr)) {
+    if (launch_norm_queries(global, q, out, B, nm, cs) != cudaSuccess) return G4_ERR_CUDA;
+    q_eff = out;
+  }
+  cudaError_t e = launch_append_decode(global, k_new, v_new, seq_len, B, pc, st, cs, nm);
   if (e != cudaSuccess) return G4_ERR_CUDA;
-  return from_cuda(launch_decode(global, q, seq_len, B, global ? 0 : layer->window, scale_log2(layer), pc, out,
+  return from_cuda(launch_decode(global, q_eff, seq_len, B, global ? 0 : layer->window, scale_log2(layer), pc, out,
                                  workspace, st, cs));
+}
+
+g4_status g4attn_decode(const g4attn_layer* layer, const void* q, const void* k_new, const void* v_new,
+                        const int32_t* seq_len, int32_t B, const g4attn_cache* cache, const int32_t* page_table,
+                        int32_t max_pages, void* out, void* workspace, size_t workspace_bytes, void* stream) {
+  return g4attn_decode_normed(layer, nullptr, q, k_new, v_new, seq_len, B, cache, page_table, max_pages, out,
+                              workspace, workspace_bytes, stream);
 }
 
 g4_status g4attn_decode_static(const g4attn_layer* layer, const void* q, const void* k_new, const void* v_new,

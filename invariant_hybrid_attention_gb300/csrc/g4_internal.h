@@ -38,6 +38,16 @@ struct PagedCache {
   int32_t max_pages;
 };
 
+// Optional per-head RMS norms of a prefill or decode (device pointers to bf16 [D] weights; a null
+// weight leaves that tensor un-normed). See the norm notes in g4_rope.cu.
+struct NormArgs {
+  const __nv_bfloat16* wq = nullptr;   // query weight
+  const __nv_bfloat16* wk = nullptr;   // key weight
+  int v_norm = 0;                      // unit RMS norm of the values (the stored S on K==V layers)
+  float eps = 1e-6f;
+  __host__ __device__ bool any() const { return wq != nullptr || wk != nullptr || v_norm != 0; }
+};
+
 cudaError_t launch_rope_apply(bool global, const void* x, const int32_t* pos, int T, int H, void* out,
                               const DeviceState& st, cudaStream_t s);
 
@@ -45,10 +55,14 @@ cudaError_t launch_rope_apply(bool global, const void* x, const int32_t* pos, in
 // (bf16) into q_out, the staging the prefill attention kernel reads its queries from.
 cudaError_t launch_append_prefill(bool global, const void* k, const void* v, const SeqRows& rows,
                                   const PagedCache& cache, const DeviceState& st, cudaStream_t s,
-                                  const void* q = nullptr, void* q_out = nullptr);
+                                  const void* q = nullptr, void* q_out = nullptr, const NormArgs& nm = NormArgs{});
 
 cudaError_t launch_append_decode(bool global, const void* k_new, const void* v_new, const int32_t* seq_len,
-                                 int B, const PagedCache& cache, const DeviceState& st, cudaStream_t s);
+                                 int B, const PagedCache& cache, const DeviceState& st, cudaStream_t s,
+                                 const NormArgs& nm = NormArgs{});
+
+// The decode queries' norms, written to out (bf16), for the decode kernel to read as its q.
+cudaError_t launch_norm_queries(bool global, const void* q, void* out, int B, const NormArgs& nm, cudaStream_t s);
 
 // Decode partials + ordered merge. ws must hold decode_workspace_bytes(global, B, max_pages).
 size_t decode_workspace_bytes(bool global, int B, int max_pages, int window);

@@ -232,6 +232,95 @@ __device__ __forceinline__ void copy_vec_warp(const __nv_bfloat16* __restrict__ 
   }
 }
 
+// ---- optional per-head RMS norms, before the rotation --------------------------------------------
+// Reading of the RFC work item qk_rmsnorm_d256_d512 and of TensorFold's tf_qk_rows_once (which
+// "can norm v by a unit RMS norm"): a head vector x of D dims becomes (x * inv) * w with
+// inv = 1/sqrt(mean(x^2) + eps), in fp32, before the rotation and the one declared bf16 cast; w
+// is a per-dim weight for queries and keys, and 1 for the unit norm of values. On a K==V layer the
+// stored S becomes n(S), which is V; the k_rot side pages hold RoPE(w_k n(S)); and the staged
+// queries carry w_k on their un-rotated dims, where the attention kernels read K from the stored
+// S: q . (w_k n(S)) = (q w_k) . n(S). The sum of squares is a fixed-order sum over the lane's 16
+// elements followed by a butterfly over the vector's lanes; additions commute, so every lane gets
+// the same bits, and a vector's result depends on that vector alone.
+template <int D>
+__device__ __forceinline__ void lane_weights(const __nv_bfloat16* w, float (&out)[16]) {
+  const int t0 = ((threadIdx.x & 31) % (D / 16)) * 8;
+  if (w == nullptr) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) out[i] = 1.f;
+    return;
+  }
+  const uint4 lo = __ldg(reinterpret_cast<const uint4*>(w + t0));
+  const uint4 hi = __ldg(reinterpret_cast<const uint4*>(w + D / 2 + t0));
+  const uint32_t lw[4] = {lo.x, lo.y, lo.z, lo.w}, hw[4] = {hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    out[2 * i] = bf16_lo(lw[i]);
+    out[2 * i + 1] = bf16_hi(lw[i]);
+    out[8 + 2 * i] = bf16_lo(hw[i]);
+    out[8 + 2 * i + 1] = bf16_hi(hw[i]);
+  }
+}
+
+// rope_vec8_cs with the norm: `norm` turns it on (weight w, all ones for a unit norm), pairs
+// t < R rotate, and lanes whose pairs start at or after fold_from multiply by `fold` (w_k on the
+// un-rotated dims of a K==V layer's queries; nullptr: no fold).
+template <int D, int R, class Dst>
+__device__ __forceinline__ void vec8_normed(const __nv_bfloat16* __restrict__ src, const Dst& dst,
+                                            const float2 (&cs)[8], bool norm, float eps, const float (&w)[16],
+                                            const float* fold, int fold_from) {
+  constexpr int half = D / 2, LPV = D / 16;
+  const int t0 = ((threadIdx.x & 31) % LPV) * 8;
+  const uint4 lo = *reinterpret_cast<const uint4*>(src + t0);
+  const uint4 hi = *reinterpret_cast<const uint4*>(src + half + t0);
+  const uint32_t lw[4] = {lo.x, lo.y, lo.z, lo.w}, hw[4] = {hi.x, hi.y, hi.z, hi.w};
+  float a[8], b[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    a[2 * i] = bf16_lo(lw[i]);
+    a[2 * i + 1] = bf16_hi(lw[i]);
+    b[2 * i] = bf16_lo(hw[i]);
+    b[2 * i + 1] = bf16_hi(hw[i]);
+  }
+  if (norm) {
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ss = fmaf(a[i], a[i], ss);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ss = fmaf(b[i], b[i], ss);
+#pragma unroll
+    for (int o = 1; o < LPV; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float inv = __frsqrt_rn(fmaf(ss, 1.0f / (float)D, eps));   // ss / D is exact: D is a power of 2
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      a[i] = (a[i] * inv) * w[i];
+      b[i] = (b[i] * inv) * w[8 + i];
+    }
+  }
+  if (t0 < R) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) rope_pair(a[i], b[i], cs[i]);
+  } else if (fold != nullptr && t0 >= fold_from) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      a[i] *= fold[i];
+      b[i] *= fold[8 + i];
+    }
+  }
+  if (RotatedOnly<Dst>::value && t0 >= R) return;
+  uint4 olo, ohi;
+  olo.x = pack_bf16(a[0], a[1]);
+  olo.y = pack_bf16(a[2], a[3]);
+  olo.z = pack_bf16(a[4], a[5]);
+  olo.w = pack_bf16(a[6], a[7]);
+  ohi.x = pack_bf16(b[0], b[1]);
+  ohi.y = pack_bf16(b[2], b[3]);
+  ohi.z = pack_bf16(b[4], b[5]);
+  ohi.w = pack_bf16(b[6], b[7]);
+  *reinterpret_cast<uint4*>(dst.at(t0)) = olo;
+  *reinterpret_cast<uint4*>(dst.at(half + t0)) = ohi;
+}
+
 template <int D, int R>
 __global__ void __launch_bounds__(256) rope_apply_kernel(const __nv_bfloat16* __restrict__ x,
                                                          const int32_t* __restrict__ pos, int T, int H,
@@ -265,9 +354,10 @@ cudaError_t launch_rope_apply(bool global, const void* x, const int32_t* pos, in
 // Writes one token's Hkv vectors into its page slot: sliding K' = bf16(RoPE(k)) and V as given;
 // global S as given (K==V: the one stored projection, rotated only where it is read as K).
 // cs: the lane's (cos, sin) at the token's position (rope_cs_lane); pos is in range.
-template <int D, int R, int HKV, bool SHARED>
+template <int D, int R, int HKV, bool SHARED, bool NORM>
 __device__ __forceinline__ void append_token_cs(const __nv_bfloat16* k_row, const __nv_bfloat16* v_row, int b, int pos,
-                                                const PagedCache& c, const float2 (&cs)[8], uint32_t* err) {
+                                                const PagedCache& c, const float2 (&cs)[8], uint32_t* err,
+                                                const NormArgs& nm, const float (&wk)[16]) {
   constexpr int VPW = 32 / (D / 16);   // vectors per warp instruction of rope_vec8_cs
   const int lane = threadIdx.x & 31;
   const int phys = c.page_table[(size_t)b * c.max_pages + (pos >> 4)];
@@ -276,6 +366,39 @@ __device__ __forceinline__ void append_token_cs(const __nv_bfloat16* k_row, cons
     return;
   }
   const int j = pos & 15;
+  if (NORM) {   // the normed path: K' (or k_rot) from w_k n(k), V (or S) as n(v) when asked
+    float ones[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) ones[i] = 1.f;
+#pragma unroll 1
+    for (int g0 = 0; g0 < HKV; g0 += VPW) {
+      const int g = g0 + lane / (D / 16);
+      const size_t blk = ((size_t)phys * HKV + g) * kPage * D;
+      const __nv_bfloat16* kg = k_row + (size_t)g * D;
+      if (SHARED) {
+        vec8_normed<D, R>(kg, RotDst{(__nv_bfloat16*)c.krot + ((size_t)phys * HKV + g) * kRotPageElems, j}, cs,
+                          nm.wk != nullptr, nm.eps, wk, nullptr, 0);
+        if (nm.v_norm)
+          vec8_normed<D, 0>(kg, PageDst<D>{(__nv_bfloat16*)c.k + blk, j}, cs, true, nm.eps, ones, nullptr, 0);
+      } else {
+        vec8_normed<D, R>(kg, PageDst<D>{(__nv_bfloat16*)c.k + blk, j}, cs, nm.wk != nullptr, nm.eps, wk, nullptr, 0);
+        if (nm.v_norm)
+          vec8_normed<D, 0>(v_row + (size_t)g * D, VDst{(__nv_bfloat16*)c.v + blk, j}, cs, true, nm.eps, ones,
+                            nullptr, 0);
+      }
+      if (!nm.v_norm) {
+#pragma unroll
+        for (int gv = g0; gv < g0 + VPW; ++gv) {
+          const size_t blkv = ((size_t)phys * HKV + gv) * kPage * D;
+          if (SHARED)
+            copy_vec_warp<D>(k_row + (size_t)gv * D, PageDst<D>{(__nv_bfloat16*)c.k + blkv, j});
+          else
+            copy_vec_warp<D>(v_row + (size_t)gv * D, VDst{(__nv_bfloat16*)c.v + blkv, j});
+        }
+      }
+    }
+    return;
+  }
 #pragma unroll 2
   for (int g0 = 0; g0 < HKV; g0 += VPW) {
     const int g = g0 + lane / (D / 16);   // this lane's KV head for the rotation
@@ -298,9 +421,10 @@ __device__ __forceinline__ void append_token_cs(const __nv_bfloat16* k_row, cons
   }
 }
 
-template <int D, int R, int HKV, bool SHARED>
+template <int D, int R, int HKV, bool SHARED, bool NORM>
 __device__ __forceinline__ void append_token(const __nv_bfloat16* k_row, const __nv_bfloat16* v_row, int b, int pos,
-                                             const PagedCache& c, const RopeTables& tb, uint32_t* err) {
+                                             const PagedCache& c, const RopeTables& tb, uint32_t* err,
+                                             const NormArgs& nm) {
   const int lane = threadIdx.x & 31;
   if (pos < 0 || pos >= kMaxPos || (pos >> 4) >= c.max_pages) {
     if (lane == 0) set_error(err, kErrPos);
@@ -308,18 +432,20 @@ __device__ __forceinline__ void append_token(const __nv_bfloat16* k_row, const _
   }
   float2 cs[8];
   rope_cs_lane8<D, R>(tb, pos, cs);
-  append_token_cs<D, R, HKV, SHARED>(k_row, v_row, b, pos, c, cs, err);
+  float wk[16];
+  if (NORM) lane_weights<D>(nm.wk, wk);
+  append_token_cs<D, R, HKV, SHARED, NORM>(k_row, v_row, b, pos, c, cs, err, nm, wk);
 }
 
 // One warp per row of the prefill batch; the owning sequence is found by a scan over B.
 // With q_out set, the row's query heads are also roped (declared bf16 cast) into q_out: the
 // attention kernel that follows reads its queries already rotated.
-template <int D, int R, int HKV, int HQ, bool SHARED>
+template <int D, int R, int HKV, int HQ, bool SHARED, bool NORM>
 __global__ void __launch_bounds__(256) append_prefill_kernel(const __nv_bfloat16* __restrict__ k,
                                                              const __nv_bfloat16* __restrict__ v,
                                                              const __nv_bfloat16* __restrict__ q,
                                                              __nv_bfloat16* q_out, SeqRows rows, PagedCache cache,
-                                                             RopeTables tb, uint32_t* err) {
+                                                             RopeTables tb, uint32_t* err, NormArgs nm) {
   const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (r >= rows.T) return;
@@ -345,55 +471,123 @@ __global__ void __launch_bounds__(256) append_prefill_kernel(const __nv_bfloat16
   }
   float2 cs[8];   // the row's angles, shared by its query heads and its key heads
   rope_cs_lane8<D, R>(tb, pos, cs);
+  float wk[16];
+  if (NORM) lane_weights<D>(nm.wk, wk);
   if (q_out != nullptr) {
     constexpr int VPW = 32 / (D / 16);
+    if (NORM) {
+      float wq[16];
+      lane_weights<D>(nm.wq, wq);
+      const float* fold = (SHARED && nm.wk != nullptr) ? wk : nullptr;   // w_k on the un-rotated dims
+#pragma unroll 2
+      for (int h0 = 0; h0 < HQ; h0 += VPW) {
+        const size_t v = (size_t)r * HQ + h0 + lane / (D / 16);
+        vec8_normed<D, R>(q + v * D, RowDst{q_out + v * D}, cs, nm.wq != nullptr, nm.eps, wq, fold, R);
+      }
+    } else {
 #pragma unroll 4
-    for (int h0 = 0; h0 < HQ; h0 += VPW) {
-      const size_t v = (size_t)r * HQ + h0 + lane / (D / 16);
-      rope_vec8_cs<D, R>(q + v * D, RowDst{q_out + v * D}, cs);
+      for (int h0 = 0; h0 < HQ; h0 += VPW) {
+        const size_t v = (size_t)r * HQ + h0 + lane / (D / 16);
+        rope_vec8_cs<D, R>(q + v * D, RowDst{q_out + v * D}, cs);
+      }
     }
   }
-  append_token_cs<D, R, HKV, SHARED>(k + (size_t)r * HKV * D, SHARED ? nullptr : v + (size_t)r * HKV * D, owner, pos,
-                                     cache, cs, err);
+  append_token_cs<D, R, HKV, SHARED, NORM>(k + (size_t)r * HKV * D, SHARED ? nullptr : v + (size_t)r * HKV * D, owner,
+                                           pos, cache, cs, err, nm, wk);
 }
 
-template <int D, int R, int HKV, bool SHARED>
+template <int D, int R, int HKV, bool SHARED, bool NORM>
 __global__ void __launch_bounds__(256) append_decode_kernel(const __nv_bfloat16* __restrict__ k,
                                                             const __nv_bfloat16* __restrict__ v,
                                                             const int32_t* __restrict__ seq_len, int B,
-                                                            PagedCache cache, RopeTables tb, uint32_t* err) {
+                                                            PagedCache cache, RopeTables tb, uint32_t* err,
+                                                            NormArgs nm) {
   const int b = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (b >= B) return;
-  append_token<D, R, HKV, SHARED>(k + (size_t)b * HKV * D, SHARED ? nullptr : v + (size_t)b * HKV * D, b,
-                                  seq_len[b] - 1, cache, tb, err);
+  append_token<D, R, HKV, SHARED, NORM>(k + (size_t)b * HKV * D, SHARED ? nullptr : v + (size_t)b * HKV * D, b,
+                                        seq_len[b] - 1, cache, tb, err, nm);
+}
+
+// The decode queries' norm (and, on a K==V layer with a key norm, the fold of w_k into their
+// un-rotated dims) ahead of the decode kernel, which ropes them itself: out[v] = bf16 of the
+// normed query, one declared cast more than the prefill staging has. No rotation here.
+template <int D, int R, bool SHARED>
+__global__ void __launch_bounds__(256) norm_queries_kernel(const __nv_bfloat16* __restrict__ q, __nv_bfloat16* out,
+                                                           int n_vec, NormArgs nm) {
+  constexpr int VPW = 32 / (D / 16);
+  const int lane = threadIdx.x & 31;
+  const int v0 = (blockIdx.x * 8 + (threadIdx.x >> 5)) * VPW;   // n_vec is a multiple of VPW
+  if (v0 >= n_vec) return;
+  const size_t v = (size_t)v0 + lane / (D / 16);
+  float wq[16], wk[16];
+  lane_weights<D>(nm.wq, wq);
+  lane_weights<D>(nm.wk, wk);
+  float2 cs[8];   // unused: no rotation
+  vec8_normed<D, 0>(q + v * D, RowDst{out + v * D}, cs, nm.wq != nullptr, nm.eps, wq,
+                    (SHARED && nm.wk != nullptr) ? wk : nullptr, R);
 }
 
 cudaError_t launch_append_prefill(bool global, const void* k, const void* v, const SeqRows& rows,
                                   const PagedCache& cache, const DeviceState& st, cudaStream_t s, const void* q,
-                                  void* q_out) {
+                                  void* q_out, const NormArgs& nm) {
   if (rows.T <= 0 || rows.B <= 0) return cudaSuccess;
   const unsigned blocks = (unsigned)((rows.T + 7) / 8);
-  if (global)
-    append_prefill_kernel<kGlobalD, kGlobalR, kGlobalHkv, kGlobalHq, true><<<blocks, 256, 0, s>>>(
-        (const __nv_bfloat16*)k, nullptr, (const __nv_bfloat16*)q, (__nv_bfloat16*)q_out, rows, cache, st.global,
-        st.err);
-  else
-    append_prefill_kernel<kSlidingD, kSlidingR, kSlidingHkv, kSlidingHq, false><<<blocks, 256, 0, s>>>(
-        (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, (const __nv_bfloat16*)q, (__nv_bfloat16*)q_out, rows,
-        cache, st.sliding, st.err);
+  const __nv_bfloat16 *kb = (const __nv_bfloat16*)k, *vb = (const __nv_bfloat16*)v, *qb = (const __nv_bfloat16*)q;
+  __nv_bfloat16* qo = (__nv_bfloat16*)q_out;
+  if (global) {
+    if (nm.any())
+      append_prefill_kernel<kGlobalD, kGlobalR, kGlobalHkv, kGlobalHq, true, true>
+          <<<blocks, 256, 0, s>>>(kb, nullptr, qb, qo, rows, cache, st.global, st.err, nm);
+    else
+      append_prefill_kernel<kGlobalD, kGlobalR, kGlobalHkv, kGlobalHq, true, false>
+          <<<blocks, 256, 0, s>>>(kb, nullptr, qb, qo, rows, cache, st.global, st.err, nm);
+  } else {
+    if (nm.any())
+      append_prefill_kernel<kSlidingD, kSlidingR, kSlidingHkv, kSlidingHq, false, true>
+          <<<blocks, 256, 0, s>>>(kb, vb, qb, qo, rows, cache, st.sliding, st.err, nm);
+    else
+      append_prefill_kernel<kSlidingD, kSlidingR, kSlidingHkv, kSlidingHq, false, false>
+          <<<blocks, 256, 0, s>>>(kb, vb, qb, qo, rows, cache, st.sliding, st.err, nm);
+  }
   return cudaGetLastError();
 }
 
 cudaError_t launch_append_decode(bool global, const void* k_new, const void* v_new, const int32_t* seq_len,
-                                 int B, const PagedCache& cache, const DeviceState& st, cudaStream_t s) {
+                                 int B, const PagedCache& cache, const DeviceState& st, cudaStream_t s,
+                                 const NormArgs& nm) {
   if (B <= 0) return cudaSuccess;
   const unsigned blocks = (unsigned)((B + 7) / 8);
-  if (global)
-    append_decode_kernel<kGlobalD, kGlobalR, kGlobalHkv, true><<<blocks, 256, 0, s>>>(
-        (const __nv_bfloat16*)k_new, nullptr, seq_len, B, cache, st.global, st.err);
-  else
-    append_decode_kernel<kSlidingD, kSlidingR, kSlidingHkv, false><<<blocks, 256, 0, s>>>(
-        (const __nv_bfloat16*)k_new, (const __nv_bfloat16*)v_new, seq_len, B, cache, st.sliding, st.err);
+  const __nv_bfloat16 *kb = (const __nv_bfloat16*)k_new, *vb = (const __nv_bfloat16*)v_new;
+  if (global) {
+    if (nm.any())
+      append_decode_kernel<kGlobalD, kGlobalR, kGlobalHkv, true, true>
+          <<<blocks, 256, 0, s>>>(kb, nullptr, seq_len, B, cache, st.global, st.err, nm);
+    else
+      append_decode_kernel<kGlobalD, kGlobalR, kGlobalHkv, true, false>
+          <<<blocks, 256, 0, s>>>(kb, nullptr, seq_len, B, cache, st.global, st.err, nm);
+  } else {
+    if (nm.any())
+      append_decode_kernel<kSlidingD, kSlidingR, kSlidingHkv, false, true>
+          <<<blocks, 256, 0, s>>>(kb, vb, seq_len, B, cache, st.sliding, st.err, nm);
+    else
+      append_decode_kernel<kSlidingD, kSlidingR, kSlidingHkv, false, false>
+          <<<blocks, 256, 0, s>>>(kb, vb, seq_len, B, cache, st.sliding, st.err, nm);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_norm_queries(bool global, const void* q, void* out, int B, const NormArgs& nm, cudaStream_t s) {
+  if (B <= 0) return cudaSuccess;
+  const int n_vec = B * kGlobalHq;   // 32 query heads on both layer kinds
+  if (global) {
+    const unsigned blocks = (unsigned)((n_vec + 7) / 8);   // one vector per warp
+    norm_queries_kernel<kGlobalD, kGlobalR, true><<<blocks, 256, 0, s>>>((const __nv_bfloat16*)q,
+                                                                         (__nv_bfloat16*)out, n_vec, nm);
+  } else {
+    const unsigned blocks = (unsigned)((n_vec + 15) / 16);   // two vectors per warp
+    norm_queries_kernel<kSlidingD, kSlidingR, false><<<blocks, 256, 0, s>>>((const __nv_bfloat16*)q,
+                                                                            (__nv_bfloat16*)out, n_vec, nm);
+  }
   return cudaGetLastError();
 }
 

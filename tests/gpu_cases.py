@@ -39,6 +39,22 @@ def assert_close(got, want, what=""):
     return mx, mean
 
 
+class Norms:
+    """Per-head norm weights drawn once (bf16, uniform in [0.5, 1.5]), as the library's argument
+    struct (device tensors kept alive here) and as the oracle's Norms on the same bf16 values."""
+
+    def __init__(self, kind, seed, q=True, k=True, v=True, eps=1e-6):
+        d = GEOM[kind]["d"]
+        g = torch.Generator().manual_seed(seed)
+        draw = lambda: (torch.rand(d, generator=g, dtype=torch.float32) + 0.5).to(torch.bfloat16)
+        self.wq = draw() if q else None
+        self.wk = draw() if k else None
+        self.dev = [None if w is None else w.cuda() for w in (self.wq, self.wk)]
+        self.arg = g4.make_norms(self.dev[0], self.dev[1], v, eps)
+        self.oracle = oracle.Norms(q_weight=None if self.wq is None else self.wq.double().numpy(),
+                                   k_weight=None if self.wk is None else self.wk.double().numpy(), v_norm=v, eps=eps)
+
+
 class Batch:
     """A prefill batch: per-sequence histories (positions 0 .. ctx_start+q_len-1) and the new rows."""
 
@@ -62,7 +78,7 @@ class Batch:
     def device_cache(self) -> PagedKV:
         return PagedKV(self.plan.num_pages, self.n_kv, self.d, shared=(self.kind == "global"))
 
-    def append_history(self, layer, cache: PagedKV, table):
+    def append_history(self, layer, cache: PagedKV, table, norms=None):
         """Writes every sequence's rows before ctx_start into the cache with g4attn_kv_append."""
         if max(self.ctx_starts) == 0:
             return
@@ -71,20 +87,25 @@ class Batch:
         k = gi.rows_of([h[:L] for h, L in zip(self.hist_k, lens)], lay, fill_nan=False).cuda()
         v = None if self.hist_v is None else gi.rows_of([h[:L] for h, L in zip(self.hist_v, lens)], lay,
                                                         fill_nan=False).cuda()
-        g4.g4attn_kv_append(layer, k, v, device_int32(lay.q_start), device_int32(lay.q_len),
-                            device_int32([0] * len(lens)), cache.desc, table)
+        rows = (device_int32(lay.q_start), device_int32(lay.q_len), device_int32([0] * len(lens)))
+        if norms is None:
+            g4.g4attn_kv_append(layer, k, v, *rows, cache.desc, table)
+        else:
+            g4.g4attn_kv_append_normed(layer, norms.arg, k, v, *rows, cache.desc, table)
 
-    def run(self, layer, out_fill=float("nan"), split=False):
+    def run(self, layer, out_fill=float("nan"), split=False, norms=None):
         """One prefill of the batch: g4attn_prefill, or (split) its two steps called apart."""
         cache = self.device_cache()
         table = self.plan.table.cuda()
-        self.append_history(layer, cache, table)
+        self.append_history(layer, cache, table, norms)
         q = self.q.cuda()
         k = self.k_rows.cuda()
         v = None if self.v_rows is None else self.v_rows.cuda()
         out = torch.full_like(q, out_fill)
         rows = (device_int32(self.layout.q_start), device_int32(self.layout.q_len), device_int32(self.layout.ctx_start))
-        if split:
+        if norms is not None:
+            g4.g4attn_prefill_normed(layer, norms.arg, q, k, v, *rows, cache.desc, table, out)
+        elif split:
             g4.g4attn_prefill_stage(layer, q, k, v, *rows, cache.desc, table, out)
             g4.g4attn_prefill_attend(layer, *rows, cache.desc, table, out)
         else:
@@ -94,13 +115,14 @@ class Batch:
         assert st == g4.G4_OK, g4.status_string(st)
         return out, cache
 
-    def oracle_rows(self, olayer, b, rows=None):
+    def oracle_rows(self, olayer, b, rows=None, norms=None):
         """fp64 answer for sequence b's new rows (all of them, or the given row indices)."""
         L, c, s = self.q_lens[b], self.ctx_starts[b], self.layout.q_start[b]
         idx = np.arange(L) if rows is None else np.asarray(rows)
         q = self.q[s + idx].double().numpy()
         v = None if self.hist_v is None else self.hist_v[b].double().numpy()
-        return oracle.layer_rows(olayer, q, c + idx, self.hist_k[b].double().numpy(), v)
+        return oracle.layer_rows(olayer, q, c + idx, self.hist_k[b].double().numpy(), v, 0,
+                                 None if norms is None else norms.oracle)
 
 
 class DecodeBatch:
@@ -127,7 +149,7 @@ class DecodeBatch:
                                       mapped_from=first, spare_pages=5)
         self.first_page = first
 
-    def run(self, layer, cache: PagedKV = None):
+    def run(self, layer, cache: PagedKV = None, norms=None):
         B = len(self.ctx_lens)
         table = self.plan.table.cuda()
         if cache is None:
@@ -140,8 +162,11 @@ class DecodeBatch:
             if lay.T > 0 and sum(lens) > 0:
                 k = gi.rows_of(self.hist_k, lay, fill_nan=False).cuda()
                 v = None if self.kind == "global" else gi.rows_of(self.hist_v, lay, fill_nan=False).cuda()
-                g4.g4attn_kv_append(layer, k, v, device_int32(lay.q_start), device_int32(lay.q_len),
-                                    device_int32(lay.ctx_start), cache.desc, table)
+                rows = (device_int32(lay.q_start), device_int32(lay.q_len), device_int32(lay.ctx_start))
+                if norms is None:
+                    g4.g4attn_kv_append(layer, k, v, *rows, cache.desc, table)
+                else:
+                    g4.g4attn_kv_append_normed(layer, norms.arg, k, v, *rows, cache.desc, table)
         k_new = torch.stack([h[L - 1] for h, L in zip(self.hist_k, self.ctx_lens)]).cuda()
         v_new = None if self.kind == "global" else torch.stack(
             [h[L - 1] for h, L in zip(self.hist_v, self.ctx_lens)]).cuda()
@@ -149,12 +174,17 @@ class DecodeBatch:
         out = torch.full_like(q, float("nan"))
         ws = torch.empty(g4.g4attn_decode_workspace_bytes(layer, B, self.plan.max_pages), dtype=torch.uint8,
                          device="cuda")
-        g4.g4attn_decode(layer, q, k_new, v_new, device_int32(self.ctx_lens), cache.desc, table, out, ws)
+        if norms is None:
+            g4.g4attn_decode(layer, q, k_new, v_new, device_int32(self.ctx_lens), cache.desc, table, out, ws)
+        else:
+            g4.g4attn_decode_normed(layer, norms.arg, q, k_new, v_new, device_int32(self.ctx_lens), cache.desc, table,
+                                    out, ws)
         torch.cuda.synchronize()
         st = g4.g4attn_status_sync()
         assert st == g4.G4_OK, g4.status_string(st)
         return out, cache
 
-    def oracle_row(self, olayer, b):
+    def oracle_row(self, olayer, b, norms=None):
         v = None if self.kind == "global" else self.hist_v[b].double().numpy()
-        return oracle.decode_row(olayer, self.q[b].double().numpy(), self.hist_k[b].double().numpy(), v)
+        return oracle.decode_row(olayer, self.q[b].double().numpy(), self.hist_k[b].double().numpy(), v,
+                                 None if norms is None else norms.oracle)

@@ -97,6 +97,29 @@ def test_invalid_arguments_refused_on_host(lib):
                              ws_need - 1, None) == g4.G4_ERR_INVALID
 
 
+def test_norm_arguments_refused_on_host(lib):
+    s, gl = g4.sliding_layer(), g4.global_layer()
+    cs = g4.g4attn_cache(16, 32, None, 4, 16)
+    cg = g4.g4attn_cache(16, None, 48, 4, 16)
+
+    def pre(layer, cache, norms, v):
+        return lib.g4attn_prefill_normed(ctypes.byref(layer), ctypes.byref(norms) if norms else None, 16, 16, v, 8,
+                                         16, 16, 16, 1, ctypes.byref(cache), 16, 1, 16, None)
+    for eps in (0.0, -1e-6, float("inf"), float("nan")):   # eps must be finite and positive
+        assert pre(s, cs, g4.g4attn_norms(16, 16, 1, eps), 16) == g4.G4_ERR_INVALID
+    assert pre(s, cs, g4.g4attn_norms(18, None, 0, 1e-6), 16) == g4.G4_ERR_INVALID    # misaligned weight
+    assert pre(s, cs, g4.g4attn_norms(None, 18, 0, 1e-6), 16) == g4.G4_ERR_INVALID
+    assert pre(s, cs, g4.g4attn_norms(None, None, 2, 1e-6), 16) == g4.G4_ERR_INVALID  # v_norm is 0 or 1
+    # K==V: the key norm and the unit value norm come together
+    assert pre(gl, cg, g4.g4attn_norms(None, 16, 0, 1e-6), None) == g4.G4_ERR_UNSUPPORTED
+    assert pre(gl, cg, g4.g4attn_norms(16, None, 1, 1e-6), None) == g4.G4_ERR_UNSUPPORTED
+    assert lib.g4attn_kv_append_normed(ctypes.byref(gl), ctypes.byref(g4.g4attn_norms(None, 16, 0, 1e-6)), 16, None,
+                                       8, 16, 16, 16, 1, ctypes.byref(cg), 16, 1, None) == g4.G4_ERR_UNSUPPORTED
+    assert lib.g4attn_decode_normed(ctypes.byref(gl), ctypes.byref(g4.g4attn_norms(None, None, 1, 1e-6)), 16, 16,
+                                    None, 16, 4, ctypes.byref(cg), 16, 100, 16, 16, 1 << 30,
+                                    None) == g4.G4_ERR_UNSUPPORTED
+
+
 def test_workspace_sizes(lib):
     s, gl = g4.sliding_layer(), g4.global_layer()
     # sliding: a 1024-key window touches at most 5 chunks of 256 keys; partial = (m, l) + 256 floats

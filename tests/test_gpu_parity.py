@@ -12,7 +12,7 @@ import oracle
 from invariant_hybrid_attention_gb300 import inputs as gi
 from invariant_hybrid_attention_gb300.paged import device_int32, untile, untile_rot, untile_v256
 
-from gpu_cases import GEOM, Batch, DecodeBatch, assert_close, f64, layers
+from gpu_cases import GEOM, Batch, DecodeBatch, Norms, assert_close, f64, layers
 
 pytestmark = pytest.mark.gpu
 
@@ -255,3 +255,76 @@ def test_chunked_prefill_is_bit_identical_to_one_prefill(kind):
             out_c, _ = ch.run(layer)
             got = out_c[:b - a].cpu().view(torch.int16)
             assert torch.equal(got, ref[a:b]), (kind, cuts, a, b)
+
+
+
+# ---------------------------------------------------------------- per-head norms before RoPE
+
+NORM_CASES = [("sliding", dict()), ("sliding", dict(k=False, v=False)), ("sliding", dict(q=False)),
+              ("global", dict()), ("global", dict(k=False, v=False))]
+NORM_IDS = ["sliding-all", "sliding-q", "sliding-kv", "global-all", "global-q"]
+
+
+def scale_raw(bt, kind, norms, f=3.0):
+    """Normed projections at f times unit scale, so that their norms have work to do. Un-normed
+    ones stay at unit scale, as in the other parity tests: an un-normed q or k at scale 3 sharpens
+    the logits until the declared bf16 casts alone reach the absolute tolerance, and an un-normed
+    value sets the output's scale. On a K==V layer the keys are the values."""
+    if norms.oracle.q_weight is not None:
+        bt.q = bt.q * f
+    if norms.oracle.k_weight is not None:
+        bt.hist_k = [h * f for h in bt.hist_k]
+        if hasattr(bt, "layout"):
+            bt.k_rows = gi.rows_of(bt.hist_k, bt.layout)
+    if norms.oracle.v_norm and kind == "sliding":
+        bt.hist_v = [h * f for h in bt.hist_v]
+        if hasattr(bt, "layout"):
+            bt.v_rows = gi.rows_of(bt.hist_v, bt.layout)
+
+
+@pytest.mark.parametrize("kind,which", NORM_CASES, ids=NORM_IDS)
+def test_prefill_normed_matches_oracle(kind, which):
+    """Raw projections normed in the stage; chunks whose history is appended with the same norms."""
+    layer, olayer = layers(kind, 1024)
+    norms = Norms(kind, seed=41, **which)
+    bt = Batch(kind, [1, 5, 127, 129, 300], ctx_starts=[0, 40, 0, 1000, 129], seed=42)
+    scale_raw(bt, kind, norms)
+    out, _ = bt.run(layer, norms=norms)
+    got = f64(out)
+    for b, L in enumerate(bt.q_lens):
+        s = bt.layout.q_start[b]
+        rows = np.unique(np.r_[0, L - 1, np.random.default_rng(b).choice(L, min(L, 40), replace=False)])
+        assert_close(got[s + rows], bt.oracle_rows(olayer, b, rows, norms), f"{kind} normed sequence {b}")
+
+
+@pytest.mark.parametrize("kind,which", NORM_CASES, ids=NORM_IDS)
+def test_decode_normed_matches_oracle(kind, which):
+    layer, olayer = layers(kind, 1024)
+    norms = Norms(kind, seed=43, **which)
+    db = DecodeBatch(kind, [1, 17, 300, 1500], seed=44)
+    scale_raw(db, kind, norms)
+    out, _ = db.run(layer, norms=norms)
+    got = f64(out)
+    for b in range(len(db.ctx_lens)):
+        assert_close(got[b], db.oracle_row(olayer, b, norms), f"{kind} normed decode request {b}")
+
+
+@pytest.mark.parametrize("kind", ["sliding", "global"])
+def test_prefill_normed_batch_invariance(kind):
+    """With the norms on, a target sequence alone and inside batches gives the same bits."""
+    layer, _ = layers(kind, 1024)
+    norms = Norms(kind, seed=45)
+    L = 700
+    alone = Batch(kind, [L], seed=46, scale=2.0)
+    out_a, _ = alone.run(layer, norms=norms)
+    for lens, padded, at in [([200, L, 33], False, 1), ([5, 77, L], True, 2)]:
+        bt = Batch(kind, lens, padded=padded, seed=47 + len(lens), scale=2.0)
+        bt.hist_k[at] = alone.hist_k[0]
+        if alone.hist_v is not None:
+            bt.hist_v[at] = alone.hist_v[0]
+        s = bt.layout.q_start[at]
+        bt.q[s:s + L] = alone.q[:L]
+        bt.k_rows = gi.rows_of(bt.hist_k, bt.layout)
+        bt.v_rows = None if bt.hist_v is None else gi.rows_of(bt.hist_v, bt.layout)
+        out_b, _ = bt.run(layer, norms=norms)
+        assert torch.equal(out_a[:L].cpu(), out_b[s:s + L].cpu()), (kind, lens, padded, at)
