@@ -10,7 +10,7 @@ import torch
 import invariant_hybrid_attention_gb300 as g4
 import oracle
 from invariant_hybrid_attention_gb300 import inputs as gi
-from invariant_hybrid_attention_gb300.paged import device_int32, untile, untile_rot, untile_v256
+from invariant_hybrid_attention_gb300.paged import PagedKV, device_int32, untile, untile_rot, untile_v256
 
 from gpu_cases import GEOM, Batch, DecodeBatch, Norms, assert_close, f64, layers
 
@@ -328,3 +328,44 @@ def test_prefill_normed_batch_invariance(kind):
         bt.v_rows = None if bt.hist_v is None else gi.rows_of(bt.hist_v, bt.layout)
         out_b, _ = bt.run(layer, norms=norms)
         assert torch.equal(out_a[:L].cpu(), out_b[s:s + L].cpu()), (kind, lens, padded, at)
+
+
+# ---------------------------------------------------------------- degenerate and faulty inputs
+
+@pytest.mark.parametrize("kind", ["sliding", "global"])
+def test_zero_length_sequences_in_a_batch(kind):
+    """q_len 0 is allowed: such sequences produce and touch nothing, the others are exact."""
+    bt = Batch(kind, [100, 0, 200, 0], ctx_starts=[0, 5, 0, 0], seed=51, scale=0.5)
+    check_prefill(bt, kind, 0 if kind == "global" else 1024)
+
+
+def test_device_detected_errors_are_reported_and_cleared(lib):
+    """A page-table entry outside the pool and a decode position beyond the page table are seen on
+    the device: the work they touch is skipped, the status word says so, and the next call starts
+    clean. Nothing traps; the context stays usable."""
+    layer, _ = layers("sliding", 1024)
+    bt = Batch("sliding", [300], seed=52, scale=0.5)
+    cache = bt.device_cache()
+    table = bt.plan.table.clone()
+    table[0, 5] = bt.plan.num_pages + 7          # keys 80..95 point outside the pool
+    rows = (device_int32(bt.layout.q_start), device_int32(bt.layout.q_len), device_int32(bt.layout.ctx_start))
+    out = torch.zeros_like(bt.q).cuda()
+    g4.g4attn_prefill(layer, bt.q.cuda(), bt.k_rows.cuda(), bt.v_rows.cuda(), *rows, cache.desc, table.cuda(), out)
+    assert g4.g4attn_status_sync() == g4.G4_ERR_DEVICE
+    assert g4.g4attn_status_sync() == g4.G4_OK   # read and cleared
+    # the same prefill with a good table is clean and exact afterwards
+    check_prefill(Batch("sliding", [300], seed=52, scale=0.5), "sliding", 1024)
+    assert g4.g4attn_status_sync() == g4.G4_OK
+    # decode: a request whose position lies beyond its page table
+    db = DecodeBatch("sliding", [40, 64], seed=53)
+    dcache = PagedKV(db.plan.num_pages, 16, 256, shared=False)
+    dt = db.plan.table.cuda()
+    q = db.q.cuda()
+    kn = torch.stack([h[L - 1] for h, L in zip(db.hist_k, db.ctx_lens)]).cuda()
+    vn = torch.stack([h[L - 1] for h, L in zip(db.hist_v, db.ctx_lens)]).cuda()
+    ws = torch.empty(g4.g4attn_decode_workspace_bytes(layer, 2, db.plan.max_pages), dtype=torch.uint8, device="cuda")
+    dout = torch.empty_like(q)
+    too_far = [40, 16 * db.plan.max_pages + 1]
+    g4.g4attn_decode(layer, q, kn, vn, device_int32(too_far), dcache.desc, dt, dout, ws)
+    assert g4.g4attn_status_sync() == g4.G4_ERR_DEVICE
+    assert g4.g4attn_status_sync() == g4.G4_OK
