@@ -104,6 +104,7 @@ struct Bars {
   // output CTAs
   uint64_t v_full[kNV], v_empty[kNV], v_ready[kNV];
   uint64_t p_full[kNP], o_ready[kNP], pv_done[kNP];
+  uint64_t ep_staged;        // output CTAs: the four epilogue warps have staged their rows
   uint64_t teardown;
   uint32_t tmem_base;
   int abort_flag;
@@ -194,6 +195,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&bar.v_empty[s], 1);
       mbar_init(&bar.v_ready[s], 1);
     }
+    mbar_init(&bar.ep_staged, kSoftmaxThreads / 32);
     mbar_init(&bar.teardown, 1);
     bar.abort_flag = 0;
     if (is_out) {   // the first two tiles' P may arrive as soon as the cluster is up
@@ -550,9 +552,16 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) arrive_leader(&bar.o_ready[sb]);
       }
-      // Epilogue: O / l -> bf16, rows of this sequence only.
+      // Epilogue: O / l -> bf16, rows of this sequence only. A tile whose 128 rows all belong to
+      // the sequence is staged in the V ring, idle once the last P.V has completed, as the eight
+      // 128B-swizzled boxes (64 dims x 128 rows) of the query tensor map, and written by eight
+      // TMA stores; any other tile is written row by row, so that rows of other sequences and
+      // padding are never touched.
       const int jl = n_tiles - 1;
-      if (ok && __all_sync(0xffffffffu, mbar_wait(&bar.pv_done[jl % kNP], (jl / kNP) & 1, abort_flag, p.err))) {
+      const bool staged = p_lo == kBM * t && p_hi == kBM * t + kBM - 1;
+      uint8_t* const ep = base + ((1024u - (smem_u32(base) & 1023u)) & 1023u);   // box-aligned
+      bool ok_ep = ok && __all_sync(0xffffffffu, mbar_wait(&bar.pv_done[jl % kNP], (jl / kNP) & 1, abort_flag, p.err));
+      if (ok_ep) {
         tc_fence_after();
         const float inv = (l_last > 0.f) ? __frcp_rn(l_last) : 0.f;
         __nv_bfloat16* orow = p.out + ((size_t)(q_row0 + r) * kGlobalHq + h) * kGD;
@@ -565,12 +574,32 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < 16; ++c)
             w16[c] = pack_bf16(__uint_as_float(o[2 * c]) * inv, __uint_as_float(o[2 * c + 1]) * inv);
-          if (row_ok) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + o_dim(32 * cc));
+          const int d0 = o_dim(32 * cc);   // 32 consecutive dims: half a box
+          if (staged) {
+            uint8_t* row = ep + (d0 >> 6) * kQChunk + r * 128;
+            const int q0 = (d0 & 63) >> 3;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              *reinterpret_cast<uint4*>(row + (((q0 + i) ^ (r & 7)) * 16)) =
+                  make_uint4(w16[4 * i], w16[4 * i + 1], w16[4 * i + 2], w16[4 * i + 3]);
+          } else if (row_ok) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + d0);
 #pragma unroll
             for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w16[4 * i], w16[4 * i + 1], w16[4 * i + 2], w16[4 * i + 3]);
           }
         }
+      }
+      if (staged) {   // one thread stores the eight boxes once every epilogue warp has staged its rows
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0 && ok_ep) mbar_arrive(&bar.ep_staged);
+        if (threadIdx.x == 64 && ok_ep && mbar_wait(&bar.ep_staged, 0, abort_flag, p.err)) {
+#pragma unroll
+          for (int c = 0; c < kGD / 64; ++c) tma_store_3d(&tmap_q, ep + c * kQChunk, 64 * c, h, q_row0);
+          bulk_commit_group();
+          bulk_wait_group_read0();   // the staging has been read; the writes complete on their own
+        }
+        __syncwarp();
       }
     } else if (warp == 6) {
       // ------------------------------------------------------------ P slot hand-back
