@@ -29,6 +29,13 @@ Readings of points the pages leave open (each is listed in the design notes):
 * K==V: the cache holds one projection S per global layer. V is S as stored; K is
   p-RoPE(S). At position 0 the rotation is the identity, so K and V agree there.
 * Window W: key j is visible to query i iff j <= i and i - j <= W - 1. Global layers: j <= i.
+* Vision tokens (the model card's ``use_bidirectional_attention="vision"``; RFC §5 row
+  ``multimodal_bidirectional_mask``): the tokens of one image see one another in both
+  directions, on top of the layer's own mask. An image is a span [s0, s1) of positions. The RFC
+  puts this mask in the global attention path; TensorFold's engine gives it to the sliding
+  layers (an image row sees every row of its image past the window) and keeps global layers
+  causal. Both readings are covered: the spans are an argument of either layer kind, and the
+  caller passes them to the layers it wants. A decode query is a text token and takes none.
 * Softmax scale defaults to 1/sqrt(D). No attention-logit soft cap (only the final logits
   are capped, RFC §2).
 * Positions are the index within the sequence: 0 .. L-1; a decode query sits at L-1.
@@ -166,15 +173,29 @@ def visible(q_pos: np.ndarray, k_pos: np.ndarray, window: int) -> np.ndarray:
     return ok
 
 
+def same_image(q_pos: np.ndarray, k_pos: np.ndarray, spans) -> np.ndarray:
+    """Boolean [n_q, n_k]: query and key are tokens of one image. spans lists the images as
+    [s0, s1) position ranges; text tokens lie in none."""
+    qp = np.asarray(q_pos, dtype=np.int64)[:, None]
+    kp = np.asarray(k_pos, dtype=np.int64)[None, :]
+    ok = np.zeros((qp.shape[0], kp.shape[1]), dtype=bool)
+    for s0, s1 in spans:
+        ok |= (qp >= s0) & (qp < s1) & (kp >= s0) & (kp < s1)
+    return ok
+
+
 def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, q_pos, k_pos, window: int,
-              scale: float) -> np.ndarray:
+              scale: float, spans=None) -> np.ndarray:
     """softmax_j(scale * q.k_j over visible j) . v_j for one head.
 
     q: [n, D] (already rotated); k: [m, D] (already rotated); v: [m, Dv]. Returns [n, Dv].
-    Every query must see at least one key.
+    Visible: the layer's mask (`visible`), or, with image spans, also a key of the query's own
+    image. Every query must see at least one key.
     """
     s = (np.asarray(q, np.float64) @ np.asarray(k, np.float64).T) * scale
     vis = visible(q_pos, k_pos, window)
+    if spans:
+        vis = vis | same_image(q_pos, k_pos, spans)
     if not vis.any(axis=1).all():
         raise ValueError("a query row sees no key")
     s = np.where(vis, s, -np.inf)
@@ -205,11 +226,13 @@ def keys_values(layer: Layer, k_hist: np.ndarray, v_hist: Optional[np.ndarray], 
 
 
 def layer_rows(layer: Layer, q_rows: np.ndarray, q_pos: Sequence[int], k_hist: np.ndarray,
-               v_hist: Optional[np.ndarray], pos_offset: int = 0, norms: Optional[Norms] = None) -> np.ndarray:
+               v_hist: Optional[np.ndarray], pos_offset: int = 0, norms: Optional[Norms] = None,
+               spans=None) -> np.ndarray:
     """Attention output of one sequence's query rows.
 
     q_rows: [n, Hq, D] raw query projections at positions q_pos (each < L, measured from the
-    first key); k_hist / v_hist as in `keys_values`. Returns [n, Hq, D] fp64.
+    first key); k_hist / v_hist as in `keys_values`; spans: the sequence's images as [s0, s1)
+    ranges of absolute positions (see `same_image`), or None. Returns [n, Hq, D] fp64.
     """
     q_rows = normed_q(norms, q_rows)
     q_pos = np.asarray(q_pos, dtype=np.int64)
@@ -221,16 +244,22 @@ def layer_rows(layer: Layer, q_rows: np.ndarray, q_pos: Sequence[int], k_hist: n
     out = np.empty((q_rows.shape[0], layer.n_q_heads, v.shape[2]), dtype=np.float64)
     for h in range(layer.n_q_heads):
         g = h // layer.group
-        out[:, h, :] = attention(q_rot[:, h, :], k_rot[:, g, :], v[:, g, :], qp, k_pos,
-                                 layer.window, layer.scale)
+        if spans:
+            out[:, h, :] = attention(q_rot[:, h, :], k_rot[:, g, :], v[:, g, :], qp, k_pos,
+                                     layer.window, layer.scale, spans)
+        else:
+            out[:, h, :] = attention(q_rot[:, h, :], k_rot[:, g, :], v[:, g, :], qp, k_pos,
+                                     layer.window, layer.scale)
     return out
 
 
 def prefill(layer: Layer, q: np.ndarray, k_hist: Sequence[np.ndarray], v_hist, q_start: Sequence[int],
-            q_len: Sequence[int], ctx_start: Sequence[int], norms: Optional[Norms] = None) -> np.ndarray:
+            q_len: Sequence[int], ctx_start: Sequence[int], norms: Optional[Norms] = None,
+            spans=None) -> np.ndarray:
     """Batched prefill: rows q_start[b] .. +q_len[b] of q [T, Hq, D] are sequence b's positions
     ctx_start[b] .. ctx_start[b]+q_len[b]-1; k_hist[b] holds that sequence's keys at positions
-    0 .. ctx_start[b]+q_len[b]-1. Rows of q outside every sequence come back as NaN."""
+    0 .. ctx_start[b]+q_len[b]-1. spans[b] (optional) lists sequence b's images as [s0, s1)
+    position ranges. Rows of q outside every sequence come back as NaN."""
     q = np.asarray(q, np.float64)
     out = np.full((q.shape[0], layer.n_q_heads, layer.head_dim), np.nan)
     for b in range(len(q_len)):
@@ -238,7 +267,8 @@ def prefill(layer: Layer, q: np.ndarray, k_hist: Sequence[np.ndarray], v_hist, q
         if L == 0:
             continue
         vb = None if v_hist is None else v_hist[b][:c + L]
-        out[s:s + L] = layer_rows(layer, q[s:s + L], np.arange(c, c + L), k_hist[b][:c + L], vb, 0, norms)
+        sp = None if spans is None else spans[b]
+        out[s:s + L] = layer_rows(layer, q[s:s + L], np.arange(c, c + L), k_hist[b][:c + L], vb, 0, norms, sp)
     return out
 
 

@@ -438,6 +438,106 @@ def test_credited_flops_closed_form():
     assert got == 4.0 * 512 * 32 * 2 * (8192 * 8193 // 2)
 
 
+# ---------------------------------------------------------------- vision-token mask
+
+def token_type_mask(token_type: np.ndarray, base: torch.Tensor) -> torch.Tensor:
+    """The usual construction of the vision mask from per-token types (1 = image token): each
+    maximal run of image tokens is one image, numbered by a cumulative sum over run starts; a
+    query and a key of the same image see each other; everything else keeps the base mask."""
+    tt = torch.from_numpy(np.asarray(token_type, np.int64))
+    starts = (tt == 1) & torch.cat([torch.ones(1, dtype=torch.bool), tt[:-1] == 0])
+    group = torch.cumsum(starts.long(), 0)
+    img = (tt[:, None] == 1) & (tt[None, :] == 1) & (group[:, None] == group[None, :])
+    return base | img
+
+
+def runs_of_ones(token_type):
+    """[s0, s1) of each maximal run of 1s, by a plain scan."""
+    spans, s0 = [], None
+    for i, t in enumerate(list(token_type) + [0]):
+        if t == 1 and s0 is None:
+            s0 = i
+        elif t != 1 and s0 is not None:
+            spans.append((s0, i))
+            s0 = None
+    return spans
+
+
+VISION_TYPES = {
+    # two images, one longer than the test window, one touching the last row
+    "mid": [0] * 5 + [1] * 13 + [0] * 6 + [1] * 4 + [0] * 9 + [1] * 3,
+    # an image at the very start, and single-token images
+    "edges": [1] * 7 + [0, 1, 0, 0, 1] + [0] * 10 + [1] * 9 + [0] * 12,
+}
+
+
+def check_vision_vs_sdpa(o, layer, types, seed=11):
+    r = rng(seed)
+    L = len(types)
+    q = r.standard_normal((L, layer.n_q_heads, layer.head_dim))
+    k = r.standard_normal((L, layer.n_kv_heads, layer.head_dim))
+    v = None if layer.kv_shared else r.standard_normal((L, layer.n_kv_heads, layer.head_dim))
+    got = o.layer_rows(layer, q, np.arange(L), k, v, spans=runs_of_ones(types))
+    pos = np.arange(L)[:, None]
+    qr = o.rope(q, pos, layer.rope_theta, layer.rope_partial)
+    kr = o.rope(k, pos, layer.rope_theta, layer.rope_partial)
+    vv = k if layer.kv_shared else v
+    tq = torch.from_numpy(qr).permute(1, 0, 2)[None]
+    tk = torch.from_numpy(kr).permute(1, 0, 2).repeat_interleave(layer.group, dim=0)[None]
+    tv = torch.from_numpy(vv).permute(1, 0, 2).repeat_interleave(layer.group, dim=0)[None]
+    ones = torch.ones(L, L, dtype=torch.bool)
+    base = torch.tril(ones)
+    if layer.window > 0:
+        base &= torch.triu(ones, diagonal=-(layer.window - 1))
+    mask = token_type_mask(np.asarray(types), base)
+    ref = F.scaled_dot_product_attention(tq, tk, tv, attn_mask=mask,
+                                         scale=1.0 / math.sqrt(layer.head_dim))[0].permute(1, 0, 2).numpy()
+    assert np.abs(got - ref).max() < 1e-11
+
+
+def check_whole_image_is_full_attention(o, L=24, seed=12):
+    """A global layer whose every token belongs to one image attends without any mask."""
+    layer = o.GLOBAL
+    r = rng(seed)
+    q = r.standard_normal((L, layer.n_q_heads, layer.head_dim))
+    s = r.standard_normal((L, layer.n_kv_heads, layer.head_dim))
+    got = o.layer_rows(layer, q, np.arange(L), s, None, spans=[(0, L)])
+    pos = np.arange(L)[:, None]
+    tq = torch.from_numpy(o.rope(q, pos, layer.rope_theta, layer.rope_partial)).permute(1, 0, 2)[None]
+    tk = torch.from_numpy(o.rope(s, pos, layer.rope_theta, layer.rope_partial)).permute(1, 0, 2)
+    tv = torch.from_numpy(s).permute(1, 0, 2)
+    ref = F.scaled_dot_product_attention(tq, tk.repeat_interleave(layer.group, 0)[None],
+                                         tv.repeat_interleave(layer.group, 0)[None], is_causal=False,
+                                         scale=1.0 / math.sqrt(layer.head_dim))[0].permute(1, 0, 2).numpy()
+    assert np.abs(got - ref).max() < 1e-11
+
+
+@pytest.mark.parametrize("types", sorted(VISION_TYPES))
+@pytest.mark.parametrize("layer", [oracle.with_window(oracle.SLIDING, 6), oracle.GLOBAL], ids=["sliding", "global"])
+def test_vision_mask_matches_token_type_construction(layer, types):
+    check_vision_vs_sdpa(oracle, layer, VISION_TYPES[types])
+
+
+def test_whole_sequence_image_is_unmasked_attention():
+    check_whole_image_is_full_attention(oracle)
+
+
+def test_vision_spans_in_batched_prefill_match_per_sequence_rows():
+    """prefill hands each sequence its own spans, also for a chunk that starts mid-context."""
+    r = rng(13)
+    layer = oracle.with_window(oracle.SLIDING, 8)
+    lens, ctx = [30, 21], [0, 9]
+    spans = [[(3, 14)], [(10, 25)]]
+    hist = [r.standard_normal((c + n, layer.n_kv_heads, layer.head_dim)) for n, c in zip(lens, ctx)]
+    vh = [r.standard_normal(h.shape) for h in hist]
+    q = r.standard_normal((sum(lens), layer.n_q_heads, layer.head_dim))
+    got = oracle.prefill(layer, q, hist, vh, [0, 30], lens, ctx, spans=spans)
+    want1 = oracle.layer_rows(layer, q[30:], np.arange(9, 30), hist[1], vh[1], spans=spans[1])
+    assert np.array_equal(got[30:], want1)
+    plain = oracle.prefill(layer, q, hist, vh, [0, 30], lens, ctx)
+    assert not np.allclose(got[:30], plain[:30])
+
+
 # ---------------------------------------------------------------- planted mistakes
 
 def _fails(fn, *a, **kw):
@@ -544,3 +644,28 @@ def test_control_norm_missing_on_queries(monkeypatch):
     monkeypatch.setattr(oa, "normed_q", lambda norms, q: np.asarray(q, np.float64))
     assert _fails(check_normed_layer_vs_torch, oa, oracle.GLOBAL)
     assert _fails(check_norm_scale_invariance, oa, oracle.with_window(oracle.SLIDING, 8))
+
+
+def test_control_vision_forward_only(monkeypatch):
+    good = oa.same_image
+    monkeypatch.setattr(oa, "same_image", lambda qp, kp, sp: good(qp, kp, sp) &
+                        (np.asarray(kp)[None, :] <= np.asarray(qp)[:, None]))
+    assert _fails(check_vision_vs_sdpa, oa, oracle.GLOBAL, VISION_TYPES["mid"])
+    assert _fails(check_whole_image_is_full_attention, oa)
+
+
+def test_control_vision_leaks_to_text_rows(monkeypatch):
+    def leaky(qp, kp, sp):
+        kp = np.asarray(kp)[None, :]
+        ok = np.zeros((len(qp), kp.shape[1]), dtype=bool)
+        for s0, s1 in sp:
+            ok |= (kp >= s0) & (kp < s1)
+        return ok
+    monkeypatch.setattr(oa, "same_image", leaky)
+    assert _fails(check_vision_vs_sdpa, oa, oracle.GLOBAL, VISION_TYPES["mid"])
+
+
+def test_control_vision_span_end_inclusive(monkeypatch):
+    good = oa.same_image
+    monkeypatch.setattr(oa, "same_image", lambda qp, kp, sp: good(qp, kp, [(a, b + 1) for a, b in sp]))
+    assert _fails(check_vision_vs_sdpa, oa, oracle.with_window(oracle.SLIDING, 6), VISION_TYPES["edges"])
