@@ -60,8 +60,8 @@
  * Errors. Host-side checks run before any launch and return G4_ERR_INVALID (bad pointer,
  * size or alignment) or G4_ERR_UNSUPPORTED (a geometry other than the two layer kinds
  * below); nothing is launched then. Problems only the device can see (a page-table entry
- * outside [0, num_pages), a position >= 262144 or beyond the page table, a bounded wait
- * that ran out) set bits in a device error word and the affected work is skipped; read and
+ * outside [0, num_pages), a position >= 262144 or beyond the page table, a bad image span
+ * (g4attn_prefill_vision), a bounded wait that ran out) set bits in a device error word and the affected work is skipped; read and
  * clear the word with g4attn_status_sync. Kernels never trap.
  */
 #ifndef G4ATTN_H
@@ -188,6 +188,29 @@ g4_status g4attn_prefill_attend(const g4attn_layer* layer, int32_t T, const int3
 g4_status g4attn_prefill_normed(const g4attn_layer* layer, const g4attn_norms* norms, const void* q,
                                 const void* k, const void* v, int32_t T, const int32_t* q_start,
                                 const int32_t* q_len, const int32_t* ctx_start, int32_t B,
+                                const g4attn_cache* cache, const int32_t* page_table, int32_t max_pages,
+                                void* out, void* stream);
+
+/* g4attn_prefill_normed with the vision-token mask: the tokens of one image see each other in
+ * both directions, on top of the layer's own mask (model card "Gemma 4 31B":
+ * use_bidirectional_attention="vision"; RFC section 5, multimodal_bidirectional_mask). Available
+ * on both layer kinds: the RFC places the mask in global attention, TensorFold's engine on the
+ * sliding layers (where an image row sees all of its image past the window); the caller passes
+ * spans to the layers it wants.
+ *   span  int32 [T][2], device, 8-byte aligned, or NULL (then exactly g4attn_prefill_normed).
+ *         Row t (a memory row, indexed like q) holds the image span [s0, s1) of absolute
+ *         positions that its token belongs to; s1 <= s0 marks a text row. Gap rows are not read.
+ *         A row's span must hold the row's position and end by ctx_start + q_len of its
+ *         sequence (an image lies within one call: its keys are appended by the same call), and
+ *         all rows of one image carry the same span. Else the device sets G4_ERR_DEVICE (read by
+ *         g4attn_status_sync); the row then falls back to the layer mask and its output is not
+ *         the masked attention.
+ * Each row then sees one run of keys, lo .. hi: the layer mask's run widened to its image. A
+ * decode query is a text token, so decoding takes no spans. Other errors as
+ * g4attn_prefill_normed; a misaligned span gives G4_ERR_INVALID before any launch. */
+g4_status g4attn_prefill_vision(const g4attn_layer* layer, const g4attn_norms* norms, const void* q,
+                                const void* k, const void* v, int32_t T, const int32_t* q_start,
+                                const int32_t* q_len, const int32_t* ctx_start, int32_t B, const int32_t* span,
                                 const g4attn_cache* cache, const int32_t* page_table, int32_t max_pages,
                                 void* out, void* stream);
 g4_status g4attn_kv_append_normed(const g4attn_layer* layer, const g4attn_norms* norms, const void* k,

@@ -23,7 +23,7 @@ PAGE_SIZE = 16
 DECODE_STATIC_SCRATCH_BYTES = 32 << 20   # the static scratch of g4attn_decode_static, per device
 
 EXPORTS = ("g4attn_rope_apply", "g4attn_prefill", "g4attn_prefill_stage", "g4attn_prefill_attend",
-           "g4attn_prefill_normed", "g4attn_kv_append_normed", "g4attn_decode_normed",
+           "g4attn_prefill_normed", "g4attn_prefill_vision", "g4attn_kv_append_normed", "g4attn_decode_normed",
            "g4attn_kv_append", "g4attn_decode_workspace_bytes",
            "g4attn_decode", "g4attn_decode_static", "g4attn_provenance", "g4attn_status_sync", "g4attn_status_string")
 
@@ -71,6 +71,7 @@ def load(path: Optional[str] = None):
         "g4attn_prefill_stage": (I32, [L, P, P, P, I32, P, P, P, I32, C, P, I32, P, P]),
         "g4attn_prefill_attend": (I32, [L, I32, P, P, P, I32, C, P, I32, P, P]),
         "g4attn_prefill_normed": (I32, [L, N, P, P, P, I32, P, P, P, I32, C, P, I32, P, P]),
+        "g4attn_prefill_vision": (I32, [L, N, P, P, P, I32, P, P, P, I32, P, C, P, I32, P, P]),
         "g4attn_kv_append_normed": (I32, [L, N, P, P, I32, P, P, P, I32, C, P, I32, P]),
         "g4attn_decode_normed": (I32, [L, N, P, P, P, P, I32, C, P, I32, P, P, SZ, P]),
         "g4attn_kv_append": (I32, [L, P, P, I32, P, P, P, I32, C, P, I32, P]),
@@ -219,6 +220,20 @@ def g4attn_prefill_normed(layer, norms: g4attn_norms, q, k, v, q_start, q_len, c
                                         _ptr(q_start), _ptr(q_len), _ptr(ctx_start), B, ctypes.byref(cache),
                                         _ptr(page_table), int(page_table.shape[1]), _ptr(out), _stream(stream)),
            "g4attn_prefill_normed")
+    return out
+
+
+def g4attn_prefill_vision(layer, norms, q, k, v, q_start, q_len, ctx_start, span, cache: g4attn_cache,
+                          page_table, out, stream=None):
+    """g4attn_prefill_normed with image spans: span is an int32 [T, 2] device tensor (or None),
+    row t's image [s0, s1) of absolute positions, s1 <= s0 for a text row. norms may be None."""
+    T, B = int(q.shape[0]), int(q_start.shape[0])
+    nrm = None if norms is None else ctypes.byref(norms)
+    _check(load().g4attn_prefill_vision(ctypes.byref(layer), nrm, _ptr(q), _ptr(k), _ptr(v), T,
+                                        _ptr(q_start), _ptr(q_len), _ptr(ctx_start), B, _ptr(span),
+                                        ctypes.byref(cache), _ptr(page_table), int(page_table.shape[1]), _ptr(out),
+                                        _stream(stream)),
+           "g4attn_prefill_vision")
     return out
 
 

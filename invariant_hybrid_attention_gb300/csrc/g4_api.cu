@@ -127,7 +127,7 @@ const char* g4attn_status_string(g4_status s) {
     case G4_ERR_CUDA: return "CUDA runtime error";
     case G4_ERR_SCRATCH: return "decode step larger than the static scratch buffer";
     case G4_ERR_TIMEOUT: return "bounded device wait timed out";
-    case G4_ERR_DEVICE: return "device-detected bad page index or position";
+    case G4_ERR_DEVICE: return "device-detected bad page index, position or image span";
   }
   return "unknown status";
 }
@@ -203,30 +203,48 @@ g4_status g4attn_prefill_stage(const g4attn_layer* layer, const void* q, const v
                        stream);
 }
 
-g4_status g4attn_prefill_attend(const g4attn_layer* layer, int32_t T, const int32_t* q_start, const int32_t* q_len,
-                                const int32_t* ctx_start, int32_t B, const g4attn_cache* cache,
+static g4_status prefill_attend(const g4attn_layer* layer, int32_t T, const int32_t* q_start, const int32_t* q_len,
+                                const int32_t* ctx_start, int32_t B, const int32_t* span, const g4attn_cache* cache,
                                 const int32_t* page_table, int32_t max_pages, void* out, void* stream) {
   bool global = false;
   g4_status s = check_layer(layer, &global);
   if (s != G4_OK) return s;
   if ((s = check_rows(out, T, q_start, q_len, ctx_start, B)) != G4_OK) return s;
   if ((s = check_cache(cache, global, page_table, max_pages)) != G4_OK) return s;
+  if (span && (reinterpret_cast<uintptr_t>(span) & 7u)) return G4_ERR_INVALID;
   if (T == 0) return G4_OK;
   DeviceState st;
   if (device_state(&st) != cudaSuccess) return G4_ERR_CUDA;
-  const SeqRows rows{q_start, q_len, ctx_start, B, T};
+  const SeqRows rows{q_start, q_len, ctx_start, B, T, span};
   return from_cuda(launch_prefill(global, rows, global ? 0 : layer->window, scale_log2(layer),
                                   paged(cache, page_table, max_pages), out, st, (cudaStream_t)stream));
+}
+
+g4_status g4attn_prefill_attend(const g4attn_layer* layer, int32_t T, const int32_t* q_start, const int32_t* q_len,
+                                const int32_t* ctx_start, int32_t B, const g4attn_cache* cache,
+                                const int32_t* page_table, int32_t max_pages, void* out, void* stream) {
+  return prefill_attend(layer, T, q_start, q_len, ctx_start, B, nullptr, cache, page_table, max_pages, out, stream);
+}
+
+g4_status g4attn_prefill_vision(const g4attn_layer* layer, const g4attn_norms* norms, const void* q, const void* k,
+                                const void* v, int32_t T, const int32_t* q_start, const int32_t* q_len,
+                                const int32_t* ctx_start, int32_t B, const int32_t* span,
+                                const g4attn_cache* cache, const int32_t* page_table, int32_t max_pages, void* out,
+                                void* stream) {
+  // The span check comes first, so that a refused call launches nothing.
+  if (span && (reinterpret_cast<uintptr_t>(span) & 7u)) return G4_ERR_INVALID;
+  g4_status s = prefill_stage(layer, norms, q, k, v, T, q_start, q_len, ctx_start, B, cache, page_table, max_pages,
+                              out, stream);
+  if (s != G4_OK) return s;
+  return prefill_attend(layer, T, q_start, q_len, ctx_start, B, span, cache, page_table, max_pages, out, stream);
 }
 
 g4_status g4attn_prefill_normed(const g4attn_layer* layer, const g4attn_norms* norms, const void* q, const void* k,
                                 const void* v, int32_t T, const int32_t* q_start, const int32_t* q_len,
                                 const int32_t* ctx_start, int32_t B, const g4attn_cache* cache,
                                 const int32_t* page_table, int32_t max_pages, void* out, void* stream) {
-  g4_status s = prefill_stage(layer, norms, q, k, v, T, q_start, q_len, ctx_start, B, cache, page_table, max_pages,
-                              out, stream);
-  if (s != G4_OK) return s;
-  return g4attn_prefill_attend(layer, T, q_start, q_len, ctx_start, B, cache, page_table, max_pages, out, stream);
+  return g4attn_prefill_vision(layer, norms, q, k, v, T, q_start, q_len, ctx_start, B, nullptr, cache, page_table,
+                               max_pages, out, stream);
 }
 
 g4_status g4attn_prefill(const g4attn_layer* layer, const void* q, const void* k, const void* v, int32_t T,
@@ -340,7 +358,7 @@ g4_status g4attn_status_sync(void* stream) {
   if (cudaMemcpy(&word, st.err, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return G4_ERR_CUDA;
   if (word != 0 && cudaMemset(st.err, 0, sizeof(word)) != cudaSuccess) return G4_ERR_CUDA;
   if (word & kErrTimeout) return G4_ERR_TIMEOUT;
-  if (word & (kErrPage | kErrPos)) return G4_ERR_DEVICE;
+  if (word & (kErrPage | kErrPos | kErrSpan)) return G4_ERR_DEVICE;
   return G4_OK;
 }
 

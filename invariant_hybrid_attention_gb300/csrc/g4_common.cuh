@@ -27,7 +27,7 @@ constexpr int kDecodeChunkSliding = 256;  // keys per fixed decode chunk (aligne
 constexpr int kDecodeChunkGlobal = 1024;
 
 // Error-word bits (g4attn_status_sync maps them to g4_status values).
-enum : uint32_t { kErrTimeout = 1u, kErrPage = 2u, kErrPos = 4u };
+enum : uint32_t { kErrTimeout = 1u, kErrPage = 2u, kErrPos = 4u, kErrSpan = 8u };
 
 // Bounded waits give up after this long; nothing legitimate waits anywhere near it.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;

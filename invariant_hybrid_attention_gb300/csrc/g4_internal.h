@@ -27,6 +27,9 @@ struct SeqRows {
   const int32_t* ctx_start;
   int32_t B;
   int32_t T;
+  // Optional int32 [T][2]: the image span [s0, s1) of absolute positions of each query row
+  // (memory row index, like q); s1 <= s0 marks a text row. NULL: every row is text.
+  const int32_t* span = nullptr;
 };
 
 struct PagedCache {

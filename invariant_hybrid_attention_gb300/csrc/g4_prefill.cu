@@ -98,7 +98,8 @@ struct Unit {
 
 // Warp-wide. False when unit u holds no rows (its slot is past the last query tile) or its
 // positions are out of range (then the error word is set); every role skips such units alike.
-// Not inlined: six roles call it, once per unit.
+// Not inlined: six roles call it, once per unit. kSpan: the batch may hold image rows.
+template <bool kSpan>
 __device__ __noinline__ bool sliding_unit(const PrefillParams& p, int u, uint32_t rank, Unit& o) {
   o.g = u % kSlidingHkv;
   o.h = 2 * o.g + (int)rank;
@@ -115,16 +116,30 @@ __device__ __noinline__ bool sliding_unit(const PrefillParams& p, int u, uint32_
     return false;
   }
   const int W = p.window;
-  o.k_lo = W > 0 ? max(0, o.p_lo - W + 1) : 0;
-  o.k_hi = o.p_hi;
+  o.q_row0 = qs + (kBM * t - cs);   // memory row of tile row 0 (may be negative)
+  if constexpr (kSpan) {
+    // The rows' key runs start no earlier than the first row's and end no later than the last
+    // row's: the layer mask moves with the position, and an image holding a row inside the tile
+    // and reaching past an end row holds that end row too.
+    int lo_l, hi_f;
+    row_keys(p.rows, W, o.q_row0 + (o.p_lo - kBM * t), o.p_lo, o.ctx_end, p.err, o.k_lo, hi_f);
+    row_keys(p.rows, W, o.q_row0 + (o.p_hi - kBM * t), o.p_hi, o.ctx_end, p.err, lo_l, o.k_hi);
+    if ((o.k_hi >> 4) >= p.max_pages) {   // an image past the page table (the rows' own pages fit)
+      if ((threadIdx.x & 31) == 0) set_error(p.err, kErrPos);
+      return false;
+    }
+  } else {
+    o.k_lo = W > 0 ? max(0, o.p_lo - W + 1) : 0;
+    o.k_hi = o.p_hi;
+  }
   o.kt0 = o.k_lo / kSN;
   o.n_tiles = o.k_hi / kSN - o.kt0 + 1;
-  o.q_row0 = qs + (kBM * t - cs);   // memory row of tile row 0 (may be negative)
   o.pt = p.page_table + (size_t)b * p.max_pages;
   o.qpos = min(kQAfter, o.n_tiles);
   return true;
 }
 
+template <bool kSpan>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     prefill_sliding_kernel(const __grid_constant__ CUtensorMap tmap_q, PrefillParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -198,7 +213,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (!is_v && lane == 0) prefetch_tmap(&tmap_q);
     auto next_valid = [&](int& uu, Unit& o) -> bool {   // this cluster's first unit >= uu with rows
       for (; uu < p.n_units; uu += n_clusters)
-        if (sliding_unit(p, uu, rank, o)) return true;
+        if (sliding_unit<kSpan>(p, uu, rank, o)) return true;
       return false;
     };
     auto raw_blocks = [&](const Unit& o, int j0) -> int {   // raw table entry of this lane's page
@@ -311,7 +326,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int u = cluster; ok && u < p.n_units; u += n_clusters) {
       Unit un;
-      if (!sliding_unit(p, u, rank, un)) continue;
+      if (!sliding_unit<kSpan>(p, u, rank, un)) continue;
       for (int idx = 0; idx <= un.n_tiles; ++idx, ++c) {   // every slot, the unit's Q included
         const int s = c % kNK;
         ok = __all_sync(0xffffffffu, mbar_wait_ool(&sm.k_full[s], (c / kNK) & 1, abort_flag, p.err));
@@ -335,7 +350,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int u = cluster; ok && u < p.n_units; u += n_clusters) {
       Unit un;
-      if (!sliding_unit(p, u, rank, un)) continue;
+      if (!sliding_unit<kSpan>(p, u, rank, un)) continue;
       // the unit's Q: its slot has landed, and both CTAs' softmax warps have moved dims 0-127
       ok = __all_sync(0xffffffffu, slot_ready(c0 + un.qpos) && mbar_wait_cl_ool(&sm.q_pair, uq & 1, abort_flag, p.err));
       for (int j = 0; ok && j < un.n_tiles; ++j, ++jt) {
@@ -378,7 +393,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int u = cluster; ok && u < p.n_units; u += n_clusters) {
       Unit un;
-      if (!sliding_unit(p, u, rank, un)) continue;
+      if (!sliding_unit<kSpan>(p, u, rank, un)) continue;
       for (int i = 0; i < un.n_tiles; ++i, ++cv, ++jt) {
         const int s = cv % kNV;
         ok = __all_sync(0xffffffffu, mbar_wait_ool(&sm.v_full[s], (cv / kNV) & 1, abort_flag, p.err));
@@ -430,7 +445,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     bool ok = true;
     auto next_unit = [&](Unit& o) -> bool {   // this cluster's next unit with rows (warp-wide)
       for (u += n_clusters; u < p.n_units; u += n_clusters)
-        if (sliding_unit(p, u, rank, o)) return true;
+        if (sliding_unit<kSpan>(p, u, rank, o)) return true;
       return false;
     };
     // Q dims 0-127 of unit o (the roped tile the producer put in K ring slot c0o + qpos, 128B
@@ -481,6 +496,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     while (ok && have) {
       const int pos = kBM * cur.t + r;
       const bool row_ok = pos >= cur.p_lo && pos <= cur.p_hi;
+      int row_lo = W > 0 ? max(0, pos - W + 1) : 0, row_hi = pos;   // the row's keys
+      if (kSpan && row_ok) {
+        row_keys(p.rows, W, cur.q_row0 + r, pos, cur.ctx_end, p.err, row_lo, row_hi);
+        if (row_lo < cur.k_lo || row_hi > cur.k_hi) {   // spans that disagree between rows
+          set_error(p.err, kErrSpan);
+          row_lo = max(row_lo, cur.k_lo);
+          row_hi = min(row_hi, cur.k_hi);
+        }
+      }
       float m_used = -INFINITY, l_run = 0.f;
       for (int j = 0; j < cur.n_tiles; ++j, ++jt) {
         const int kb = (cur.kt0 + j) * kSN;
@@ -502,10 +526,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         float s[kSN];
 #pragma unroll
         for (int c = 0; c < kSN; ++c) s[c] = __uint_as_float(sr[c]);
-        const bool full = row_ok && kb + kSN - 1 <= pos && (W == 0 || pos - kb <= W - 1);
+        const bool full = kSpan ? row_ok && kb >= row_lo && kb + kSN - 1 <= row_hi
+                                : row_ok && kb + kSN - 1 <= pos && (W == 0 || pos - kb <= W - 1);
         if (!full) {   // the row's visible keys in this tile are one run of columns [lo, hi]
-          int lo = W > 0 ? max(0, pos - W + 1 - kb) : 0;
-          int hi = row_ok ? min(kSN - 1, pos - kb) : -1;
+          int lo = kSpan ? max(0, row_lo - kb) : (W > 0 ? max(0, pos - W + 1 - kb) : 0);
+          int hi = row_ok ? min(kSN - 1, (kSpan ? row_hi : pos) - kb) : -1;
           if (hi < lo) lo = hi = 1 << 20;   // none
           const unsigned span = (unsigned)(hi - lo);
 #pragma unroll
@@ -681,14 +706,16 @@ cudaError_t launch_prefill(bool global, const SeqRows& rows, int window, float s
   p.v_cache = cache.v;
   CUtensorMap mq;
   if (!q_map(&mq, out, rows.T, kSlidingHq, kSD)) return cudaErrorInvalidValue;
-  static bool attr[64] = {};
-  static int max_clusters[64] = {};
+  // Batches with image rows take their own instantiation, so that the plain one carries no span code.
+  auto kernel = rows.span ? prefill_sliding_kernel<true> : prefill_sliding_kernel<false>;
+  const int ki = rows.span ? 1 : 0;
+  static bool attr[64][2] = {};
+  static int max_clusters[64][2] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!attr[dev]) {
-    cudaError_t e =
-        cudaFuncSetAttribute(prefill_sliding_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSlidingSmemBytes);
+  if (!attr[dev][ki]) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSlidingSmemBytes);
     if (e != cudaSuccess) return e;
     // clusters that fit on the device at once: the persistent grid
     cudaLaunchConfig_t cfg = {};
@@ -703,17 +730,17 @@ cudaError_t launch_prefill(bool global, const SeqRows& rows, int window, float s
     cfg.attrs = la;
     cfg.numAttrs = 1;
     int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, prefill_sliding_kernel, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
     if (e != cudaSuccess) return e;
-    max_clusters[dev] = n > 0 ? n : 1;
-    attr[dev] = true;
+    max_clusters[dev][ki] = n > 0 ? n : 1;
+    attr[dev][ki] = true;
   }
   const long long slots = (long long)rows.T / kBM + 2LL * rows.B;
   const long long n_units = slots * kSlidingHkv;   // (query tile, KV head) units, one per cluster at a time
   if (n_units <= 0 || n_units > 0x3fffffffLL) return cudaErrorInvalidValue;
   p.n_units = (int)n_units;
-  const int n_clusters = (int)(n_units < max_clusters[dev] ? n_units : max_clusters[dev]);
-  prefill_sliding_kernel<<<2u * (unsigned)n_clusters, kThreads, kSlidingSmemBytes, s>>>(mq, p);
+  const int n_clusters = (int)(n_units < max_clusters[dev][ki] ? n_units : max_clusters[dev][ki]);
+  kernel<<<2u * (unsigned)n_clusters, kThreads, kSlidingSmemBytes, s>>>(mq, p);
   return cudaGetLastError();
 }
 

@@ -111,6 +111,33 @@ inline __device__ int page_check(int raw, int num_pages, int hkv, int g, uint32_
   return raw * hkv + g;
 }
 
+// Keys [lo, hi] that the query at position pos (memory row `row`) sees, in a sequence whose keys
+// end at ctx_end - 1: the layer's mask (causal; with a window W > 0 also pos - j <= W - 1),
+// widened for an image token to every token of its image, in both directions (the model card's
+// use_bidirectional_attention="vision"). As the layer mask already holds pos, the union is one run
+// of keys. An image span must hold pos and end by ctx_end (its keys are in the cache); any other
+// non-empty span sets kErrSpan and leaves the row to the layer mask.
+inline __device__ void row_keys(const SeqRows& rows, int window, int row, int pos, int ctx_end, uint32_t* err,
+                                int& lo, int& hi) {
+  lo = window > 0 ? max(0, pos - window + 1) : 0;
+  hi = pos;
+  if (rows.span) {
+    if ((unsigned)row >= (unsigned)rows.T) {   // a sequence laid out past the q rows
+      set_error(err, kErrPos);
+      return;
+    }
+    const int2 s = __ldg(reinterpret_cast<const int2*>(rows.span) + row);
+    if (s.y > s.x) {
+      if (s.x >= 0 && s.x <= pos && pos < s.y && s.y <= ctx_end) {
+        lo = min(lo, s.x);
+        hi = s.y - 1;
+      } else {
+        set_error(err, kErrSpan);
+      }
+    }
+  }
+}
+
 inline __device__ uint32_t tmem_lane_base(int warp) { return (uint32_t)(32 * (warp & 3)) << 16; }
 
 // Full cluster barrier (every thread of both CTAs); used once, after the mbarriers are set up.

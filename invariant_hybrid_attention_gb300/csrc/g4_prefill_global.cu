@@ -166,9 +166,16 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0 && rank == 0 && hp == 0) set_error(p.err, kErrPos);
     return;
   }
-  const int k_hi = p_hi;
-  const int n_tiles = k_hi / kTN + 1;
   const int q_row0 = qs + (kBM * t - cs);
+  // Keys 0 .. k_hi: the last row's run ends no earlier than any other row's (an image holding a
+  // row of the tile and reaching past the last row holds the last row too).
+  int k_hi, k_lo_unused;
+  row_keys(p.rows, 0, q_row0 + (p_hi - kBM * t), p_hi, ctx_end, p.err, k_lo_unused, k_hi);
+  if ((k_hi >> 4) >= p.max_pages) {   // an image past the page table (the rows' own pages fit)
+    if (threadIdx.x == 0 && rank == 0 && hp == 0) set_error(p.err, kErrPos);
+    return;
+  }
+  const int n_tiles = k_hi / kTN + 1;
   const int32_t* pt = p.page_table + (size_t)b * p.max_pages;
 
   if (threadIdx.x == 32) {
@@ -317,6 +324,15 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t tq = tm + tmem_lane_base(warp);
       const int pos = kBM * t + r;
       const bool row_ok = pos >= p_lo && pos <= p_hi;
+      int row_hi = pos;   // the row sees keys 0 .. row_hi
+      if (p.rows.span && row_ok) {
+        int row_lo;
+        row_keys(p.rows, 0, q_row0 + r, pos, ctx_end, p.err, row_lo, row_hi);
+        if (row_hi > k_hi) {   // spans that disagree between rows
+          set_error(p.err, kErrSpan);
+          row_hi = k_hi;
+        }
+      }
       bool ok = __all_sync(0xffffffffu, mbar_wait(&bar.q_full, 0, abort_flag, p.err));
       if (ok) {   // Q (128B-swizzled boxes in K stages 1-2) -> tensor memory, bf16 pairs
         const uint8_t* qrow = q_stage + r * 128;
@@ -367,8 +383,8 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         float s[kTN];
 #pragma unroll
         for (int c = 0; c < kTN; ++c) s[c] = __uint_as_float(sr[c]);
-        if (!(row_ok && kb + kTN - 1 <= pos)) {   // causal mask (and rows outside the sequence)
-          const int hi = row_ok ? pos - kb : -1;
+        if (!(row_ok && kb + kTN - 1 <= row_hi)) {   // causal mask (and rows outside the sequence)
+          const int hi = row_ok ? row_hi - kb : -1;
 #pragma unroll
           for (int c = 0; c < kTN; ++c) s[c] = (c <= hi) ? s[c] : -INFINITY;
         }

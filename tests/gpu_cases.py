@@ -59,8 +59,9 @@ class Batch:
     """A prefill batch: per-sequence histories (positions 0 .. ctx_start+q_len-1) and the new rows."""
 
     def __init__(self, kind, q_lens, ctx_starts=None, padded=False, seed=0, scale=1.0, pad_to=None,
-                 spare_pages=3, page_seed=None):
+                 spare_pages=3, page_seed=None, spans=None):
         self.kind = kind
+        self.spans = spans   # per sequence: its images as [s0, s1) position ranges, or None
         geo = GEOM[kind]
         self.n_kv, self.d = geo["n_kv"], geo["d"]
         self.q_lens = [int(x) for x in q_lens]
@@ -93,8 +94,22 @@ class Batch:
         else:
             g4.g4attn_kv_append_normed(layer, norms.arg, k, v, *rows, cache.desc, table)
 
+    def span_rows(self) -> torch.Tensor:
+        """int32 [T, 2]: each sequence row's image span, (0, 0) for text rows, and for gap rows
+        values that would be refused if the kernels read them."""
+        t = torch.tensor([[-7, 1 << 30]] * self.layout.T, dtype=torch.int32).reshape(-1, 2)
+        for b, L in enumerate(self.q_lens):
+            s, c = self.layout.q_start[b], self.ctx_starts[b]
+            for r in range(L):
+                t[s + r] = torch.tensor([0, 0])
+                for s0, s1 in (self.spans[b] if self.spans else []):
+                    if s0 <= c + r < s1:
+                        t[s + r] = torch.tensor([s0, s1])
+        return t
+
     def run(self, layer, out_fill=float("nan"), split=False, norms=None):
-        """One prefill of the batch: g4attn_prefill, or (split) its two steps called apart."""
+        """One prefill of the batch: g4attn_prefill, or (split) its two steps called apart; with
+        spans, g4attn_prefill_vision."""
         cache = self.device_cache()
         table = self.plan.table.cuda()
         self.append_history(layer, cache, table, norms)
@@ -103,7 +118,10 @@ class Batch:
         v = None if self.v_rows is None else self.v_rows.cuda()
         out = torch.full_like(q, out_fill)
         rows = (device_int32(self.layout.q_start), device_int32(self.layout.q_len), device_int32(self.layout.ctx_start))
-        if norms is not None:
+        if self.spans is not None:
+            g4.g4attn_prefill_vision(layer, None if norms is None else norms.arg, q, k, v, *rows,
+                                     self.span_rows().cuda(), cache.desc, table, out)
+        elif norms is not None:
             g4.g4attn_prefill_normed(layer, norms.arg, q, k, v, *rows, cache.desc, table, out)
         elif split:
             g4.g4attn_prefill_stage(layer, q, k, v, *rows, cache.desc, table, out)
@@ -122,7 +140,8 @@ class Batch:
         q = self.q[s + idx].double().numpy()
         v = None if self.hist_v is None else self.hist_v[b].double().numpy()
         return oracle.layer_rows(olayer, q, c + idx, self.hist_k[b].double().numpy(), v, 0,
-                                 None if norms is None else norms.oracle)
+                                 None if norms is None else norms.oracle,
+                                 self.spans[b] if self.spans else None)
 
 
 class DecodeBatch:

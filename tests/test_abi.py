@@ -120,6 +120,17 @@ def test_norm_arguments_refused_on_host(lib):
                                     None) == g4.G4_ERR_UNSUPPORTED
 
 
+
+def test_misaligned_image_span_refused_on_host(lib):
+    """g4attn_prefill_vision reads spans as int32 pairs: a pointer off an 8-byte boundary is
+    refused before anything runs (the other pointers here are fake and never touched)."""
+    s, gl = g4.sliding_layer(), g4.global_layer()
+    cs = g4.g4attn_cache(16, 32, None, 4, 16)
+    cg = g4.g4attn_cache(16, None, 48, 4, 16)
+    for layer, cache, v in ((s, cs, 16), (gl, cg, None)):
+        assert lib.g4attn_prefill_vision(ctypes.byref(layer), None, 16, 16, v, 8, 16, 16, 16, 1, 20,
+                                         ctypes.byref(cache), 16, 1, 16, None) == g4.G4_ERR_INVALID
+
 def test_workspace_sizes(lib):
     s, gl = g4.sliding_layer(), g4.global_layer()
     # sliding: a 1024-key window touches at most 5 chunks of 256 keys; partial = (m, l) + 256 floats

@@ -330,6 +330,98 @@ def test_prefill_normed_batch_invariance(kind):
         assert torch.equal(out_a[:L].cpu(), out_b[s:s + L].cpu()), (kind, lens, padded, at)
 
 
+# ---------------------------------------------------------------- vision-token mask
+
+VISION_CASES = {
+    # an image longer than the window and across query and key tiles, one touching the last row,
+    # a one-token image, and (second sequence) an image that began in the cached history
+    "sliding": dict(q_lens=[300, 517, 129], ctx=[0, 40, 0], window=96,
+                    spans=[[(20, 150), (290, 300)], [(30, 90), (200, 201), (400, 557)], [(0, 129)]]),
+    "global": dict(q_lens=[260, 130, 64], ctx=[0, 5, 0], window=0,
+                   spans=[[(10, 200), (255, 260)], [(5, 6), (100, 135)], [(0, 64)]]),
+}
+
+
+@pytest.mark.parametrize("padded", [False, True], ids=["packed", "padded"])
+@pytest.mark.parametrize("kind", ["sliding", "global"])
+def test_prefill_vision_matches_oracle(kind, padded):
+    c = VISION_CASES[kind]
+    bt = Batch(kind, c["q_lens"], ctx_starts=c["ctx"], padded=padded, seed=61, scale=0.5, spans=c["spans"])
+    check_prefill(bt, kind, c["window"])
+    assert g4.g4attn_status_sync() == g4.G4_OK
+
+
+@pytest.mark.parametrize("kind", ["sliding", "global"])
+def test_prefill_vision_text_only_is_bit_identical_to_prefill(kind):
+    """No image rows, or one-token images (which widen nothing), give the plain prefill's bits."""
+    c = VISION_CASES[kind]
+    layer, _ = layers(kind, c["window"] or 1024)
+    plain = Batch(kind, c["q_lens"], ctx_starts=c["ctx"], seed=62, scale=0.5)
+    out_p, _ = plain.run(layer)
+    for spans in ([[] for _ in c["q_lens"]], [[(c0 + 3, c0 + 4)] for c0 in c["ctx"]]):
+        vis = Batch(kind, c["q_lens"], ctx_starts=c["ctx"], seed=62, scale=0.5, spans=spans)
+        out_v, _ = vis.run(layer)
+        assert torch.equal(out_p.cpu(), out_v.cpu())
+
+
+@pytest.mark.parametrize("kind", ["sliding", "global"])
+def test_prefill_vision_batch_invariance(kind):
+    """A sequence with images, alone and among other sequences with their own images: same bits."""
+    window = 1024 if kind == "sliding" else 0
+    layer, _ = layers(kind, window or 1024)
+    L = 1400
+    spans = [(100, 1300), (1350, 1360)]
+    alone = Batch(kind, [L], seed=63, scale=0.5, spans=[spans])
+    out_a, _ = alone.run(layer)
+    for lens, padded, at, others in [([200, L, 33], False, 1, [[(0, 150)], None, [(5, 33)]]),
+                                     ([L, 700], True, 0, [None, [(600, 700)]])]:
+        bt = Batch(kind, lens, padded=padded, seed=64 + len(lens), scale=0.5,
+                   spans=[spans if i == at else (o or []) for i, o in enumerate(others)])
+        bt.hist_k[at] = alone.hist_k[0]
+        if kind == "sliding":
+            bt.hist_v[at] = alone.hist_v[0]
+        s = bt.layout.q_start[at]
+        bt.q[s:s + L] = alone.q[:L]
+        bt.k_rows = gi.rows_of(bt.hist_k, bt.layout)
+        if kind == "sliding":
+            bt.v_rows = gi.rows_of(bt.hist_v, bt.layout)
+        out_b, _ = bt.run(layer)
+        assert torch.equal(out_a[:L].cpu(), out_b[s:s + L].cpu()), (lens, padded, at)
+
+
+@pytest.mark.parametrize("kind", ["sliding", "global"])
+def test_prefill_vision_bad_spans_are_reported(kind):
+    """A span reaching past the call's rows, and rows of one image that disagree on its span, are
+    seen on the device: the status says so, and the next call starts clean."""
+    window = 1024 if kind == "sliding" else 0
+    layer, _ = layers(kind, window or 1024)
+    for spans in ([[(50, 400)]],                    # ends past the sequence's 300 keys
+                  [[(10, 60)], ]):                  # consistent, as a control
+        bt = Batch(kind, [300], seed=65, scale=0.5, spans=spans)
+        cache = bt.device_cache()
+        rows = (device_int32(bt.layout.q_start), device_int32(bt.layout.q_len), device_int32(bt.layout.ctx_start))
+        out = torch.zeros_like(bt.q).cuda()
+        sp = bt.span_rows()
+        g4.g4attn_prefill_vision(layer, None, bt.q.cuda(), bt.k_rows.cuda(),
+                                 None if bt.v_rows is None else bt.v_rows.cuda(), *rows, sp.cuda(), cache.desc,
+                                 bt.plan.table.cuda(), out)
+        want = g4.G4_ERR_DEVICE if spans[0][0][1] > 300 else g4.G4_OK
+        assert g4.g4attn_status_sync() == want
+    # rows 10..199 form one image, but row 127, the last of the first query tile, claims to be
+    # text: that tile's key range then stops at key 127 while its rows 10..126 reach key 199
+    bt = Batch(kind, [300], seed=65, scale=0.5, spans=[[(10, 200)]])
+    sp = bt.span_rows()
+    sp[127] = torch.tensor([0, 0])
+    cache = bt.device_cache()
+    rows = (device_int32(bt.layout.q_start), device_int32(bt.layout.q_len), device_int32(bt.layout.ctx_start))
+    out = torch.zeros_like(bt.q).cuda()
+    g4.g4attn_prefill_vision(layer, None, bt.q.cuda(), bt.k_rows.cuda(),
+                             None if bt.v_rows is None else bt.v_rows.cuda(), *rows, sp.cuda(), cache.desc,
+                             bt.plan.table.cuda(), out)
+    assert g4.g4attn_status_sync() == g4.G4_ERR_DEVICE
+    assert g4.g4attn_status_sync() == g4.G4_OK
+
+
 # ---------------------------------------------------------------- degenerate and faulty inputs
 
 @pytest.mark.parametrize("kind", ["sliding", "global"])
