@@ -253,11 +253,49 @@ class DecodeMix:
             self.run_sliding(i)
         self.run_global()
 
+    # The same steps through g4attn_decode_exact (the prefill kernels on one-row chunks): rows with
+    # a prefill's bits. Timed apart from the step, as the opt-in strict mode's cost.
+    def run_sliding_exact(self, i):
+        self.g4.g4attn_decode_exact(self.sl, None, self.q_s, self.k_s, self.v_s, self.seq_len, self.s_caches[i].desc,
+                                    self.s_tables[i], self.o_s, self.ws_s)
+
+    def run_global_exact(self):
+        self.g4.g4attn_decode_exact(self.gl, None, self.q_g, self.k_g, None, self.seq_len, self.g_cache.desc,
+                                    self.g_table, self.o_g, self.ws_g)
+
     def host_io(self):
         return [self.q_s, self.k_s, self.v_s, self.q_g, self.k_g], [self.o_s, self.o_g]
 
 
 # ---------------------------------------------------------------- timing helpers
+
+def exact_decode_times(dec, flush, reps):
+    """ms per layer of the decode mix through g4attn_decode_exact (after two warm-up calls each),
+    CUDA events around each call, L2 flushed before each; outside the timed step."""
+    import torch
+
+    out = {}
+    for name, fn in (("sliding_layer_ms", lambda: dec.run_sliding_exact(0)), ("global_layer_ms", dec.run_global_exact)):
+        fn()
+        fn()
+        ts = []
+        for _ in range(reps):
+            flush()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        out[name] = statistics.median(ts)
+    st = dec.g4.g4attn_status_sync()
+    if st != dec.g4.G4_OK:
+        raise SystemExit(f"device error in the exact decode calls: {dec.g4.status_string(st)}")
+    out["mix_ms"] = dec.n_sliding * out["sliding_layer_ms"] + out["global_layer_ms"]
+    out["note"] = ("g4attn_decode_exact: rows bit-identical to a prefill's; 3 launches per call; "
+                   "not part of the timed step")
+    return out
+
 
 def traffic_record(kernel: str):
     """dram bytes per launch from the committed ncu summary, if it was taken on the current source."""
@@ -358,6 +396,8 @@ def main():
     ap.add_argument("--impl", default="g4attn", choices=["g4attn", "reference"])
     ap.add_argument("--parts", default="sliding,global,decode")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--exact-decode-reps", type=int, default=5,
+                    help="timed calls per layer kind of g4attn_decode_exact after the step (0: skip)")
     ap.add_argument("--decode-batch", type=int, default=64,
                     help="requests in the decode mix (64 is the measured workload; smaller only for profiling)")
     args = ap.parse_args()
@@ -514,6 +554,9 @@ def main():
                                "unit": "GB/s", "frac": ach / pk["hbm_gbs"], "traffic": traffic_record(kname),
                                "peak_kind": f"HBM copy, {pk['source']}",
                                "duration_from": "whole decode call (3 launches): a lower bound on the kernel"}))
+        if args.exact_decode_reps > 0:
+            decode["exact"] = exact_decode_times(dec, flush, args.exact_decode_reps)
+            decode["exact"]["vs_fast_mix"] = decode["exact"]["mix_ms"] / d_ms
     # dominant kernel: the one the step spends the most time in (per step: decode sliding x5)
     weight = {"decode_sliding_kernel": dec.n_sliding if dec else 0}
     roofs.sort(key=lambda r: -r[0] * weight.get(r[1]["kernel"], 1))

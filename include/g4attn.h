@@ -213,6 +213,23 @@ g4_status g4attn_prefill_vision(const g4attn_layer* layer, const g4attn_norms* n
                                 const int32_t* q_len, const int32_t* ctx_start, int32_t B, const int32_t* span,
                                 const g4attn_cache* cache, const int32_t* page_table, int32_t max_pages,
                                 void* out, void* stream);
+
+/* One decode step with the prefill's bits (RFC section 1: training and rollout give exactly equal
+ * selected-token log-probabilities in strict mode; section 5, hybrid_kv_cache_contract: the
+ * prefill / chunked-prefill / decode handoff). Same arguments and row conventions as
+ * g4attn_decode_normed (norms may be NULL), but the step runs as B one-row prefill chunks through
+ * the prefill kernels: request b's output row is bit for bit the row a prefill of its whole
+ * sequence computes at position seq_len[b] - 1 (for any batch and chunking of that prefill),
+ * which g4attn_decode's split-key kernels do not give. It costs more than g4attn_decode: a
+ * query tile of the tensor-core kernels holds one row.
+ *   workspace  device, 16-byte aligned, at least g4attn_decode_exact_workspace_bytes(B) bytes
+ *              (the rows of the B chunks; a g4attn_decode workspace is always large enough).
+ * A request with seq_len[b] < 1 computes nothing and sets G4_ERR_DEVICE. */
+g4_status g4attn_decode_exact(const g4attn_layer* layer, const g4attn_norms* norms, const void* q,
+                              const void* k_new, const void* v_new, const int32_t* seq_len, int32_t B,
+                              const g4attn_cache* cache, const int32_t* page_table, int32_t max_pages,
+                              void* out, void* workspace, size_t workspace_bytes, void* stream);
+size_t g4attn_decode_exact_workspace_bytes(int32_t B);
 g4_status g4attn_kv_append_normed(const g4attn_layer* layer, const g4attn_norms* norms, const void* k,
                                   const void* v, int32_t T, const int32_t* q_start, const int32_t* q_len,
                                   const int32_t* ctx_start, int32_t B, const g4attn_cache* cache,

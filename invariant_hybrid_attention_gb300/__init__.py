@@ -24,6 +24,7 @@ DECODE_STATIC_SCRATCH_BYTES = 32 << 20   # the static scratch of g4attn_decode_s
 
 EXPORTS = ("g4attn_rope_apply", "g4attn_prefill", "g4attn_prefill_stage", "g4attn_prefill_attend",
            "g4attn_prefill_normed", "g4attn_prefill_vision", "g4attn_kv_append_normed", "g4attn_decode_normed",
+           "g4attn_decode_exact", "g4attn_decode_exact_workspace_bytes",
            "g4attn_kv_append", "g4attn_decode_workspace_bytes",
            "g4attn_decode", "g4attn_decode_static", "g4attn_provenance", "g4attn_status_sync", "g4attn_status_string")
 
@@ -74,6 +75,8 @@ def load(path: Optional[str] = None):
         "g4attn_prefill_vision": (I32, [L, N, P, P, P, I32, P, P, P, I32, P, C, P, I32, P, P]),
         "g4attn_kv_append_normed": (I32, [L, N, P, P, I32, P, P, P, I32, C, P, I32, P]),
         "g4attn_decode_normed": (I32, [L, N, P, P, P, P, I32, C, P, I32, P, P, SZ, P]),
+        "g4attn_decode_exact": (I32, [L, N, P, P, P, P, I32, C, P, I32, P, P, SZ, P]),
+        "g4attn_decode_exact_workspace_bytes": (SZ, [I32]),
         "g4attn_kv_append": (I32, [L, P, P, I32, P, P, P, I32, C, P, I32, P]),
         "g4attn_decode_workspace_bytes": (SZ, [L, I32, I32]),
         "g4attn_decode": (I32, [L, P, P, P, P, I32, C, P, I32, P, P, SZ, P]),
@@ -254,4 +257,22 @@ def g4attn_decode_normed(layer, norms: g4attn_norms, q, k_new, v_new, seq_len, c
                                        int(page_table.shape[1]), _ptr(out), _ptr(workspace),
                                        int(workspace.numel() * workspace.element_size()), _stream(stream)),
            "g4attn_decode_normed")
+    return out
+
+
+def g4attn_decode_exact_workspace_bytes(B: int) -> int:
+    return int(load().g4attn_decode_exact_workspace_bytes(int(B)))
+
+
+def g4attn_decode_exact(layer, norms, q, k_new, v_new, seq_len, cache: g4attn_cache, page_table, out, workspace,
+                        stream=None):
+    """One decode step through the prefill kernels: the rows' bits equal a prefill's. norms may be
+    None; workspace holds at least g4attn_decode_exact_workspace_bytes(B) bytes."""
+    B = int(q.shape[0])
+    nrm = None if norms is None else ctypes.byref(norms)
+    _check(load().g4attn_decode_exact(ctypes.byref(layer), nrm, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(seq_len), B,
+                                      ctypes.byref(cache), _ptr(page_table), int(page_table.shape[1]), _ptr(out),
+                                      _ptr(workspace), int(workspace.numel() * workspace.element_size()),
+                                      _stream(stream)),
+           "g4attn_decode_exact")
     return out

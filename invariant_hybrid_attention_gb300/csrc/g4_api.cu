@@ -300,6 +300,35 @@ g4_status g4attn_decode(const g4attn_layer* layer, const void* q, const void* k_
                               workspace, workspace_bytes, stream);
 }
 
+size_t g4attn_decode_exact_workspace_bytes(int32_t B) {
+  return B <= 0 ? 0 : ((size_t)B * 3 * sizeof(int32_t) + 15) / 16 * 16;
+}
+
+g4_status g4attn_decode_exact(const g4attn_layer* layer, const g4attn_norms* norms, const void* q, const void* k_new,
+                              const void* v_new, const int32_t* seq_len, int32_t B, const g4attn_cache* cache,
+                              const int32_t* page_table, int32_t max_pages, void* out, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  bool global = false;
+  g4_status s = check_layer(layer, &global);
+  if (s != G4_OK) return s;
+  NormArgs nm;
+  if ((s = check_norms(norms, global, &nm)) != G4_OK) return s;
+  // Every check of the two prefill steps runs here, before the first launch.
+  if (B <= 0 || !q || !k_new || !seq_len || !out || !workspace) return G4_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(out) || !aligned16(workspace)) return G4_ERR_INVALID;
+  if (global ? v_new != nullptr : (!v_new || !aligned16(v_new))) return G4_ERR_INVALID;
+  if ((s = check_cache(cache, global, page_table, max_pages)) != G4_OK) return s;
+  if (workspace_bytes < g4attn_decode_exact_workspace_bytes(B)) return G4_ERR_INVALID;
+  DeviceState st;
+  if (device_state(&st) != cudaSuccess) return G4_ERR_CUDA;
+  int32_t* rows = static_cast<int32_t*>(workspace);
+  if (launch_decode_rows(seq_len, B, rows, st, (cudaStream_t)stream) != cudaSuccess) return G4_ERR_CUDA;
+  if ((s = prefill_stage(layer, norms, q, k_new, v_new, B, rows, rows + B, rows + 2 * B, B, cache, page_table,
+                         max_pages, out, stream)) != G4_OK)
+    return s;
+  return prefill_attend(layer, B, rows, rows + B, rows + 2 * B, B, nullptr, cache, page_table, max_pages, out, stream);
+}
+
 g4_status g4attn_decode_static(const g4attn_layer* layer, const void* q, const void* k_new, const void* v_new,
                                const int32_t* seq_len, int32_t B, const g4attn_cache* cache,
                                const int32_t* page_table, int32_t max_pages, void* out, void* stream) {

@@ -642,6 +642,24 @@ size_t decode_workspace_bytes(bool global, int B, int max_pages, int window) {
   return ml + (size_t)B * 32 * nc * D * sizeof(float);
 }
 
+// A decode step laid out as B one-row prefill chunks: request b's query is row b, at position
+// seq_len[b] - 1. A request with seq_len < 1 gets no row (and sets kErrPos).
+__global__ void decode_rows_kernel(const int32_t* seq_len, int B, int32_t* q_start, int32_t* q_len,
+                                   int32_t* ctx_start, uint32_t* err) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= B) return;
+  const int n = seq_len[b];
+  q_start[b] = b;
+  q_len[b] = n >= 1 ? 1 : 0;
+  ctx_start[b] = n >= 1 ? n - 1 : 0;
+  if (n < 1) set_error(err, kErrPos);
+}
+
+cudaError_t launch_decode_rows(const int32_t* seq_len, int B, int32_t* rows, const DeviceState& st, cudaStream_t s) {
+  decode_rows_kernel<<<(B + 127) / 128, 128, 0, s>>>(seq_len, B, rows, rows + B, rows + 2 * B, st.err);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_decode(bool global, const void* q, const int32_t* seq_len, int B, int window, float scale_log2,
                           const PagedCache& cache, void* out, void* ws, const DeviceState& st, cudaStream_t s) {
   if (B <= 0) return cudaSuccess;

@@ -73,6 +73,9 @@ cudaError_t launch_decode(bool global, const void* q, const int32_t* seq_len, in
                           float scale_log2, const PagedCache& cache, void* out, void* ws,
                           const DeviceState& st, cudaStream_t s);
 
+// Writes rows [3][B] (q_start, q_len, ctx_start) of a decode step taken as B one-row prefill chunks.
+cudaError_t launch_decode_rows(const int32_t* seq_len, int B, int32_t* rows, const DeviceState& st, cudaStream_t s);
+
 // Attention over roped queries staged in `out` (by launch_append_prefill); writes the output
 // rows over them.
 cudaError_t launch_prefill(bool global, const SeqRows& rows, int window, float scale_log2, const PagedCache& cache,

@@ -168,7 +168,9 @@ class DecodeBatch:
                                       mapped_from=first, spare_pages=5)
         self.first_page = first
 
-    def run(self, layer, cache: PagedKV = None, norms=None):
+    def run(self, layer, cache: PagedKV = None, norms=None, exact=False):
+        """g4attn_decode (or g4attn_decode_normed); exact: g4attn_decode_exact on the smallest
+        workspace it accepts."""
         B = len(self.ctx_lens)
         table = self.plan.table.cuda()
         if cache is None:
@@ -193,7 +195,11 @@ class DecodeBatch:
         out = torch.full_like(q, float("nan"))
         ws = torch.empty(g4.g4attn_decode_workspace_bytes(layer, B, self.plan.max_pages), dtype=torch.uint8,
                          device="cuda")
-        if norms is None:
+        if exact:
+            ws = torch.empty(g4.g4attn_decode_exact_workspace_bytes(B), dtype=torch.uint8, device="cuda")
+            g4.g4attn_decode_exact(layer, None if norms is None else norms.arg, q, k_new, v_new,
+                                   device_int32(self.ctx_lens), cache.desc, table, out, ws)
+        elif norms is None:
             g4.g4attn_decode(layer, q, k_new, v_new, device_int32(self.ctx_lens), cache.desc, table, out, ws)
         else:
             g4.g4attn_decode_normed(layer, norms.arg, q, k_new, v_new, device_int32(self.ctx_lens), cache.desc, table,

@@ -131,6 +131,20 @@ def test_misaligned_image_span_refused_on_host(lib):
         assert lib.g4attn_prefill_vision(ctypes.byref(layer), None, 16, 16, v, 8, 16, 16, 16, 1, 20,
                                          ctypes.byref(cache), 16, 1, 16, None) == g4.G4_ERR_INVALID
 
+def test_decode_exact_workspace_refused_on_host(lib):
+    """The exact decode's rows live in the caller's workspace: too small or misaligned is refused
+    before any launch (the other pointers are fake and never touched)."""
+    s = g4.sliding_layer()
+    cs = g4.g4attn_cache(16, 32, None, 4, 16)
+    need = lib.g4attn_decode_exact_workspace_bytes(5)
+    assert need >= 5 * 3 * 4 and need % 16 == 0
+    assert lib.g4attn_decode_exact_workspace_bytes(0) == 0
+    assert lib.g4attn_decode_exact(ctypes.byref(s), None, 16, 16, 16, 16, 5, ctypes.byref(cs), 16, 1, 16, 16,
+                                   need - 16, None) == g4.G4_ERR_INVALID
+    assert lib.g4attn_decode_exact(ctypes.byref(s), None, 16, 16, 16, 16, 5, ctypes.byref(cs), 16, 1, 16, 24,
+                                   need, None) == g4.G4_ERR_INVALID
+
+
 def test_workspace_sizes(lib):
     s, gl = g4.sliding_layer(), g4.global_layer()
     # sliding: a 1024-key window touches at most 5 chunks of 256 keys; partial = (m, l) + 256 floats

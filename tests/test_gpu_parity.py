@@ -330,6 +330,66 @@ def test_prefill_normed_batch_invariance(kind):
         assert torch.equal(out_a[:L].cpu(), out_b[s:s + L].cpu()), (kind, lens, padded, at)
 
 
+# ---------------------------------------------------------------- decode with the prefill's bits
+
+EXACT_LENS = {"sliding": [1, 17, 130, 700, 1500], "global": [1, 17, 130, 700, 2100]}
+
+
+def full_prefill_last_rows(db: DecodeBatch, layer, norms=None, seed=0):
+    """Each request's whole sequence prefilled in one batched call; returns the rows at each
+    sequence's last position (the decode query there, random queries before it)."""
+    lens = db.ctx_lens
+    lay = gi.packed_layout(lens)
+    qs = []
+    for b, L in enumerate(lens):
+        q = gi.bf16_normal((L, 32, db.d), seed * 7 + b, 0.5)
+        q[L - 1] = db.q[b]
+        qs.append(q)
+    q = gi.rows_of(qs, lay, fill_nan=False).cuda()
+    k = gi.rows_of(db.hist_k, lay, fill_nan=False).cuda()
+    v = None if db.kind == "global" else gi.rows_of(db.hist_v, lay, fill_nan=False).cuda()
+    cache = PagedKV(db.plan.num_pages, db.n_kv, db.d, shared=(db.kind == "global"))
+    rows = (device_int32(lay.q_start), device_int32(lay.q_len), device_int32(lay.ctx_start))
+    out = torch.full_like(q, float("nan"))
+    if norms is None:
+        g4.g4attn_prefill(layer, q, k, v, *rows, cache.desc, db.plan.table.cuda(), out)
+    else:
+        g4.g4attn_prefill_normed(layer, norms.arg, q, k, v, *rows, cache.desc, db.plan.table.cuda(), out)
+    torch.cuda.synchronize()
+    assert g4.g4attn_status_sync() == g4.G4_OK
+    return torch.stack([out[s + L - 1] for s, L in zip(lay.q_start, lens)]).cpu()
+
+
+@pytest.mark.parametrize("normed", [False, True], ids=["plain", "normed"])
+@pytest.mark.parametrize("kind", ["sliding", "global"])
+def test_decode_exact_has_the_prefill_bits(kind, normed):
+    """g4attn_decode_exact gives, bit for bit, the row a prefill of the whole sequence computes at
+    the decode position, and matches the oracle."""
+    layer, olayer = layers(kind, 1024)
+    norms = Norms(kind, 72) if normed else None
+    db = DecodeBatch(kind, EXACT_LENS[kind], seed=71, scale=0.5)
+    out, _ = db.run(layer, norms=norms, exact=True)
+    want_bits = full_prefill_last_rows(db, layer, norms, seed=71)
+    assert torch.equal(out.cpu(), want_bits)
+    for b in range(len(db.ctx_lens)):
+        assert_close(f64(out[b]), db.oracle_row(olayer, b, None if norms is None else norms), f"request {b}")
+
+
+def test_decode_exact_bad_seq_len_is_reported():
+    layer, _ = layers("sliding", 1024)
+    db = DecodeBatch("sliding", [40, 64], seed=73)
+    dcache = PagedKV(db.plan.num_pages, 16, 256, shared=False)
+    q = db.q.cuda()
+    kn = torch.stack([h[L - 1] for h, L in zip(db.hist_k, db.ctx_lens)]).cuda()
+    vn = torch.stack([h[L - 1] for h, L in zip(db.hist_v, db.ctx_lens)]).cuda()
+    ws = torch.empty(g4.g4attn_decode_exact_workspace_bytes(2), dtype=torch.uint8, device="cuda")
+    out = torch.zeros_like(q)
+    g4.g4attn_decode_exact(layer, None, q, kn, vn, device_int32([40, 0]), dcache.desc, db.plan.table.cuda(), out, ws)
+    assert g4.g4attn_status_sync() == g4.G4_ERR_DEVICE
+    assert g4.g4attn_status_sync() == g4.G4_OK
+    assert (out[1] == 0).all()   # the request without a position is left untouched
+
+
 # ---------------------------------------------------------------- vision-token mask
 
 VISION_CASES = {
