@@ -581,29 +581,32 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const float inv = (l_last > 0.f) ? __frcp_rn(l_last) : 0.f;
         __nv_bfloat16* orow = p.out + ((size_t)(q_row0 + r) * kGlobalHq + h) * kGD;
-#pragma unroll 1
-        for (int cc = 0; cc < kGD / 32; ++cc) {
-          uint32_t o[32];
-          tmem_ld32(tq + kTmO + 32 * cc, o);
-          tmem_ld_wait();
-          uint32_t w16[16];
+        tmem_ld_stream64<kGD / 64>(
+            tq + kTmO, [] {},
+            [&](int c, const uint32_t(&o)[64]) {
 #pragma unroll
-          for (int c = 0; c < 16; ++c)
-            w16[c] = pack_bf16(__uint_as_float(o[2 * c]) * inv, __uint_as_float(o[2 * c + 1]) * inv);
-          const int d0 = o_dim(32 * cc);   // 32 consecutive dims: half a box
-          if (staged) {
-            uint8_t* row = ep + (d0 >> 6) * kQChunk + r * 128;
-            const int q0 = (d0 & 63) >> 3;
+              for (int half = 0; half < 2; ++half) {
+                uint32_t w16[16];
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              *reinterpret_cast<uint4*>(row + (((q0 + i) ^ (r & 7)) * 16)) =
-                  make_uint4(w16[4 * i], w16[4 * i + 1], w16[4 * i + 2], w16[4 * i + 3]);
-          } else if (row_ok) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + d0);
+                for (int k = 0; k < 16; ++k)
+                  w16[k] = pack_bf16(__uint_as_float(o[32 * half + 2 * k]) * inv,
+                                     __uint_as_float(o[32 * half + 2 * k + 1]) * inv);
+                const int d0 = o_dim(64 * c + 32 * half);   // 32 consecutive dims: half a box
+                if (staged) {
+                  uint8_t* row = ep + (d0 >> 6) * kQChunk + r * 128;
+                  const int q0 = (d0 & 63) >> 3;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w16[4 * i], w16[4 * i + 1], w16[4 * i + 2], w16[4 * i + 3]);
-          }
-        }
+                  for (int i = 0; i < 4; ++i)
+                    *reinterpret_cast<uint4*>(row + (((q0 + i) ^ (r & 7)) * 16)) =
+                        make_uint4(w16[4 * i], w16[4 * i + 1], w16[4 * i + 2], w16[4 * i + 3]);
+                } else if (row_ok) {
+                  uint4* dst = reinterpret_cast<uint4*>(orow + d0);
+#pragma unroll
+                  for (int i = 0; i < 4; ++i)
+                    dst[i] = make_uint4(w16[4 * i], w16[4 * i + 1], w16[4 * i + 2], w16[4 * i + 3]);
+                }
+              }
+            });
       }
       if (staged) {   // one thread stores the eight boxes once every epilogue warp has staged its rows
         fence_proxy_async();
