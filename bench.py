@@ -8,8 +8,9 @@ One step runs the whole path once over seeded synthetic inputs already resident 
   3. one decode pass of the 5 sliding : 1 global mix: 64 requests, one query each, contexts
      uniform in [1024, 32768] (seed 7), pages scattered by random permutation.
 Each part is timed with CUDA events on the launching stream after an L2 flush (a 512 MB write); a
-prefill part runs its two launches through g4attn_prefill_stage and g4attn_prefill_attend (exactly
-g4attn_prefill) with an event between them, so the attention kernel is timed on its own.
+prefill part runs its stage and attention launches through g4attn_prefill_stage and
+g4attn_prefill_attend (exactly g4attn_prefill) with an event between them, so the attention kernel
+is timed on its own.
 
 Headline value: prefill TFLOP/s (credited FLOPs of parts 1+2 over their time); the decode part
 reports KV GB/s. Both also as fractions of the measured GB300 peaks.
@@ -155,7 +156,7 @@ class SlidingPrefill:
         self.qs, self.ql, self.cs = (device_int32(x) for x in (lay.q_start, lay.q_len, lay.ctx_start))
         self.out = torch.empty_like(self.q)
         self.flops = prefill_flops(256, 32, self.lens, W)
-        self.launches = 2
+        self.launches = 3   # stage: K'/V by key groups, roped q by rows; then attention
 
     def run(self):
         self.g4.g4attn_prefill(self.layer, self.q, self.k, self.v, self.qs, self.ql, self.cs, self.cache.desc,

@@ -445,7 +445,7 @@ __global__ void __launch_bounds__(256) append_prefill_kernel(const __nv_bfloat16
                                                              const __nv_bfloat16* __restrict__ v,
                                                              const __nv_bfloat16* __restrict__ q,
                                                              __nv_bfloat16* q_out, SeqRows rows, PagedCache cache,
-                                                             RopeTables tb, uint32_t* err, NormArgs nm) {
+                                                             RopeTables tb, uint32_t* err, NormArgs nm, bool rows_kv) {
   const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (r >= rows.T) return;
@@ -492,8 +492,124 @@ __global__ void __launch_bounds__(256) append_prefill_kernel(const __nv_bfloat16
       }
     }
   }
-  append_token_cs<D, R, HKV, SHARED, NORM>(k + (size_t)r * HKV * D, SHARED ? nullptr : v + (size_t)r * HKV * D, owner,
-                                           pos, cache, cs, err, nm, wk);
+  if (rows_kv)
+    append_token_cs<D, R, HKV, SHARED, NORM>(k + (size_t)r * HKV * D, SHARED ? nullptr : v + (size_t)r * HKV * D,
+                                             owner, pos, cache, cs, err, nm, wk);
+}
+
+// ---- the sliding K'/V append by key groups ---------------------------------------------------------
+// A page-head block stores 8 keys x 8 dims per 128-byte core matrix, so a warp that appends one key
+// writes 16 bytes into each of its 32-byte sectors, and the L2 completes the sector with data read
+// back from DRAM. This kernel gives each warp one group of 8 positions aligned to 8 (keys of one
+// core-matrix row group) and 4 KV heads: lane (key kk = lane & 7, piece p = lane >> 3) handles dims
+// 8(p + 4i) .. +7 and their pair partners 128 + 8(p + 4i) .. +7, i = 0..3, so one warp store writes
+// four whole core matrices. The arithmetic per element is that of the per-row append: the same
+// angles (rope_cs) and the same rotation (rope_pair), so the cache bits are the same.
+
+// Key group `gi` of the batch: the groups of sequence b are its positions' groups ctx_start / 8 ..
+// (ctx_start + q_len - 1) / 8, numbered in sequence order. Warp-wide; b = -1 past the last group.
+// A sequence with a negative ctx_start has no groups and sets kErrPos.
+__device__ __forceinline__ void find_group(const SeqRows& rows, int gi, int& out_b, int& out_grp, uint32_t* err) {
+  const int lane = threadIdx.x & 31;
+  int base = 0;
+  out_b = -1;
+  out_grp = 0;
+  for (int b0 = 0; b0 < rows.B; b0 += 32) {
+    const int b = b0 + lane;
+    int cnt = 0, first = 0;
+    if (b < rows.B) {
+      const int L = rows.q_len[b], cs = rows.ctx_start[b];
+      if (L > 0 && cs >= 0) {
+        first = cs >> 3;
+        cnt = ((cs + L - 1) >> 3) - first + 1;
+      } else if (L > 0 && gi == 0) {
+        set_error(err, kErrPos);
+      }
+    }
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += n;
+    }
+    const int excl = incl - cnt;
+    const unsigned m = __ballot_sync(0xffffffffu, cnt > 0 && gi >= base + excl && gi < base + incl);
+    if (m) {
+      const int src = __ffs(m) - 1;
+      out_b = b0 + src;
+      out_grp = __shfl_sync(0xffffffffu, first, src) + (gi - base - __shfl_sync(0xffffffffu, excl, src));
+      return;
+    }
+    base += __shfl_sync(0xffffffffu, incl, 31);
+  }
+}
+
+constexpr int kGroupHeads = 4;   // KV heads per warp of append_kv_groups_kernel
+
+template <int D, int R, int HKV>
+__global__ void __launch_bounds__(256) append_kv_groups_kernel(const __nv_bfloat16* __restrict__ k,
+                                                               const __nv_bfloat16* __restrict__ v, SeqRows rows,
+                                                               PagedCache c, RopeTables tb, uint32_t* err) {
+  static_assert(D == 256 && R == 128 && HKV % kGroupHeads == 0, "the group path serves the sliding geometry");
+  const int lane = threadIdx.x & 31;
+  const int unit = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int gi = unit / (HKV / kGroupHeads), g0 = (unit % (HKV / kGroupHeads)) * kGroupHeads;
+  int b, grp;
+  find_group(rows, gi, b, grp, err);
+  if (b < 0) return;
+  const int cs0 = rows.ctx_start[b], L = rows.q_len[b], qs = rows.q_start[b];
+  const int key0 = 8 * grp;   // the 8 keys share one page (groups are aligned within pages)
+  if (key0 >= kMaxPos || (key0 >> 4) >= c.max_pages) {
+    if (lane == 0) set_error(err, kErrPos);
+    return;
+  }
+  const int phys = c.page_table[(size_t)b * c.max_pages + (key0 >> 4)];
+  if (phys < 0 || phys >= c.num_pages) {
+    if (lane == 0) set_error(err, kErrPage);
+    return;
+  }
+  const int kk = lane & 7, p = lane >> 3;
+  const int pos = key0 + kk;
+  if (pos < cs0 || pos >= cs0 + L) return;   // outside the call's rows (the group's ragged ends)
+  const int j = pos & 15;
+  const size_t row = (size_t)(qs + (pos - cs0));
+#pragma unroll 1
+  for (int i = 0; i < 4; ++i) {
+    const int d0 = 8 * (p + 4 * i);
+    float2 cs[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) cs[e] = rope_cs(tb, d0 + e, pos);
+    uint4 lo[kGroupHeads], hi[kGroupHeads], vl[kGroupHeads], vh[kGroupHeads];
+#pragma unroll
+    for (int hh = 0; hh < kGroupHeads; ++hh) {
+      const size_t src = (row * HKV + g0 + hh) * D;
+      lo[hh] = *reinterpret_cast<const uint4*>(k + src + d0);
+      hi[hh] = *reinterpret_cast<const uint4*>(k + src + D / 2 + d0);
+      vl[hh] = *reinterpret_cast<const uint4*>(v + src + d0);
+      vh[hh] = *reinterpret_cast<const uint4*>(v + src + D / 2 + d0);
+    }
+#pragma unroll
+    for (int hh = 0; hh < kGroupHeads; ++hh) {
+      uint32_t* lw = reinterpret_cast<uint32_t*>(&lo[hh]);
+      uint32_t* hw = reinterpret_cast<uint32_t*>(&hi[hh]);
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        float a0 = bf16_lo(lw[w]), a1 = bf16_hi(lw[w]);
+        float b0 = bf16_lo(hw[w]), b1 = bf16_hi(hw[w]);
+        rope_pair(a0, b0, cs[2 * w]);
+        rope_pair(a1, b1, cs[2 * w + 1]);
+        lw[w] = pack_bf16(a0, a1);
+        hw[w] = pack_bf16(b0, b1);
+      }
+      const size_t blk = ((size_t)phys * HKV + g0 + hh) * kPage * D;
+      __nv_bfloat16* kd = (__nv_bfloat16*)c.k + blk;
+      __nv_bfloat16* vd = (__nv_bfloat16*)c.v + blk;
+      *reinterpret_cast<uint4*>(kd + tiled_offset(j, d0, D)) = lo[hh];
+      *reinterpret_cast<uint4*>(kd + tiled_offset(j, D / 2 + d0, D)) = hi[hh];
+      *reinterpret_cast<uint4*>(vd + tiled_offset_v256(j, d0)) = vl[hh];
+      *reinterpret_cast<uint4*>(vd + tiled_offset_v256(j, D / 2 + d0)) = vh[hh];
+    }
+  }
 }
 
 template <int D, int R, int HKV, bool SHARED, bool NORM>
@@ -537,17 +653,23 @@ cudaError_t launch_append_prefill(bool global, const void* k, const void* v, con
   if (global) {
     if (nm.any())
       append_prefill_kernel<kGlobalD, kGlobalR, kGlobalHkv, kGlobalHq, true, true>
-          <<<blocks, 256, 0, s>>>(kb, nullptr, qb, qo, rows, cache, st.global, st.err, nm);
+          <<<blocks, 256, 0, s>>>(kb, nullptr, qb, qo, rows, cache, st.global, st.err, nm, true);
     else
       append_prefill_kernel<kGlobalD, kGlobalR, kGlobalHkv, kGlobalHq, true, false>
-          <<<blocks, 256, 0, s>>>(kb, nullptr, qb, qo, rows, cache, st.global, st.err, nm);
+          <<<blocks, 256, 0, s>>>(kb, nullptr, qb, qo, rows, cache, st.global, st.err, nm, true);
+  } else if (nm.any()) {
+    append_prefill_kernel<kSlidingD, kSlidingR, kSlidingHkv, kSlidingHq, false, true>
+        <<<blocks, 256, 0, s>>>(kb, vb, qb, qo, rows, cache, st.sliding, st.err, nm, true);
   } else {
-    if (nm.any())
-      append_prefill_kernel<kSlidingD, kSlidingR, kSlidingHkv, kSlidingHq, false, true>
-          <<<blocks, 256, 0, s>>>(kb, vb, qb, qo, rows, cache, st.sliding, st.err, nm);
-    else
+    // K' and V by key groups (whole-sector writes), the queries by rows.
+    const long long groups = (long long)rows.T / 8 + 2LL * rows.B;   // a sequence adds at most two partial groups
+    const long long units = groups * (kSlidingHkv / kGroupHeads);
+    if (units > 0x3fffffffLL) return cudaErrorInvalidValue;
+    append_kv_groups_kernel<kSlidingD, kSlidingR, kSlidingHkv>
+        <<<(unsigned)((units + 7) / 8), 256, 0, s>>>(kb, vb, rows, cache, st.sliding, st.err);
+    if (qo != nullptr)
       append_prefill_kernel<kSlidingD, kSlidingR, kSlidingHkv, kSlidingHq, false, false>
-          <<<blocks, 256, 0, s>>>(kb, vb, qb, qo, rows, cache, st.sliding, st.err, nm);
+          <<<blocks, 256, 0, s>>>(kb, vb, qb, qo, rows, cache, st.sliding, st.err, nm, false);
   }
   return cudaGetLastError();
 }
