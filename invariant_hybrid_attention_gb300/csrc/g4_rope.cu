@@ -357,7 +357,8 @@ cudaError_t launch_rope_apply(bool global, const void* x, const int32_t* pos, in
 template <int D, int R, int HKV, bool SHARED, bool NORM>
 __device__ __forceinline__ void append_token_cs(const __nv_bfloat16* k_row, const __nv_bfloat16* v_row, int b, int pos,
                                                 const PagedCache& c, const float2 (&cs)[8], uint32_t* err,
-                                                const NormArgs& nm, const float (&wk)[16]) {
+                                                const NormArgs& nm, const float (&wk)[16], int g_begin = 0,
+                                                int g_end = HKV) {
   constexpr int VPW = 32 / (D / 16);   // vectors per warp instruction of rope_vec8_cs
   const int lane = threadIdx.x & 31;
   const int phys = c.page_table[(size_t)b * c.max_pages + (pos >> 4)];
@@ -371,7 +372,7 @@ __device__ __forceinline__ void append_token_cs(const __nv_bfloat16* k_row, cons
 #pragma unroll
     for (int i = 0; i < 16; ++i) ones[i] = 1.f;
 #pragma unroll 1
-    for (int g0 = 0; g0 < HKV; g0 += VPW) {
+    for (int g0 = g_begin; g0 < g_end; g0 += VPW) {
       const int g = g0 + lane / (D / 16);
       const size_t blk = ((size_t)phys * HKV + g) * kPage * D;
       const __nv_bfloat16* kg = k_row + (size_t)g * D;
@@ -400,7 +401,7 @@ __device__ __forceinline__ void append_token_cs(const __nv_bfloat16* k_row, cons
     return;
   }
 #pragma unroll 2
-  for (int g0 = 0; g0 < HKV; g0 += VPW) {
+  for (int g0 = g_begin; g0 < g_end; g0 += VPW) {
     const int g = g0 + lane / (D / 16);   // this lane's KV head for the rotation
     const size_t blk = ((size_t)phys * HKV + g) * kPage * D;   // page-head block
     if (SHARED) {
@@ -424,7 +425,7 @@ __device__ __forceinline__ void append_token_cs(const __nv_bfloat16* k_row, cons
 template <int D, int R, int HKV, bool SHARED, bool NORM>
 __device__ __forceinline__ void append_token(const __nv_bfloat16* k_row, const __nv_bfloat16* v_row, int b, int pos,
                                              const PagedCache& c, const RopeTables& tb, uint32_t* err,
-                                             const NormArgs& nm) {
+                                             const NormArgs& nm, int g_begin = 0, int g_end = HKV) {
   const int lane = threadIdx.x & 31;
   if (pos < 0 || pos >= kMaxPos || (pos >> 4) >= c.max_pages) {
     if (lane == 0) set_error(err, kErrPos);
@@ -434,7 +435,7 @@ __device__ __forceinline__ void append_token(const __nv_bfloat16* k_row, const _
   rope_cs_lane8<D, R>(tb, pos, cs);
   float wk[16];
   if (NORM) lane_weights<D>(nm.wk, wk);
-  append_token_cs<D, R, HKV, SHARED, NORM>(k_row, v_row, b, pos, c, cs, err, nm, wk);
+  append_token_cs<D, R, HKV, SHARED, NORM>(k_row, v_row, b, pos, c, cs, err, nm, wk, g_begin, g_end);
 }
 
 // One warp per row of the prefill batch; the owning sequence is found by a scan over B.
@@ -618,10 +619,15 @@ __global__ void __launch_bounds__(256) append_decode_kernel(const __nv_bfloat16*
                                                             const int32_t* __restrict__ seq_len, int B,
                                                             PagedCache cache, RopeTables tb, uint32_t* err,
                                                             NormArgs nm) {
-  const int b = blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (b >= B) return;
+  // One warp per (request, VPW KV heads): the heads of one request run in parallel, each with the
+  // lane mapping and arithmetic of the one-warp-per-token append (so the same bits).
+  constexpr int VPW = 32 / (D / 16);
+  constexpr int NC = HKV / VPW;
+  const int unit = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (unit >= B * NC) return;
+  const int b = unit / NC, g0 = (unit % NC) * VPW;
   append_token<D, R, HKV, SHARED, NORM>(k + (size_t)b * HKV * D, SHARED ? nullptr : v + (size_t)b * HKV * D, b,
-                                        seq_len[b] - 1, cache, tb, err, nm);
+                                        seq_len[b] - 1, cache, tb, err, nm, g0, g0 + VPW);
 }
 
 // The decode queries' norm (and, on a K==V layer with a key norm, the fold of w_k into their
@@ -678,7 +684,9 @@ cudaError_t launch_append_decode(bool global, const void* k_new, const void* v_n
                                  int B, const PagedCache& cache, const DeviceState& st, cudaStream_t s,
                                  const NormArgs& nm) {
   if (B <= 0) return cudaSuccess;
-  const unsigned blocks = (unsigned)((B + 7) / 8);
+  // warps: B x (KV heads / heads per warp instruction): 8 per request on sliding, 4 on global layers
+  const int per_req = global ? kGlobalHkv / (32 / (kGlobalD / 16)) : kSlidingHkv / (32 / (kSlidingD / 16));
+  const unsigned blocks = (unsigned)(((long long)B * per_req + 7) / 8);
   const __nv_bfloat16 *kb = (const __nv_bfloat16*)k_new, *vb = (const __nv_bfloat16*)v_new;
   if (global) {
     if (nm.any())
