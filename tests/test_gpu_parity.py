@@ -482,6 +482,57 @@ def test_prefill_vision_bad_spans_are_reported(kind):
     assert g4.g4attn_status_sync() == g4.G4_OK
 
 
+# ---------------------------------------------------------------- the end of the position range
+
+def test_sliding_prefill_and_decode_at_the_last_positions():
+    """A 300-row chunk whose last row sits at position 262143, the last one a sequence may use, then a
+    decode step that lands on it again from a one-row-shorter history: the RoPE angles are at their
+    largest there. Only the window's pages are mapped (the rest of the 16384-entry table is -1),
+    and the oracle is given just the window's keys, at their absolute positions."""
+    layer, olayer = layers("sliding", 1024)
+    n_max = oracle.MAX_POSITIONS
+    L = 300
+    c = n_max - L                                  # the chunk's first position
+    p0 = ((c - 1024) // 16) * 16                   # first kept key: the window of the chunk's first row
+    hist_len = n_max - p0
+    k_hist = gi.bf16_normal((hist_len, 16, 256), 71, 0.5)
+    v_hist = gi.bf16_normal((hist_len, 16, 256), 72, 0.5)
+    q = gi.bf16_normal((L, 32, 256), 73, 0.5)
+    plan = gi.make_page_plan([n_max], seed=74, mapped_from=[p0 // 16], spare_pages=2)
+    table = plan.table.cuda()
+    cache = PagedKV(plan.num_pages, 16, 256, shared=False)
+    # history p0 .. c-1 through kv_append, then the chunk through prefill
+    pre = c - p0
+    g4.g4attn_kv_append(layer, k_hist[:pre].cuda(), v_hist[:pre].cuda(), device_int32([0]), device_int32([pre]),
+                        device_int32([p0]), cache.desc, table)
+    out = torch.full((L, 32, 256), float("nan"), dtype=torch.bfloat16, device="cuda")
+    g4.g4attn_prefill(layer, q.cuda(), k_hist[pre:].cuda(), v_hist[pre:].cuda(), device_int32([0]),
+                      device_int32([L]), device_int32([c]), cache.desc, table, out)
+    torch.cuda.synchronize()
+    assert g4.g4attn_status_sync() == g4.G4_OK
+    rows = np.array([0, 1, 150, L - 2, L - 1])
+    want = oracle.layer_rows(olayer, q[rows].double().numpy(), c - p0 + rows, k_hist.double().numpy(),
+                             v_hist.double().numpy(), pos_offset=p0)
+    assert_close(f64(out)[rows], want, "prefill rows at the end of the position range")
+    # a decode step at position n_max - 1 over the same history (its own key rewritten identically)
+    qd = gi.bf16_normal((1, 32, 256), 75, 0.5)
+    ws = torch.empty(g4.g4attn_decode_workspace_bytes(layer, 1, plan.table.shape[1]), dtype=torch.uint8,
+                     device="cuda")
+    dout = torch.empty_like(qd).cuda()
+    g4.g4attn_decode(layer, qd.cuda(), k_hist[-1:].cuda(), v_hist[-1:].cuda(), device_int32([n_max]), cache.desc,
+                     table, dout, ws)
+    torch.cuda.synchronize()
+    assert g4.g4attn_status_sync() == g4.G4_OK
+    want_d = oracle.layer_rows(olayer, qd.double().numpy(), [hist_len - 1], k_hist.double().numpy(),
+                               v_hist.double().numpy(), pos_offset=p0)
+    assert_close(f64(dout), want_d, "decode at the last position")
+    # one position further is refused on the device (the status says so; the context stays usable)
+    g4.g4attn_decode(layer, qd.cuda(), k_hist[-1:].cuda(), v_hist[-1:].cuda(), device_int32([n_max + 1]),
+                     cache.desc, table, dout, ws)
+    assert g4.g4attn_status_sync() == g4.G4_ERR_DEVICE
+    assert g4.g4attn_status_sync() == g4.G4_OK
+
+
 # ---------------------------------------------------------------- degenerate and faulty inputs
 
 @pytest.mark.parametrize("kind", ["sliding", "global"])
