@@ -258,6 +258,35 @@ def test_chunked_prefill_is_bit_identical_to_one_prefill(kind):
 
 
 
+def test_context_parallel_sliding_shards_with_window_halo_are_bit_identical():
+    """Context parallelism of a sliding layer, simulated on one GPU: a 4096-token sequence split into
+    four uneven shards (cuts mid-tile) as four ranks would hold it. Each shard's cache holds only
+    its own keys and the pages of the W - 1 keys before them (the halo a rank would receive from the
+    rank on its left); every other page-table entry is -1. Each shard is one prefill call at its
+    absolute positions, and its rows are bit-identical to one prefill of the whole sequence."""
+    layer, _ = layers("sliding", 1024)
+    W, L = 1024, 4096
+    full = Batch("sliding", [L], seed=81, scale=0.5)
+    out_full, _ = full.run(layer)
+    ref = out_full[:L].cpu().view(torch.int16)
+    kh, vh = full.hist_k[0], full.hist_v[0]
+    for a, b in [(0, 1000), (1000, 2100), (2100, 3333), (3333, 4096)]:
+        p0 = max(0, a - (W - 1)) // 16                  # first page of the halo
+        plan = gi.make_page_plan([b], seed=90 + a, mapped_from=[p0], spare_pages=1)
+        table = plan.table.cuda()
+        cache = PagedKV(plan.num_pages, 16, 256, shared=False)
+        h = a - 16 * p0                                 # halo keys, from the page boundary
+        if h > 0:
+            g4.g4attn_kv_append(layer, kh[16 * p0:a].cuda(), vh[16 * p0:a].cuda(), device_int32([0]),
+                                device_int32([h]), device_int32([16 * p0]), cache.desc, table)
+        out = torch.full((b - a, 32, 256), float("nan"), dtype=torch.bfloat16, device="cuda")
+        g4.g4attn_prefill(layer, full.q[a:b].cuda(), kh[a:b].cuda(), vh[a:b].cuda(), device_int32([0]),
+                          device_int32([b - a]), device_int32([a]), cache.desc, table, out)
+        torch.cuda.synchronize()
+        assert g4.g4attn_status_sync() == g4.G4_OK
+        assert torch.equal(out.cpu().view(torch.int16), ref[a:b]), (a, b)
+
+
 # ---------------------------------------------------------------- per-head norms before RoPE
 
 NORM_CASES = [("sliding", dict()), ("sliding", dict(k=False, v=False)), ("sliding", dict(q=False)),
