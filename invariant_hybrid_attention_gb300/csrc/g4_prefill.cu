@@ -60,6 +60,9 @@ constexpr int kSD = kSlidingD;                    // 256
 constexpr int kSN = 128;                          // keys per tile
 constexpr int kNK = 3, kNV = 3;                   // K and V ring stages
 constexpr int kQAfter = 2;                        // a unit's Q takes the K ring slot after its first two tiles
+// QK^T of a unit's first tile needs its Q, so the Q slot must come while that tile's slot is still
+// held: a Q slot behind kNK or more key tiles would wait on a ring that only QK^T can free.
+static_assert(kQAfter < kNK, "the Q slot must fit in the ring beside the tiles issued before it");
 constexpr int kPageBytes = kPage * kSD * 2;       // one tiled page-head block: 8 KB
 constexpr int kKeyGroupBytes = 8 * kSD * 2;       // K: 8 keys x 256 dims, 4 KB
 constexpr int kVGroupBytes = 8 * (kSD / 2) * 2;   // V half: 8 keys x 128 dims, 2 KB
