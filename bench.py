@@ -17,7 +17,7 @@ reports KV GB/s. Both also as fractions of the measured GB300 peaks.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl g4attn|reference]
 
---impl reference times the fp64 CPU oracle (the only reference this build has) on a bounded
+--impl reference times the fp64 CPU oracle (the method is published without installable code) on a bounded
 sample of the same workload, on the host cores. With N > 1 (torchrun) every rank runs an
 independent replica (the path has no exchange step); rank 0 prints one JSON line.
 """
