@@ -147,7 +147,7 @@ __device__ __noinline__ bool sliding_unit(const PrefillParams& p, int u, uint32_
   o.g = u % kSlidingHkv;
   o.h = 2 * o.g + (int)rank;
   int b, t, f[3];
-  find_unit(p.rows, u / kSlidingHkv, b, t, f);
+  find_unit(p.rows, u / kSlidingHkv, b, t, p.err, f);
   if (b < 0) return false;
   const int cs = f[0], L = f[1], qs = f[2];
   o.t = t;

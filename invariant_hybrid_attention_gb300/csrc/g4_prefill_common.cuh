@@ -35,8 +35,11 @@ struct PrefillParams {
 // read through the read-only path: a CTA reads them again for every unit it computes, and they
 // then come from L1 instead of costing an L2 round trip each time.
 // With `fields` set, the sequence's ctx_start, q_len and q_start come back in fields[0..2], read
-// in the same round trip as the search.
-inline __device__ void find_unit(const SeqRows& rows, int slot, int& out_b, int& out_t, int* fields = nullptr) {
+// in the same round trip as the search. A sequence whose rows do not lie inside the T rows of q and
+// out (q_start < 0 or q_start + q_len > T) has no tiles: its rows are never read or written, and
+// kErrPos is set.
+inline __device__ void find_unit(const SeqRows& rows, int slot, int& out_b, int& out_t, uint32_t* err,
+                                 int* fields = nullptr) {
   const int lane = threadIdx.x & 31;
   int base = 0;
   out_b = -1;
@@ -47,10 +50,12 @@ inline __device__ void find_unit(const SeqRows& rows, int slot, int& out_b, int&
     if (b < rows.B) {
       L = __ldg(rows.q_len + b);
       cs = __ldg(rows.ctx_start + b);
-      if (fields) qs = __ldg(rows.q_start + b);
-      if (L > 0 && cs >= 0) {
+      qs = __ldg(rows.q_start + b);
+      if (L > 0 && cs >= 0 && qs >= 0 && L <= rows.T - qs) {
         tl = (cs + L - 1) / kBM;
         cnt = tl - cs / kBM + 1;
+      } else if (L > 0 && cs >= 0) {
+        set_error(err, kErrPos);
       }
     }
     int incl = cnt;

@@ -149,7 +149,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     int ub, ut;
-    find_unit(p.rows, slot, ub, ut);
+    find_unit(p.rows, slot, ub, ut, p.err);
     if (lane == 0) {
       bar.unit_b = ub;
       bar.unit_t = ut;

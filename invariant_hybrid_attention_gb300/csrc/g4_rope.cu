@@ -509,7 +509,8 @@ __global__ void __launch_bounds__(256) append_prefill_kernel(const __nv_bfloat16
 
 // Key group `gi` of the batch: the groups of sequence b are its positions' groups ctx_start / 8 ..
 // (ctx_start + q_len - 1) / 8, numbered in sequence order. Warp-wide; b = -1 past the last group.
-// A sequence with a negative ctx_start has no groups and sets kErrPos.
+// A sequence with a negative ctx_start, or whose rows do not lie inside the T rows of k and v
+// (q_start < 0 or q_start + q_len > T), has no groups and sets kErrPos.
 __device__ __forceinline__ void find_group(const SeqRows& rows, int gi, int& out_b, int& out_grp, uint32_t* err) {
   const int lane = threadIdx.x & 31;
   int base = 0;
@@ -519,8 +520,8 @@ __device__ __forceinline__ void find_group(const SeqRows& rows, int gi, int& out
     const int b = b0 + lane;
     int cnt = 0, first = 0;
     if (b < rows.B) {
-      const int L = rows.q_len[b], cs = rows.ctx_start[b];
-      if (L > 0 && cs >= 0) {
+      const int L = rows.q_len[b], cs = rows.ctx_start[b], qs = rows.q_start[b];
+      if (L > 0 && cs >= 0 && qs >= 0 && L <= rows.T - qs) {
         first = cs >> 3;
         cnt = ((cs + L - 1) >> 3) - first + 1;
       } else if (L > 0 && gi == 0) {

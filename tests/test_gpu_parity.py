@@ -571,6 +571,30 @@ def test_zero_length_sequences_in_a_batch(kind):
     check_prefill(bt, kind, 0 if kind == "global" else 1024)
 
 
+@pytest.mark.parametrize("kind", ["sliding", "global"])
+def test_rows_past_the_end_of_q_are_refused(kind):
+    """A sequence whose q_start + q_len reaches past the T rows of the call is refused on the
+    device (the status word says so) and none of its rows is read or written: q, k, v and out carry
+    40 guard rows past T here, and the guard rows of out stay NaN. The other sequence is exact."""
+    layer, olayer = layers(kind, 1024)
+    bt = Batch(kind, [100, 200], seed=91, scale=0.5)   # T = 300
+    T, guard = 300, 40
+    plan = gi.make_page_plan([100, 240], seed=92)
+    cache = PagedKV(plan.num_pages, bt.n_kv, bt.d, shared=(kind == "global"))
+    pad = lambda x: torch.cat([x, torch.zeros((guard,) + tuple(x.shape[1:]), dtype=x.dtype)]).cuda()
+    q, k = pad(bt.q), pad(bt.k_rows)
+    v = None if bt.v_rows is None else pad(bt.v_rows)
+    out = torch.full((T + guard, 32, bt.d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    rows = (device_int32([0, 100]), device_int32([100, 230]), device_int32([0, 0]))   # 100 + 230 > T
+    g4.g4attn_prefill(layer, q[:T], k[:T], None if v is None else v[:T], *rows, cache.desc, plan.table.cuda(),
+                      out[:T])
+    torch.cuda.synchronize()
+    assert g4.g4attn_status_sync() == g4.G4_ERR_DEVICE
+    assert g4.g4attn_status_sync() == g4.G4_OK
+    assert torch.isnan(out[T:].float()).all()
+    assert_close(f64(out[:100]), bt.oracle_rows(olayer, 0), "the valid sequence")
+
+
 def test_device_detected_errors_are_reported_and_cleared(lib):
     """A page-table entry outside the pool and a decode position beyond the page table are seen on
     the device: the work they touch is skipped, the status word says so, and the next call starts
