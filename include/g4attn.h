@@ -152,7 +152,9 @@ g4_status g4attn_rope_apply(const g4attn_layer* layer, const void* x, const int3
  * in the cache. The call first writes the new rows' K'/V (sliding) or S (global) into the
  * cache through page_table, then computes out for those rows. Rows of out that belong to no
  * sequence are not written. q_start, q_len, ctx_start: int32 [B], device, read on the device
- * (q_len 0 is allowed); sequences' row ranges must not overlap. T: rows in q/k/v/out.
+ * (q_len 0 is allowed); sequences' row ranges must not overlap and must lie inside [0, T) (a
+ * range that does not is refused on the device: none of its rows is read or written, and
+ * G4_ERR_DEVICE is reported). T: rows in q/k/v/out.
  * v: NULL on global layers (K==V). Launch geometry depends on T, B and the layer only. */
 g4_status g4attn_prefill(const g4attn_layer* layer, const void* q, const void* k, const void* v,
                          int32_t T, const int32_t* q_start, const int32_t* q_len,
