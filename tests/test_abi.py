@@ -145,6 +145,40 @@ def test_decode_exact_workspace_refused_on_host(lib):
                                    need, None) == g4.G4_ERR_INVALID
 
 
+def test_split_steps_append_and_new_calls_refused_on_host(lib):
+    """The split prefill steps, the plain append, the exact decode and the vision prefill refuse
+    bad arguments before any launch (the other pointers are fake and never touched)."""
+    s, gl = g4.sliding_layer(), g4.global_layer()
+    bad = g4.sliding_layer()
+    bad.n_q_heads = 16
+    cs = g4.g4attn_cache(16, 32, None, 4, 16)
+    cg = g4.g4attn_cache(16, None, 48, 4, 16)
+    L = ctypes.byref
+    # g4attn_prefill_stage: misaligned out; unsupported geometry
+    assert lib.g4attn_prefill_stage(L(s), 16, 16, 16, 8, 16, 16, 16, 1, L(cs), 16, 1, 24, None) == g4.G4_ERR_INVALID
+    assert lib.g4attn_prefill_stage(L(bad), 16, 16, 16, 8, 16, 16, 16, 1, L(cs), 16, 1, 16, None) == \
+        g4.G4_ERR_UNSUPPORTED
+    # g4attn_prefill_attend: NULL q_start; B = 0; unsupported geometry
+    assert lib.g4attn_prefill_attend(L(s), 8, None, 16, 16, 1, L(cs), 16, 1, 16, None) == g4.G4_ERR_INVALID
+    assert lib.g4attn_prefill_attend(L(s), 8, 16, 16, 16, 0, L(cs), 16, 1, 16, None) == g4.G4_ERR_INVALID
+    assert lib.g4attn_prefill_attend(L(bad), 8, 16, 16, 16, 1, L(cs), 16, 1, 16, None) == g4.G4_ERR_UNSUPPORTED
+    # g4attn_kv_append: a V tensor on a K==V layer; no V on a sliding layer; negative T
+    assert lib.g4attn_kv_append(L(gl), 16, 16, 8, 16, 16, 16, 1, L(cg), 16, 1, None) == g4.G4_ERR_INVALID
+    assert lib.g4attn_kv_append(L(s), 16, None, 8, 16, 16, 16, 1, L(cs), 16, 1, None) == g4.G4_ERR_INVALID
+    assert lib.g4attn_kv_append(L(s), 16, 16, -1, 16, 16, 16, 1, L(cs), 16, 1, None) == g4.G4_ERR_INVALID
+    # g4attn_decode_exact: unsupported geometry; B = 0; NULL seq_len
+    need = lib.g4attn_decode_exact_workspace_bytes(4)
+    assert lib.g4attn_decode_exact(L(bad), None, 16, 16, 16, 16, 4, L(cs), 16, 1, 16, 16, need, None) == \
+        g4.G4_ERR_UNSUPPORTED
+    assert lib.g4attn_decode_exact(L(s), None, 16, 16, 16, 16, 0, L(cs), 16, 1, 16, 16, need, None) == \
+        g4.G4_ERR_INVALID
+    assert lib.g4attn_decode_exact(L(s), None, 16, 16, 16, None, 4, L(cs), 16, 1, 16, 16, need, None) == \
+        g4.G4_ERR_INVALID
+    # g4attn_prefill_vision: unsupported geometry (the span itself aligned)
+    assert lib.g4attn_prefill_vision(L(bad), None, 16, 16, 16, 8, 16, 16, 16, 1, 16, L(cs), 16, 1, 16, None) == \
+        g4.G4_ERR_UNSUPPORTED
+
+
 def test_workspace_sizes(lib):
     s, gl = g4.sliding_layer(), g4.global_layer()
     # sliding: a 1024-key window touches at most 5 chunks of 256 keys; partial = (m, l) + 256 floats
