@@ -36,8 +36,9 @@ struct PrefillParams {
 // then come from L1 instead of costing an L2 round trip each time.
 // With `fields` set, the sequence's ctx_start, q_len and q_start come back in fields[0..2], read
 // in the same round trip as the search. A sequence whose rows do not lie inside the T rows of q and
-// out (q_start < 0 or q_start + q_len > T) has no tiles: its rows are never read or written, and
-// kErrPos is set.
+// out (q_start < 0 or q_start + q_len > T), or whose positions reach past the last usable one
+// (ctx_start + q_len > 262144, tested without forming the sum, which could overflow), has no tiles:
+// its rows are never read or written, and kErrPos is set.
 inline __device__ void find_unit(const SeqRows& rows, int slot, int& out_b, int& out_t, uint32_t* err,
                                  int* fields = nullptr) {
   const int lane = threadIdx.x & 31;
@@ -51,7 +52,7 @@ inline __device__ void find_unit(const SeqRows& rows, int slot, int& out_b, int&
       L = __ldg(rows.q_len + b);
       cs = __ldg(rows.ctx_start + b);
       qs = __ldg(rows.q_start + b);
-      if (L > 0 && cs >= 0 && qs >= 0 && L <= rows.T - qs) {
+      if (L > 0 && cs >= 0 && qs >= 0 && L <= rows.T - qs && L <= kMaxPos && cs <= kMaxPos - L) {
         tl = (cs + L - 1) / kBM;
         cnt = tl - cs / kBM + 1;
       } else if (L > 0 && cs >= 0) {

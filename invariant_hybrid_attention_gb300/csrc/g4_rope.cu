@@ -465,11 +465,12 @@ __global__ void __launch_bounds__(256) append_prefill_kernel(const __nv_bfloat16
     }
   }
   if (owner < 0) return;
-  const int pos = rows.ctx_start[owner] + (r - rows.q_start[owner]);
-  if (pos < 0 || pos >= kMaxPos || (pos >> 4) >= cache.max_pages) {
+  const long long pos64 = (long long)rows.ctx_start[owner] + (r - rows.q_start[owner]);   // no int overflow
+  if (pos64 < 0 || pos64 >= kMaxPos || (int)(pos64 >> 4) >= cache.max_pages) {
     if (lane == 0) set_error(err, kErrPos);
     return;
   }
+  const int pos = (int)pos64;
   float2 cs[8];   // the row's angles, shared by its query heads and its key heads
   rope_cs_lane8<D, R>(tb, pos, cs);
   float wk[16];
@@ -509,8 +510,9 @@ __global__ void __launch_bounds__(256) append_prefill_kernel(const __nv_bfloat16
 
 // Key group `gi` of the batch: the groups of sequence b are its positions' groups ctx_start / 8 ..
 // (ctx_start + q_len - 1) / 8, numbered in sequence order. Warp-wide; b = -1 past the last group.
-// A sequence with a negative ctx_start, or whose rows do not lie inside the T rows of k and v
-// (q_start < 0 or q_start + q_len > T), has no groups and sets kErrPos.
+// A sequence with a negative ctx_start, whose rows do not lie inside the T rows of k and v
+// (q_start < 0 or q_start + q_len > T), or whose positions reach past the last usable one
+// (ctx_start + q_len > 262144, tested without forming the sum), has no groups and sets kErrPos.
 __device__ __forceinline__ void find_group(const SeqRows& rows, int gi, int& out_b, int& out_grp, uint32_t* err) {
   const int lane = threadIdx.x & 31;
   int base = 0;
@@ -521,7 +523,7 @@ __device__ __forceinline__ void find_group(const SeqRows& rows, int gi, int& out
     int cnt = 0, first = 0;
     if (b < rows.B) {
       const int L = rows.q_len[b], cs = rows.ctx_start[b], qs = rows.q_start[b];
-      if (L > 0 && cs >= 0 && qs >= 0 && L <= rows.T - qs) {
+      if (L > 0 && cs >= 0 && qs >= 0 && L <= rows.T - qs && L <= kMaxPos && cs <= kMaxPos - L) {
         first = cs >> 3;
         cnt = ((cs + L - 1) >> 3) - first + 1;
       } else if (L > 0 && gi == 0) {

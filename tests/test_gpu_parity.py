@@ -595,6 +595,25 @@ def test_rows_past_the_end_of_q_are_refused(kind):
     assert_close(f64(out[:100]), bt.oracle_rows(olayer, 0), "the valid sequence")
 
 
+@pytest.mark.parametrize("kind", ["sliding", "global"])
+def test_positions_past_the_limit_are_refused_without_overflow(kind):
+    """A chunk whose ctx_start lies so close to 2^31 that ctx_start + q_len overflows int32 is
+    refused on the device as a whole (none of its rows is read or written, the status says so),
+    and the other sequence of the batch is exact."""
+    layer, olayer = layers(kind, 1024)
+    bt = Batch(kind, [100, 200], seed=93, scale=0.5)
+    cache = bt.device_cache()
+    out = torch.full_like(bt.q, float("nan")).cuda()
+    rows = (device_int32(bt.layout.q_start), device_int32(bt.layout.q_len), device_int32([0, 2**31 - 150]))
+    g4.g4attn_prefill(layer, bt.q.cuda(), bt.k_rows.cuda(), None if bt.v_rows is None else bt.v_rows.cuda(), *rows,
+                      cache.desc, bt.plan.table.cuda(), out)
+    torch.cuda.synchronize()
+    assert g4.g4attn_status_sync() == g4.G4_ERR_DEVICE
+    assert g4.g4attn_status_sync() == g4.G4_OK
+    assert torch.isnan(out[100:].float()).all()
+    assert_close(f64(out[:100]), bt.oracle_rows(olayer, 0), "the valid sequence")
+
+
 def test_device_detected_errors_are_reported_and_cleared(lib):
     """A page-table entry outside the pool and a decode position beyond the page table are seen on
     the device: the work they touch is skipped, the status word says so, and the next call starts
