@@ -25,7 +25,9 @@
  *   v_j = the stored V (sliding) or the stored un-rotated S (global, K==V).
  *   Declared bf16 (round-to-nearest-even) casts: roped q, roped sliding K written to the
  *   cache, roped global K columns, the softmax probabilities P before P.V, and the output.
- *   Everything else accumulates in fp32.
+ *   Everything else accumulates in fp32. The softmax exponentials are the multi-function
+ *   unit's 2^x (PTX ex2.approx.ftz.f32, deterministic; weights below 2^-126 flush to zero), a
+ *   declared choice that g4attn_provenance records.
  *
  * Memory. Every tensor is a device buffer owned by the caller. The library allocates no
  * device memory: its only device-side state is static (the RoPE cos/sin tables, filled once
@@ -61,8 +63,8 @@
  * size or alignment) or G4_ERR_UNSUPPORTED (a geometry other than the two layer kinds
  * below); nothing is launched then. Problems only the device can see (a page-table entry
  * outside [0, num_pages), a position >= 262144 or beyond the page table, a bad image span
- * (g4attn_prefill_vision), a bounded wait that ran out) set bits in a device error word and the affected work is skipped; read and
- * clear the word with g4attn_status_sync. Kernels never trap.
+ * (g4attn_prefill_vision), a bounded wait that ran out) set bits in a device error word, and the
+ * affected work is skipped; read and clear the word with g4attn_status_sync. Kernels never trap.
  */
 #ifndef G4ATTN_H
 #define G4ATTN_H
@@ -183,7 +185,8 @@ g4_status g4attn_prefill_attend(const g4attn_layer* layer, int32_t T, const int3
                                 void* out, void* stream);
 
 /* g4attn_prefill, g4attn_kv_append and g4attn_decode with the per-head norms of g4attn_norms
- * applied to the raw q, k and v they are given (norms NULL: exactly the plain calls). A
+ * (RFC section 5, qk_rmsnorm_d256_d512, fused into the staging of each call) applied to the raw
+ * q, k and v they are given (norms NULL: exactly the plain calls). A
  * sequence's history must have been appended with the same norms. Errors as the plain calls,
  * plus G4_ERR_INVALID for a bad eps, v_norm or weight alignment, and G4_ERR_UNSUPPORTED for a
  * K==V layer whose key norm and value norm do not come together. */
@@ -192,6 +195,14 @@ g4_status g4attn_prefill_normed(const g4attn_layer* layer, const g4attn_norms* n
                                 const int32_t* q_len, const int32_t* ctx_start, int32_t B,
                                 const g4attn_cache* cache, const int32_t* page_table, int32_t max_pages,
                                 void* out, void* stream);
+g4_status g4attn_kv_append_normed(const g4attn_layer* layer, const g4attn_norms* norms, const void* k,
+                                  const void* v, int32_t T, const int32_t* q_start, const int32_t* q_len,
+                                  const int32_t* ctx_start, int32_t B, const g4attn_cache* cache,
+                                  const int32_t* page_table, int32_t max_pages, void* stream);
+g4_status g4attn_decode_normed(const g4attn_layer* layer, const g4attn_norms* norms, const void* q,
+                               const void* k_new, const void* v_new, const int32_t* seq_len, int32_t B,
+                               const g4attn_cache* cache, const int32_t* page_table, int32_t max_pages,
+                               void* out, void* workspace, size_t workspace_bytes, void* stream);
 
 /* g4attn_prefill_normed with the vision-token mask: the tokens of one image see each other in
  * both directions, on top of the layer's own mask (model card "Gemma 4 31B":
@@ -231,15 +242,9 @@ g4_status g4attn_decode_exact(const g4attn_layer* layer, const g4attn_norms* nor
                               const void* k_new, const void* v_new, const int32_t* seq_len, int32_t B,
                               const g4attn_cache* cache, const int32_t* page_table, int32_t max_pages,
                               void* out, void* workspace, size_t workspace_bytes, void* stream);
+/* Bytes of workspace g4attn_decode_exact needs for B requests (RFC section 5,
+ * hybrid_kv_cache_contract: the rows of the B one-row chunks, int32 [3][B]); 0 when B <= 0. */
 size_t g4attn_decode_exact_workspace_bytes(int32_t B);
-g4_status g4attn_kv_append_normed(const g4attn_layer* layer, const g4attn_norms* norms, const void* k,
-                                  const void* v, int32_t T, const int32_t* q_start, const int32_t* q_len,
-                                  const int32_t* ctx_start, int32_t B, const g4attn_cache* cache,
-                                  const int32_t* page_table, int32_t max_pages, void* stream);
-g4_status g4attn_decode_normed(const g4attn_layer* layer, const g4attn_norms* norms, const void* q,
-                               const void* k_new, const void* v_new, const int32_t* seq_len, int32_t B,
-                               const g4attn_cache* cache, const int32_t* page_table, int32_t max_pages,
-                               void* out, void* workspace, size_t workspace_bytes, void* stream);
 
 /* Writes the K'/V (sliding) or S (global) rows of a prefill batch into the paged cache
  * without computing attention: the first step of g4attn_prefill on its own (RFC section 5,
@@ -251,10 +256,17 @@ g4_status g4attn_kv_append(const g4attn_layer* layer, const void* k, const void*
                            int32_t max_pages, void* stream);
 
 /* Bytes of device workspace g4attn_decode needs for B requests whose page table has
- * max_pages columns (partial softmax states of the fixed key chunks). */
+ * max_pages columns: the partial softmax states (m, l, O in fp32) of the fixed key chunks whose
+ * split and ordered merge RFC section 4 rule 3 allows only when the merge tree is fixed by the
+ * contract. The size is taken from the page-table width, the one context bound the host knows
+ * without reading device memory (a context never exceeds 16 * max_pages keys, and never 262144);
+ * it is 0 for an unsupported layer, B <= 0 or max_pages <= 0. */
 size_t g4attn_decode_workspace_bytes(const g4attn_layer* layer, int32_t B, int32_t max_pages);
 
-/* One decode step for B requests. Request b's new token sits at position seq_len[b]-1
+/* One decode step for B requests (RFC section 5, sliding_attention_core / global_attention_core
+ * at one query row, and hybrid_kv_cache_contract: the decode side of the paged-cache handoff;
+ * section 4 rules 2 and 3: a fixed chunk split with a fixed merge order, no split that depends on
+ * the batch or the occupancy). Request b's new token sits at position seq_len[b]-1
  * (seq_len counts the new token); its key/value (k_new, v_new; v_new NULL on global layers)
  * are first written into the cache at that position, then out[b] = attention of q[b] over
  * positions 0 .. seq_len[b]-1 (the last `window` of them on sliding layers). Keys are split
@@ -300,11 +312,14 @@ g4_status g4attn_decode_static(const g4attn_layer* layer, const void* q, const v
  * layer is unsupported. Truncates to len-1 characters. */
 int32_t g4attn_provenance(const g4attn_layer* layer, char* buf, size_t len);
 
-/* Synchronises `stream`, then reads and clears the device error word of the current device:
- * G4_OK, G4_ERR_TIMEOUT or G4_ERR_DEVICE (or G4_ERR_CUDA if a CUDA call failed). */
+/* The fail-closed report of RFC section 4 rule 7: problems only the device can see (a bad page,
+ * position or image span, a bounded wait that ran out) are never absorbed by a silent fallback but
+ * surface here. Synchronises `stream`, then reads and clears the device error word of the current
+ * device: G4_OK, G4_ERR_TIMEOUT or G4_ERR_DEVICE (or G4_ERR_CUDA if a CUDA call failed). */
 g4_status g4attn_status_sync(void* stream);
 
-/* A static, human-readable name for a status code. */
+/* A static, human-readable name for a status code (the failure half of the provenance that RFC
+ * section 4 rules 7 and 8 ask for: what was refused, and why). Never NULL. */
 const char* g4attn_status_string(g4_status s);
 
 #ifdef __cplusplus

@@ -360,7 +360,7 @@ int32_t g4attn_provenance(const g4attn_layer* layer, char* buf, size_t len) {
                  "prefill_global_tcgen05_2sm_x2,decode_global_mma_bf16,merge_ordered;schedule=qtile128@abs-pos,"
                  "ktile128@abs-pos,ascending;split=decode-fixed-chunk-1024@abs-key0,4-warp-round-robin,ordered-merge;"
                  "exact-decode=prefill-kernels-one-row-chunks;vision=image-span-per-row;"
-                 "accumulator=fp32;casts=roped-q,roped-k,p,out:bf16-rne;device=%s;dtype=bf16;"
+                 "accumulator=fp32;casts=roped-q,roped-k,p,out:bf16-rne;exp=ex2.approx.ftz.f32;device=%s;dtype=bf16;"
                  "shape=Hq32,Hkv4,D512,k_eq_v,prope0.25,theta1e6,scale%.9g;fallback=none",
                  dev, (double)layer->softmax_scale);
   else
@@ -370,7 +370,7 @@ int32_t g4attn_provenance(const g4attn_layer* layer, char* buf, size_t len) {
                  "schedule=qtile128@abs-pos,ktile128@abs-pos,ascending,window-skip;"
                  "split=decode-fixed-chunk-256@abs-key0,4-warp-round-robin,ordered-merge;"
                  "exact-decode=prefill-kernels-one-row-chunks;vision=image-span-per-row;"
-                 "accumulator=fp32;casts=roped-q,roped-k,p,out:bf16-rne;device=%s;dtype=bf16;"
+                 "accumulator=fp32;casts=roped-q,roped-k,p,out:bf16-rne;exp=ex2.approx.ftz.f32;device=%s;dtype=bf16;"
                  "shape=Hq32,Hkv16,D256,W%d,theta1e4,scale%.9g;fallback=none",
                  dev, layer->window, (double)layer->softmax_scale);
   if (n < 0) return -1;

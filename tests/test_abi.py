@@ -31,6 +31,43 @@ def test_header_declares_the_entry_points():
     assert set(names) == set(g4.EXPORTS)
 
 
+def declaration_blocks():
+    """(comment, declared function names) for each comment of the header after the file comment:
+    the functions declared between that comment and the next one."""
+    text = open(os.path.join(ROOT, "include", "g4attn.h")).read()
+    parts = re.split(r"(/\*.*?\*/)", text, flags=re.S)
+    blocks, comment = [], None
+    for part in parts[2:]:          # parts[1] is the file comment
+        if part.startswith("/*"):
+            comment = part
+        else:
+            names = re.findall(r"\b(g4attn_\w+)\s*\(", part)
+            if names:
+                blocks.append((comment or "", names))
+    return blocks
+
+
+def test_every_entry_point_cites_its_passage():
+    """Each declared call sits under a comment that names the passage of the pages it implements
+    (an RFC section and row or rule), or says that the pages have no counterpart of it."""
+    seen = set()
+    for comment, names in declaration_blocks():
+        flat = " ".join(re.sub(r"\n\s*\*(?!/)", " ", comment).split())
+        assert re.search(r"RFC section \d", flat) or "no counterpart" in flat, names
+        seen.update(names)
+    assert seen == set(declared_functions())
+
+
+def test_provenance_names_the_exponential(lib):
+    """The softmax exponential's flavour is a declared choice, so the provenance record names it."""
+    for layer in (g4.sliding_layer(), g4.global_layer()):
+        buf = ctypes.create_string_buffer(2048)
+        n = lib.g4attn_provenance(ctypes.byref(layer), buf, len(buf))
+        assert n > 0
+        rec = buf.value.decode()
+        assert "exp=ex2.approx.ftz.f32" in rec and "fallback=none" in rec and "accumulator=fp32" in rec
+
+
 def test_library_exports_every_declared_symbol(lib):
     for name in declared_functions():
         assert hasattr(lib, name), name
