@@ -2,9 +2,11 @@
 cannot allocate device memory) against g4attn_decode with a caller workspace.
 
 Two static calls in a row per layer kind, the first with the larger batch, so that whatever
-the first call leaves in the shared scratch is still there when the second runs. Each output
-must match the workspace entry point's within the tests' tolerance. The file is named so that
-it is collected last; it passes alone in a fresh process as well.
+the first call leaves in the shared scratch is still there when the second runs. Both entry
+points run the same deterministic kernels on the same inputs, so each output must equal the
+workspace entry point's bit for bit (a partly stale read of the shared scratch would show), and
+it must also be finite. The file is named so that it is collected last; it passes alone in a
+fresh process as well.
 """
 import numpy as np
 import pytest
@@ -13,7 +15,7 @@ import torch
 import invariant_hybrid_attention_gb300 as g4
 from invariant_hybrid_attention_gb300.paged import device_int32
 
-from gpu_cases import TOL_MAX, TOL_MEAN, DecodeBatch, errors, f64, layers
+from gpu_cases import DecodeBatch, f64, layers
 
 pytestmark = pytest.mark.gpu
 
@@ -47,7 +49,5 @@ def test_decode_static_matches_decode_on_two_calls_in_a_row(kind):
         assert 0 < need <= g4.DECODE_STATIC_SCRATCH_BYTES
         want, cache = db.run(layer)              # the workspace entry point (it also fills the cache)
         got = static_decode(db, layer, cache)    # re-appends the same token at the same slot
-        g, w = f64(got), f64(want)
-        assert np.isfinite(g).all(), f"call {call}: non-finite output"
-        mx, mean = errors(g, w)
-        assert mx <= TOL_MAX and mean <= TOL_MEAN, f"call {call}: max-abs {mx:.3e}, mean-abs {mean:.3e}"
+        assert np.isfinite(f64(got)).all(), f"call {call}: non-finite output"
+        assert torch.equal(got, want), f"call {call}: the static-scratch decode differs from g4attn_decode"
