@@ -190,3 +190,32 @@ def rows_of(hist: List[torch.Tensor], layout: RowLayout, fill_nan: bool = True) 
         c0, L, s = layout.ctx_start[b], layout.q_len[b], layout.q_start[b]
         out[s:s + L] = h[c0:c0 + L]
     return out
+
+
+# ---- the decode mix, one cache per layer ---------------------------------------------------
+
+def decode_mix_lengths(wl: DecodeWorkload = DECODE_MIX) -> List[int]:
+    """Context lengths of the decode mix (the new token included): `batch` integers uniform in
+    [ctx_lo, ctx_hi], drawn with the workload's length seed."""
+    return uniform_ints(wl.batch, wl.ctx_lo, wl.ctx_hi, wl.length_seed)
+
+
+def decode_mix_first_keys(lens: Sequence[int], window: int) -> List[int]:
+    """First key position each request's sliding cache holds: the page holding the window's first
+    key (a sliding layer maps only the window's pages; earlier table entries stay -1)."""
+    return [PAGE_SIZE * (max(0, int(L) - int(window)) // PAGE_SIZE) for L in lens]
+
+
+def decode_mix_values(value_seed: int, layer: int, b: int, n_rows: int, n_kv: int, d: int, with_v: bool,
+                      device="cuda"):
+    """Key (and value) rows of request b of layer `layer` of the decode mix: the rows its cache holds,
+    the new token's last. Seeded per (layer, request), so that any one request can be drawn again."""
+    base = int(value_seed) * 1_000_000 + int(layer) * 10_000 + int(b) * 10
+    k = bf16_normal_device((n_rows, n_kv, d), base + 1, device=device)
+    v = bf16_normal_device((n_rows, n_kv, d), base + 2, device=device) if with_v else None
+    return k, v
+
+
+def decode_mix_queries(value_seed: int, layer: int, B: int, d: int, device="cuda") -> torch.Tensor:
+    """The B decode queries [B, 32, d] of layer `layer` of the decode mix."""
+    return bf16_normal_device((B, 32, d), int(value_seed) * 1_000_000 + int(layer) * 10_000 + 9999, device=device)
