@@ -9,9 +9,8 @@ One step runs the whole path once over seeded synthetic inputs already resident 
      uniform in [1024, 32768] (seed 7), one cache per layer filled through g4attn_kv_append, pages
      scattered by random permutations.
 Each part is timed with CUDA events on the launching stream after an L2 flush (a 512 MB write); a
-prefill part runs its stage and attention launches through g4attn_prefill_stage and
-g4attn_prefill_attend (exactly g4attn_prefill) with an event between them, so the attention kernel
-is timed on its own. After the timed region, sampled outputs of the last step are checked against
+prefill part runs its two launches through g4attn_kv_append and g4attn_prefill_attend (exactly
+g4attn_prefill) with an event between them, so the attention kernel is timed on its own. After the timed region, sampled outputs of the last step are checked against
 the fp64 oracle; a miss ends the run without a result line. The end-to-end figures then time the
 same parts through the public calls with host buffers (pinned host -> device inputs and device ->
 host outputs inside the timed region).
@@ -178,18 +177,18 @@ class SlidingPrefill:
         self.qs, self.ql, self.cs = (device_int32(x) for x in (lay.q_start, lay.q_len, lay.ctx_start))
         self.out = torch.empty_like(self.q)
         self.flops = prefill_flops(256, 32, self.lens, W)
-        self.launches = 3   # stage: K'/V by key groups, roped q by rows; then attention
+        self.launches = 2   # the K'/V append by key groups, then attention
 
     def run(self):
         self.g4.g4attn_prefill(self.layer, self.q, self.k, self.v, self.qs, self.ql, self.cs, self.cache.desc,
                                self.table, self.out)
 
-    def run_stage(self):   # launch 1 of g4attn_prefill: cache append + roped-q staging
-        self.g4.g4attn_prefill_stage(self.layer, self.q, self.k, self.v, self.qs, self.ql, self.cs, self.cache.desc,
-                                     self.table, self.out)
+    def run_stage(self):   # launch 1 of g4attn_prefill: the cache append
+        self.g4.g4attn_kv_append(self.layer, self.k, self.v, self.qs, self.ql, self.cs, self.cache.desc, self.table)
 
-    def run_attend(self):  # launch 2: the attention kernel
-        self.g4.g4attn_prefill_attend(self.layer, self.qs, self.ql, self.cs, self.cache.desc, self.table, self.out)
+    def run_attend(self):  # launch 2: the attention kernel, rotating the raw queries itself
+        self.g4.g4attn_prefill_attend(self.layer, self.q, self.qs, self.ql, self.cs, self.cache.desc, self.table,
+                                      self.out)
 
     def host_io(self):
         return [self.q, self.k, self.v], [self.out]

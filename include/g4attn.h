@@ -152,7 +152,8 @@ g4_status g4attn_rope_apply(const g4attn_layer* layer, const void* x, const int3
  * q_start[b] .. q_start[b]+q_len[b]-1 of q, k, v and out; they are its positions
  * ctx_start[b] .. ctx_start[b]+q_len[b]-1. Keys at positions < ctx_start[b] must already be
  * in the cache. The call first writes the new rows' K'/V (sliding) or S (global) into the
- * cache through page_table, then computes out for those rows. Rows of out that belong to no
+ * cache through page_table, then computes out for those rows (two launches; the queries are
+ * rotated inside the attention kernel). Rows of out that belong to no
  * sequence are not written. q_start, q_len, ctx_start: int32 [B], device, read on the device
  * (q_len 0 is allowed); sequences' row ranges must not overlap and must lie inside [0, T) (a
  * range that does not is refused on the device: none of its rows is read or written, and
@@ -163,23 +164,27 @@ g4_status g4attn_prefill(const g4attn_layer* layer, const void* q, const void* k
                          const int32_t* ctx_start, int32_t B, const g4attn_cache* cache,
                          const int32_t* page_table, int32_t max_pages, void* out, void* stream);
 
-/* The two steps of g4attn_prefill, for callers that schedule or time them apart; the pair gives
- * the same bits as g4attn_prefill, which is exactly g4attn_prefill_stage followed by
- * g4attn_prefill_attend on one stream.
- * g4attn_prefill_stage: the cache append of the new rows (RFC section 5,
- * hybrid_kv_cache_contract) and the declared bf16 cast of the roped queries, which it writes
- * into the sequences' rows of `out` (sliding_rope_d256 / global_proportional_p_rope). Arguments
- * and errors as g4attn_prefill.
- * g4attn_prefill_attend: the attention step (sliding_attention_core / global_attention_core)
- * over queries that g4attn_prefill_stage staged in `out` with the same rows, cache and page
- * table; it overwrites those rows with the output and writes no other row. Arguments as
- * g4attn_prefill without q, k and v; out must be 16-byte aligned when T > 0. Calling it on rows
- * that were not staged gives meaningless (but bounded, fault-free) output. */
+/* g4attn_prefill in two steps, for callers that schedule or time them apart (RFC section 5,
+ * hybrid_kv_cache_contract for the append, sliding_attention_core / global_attention_core and
+ * sliding_rope_d256 / global_proportional_p_rope for the attention). g4attn_prefill is exactly
+ * g4attn_kv_append followed by g4attn_prefill_attend with its q on one stream.
+ * g4attn_prefill_attend: the attention step over the cache and page table the append filled; it
+ *   writes the output rows of the sequences into `out` and no other row. Arguments as
+ *   g4attn_prefill without k and v. q: the raw query rows [T][Hq][D] (16-byte aligned), which the
+ *   attention kernel rotates itself, with the angles, rotation and bf16 cast of the declared
+ *   roped-q cast point; or NULL, when g4attn_prefill_stage has staged the roped queries in `out`
+ *   (the staged form, then overwritten with the output). out must be 16-byte aligned when T > 0.
+ *   Calling it with q NULL on rows that were not staged gives meaningless (but bounded, fault-free)
+ *   output.
+ * g4attn_prefill_stage: the staged form's first step: the cache append of the new rows, plus the
+ *   declared bf16 cast of the roped queries written into the sequences' rows of `out`. Arguments
+ *   and errors as g4attn_prefill. Stage, then attend with q NULL, gives the same bits as
+ *   g4attn_prefill; it costs one more pass over q and out. */
 g4_status g4attn_prefill_stage(const g4attn_layer* layer, const void* q, const void* k, const void* v,
                                int32_t T, const int32_t* q_start, const int32_t* q_len,
                                const int32_t* ctx_start, int32_t B, const g4attn_cache* cache,
                                const int32_t* page_table, int32_t max_pages, void* out, void* stream);
-g4_status g4attn_prefill_attend(const g4attn_layer* layer, int32_t T, const int32_t* q_start,
+g4_status g4attn_prefill_attend(const g4attn_layer* layer, const void* q, int32_t T, const int32_t* q_start,
                                 const int32_t* q_len, const int32_t* ctx_start, int32_t B,
                                 const g4attn_cache* cache, const int32_t* page_table, int32_t max_pages,
                                 void* out, void* stream);
@@ -317,6 +322,18 @@ int32_t g4attn_provenance(const g4attn_layer* layer, char* buf, size_t len);
  * surface here. Synchronises `stream`, then reads and clears the device error word of the current
  * device: G4_OK, G4_ERR_TIMEOUT or G4_ERR_DEVICE (or G4_ERR_CUDA if a CUDA call failed). */
 g4_status g4attn_status_sync(void* stream);
+
+/* The bound of every wait in the kernels (RFC section 4 rule 7: a kernel that cannot make progress
+ * fails closed instead of hanging). Each spin-wait of the kernels' barrier protocols gives up once
+ * this many nanoseconds have passed since its first poll failed; the kernel then sets the timeout
+ * bit of the device error word (G4_ERR_TIMEOUT from g4attn_status_sync), lets the copies and
+ * tensor-core operations it already issued finish (those drains keep their own 2 s bound), frees
+ * its tensor memory and returns; its output rows are then unspecified. Process-wide, read at each
+ * launch; ns in [0, 2e9] (2e9, 2 s, is the default; 0 gives up at the first failed poll, which
+ * exercises the fail-closed path of every kernel on purpose). Larger values: G4_ERR_INVALID.
+ * g4attn_wait_limit_ns returns the current value. */
+g4_status g4attn_set_wait_limit_ns(uint64_t ns);
+uint64_t g4attn_wait_limit_ns(void);
 
 /* A static, human-readable name for a status code (the failure half of the provenance that RFC
  * section 4 rules 7 and 8 ask for: what was refused, and why). Never NULL. */

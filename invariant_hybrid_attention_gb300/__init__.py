@@ -26,7 +26,9 @@ EXPORTS = ("g4attn_rope_apply", "g4attn_prefill", "g4attn_prefill_stage", "g4att
            "g4attn_prefill_normed", "g4attn_prefill_vision", "g4attn_kv_append_normed", "g4attn_decode_normed",
            "g4attn_decode_exact", "g4attn_decode_exact_workspace_bytes",
            "g4attn_kv_append", "g4attn_decode_workspace_bytes",
-           "g4attn_decode", "g4attn_decode_static", "g4attn_provenance", "g4attn_status_sync", "g4attn_status_string")
+           "g4attn_decode", "g4attn_decode_static", "g4attn_provenance", "g4attn_status_sync", "g4attn_status_string",
+           "g4attn_set_wait_limit_ns", "g4attn_wait_limit_ns")
+DEFAULT_WAIT_LIMIT_NS = 2_000_000_000   # the kernels' bounded waits give up after 2 s by default
 
 
 class g4attn_layer(ctypes.Structure):
@@ -70,7 +72,7 @@ def load(path: Optional[str] = None):
         "g4attn_rope_apply": (I32, [L, P, P, I32, I32, P, P]),
         "g4attn_prefill": (I32, [L, P, P, P, I32, P, P, P, I32, C, P, I32, P, P]),
         "g4attn_prefill_stage": (I32, [L, P, P, P, I32, P, P, P, I32, C, P, I32, P, P]),
-        "g4attn_prefill_attend": (I32, [L, I32, P, P, P, I32, C, P, I32, P, P]),
+        "g4attn_prefill_attend": (I32, [L, P, I32, P, P, P, I32, C, P, I32, P, P]),
         "g4attn_prefill_normed": (I32, [L, N, P, P, P, I32, P, P, P, I32, C, P, I32, P, P]),
         "g4attn_prefill_vision": (I32, [L, N, P, P, P, I32, P, P, P, I32, P, C, P, I32, P, P]),
         "g4attn_kv_append_normed": (I32, [L, N, P, P, I32, P, P, P, I32, C, P, I32, P]),
@@ -84,6 +86,8 @@ def load(path: Optional[str] = None):
         "g4attn_provenance": (I32, [L, ctypes.c_char_p, SZ]),
         "g4attn_status_sync": (I32, [P]),
         "g4attn_status_string": (ctypes.c_char_p, [I32]),
+        "g4attn_set_wait_limit_ns": (I32, [ctypes.c_uint64]),
+        "g4attn_wait_limit_ns": (ctypes.c_uint64, []),
     }
     for name, (res, args) in sigs.items():
         f = getattr(lib, name)
@@ -166,10 +170,12 @@ def g4attn_prefill_stage(layer, q, k, v, q_start, q_len, ctx_start, cache: g4att
     return out
 
 
-def g4attn_prefill_attend(layer, q_start, q_len, ctx_start, cache: g4attn_cache, page_table, out, stream=None):
+def g4attn_prefill_attend(layer, q, q_start, q_len, ctx_start, cache: g4attn_cache, page_table, out, stream=None):
+    """The attention step of a prefill: q the raw query rows (rotated in the kernel), or None when
+    g4attn_prefill_stage staged the roped queries in out."""
     T, B = int(out.shape[0]), int(q_start.shape[0])
-    _check(load().g4attn_prefill_attend(ctypes.byref(layer), T, _ptr(q_start), _ptr(q_len), _ptr(ctx_start), B,
-                                        ctypes.byref(cache), _ptr(page_table), int(page_table.shape[1]),
+    _check(load().g4attn_prefill_attend(ctypes.byref(layer), _ptr(q), T, _ptr(q_start), _ptr(q_len), _ptr(ctx_start),
+                                        B, ctypes.byref(cache), _ptr(page_table), int(page_table.shape[1]),
                                         _ptr(out), _stream(stream)), "g4attn_prefill_attend")
     return out
 
@@ -276,3 +282,12 @@ def g4attn_decode_exact(layer, norms, q, k_new, v_new, seq_len, cache: g4attn_ca
                                       _stream(stream)),
            "g4attn_decode_exact")
     return out
+
+
+def g4attn_set_wait_limit_ns(ns: int) -> None:
+    """Bound of every protocol wait in kernels launched from now on (0 .. 2e9 ns; default 2 s)."""
+    _check(load().g4attn_set_wait_limit_ns(int(ns)), "g4attn_set_wait_limit_ns")
+
+
+def g4attn_wait_limit_ns() -> int:
+    return int(load().g4attn_wait_limit_ns())

@@ -203,27 +203,32 @@ g4_status g4attn_prefill_stage(const g4attn_layer* layer, const void* q, const v
                        stream);
 }
 
-static g4_status prefill_attend(const g4attn_layer* layer, int32_t T, const int32_t* q_start, const int32_t* q_len,
-                                const int32_t* ctx_start, int32_t B, const int32_t* span, const g4attn_cache* cache,
-                                const int32_t* page_table, int32_t max_pages, void* out, void* stream) {
+// The attention step. q: the raw query rows, rotated inside the attention kernel; NULL: the roped
+// queries staged in `out` by prefill_stage (image spans come only with staged queries).
+static g4_status prefill_attend(const g4attn_layer* layer, const void* q, int32_t T, const int32_t* q_start,
+                                const int32_t* q_len, const int32_t* ctx_start, int32_t B, const int32_t* span,
+                                const g4attn_cache* cache, const int32_t* page_table, int32_t max_pages, void* out,
+                                void* stream) {
   bool global = false;
   g4_status s = check_layer(layer, &global);
   if (s != G4_OK) return s;
   if ((s = check_rows(out, T, q_start, q_len, ctx_start, B)) != G4_OK) return s;
   if ((s = check_cache(cache, global, page_table, max_pages)) != G4_OK) return s;
   if (span && (reinterpret_cast<uintptr_t>(span) & 7u)) return G4_ERR_INVALID;
+  if (q && (!aligned16(q) || span)) return G4_ERR_INVALID;
   if (T == 0) return G4_OK;
   DeviceState st;
   if (device_state(&st) != cudaSuccess) return G4_ERR_CUDA;
   const SeqRows rows{q_start, q_len, ctx_start, B, T, span};
   return from_cuda(launch_prefill(global, rows, global ? 0 : layer->window, scale_log2(layer),
-                                  paged(cache, page_table, max_pages), out, st, (cudaStream_t)stream));
+                                  paged(cache, page_table, max_pages), out, st, (cudaStream_t)stream, q));
 }
 
-g4_status g4attn_prefill_attend(const g4attn_layer* layer, int32_t T, const int32_t* q_start, const int32_t* q_len,
-                                const int32_t* ctx_start, int32_t B, const g4attn_cache* cache,
+g4_status g4attn_prefill_attend(const g4attn_layer* layer, const void* q, int32_t T, const int32_t* q_start,
+                                const int32_t* q_len, const int32_t* ctx_start, int32_t B, const g4attn_cache* cache,
                                 const int32_t* page_table, int32_t max_pages, void* out, void* stream) {
-  return prefill_attend(layer, T, q_start, q_len, ctx_start, B, nullptr, cache, page_table, max_pages, out, stream);
+  return prefill_attend(layer, q, T, q_start, q_len, ctx_start, B, nullptr, cache, page_table, max_pages, out,
+                        stream);
 }
 
 g4_status g4attn_prefill_vision(const g4attn_layer* layer, const g4attn_norms* norms, const void* q, const void* k,
@@ -233,10 +238,27 @@ g4_status g4attn_prefill_vision(const g4attn_layer* layer, const g4attn_norms* n
                                 void* stream) {
   // The span check comes first, so that a refused call launches nothing.
   if (span && (reinterpret_cast<uintptr_t>(span) & 7u)) return G4_ERR_INVALID;
-  g4_status s = prefill_stage(layer, norms, q, k, v, T, q_start, q_len, ctx_start, B, cache, page_table, max_pages,
-                              out, stream);
+  bool global = false;
+  g4_status s = check_layer(layer, &global);
   if (s != G4_OK) return s;
-  return prefill_attend(layer, T, q_start, q_len, ctx_start, B, span, cache, page_table, max_pages, out, stream);
+  NormArgs nm;
+  if ((s = check_norms(norms, global, &nm)) != G4_OK) return s;
+  if (!nm.any() && !span) {
+    // Plain queries: the cache append, then the attention kernel on the raw queries, which it
+    // rotates itself (the same bits as the staged form below, one pass over q and out less).
+    if (T > 0 && (!q || !aligned16(q) || !out || !aligned16(out))) return G4_ERR_INVALID;
+    if ((s = check_rows(q, T, q_start, q_len, ctx_start, B)) != G4_OK) return s;
+    if ((s = check_cache(cache, global, page_table, max_pages)) != G4_OK) return s;
+    if ((s = g4attn_kv_append(layer, k, v, T, q_start, q_len, ctx_start, B, cache, page_table, max_pages, stream)) !=
+        G4_OK)
+      return s;
+    return prefill_attend(layer, q, T, q_start, q_len, ctx_start, B, nullptr, cache, page_table, max_pages, out,
+                          stream);
+  }
+  s = prefill_stage(layer, norms, q, k, v, T, q_start, q_len, ctx_start, B, cache, page_table, max_pages, out, stream);
+  if (s != G4_OK) return s;
+  return prefill_attend(layer, nullptr, T, q_start, q_len, ctx_start, B, span, cache, page_table, max_pages, out,
+                        stream);
 }
 
 g4_status g4attn_prefill_normed(const g4attn_layer* layer, const g4attn_norms* norms, const void* q, const void* k,
@@ -326,7 +348,8 @@ g4_status g4attn_decode_exact(const g4attn_layer* layer, const g4attn_norms* nor
   if ((s = prefill_stage(layer, norms, q, k_new, v_new, B, rows, rows + B, rows + 2 * B, B, cache, page_table,
                          max_pages, out, stream)) != G4_OK)
     return s;
-  return prefill_attend(layer, B, rows, rows + B, rows + 2 * B, B, nullptr, cache, page_table, max_pages, out, stream);
+  return prefill_attend(layer, nullptr, B, rows, rows + B, rows + 2 * B, B, nullptr, cache, page_table, max_pages, out,
+                        stream);
 }
 
 g4_status g4attn_decode_static(const g4attn_layer* layer, const void* q, const void* k_new, const void* v_new,
@@ -357,8 +380,9 @@ int32_t g4attn_provenance(const g4attn_layer* layer, char* buf, size_t len) {
   if (global)
     n = snprintf(rec, sizeof(rec),
                  "requested=g4attn;actual=g4attn-cuda-sm_103a;layer=global;kernels=append_shared_s,"
-                 "prefill_global_tcgen05_2sm_x2,decode_global_mma_bf16,merge_ordered;schedule=qtile128@abs-pos,"
+                 "prefill_global_tcgen05_2sm_x2_rope_q,decode_global_mma_bf16,merge_ordered;schedule=qtile128@abs-pos,"
                  "ktile128@abs-pos,ascending;split=decode-fixed-chunk-1024@abs-key0,4-warp-round-robin,ordered-merge;"
+                 "qrope=attention-kernel(plain),append-pass(normed,vision,exact-decode);"
                  "exact-decode=prefill-kernels-one-row-chunks;vision=image-span-per-row;"
                  "accumulator=fp32;casts=roped-q,roped-k,p,out:bf16-rne;exp=ex2.approx.ftz.f32;device=%s;dtype=bf16;"
                  "shape=Hq32,Hkv4,D512,k_eq_v,prope0.25,theta1e6,scale%.9g;fallback=none",
@@ -366,9 +390,10 @@ int32_t g4attn_provenance(const g4attn_layer* layer, char* buf, size_t len) {
   else
     n = snprintf(rec, sizeof(rec),
                  "requested=g4attn;actual=g4attn-cuda-sm_103a;layer=sliding;kernels=append_kv_keygroups,"
-                 "append_rope_q,prefill_sliding_tcgen05_2sm,decode_sliding_mma_bf16,merge_ordered;"
+                 "prefill_sliding_tcgen05_2sm_rope_q,decode_sliding_mma_bf16,merge_ordered;"
                  "schedule=qtile128@abs-pos,ktile128@abs-pos,ascending,window-skip;"
                  "split=decode-fixed-chunk-256@abs-key0,4-warp-round-robin,ordered-merge;"
+                 "qrope=attention-kernel(plain),append-pass(normed,vision,exact-decode);"
                  "exact-decode=prefill-kernels-one-row-chunks;vision=image-span-per-row;"
                  "accumulator=fp32;casts=roped-q,roped-k,p,out:bf16-rne;exp=ex2.approx.ftz.f32;device=%s;dtype=bf16;"
                  "shape=Hq32,Hkv16,D256,W%d,theta1e4,scale%.9g;fallback=none",
@@ -381,6 +406,14 @@ int32_t g4attn_provenance(const g4attn_layer* layer, char* buf, size_t len) {
   }
   return n;
 }
+
+g4_status g4attn_set_wait_limit_ns(uint64_t ns) {
+  if (ns > kWaitLimitNs) return G4_ERR_INVALID;
+  set_wait_limit_ns(ns);
+  return G4_OK;
+}
+
+uint64_t g4attn_wait_limit_ns(void) { return wait_limit_ns(); }
 
 g4_status g4attn_status_sync(void* stream) {
   if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return G4_ERR_CUDA;

@@ -29,7 +29,10 @@ constexpr int kDecodeChunkGlobal = 1024;
 // Error-word bits (g4attn_status_sync maps them to g4_status values).
 enum : uint32_t { kErrTimeout = 1u, kErrPage = 2u, kErrPos = 4u, kErrSpan = 8u };
 
-// Bounded waits give up after this long; nothing legitimate waits anywhere near it.
+// Bounded waits give up after this long; nothing legitimate waits anywhere near it. The waits of
+// the kernels' protocols take their limit from the launch (g4attn_set_wait_limit_ns; this is the
+// default and the largest allowed); the drains of an aborted kernel (copies and MMAs it issued
+// that must finish before it may leave) always use this one.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
 // Cache page layout. One page of one KV head holds 16 keys x D dims as core matrices of
@@ -68,10 +71,16 @@ __host__ __device__ constexpr int rot_offset(int j, int d) {
 // RoPE cos/sin tables for one layer kind, built in fp64 on the host and stored as fp32:
 // coarse[t][c] = (cos, sin)(256*c*f_t), mid[t][a] = (cos, sin)(16*a*f_t) and
 // fine[t][b] = (cos, sin)(b*f_t). The mid and fine tables are small enough to stay in L1.
+// The same values are also kept transposed (entry-major, [entry][R]), for the prefill kernels'
+// in-kernel query rotation, whose threads hold consecutive pairs t: there a warp's load of one
+// entry for 32 pairs reads 256 contiguous bytes instead of 32 lines.
 struct RopeTables {
   const float2* coarse;   // [R][kRopeCoarse]
   const float2* mid;      // [R][kRopeMid]
   const float2* fine;     // [R][kRopeFine]
+  const float2* coarse_t; // [kRopeCoarse][R]
+  const float2* mid_t;    // [kRopeMid][R]
+  const float2* fine_t;   // [kRopeFine][R]
 };
 
 // ---- small helpers -------------------------------------------------------------------------
@@ -156,20 +165,22 @@ G4_DEV bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Waits for phase `parity` of `bar` to complete. Gives up (returns false, sets *abort and the
-// timeout bit) after kWaitLimitNs, or at once when *abort is already set by another thread.
-G4_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, uint32_t* err) {
+// timeout bit) once limit_ns have passed since the first poll failed (limit 0: at once), or as
+// soon as *abort is set by another thread.
+G4_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, uint32_t* err,
+                      unsigned long long limit_ns = kWaitLimitNs) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const unsigned long long t0 = globaltimer();
   while (true) {
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(a, parity)) return true;
     if (abort && *abort) return false;
-    if (globaltimer() - t0 > kWaitLimitNs) {
+    if (globaltimer() - t0 >= limit_ns) {
       if (abort) *abort = 1;
       set_error(err, kErrTimeout);
       return false;
     }
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(a, parity)) return true;
   }
 }
 
@@ -234,20 +245,21 @@ G4_DEV bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
 }
 // mbar_wait for barriers that the other CTA of the cluster arrives on: acquires their writes at
 // cluster scope. Bounded like mbar_wait.
-G4_DEV bool mbar_wait_cl(uint64_t* bar, uint32_t parity, volatile int* abort, uint32_t* err) {
+G4_DEV bool mbar_wait_cl(uint64_t* bar, uint32_t parity, volatile int* abort, uint32_t* err,
+                         unsigned long long limit_ns = kWaitLimitNs) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait_cluster(a, parity)) return true;
   const unsigned long long t0 = globaltimer();
   while (true) {
-    for (int i = 0; i < 32; ++i) {
-      if (mbar_try_wait_cluster(a, parity)) return true;
-      __nanosleep(32);   // a cluster-scope poll does not suspend: leave issue slots to the other warps
-    }
     if (abort && *abort) return false;
-    if (globaltimer() - t0 > kWaitLimitNs) {
+    if (globaltimer() - t0 >= limit_ns) {
       if (abort) *abort = 1;
       set_error(err, kErrTimeout);
       return false;
+    }
+    for (int i = 0; i < 32; ++i) {
+      if (mbar_try_wait_cluster(a, parity)) return true;
+      __nanosleep(32);   // a cluster-scope poll does not suspend: leave issue slots to the other warps
     }
   }
 }
@@ -255,12 +267,13 @@ G4_DEV bool mbar_wait_cl(uint64_t* bar, uint32_t parity, volatile int* abort, ui
 // Out-of-line copies of the two waits, for kernels that wait in many places (one copy of each
 // polling loop keeps their hot loops small enough for the instruction caches; a kernel whose
 // inner loop waits on every step keeps the inlined form).
-static __device__ __noinline__ bool mbar_wait_ool(uint64_t* bar, uint32_t parity, volatile int* abort, uint32_t* err) {
-  return mbar_wait(bar, parity, abort, err);
+static __device__ __noinline__ bool mbar_wait_ool(uint64_t* bar, uint32_t parity, volatile int* abort, uint32_t* err,
+                                                  unsigned long long limit_ns) {
+  return mbar_wait(bar, parity, abort, err, limit_ns);
 }
 static __device__ __noinline__ bool mbar_wait_cl_ool(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                                     uint32_t* err) {
-  return mbar_wait_cl(bar, parity, abort, err);
+                                                     uint32_t* err, unsigned long long limit_ns) {
+  return mbar_wait_cl(bar, parity, abort, err, limit_ns);
 }
 
 // ---- bulk copies (TMA) -------------------------------------------------------------------------

@@ -34,6 +34,7 @@ struct DecodeParams {
   int NC;                   // chunk slots per (request, head)
   RopeTables tb;
   uint32_t* err;
+  unsigned long long wait_ns;   // limit of every protocol wait (g4attn_set_wait_limit_ns)
 };
 
 // ---------------------------------------------------------------- sliding: D 256, Hkv 16, G 2
@@ -167,7 +168,7 @@ __global__ void __launch_bounds__(128, 2) decode_sliding_kernel(DecodeParams p) 
           ok = false;
           break;
         }
-        if (globaltimer() - t0 > kWaitLimitNs) {
+        if (globaltimer() - t0 >= p.wait_ns) {
           abort_flag = 1;
           set_error(p.err, kErrTimeout);
           ok = false;
@@ -177,7 +178,7 @@ __global__ void __launch_bounds__(128, 2) decode_sliding_kernel(DecodeParams p) 
       if (!__all_sync(0xffffffffu, ok)) break;
       __threadfence_block();
     }
-    if (!mbar_wait(&full[st], ph & 1, &abort_flag, p.err)) break;
+    if (!mbar_wait(&full[st], ph & 1, &abort_flag, p.err, p.wait_ns)) break;
     uint8_t* kp = ring + st * kSStageBytes;
     uint8_t* vp = kp + kSPageBytes;
     const int key0 = (pg0 + i) * kPage;
@@ -435,7 +436,7 @@ __global__ void __launch_bounds__(128, 2) decode_global_kernel(DecodeParams p) {
           ok = false;
           break;
         }
-        if (globaltimer() - t0 > kWaitLimitNs) {
+        if (globaltimer() - t0 >= p.wait_ns) {
           abort_flag = 1;
           set_error(p.err, kErrTimeout);
           ok = false;
@@ -445,7 +446,7 @@ __global__ void __launch_bounds__(128, 2) decode_global_kernel(DecodeParams p) {
       if (!__all_sync(0xffffffffu, ok)) break;
       __threadfence_block();
     }
-    if (!mbar_wait(&full[st], ph & 1, &abort_flag, p.err)) break;
+    if (!mbar_wait(&full[st], ph & 1, &abort_flag, p.err, p.wait_ns)) break;
     uint8_t* page = stage_base + st * kGStageBytes;
     const int key0 = (pg0 + i) * kPage;
     if (key0 + kPage - 1 > k_end) {   // zero stale rows (NaN-safe V), then make them visible
@@ -675,6 +676,7 @@ cudaError_t launch_decode(bool global, const void* q, const int32_t* seq_len, in
   p.ws_ml = (float*)ws;
   p.ws_o = (float*)((uint8_t*)ws + ml);
   p.err = st.err;
+  p.wait_ns = wait_limit_ns();
   if (global) {
     p.tb = st.global;
     static bool attr_set[64] = {};

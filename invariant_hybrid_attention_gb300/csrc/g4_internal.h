@@ -20,6 +20,11 @@ struct DeviceState {
 };
 cudaError_t device_state(DeviceState* st);
 
+// The limit of every protocol wait in the kernels launched from now on (process-wide; kWaitLimitNs
+// unless g4attn_set_wait_limit_ns changed it).
+unsigned long long wait_limit_ns();
+void set_wait_limit_ns(unsigned long long ns);
+
 // Row-to-sequence description of a prefill batch (all device pointers, int32 [B]).
 struct SeqRows {
   const int32_t* q_start;
@@ -76,11 +81,12 @@ cudaError_t launch_decode(bool global, const void* q, const int32_t* seq_len, in
 // Writes rows [3][B] (q_start, q_len, ctx_start) of a decode step taken as B one-row prefill chunks.
 cudaError_t launch_decode_rows(const int32_t* seq_len, int B, int32_t* rows, const DeviceState& st, cudaStream_t s);
 
-// Attention over roped queries staged in `out` (by launch_append_prefill); writes the output
-// rows over them.
+// Attention of the rows of a prefill batch, written into `out`. With q_raw set the kernel reads the raw
+// query rows there and rotates them itself; otherwise it reads the roped queries that
+// launch_append_prefill staged in `out` and writes the output rows over them.
 cudaError_t launch_prefill(bool global, const SeqRows& rows, int window, float scale_log2, const PagedCache& cache,
-                           void* out, const DeviceState& st, cudaStream_t s);
+                           void* out, const DeviceState& st, cudaStream_t s, const void* q_raw = nullptr);
 cudaError_t launch_prefill_global(const SeqRows& rows, float scale_log2, const PagedCache& cache, void* out,
-                                  const DeviceState& st, cudaStream_t s);
+                                  const DeviceState& st, cudaStream_t s, const void* q_raw = nullptr);
 
 }  // namespace g4

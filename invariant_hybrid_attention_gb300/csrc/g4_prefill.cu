@@ -37,8 +37,14 @@
 //   warps 2-5  one thread per query row of this CTA's head: Q dims 0-127 into tensor memory,
 //              mask, online softmax (lazy rescale, threshold 2^8), P (bf16), the O correction
 //              when needed, and the epilogue O / l -> bf16.
-// The queries arrive already roped: the cache-append pass before this kernel wrote
-// bf16(RoPE(q)) into the sequence rows of `out`; the epilogue later overwrites exactly those
+// Queries (kRope): the Q tile is copied from the raw query rows and rotated in place in shared
+// memory before it moves: all 128 pairs (t, t + 128) turn, t in Q dims 0-127 (the K ring slot,
+// bound for tensor memory) and t + 128 in the shared-memory half. Softmax thread t rotates pair t
+// of every row of the tile (rotate_q_pair), the four softmax warps meet on an mbarrier, and each
+// thread then moves its row. The angles, the rotation and the bf16 cast are those of the append
+// pass, so the roped queries, and with them every output bit, are those a staged call gives. Otherwise (the staged form: normed queries,
+// image spans, the exact decode) the append pass before this kernel wrote bf16(RoPE(q)) into the
+// sequence rows of `out`, which the Q copies read; the epilogue later overwrites exactly those
 // rows (each row belongs to one unit).
 // Tensor memory (512 columns, allocated jointly by the pair): O [0,256), Q dims 0-127 [256,320)
 // as bf16 pairs, P [320,384) as bf16 key pairs, S [384,512). With one S buffer, QK^T of tile
@@ -83,7 +89,7 @@ struct SlidingSmem {
   uint64_t k_full[kNK], k_empty[kNK], k_peer[kNK];
   uint64_t v_full[kNV], v_empty[kNV], v_ready[kNV];
   uint64_t s_full, s_free, p_full, pv_done;
-  uint64_t q_full, q_pair, q_free, o_free, q_read, teardown;
+  uint64_t q_full, q_pair, q_free, o_free, q_read, q_rot, teardown;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -182,7 +188,7 @@ __device__ __noinline__ bool sliding_unit(const PrefillParams& p, int u, uint32_
   return true;
 }
 
-template <bool kSpan>
+template <bool kSpan, bool kRope>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     prefill_sliding_kernel(const __grid_constant__ CUtensorMap tmap_q, PrefillParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -215,6 +221,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(&sm.q_free, 1);            // the unit's last QK^T is done: Q may be replaced
     mbar_init(&sm.o_free, kPairWarps);   // even CTA: both CTAs have read O out
     mbar_init(&sm.q_read, kSoftmaxThreads / 32);   // this CTA's softmax warps have read the Q slot
+    mbar_init(&sm.q_rot, kSoftmaxThreads / 32);    // kRope: this CTA's softmax warps have rotated Q
     mbar_init(&sm.teardown, 2);          // on an abort both issuers commit
     sm.abort_flag = 0;
     fence_mbar_init();
@@ -297,9 +304,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const unsigned live = __ballot_sync(0xffffffffu, !is_q && mine && my_blk >= 0);
         bool okw = true;
         if (lane == 0) {
-          if (c >= (uint32_t)n_st) okw = mbar_wait_ool(&empty[s], ((c / n_st) - 1) & 1, abort_flag, p.err);
+          if (c >= (uint32_t)n_st) okw = mbar_wait_ool(&empty[s], ((c / n_st) - 1) & 1, abort_flag, p.err, p.wait_ns);
           // the unit's Q replaces the previous unit's only once that unit's last QK^T is done
-          if (okw && is_q && uq > 0) okw = mbar_wait_ool(&sm.q_free, (uq - 1) & 1, abort_flag, p.err);
+          if (okw && is_q && uq > 0) okw = mbar_wait_ool(&sm.q_free, (uq - 1) & 1, abort_flag, p.err, p.wait_ns);
         }
         if (!__shfl_sync(0xffffffffu, okw, 0)) {
           ok = false;
@@ -372,7 +379,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!sliding_unit<kSpan>(p, u, rank, un)) continue;
       for (int idx = 0; idx <= un.n_tiles; ++idx, ++c) {   // every slot, the unit's Q included
         const int s = c % kNK;
-        ok = __all_sync(0xffffffffu, mbar_wait_ool(&sm.k_full[s], (c / kNK) & 1, abort_flag, p.err));
+        ok = __all_sync(0xffffffffu, mbar_wait_ool(&sm.k_full[s], (c / kNK) & 1, abort_flag, p.err, p.wait_ns));
         if (!ok) break;
         if (lane == 0) mbar_arrive_remote(map_peer(smem_u32(&sm.k_peer[s]), peer));
         __syncwarp();
@@ -385,8 +392,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // tracks its own thread's MMAs only. Waits are warp-uniform, so that every lane leaves the
     // loops together on an abort.
     auto slot_ready = [&](uint32_t c) -> bool {   // K ring slot c has landed in both CTAs
-      return mbar_wait_ool(&sm.k_full[c % kNK], (c / kNK) & 1, abort_flag, p.err) &&
-             mbar_wait_cl_ool(&sm.k_peer[c % kNK], (c / kNK) & 1, abort_flag, p.err);
+      return mbar_wait_ool(&sm.k_full[c % kNK], (c / kNK) & 1, abort_flag, p.err, p.wait_ns) &&
+             mbar_wait_cl_ool(&sm.k_peer[c % kNK], (c / kNK) & 1, abort_flag, p.err, p.wait_ns);
     };
     uint32_t c0 = 0, jt = 0;
     int uq = 0;
@@ -395,13 +402,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       Unit un;
       if (!sliding_unit<kSpan>(p, u, rank, un)) continue;
       // the unit's Q: its slot has landed, and both CTAs' softmax warps have moved dims 0-127
-      ok = __all_sync(0xffffffffu, slot_ready(c0 + un.qpos) && mbar_wait_cl_ool(&sm.q_pair, uq & 1, abort_flag, p.err));
+      ok = __all_sync(0xffffffffu, slot_ready(c0 + un.qpos) && mbar_wait_cl_ool(&sm.q_pair, uq & 1, abort_flag, p.err, p.wait_ns));
       for (int j = 0; ok && j < un.n_tiles; ++j, ++jt) {
         const uint32_t c = c0 + un.kslot(j);
         const int s = c % kNK;
         // the single S buffer: both CTAs' softmax threads have read the previous S into registers
         ok = __all_sync(0xffffffffu,
-                        slot_ready(c) && (jt == 0 || mbar_wait_cl_ool(&sm.s_free, (jt - 1) & 1, abort_flag, p.err)));
+                        slot_ready(c) && (jt == 0 || mbar_wait_cl_ool(&sm.s_free, (jt - 1) & 1, abort_flag, p.err, p.wait_ns)));
         if (!ok) break;
         tc_fence_after();
         if (lane == 0) {
@@ -439,7 +446,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!sliding_unit<kSpan>(p, u, rank, un)) continue;
       for (int i = 0; i < un.n_tiles; ++i, ++cv, ++jt) {
         const int s = cv % kNV;
-        ok = __all_sync(0xffffffffu, mbar_wait_ool(&sm.v_full[s], (cv / kNV) & 1, abort_flag, p.err));
+        ok = __all_sync(0xffffffffu, mbar_wait_ool(&sm.v_full[s], (cv / kNV) & 1, abort_flag, p.err, p.wait_ns));
         if (!ok) break;
         const int kb = (un.kt0 + i) * kSN;
         const int v0 = max(kb, (un.k_lo >> 4) * kPage);
@@ -460,9 +467,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         // P_i is in place in both CTAs, the odd CTA's V half is ready, and (first tile of a
         // unit) the previous unit's O has been read out before this P.V overwrites it
-        ok = __all_sync(0xffffffffu, mbar_wait_cl_ool(&sm.p_full, jt & 1, abort_flag, p.err) &&
-                                         mbar_wait_cl_ool(&sm.v_ready[s], (cv / kNV) & 1, abort_flag, p.err) &&
-                                         (i > 0 || uq == 0 || mbar_wait_cl_ool(&sm.o_free, (uq - 1) & 1, abort_flag, p.err)));
+        ok = __all_sync(0xffffffffu, mbar_wait_cl_ool(&sm.p_full, jt & 1, abort_flag, p.err, p.wait_ns) &&
+                                         mbar_wait_cl_ool(&sm.v_ready[s], (cv / kNV) & 1, abort_flag, p.err, p.wait_ns) &&
+                                         (i > 0 || uq == 0 || mbar_wait_cl_ool(&sm.o_free, (uq - 1) & 1, abort_flag, p.err, p.wait_ns)));
         if (!ok) break;
         tc_fence_after();
         if (lane == 0) {
@@ -491,17 +498,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (sliding_unit<kSpan>(p, u, rank, o)) return true;
       return false;
     };
-    // Q dims 0-127 of unit o (the roped tile the producer put in K ring slot c0o + qpos, 128B
-    // swizzle) into tensor memory as bf16 pairs: the A operand of half of the QK^T k-steps. The
-    // load was issued only after the previous unit's last QK^T, so the columns are free. Once
-    // all four warps have read the slot, one thread releases it.
+    // Q dims 0-127 of unit o (the tile the producer put in K ring slot c0o + qpos, 128B swizzle)
+    // into tensor memory as bf16 pairs: the A operand of half of the QK^T k-steps; with kRope the
+    // row is rotated on the way (dims 128-255 in place in shared memory). The load was issued only
+    // after the previous unit's last QK^T, so the columns and the shared-memory half are free.
+    // Once all four warps have read the slot, one thread releases it.
     auto move_q = [&](const Unit& o, uint32_t c0o, int uqo) -> bool {
       const uint32_t cq = c0o + o.qpos;
       const int s = cq % kNK;
-      if (!__all_sync(0xffffffffu, mbar_wait_ool(&sm.k_full[s], (cq / kNK) & 1, abort_flag, p.err) &&
-                                       mbar_wait_ool(&sm.q_full, uqo & 1, abort_flag, p.err)))
+      if (!__all_sync(0xffffffffu, mbar_wait_ool(&sm.k_full[s], (cq / kNK) & 1, abort_flag, p.err, p.wait_ns) &&
+                                       mbar_wait_ool(&sm.q_full, uqo & 1, abort_flag, p.err, p.wait_ns)))
         return false;
       const uint8_t* qrow = sm.k[s] + r * 128;
+      if constexpr (kRope) {
+        // thread t rotates pair t of every row of the tile
+        const int t = threadIdx.x - 64;
+        rotate_q_pair<8, kSlidingR>(sm.k[s] + (t >> 6) * kQChunk, sm.qhi + (t >> 6) * kQChunk, p.tb, t, kBM * o.t, 0);
+        fence_proxy_async();   // QK^T reads the rewritten half, and the ring slot is refilled, by the async proxy
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.q_rot);
+        if (!__all_sync(0xffffffffu, mbar_wait_ool(&sm.q_rot, uqo & 1, abort_flag, p.err, p.wait_ns))) return false;
+      }
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t w[32];
@@ -524,7 +541,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       bool okr = true;
       if (threadIdx.x == 64) {
-        okr = mbar_wait_ool(&sm.q_read, uqo & 1, abort_flag, p.err);
+        okr = mbar_wait_ool(&sm.q_read, uqo & 1, abort_flag, p.err, p.wait_ns);
         if (okr) mbar_arrive(&sm.k_empty[s]);
       }
       return __shfl_sync(0xffffffffu, okr, 0);
@@ -552,7 +569,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int j = 0; j < cur.n_tiles; ++j, ++jt) {
         const int kb = (cur.kt0 + j) * kSN;
         // Waits are made warp-uniform so that every lane leaves the loop together on an abort.
-        if (!__all_sync(0xffffffffu, mbar_wait_ool(&sm.s_full, jt & 1, abort_flag, p.err))) {
+        if (!__all_sync(0xffffffffu, mbar_wait_ool(&sm.s_full, jt & 1, abort_flag, p.err, p.wait_ns))) {
           ok = false;
           break;
         }
@@ -609,7 +626,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         l_run = fmaf(l_run, alpha, (ls[0] + ls[1]) + (ls[2] + ls[3]));
 
         // The previous P.V has completed: the P buffer is free and O holds every earlier tile.
-        if (jt > 0 && !__all_sync(0xffffffffu, mbar_wait_ool(&sm.pv_done, (jt - 1) & 1, abort_flag, p.err))) {
+        if (jt > 0 && !__all_sync(0xffffffffu, mbar_wait_ool(&sm.pv_done, (jt - 1) & 1, abort_flag, p.err, p.wait_ns))) {
           ok = false;
           break;
         }
@@ -646,7 +663,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
       // Epilogue: O / l -> bf16, rows of this sequence only. Once O is in registers the even
       // CTA may start the next unit's P.V, which overwrites it.
-      if (!__all_sync(0xffffffffu, mbar_wait_ool(&sm.pv_done, (jt - 1) & 1, abort_flag, p.err))) {
+      if (!__all_sync(0xffffffffu, mbar_wait_ool(&sm.pv_done, (jt - 1) & 1, abort_flag, p.err, p.wait_ns))) {
         ok = false;
         break;
       }
@@ -730,8 +747,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 }  // namespace
 
 cudaError_t launch_prefill(bool global, const SeqRows& rows, int window, float scale_log2, const PagedCache& cache,
-                           void* out, const DeviceState& st, cudaStream_t s) {
-  if (global) return launch_prefill_global(rows, scale_log2, cache, out, st, s);
+                           void* out, const DeviceState& st, cudaStream_t s, const void* q_raw) {
+  if (global) return launch_prefill_global(rows, scale_log2, cache, out, st, s, q_raw);
   PrefillParams p{};
   p.rows = rows;
   p.window = window;
@@ -742,15 +759,20 @@ cudaError_t launch_prefill(bool global, const SeqRows& rows, int window, float s
   p.out = (__nv_bfloat16*)out;
   p.tb = st.sliding;
   p.err = st.err;
+  p.wait_ns = wait_limit_ns();
   p.k_cache = cache.k;
   p.v_cache = cache.v;
+  // Raw queries are rotated in the kernel; otherwise the staged roped queries are read from `out`.
+  // Image spans come only with staged queries.
+  if (rows.span && q_raw) return cudaErrorInvalidValue;
   CUtensorMap mq;
-  if (!q_map(&mq, out, rows.T, kSlidingHq, kSD)) return cudaErrorInvalidValue;
+  if (!q_map(&mq, q_raw ? q_raw : out, rows.T, kSlidingHq, kSD)) return cudaErrorInvalidValue;
   // Batches with image rows take their own instantiation, so that the plain one carries no span code.
-  auto kernel = rows.span ? prefill_sliding_kernel<true> : prefill_sliding_kernel<false>;
-  const int ki = rows.span ? 1 : 0;
-  static bool attr[64][2] = {};
-  static int max_clusters[64][2] = {};
+  auto kernel = rows.span ? prefill_sliding_kernel<true, false>
+                          : (q_raw ? prefill_sliding_kernel<false, true> : prefill_sliding_kernel<false, false>);
+  const int ki = rows.span ? 1 : (q_raw ? 2 : 0);
+  static bool attr[64][3] = {};
+  static int max_clusters[64][3] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;

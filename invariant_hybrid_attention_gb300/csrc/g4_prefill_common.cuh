@@ -1,5 +1,5 @@
 // Pieces shared by the prefill kernels (sliding and global): parameters, the work-unit
-// enumeration, page lookups and the tensor map over the roped query rows.
+// enumeration, page lookups, the query rotation and the tensor map over the query rows.
 #pragma once
 
 #include "g4_internal.h"
@@ -27,6 +27,7 @@ struct PrefillParams {
   RopeTables tb;
   uint32_t* err;
   int n_units;              // persistent sliding kernel: (query tile, KV head) units of the batch
+  unsigned long long wait_ns;   // limit of every protocol wait (g4attn_set_wait_limit_ns)
 };
 
 // Finds this CTA's (sequence, query tile) among all sequences' tiles: slot s of sequence b
@@ -140,6 +141,64 @@ inline __device__ void row_keys(const SeqRows& rows, int window, int row, int po
       } else {
         set_error(err, kErrSpan);
       }
+    }
+  }
+}
+
+// The in-kernel query rotation. A 128-row query tile sits in shared memory as 128B-swizzled boxes
+// of 64 dims x 128 rows (row r of a box at r * 128, its 16-byte piece j at piece j ^ (r % 8)). One
+// thread rotates one pair t of rows r_begin .. r_begin + 16 NK - 1 (r_begin a multiple of 16). Row
+// r sits at position p0 + r, with p0 a multiple of 128 (and p0 + 127 < 262144), so every row of the
+// tile shares the coarse table entry, a 16-row group the mid entry and rows with one r % 16 the
+// fine entry: the thread loads 1 + NK + 16 table entries (from the entry-major copies of the
+// tables, R pairs per entry), all at once, instead of 3 per row, and keeps them in registers. The angle of row r is cmul(cmul(coarse, mid), fine), exactly as rope_cs
+// forms it, and the rotation and the bf16 cast (round to nearest even) are those of the
+// cache-append pass, so a query rotated here has the bits a staged one has. A 16-row group goes in
+// three phases (all its loads, then the arithmetic, then all its stores): rotated in place, a row's
+// stores could otherwise alias the next row's loads as far as the compiler can tell, and every row
+// would pay a whole load-rotate-store latency. Every row turns, those outside the sequence too
+// (their outputs are never written), so that no branch splits a group. lo_box is the box holding
+// dim t, hi_box the one holding its partner t + D/2.
+template <int NK, int R>
+inline __device__ void rotate_q_pair(uint8_t* lo_box, uint8_t* hi_box, const RopeTables& tb, int t, int p0,
+                                     int r_begin) {
+  const int e = t & 63;
+  const int k0 = r_begin >> 4;
+  // the entry-major copies: lanes hold consecutive t, so each load is two whole lines
+  const float2 c = __ldg(tb.coarse_t + (size_t)(p0 >> 8) * R + t);
+  const int a0 = (p0 >> 4) & 15;
+  float2 m[NK], f[16];
+#pragma unroll
+  for (int k = 0; k < NK; ++k) m[k] = __ldg(tb.mid_t + (a0 + k0 + k) * R + t);
+#pragma unroll
+  for (int b = 0; b < 16; ++b) f[b] = __ldg(tb.fine_t + b * R + t);
+  uint8_t* lo = lo_box + ((e & 7) << 1);
+  uint8_t* hi = hi_box + ((e & 7) << 1);
+  const int piece = e >> 3;
+  int sw[8];   // the swizzled piece offset of rows with r % 8 = j
+#pragma unroll
+  for (int j = 0; j < 8; ++j) sw[j] = (piece ^ j) << 4;
+#pragma unroll 1
+  for (int k = 0; k < NK; ++k) {
+    float2 mk = m[0];   // m[k] by selects: a dynamic index would put m in local memory
+#pragma unroll
+    for (int j = 1; j < NK; ++j)
+      if (k == j) mk = m[j];
+    const float2 cm = cmul(c, mk);
+    uint8_t* lo_k = lo + 16 * (k0 + k) * 128;
+    uint8_t* hi_k = hi + 16 * (k0 + k) * 128;
+    float x[16], y[16];
+#pragma unroll
+    for (int b = 0; b < 16; ++b) {
+      x[b] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(lo_k + b * 128 + sw[b & 7]));
+      y[b] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(hi_k + b * 128 + sw[b & 7]));
+    }
+#pragma unroll
+    for (int b = 0; b < 16; ++b) rope_pair(x[b], y[b], cmul(cm, f[b]));
+#pragma unroll
+    for (int b = 0; b < 16; ++b) {
+      *reinterpret_cast<__nv_bfloat16*>(lo_k + b * 128 + sw[b & 7]) = __float2bfloat16_rn(x[b]);
+      *reinterpret_cast<__nv_bfloat16*>(hi_k + b * 128 + sw[b & 7]) = __float2bfloat16_rn(y[b]);
     }
   }
 }

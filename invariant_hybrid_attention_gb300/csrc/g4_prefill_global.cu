@@ -22,13 +22,19 @@
 // tiles to absolute position; every row's arithmetic depends only on its own position and its
 // sequence's keys (section 4 rules 2, 3 and 6).
 //
-// Score CTA warps: 0 copies the roped Q tile (TMA) and this CTA's K half of each key tile into a
+// Score CTA warps: 0 copies the Q tile (TMA) and this CTA's K half of each key tile into a
 // 3-stage ring; 1 issues QK^T (rank 0) or tells rank 0 that its ring slot has landed (rank 1);
 // 2-5 move Q into tensor memory, then run mask, online softmax and P (one thread per row).
 // Output CTA warps: 0 copies this CTA's V half of each 64-key half tile into a 4-stage ring;
 // 1 zeroes value rows that hold no key of the sequence, then issues P.V (rank 2) or tells rank
 // 2 that its half is ready (rank 3); 2-5 check alpha, rescale O when asked, and write the
 // output; 6 hands P slots back to the score CTA once P.V has read them.
+// Queries (kRope): the Q tile is copied from the raw query rows and its 64 turning pairs (dims 0-63
+// with 256-319) are rotated in place in shared memory before the move into tensor memory: softmax
+// thread i rotates pair i % 64 of rows 64 (i / 64) .. +63 (rotate_q_pair; rows outside the sequence
+// turn too, harmlessly), and the four softmax warps meet on an mbarrier before each moves its row. The angles, rotation and bf16 cast are the
+// append pass's, so the queries get the bits a staged call gives. Otherwise (the staged form: normed queries, image spans, the exact decode) the append pass
+// wrote bf16(p-RoPE(q)) into the sequence rows of `out`, which the Q copies read.
 // Tensor memory, score CTAs: Q [0,256) as bf16 pairs, two S buffers [256,384), [384,512).
 // Output CTAs: O [0,512), where column c holds dim c for c < 128 or c >= 384, dim c + 128 for
 // 128 <= c < 256 and dim c - 128 for 256 <= c < 384 (each instruction's N = 256 columns are
@@ -69,7 +75,7 @@ constexpr int kRotPage = 2 * kRotKG;             // 4 KB
 constexpr int kRotOff = 4 * kUnrotPage;          // 48 KB
 constexpr int kKStage = kRotOff + 4 * kRotPage;  // 64 KB
 constexpr int kKPageBytes = kUnrotPage + kRotPage;   // 16 KB: one page's share of a stage
-// The roped Q tile (8 boxes of 64 dims x 128 rows, 128B swizzle) lands at the first 1024-byte
+// The Q tile (8 boxes of 64 dims x 128 rows, 128B swizzle) lands at the first 1024-byte
 // boundary at or after K stage 1; it may reach up to 1008 bytes into the P staging area, which is
 // first written after every softmax warp of both score CTAs has moved Q into tensor memory.
 // P tile of one head: [row group (16)][key group (17)][8 rows][8 keys] bf16. Key groups 0-15 are
@@ -100,7 +106,7 @@ struct Bars {
   // score CTAs
   uint64_t k_full[kNK], k_empty[kNK], k_peer[kNK];
   uint64_t s_full[kNP], s_free[kNP], p_free[kNP];
-  uint64_t q_full, q_moved, q_pair, stg_free;
+  uint64_t q_full, q_moved, q_pair, stg_free, q_rot;
   // output CTAs
   uint64_t v_full[kNV], v_empty[kNV], v_ready[kNV];
   uint64_t p_full[kNP], o_ready[kNP], pv_done[kNP];
@@ -126,9 +132,11 @@ __device__ __forceinline__ int o_dim(int col) {
   return (col < 128 || col >= 384) ? col : (col < 256 ? col + 128 : col - 128);
 }
 
+template <bool kRope>
 __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
-    prefill_global_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_s,
-                          const __grid_constant__ CUtensorMap tmap_rot, PrefillParams p) {
+    prefill_global_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_o,
+                          const __grid_constant__ CUtensorMap tmap_s, const __grid_constant__ CUtensorMap tmap_rot,
+                          PrefillParams p) {
   extern __shared__ uint8_t smem_raw[];
   GlobalSmem& sm = *reinterpret_cast<GlobalSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   uint8_t* const base = sm.data;
@@ -197,6 +205,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(&bar.q_moved, kSoftmaxThreads / 32);
     mbar_init(&bar.q_pair, 8);
     mbar_init(&bar.stg_free, 1);
+    mbar_init(&bar.q_rot, kSoftmaxThreads / 32);   // kRope: the softmax warps have rotated Q
     for (int s = 0; s < kNV; ++s) {
       mbar_init(&bar.v_full[s], 1);
       mbar_init(&bar.v_empty[s], 1);
@@ -231,7 +240,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
     // ================================================================ score CTAs
     if (warp == 0) {
       // ------------------------------------------------------------ Q and K copies
-      if (lane == 0) {   // roped Q of head h: 8 boxes of 64 dims x 128 rows (rows outside T read as 0)
+      if (lane == 0) {   // Q of head h: 8 boxes of 64 dims x 128 rows (rows outside T read as 0)
         prefetch_tmap(&tmap_q);
         mbar_arrive_expect_tx(&bar.q_full, 8 * kQChunk);
 #pragma unroll
@@ -266,9 +275,9 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         bool okw = true;
         if (lane == 0) {
           if (j == 1 || j == 2)   // stages 1-2 held Q until the softmax warps moved it
-            okw = mbar_wait(&bar.q_moved, 0, abort_flag, p.err);
+            okw = mbar_wait(&bar.q_moved, 0, abort_flag, p.err, p.wait_ns);
           else if (j >= kNK)
-            okw = mbar_wait(&bar.k_empty[s], ((j / kNK) - 1) & 1, abort_flag, p.err);
+            okw = mbar_wait(&bar.k_empty[s], ((j / kNK) - 1) & 1, abort_flag, p.err, p.wait_ns);
         }
         if (!__shfl_sync(0xffffffffu, okw, 0)) break;
         if (lane == 0) mbar_arrive_expect_tx(&bar.k_full[s], __popc(live) * kKPageBytes);
@@ -287,19 +296,19 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
       // ------------------------------------------------------------ K relay (rank 1)
       for (int j = 0; j < n_tiles; ++j) {
         const int s = j % kNK;
-        if (!__all_sync(0xffffffffu, mbar_wait(&bar.k_full[s], (j / kNK) & 1, abort_flag, p.err))) break;
+        if (!__all_sync(0xffffffffu, mbar_wait(&bar.k_full[s], (j / kNK) & 1, abort_flag, p.err, p.wait_ns))) break;
         if (lane == 0) mbar_arrive_remote(map_peer(smem_u32(&bar.k_peer[s]), pair_peer));
         __syncwarp();
       }
     } else if (warp == 1) {
       // ------------------------------------------------------------ QK^T issuer (rank 0)
-      bool ok = __all_sync(0xffffffffu, mbar_wait_cl(&bar.q_pair, 0, abort_flag, p.err));
+      bool ok = __all_sync(0xffffffffu, mbar_wait_cl(&bar.q_pair, 0, abort_flag, p.err, p.wait_ns));
       for (int j = 0; ok && j < n_tiles; ++j) {
         const int s = j % kNK, sb = j % kNP;
         // both CTAs' halves of the tile have landed; S buffer sb was read by tile j-2's softmax
-        ok = __all_sync(0xffffffffu, mbar_wait(&bar.k_full[s], (j / kNK) & 1, abort_flag, p.err) &&
-                                         mbar_wait_cl(&bar.k_peer[s], (j / kNK) & 1, abort_flag, p.err) &&
-                                         (j < kNP || mbar_wait_cl(&bar.s_free[sb], ((j - kNP) / kNP) & 1, abort_flag, p.err)));
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar.k_full[s], (j / kNK) & 1, abort_flag, p.err, p.wait_ns) &&
+                                         mbar_wait_cl(&bar.k_peer[s], (j / kNK) & 1, abort_flag, p.err, p.wait_ns) &&
+                                         (j < kNP || mbar_wait_cl(&bar.s_free[sb], ((j - kNP) / kNP) & 1, abort_flag, p.err, p.wait_ns)));
         if (!ok) break;
         tc_fence_after();
         if (lane == 0) {
@@ -333,12 +342,18 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
           row_hi = k_hi;
         }
       }
-      bool ok = __all_sync(0xffffffffu, mbar_wait(&bar.q_full, 0, abort_flag, p.err));
+      bool ok = __all_sync(0xffffffffu, mbar_wait(&bar.q_full, 0, abort_flag, p.err, p.wait_ns));
+      if (kRope && ok) {   // thread i rotates pair i % 64 of rows 64 (i / 64) .. + 63
+        const int qi = threadIdx.x - 64;
+        rotate_q_pair<4, kGlobalR>(q_stage, q_stage + 4 * kQChunk, p.tb, qi & 63, kBM * t, 64 * (qi >> 6));
+        fence_proxy_async();   // the K copies that later refill this area write through the async proxy
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar.q_rot);
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar.q_rot, 0, abort_flag, p.err, p.wait_ns));
+      }
       if (ok) {   // Q (128B-swizzled boxes in K stages 1-2) -> tensor memory, bf16 pairs
         const uint8_t* qrow = q_stage + r * 128;
-#pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
-          uint32_t w[32];
+        auto load_chunk = [&](int c, uint32_t (&w)[32]) {
 #pragma unroll
           for (int q8 = 0; q8 < 8; ++q8) {
             const uint4 v = *reinterpret_cast<const uint4*>(qrow + c * kQChunk + ((q8 ^ (r & 7)) * 16));
@@ -347,6 +362,11 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
             w[4 * q8 + 2] = v.z;
             w[4 * q8 + 3] = v.w;
           }
+        };
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          uint32_t w[32];
+          load_chunk(c, w);
           tmem_st32(tq + kTmQ + 32 * c, w);   // dims 64c .. 64c+63 -> columns 32c .. 32c+31
         }
         tmem_st_wait();
@@ -366,7 +386,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         const int sb = j % kNP;
         const int kb = j * kTN;
         // Waits are made warp-uniform so that every lane leaves the loop together on an abort.
-        if (!__all_sync(0xffffffffu, mbar_wait(&bar.s_full[sb], (j / kNP) & 1, abort_flag, p.err))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&bar.s_full[sb], (j / kNP) & 1, abort_flag, p.err, p.wait_ns))) {
           ok = false;
           break;
         }
@@ -416,7 +436,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         l_run = fmaf(l_run, alpha, (ls[0] + ls[1]) + (ls[2] + ls[3]));
 
         // The staging area is free once the previous tile's copies have landed.
-        if (j > 0 && !__all_sync(0xffffffffu, mbar_wait_cl(&bar.stg_free, (j - 1) & 1, abort_flag, p.err))) {
+        if (j > 0 && !__all_sync(0xffffffffu, mbar_wait_cl(&bar.stg_free, (j - 1) & 1, abort_flag, p.err, p.wait_ns))) {
           ok = false;
           break;
         }
@@ -430,7 +450,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         bool okp = true;
         if (lane == 0) {
           // P slot sb of the output CTA was last read by P.V of tile j-2
-          okp = j < kNP || mbar_wait_cl(&bar.p_free[sb], ((j - kNP) / kNP) & 1, abort_flag, p.err);
+          okp = j < kNP || mbar_wait_cl(&bar.p_free[sb], ((j - kNP) / kNP) & 1, abort_flag, p.err, p.wait_ns);
           if (okp) {
             bulk_s2peer(p_dst + sb * kPSlot + wq * kPWarpBytes, stg + wq * kPWarpBytes, kPWarpBytes, pfull_dst + sb * 8);
           }
@@ -464,7 +484,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         const int bl = lane < 4 ? bl0 : -1;
         const unsigned live = __ballot_sync(0xffffffffu, bl >= 0);
         bool okw = true;
-        if (lane == 0 && c >= kNV) okw = mbar_wait(&bar.v_empty[s], ((c / kNV) - 1) & 1, abort_flag, p.err);
+        if (lane == 0 && c >= kNV) okw = mbar_wait(&bar.v_empty[s], ((c / kNV) - 1) & 1, abort_flag, p.err, p.wait_ns);
         if (!__shfl_sync(0xffffffffu, okw, 0)) break;
         if (lane == 0) mbar_arrive_expect_tx(&bar.v_full[s], __popc(live) * kVPageBytes);
         __syncwarp();
@@ -483,7 +503,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
       const int n_st = 2 * n_tiles;
       for (int c = 0; ok && c < n_st; ++c) {
         const int s = c % kNV, j = c >> 1, e = c & 1;
-        ok = __all_sync(0xffffffffu, mbar_wait(&bar.v_full[s], (c / kNV) & 1, abort_flag, p.err));
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar.v_full[s], (c / kNV) & 1, abort_flag, p.err, p.wait_ns));
         if (!ok) break;
         const int kb = c * kVN;
         const int v1 = min(min(kb + kVN, ((k_hi >> 4) + 1) * kPage), ctx_end);
@@ -503,8 +523,8 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
           continue;
         }
         // rank 3's half is ready; at a tile's first half, both CTAs have P_j and have applied alpha
-        ok = __all_sync(0xffffffffu, mbar_wait_cl(&bar.v_ready[s], (c / kNV) & 1, abort_flag, p.err) &&
-                                         (e == 1 || mbar_wait_cl(&bar.o_ready[j % kNP], (j / kNP) & 1, abort_flag, p.err)));
+        ok = __all_sync(0xffffffffu, mbar_wait_cl(&bar.v_ready[s], (c / kNV) & 1, abort_flag, p.err, p.wait_ns) &&
+                                         (e == 1 || mbar_wait_cl(&bar.o_ready[j % kNP], (j / kNP) & 1, abort_flag, p.err, p.wait_ns)));
         if (!ok) break;
         tc_fence_after();
         if (lane == 0) {
@@ -533,7 +553,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int j = 0; j < n_tiles; ++j) {
         const int sb = j % kNP;
-        if (!__all_sync(0xffffffffu, mbar_wait_cl(&bar.p_full[sb], (j / kNP) & 1, abort_flag, p.err))) {
+        if (!__all_sync(0xffffffffu, mbar_wait_cl(&bar.p_full[sb], (j / kNP) & 1, abort_flag, p.err, p.wait_ns))) {
           ok = false;
           break;
         }
@@ -547,7 +567,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         const bool need = j > 0 && ax.x != 1.f;
         if (__any_sync(0xffffffffu, need)) {   // O correction, after P_{j-1} V_{j-1} has landed
           const int jp = j - 1;
-          if (!__all_sync(0xffffffffu, mbar_wait(&bar.pv_done[jp % kNP], (jp / kNP) & 1, abort_flag, p.err))) {
+          if (!__all_sync(0xffffffffu, mbar_wait(&bar.pv_done[jp % kNP], (jp / kNP) & 1, abort_flag, p.err, p.wait_ns))) {
             ok = false;
             break;
           }
@@ -570,13 +590,13 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
       }
       // Epilogue: O / l -> bf16, rows of this sequence only. A tile whose 128 rows all belong to
       // the sequence is staged in the V ring, idle once the last P.V has completed, as the eight
-      // 128B-swizzled boxes (64 dims x 128 rows) of the query tensor map, and written by eight
+      // 128B-swizzled boxes (64 dims x 128 rows) of the output tensor map, and written by eight
       // TMA stores; any other tile is written row by row, so that rows of other sequences and
       // padding are never touched.
       const int jl = n_tiles - 1;
       const bool staged = p_lo == kBM * t && p_hi == kBM * t + kBM - 1;
       uint8_t* const ep = base + ((1024u - (smem_u32(base) & 1023u)) & 1023u);   // box-aligned
-      bool ok_ep = ok && __all_sync(0xffffffffu, mbar_wait(&bar.pv_done[jl % kNP], (jl / kNP) & 1, abort_flag, p.err));
+      bool ok_ep = ok && __all_sync(0xffffffffu, mbar_wait(&bar.pv_done[jl % kNP], (jl / kNP) & 1, abort_flag, p.err, p.wait_ns));
       if (ok_ep) {
         tc_fence_after();
         const float inv = (l_last > 0.f) ? __frcp_rn(l_last) : 0.f;
@@ -612,9 +632,9 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         fence_proxy_async();
         __syncwarp();
         if (lane == 0 && ok_ep) mbar_arrive(&bar.ep_staged);
-        if (threadIdx.x == 64 && ok_ep && mbar_wait(&bar.ep_staged, 0, abort_flag, p.err)) {
+        if (threadIdx.x == 64 && ok_ep && mbar_wait(&bar.ep_staged, 0, abort_flag, p.err, p.wait_ns)) {
 #pragma unroll
-          for (int c = 0; c < kGD / 64; ++c) tma_store_3d(&tmap_q, ep + c * kQChunk, 64 * c, h, q_row0);
+          for (int c = 0; c < kGD / 64; ++c) tma_store_3d(&tmap_o, ep + c * kQChunk, 64 * c, h, q_row0);
           bulk_commit_group();
           bulk_wait_group_read0();   // the staging has been read; the writes complete on their own
         }
@@ -627,7 +647,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         const uint32_t pfree_dst = map_peer(smem_u32(&bar.p_free[0]), partner);
         for (int j = 0; j < n_tiles; ++j) {
-          if (!mbar_wait(&bar.pv_done[j % kNP], (j / kNP) & 1, abort_flag, p.err)) break;
+          if (!mbar_wait(&bar.pv_done[j % kNP], (j / kNP) & 1, abort_flag, p.err, p.wait_ns)) break;
           if (j + kNP < n_tiles) {
             mbar_arrive_expect_tx(&bar.p_full[j % kNP], kPSendBytes);
             mbar_arrive_remote(pfree_dst + (j % kNP) * 8);
@@ -725,7 +745,7 @@ bool page_maps(CUtensorMap* ms, CUtensorMap* mr, const void* s_cache, const void
 }  // namespace
 
 cudaError_t launch_prefill_global(const SeqRows& rows, float scale_log2, const PagedCache& cache, void* out,
-                                  const DeviceState& st, cudaStream_t s) {
+                                  const DeviceState& st, cudaStream_t s, const void* q_raw) {
   PrefillParams p{};
   p.rows = rows;
   p.window = 0;
@@ -739,23 +759,28 @@ cudaError_t launch_prefill_global(const SeqRows& rows, float scale_log2, const P
   p.out = (__nv_bfloat16*)out;
   p.tb = st.global;
   p.err = st.err;
-  CUtensorMap mq, ms, mr;
-  if (!q_map(&mq, out, rows.T, kGlobalHq, kGD)) return cudaErrorInvalidValue;
+  p.wait_ns = wait_limit_ns();
+  // Raw queries are rotated in the kernel; otherwise the staged roped queries are read from `out`.
+  if (rows.span && q_raw) return cudaErrorInvalidValue;
+  CUtensorMap mq, mo, ms, mr;   // queries (raw or staged), output rows, the cache's S and k_rot pages
+  if (!q_map(&mq, q_raw ? q_raw : out, rows.T, kGlobalHq, kGD)) return cudaErrorInvalidValue;
+  if (!q_map(&mo, out, rows.T, kGlobalHq, kGD)) return cudaErrorInvalidValue;
   if (!page_maps(&ms, &mr, cache.k, cache.krot, cache.num_pages)) return cudaErrorInvalidValue;
-  static bool attr[64] = {};
+  auto kernel = q_raw ? prefill_global_kernel<true> : prefill_global_kernel<false>;
+  const int ki = q_raw ? 1 : 0;
+  static bool attr[64][2] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!attr[dev]) {
-    cudaError_t e =
-        cudaFuncSetAttribute(prefill_global_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGlobalSmemBytes);
+  if (!attr[dev][ki]) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGlobalSmemBytes);
     if (e != cudaSuccess) return e;
-    attr[dev] = true;
+    attr[dev][ki] = true;
   }
   const long long slots = (long long)rows.T / kBM + 2LL * rows.B;
   const long long blocks = slots * (kGlobalHq / 2) * 4;   // a cluster of four CTAs per (query tile, head pair)
   if (blocks <= 0 || blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-  prefill_global_kernel<<<(unsigned)blocks, kThreads, kGlobalSmemBytes, s>>>(mq, ms, mr, p);
+  kernel<<<(unsigned)blocks, kThreads, kGlobalSmemBytes, s>>>(mq, mo, ms, mr, p);
   return cudaGetLastError();
 }
 

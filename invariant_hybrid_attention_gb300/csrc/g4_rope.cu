@@ -14,6 +14,7 @@
 // are static device arrays: the library allocates no device memory.
 #include <math.h>
 
+#include <atomic>
 #include <mutex>
 #include <type_traits>
 #include <vector>
@@ -28,13 +29,27 @@ static __device__ float2 g_rope_sliding_fine[kSlidingR * kRopeFine];
 static __device__ float2 g_rope_global_coarse[kGlobalR * kRopeCoarse];
 static __device__ float2 g_rope_global_mid[kGlobalR * kRopeMid];
 static __device__ float2 g_rope_global_fine[kGlobalR * kRopeFine];
+static __device__ float2 g_rope_sliding_coarse_t[kRopeCoarse * kSlidingR];
+static __device__ float2 g_rope_sliding_mid_t[kRopeMid * kSlidingR];
+static __device__ float2 g_rope_sliding_fine_t[kRopeFine * kSlidingR];
+static __device__ float2 g_rope_global_coarse_t[kRopeCoarse * kGlobalR];
+static __device__ float2 g_rope_global_mid_t[kRopeMid * kGlobalR];
+static __device__ float2 g_rope_global_fine_t[kRopeFine * kGlobalR];
 static __device__ uint32_t g_error_word;
 
 namespace {
 
 struct HostTables {
   std::vector<float2> coarse, mid, fine;
+  std::vector<float2> coarse_t, mid_t, fine_t;   // the same values, entry-major
 };
+
+std::vector<float2> transpose(const std::vector<float2>& a, int rows, int cols) {
+  std::vector<float2> t(a.size());
+  for (int i = 0; i < rows; ++i)
+    for (int j = 0; j < cols; ++j) t[(size_t)j * rows + i] = a[(size_t)i * cols + j];
+  return t;
+}
 
 void build_tables(int D, int R, double theta, HostTables& h) {
   h.coarse.resize((size_t)R * kRopeCoarse);
@@ -47,14 +62,21 @@ void build_tables(int D, int R, double theta, HostTables& h) {
     for (int a = 0; a < kRopeMid; ++a) h.mid[(size_t)t * kRopeMid + a] = cs((16.0 * a) * f);
     for (int b = 0; b < kRopeFine; ++b) h.fine[(size_t)t * kRopeFine + b] = cs((double)b * f);
   }
+  h.coarse_t = transpose(h.coarse, R, kRopeCoarse);
+  h.mid_t = transpose(h.mid, R, kRopeMid);
+  h.fine_t = transpose(h.fine, R, kRopeFine);
 }
 
 constexpr int kMaxDevices = 64;
+std::atomic<unsigned long long> g_wait_ns{kWaitLimitNs};
 std::mutex g_state_mutex;
 bool g_state_ready[kMaxDevices];
 DeviceState g_state[kMaxDevices];
 
 }  // namespace
+
+unsigned long long wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
+void set_wait_limit_ns(unsigned long long ns) { g_wait_ns.store(ns, std::memory_order_relaxed); }
 
 cudaError_t device_state(DeviceState* st) {
   int dev = 0;
@@ -81,12 +103,24 @@ cudaError_t device_state(DeviceState* st) {
     G4_UPLOAD(g_rope_global_coarse, hg.coarse);
     G4_UPLOAD(g_rope_global_mid, hg.mid);
     G4_UPLOAD(g_rope_global_fine, hg.fine);
+    G4_UPLOAD(g_rope_sliding_coarse_t, hs.coarse_t);
+    G4_UPLOAD(g_rope_sliding_mid_t, hs.mid_t);
+    G4_UPLOAD(g_rope_sliding_fine_t, hs.fine_t);
+    G4_UPLOAD(g_rope_global_coarse_t, hg.coarse_t);
+    G4_UPLOAD(g_rope_global_mid_t, hg.mid_t);
+    G4_UPLOAD(g_rope_global_fine_t, hg.fine_t);
     G4_ADDR(g_rope_sliding_coarse, s.sliding.coarse);
     G4_ADDR(g_rope_sliding_mid, s.sliding.mid);
     G4_ADDR(g_rope_sliding_fine, s.sliding.fine);
     G4_ADDR(g_rope_global_coarse, s.global.coarse);
     G4_ADDR(g_rope_global_mid, s.global.mid);
     G4_ADDR(g_rope_global_fine, s.global.fine);
+    G4_ADDR(g_rope_sliding_coarse_t, s.sliding.coarse_t);
+    G4_ADDR(g_rope_sliding_mid_t, s.sliding.mid_t);
+    G4_ADDR(g_rope_sliding_fine_t, s.sliding.fine_t);
+    G4_ADDR(g_rope_global_coarse_t, s.global.coarse_t);
+    G4_ADDR(g_rope_global_mid_t, s.global.mid_t);
+    G4_ADDR(g_rope_global_fine_t, s.global.fine_t);
 #undef G4_UPLOAD
 #undef G4_ADDR
     const uint32_t zero = 0;

@@ -108,8 +108,10 @@ class Batch:
         return t
 
     def run(self, layer, out_fill=float("nan"), split=False, norms=None):
-        """One prefill of the batch: g4attn_prefill, or (split) its two steps called apart; with
-        spans, g4attn_prefill_vision."""
+        """One prefill of the batch: g4attn_prefill; split="append": g4attn_kv_append then
+        g4attn_prefill_attend on the raw queries (the launches of g4attn_prefill called apart);
+        split=True: the staged form, g4attn_prefill_stage then g4attn_prefill_attend on the staged
+        queries; with spans, g4attn_prefill_vision."""
         cache = self.device_cache()
         table = self.plan.table.cuda()
         self.append_history(layer, cache, table, norms)
@@ -123,9 +125,12 @@ class Batch:
                                      self.span_rows().cuda(), cache.desc, table, out)
         elif norms is not None:
             g4.g4attn_prefill_normed(layer, norms.arg, q, k, v, *rows, cache.desc, table, out)
-        elif split:
+        elif split == "append":   # the two launches of g4attn_prefill called apart
+            g4.g4attn_kv_append(layer, k, v, *rows, cache.desc, table)
+            g4.g4attn_prefill_attend(layer, q, *rows, cache.desc, table, out)
+        elif split:               # the staged form: roped queries staged in out, then attention
             g4.g4attn_prefill_stage(layer, q, k, v, *rows, cache.desc, table, out)
-            g4.g4attn_prefill_attend(layer, *rows, cache.desc, table, out)
+            g4.g4attn_prefill_attend(layer, None, *rows, cache.desc, table, out)
         else:
             g4.g4attn_prefill(layer, q, k, v, *rows, cache.desc, table, out)
         torch.cuda.synchronize()

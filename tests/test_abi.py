@@ -195,10 +195,13 @@ def test_split_steps_append_and_new_calls_refused_on_host(lib):
     assert lib.g4attn_prefill_stage(L(s), 16, 16, 16, 8, 16, 16, 16, 1, L(cs), 16, 1, 24, None) == g4.G4_ERR_INVALID
     assert lib.g4attn_prefill_stage(L(bad), 16, 16, 16, 8, 16, 16, 16, 1, L(cs), 16, 1, 16, None) == \
         g4.G4_ERR_UNSUPPORTED
-    # g4attn_prefill_attend: NULL q_start; B = 0; unsupported geometry
-    assert lib.g4attn_prefill_attend(L(s), 8, None, 16, 16, 1, L(cs), 16, 1, 16, None) == g4.G4_ERR_INVALID
-    assert lib.g4attn_prefill_attend(L(s), 8, 16, 16, 16, 0, L(cs), 16, 1, 16, None) == g4.G4_ERR_INVALID
-    assert lib.g4attn_prefill_attend(L(bad), 8, 16, 16, 16, 1, L(cs), 16, 1, 16, None) == g4.G4_ERR_UNSUPPORTED
+    # g4attn_prefill_attend: NULL q_start; B = 0; unsupported geometry; misaligned raw queries
+    assert lib.g4attn_prefill_attend(L(s), None, 8, None, 16, 16, 1, L(cs), 16, 1, 16, None) == g4.G4_ERR_INVALID
+    assert lib.g4attn_prefill_attend(L(s), None, 8, 16, 16, 16, 0, L(cs), 16, 1, 16, None) == g4.G4_ERR_INVALID
+    assert lib.g4attn_prefill_attend(L(bad), None, 8, 16, 16, 16, 1, L(cs), 16, 1, 16, None) == \
+        g4.G4_ERR_UNSUPPORTED
+    # raw queries off a 16-byte boundary
+    assert lib.g4attn_prefill_attend(L(s), 24, 8, 16, 16, 16, 1, L(cs), 16, 1, 16, None) == g4.G4_ERR_INVALID
     # g4attn_kv_append: a V tensor on a K==V layer; no V on a sliding layer; negative T
     assert lib.g4attn_kv_append(L(gl), 16, 16, 8, 16, 16, 16, 1, L(cg), 16, 1, None) == g4.G4_ERR_INVALID
     assert lib.g4attn_kv_append(L(s), 16, None, 8, 16, 16, 16, 1, L(cs), 16, 1, None) == g4.G4_ERR_INVALID
@@ -268,3 +271,18 @@ def test_decode_static_scratch_limit(lib):
     bad.head_dim = 256
     assert lib.g4attn_decode_static(ctypes.byref(bad), 16, 16, None, 16, 1, ctypes.byref(cache), 16, 8, 16,
                                     None) == g4.G4_ERR_UNSUPPORTED
+
+
+def test_wait_limit_is_set_and_read_on_the_host(lib):
+    """The kernels' wait bound is a host setting read at each launch: 0 .. 2e9 ns, 2 s by default;
+    larger values are refused and leave it unchanged. No CUDA call is involved."""
+    assert lib.g4attn_wait_limit_ns() == g4.DEFAULT_WAIT_LIMIT_NS
+    try:
+        assert lib.g4attn_set_wait_limit_ns(1000) == g4.G4_OK
+        assert lib.g4attn_wait_limit_ns() == 1000
+        assert lib.g4attn_set_wait_limit_ns(g4.DEFAULT_WAIT_LIMIT_NS + 1) == g4.G4_ERR_INVALID
+        assert lib.g4attn_wait_limit_ns() == 1000
+        assert lib.g4attn_set_wait_limit_ns(0) == g4.G4_OK
+        assert lib.g4attn_wait_limit_ns() == 0
+    finally:
+        assert lib.g4attn_set_wait_limit_ns(g4.DEFAULT_WAIT_LIMIT_NS) == g4.G4_OK

@@ -218,16 +218,23 @@ def test_prefill_global_batch_invariance():
         assert torch.equal(out_a[:L].cpu(), out_b[s:s + L].cpu()), (lens, padded, at)
 
 
+@pytest.mark.parametrize("padded", [False, True], ids=["packed", "padded"])
 @pytest.mark.parametrize("kind", ["sliding", "global"])
-def test_prefill_split_steps_equal_prefill(kind):
-    """g4attn_prefill_stage then g4attn_prefill_attend give exactly g4attn_prefill's bits."""
+def test_prefill_split_steps_equal_prefill(kind, padded):
+    """The queries rotated inside the attention kernel (g4attn_prefill, or g4attn_kv_append then
+    g4attn_prefill_attend on the raw queries) and the staged form (g4attn_prefill_stage writes the
+    roped queries into out, g4attn_prefill_attend reads them there) give the same bits: the same
+    angles, rotation and bf16 cast at the declared roped-q cast point."""
     layer, _ = layers(kind, 1024)
     lens, starts = [300, 1, 129, 700], [0, 40, 256, 1000]
-    whole, cache_a = Batch(kind, lens, ctx_starts=starts, seed=21, scale=0.5).run(layer)
-    split, cache_b = Batch(kind, lens, ctx_starts=starts, seed=21, scale=0.5).run(layer, split=True)
-    # bit patterns: rows outside every sequence and unwritten cache slots hold NaN in both
-    assert torch.equal(whole.cpu().view(torch.int16), split.cpu().view(torch.int16))
-    assert torch.equal(cache_a.k.cpu().view(torch.int16), cache_b.k.cpu().view(torch.int16))
+    mk = lambda: Batch(kind, lens, ctx_starts=starts, padded=padded, seed=21, scale=0.5)
+    whole, cache_a = mk().run(layer)
+    staged, cache_b = mk().run(layer, split=True)
+    apart, cache_c = mk().run(layer, split="append")
+    # bit patterns: rows outside every sequence and unwritten cache slots hold NaN in all three
+    for other, cache in ((staged, cache_b), (apart, cache_c)):
+        assert torch.equal(whole.cpu().view(torch.int16), other.cpu().view(torch.int16))
+        assert torch.equal(cache_a.k.cpu().view(torch.int16), cache.k.cpu().view(torch.int16))
 
 
 @pytest.mark.parametrize("kind", ["sliding", "global"])
