@@ -93,7 +93,7 @@ __global__ void __launch_bounds__(128, 2) decode_sliding_kernel(DecodeParams p) 
     issued[threadIdx.x] = 0;
   }
   fence_mbar_init();
-  const size_t slot = (((size_t)b * kSlidingHq + 2 * g) * p.NC + cr);
+  const size_t slot = (((size_t)b * p.cache.hq + 2 * g) * p.NC + cr);
   if (__syncthreads_or(bad)) {
     if (threadIdx.x == 0) {
       set_error(p.err, kErrPage);
@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(128, 2) decode_sliding_kernel(DecodeParams p) 
   const __nv_bfloat16* vc = (const __nv_bfloat16*)p.cache.v;
   auto issue = [&](int i) {   // one thread
     const int st = i % kSStages;
-    const size_t blk = (size_t)pt[pg0 + i] * kSlidingHkv + g;
+    const size_t blk = (size_t)pt[pg0 + i] * p.cache.hkv + g;
     uint8_t* dst = ring + st * kSStageBytes;
     mbar_arrive_expect_tx(&full[st], kSStageBytes);
     bulk_g2s(dst, kc + blk * kPage * kSD, kSPageBytes, &full[st]);
@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(128, 2) decode_sliding_kernel(DecodeParams p) 
 #pragma unroll
   for (int ks = 0; ks < 16; ++ks) qb[ks][0] = qb[ks][1] = 0u;
   if (gq < 2) {
-    const __nv_bfloat16* qr = p.q + ((size_t)b * kSlidingHq + 2 * g + gq) * kSD;
+    const __nv_bfloat16* qr = p.q + ((size_t)b * p.cache.hq + 2 * g + gq) * kSD;
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
 #pragma unroll
@@ -351,7 +351,8 @@ __global__ void __launch_bounds__(128, 2) decode_global_kernel(DecodeParams p) {
   const int k_end = min(pos, k_begin + kDecodeChunkGlobal - 1);
   const int pg0 = k_begin >> 4, pg1 = k_end >> 4;
   const int32_t* pt = p.cache.page_table + (size_t)b * p.cache.max_pages;
-  const size_t slot = ((size_t)b * kGlobalHq + 8 * g) * p.NC + c;   // head 8g + j adds j * NC
+  const int G = p.cache.hq / p.cache.hkv;   // query heads of KV head g: 8, or 4 on a tp = 8 rank slice
+  const size_t slot = ((size_t)b * p.cache.hq + G * g) * p.NC + c;   // head G g + j adds j * NC
 
   bool bad = false;
   for (int i = pg0 + (int)threadIdx.x; i <= pg1; i += 128) {
@@ -367,7 +368,7 @@ __global__ void __launch_bounds__(128, 2) decode_global_kernel(DecodeParams p) {
   if (__syncthreads_or(bad)) {
     if (threadIdx.x == 0) {
       set_error(p.err, kErrPage);
-      for (int j = 0; j < 8; ++j) {
+      for (int j = 0; j < G; ++j) {
         p.ws_ml[(slot + (size_t)j * p.NC) * 2 + 0] = -INFINITY;
         p.ws_ml[(slot + (size_t)j * p.NC) * 2 + 1] = 0.f;
       }
@@ -380,7 +381,7 @@ __global__ void __launch_bounds__(128, 2) decode_global_kernel(DecodeParams p) {
   const __nv_bfloat16* rc = (const __nv_bfloat16*)p.cache.krot;
   auto issue = [&](int i) {   // one thread
     const int st = i % kGStages;
-    const size_t blk = (size_t)pt[pg0 + i] * kGlobalHkv + g;
+    const size_t blk = (size_t)pt[pg0 + i] * p.cache.hkv + g;
     uint8_t* dst = stage_base + st * kGStageBytes;
     mbar_arrive_expect_tx(&full[st], kGStageBytes);
     bulk_g2s(dst, sc + blk * kPage * kGD, kGSBytes, &full[st]);
@@ -391,12 +392,17 @@ __global__ void __launch_bounds__(128, 2) decode_global_kernel(DecodeParams p) {
   if (threadIdx.x == 0)
     for (int i = 0; i < min(kGStages, n_pages); ++i) issue(i);
 
-  // Stage the 8 roped query heads (bf16) while the first pages are in flight.
+  // Stage the G roped query heads (bf16) while the first pages are in flight; the columns of the
+  // MMA past G (a rank slice's 4 heads) carry q = 0 and are never read out.
   {
-    const __nv_bfloat16* qb = p.q + ((size_t)b * kGlobalHq + 8 * g) * kGD;
+    const __nv_bfloat16* qb = p.q + ((size_t)b * p.cache.hq + G * g) * kGD;
     for (int idx = threadIdx.x; idx < 8 * (kGD / 2); idx += 128) {
       const int h = idx / (kGD / 2), t = idx % (kGD / 2);
-      float x = bf16_to_f(qb[h * kGD + t]), y = bf16_to_f(qb[h * kGD + t + kGD / 2]);
+      float x = 0.f, y = 0.f;
+      if (h < G) {
+        x = bf16_to_f(qb[h * kGD + t]);
+        y = bf16_to_f(qb[h * kGD + t + kGD / 2]);
+      }
       if (t < kGlobalR) rope_pair(x, y, rope_cs(p.tb, t, pos));
       *reinterpret_cast<__nv_bfloat16*>(q_s + h * kGRow + t * 2) = __float2bfloat16_rn(x);
       *reinterpret_cast<__nv_bfloat16*>(q_s + h * kGRow + (t + kGD / 2) * 2) = __float2bfloat16_rn(y);
@@ -565,7 +571,7 @@ __global__ void __launch_bounds__(128, 2) decode_global_kernel(DecodeParams p) {
     }
   }
   __syncthreads();
-  for (int idx = threadIdx.x; idx < 8 * kGD; idx += 128) {
+  for (int idx = threadIdx.x; idx < G * kGD; idx += 128) {
     const int h = idx / kGD, d = idx % kGD;
     float M = red_m[0][h];
 #pragma unroll
@@ -636,11 +642,11 @@ int decode_chunks(bool global, int max_pages, int window) {
 
 }  // namespace
 
-size_t decode_workspace_bytes(bool global, int B, int max_pages, int window) {
+size_t decode_workspace_bytes(bool global, int B, int max_pages, int window, int hq) {
   const size_t nc = (size_t)decode_chunks(global, max_pages, window);
   const size_t D = global ? kGD : kSD;
-  const size_t ml = ((size_t)B * 32 * nc * 2 * sizeof(float) + 255) / 256 * 256;
-  return ml + (size_t)B * 32 * nc * D * sizeof(float);
+  const size_t ml = ((size_t)B * hq * nc * 2 * sizeof(float) + 255) / 256 * 256;
+  return ml + (size_t)B * hq * nc * D * sizeof(float);
 }
 
 // A decode step laid out as B one-row prefill chunks: request b's query is row b, at position
@@ -672,7 +678,7 @@ cudaError_t launch_decode(bool global, const void* q, const int32_t* seq_len, in
   p.scale_log2 = scale_log2;
   p.cache = cache;
   p.NC = decode_chunks(global, cache.max_pages, window);
-  const size_t ml = ((size_t)B * 32 * p.NC * 2 * sizeof(float) + 255) / 256 * 256;
+  const size_t ml = ((size_t)B * cache.hq * p.NC * 2 * sizeof(float) + 255) / 256 * 256;
   p.ws_ml = (float*)ws;
   p.ws_o = (float*)((uint8_t*)ws + ml);
   p.err = st.err;
@@ -687,10 +693,10 @@ cudaError_t launch_decode(bool global, const void* q, const int32_t* seq_len, in
       if (e != cudaSuccess) return e;
       attr_set[dev] = true;
     }
-    decode_global_kernel<<<dim3(p.NC, kGlobalHkv, B), 128, kGSmem, s>>>(p);
+    decode_global_kernel<<<dim3(p.NC, cache.hkv, B), 128, kGSmem, s>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    decode_merge_kernel<kGD><<<dim3(kGlobalHq, B), kGD / 4, 0, s>>>(p.ws_ml, p.ws_o, seq_len, p.NC, 0,
+    decode_merge_kernel<kGD><<<dim3(cache.hq, B), kGD / 4, 0, s>>>(p.ws_ml, p.ws_o, seq_len, p.NC, 0,
                                                                     kDecodeChunkGlobal, (__nv_bfloat16*)out);
   } else {
     p.tb = st.sliding;
@@ -702,10 +708,10 @@ cudaError_t launch_decode(bool global, const void* q, const int32_t* seq_len, in
       if (e != cudaSuccess) return e;
       attr_set_s[dev] = true;
     }
-    decode_sliding_kernel<<<dim3(p.NC, kSlidingHkv, B), 128, kSSmem, s>>>(p);
+    decode_sliding_kernel<<<dim3(p.NC, cache.hkv, B), 128, kSSmem, s>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    decode_merge_kernel<kSD><<<dim3(kSlidingHq, B), kSD / 4, 0, s>>>(p.ws_ml, p.ws_o, seq_len, p.NC, window,
+    decode_merge_kernel<kSD><<<dim3(cache.hq, B), kSD / 4, 0, s>>>(p.ws_ml, p.ws_o, seq_len, p.NC, window,
                                                                     kDecodeChunkSliding, (__nv_bfloat16*)out);
   }
   return cudaGetLastError();

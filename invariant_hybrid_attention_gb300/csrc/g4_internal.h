@@ -37,6 +37,10 @@ struct SeqRows {
   const int32_t* span = nullptr;
 };
 
+// A layer's paged cache and the head counts of the call: hkv KV heads in the cache (its page-head
+// blocks), hq query heads in the q and out rows. The full geometry has 32 / 16 (sliding) or 32 / 4
+// (global); a tensor-parallel rank slice has 32 / tp query heads and 16 / tp or max(1, 4 / tp) KV
+// heads.
 struct PagedCache {
   void* k;
   void* v;
@@ -44,6 +48,8 @@ struct PagedCache {
   int32_t num_pages;
   const int32_t* page_table;
   int32_t max_pages;
+  int32_t hq = 32;
+  int32_t hkv = 16;
 };
 
 // Optional per-head RMS norms of a prefill or decode (device pointers to bf16 [D] weights; a null
@@ -70,10 +76,11 @@ cudaError_t launch_append_decode(bool global, const void* k_new, const void* v_n
                                  const NormArgs& nm = NormArgs{});
 
 // The decode queries' norms, written to out (bf16), for the decode kernel to read as its q.
-cudaError_t launch_norm_queries(bool global, const void* q, void* out, int B, const NormArgs& nm, cudaStream_t s);
+cudaError_t launch_norm_queries(bool global, const void* q, void* out, int B, int hq, const NormArgs& nm,
+                                cudaStream_t s);
 
-// Decode partials + ordered merge. ws must hold decode_workspace_bytes(global, B, max_pages).
-size_t decode_workspace_bytes(bool global, int B, int max_pages, int window);
+// Decode partials + ordered merge. ws must hold decode_workspace_bytes(global, B, max_pages, window, hq).
+size_t decode_workspace_bytes(bool global, int B, int max_pages, int window, int hq);
 cudaError_t launch_decode(bool global, const void* q, const int32_t* seq_len, int B, int window,
                           float scale_log2, const PagedCache& cache, void* out, void* ws,
                           const DeviceState& st, cudaStream_t s);
@@ -86,7 +93,29 @@ cudaError_t launch_decode_rows(const int32_t* seq_len, int B, int32_t* rows, con
 // launch_append_prefill staged in `out` and writes the output rows over them.
 cudaError_t launch_prefill(bool global, const SeqRows& rows, int window, float scale_log2, const PagedCache& cache,
                            void* out, const DeviceState& st, cudaStream_t s, const void* q_raw = nullptr);
+// A partial global prefill (context parallelism over keys): sequence b attends only to its keys
+// key_begin[b] .. key_end[b]-1 (device int32 [B]); the rows' un-normalised output o (fp32
+// [T][hq][512]) and softmax state ml (fp32 [T][hq][2]) are written instead of bf16 output rows.
+struct PartialOut {
+  const int32_t* key_begin;
+  const int32_t* key_end;
+  float* o;
+  float* ml;
+};
 cudaError_t launch_prefill_global(const SeqRows& rows, float scale_log2, const PagedCache& cache, void* out,
-                                  const DeviceState& st, cudaStream_t s, const void* q_raw = nullptr);
+                                  const DeviceState& st, cudaStream_t s, const void* q_raw = nullptr,
+                                  const PartialOut* part = nullptr);
+
+// Merges n partials of a global prefill, in the order given, into bf16 output rows (the rows of
+// the sequences only): M = max m_r, then O = sum_r o_r 2^(m_r - M) and L = sum_r l_r 2^(m_r - M),
+// out = O / L.
+constexpr int kMaxParts = 8;
+struct PartialSet {
+  const float* o[kMaxParts];
+  const float* ml[kMaxParts];
+  int n;
+};
+cudaError_t launch_merge_partials(const PartialSet& parts, const SeqRows& rows, int hq, void* out, const DeviceState& st,
+                                  cudaStream_t s);
 
 }  // namespace g4

@@ -122,8 +122,8 @@ __device__ __forceinline__ void xpose_pieces(uint32_t (&w)[16], int lane) {
 }
 // Stores dims col0 .. col0+31 of the warp's 32 rows; row0 is the warp's first row (a row index
 // into `out`, may be out of range: only rows set in `valid` are written).
-__device__ __forceinline__ void store_rows32(uint32_t (&w)[16], __nv_bfloat16* out, long long row0, int h, int col0,
-                                             unsigned valid, int lane) {
+__device__ __forceinline__ void store_rows32(uint32_t (&w)[16], __nv_bfloat16* out, long long row0, int hq, int h,
+                                             int col0, unsigned valid, int lane) {
   xpose_pieces<1>(w, lane);
   xpose_pieces<2>(w, lane);
   const int a = lane >> 2, i = lane & 3;
@@ -131,7 +131,7 @@ __device__ __forceinline__ void store_rows32(uint32_t (&w)[16], __nv_bfloat16* o
   for (int t = 0; t < 4; ++t) {
     const int row = 4 * a + t;
     if ((valid >> row) & 1u) {
-      __nv_bfloat16* dst = out + ((row0 + row) * kSlidingHq + h) * kSD + col0 + 8 * i;
+      __nv_bfloat16* dst = out + ((row0 + row) * hq + h) * kSD + col0 + 8 * i;
       *reinterpret_cast<uint4*>(dst) = make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
     }
   }
@@ -150,10 +150,10 @@ struct Unit {
 // Not inlined: six roles call it, once per unit. kSpan: the batch may hold image rows.
 template <bool kSpan>
 __device__ __noinline__ bool sliding_unit(const PrefillParams& p, int u, uint32_t rank, Unit& o) {
-  o.g = u % kSlidingHkv;
+  o.g = u % p.hkv;
   o.h = 2 * o.g + (int)rank;
   int b, t, f[3];
-  find_unit(p.rows, u / kSlidingHkv, b, t, p.err, f);
+  find_unit(p.rows, u / p.hkv, b, t, p.err, f);
   if (b < 0) return false;
   const int cs = f[0], L = f[1], qs = f[2];
   o.t = t;
@@ -284,10 +284,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       bool have_n = false;
       int nraw0 = kNoPage, nraw1 = kNoPage;
       auto load_blocks = [&](int j0) -> int {
-        return page_check(raw_blocks(un, j0), p.num_pages, kSlidingHkv, un.g, p.err);
+        return page_check(raw_blocks(un, j0), p.num_pages, p.hkv, un.g, p.err);
       };
-      int blk_cur = page_check(raw0, p.num_pages, kSlidingHkv, un.g, p.err);
-      int blk_next = page_check(raw1, p.num_pages, kSlidingHkv, un.g, p.err);
+      int blk_cur = page_check(raw0, p.num_pages, p.hkv, un.g, p.err);
+      int blk_next = page_check(raw1, p.num_pages, p.hkv, un.g, p.err);
       const int n_slots = is_v ? un.n_tiles : un.n_tiles + 1;
       for (int idx = 0; idx < n_slots; ++idx, ++c) {
         const int s = c % n_st;
@@ -685,7 +685,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 16; ++c)
           w16[c] = pack_bf16(__uint_as_float(o[2 * c]) * inv, __uint_as_float(o[2 * c + 1]) * inv);
-        store_rows32(w16, p.out, wrow0, cur.h, 32 * cc, valid, lane);
+        store_rows32(w16, p.out, wrow0, p.hq, cur.h, 32 * cc, valid, lane);
       }
       c0 = c0n;
       ++uq;
@@ -762,11 +762,13 @@ cudaError_t launch_prefill(bool global, const SeqRows& rows, int window, float s
   p.wait_ns = wait_limit_ns();
   p.k_cache = cache.k;
   p.v_cache = cache.v;
+  p.hq = cache.hq;
+  p.hkv = cache.hkv;
   // Raw queries are rotated in the kernel; otherwise the staged roped queries are read from `out`.
   // Image spans come only with staged queries.
   if (rows.span && q_raw) return cudaErrorInvalidValue;
   CUtensorMap mq;
-  if (!q_map(&mq, q_raw ? q_raw : out, rows.T, kSlidingHq, kSD)) return cudaErrorInvalidValue;
+  if (!q_map(&mq, q_raw ? q_raw : out, rows.T, cache.hq, kSD)) return cudaErrorInvalidValue;
   // Batches with image rows take their own instantiation, so that the plain one carries no span code.
   auto kernel = rows.span ? prefill_sliding_kernel<true, false>
                           : (q_raw ? prefill_sliding_kernel<false, true> : prefill_sliding_kernel<false, false>);
@@ -798,7 +800,7 @@ cudaError_t launch_prefill(bool global, const SeqRows& rows, int window, float s
     attr[dev][ki] = true;
   }
   const long long slots = (long long)rows.T / kBM + 2LL * rows.B;
-  const long long n_units = slots * kSlidingHkv;   // (query tile, KV head) units, one per cluster at a time
+  const long long n_units = slots * cache.hkv;   // (query tile, KV head) units, one per cluster at a time
   if (n_units <= 0 || n_units > 0x3fffffffLL) return cudaErrorInvalidValue;
   p.n_units = (int)n_units;
   const int n_clusters = (int)(n_units < max_clusters[dev][ki] ? n_units : max_clusters[dev][ki]);

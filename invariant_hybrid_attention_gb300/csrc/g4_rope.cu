@@ -388,11 +388,11 @@ cudaError_t launch_rope_apply(bool global, const void* x, const int32_t* pos, in
 // Writes one token's Hkv vectors into its page slot: sliding K' = bf16(RoPE(k)) and V as given;
 // global S as given (K==V: the one stored projection, rotated only where it is read as K).
 // cs: the lane's (cos, sin) at the token's position (rope_cs_lane); pos is in range.
-template <int D, int R, int HKV, bool SHARED, bool NORM>
+template <int D, int R, bool SHARED, bool NORM>
 __device__ __forceinline__ void append_token_cs(const __nv_bfloat16* k_row, const __nv_bfloat16* v_row, int b, int pos,
                                                 const PagedCache& c, const float2 (&cs)[8], uint32_t* err,
-                                                const NormArgs& nm, const float (&wk)[16], int g_begin = 0,
-                                                int g_end = HKV) {
+                                                const NormArgs& nm, const float (&wk)[16], int g_begin, int g_end) {
+  const int HKV = c.hkv;
   constexpr int VPW = 32 / (D / 16);   // vectors per warp instruction of rope_vec8_cs
   const int lane = threadIdx.x & 31;
   const int phys = c.page_table[(size_t)b * c.max_pages + (pos >> 4)];
@@ -456,10 +456,10 @@ __device__ __forceinline__ void append_token_cs(const __nv_bfloat16* k_row, cons
   }
 }
 
-template <int D, int R, int HKV, bool SHARED, bool NORM>
+template <int D, int R, bool SHARED, bool NORM>
 __device__ __forceinline__ void append_token(const __nv_bfloat16* k_row, const __nv_bfloat16* v_row, int b, int pos,
                                              const PagedCache& c, const RopeTables& tb, uint32_t* err,
-                                             const NormArgs& nm, int g_begin = 0, int g_end = HKV) {
+                                             const NormArgs& nm, int g_begin, int g_end) {
   const int lane = threadIdx.x & 31;
   if (pos < 0 || pos >= kMaxPos || (pos >> 4) >= c.max_pages) {
     if (lane == 0) set_error(err, kErrPos);
@@ -469,13 +469,13 @@ __device__ __forceinline__ void append_token(const __nv_bfloat16* k_row, const _
   rope_cs_lane8<D, R>(tb, pos, cs);
   float wk[16];
   if (NORM) lane_weights<D>(nm.wk, wk);
-  append_token_cs<D, R, HKV, SHARED, NORM>(k_row, v_row, b, pos, c, cs, err, nm, wk, g_begin, g_end);
+  append_token_cs<D, R, SHARED, NORM>(k_row, v_row, b, pos, c, cs, err, nm, wk, g_begin, g_end);
 }
 
 // One warp per row of the prefill batch; the owning sequence is found by a scan over B.
 // With q_out set, the row's query heads are also roped (declared bf16 cast) into q_out: the
 // attention kernel that follows reads its queries already rotated.
-template <int D, int R, int HKV, int HQ, bool SHARED, bool NORM>
+template <int D, int R, bool SHARED, bool NORM>
 __global__ void __launch_bounds__(256) append_prefill_kernel(const __nv_bfloat16* __restrict__ k,
                                                              const __nv_bfloat16* __restrict__ v,
                                                              const __nv_bfloat16* __restrict__ q,
@@ -483,6 +483,7 @@ __global__ void __launch_bounds__(256) append_prefill_kernel(const __nv_bfloat16
                                                              RopeTables tb, uint32_t* err, NormArgs nm, bool rows_kv) {
   const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
+  const int HQ = cache.hq, HKV = cache.hkv;
   if (r >= rows.T) return;
   int owner = -1;
   for (int b0 = 0; b0 < rows.B; b0 += 32) {
@@ -529,8 +530,8 @@ __global__ void __launch_bounds__(256) append_prefill_kernel(const __nv_bfloat16
     }
   }
   if (rows_kv)
-    append_token_cs<D, R, HKV, SHARED, NORM>(k + (size_t)r * HKV * D, SHARED ? nullptr : v + (size_t)r * HKV * D,
-                                             owner, pos, cache, cs, err, nm, wk);
+    append_token_cs<D, R, SHARED, NORM>(k + (size_t)r * HKV * D, SHARED ? nullptr : v + (size_t)r * HKV * D,
+                                        owner, pos, cache, cs, err, nm, wk, 0, HKV);
 }
 
 // ---- the sliding K'/V append by key groups ---------------------------------------------------------
@@ -582,14 +583,15 @@ __device__ __forceinline__ void find_group(const SeqRows& rows, int gi, int& out
   }
 }
 
-constexpr int kGroupHeads = 4;   // KV heads per warp of append_kv_groups_kernel
-
-template <int D, int R, int HKV>
+// kGroupHeads KV heads per warp (4; 2 for a cache of 2 KV heads, the sliding layer's tensor-parallel
+// rank slice at tp = 8).
+template <int D, int R, int kGroupHeads>
 __global__ void __launch_bounds__(256) append_kv_groups_kernel(const __nv_bfloat16* __restrict__ k,
                                                                const __nv_bfloat16* __restrict__ v, SeqRows rows,
                                                                PagedCache c, RopeTables tb, uint32_t* err) {
-  static_assert(D == 256 && R == 128 && HKV % kGroupHeads == 0, "the group path serves the sliding geometry");
+  static_assert(D == 256 && R == 128, "the group path serves the sliding geometry");
   const int lane = threadIdx.x & 31;
+  const int HKV = c.hkv;   // a multiple of kGroupHeads
   const int unit = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int gi = unit / (HKV / kGroupHeads), g0 = (unit % (HKV / kGroupHeads)) * kGroupHeads;
   int b, grp;
@@ -650,7 +652,7 @@ __global__ void __launch_bounds__(256) append_kv_groups_kernel(const __nv_bfloat
   }
 }
 
-template <int D, int R, int HKV, bool SHARED, bool NORM>
+template <int D, int R, bool SHARED, bool NORM>
 __global__ void __launch_bounds__(256) append_decode_kernel(const __nv_bfloat16* __restrict__ k,
                                                             const __nv_bfloat16* __restrict__ v,
                                                             const int32_t* __restrict__ seq_len, int B,
@@ -659,12 +661,13 @@ __global__ void __launch_bounds__(256) append_decode_kernel(const __nv_bfloat16*
   // One warp per (request, VPW KV heads): the heads of one request run in parallel, each with the
   // lane mapping and arithmetic of the one-warp-per-token append (so the same bits).
   constexpr int VPW = 32 / (D / 16);
-  constexpr int NC = HKV / VPW;
+  const int HKV = cache.hkv;   // a multiple of VPW
+  const int NC = HKV / VPW;
   const int unit = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (unit >= B * NC) return;
   const int b = unit / NC, g0 = (unit % NC) * VPW;
-  append_token<D, R, HKV, SHARED, NORM>(k + (size_t)b * HKV * D, SHARED ? nullptr : v + (size_t)b * HKV * D, b,
-                                        seq_len[b] - 1, cache, tb, err, nm, g0, g0 + VPW);
+  append_token<D, R, SHARED, NORM>(k + (size_t)b * HKV * D, SHARED ? nullptr : v + (size_t)b * HKV * D, b,
+                                   seq_len[b] - 1, cache, tb, err, nm, g0, g0 + VPW);
 }
 
 // The decode queries' norm (and, on a K==V layer with a key norm, the fold of w_k into their
@@ -695,23 +698,27 @@ cudaError_t launch_append_prefill(bool global, const void* k, const void* v, con
   __nv_bfloat16* qo = (__nv_bfloat16*)q_out;
   if (global) {
     if (nm.any())
-      append_prefill_kernel<kGlobalD, kGlobalR, kGlobalHkv, kGlobalHq, true, true>
+      append_prefill_kernel<kGlobalD, kGlobalR, true, true>
           <<<blocks, 256, 0, s>>>(kb, nullptr, qb, qo, rows, cache, st.global, st.err, nm, true);
     else
-      append_prefill_kernel<kGlobalD, kGlobalR, kGlobalHkv, kGlobalHq, true, false>
+      append_prefill_kernel<kGlobalD, kGlobalR, true, false>
           <<<blocks, 256, 0, s>>>(kb, nullptr, qb, qo, rows, cache, st.global, st.err, nm, true);
   } else if (nm.any()) {
-    append_prefill_kernel<kSlidingD, kSlidingR, kSlidingHkv, kSlidingHq, false, true>
+    append_prefill_kernel<kSlidingD, kSlidingR, false, true>
         <<<blocks, 256, 0, s>>>(kb, vb, qb, qo, rows, cache, st.sliding, st.err, nm, true);
   } else {
     // K' and V by key groups (whole-sector writes), the queries by rows.
+    const int gh = cache.hkv % 4 == 0 ? 4 : 2;   // KV heads per warp
     const long long groups = (long long)rows.T / 8 + 2LL * rows.B;   // a sequence adds at most two partial groups
-    const long long units = groups * (kSlidingHkv / kGroupHeads);
+    const long long units = groups * (cache.hkv / gh);
     if (units > 0x3fffffffLL) return cudaErrorInvalidValue;
-    append_kv_groups_kernel<kSlidingD, kSlidingR, kSlidingHkv>
-        <<<(unsigned)((units + 7) / 8), 256, 0, s>>>(kb, vb, rows, cache, st.sliding, st.err);
+    const unsigned gblocks = (unsigned)((units + 7) / 8);
+    if (gh == 4)
+      append_kv_groups_kernel<kSlidingD, kSlidingR, 4><<<gblocks, 256, 0, s>>>(kb, vb, rows, cache, st.sliding, st.err);
+    else
+      append_kv_groups_kernel<kSlidingD, kSlidingR, 2><<<gblocks, 256, 0, s>>>(kb, vb, rows, cache, st.sliding, st.err);
     if (qo != nullptr)
-      append_prefill_kernel<kSlidingD, kSlidingR, kSlidingHkv, kSlidingHq, false, false>
+      append_prefill_kernel<kSlidingD, kSlidingR, false, false>
           <<<blocks, 256, 0, s>>>(kb, vb, qb, qo, rows, cache, st.sliding, st.err, nm, false);
   }
   return cudaGetLastError();
@@ -721,31 +728,32 @@ cudaError_t launch_append_decode(bool global, const void* k_new, const void* v_n
                                  int B, const PagedCache& cache, const DeviceState& st, cudaStream_t s,
                                  const NormArgs& nm) {
   if (B <= 0) return cudaSuccess;
-  // warps: B x (KV heads / heads per warp instruction): 8 per request on sliding, 4 on global layers
-  const int per_req = global ? kGlobalHkv / (32 / (kGlobalD / 16)) : kSlidingHkv / (32 / (kSlidingD / 16));
+  // warps: B x (KV heads / heads per warp instruction)
+  const int per_req = cache.hkv / (32 / ((global ? kGlobalD : kSlidingD) / 16));
   const unsigned blocks = (unsigned)(((long long)B * per_req + 7) / 8);
   const __nv_bfloat16 *kb = (const __nv_bfloat16*)k_new, *vb = (const __nv_bfloat16*)v_new;
   if (global) {
     if (nm.any())
-      append_decode_kernel<kGlobalD, kGlobalR, kGlobalHkv, true, true>
+      append_decode_kernel<kGlobalD, kGlobalR, true, true>
           <<<blocks, 256, 0, s>>>(kb, nullptr, seq_len, B, cache, st.global, st.err, nm);
     else
-      append_decode_kernel<kGlobalD, kGlobalR, kGlobalHkv, true, false>
+      append_decode_kernel<kGlobalD, kGlobalR, true, false>
           <<<blocks, 256, 0, s>>>(kb, nullptr, seq_len, B, cache, st.global, st.err, nm);
   } else {
     if (nm.any())
-      append_decode_kernel<kSlidingD, kSlidingR, kSlidingHkv, false, true>
+      append_decode_kernel<kSlidingD, kSlidingR, false, true>
           <<<blocks, 256, 0, s>>>(kb, vb, seq_len, B, cache, st.sliding, st.err, nm);
     else
-      append_decode_kernel<kSlidingD, kSlidingR, kSlidingHkv, false, false>
+      append_decode_kernel<kSlidingD, kSlidingR, false, false>
           <<<blocks, 256, 0, s>>>(kb, vb, seq_len, B, cache, st.sliding, st.err, nm);
   }
   return cudaGetLastError();
 }
 
-cudaError_t launch_norm_queries(bool global, const void* q, void* out, int B, const NormArgs& nm, cudaStream_t s) {
+cudaError_t launch_norm_queries(bool global, const void* q, void* out, int B, int hq, const NormArgs& nm,
+                                cudaStream_t s) {
   if (B <= 0) return cudaSuccess;
-  const int n_vec = B * kGlobalHq;   // 32 query heads on both layer kinds
+  const int n_vec = B * hq;
   if (global) {
     const unsigned blocks = (unsigned)((n_vec + 7) / 8);   // one vector per warp
     norm_queries_kernel<kGlobalD, kGlobalR, true><<<blocks, 256, 0, s>>>((const __nv_bfloat16*)q,

@@ -286,3 +286,25 @@ def test_wait_limit_is_set_and_read_on_the_host(lib):
         assert lib.g4attn_wait_limit_ns() == 0
     finally:
         assert lib.g4attn_set_wait_limit_ns(g4.DEFAULT_WAIT_LIMIT_NS) == g4.G4_OK
+
+
+def test_tensor_parallel_head_slices_are_the_only_other_geometries(lib):
+    """A layer descriptor may name one tensor-parallel rank's heads: 32/tp query heads with 16/tp
+    (sliding) or max(1, 4/tp) (global) KV heads, tp in {1, 2, 4, 8}; other head counts fail closed.
+    The provenance record names the slice's shape. No CUDA call is involved."""
+    for tp in (1, 2, 4, 8):
+        for layer in (g4.sliding_layer(tp=tp), g4.global_layer(tp=tp)):
+            buf = ctypes.create_string_buffer(2048)
+            assert lib.g4attn_provenance(ctypes.byref(layer), buf, len(buf)) > 0
+            assert f"Hq{layer.n_q_heads},Hkv{layer.n_kv_heads}," in buf.value.decode()
+    assert g4.global_layer(tp=8).n_kv_heads == 1 and g4.global_layer(tp=4).n_kv_heads == 1
+    for kind, nq, nkv in (("sliding", 16, 16), ("sliding", 8, 2), ("sliding", 2, 1), ("sliding", 64, 32),
+                          ("global", 4, 2), ("global", 16, 4), ("global", 2, 1), ("global", 8, 2)):
+        layer = g4.sliding_layer() if kind == "sliding" else g4.global_layer()
+        layer.n_q_heads, layer.n_kv_heads = nq, nkv
+        assert lib.g4attn_provenance(ctypes.byref(layer), None, 0) == -1, (kind, nq, nkv)
+        assert lib.g4attn_decode_workspace_bytes(ctypes.byref(layer), 4, 8) == 0
+    # the decode workspace scales with the slice's query heads
+    full = lib.g4attn_decode_workspace_bytes(ctypes.byref(g4.global_layer()), 4, 100)
+    eighth = lib.g4attn_decode_workspace_bytes(ctypes.byref(g4.global_layer(tp=8)), 4, 100)
+    assert 0 < eighth < full and abs(8 * eighth - full) <= 8 * 256
