@@ -52,7 +52,7 @@
  *                  global: NULL
  *   cache->k_rot   global only (NULL on sliding layers): p-RoPE(S) on the 128 rotated
  *                  columns d in [0,64) U [256,320), 2048 bf16 per (page, KV head) at
- *                  k_rot + (page*4 + head)*2048, as [d/256][j/8][(d%64)/8][j%8][d%8].
+ *                  k_rot + (page*n_kv_heads + head)*2048, as [d/256][j/8][(d%64)/8][j%8][d%8].
  *                  Written by the library with S; it spares the prefill kernels from
  *                  rotating every key tile again for every query tile and head.
  *   page_table     int32 [B][max_pages]: physical page of logical page i of sequence b
@@ -96,6 +96,12 @@ typedef enum { G4_SLIDING = 0, G4_GLOBAL = 1 } g4_kind;
  *            rope_theta 1e4, rope_partial 1.0, kv_shared 0;
  *   global:  kind 1, n_q_heads 32, n_kv_heads 4, head_dim 512, window 0,
  *            rope_theta 1e6, rope_partial 0.25, kv_shared 1.
+ * Or one tensor-parallel rank's slice of either (RFC section 5, ws2_tp2, ws2_tp4 and
+ * ws2_tp8_kv_replication): with tp in {2, 4, 8} ranks, n_q_heads 32/tp and n_kv_heads 16/tp
+ * (sliding) or max(1, 4/tp) (global; at tp = 8 ranks 2g and 2g+1 both hold KV head g). The rank's
+ * q, out, k, v and cache hold only its heads, in the same layouts with those head counts; query
+ * head h of the slice reads KV head h / (n_q_heads / n_kv_heads) of the slice. Each head's rows
+ * get the bits the full layer gives that head: the arithmetic of a head never involves another.
  * softmax_scale: any finite value > 0 (1/sqrt(head_dim) is the model's). */
 typedef struct {
   int32_t kind;
@@ -259,6 +265,35 @@ g4_status g4attn_kv_append(const g4attn_layer* layer, const void* k, const void*
                            const int32_t* q_start, const int32_t* q_len, const int32_t* ctx_start,
                            int32_t B, const g4attn_cache* cache, const int32_t* page_table,
                            int32_t max_pages, void* stream);
+
+/* Context parallelism of a global (K==V) layer over keys (RFC section 5, ws2_tp4_cp2 and
+ * cp_sliding_window_policy; section 4 rule 3: a split is allowed only with a merge tree fixed by the
+ * contract). A sequence's keys are split into contiguous ranges, each held by one rank (its cache
+ * need hold only its range's keys); every rank computes, for the query rows it is given, a partial
+ * over its own keys, and the partials are merged in rank order.
+ * g4attn_prefill_partial: g4attn_prefill_attend (with raw q) restricted to keys
+ *   key_begin[b] .. key_end[b]-1 of sequence b (int32 [B], device; the causal mask still applies,
+ *   and a row with no such key gets an empty partial). Instead of bf16 output rows it writes, for
+ *   every row of the sequences and each query head: o_part fp32 [T][n_q_heads][512], the output
+ *   not yet divided by the softmax sum (16-byte aligned), and ml_part fp32 [T][n_q_heads][2], the
+ *   running maximum of the scaled scores in log2 units (-inf for an empty partial) and the sum of
+ *   2^(score - maximum) (8-byte aligned). The rows' keys in range must be in the cache (appended
+ *   with g4attn_kv_append). Global layers only (G4_ERR_UNSUPPORTED otherwise: sliding layers split
+ *   with a window halo); no image spans. Other arguments and errors as g4attn_prefill_attend.
+ * g4attn_merge_partials: for every row of the sequences (q_start, q_len: int32 [B], device) and
+ *   every head, merges the n_parts partials (1 <= n_parts <= 8; o_parts and ml_parts are HOST
+ *   arrays of n_parts device pointers laid out as above) in the order given: M = max_r m_r, then
+ *   O = sum_r o_r 2^(m_r - M) and L = sum_r l_r 2^(m_r - M) over r ascending, out = bf16(O / L)
+ *   ([T][n_q_heads][512], 16-byte aligned). Rows of no sequence are not written. The order is
+ *   fixed by the caller, not by timing, so the result does not depend on the batch around a row. */
+g4_status g4attn_prefill_partial(const g4attn_layer* layer, const void* q, int32_t T, const int32_t* q_start,
+                                 const int32_t* q_len, const int32_t* ctx_start, int32_t B,
+                                 const int32_t* key_begin, const int32_t* key_end, const g4attn_cache* cache,
+                                 const int32_t* page_table, int32_t max_pages, float* o_part, float* ml_part,
+                                 void* stream);
+g4_status g4attn_merge_partials(const g4attn_layer* layer, int32_t n_parts, const float* const* o_parts,
+                                const float* const* ml_parts, int32_t T, const int32_t* q_start,
+                                const int32_t* q_len, int32_t B, void* out, void* stream);
 
 /* Bytes of device workspace g4attn_decode needs for B requests whose page table has
  * max_pages columns: the partial softmax states (m, l, O in fp32) of the fixed key chunks whose

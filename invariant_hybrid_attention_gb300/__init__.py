@@ -27,7 +27,7 @@ EXPORTS = ("g4attn_rope_apply", "g4attn_prefill", "g4attn_prefill_stage", "g4att
            "g4attn_decode_exact", "g4attn_decode_exact_workspace_bytes",
            "g4attn_kv_append", "g4attn_decode_workspace_bytes",
            "g4attn_decode", "g4attn_decode_static", "g4attn_provenance", "g4attn_status_sync", "g4attn_status_string",
-           "g4attn_set_wait_limit_ns", "g4attn_wait_limit_ns")
+           "g4attn_set_wait_limit_ns", "g4attn_wait_limit_ns", "g4attn_prefill_partial", "g4attn_merge_partials")
 DEFAULT_WAIT_LIMIT_NS = 2_000_000_000   # the kernels' bounded waits give up after 2 s by default
 
 
@@ -88,6 +88,9 @@ def load(path: Optional[str] = None):
         "g4attn_status_string": (ctypes.c_char_p, [I32]),
         "g4attn_set_wait_limit_ns": (I32, [ctypes.c_uint64]),
         "g4attn_wait_limit_ns": (ctypes.c_uint64, []),
+        "g4attn_prefill_partial": (I32, [L, P, I32, P, P, P, I32, P, P, C, P, I32, P, P, P]),
+        "g4attn_merge_partials": (I32, [L, I32, ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_void_p),
+                                        I32, P, P, I32, P, P]),
     }
     for name, (res, args) in sigs.items():
         f = getattr(lib, name)
@@ -103,13 +106,17 @@ def status_string(status: int) -> str:
         return "unknown"
 
 
-def sliding_layer(window: int = 1024, softmax_scale: Optional[float] = None) -> g4attn_layer:
-    return g4attn_layer(G4_SLIDING, 32, 16, 256, int(window), 1.0e4, 1.0,
+def sliding_layer(window: int = 1024, softmax_scale: Optional[float] = None, tp: int = 1) -> g4attn_layer:
+    """The sliding layer, or (tp > 1) one tensor-parallel rank's slice of it: 32/tp query heads,
+    16/tp KV heads."""
+    return g4attn_layer(G4_SLIDING, 32 // tp, 16 // tp, 256, int(window), 1.0e4, 1.0,
                         1.0 / math.sqrt(256) if softmax_scale is None else float(softmax_scale), 0)
 
 
-def global_layer(softmax_scale: Optional[float] = None) -> g4attn_layer:
-    return g4attn_layer(G4_GLOBAL, 32, 4, 512, 0, 1.0e6, 0.25,
+def global_layer(softmax_scale: Optional[float] = None, tp: int = 1) -> g4attn_layer:
+    """The global K==V layer, or (tp > 1) one rank's slice: 32/tp query heads and max(1, 4/tp) KV
+    heads (at tp = 8 two ranks hold the same KV head)."""
+    return g4attn_layer(G4_GLOBAL, 32 // tp, max(1, 4 // tp), 512, 0, 1.0e6, 0.25,
                         1.0 / math.sqrt(512) if softmax_scale is None else float(softmax_scale), 1)
 
 
@@ -291,3 +298,26 @@ def g4attn_set_wait_limit_ns(ns: int) -> None:
 
 def g4attn_wait_limit_ns() -> int:
     return int(load().g4attn_wait_limit_ns())
+
+
+def g4attn_prefill_partial(layer, q, q_start, q_len, ctx_start, key_begin, key_end, cache: g4attn_cache, page_table,
+                           o_part, ml_part, stream=None):
+    """A global layer's attention restricted to each sequence's keys key_begin .. key_end-1 (int32 [B]
+    device tensors): writes the un-normalised fp32 output o_part [T, Hq, 512] and the softmax state
+    ml_part [T, Hq, 2] (max in log2 units, sum) of every sequence row."""
+    T, B = int(q.shape[0]), int(q_start.shape[0])
+    _check(load().g4attn_prefill_partial(ctypes.byref(layer), _ptr(q), T, _ptr(q_start), _ptr(q_len), _ptr(ctx_start),
+                                         B, _ptr(key_begin), _ptr(key_end), ctypes.byref(cache), _ptr(page_table),
+                                         int(page_table.shape[1]), _ptr(o_part), _ptr(ml_part), _stream(stream)),
+           "g4attn_prefill_partial")
+
+
+def g4attn_merge_partials(layer, o_parts, ml_parts, q_start, q_len, out, stream=None):
+    """Merges the partials (lists of device tensors, in rank order) into out [T, Hq, 512] bf16."""
+    n = len(o_parts)
+    arr_o = (ctypes.c_void_p * n)(*[_ptr(t) for t in o_parts])
+    arr_m = (ctypes.c_void_p * n)(*[_ptr(t) for t in ml_parts])
+    T, B = int(out.shape[0]), int(q_start.shape[0])
+    _check(load().g4attn_merge_partials(ctypes.byref(layer), n, arr_o, arr_m, T, _ptr(q_start), _ptr(q_len), B,
+                                        _ptr(out), _stream(stream)), "g4attn_merge_partials")
+    return out

@@ -20,17 +20,29 @@ namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Head counts of the full layer or of one tensor-parallel rank slice (RFC section 5, ws2_tp2 / ws2_tp4
+// / ws2_tp8_kv_replication): tp in {1, 2, 4, 8} ranks each hold 32 / tp query heads and the KV
+// heads they read, 16 / tp on sliding layers and 4 / tp on global ones, at least one: at tp = 8
+// two ranks hold a copy of the same global KV head.
+bool tp_heads(int n_q, int n_kv, bool global) {
+  for (int tp = 1; tp <= 8; tp *= 2) {
+    const int kv = global ? (kGlobalHkv / tp > 0 ? kGlobalHkv / tp : 1) : kSlidingHkv / tp;
+    if (n_q == kSlidingHq / tp && n_kv == kv) return true;
+  }
+  return false;
+}
+
 g4_status check_layer(const g4attn_layer* L, bool* global) {
   if (!L) return G4_ERR_INVALID;
   if (L->kind == G4_SLIDING) {
-    if (L->n_q_heads != kSlidingHq || L->n_kv_heads != kSlidingHkv || L->head_dim != kSlidingD ||
-        L->kv_shared != 0 || L->rope_theta != 1.0e4f || L->rope_partial != 1.0f)
+    if (!tp_heads(L->n_q_heads, L->n_kv_heads, false) || L->head_dim != kSlidingD || L->kv_shared != 0 ||
+        L->rope_theta != 1.0e4f || L->rope_partial != 1.0f)
       return G4_ERR_UNSUPPORTED;
     if (L->window < 1 || L->window > kMaxPos) return G4_ERR_UNSUPPORTED;
     *global = false;
   } else if (L->kind == G4_GLOBAL) {
-    if (L->n_q_heads != kGlobalHq || L->n_kv_heads != kGlobalHkv || L->head_dim != kGlobalD ||
-        L->kv_shared != 1 || L->rope_theta != 1.0e6f || L->rope_partial != 0.25f || L->window != 0)
+    if (!tp_heads(L->n_q_heads, L->n_kv_heads, true) || L->head_dim != kGlobalD || L->kv_shared != 1 ||
+        L->rope_theta != 1.0e6f || L->rope_partial != 0.25f || L->window != 0)
       return G4_ERR_UNSUPPORTED;
     *global = true;
   } else {
@@ -56,7 +68,7 @@ float scale_log2(const g4attn_layer* L) { return (float)((double)L->softmax_scal
 
 g4_status from_cuda(cudaError_t e) { return e == cudaSuccess ? G4_OK : G4_ERR_CUDA; }
 
-PagedCache paged(const g4attn_cache* c, const int32_t* page_table, int32_t max_pages) {
+PagedCache paged(const g4attn_layer* L, const g4attn_cache* c, const int32_t* page_table, int32_t max_pages) {
   PagedCache pc;
   pc.k = c->k;
   pc.v = c->v;
@@ -64,6 +76,8 @@ PagedCache paged(const g4attn_cache* c, const int32_t* page_table, int32_t max_p
   pc.num_pages = c->num_pages;
   pc.page_table = page_table;
   pc.max_pages = max_pages;
+  pc.hq = L->n_q_heads;
+  pc.hkv = L->n_kv_heads;
   return pc;
 }
 
@@ -161,7 +175,7 @@ g4_status g4attn_kv_append_normed(const g4attn_layer* layer, const g4attn_norms*
   DeviceState st;
   if (device_state(&st) != cudaSuccess) return G4_ERR_CUDA;
   SeqRows rows{q_start, q_len, ctx_start, B, T};
-  return from_cuda(launch_append_prefill(global, k, v, rows, paged(cache, page_table, max_pages), st,
+  return from_cuda(launch_append_prefill(global, k, v, rows, paged(layer, cache, page_table, max_pages), st,
                                          (cudaStream_t)stream, nullptr, nullptr, nm));
 }
 
@@ -191,7 +205,7 @@ static g4_status prefill_stage(const g4attn_layer* layer, const g4attn_norms* no
   // Cache append, and the roped queries staged in `out`: each sequence row of `out` holds its
   // roped query until g4attn_prefill_attend overwrites it with the attention output.
   const SeqRows rows{q_start, q_len, ctx_start, B, T};
-  return from_cuda(launch_append_prefill(global, k, v, rows, paged(cache, page_table, max_pages), st,
+  return from_cuda(launch_append_prefill(global, k, v, rows, paged(layer, cache, page_table, max_pages), st,
                                          (cudaStream_t)stream, q, out, nm));
 }
 
@@ -221,7 +235,7 @@ static g4_status prefill_attend(const g4attn_layer* layer, const void* q, int32_
   if (device_state(&st) != cudaSuccess) return G4_ERR_CUDA;
   const SeqRows rows{q_start, q_len, ctx_start, B, T, span};
   return from_cuda(launch_prefill(global, rows, global ? 0 : layer->window, scale_log2(layer),
-                                  paged(cache, page_table, max_pages), out, st, (cudaStream_t)stream, q));
+                                  paged(layer, cache, page_table, max_pages), out, st, (cudaStream_t)stream, q));
 }
 
 g4_status g4attn_prefill_attend(const g4attn_layer* layer, const void* q, int32_t T, const int32_t* q_start,
@@ -277,10 +291,57 @@ g4_status g4attn_prefill(const g4attn_layer* layer, const void* q, const void* k
                                out, stream);
 }
 
+g4_status g4attn_prefill_partial(const g4attn_layer* layer, const void* q, int32_t T, const int32_t* q_start,
+                                 const int32_t* q_len, const int32_t* ctx_start, int32_t B, const int32_t* key_begin,
+                                 const int32_t* key_end, const g4attn_cache* cache, const int32_t* page_table,
+                                 int32_t max_pages, float* o_part, float* ml_part, void* stream) {
+  bool global = false;
+  g4_status s = check_layer(layer, &global);
+  if (s != G4_OK) return s;
+  if (!global) return G4_ERR_UNSUPPORTED;   // sliding layers split a sequence with a window halo instead
+  if ((s = check_rows(q, T, q_start, q_len, ctx_start, B)) != G4_OK) return s;
+  if ((s = check_cache(cache, global, page_table, max_pages)) != G4_OK) return s;
+  if (!key_begin || !key_end) return G4_ERR_INVALID;
+  if (T > 0 && (!o_part || !ml_part || !aligned16(o_part) || (reinterpret_cast<uintptr_t>(ml_part) & 7u)))
+    return G4_ERR_INVALID;
+  if (T == 0) return G4_OK;
+  DeviceState st;
+  if (device_state(&st) != cudaSuccess) return G4_ERR_CUDA;
+  const SeqRows rows{q_start, q_len, ctx_start, B, T};
+  const PartialOut part{key_begin, key_end, o_part, ml_part};
+  return from_cuda(launch_prefill_global(rows, scale_log2(layer), paged(layer, cache, page_table, max_pages), nullptr,
+                                         st, (cudaStream_t)stream, q, &part));
+}
+
+g4_status g4attn_merge_partials(const g4attn_layer* layer, int32_t n_parts, const float* const* o_parts,
+                                const float* const* ml_parts, int32_t T, const int32_t* q_start, const int32_t* q_len,
+                                int32_t B, void* out, void* stream) {
+  bool global = false;
+  g4_status s = check_layer(layer, &global);
+  if (s != G4_OK) return s;
+  if (!global) return G4_ERR_UNSUPPORTED;
+  if (n_parts < 1 || n_parts > kMaxParts || !o_parts || !ml_parts) return G4_ERR_INVALID;
+  if (T < 0 || B <= 0 || !q_start || !q_len) return G4_ERR_INVALID;
+  if (T == 0) return G4_OK;
+  if (!out || !aligned16(out)) return G4_ERR_INVALID;
+  PartialSet ps{};
+  ps.n = n_parts;
+  for (int i = 0; i < n_parts; ++i) {
+    if (!o_parts[i] || !ml_parts[i] || !aligned16(o_parts[i]) || (reinterpret_cast<uintptr_t>(ml_parts[i]) & 7u))
+      return G4_ERR_INVALID;
+    ps.o[i] = o_parts[i];
+    ps.ml[i] = ml_parts[i];
+  }
+  DeviceState st;
+  if (device_state(&st) != cudaSuccess) return G4_ERR_CUDA;
+  const SeqRows rows{q_start, q_len, nullptr, B, T};
+  return from_cuda(launch_merge_partials(ps, rows, layer->n_q_heads, out, st, (cudaStream_t)stream));
+}
+
 size_t g4attn_decode_workspace_bytes(const g4attn_layer* layer, int32_t B, int32_t max_pages) {
   bool global = false;
   if (check_layer(layer, &global) != G4_OK || B <= 0 || max_pages <= 0) return 0;
-  return decode_workspace_bytes(global, B, max_pages, global ? 0 : layer->window);
+  return decode_workspace_bytes(global, B, max_pages, global ? 0 : layer->window, layer->n_q_heads);
 }
 
 g4_status g4attn_decode_normed(const g4attn_layer* layer, const g4attn_norms* norms, const void* q,
@@ -296,17 +357,17 @@ g4_status g4attn_decode_normed(const g4attn_layer* layer, const g4attn_norms* no
   if (!aligned16(q) || !aligned16(k_new) || !aligned16(out) || !aligned16(workspace)) return G4_ERR_INVALID;
   if (global ? v_new != nullptr : (!v_new || !aligned16(v_new))) return G4_ERR_INVALID;
   if ((s = check_cache(cache, global, page_table, max_pages)) != G4_OK) return s;
-  if (workspace_bytes < decode_workspace_bytes(global, B, max_pages, global ? 0 : layer->window))
+  if (workspace_bytes < decode_workspace_bytes(global, B, max_pages, global ? 0 : layer->window, layer->n_q_heads))
     return G4_ERR_INVALID;
   DeviceState st;
   if (device_state(&st) != cudaSuccess) return G4_ERR_CUDA;
   const cudaStream_t cs = (cudaStream_t)stream;
-  const PagedCache pc = paged(cache, page_table, max_pages);
+  const PagedCache pc = paged(layer, cache, page_table, max_pages);
   // Normed queries go through `out`: the decode kernel reads them there before the merge writes
   // the output rows.
   const void* q_eff = q;
   if (nm.wq != nullptr || (global && nm.wk != nullptr)) {
-    if (launch_norm_queries(global, q, out, B, nm, cs) != cudaSuccess) return G4_ERR_CUDA;
+    if (launch_norm_queries(global, q, out, B, layer->n_q_heads, nm, cs) != cudaSuccess) return G4_ERR_CUDA;
     q_eff = out;
   }
   cudaError_t e = launch_append_decode(global, k_new, v_new, seq_len, B, pc, st, cs, nm);
@@ -359,7 +420,7 @@ g4_status g4attn_decode_static(const g4attn_layer* layer, const void* q, const v
   g4_status s = check_layer(layer, &global);
   if (s != G4_OK) return s;
   if (B <= 0 || max_pages <= 0) return G4_ERR_INVALID;
-  const size_t need = decode_workspace_bytes(global, B, max_pages, global ? 0 : layer->window);
+  const size_t need = decode_workspace_bytes(global, B, max_pages, global ? 0 : layer->window, layer->n_q_heads);
   if (need > G4ATTN_DECODE_STATIC_SCRATCH_BYTES) return G4_ERR_SCRATCH;
   void* ws = nullptr;
   if (decode_scratch(&ws) != cudaSuccess) return G4_ERR_CUDA;
@@ -385,8 +446,8 @@ int32_t g4attn_provenance(const g4attn_layer* layer, char* buf, size_t len) {
                  "qrope=attention-kernel(plain),append-pass(normed,vision,exact-decode);"
                  "exact-decode=prefill-kernels-one-row-chunks;vision=image-span-per-row;"
                  "accumulator=fp32;casts=roped-q,roped-k,p,out:bf16-rne;exp=ex2.approx.ftz.f32;device=%s;dtype=bf16;"
-                 "shape=Hq32,Hkv4,D512,k_eq_v,prope0.25,theta1e6,scale%.9g;fallback=none",
-                 dev, (double)layer->softmax_scale);
+                 "shape=Hq%d,Hkv%d,D512,k_eq_v,prope0.25,theta1e6,scale%.9g;fallback=none",
+                 dev, layer->n_q_heads, layer->n_kv_heads, (double)layer->softmax_scale);
   else
     n = snprintf(rec, sizeof(rec),
                  "requested=g4attn;actual=g4attn-cuda-sm_103a;layer=sliding;kernels=append_kv_keygroups,"
@@ -396,8 +457,8 @@ int32_t g4attn_provenance(const g4attn_layer* layer, char* buf, size_t len) {
                  "qrope=attention-kernel(plain),append-pass(normed,vision,exact-decode);"
                  "exact-decode=prefill-kernels-one-row-chunks;vision=image-span-per-row;"
                  "accumulator=fp32;casts=roped-q,roped-k,p,out:bf16-rne;exp=ex2.approx.ftz.f32;device=%s;dtype=bf16;"
-                 "shape=Hq32,Hkv16,D256,W%d,theta1e4,scale%.9g;fallback=none",
-                 dev, layer->window, (double)layer->softmax_scale);
+                 "shape=Hq%d,Hkv%d,D256,W%d,theta1e4,scale%.9g;fallback=none",
+                 dev, layer->n_q_heads, layer->n_kv_heads, layer->window, (double)layer->softmax_scale);
   if (n < 0) return -1;
   if (buf && len > 0) {
     const size_t c = (size_t)n < len - 1 ? (size_t)n : len - 1;

@@ -26,6 +26,15 @@ struct PrefillParams {
   __nv_bfloat16* out;
   RopeTables tb;
   uint32_t* err;
+  int hq, hkv;              // query heads of the q and out rows; KV heads of the cache
+  // Partial calls (global layers, context parallelism over keys): sequence b attends only to keys
+  // key_begin[b] .. key_end[b]-1, and the rows' un-normalised output o_part (fp32 [T][hq][D]) and
+  // softmax state ml_part (fp32 [T][hq][2]: running max in log2 units, sum) are written instead of
+  // out. NULL otherwise.
+  const int32_t* key_begin;
+  const int32_t* key_end;
+  float* o_part;
+  float* ml_part;
   int n_units;              // persistent sliding kernel: (query tile, KV head) units of the batch
   unsigned long long wait_ns;   // limit of every protocol wait (g4attn_set_wait_limit_ns)
 };

@@ -132,7 +132,7 @@ __device__ __forceinline__ int o_dim(int col) {
   return (col < 128 || col >= 384) ? col : (col < 256 ? col + 128 : col - 128);
 }
 
-template <bool kRope>
+template <bool kRope, bool kPart>
 __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
     prefill_global_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_o,
                           const __grid_constant__ CUtensorMap tmap_s, const __grid_constant__ CUtensorMap tmap_rot,
@@ -150,10 +150,10 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t partner = rank ^ 2u;        // score CTA r <-> output CTA r + 2 (same head)
   const bool leader = pr == 0;               // issues the pair's MMAs
   const int unit = blockIdx.x >> 2;
-  const int hp = unit % (kGlobalHq / 2);
-  const int slot = unit / (kGlobalHq / 2);
+  const int hp = unit % (p.hq / 2);
+  const int slot = unit / (p.hq / 2);
   const int h = 2 * hp + (int)pr;
-  const int g = h / (kGlobalHq / kGlobalHkv);   // both heads of the pair share KV head g
+  const int g = h / (p.hq / p.hkv);   // both heads of the pair share KV head g
 
   if (warp == 0) {
     int ub, ut;
@@ -183,8 +183,29 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0 && rank == 0 && hp == 0) set_error(p.err, kErrPos);
     return;
   }
-  const int n_tiles = k_hi / kTN + 1;
+  // kPart: only keys key_begin .. key_end-1 of the sequence; the tiles start at the one holding
+  // key_begin (tile j of the unit is key tile kt0 + j).
+  int k_lo = 0;
+  if (kPart) {
+    k_lo = max(0, __ldg(p.key_begin + b));
+    k_hi = min(k_hi, __ldg(p.key_end + b) - 1);
+  }
+  const int kt0 = k_lo / kTN;
+  const int n_tiles = k_hi >= k_lo ? k_hi / kTN - kt0 + 1 : 0;
   const int32_t* pt = p.page_table + (size_t)b * p.max_pages;
+  if (kPart && n_tiles == 0) {   // no key of the range: an empty partial (every CTA of the unit returns)
+    for (int i = threadIdx.x; i < kBM * (is_out ? kGD / 4 : 1); i += kThreads) {
+      const int rr = is_out ? i / (kGD / 4) : i;
+      const int pos = kBM * t + rr;
+      if (pos < p_lo || pos > p_hi) continue;
+      const size_t v = (size_t)(q_row0 + rr) * p.hq + h;
+      if (is_out)
+        reinterpret_cast<float4*>(p.o_part + v * kGD)[i % (kGD / 4)] = make_float4(0.f, 0.f, 0.f, 0.f);
+      else
+        reinterpret_cast<float2*>(p.ml_part)[v] = make_float2(-INFINITY, 0.f);
+    }
+    return;
+  }
 
   if (threadIdx.x == 32) {
     for (int s = 0; s < kNK; ++s) {
@@ -258,8 +279,8 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
       auto load_blocks = [&](int j0) -> int {
         const int jt = j0 + (lane >> 2);
         if (jt >= n_tiles) return -1;
-        return page_block(jt * kTN + 64 * (int)pr + kPage * (lane & 3), 0, k_hi, pt, p.num_pages, kGlobalHkv, g,
-                          p.err);
+        return page_block((kt0 + jt) * kTN + 64 * (int)pr + kPage * (lane & 3), k_lo, k_hi, pt, p.num_pages, p.hkv,
+                          g, p.err);
       };
       int blk_cur = load_blocks(0), blk_next = load_blocks(8);
       int j = 0;
@@ -333,10 +354,11 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t tq = tm + tmem_lane_base(warp);
       const int pos = kBM * t + r;
       const bool row_ok = pos >= p_lo && pos <= p_hi;
-      int row_hi = pos;   // the row sees keys 0 .. row_hi
+      int row_hi = pos, row_lo = k_lo;   // the row sees keys row_lo .. row_hi
+      if (kPart) row_hi = min(pos, k_hi);
       if (p.rows.span && row_ok) {
-        int row_lo;
-        row_keys(p.rows, 0, q_row0 + r, pos, ctx_end, p.err, row_lo, row_hi);
+        int span_lo;   // 0 on a global layer
+        row_keys(p.rows, 0, q_row0 + r, pos, ctx_end, p.err, span_lo, row_hi);
         if (row_hi > k_hi) {   // spans that disagree between rows
           set_error(p.err, kErrSpan);
           row_hi = k_hi;
@@ -384,7 +406,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
       float m_used = -INFINITY, l_run = 0.f;
       for (int j = 0; ok && j < n_tiles; ++j) {
         const int sb = j % kNP;
-        const int kb = j * kTN;
+        const int kb = (kt0 + j) * kTN;
         // Waits are made warp-uniform so that every lane leaves the loop together on an abort.
         if (!__all_sync(0xffffffffu, mbar_wait(&bar.s_full[sb], (j / kNP) & 1, abort_flag, p.err, p.wait_ns))) {
           ok = false;
@@ -403,7 +425,15 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         float s[kTN];
 #pragma unroll
         for (int c = 0; c < kTN; ++c) s[c] = __uint_as_float(sr[c]);
-        if (!(row_ok && kb + kTN - 1 <= row_hi)) {   // causal mask (and rows outside the sequence)
+        if constexpr (kPart) {   // the row's keys in this tile: one run [lo, hi] of columns
+          if (!(row_ok && kb >= row_lo && kb + kTN - 1 <= row_hi)) {
+            int lo = row_lo - kb, hi = row_ok ? row_hi - kb : -1;
+            if (hi < lo) lo = hi = 1 << 20;   // none
+            const unsigned span = (unsigned)(hi - lo);
+#pragma unroll
+            for (int c = 0; c < kTN; ++c) s[c] = ((unsigned)(c - lo) <= span) ? s[c] : -INFINITY;
+          }
+        } else if (!(row_ok && kb + kTN - 1 <= row_hi)) {   // causal mask (and rows outside the sequence)
           const int hi = row_ok ? row_hi - kb : -1;
 #pragma unroll
           for (int c = 0; c < kTN; ++c) s[c] = (c <= hi) ? s[c] : -INFINITY;
@@ -457,6 +487,9 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         }
         if (!__shfl_sync(0xffffffffu, okp, 0)) ok = false;
       }
+      // kPart: the row's softmax state; O (in the output CTA) is relative to the same running max
+      if (kPart && ok && row_ok)
+        reinterpret_cast<float2*>(p.ml_part)[(size_t)(q_row0 + r) * p.hq + h] = make_float2(m_used, l_run);
     }
   } else {
     // ================================================================ output CTAs
@@ -470,7 +503,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
       auto load_blocks = [&](int c0) -> int {
         const int cs2 = c0 + (lane >> 2);
         if (cs2 >= n_st) return -1;
-        return page_block(cs2 * kVN + kPage * (lane & 3), 0, k_hi, pt, p.num_pages, kGlobalHkv, g, p.err);
+        return page_block(kt0 * kTN + cs2 * kVN + kPage * (lane & 3), k_lo, k_hi, pt, p.num_pages, p.hkv, g, p.err);
       };
       int blk_cur = load_blocks(0), blk_next = load_blocks(8);
       int c = 0;
@@ -505,13 +538,15 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         const int s = c % kNV, j = c >> 1, e = c & 1;
         ok = __all_sync(0xffffffffu, mbar_wait(&bar.v_full[s], (c / kNV) & 1, abort_flag, p.err, p.wait_ns));
         if (!ok) break;
-        const int kb = c * kVN;
-        const int v1 = min(min(kb + kVN, ((k_hi >> 4) + 1) * kPage), ctx_end);
-        if (v1 < kb + kVN) {
+        const int kb = kt0 * kTN + c * kVN;
+        // kPart: a rank's cache may hold another rank's keys, or nothing, around its range
+        const int v0 = kPart ? k_lo : 0;
+        const int v1 = kPart ? min(kb + kVN, k_hi + 1) : min(min(kb + kVN, ((k_hi >> 4) + 1) * kPage), ctx_end);
+        if (v0 > kb || v1 < kb + kVN) {
           uint8_t* vt = base + s * kVStage;
           for (int idx = lane; idx < kVN * 32; idx += 32) {
             const int rr = idx >> 5, dg = idx & 31;
-            if (kb + rr >= v1)
+            if (kb + rr < v0 || kb + rr >= v1)
               *reinterpret_cast<uint4*>(vt + (rr >> 3) * kVKG + dg * 128 + (rr & 7) * 16) = make_uint4(0, 0, 0, 0);
           }
           fence_proxy_async();
@@ -594,18 +629,30 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
       // TMA stores; any other tile is written row by row, so that rows of other sequences and
       // padding are never touched.
       const int jl = n_tiles - 1;
-      const bool staged = p_lo == kBM * t && p_hi == kBM * t + kBM - 1;
+      const bool staged = !kPart && p_lo == kBM * t && p_hi == kBM * t + kBM - 1;
       uint8_t* const ep = base + ((1024u - (smem_u32(base) & 1023u)) & 1023u);   // box-aligned
       bool ok_ep = ok && __all_sync(0xffffffffu, mbar_wait(&bar.pv_done[jl % kNP], (jl / kNP) & 1, abort_flag, p.err, p.wait_ns));
       if (ok_ep) {
         tc_fence_after();
         const float inv = (l_last > 0.f) ? __frcp_rn(l_last) : 0.f;
-        __nv_bfloat16* orow = p.out + ((size_t)(q_row0 + r) * kGlobalHq + h) * kGD;
+        __nv_bfloat16* orow = p.out + ((size_t)(q_row0 + r) * p.hq + h) * kGD;
+        float* prow = kPart ? p.o_part + ((size_t)(q_row0 + r) * p.hq + h) * kGD : nullptr;
         tmem_ld_stream64<kGD / 64>(
             tq + kTmO, [] {},
             [&](int c, const uint32_t(&o)[64]) {
 #pragma unroll
               for (int half = 0; half < 2; ++half) {
+                if constexpr (kPart) {   // the un-normalised fp32 output of the row
+                  if (row_ok) {
+                    float4* dst = reinterpret_cast<float4*>(prow + o_dim(64 * c + 32 * half));
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                      dst[i] = make_float4(__uint_as_float(o[32 * half + 4 * i]), __uint_as_float(o[32 * half + 4 * i + 1]),
+                                           __uint_as_float(o[32 * half + 4 * i + 2]),
+                                           __uint_as_float(o[32 * half + 4 * i + 3]));
+                  }
+                  continue;
+                }
                 uint32_t w16[16];
 #pragma unroll
                 for (int k = 0; k < 16; ++k)
@@ -716,10 +763,10 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
 // dim half comes before the key group although its stride is larger, so that a box lands with the
 // key group outermost (see the K stage layout). S: 32 dim groups per half, box from dim group 8;
 // k_rot: 8 dim groups per half.
-bool page_maps(CUtensorMap* ms, CUtensorMap* mr, const void* s_cache, const void* rot_cache, int num_pages) {
+bool page_maps(CUtensorMap* ms, CUtensorMap* mr, const void* s_cache, const void* rot_cache, int num_pages, int hkv) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
-  const cuuint64_t blocks = (cuuint64_t)num_pages * kGlobalHkv;
+  const cuuint64_t blocks = (cuuint64_t)num_pages * hkv;
   const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   {
     const cuuint64_t dims[5] = {64, 32, 2, 2, blocks};
@@ -742,10 +789,66 @@ bool page_maps(CUtensorMap* ms, CUtensorMap* mr, const void* s_cache, const void
   return true;
 }
 
+// ---------------------------------------------------------------- merge of partials (context parallelism)
+// One CTA per query row: thread i merges dims 4i .. 4i+3 of every head of the row, over the parts in
+// the order given. A row no sequence owns is not written.
+__global__ void __launch_bounds__(kGD / 4) merge_partials_kernel(PartialSet parts, SeqRows rows, int hq,
+                                                                 __nv_bfloat16* out) {
+  const int r = blockIdx.x;
+  __shared__ int owned;
+  if (threadIdx.x < 32) {
+    bool mine = false;
+    for (int b0 = 0; b0 < rows.B && !mine; b0 += 32) {
+      const int b = b0 + (int)threadIdx.x;
+      if (b < rows.B) {
+        const int s0 = rows.q_start[b], L = rows.q_len[b];
+        mine = L > 0 && r >= s0 && r - s0 < L;
+      }
+      mine = __any_sync(0xffffffffu, mine);
+    }
+    if (threadIdx.x == 0) owned = mine ? 1 : 0;
+  }
+  __syncthreads();
+  if (!owned) return;
+  const int d0 = 4 * threadIdx.x;
+  for (int h = 0; h < hq; ++h) {
+    const size_t v = (size_t)r * hq + h;
+    float M = -INFINITY;
+    for (int i = 0; i < parts.n; ++i) M = fmaxf(M, parts.ml[i][2 * v]);
+    float L = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
+    if (M != -INFINITY) {
+      for (int i = 0; i < parts.n; ++i) {
+        const float mi = parts.ml[i][2 * v];
+        if (mi == -INFINITY) continue;   // a part with no key for this row
+        const float w = exp2f(mi - M);
+        L = fmaf(parts.ml[i][2 * v + 1], w, L);
+        const float4 o = *reinterpret_cast<const float4*>(parts.o[i] + v * kGD + d0);
+        acc[0] = fmaf(o.x, w, acc[0]);
+        acc[1] = fmaf(o.y, w, acc[1]);
+        acc[2] = fmaf(o.z, w, acc[2]);
+        acc[3] = fmaf(o.w, w, acc[3]);
+      }
+    }
+    const float inv = (L > 0.f) ? __frcp_rn(L) : 0.f;
+    uint2 pk;
+    pk.x = pack_bf16(acc[0] * inv, acc[1] * inv);
+    pk.y = pack_bf16(acc[2] * inv, acc[3] * inv);
+    *reinterpret_cast<uint2*>(out + v * kGD + d0) = pk;
+  }
+}
+
 }  // namespace
 
+cudaError_t launch_merge_partials(const PartialSet& parts, const SeqRows& rows, int hq, void* out, const DeviceState& st,
+                                  cudaStream_t s) {
+  (void)st;
+  if (rows.T <= 0) return cudaSuccess;
+  merge_partials_kernel<<<(unsigned)rows.T, kGD / 4, 0, s>>>(parts, rows, hq, (__nv_bfloat16*)out);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_prefill_global(const SeqRows& rows, float scale_log2, const PagedCache& cache, void* out,
-                                  const DeviceState& st, cudaStream_t s, const void* q_raw) {
+                                  const DeviceState& st, cudaStream_t s, const void* q_raw, const PartialOut* part) {
   PrefillParams p{};
   p.rows = rows;
   p.window = 0;
@@ -759,16 +862,27 @@ cudaError_t launch_prefill_global(const SeqRows& rows, float scale_log2, const P
   p.out = (__nv_bfloat16*)out;
   p.tb = st.global;
   p.err = st.err;
+  p.hq = cache.hq;
+  p.hkv = cache.hkv;
   p.wait_ns = wait_limit_ns();
+  if (part) {
+    p.key_begin = part->key_begin;
+    p.key_end = part->key_end;
+    p.o_part = part->o;
+    p.ml_part = part->ml;
+  }
   // Raw queries are rotated in the kernel; otherwise the staged roped queries are read from `out`.
+  // Partial calls take raw queries and no image spans.
   if (rows.span && q_raw) return cudaErrorInvalidValue;
+  if (part && (!q_raw || rows.span)) return cudaErrorInvalidValue;
   CUtensorMap mq, mo, ms, mr;   // queries (raw or staged), output rows, the cache's S and k_rot pages
-  if (!q_map(&mq, q_raw ? q_raw : out, rows.T, kGlobalHq, kGD)) return cudaErrorInvalidValue;
-  if (!q_map(&mo, out, rows.T, kGlobalHq, kGD)) return cudaErrorInvalidValue;
-  if (!page_maps(&ms, &mr, cache.k, cache.krot, cache.num_pages)) return cudaErrorInvalidValue;
-  auto kernel = q_raw ? prefill_global_kernel<true> : prefill_global_kernel<false>;
-  const int ki = q_raw ? 1 : 0;
-  static bool attr[64][2] = {};
+  if (!q_map(&mq, q_raw ? q_raw : out, rows.T, cache.hq, kGD)) return cudaErrorInvalidValue;
+  if (!q_map(&mo, part ? q_raw : out, rows.T, cache.hq, kGD)) return cudaErrorInvalidValue;   // unused by partials
+  if (!page_maps(&ms, &mr, cache.k, cache.krot, cache.num_pages, cache.hkv)) return cudaErrorInvalidValue;
+  auto kernel = part ? prefill_global_kernel<true, true>
+                     : (q_raw ? prefill_global_kernel<true, false> : prefill_global_kernel<false, false>);
+  const int ki = part ? 2 : (q_raw ? 1 : 0);
+  static bool attr[64][3] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
@@ -778,7 +892,7 @@ cudaError_t launch_prefill_global(const SeqRows& rows, float scale_log2, const P
     attr[dev][ki] = true;
   }
   const long long slots = (long long)rows.T / kBM + 2LL * rows.B;
-  const long long blocks = slots * (kGlobalHq / 2) * 4;   // a cluster of four CTAs per (query tile, head pair)
+  const long long blocks = slots * (cache.hq / 2) * 4;   // a cluster of four CTAs per (query tile, head pair)
   if (blocks <= 0 || blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
   kernel<<<(unsigned)blocks, kThreads, kGlobalSmemBytes, s>>>(mq, mo, ms, mr, p);
   return cudaGetLastError();
