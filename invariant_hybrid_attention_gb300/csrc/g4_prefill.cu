@@ -97,46 +97,6 @@ static_assert(2 * kQChunk <= kKStage, "Q dims 0-127 must fit in one K stage");
 constexpr size_t kSlidingSmemBytes = sizeof(SlidingSmem) + 1024;
 static_assert(kSlidingSmemBytes <= 232448, "sliding prefill exceeds the 227 KB shared-memory limit");
 
-// Epilogue stores. Lane L of a softmax warp holds row L's 16 packed words (32 dims) of an output
-// chunk, and rows lie 16 KB apart, so a store instruction per lane would touch 32 rows (32 cache
-// lines) for 16 bytes each. Two xor-shuffle stages transpose the 16-byte pieces inside each group
-// of four lanes (each stage swaps one bit of the lane index with the same bit of the piece index),
-// after which lane 4a + i holds piece i of rows 4a .. 4a+3: each store then writes 64 contiguous
-// bytes of eight rows.
-template <int M>
-__device__ __forceinline__ void xpose_pieces(uint32_t (&w)[16], int lane) {
-  const bool hi = (lane & M) != 0;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    if (j & M) continue;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint32_t send = hi ? w[4 * j + k] : w[4 * (j | M) + k];
-      const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, M);
-      if (hi)
-        w[4 * j + k] = recv;
-      else
-        w[4 * (j | M) + k] = recv;
-    }
-  }
-}
-// Stores dims col0 .. col0+31 of the warp's 32 rows; row0 is the warp's first row (a row index
-// into `out`, may be out of range: only rows set in `valid` are written).
-__device__ __forceinline__ void store_rows32(uint32_t (&w)[16], __nv_bfloat16* out, long long row0, int hq, int h,
-                                             int col0, unsigned valid, int lane) {
-  xpose_pieces<1>(w, lane);
-  xpose_pieces<2>(w, lane);
-  const int a = lane >> 2, i = lane & 3;
-#pragma unroll
-  for (int t = 0; t < 4; ++t) {
-    const int row = 4 * a + t;
-    if ((valid >> row) & 1u) {
-      __nv_bfloat16* dst = out + ((row0 + row) * hq + h) * kSD + col0 + 8 * i;
-      *reinterpret_cast<uint4*>(dst) = make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
-    }
-  }
-}
-
 // One unit as one CTA of its pair sees it.
 struct Unit {
   int g, h, t, p_lo, p_hi, ctx_end, k_lo, k_hi, kt0, n_tiles, q_row0, qpos;
@@ -685,7 +645,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 16; ++c)
           w16[c] = pack_bf16(__uint_as_float(o[2 * c]) * inv, __uint_as_float(o[2 * c + 1]) * inv);
-        store_rows32(w16, p.out, wrow0, p.hq, cur.h, 32 * cc, valid, lane);
+        store_rows32<kSD>(w16, p.out, wrow0, p.hq, cur.h, 32 * cc, valid, lane);
       }
       c0 = c0n;
       ++uq;

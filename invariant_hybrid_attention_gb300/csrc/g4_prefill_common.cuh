@@ -212,6 +212,47 @@ inline __device__ void rotate_q_pair(uint8_t* lo_box, uint8_t* hi_box, const Rop
   }
 }
 
+// Epilogue stores. Lane L of an epilogue warp holds row L's 16 packed words (32 dims) of an output
+// chunk, and rows lie hq * D * 2 bytes apart, so a store per lane would touch 32 rows (32 cache
+// lines) for 16 bytes each. Two xor-shuffle stages transpose the 16-byte pieces inside each group
+// of four lanes (each stage swaps one bit of the lane index with the same bit of the piece index),
+// after which lane 4a + i holds piece i of rows 4a .. 4a+3: each store then writes 64 contiguous
+// bytes of eight rows.
+template <int M>
+inline __device__ void xpose_pieces(uint32_t (&w)[16], int lane) {
+  const bool hi = (lane & M) != 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    if (j & M) continue;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t send = hi ? w[4 * j + k] : w[4 * (j | M) + k];
+      const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, M);
+      if (hi)
+        w[4 * j + k] = recv;
+      else
+        w[4 * (j | M) + k] = recv;
+    }
+  }
+}
+// Stores dims col0 .. col0+31 of head h of the warp's 32 rows of out [rows][hq][D]; row0 is the
+// warp's first row (may be out of range: only rows set in `valid` are written).
+template <int D>
+inline __device__ void store_rows32(uint32_t (&w)[16], __nv_bfloat16* out, long long row0, int hq, int h, int col0,
+                                    unsigned valid, int lane) {
+  xpose_pieces<1>(w, lane);
+  xpose_pieces<2>(w, lane);
+  const int a = lane >> 2, i = lane & 3;
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const int row = 4 * a + t;
+    if ((valid >> row) & 1u) {
+      __nv_bfloat16* dst = out + ((row0 + row) * hq + h) * D + col0 + 8 * i;
+      *reinterpret_cast<uint4*>(dst) = make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
+    }
+  }
+}
+
 inline __device__ uint32_t tmem_lane_base(int warp) { return (uint32_t)(32 * (warp & 3)) << 16; }
 
 // Full cluster barrier (every thread of both CTAs); used once, after the mbarriers are set up.

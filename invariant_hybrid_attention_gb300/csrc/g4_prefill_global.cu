@@ -110,12 +110,12 @@ struct Bars {
   // output CTAs
   uint64_t v_full[kNV], v_empty[kNV], v_ready[kNV];
   uint64_t p_full[kNP], o_ready[kNP], pv_done[kNP];
-  uint64_t ep_staged;        // output CTAs: the four epilogue warps have staged their rows
+  uint64_t o_free;           // output CTAs (rank 2): both CTAs' epilogue warps have read O out
   uint64_t teardown;
   uint32_t tmem_base;
   int abort_flag;
-  int unit_b, unit_t;
   int p_seen[kNP];   // output CTAs: phases of each P slot consumed (for the abort drain)
+  int q_issued;      // score CTAs: Q tiles issued (by thread 64; read by the abort drain)
 };
 
 struct GlobalSmem {
@@ -132,11 +132,61 @@ __device__ __forceinline__ int o_dim(int col) {
   return (col < 128 || col >= 384) ? col : (col < 256 ? col + 128 : col - 128);
 }
 
+// One unit as the CTAs of its cluster see it: (sequence b, query tile t, head pair hp); this CTA's
+// head h (of the pair) reads KV head g. Keys k_lo .. k_hi in n_tiles tiles from key tile kt0.
+struct GUnit {
+  int b, t, hp, h, g, p_lo, p_hi, ctx_end, q_row0, k_lo, k_hi, kt0, n_tiles;
+  const int32_t* pt;
+};
+
+// Warp-wide. False when unit u holds no rows or is refused (the error word is then set); every role
+// of the four CTAs skips such units alike, so all of them walk the same units in the same order. A
+// partial call's unit may have no key of its range (n_tiles 0): the roles that write rows write an
+// empty partial, the others skip it. Not inlined: nine roles call it.
+template <bool kPart>
+__device__ __noinline__ bool global_unit(const PrefillParams& p, int u, uint32_t pr, GUnit& o) {
+  o.hp = u % (p.hq / 2);
+  o.h = 2 * o.hp + (int)pr;
+  o.g = o.h / (p.hq / p.hkv);   // both heads of the pair share KV head g
+  int b, t, f[3];
+  find_unit(p.rows, u / (p.hq / 2), b, t, p.err, f);
+  if (b < 0) return false;
+  const int cs = f[0], L = f[1], qs = f[2];
+  o.b = b;
+  o.t = t;
+  o.p_lo = max(kBM * t, cs);
+  o.p_hi = min(kBM * t + kBM - 1, cs + L - 1);
+  o.ctx_end = cs + L;
+  if (o.p_hi >= kMaxPos || (o.p_hi >> 4) >= p.max_pages) {
+    if ((threadIdx.x & 31) == 0) set_error(p.err, kErrPos);
+    return false;
+  }
+  o.q_row0 = qs + (kBM * t - cs);
+  // Keys 0 .. k_hi: the last row's run ends no earlier than any other row's (an image holding a
+  // row of the tile and reaching past the last row holds the last row too).
+  int lo_unused;
+  row_keys(p.rows, 0, o.q_row0 + (o.p_hi - kBM * t), o.p_hi, o.ctx_end, p.err, lo_unused, o.k_hi);
+  if ((o.k_hi >> 4) >= p.max_pages) {   // an image past the page table (the rows' own pages fit)
+    if ((threadIdx.x & 31) == 0) set_error(p.err, kErrPos);
+    return false;
+  }
+  // kPart: only keys key_begin .. key_end-1 of the sequence; the tiles start at the one holding
+  // key_begin (tile j of the unit is key tile kt0 + j).
+  o.k_lo = 0;
+  if (kPart) {
+    o.k_lo = max(0, __ldg(p.key_begin + b));
+    o.k_hi = min(o.k_hi, __ldg(p.key_end + b) - 1);
+  }
+  o.kt0 = o.k_lo / kTN;
+  o.n_tiles = o.k_hi >= o.k_lo ? o.k_hi / kTN - o.kt0 + 1 : 0;
+  o.pt = p.page_table + (size_t)b * p.max_pages;
+  return true;
+}
+
 template <bool kRope, bool kPart>
 __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
-    prefill_global_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_o,
-                          const __grid_constant__ CUtensorMap tmap_s, const __grid_constant__ CUtensorMap tmap_rot,
-                          PrefillParams p) {
+    prefill_global_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_s,
+                          const __grid_constant__ CUtensorMap tmap_rot, PrefillParams p) {
   extern __shared__ uint8_t smem_raw[];
   GlobalSmem& sm = *reinterpret_cast<GlobalSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   uint8_t* const base = sm.data;
@@ -149,64 +199,17 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t pair_peer = rank ^ 1u;      // the other CTA of this MMA pair
   const uint32_t partner = rank ^ 2u;        // score CTA r <-> output CTA r + 2 (same head)
   const bool leader = pr == 0;               // issues the pair's MMAs
-  const int unit = blockIdx.x >> 2;
-  const int hp = unit % (p.hq / 2);
-  const int slot = unit / (p.hq / 2);
-  const int h = 2 * hp + (int)pr;
-  const int g = h / (p.hq / p.hkv);   // both heads of the pair share KV head g
+  const int cluster = blockIdx.x >> 2, n_clusters = gridDim.x >> 2;
 
-  if (warp == 0) {
-    int ub, ut;
-    find_unit(p.rows, slot, ub, ut, p.err);
-    if (lane == 0) {
-      bar.unit_b = ub;
-      bar.unit_t = ut;
+  // The output CTAs' P-slot warp counts the cluster's key tiles over all its units before the
+  // cluster barrier: it posts the bytes of the first two tiles' P before any copy can arrive.
+  int total_tiles = 0;
+  if (is_out && warp == 6) {
+    for (int u = cluster; u < p.n_units; u += n_clusters) {
+      GUnit o;
+      if (global_unit<kPart>(p, u, pr, o)) total_tiles += o.n_tiles;
     }
   }
-  __syncthreads();
-  const int b = bar.unit_b;   // all four CTAs find the same unit
-  if (b < 0) return;
-  const int t = bar.unit_t;
-  const int cs = p.rows.ctx_start[b], L = p.rows.q_len[b], qs = p.rows.q_start[b];
-  const int p_lo = max(kBM * t, cs), p_hi = min(kBM * t + kBM - 1, cs + L - 1);
-  const int ctx_end = cs + L;
-  if (p_hi >= kMaxPos || (p_hi >> 4) >= p.max_pages) {
-    if (threadIdx.x == 0 && rank == 0 && hp == 0) set_error(p.err, kErrPos);
-    return;
-  }
-  const int q_row0 = qs + (kBM * t - cs);
-  // Keys 0 .. k_hi: the last row's run ends no earlier than any other row's (an image holding a
-  // row of the tile and reaching past the last row holds the last row too).
-  int k_hi, k_lo_unused;
-  row_keys(p.rows, 0, q_row0 + (p_hi - kBM * t), p_hi, ctx_end, p.err, k_lo_unused, k_hi);
-  if ((k_hi >> 4) >= p.max_pages) {   // an image past the page table (the rows' own pages fit)
-    if (threadIdx.x == 0 && rank == 0 && hp == 0) set_error(p.err, kErrPos);
-    return;
-  }
-  // kPart: only keys key_begin .. key_end-1 of the sequence; the tiles start at the one holding
-  // key_begin (tile j of the unit is key tile kt0 + j).
-  int k_lo = 0;
-  if (kPart) {
-    k_lo = max(0, __ldg(p.key_begin + b));
-    k_hi = min(k_hi, __ldg(p.key_end + b) - 1);
-  }
-  const int kt0 = k_lo / kTN;
-  const int n_tiles = k_hi >= k_lo ? k_hi / kTN - kt0 + 1 : 0;
-  const int32_t* pt = p.page_table + (size_t)b * p.max_pages;
-  if (kPart && n_tiles == 0) {   // no key of the range: an empty partial (every CTA of the unit returns)
-    for (int i = threadIdx.x; i < kBM * (is_out ? kGD / 4 : 1); i += kThreads) {
-      const int rr = is_out ? i / (kGD / 4) : i;
-      const int pos = kBM * t + rr;
-      if (pos < p_lo || pos > p_hi) continue;
-      const size_t v = (size_t)(q_row0 + rr) * p.hq + h;
-      if (is_out)
-        reinterpret_cast<float4*>(p.o_part + v * kGD)[i % (kGD / 4)] = make_float4(0.f, 0.f, 0.f, 0.f);
-      else
-        reinterpret_cast<float2*>(p.ml_part)[v] = make_float2(-INFINITY, 0.f);
-    }
-    return;
-  }
-
   if (threadIdx.x == 32) {
     for (int s = 0; s < kNK; ++s) {
       mbar_init(&bar.k_full[s], 1);
@@ -222,6 +225,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&bar.pv_done[s], 1);   // P.V of tiles of this parity
       bar.p_seen[s] = 0;
     }
+    bar.q_issued = 0;
     mbar_init(&bar.q_full, 1);
     mbar_init(&bar.q_moved, kSoftmaxThreads / 32);
     mbar_init(&bar.q_pair, 8);
@@ -232,13 +236,14 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&bar.v_empty[s], 1);
       mbar_init(&bar.v_ready[s], 1);
     }
-    mbar_init(&bar.ep_staged, kSoftmaxThreads / 32);
+    mbar_init(&bar.o_free, 8);   // rank 2: both output CTAs' epilogue warps have read O out
     mbar_init(&bar.teardown, 1);
     bar.abort_flag = 0;
-    if (is_out) {   // the first two tiles' P may arrive as soon as the cluster is up
-      for (int s = 0; s < kNP && s < n_tiles; ++s) mbar_arrive_expect_tx(&bar.p_full[s], kPSendBytes);
-    }
     fence_mbar_init();
+  }
+  __syncthreads();
+  if (is_out && threadIdx.x == 192) {   // the first two tiles' P may arrive once the cluster is up
+    for (int s = 0; s < kNP && s < total_tiles; ++s) mbar_arrive_expect_tx(&bar.p_full[s], kPSendBytes);
   }
   if (warp == 1) {
     tmem_alloc2(&bar.tmem_base, 512);
@@ -255,241 +260,305 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
     else
       mbar_arrive_remote(map_peer(smem_u32(br), pair_peer));
   };
-  int k_issued = 0, v_issued = 0;   // copies in flight at an abort (producer warps)
+  // Copies in flight at an abort, kept by the producer warps (lane 0 is thread 0).
+  uint32_t kuse[kNK] = {0u, 0u, 0u};   // score CTAs: uses of each K stage (each unit starts at stage 0)
+  uint32_t vc_total = 0;               // output CTAs: V stages issued
 
   if (!is_out) {
     // ================================================================ score CTAs
     if (warp == 0) {
-      // ------------------------------------------------------------ Q and K copies
-      if (lane == 0) {   // Q of head h: 8 boxes of 64 dims x 128 rows (rows outside T read as 0)
-        prefetch_tmap(&tmap_q);
-        mbar_arrive_expect_tx(&bar.q_full, 8 * kQChunk);
-#pragma unroll
-        for (int c = 0; c < 8; ++c) tma_load_3d(q_stage + c * kQChunk, &tmap_q, 64 * c, h, q_row0, &bar.q_full);
-      }
-      // Lanes 0-3 copy the un-rotated dims of page `lane` of this CTA's 64 keys, lanes 4-7 its
-      // k_rot block. Pages outside [0, k_hi] are neither looked up nor copied. Block indices come
-      // from the page table ahead of use: lane l holds page (l & 3) of tile (l >> 2) of the
-      // current group of 8 tiles, and the next group is looked up one group early.
+      // ------------------------------------------------------------ K copies
       if (lane == 0) {
         prefetch_tmap(&tmap_s);
         prefetch_tmap(&tmap_rot);
       }
       const int pl = lane & 3;
-      auto load_blocks = [&](int j0) -> int {
-        const int jt = j0 + (lane >> 2);
-        if (jt >= n_tiles) return -1;
-        return page_block((kt0 + jt) * kTN + 64 * (int)pr + kPage * (lane & 3), k_lo, k_hi, pt, p.num_pages, p.hkv,
-                          g, p.err);
-      };
-      int blk_cur = load_blocks(0), blk_next = load_blocks(8);
-      int j = 0;
-      for (; j < n_tiles; ++j) {
-        const int s = j % kNK;
-        if (j > 0 && (j & 7) == 0) {
-          blk_cur = blk_next;
-          blk_next = load_blocks(j + 8);
+      bool ok = true;
+      for (int u = cluster, ui = 0; ok && u < p.n_units; u += n_clusters) {
+        GUnit un;
+        if (!global_unit<kPart>(p, u, pr, un) || un.n_tiles == 0) continue;
+        // Lanes 0-3 copy the un-rotated dims of page `lane` of this CTA's 64 keys, lanes 4-7 its
+        // k_rot block. Pages outside [k_lo, k_hi] are neither looked up nor copied. Block indices
+        // come from the page table ahead of use: lane l holds page (l & 3) of tile (l >> 2) of the
+        // current group of 8 tiles, and the next group is looked up one group early.
+        auto load_blocks = [&](int j0) -> int {
+          const int jt = j0 + (lane >> 2);
+          if (jt >= un.n_tiles) return -1;
+          return page_block((un.kt0 + jt) * kTN + 64 * (int)pr + kPage * (lane & 3), un.k_lo, un.k_hi, un.pt,
+                            p.num_pages, p.hkv, un.g, p.err);
+        };
+        int blk_cur = load_blocks(0), blk_next = load_blocks(8);
+        for (int j = 0; j < un.n_tiles; ++j) {
+          const int s = j % kNK;
+          if (j > 0 && (j & 7) == 0) {
+            blk_cur = blk_next;
+            blk_next = load_blocks(j + 8);
+          }
+          const int bl = __shfl_sync(0xffffffffu, blk_cur, (j & 7) * 4 + (lane & 3));
+          const unsigned live = __ballot_sync(0xffffffffu, lane < 4 && bl >= 0);
+          const int blk = __shfl_sync(0xffffffffu, bl, pl);
+          bool okw = true;
+          if (lane == 0) {
+            // Stages 1-2 hold the unit's Q until the softmax warps have moved it; Q landed there
+            // only after the earlier tiles in them were read, so tile 2 needs no wait of its own.
+            if (j == 1)
+              okw = mbar_wait(&bar.q_moved, ui & 1, abort_flag, p.err, p.wait_ns);
+            else if (j != 2 && kuse[s] > 0)
+              okw = mbar_wait(&bar.k_empty[s], (kuse[s] - 1) & 1, abort_flag, p.err, p.wait_ns);
+          }
+          if (!__shfl_sync(0xffffffffu, okw, 0)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) mbar_arrive_expect_tx(&bar.k_full[s], __popc(live) * kKPageBytes);
+          __syncwarp();
+          if (lane < 8 && blk >= 0) {
+            uint8_t* st = base + s * kKStage;
+            if (lane < 4)   // box {64, 24 dim groups from 8, 2 halves, 2 key groups, 1 block}
+              tma_load_5d(st + pl * kUnrotPage, &tmap_s, 0, 8, 0, 0, blk, &bar.k_full[s]);
+            else            // box {64, 8 dim groups, 2 halves, 2 key groups, 1 block}
+              tma_load_5d(st + kRotOff + pl * kRotPage, &tmap_rot, 0, 0, 0, 0, blk, &bar.k_full[s]);
+          }
+          __syncwarp();
+          ++kuse[s];
         }
-        const int bl = __shfl_sync(0xffffffffu, blk_cur, (j & 7) * 4 + (lane & 3));
-        const unsigned live = __ballot_sync(0xffffffffu, lane < 4 && bl >= 0);
-        const int blk = __shfl_sync(0xffffffffu, bl, pl);
-        bool okw = true;
-        if (lane == 0) {
-          if (j == 1 || j == 2)   // stages 1-2 held Q until the softmax warps moved it
-            okw = mbar_wait(&bar.q_moved, 0, abort_flag, p.err, p.wait_ns);
-          else if (j >= kNK)
-            okw = mbar_wait(&bar.k_empty[s], ((j / kNK) - 1) & 1, abort_flag, p.err, p.wait_ns);
-        }
-        if (!__shfl_sync(0xffffffffu, okw, 0)) break;
-        if (lane == 0) mbar_arrive_expect_tx(&bar.k_full[s], __popc(live) * kKPageBytes);
-        __syncwarp();
-        if (lane < 8 && blk >= 0) {
-          uint8_t* st = base + s * kKStage;
-          if (lane < 4)   // box {64, 24 dim groups from 8, 2 halves, 2 key groups, 1 block}
-            tma_load_5d(st + pl * kUnrotPage, &tmap_s, 0, 8, 0, 0, blk, &bar.k_full[s]);
-          else            // box {64, 8 dim groups, 2 halves, 2 key groups, 1 block}
-            tma_load_5d(st + kRotOff + pl * kRotPage, &tmap_rot, 0, 0, 0, 0, blk, &bar.k_full[s]);
-        }
-        __syncwarp();
+        // (A unit of one tile never waits on q_moved; still, this warp is never two phases of it
+        // ahead, which a parity wait could not tell apart: the next unit's tile 0 waits for stage
+        // 0's last use, whose QK^T came after that unit's Q had moved.)
+        ++ui;
       }
-      k_issued = j;
     } else if (warp == 1 && !leader) {
       // ------------------------------------------------------------ K relay (rank 1)
-      for (int j = 0; j < n_tiles; ++j) {
-        const int s = j % kNK;
-        if (!__all_sync(0xffffffffu, mbar_wait(&bar.k_full[s], (j / kNK) & 1, abort_flag, p.err, p.wait_ns))) break;
-        if (lane == 0) mbar_arrive_remote(map_peer(smem_u32(&bar.k_peer[s]), pair_peer));
-        __syncwarp();
+      bool ok = true;
+      for (int u = cluster; ok && u < p.n_units; u += n_clusters) {
+        GUnit un;
+        if (!global_unit<kPart>(p, u, pr, un) || un.n_tiles == 0) continue;
+        for (int j = 0; j < un.n_tiles; ++j) {
+          const int s = j % kNK;
+          if (!__all_sync(0xffffffffu, mbar_wait(&bar.k_full[s], kuse[s] & 1, abort_flag, p.err, p.wait_ns))) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) mbar_arrive_remote(map_peer(smem_u32(&bar.k_peer[s]), pair_peer));
+          __syncwarp();
+          ++kuse[s];
+        }
       }
     } else if (warp == 1) {
       // ------------------------------------------------------------ QK^T issuer (rank 0)
-      bool ok = __all_sync(0xffffffffu, mbar_wait_cl(&bar.q_pair, 0, abort_flag, p.err, p.wait_ns));
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        const int s = j % kNK, sb = j % kNP;
-        // both CTAs' halves of the tile have landed; S buffer sb was read by tile j-2's softmax
-        ok = __all_sync(0xffffffffu, mbar_wait(&bar.k_full[s], (j / kNK) & 1, abort_flag, p.err, p.wait_ns) &&
-                                         mbar_wait_cl(&bar.k_peer[s], (j / kNK) & 1, abort_flag, p.err, p.wait_ns) &&
-                                         (j < kNP || mbar_wait_cl(&bar.s_free[sb], ((j - kNP) / kNP) & 1, abort_flag, p.err, p.wait_ns)));
-        if (!ok) break;
-        tc_fence_after();
-        if (lane == 0) {
-          const uint32_t st = smem_u32(base + s * kKStage);
-          const uint32_t sd = tm + kTmS + kTN * sb;
+      bool ok = true;
+      int tc = 0;
+      for (int u = cluster, ui = 0; ok && u < p.n_units; u += n_clusters) {
+        GUnit un;
+        if (!global_unit<kPart>(p, u, pr, un) || un.n_tiles == 0) continue;
+        ok = __all_sync(0xffffffffu, mbar_wait_cl(&bar.q_pair, ui & 1, abort_flag, p.err, p.wait_ns));
+        for (int j = 0; ok && j < un.n_tiles; ++j) {
+          const int s = j % kNK, gt = tc + j, sb = gt % kNP;
+          // both CTAs' halves of the tile have landed; S buffer sb was read by tile gt-2's softmax
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait(&bar.k_full[s], kuse[s] & 1, abort_flag, p.err, p.wait_ns) &&
+                              mbar_wait_cl(&bar.k_peer[s], kuse[s] & 1, abort_flag, p.err, p.wait_ns) &&
+                              (gt < kNP ||
+                               mbar_wait_cl(&bar.s_free[sb], ((gt - kNP) / kNP) & 1, abort_flag, p.err, p.wait_ns)));
+          if (!ok) break;
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t st = smem_u32(base + s * kKStage);
+            const uint32_t sd = tm + kTmS + kTN * sb;
 #pragma unroll
-          for (int ks = 0; ks < kGD / 16; ++ks) {   // dims 16ks .. 16ks+15
-            const int hh = ks >> 4, kk = ks & 15;
-            const uint64_t bd = kk < 4 ? desc_tiled(st + kRotOff + hh * kRotCM + kk * 256, 128, kRotKG)
-                                       : desc_tiled(st + hh * kUnrotCM + (kk - 4) * 256, 128, kUnrotKG);
-            mma2_ts(sd, tm + kTmQ + 8 * ks, bd, kIdescQK, ks > 0 ? 1u : 0u);
+            for (int ks = 0; ks < kGD / 16; ++ks) {   // dims 16ks .. 16ks+15
+              const int hh = ks >> 4, kk = ks & 15;
+              const uint64_t bd = kk < 4 ? desc_tiled(st + kRotOff + hh * kRotCM + kk * 256, 128, kRotKG)
+                                         : desc_tiled(st + hh * kUnrotCM + (kk - 4) * 256, 128, kUnrotKG);
+              mma2_ts(sd, tm + kTmQ + 8 * ks, bd, kIdescQK, ks > 0 ? 1u : 0u);
+            }
+            mma2_commit_mc(&bar.s_full[sb], kScorePair);
+            mma2_commit_mc(&bar.k_empty[s], kScorePair);
           }
-          mma2_commit_mc(&bar.s_full[sb], kScorePair);
-          mma2_commit_mc(&bar.k_empty[s], kScorePair);
+          __syncwarp();
+          ++kuse[s];
         }
-        __syncwarp();
+        tc += un.n_tiles;
+        ++ui;
       }
     } else if (warp >= 2 && warp <= 5) {
-      // ------------------------------------------------------------ Q move, softmax, P
+      // ------------------------------------------------------------ Q issue and move, softmax, P
       const int r = 32 * (warp & 3) + lane;   // query row = tensor-memory lane
       const int wq = warp & 3;
       const uint32_t tq = tm + tmem_lane_base(warp);
-      const int pos = kBM * t + r;
-      const bool row_ok = pos >= p_lo && pos <= p_hi;
-      int row_hi = pos, row_lo = k_lo;   // the row sees keys row_lo .. row_hi
-      if (kPart) row_hi = min(pos, k_hi);
-      if (p.rows.span && row_ok) {
-        int span_lo;   // 0 on a global layer
-        row_keys(p.rows, 0, q_row0 + r, pos, ctx_end, p.err, span_lo, row_hi);
-        if (row_hi > k_hi) {   // spans that disagree between rows
-          set_error(p.err, kErrSpan);
-          row_hi = k_hi;
-        }
-      }
-      bool ok = __all_sync(0xffffffffu, mbar_wait(&bar.q_full, 0, abort_flag, p.err, p.wait_ns));
-      if (kRope && ok) {   // thread i rotates pair i % 64 of rows 64 (i / 64) .. + 63
-        const int qi = threadIdx.x - 64;
-        rotate_q_pair<4, kGlobalR>(q_stage, q_stage + 4 * kQChunk, p.tb, qi & 63, kBM * t, 64 * (qi >> 6));
-        fence_proxy_async();   // the K copies that later refill this area write through the async proxy
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bar.q_rot);
-        ok = __all_sync(0xffffffffu, mbar_wait(&bar.q_rot, 0, abort_flag, p.err, p.wait_ns));
-      }
-      if (ok) {   // Q (128B-swizzled boxes in K stages 1-2) -> tensor memory, bf16 pairs
-        const uint8_t* qrow = q_stage + r * 128;
-        auto load_chunk = [&](int c, uint32_t (&w)[32]) {
-#pragma unroll
-          for (int q8 = 0; q8 < 8; ++q8) {
-            const uint4 v = *reinterpret_cast<const uint4*>(qrow + c * kQChunk + ((q8 ^ (r & 7)) * 16));
-            w[4 * q8] = v.x;
-            w[4 * q8 + 1] = v.y;
-            w[4 * q8 + 2] = v.z;
-            w[4 * q8 + 3] = v.w;
-          }
-        };
-#pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
-          uint32_t w[32];
-          load_chunk(c, w);
-          tmem_st32(tq + kTmQ + 32 * c, w);   // dims 64c .. 64c+63 -> columns 32c .. 32c+31
-        }
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&bar.q_moved);
-          arrive_leader(&bar.q_pair);
-        }
-      }
       const uint32_t p_dst = map_peer(smem_u32(base + kOOffP), partner);
       const uint32_t pfull_dst = map_peer(smem_u32(&bar.p_full[0]), partner);
       uint8_t* stg = base + kSOffStage;
       const float cl2 = p.scale_log2;
-      float m_used = -INFINITY, l_run = 0.f;
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        const int sb = j % kNP;
-        const int kb = (kt0 + j) * kTN;
-        // Waits are made warp-uniform so that every lane leaves the loop together on an abort.
-        if (!__all_sync(0xffffffffu, mbar_wait(&bar.s_full[sb], (j / kNP) & 1, abort_flag, p.err, p.wait_ns))) {
-          ok = false;
-          break;
+      bool ok = true;
+      int tc = 0;
+      uint32_t kq[kNK] = {0u, 0u, 0u};   // uses of each K stage by the earlier units (thread 64)
+      if (threadIdx.x == 64) prefetch_tmap(&tmap_q);
+      for (int u = cluster, ui = 0; ok && u < p.n_units; u += n_clusters) {
+        GUnit un;
+        if (!global_unit<kPart>(p, u, pr, un)) continue;
+        const int pos = kBM * un.t + r;
+        const bool row_ok = pos >= un.p_lo && pos <= un.p_hi;
+        if (un.n_tiles == 0) {   // kPart: no key of the range: an empty partial
+          if (row_ok)
+            reinterpret_cast<float2*>(p.ml_part)[(size_t)(un.q_row0 + r) * p.hq + un.h] = make_float2(-INFINITY, 0.f);
+          continue;
         }
-        tc_fence_after();
-        uint32_t sr[kTN];
+        // The unit's Q (8 boxes of 64 dims x 128 rows, rows outside T read as 0) goes into K stages
+        // 1-2 and the first bytes of the P staging, once the earlier units' key tiles there have
+        // been read by QK^T and the last P copy has left the staging. Thread 64 issues it: the
+        // softmax warps wait every phase of the staging barrier in order, so this wait is one
+        // phase ahead at most.
+        if (threadIdx.x == 64) {
+          bool okq = true;
+          for (int s = 1; okq && s <= 2; ++s)
+            if (kq[s] > 0) okq = mbar_wait(&bar.k_empty[s], (kq[s] - 1) & 1, abort_flag, p.err, p.wait_ns);
+          if (okq && tc > 0) okq = mbar_wait_cl(&bar.stg_free, (tc - 1) & 1, abort_flag, p.err, p.wait_ns);
+          if (okq) {
+            mbar_arrive_expect_tx(&bar.q_full, 8 * kQChunk);
 #pragma unroll
-        for (int c = 0; c < kTN / 32; ++c)
-          tmem_ld32(tq + kTmS + kTN * sb + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
-        tmem_ld_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) arrive_leader(&bar.s_free[sb]);   // buffer sb may take QK^T of tile j+2
-
-        float s[kTN];
-#pragma unroll
-        for (int c = 0; c < kTN; ++c) s[c] = __uint_as_float(sr[c]);
-        if constexpr (kPart) {   // the row's keys in this tile: one run [lo, hi] of columns
-          if (!(row_ok && kb >= row_lo && kb + kTN - 1 <= row_hi)) {
-            int lo = row_lo - kb, hi = row_ok ? row_hi - kb : -1;
-            if (hi < lo) lo = hi = 1 << 20;   // none
-            const unsigned span = (unsigned)(hi - lo);
-#pragma unroll
-            for (int c = 0; c < kTN; ++c) s[c] = ((unsigned)(c - lo) <= span) ? s[c] : -INFINITY;
-          }
-        } else if (!(row_ok && kb + kTN - 1 <= row_hi)) {   // causal mask (and rows outside the sequence)
-          const int hi = row_ok ? row_hi - kb : -1;
-#pragma unroll
-          for (int c = 0; c < kTN; ++c) s[c] = (c <= hi) ? s[c] : -INFINITY;
-        }
-        float mx[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          mx[i] = s[i];
-#pragma unroll
-          for (int c = 1; c < kTN / 8; ++c) mx[i] = fmaxf(mx[i], s[i + 8 * c]);
-        }
-        const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * cl2;
-        float alpha = 1.f;   // O rescale owed before P_j V_j (1 unless the reference rose by > 2^8)
-        if (mt > m_used + kLazyRescale) {
-          if (m_used != -INFINITY) alpha = ex2(m_used - mt);
-          m_used = mt;
-        }
-        const float neg_m = (m_used == -INFINITY) ? 0.f : -m_used;
-        uint32_t pw[kTN / 2];
-        float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int w = 0; w < kTN / 2; ++w) {
-          const float e0 = ex2(fmaf(s[2 * w], cl2, neg_m));
-          const float e1 = ex2(fmaf(s[2 * w + 1], cl2, neg_m));
-          ls[w & 3] += e0;
-          ls[w & 3] += e1;
-          pw[w] = pack_bf16(e0, e1);   // declared cast: P in bf16 for P.V
-        }
-        l_run = fmaf(l_run, alpha, (ls[0] + ls[1]) + (ls[2] + ls[3]));
-
-        // The staging area is free once the previous tile's copies have landed.
-        if (j > 0 && !__all_sync(0xffffffffu, mbar_wait_cl(&bar.stg_free, (j - 1) & 1, abort_flag, p.err, p.wait_ns))) {
-          ok = false;
-          break;
-        }
-        uint8_t* prow = stg + (r >> 3) * kPRowGroup + (r & 7) * 16;
-#pragma unroll
-        for (int kg = 0; kg < kTN / 8; ++kg)   // keys 8kg .. 8kg+7 of row r: one core-matrix row
-          *reinterpret_cast<uint4*>(prow + kg * 128) = make_uint4(pw[4 * kg], pw[4 * kg + 1], pw[4 * kg + 2], pw[4 * kg + 3]);
-        *reinterpret_cast<uint4*>(prow + 16 * 128) = make_uint4(__float_as_uint(alpha), __float_as_uint(l_run), 0u, 0u);
-        fence_proxy_async();   // the bulk copies read what the generic stores wrote
-        __syncwarp();
-        bool okp = true;
-        if (lane == 0) {
-          // P slot sb of the output CTA was last read by P.V of tile j-2
-          okp = j < kNP || mbar_wait_cl(&bar.p_free[sb], ((j - kNP) / kNP) & 1, abort_flag, p.err, p.wait_ns);
-          if (okp) {
-            bulk_s2peer(p_dst + sb * kPSlot + wq * kPWarpBytes, stg + wq * kPWarpBytes, kPWarpBytes, pfull_dst + sb * 8);
+            for (int c = 0; c < 8; ++c)
+              tma_load_3d(q_stage + c * kQChunk, &tmap_q, 64 * c, un.h, un.q_row0, &bar.q_full);
+            bar.q_issued = ui + 1;
           }
         }
-        if (!__shfl_sync(0xffffffffu, okp, 0)) ok = false;
+        for (int j = 0; j < un.n_tiles; ++j) ++kq[j % kNK];
+        int row_hi = pos, row_lo = un.k_lo;   // the row sees keys row_lo .. row_hi
+        if (kPart) row_hi = min(pos, un.k_hi);
+        if (p.rows.span && row_ok) {
+          int span_lo;   // 0 on a global layer
+          row_keys(p.rows, 0, un.q_row0 + r, pos, un.ctx_end, p.err, span_lo, row_hi);
+          if (row_hi > un.k_hi) {   // spans that disagree between rows
+            set_error(p.err, kErrSpan);
+            row_hi = un.k_hi;
+          }
+        }
+        // The earlier unit's QK^T are all done (its last S was read), so Q may be replaced.
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar.q_full, ui & 1, abort_flag, p.err, p.wait_ns));
+        if (kRope && ok) {   // thread i rotates pair i % 64 of rows 64 (i / 64) .. + 63
+          const int qi = threadIdx.x - 64;
+          rotate_q_pair<4, kGlobalR>(q_stage, q_stage + 4 * kQChunk, p.tb, qi & 63, kBM * un.t, 64 * (qi >> 6));
+          fence_proxy_async();   // the K copies that later refill this area write through the async proxy
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar.q_rot);
+          ok = __all_sync(0xffffffffu, mbar_wait(&bar.q_rot, ui & 1, abort_flag, p.err, p.wait_ns));
+        }
+        if (!ok) break;
+        {   // Q (128B-swizzled boxes in K stages 1-2) -> tensor memory, bf16 pairs
+          const uint8_t* qrow = q_stage + r * 128;
+#pragma unroll 1
+          for (int c = 0; c < 8; ++c) {
+            uint32_t w[32];
+#pragma unroll
+            for (int q8 = 0; q8 < 8; ++q8) {
+              const uint4 v = *reinterpret_cast<const uint4*>(qrow + c * kQChunk + ((q8 ^ (r & 7)) * 16));
+              w[4 * q8] = v.x;
+              w[4 * q8 + 1] = v.y;
+              w[4 * q8 + 2] = v.z;
+              w[4 * q8 + 3] = v.w;
+            }
+            tmem_st32(tq + kTmQ + 32 * c, w);   // dims 64c .. 64c+63 -> columns 32c .. 32c+31
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&bar.q_moved);
+            arrive_leader(&bar.q_pair);
+          }
+        }
+        float m_used = -INFINITY, l_run = 0.f;
+        for (int j = 0; ok && j < un.n_tiles; ++j) {
+          const int gt = tc + j, sb = gt % kNP;
+          const int kb = (un.kt0 + j) * kTN;
+          // Waits are made warp-uniform so that every lane leaves the loop together on an abort.
+          if (!__all_sync(0xffffffffu, mbar_wait(&bar.s_full[sb], (gt / kNP) & 1, abort_flag, p.err, p.wait_ns))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          uint32_t sr[kTN];
+#pragma unroll
+          for (int c = 0; c < kTN / 32; ++c)
+            tmem_ld32(tq + kTmS + kTN * sb + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
+          tmem_ld_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) arrive_leader(&bar.s_free[sb]);   // buffer sb may take QK^T of tile gt+2
+
+          float s[kTN];
+#pragma unroll
+          for (int c = 0; c < kTN; ++c) s[c] = __uint_as_float(sr[c]);
+          if constexpr (kPart) {   // the row's keys in this tile: one run [lo, hi] of columns
+            if (!(row_ok && kb >= row_lo && kb + kTN - 1 <= row_hi)) {
+              int lo = row_lo - kb, hi = row_ok ? row_hi - kb : -1;
+              if (hi < lo) lo = hi = 1 << 20;   // none
+              const unsigned span = (unsigned)(hi - lo);
+#pragma unroll
+              for (int c = 0; c < kTN; ++c) s[c] = ((unsigned)(c - lo) <= span) ? s[c] : -INFINITY;
+            }
+          } else if (!(row_ok && kb + kTN - 1 <= row_hi)) {   // causal mask (and rows outside the sequence)
+            const int hi = row_ok ? row_hi - kb : -1;
+#pragma unroll
+            for (int c = 0; c < kTN; ++c) s[c] = (c <= hi) ? s[c] : -INFINITY;
+          }
+          float mx[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            mx[i] = s[i];
+#pragma unroll
+            for (int c = 1; c < kTN / 8; ++c) mx[i] = fmaxf(mx[i], s[i + 8 * c]);
+          }
+          const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * cl2;
+          float alpha = 1.f;   // O rescale owed before P_j V_j (1 unless the reference rose by > 2^8)
+          if (mt > m_used + kLazyRescale) {
+            if (m_used != -INFINITY) alpha = ex2(m_used - mt);
+            m_used = mt;
+          }
+          const float neg_m = (m_used == -INFINITY) ? 0.f : -m_used;
+          uint32_t pw[kTN / 2];
+          float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int w = 0; w < kTN / 2; ++w) {
+            const float e0 = ex2(fmaf(s[2 * w], cl2, neg_m));
+            const float e1 = ex2(fmaf(s[2 * w + 1], cl2, neg_m));
+            ls[w & 3] += e0;
+            ls[w & 3] += e1;
+            pw[w] = pack_bf16(e0, e1);   // declared cast: P in bf16 for P.V
+          }
+          l_run = fmaf(l_run, alpha, (ls[0] + ls[1]) + (ls[2] + ls[3]));
+
+          // The staging area is free once the previous tile's copies have landed.
+          if (gt > 0 &&
+              !__all_sync(0xffffffffu, mbar_wait_cl(&bar.stg_free, (gt - 1) & 1, abort_flag, p.err, p.wait_ns))) {
+            ok = false;
+            break;
+          }
+          uint8_t* prow = stg + (r >> 3) * kPRowGroup + (r & 7) * 16;
+#pragma unroll
+          for (int kg = 0; kg < kTN / 8; ++kg)   // keys 8kg .. 8kg+7 of row r: one core-matrix row
+            *reinterpret_cast<uint4*>(prow + kg * 128) =
+                make_uint4(pw[4 * kg], pw[4 * kg + 1], pw[4 * kg + 2], pw[4 * kg + 3]);
+          *reinterpret_cast<uint4*>(prow + 16 * 128) = make_uint4(__float_as_uint(alpha), __float_as_uint(l_run), 0u, 0u);
+          fence_proxy_async();   // the bulk copies read what the generic stores wrote
+          __syncwarp();
+          bool okp = true;
+          if (lane == 0) {
+            // P slot sb of the output CTA was last read by P.V of tile gt-2
+            okp = gt < kNP || mbar_wait_cl(&bar.p_free[sb], ((gt - kNP) / kNP) & 1, abort_flag, p.err, p.wait_ns);
+            if (okp)
+              bulk_s2peer(p_dst + sb * kPSlot + wq * kPWarpBytes, stg + wq * kPWarpBytes, kPWarpBytes,
+                          pfull_dst + sb * 8);
+          }
+          if (!__shfl_sync(0xffffffffu, okp, 0)) ok = false;
+        }
+        // kPart: the row's softmax state; O (in the output CTA) is relative to the same running max
+        if (kPart && ok && row_ok)
+          reinterpret_cast<float2*>(p.ml_part)[(size_t)(un.q_row0 + r) * p.hq + un.h] = make_float2(m_used, l_run);
+        tc += un.n_tiles;
+        ++ui;
       }
-      // kPart: the row's softmax state; O (in the output CTA) is relative to the same running max
-      if (kPart && ok && row_ok)
-        reinterpret_cast<float2*>(p.ml_part)[(size_t)(q_row0 + r) * p.hq + h] = make_float2(m_used, l_run);
     }
   } else {
     // ================================================================ output CTAs
@@ -497,207 +566,225 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
     if (warp == 0) {
       // ------------------------------------------------------------ V copies
       const __nv_bfloat16* sc = (const __nv_bfloat16*)p.k_cache;
-      // Block indices ahead of use: lane l holds page (l & 3) of stage (l >> 2) of the current
-      // group of 8 stages; the next group is looked up one group early.
-      const int n_st = 2 * n_tiles;
-      auto load_blocks = [&](int c0) -> int {
-        const int cs2 = c0 + (lane >> 2);
-        if (cs2 >= n_st) return -1;
-        return page_block(kt0 * kTN + cs2 * kVN + kPage * (lane & 3), k_lo, k_hi, pt, p.num_pages, p.hkv, g, p.err);
-      };
-      int blk_cur = load_blocks(0), blk_next = load_blocks(8);
-      int c = 0;
-      for (; c < n_st; ++c) {
-        const int s = c % kNV;
-        if (c > 0 && (c & 7) == 0) {
-          blk_cur = blk_next;
-          blk_next = load_blocks(c + 8);
+      bool ok = true;
+      for (int u = cluster; ok && u < p.n_units; u += n_clusters) {
+        GUnit un;
+        if (!global_unit<kPart>(p, u, pr, un) || un.n_tiles == 0) continue;
+        // Block indices ahead of use: lane l holds page (l & 3) of stage (l >> 2) of the current
+        // group of 8 stages; the next group is looked up one group early.
+        const int n_st = 2 * un.n_tiles;
+        auto load_blocks = [&](int c0) -> int {
+          const int cs2 = c0 + (lane >> 2);
+          if (cs2 >= n_st) return -1;
+          return page_block(un.kt0 * kTN + cs2 * kVN + kPage * (lane & 3), un.k_lo, un.k_hi, un.pt, p.num_pages,
+                            p.hkv, un.g, p.err);
+        };
+        int blk_cur = load_blocks(0), blk_next = load_blocks(8);
+        for (int c = 0; c < n_st; ++c) {
+          const uint32_t vc = vc_total;
+          const int s = vc % kNV;
+          if (c > 0 && (c & 7) == 0) {
+            blk_cur = blk_next;
+            blk_next = load_blocks(c + 8);
+          }
+          const int bl0 = __shfl_sync(0xffffffffu, blk_cur, (c & 7) * 4 + (lane & 3));
+          const int bl = lane < 4 ? bl0 : -1;
+          const unsigned live = __ballot_sync(0xffffffffu, bl >= 0);
+          bool okw = true;
+          if (lane == 0 && vc >= (uint32_t)kNV)
+            okw = mbar_wait(&bar.v_empty[s], ((vc / kNV) - 1) & 1, abort_flag, p.err, p.wait_ns);
+          if (!__shfl_sync(0xffffffffu, okw, 0)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) mbar_arrive_expect_tx(&bar.v_full[s], __popc(live) * kVPageBytes);
+          __syncwarp();
+          if (bl >= 0)
+            bulk_g2s(base + s * kVStage + lane * kVPageBytes, sc + (size_t)bl * (kPage * kGD) + hv * (kPage * kHalf),
+                     kVPageBytes, &bar.v_full[s]);
+          __syncwarp();
+          ++vc_total;
         }
-        const int bl0 = __shfl_sync(0xffffffffu, blk_cur, (c & 7) * 4 + (lane & 3));
-        const int bl = lane < 4 ? bl0 : -1;
-        const unsigned live = __ballot_sync(0xffffffffu, bl >= 0);
-        bool okw = true;
-        if (lane == 0 && c >= kNV) okw = mbar_wait(&bar.v_empty[s], ((c / kNV) - 1) & 1, abort_flag, p.err, p.wait_ns);
-        if (!__shfl_sync(0xffffffffu, okw, 0)) break;
-        if (lane == 0) mbar_arrive_expect_tx(&bar.v_full[s], __popc(live) * kVPageBytes);
-        __syncwarp();
-        if (bl >= 0)
-          bulk_g2s(base + s * kVStage + lane * kVPageBytes, sc + (size_t)bl * (kPage * kGD) + hv * (kPage * kHalf),
-                   kVPageBytes, &bar.v_full[s]);
-        __syncwarp();
       }
-      v_issued = c;
     } else if (warp == 1) {
       // ------------------------------------------------------------ V check; P.V issuer (rank 2) or relay (rank 3)
       // Value rows of keys that hold no data of this sequence are zeroed before P.V: pages past
       // the last needed one were not copied and keep an older tile, and slots past the
       // sequence's last key may hold anything (NaN); P = 0 there does not cancel NaN.
       bool ok = true;
-      const int n_st = 2 * n_tiles;
-      for (int c = 0; ok && c < n_st; ++c) {
-        const int s = c % kNV, j = c >> 1, e = c & 1;
-        ok = __all_sync(0xffffffffu, mbar_wait(&bar.v_full[s], (c / kNV) & 1, abort_flag, p.err, p.wait_ns));
-        if (!ok) break;
-        const int kb = kt0 * kTN + c * kVN;
-        // kPart: a rank's cache may hold another rank's keys, or nothing, around its range
-        const int v0 = kPart ? k_lo : 0;
-        const int v1 = kPart ? min(kb + kVN, k_hi + 1) : min(min(kb + kVN, ((k_hi >> 4) + 1) * kPage), ctx_end);
-        if (v0 > kb || v1 < kb + kVN) {
-          uint8_t* vt = base + s * kVStage;
-          for (int idx = lane; idx < kVN * 32; idx += 32) {
-            const int rr = idx >> 5, dg = idx & 31;
-            if (kb + rr < v0 || kb + rr >= v1)
-              *reinterpret_cast<uint4*>(vt + (rr >> 3) * kVKG + dg * 128 + (rr & 7) * 16) = make_uint4(0, 0, 0, 0);
+      uint32_t vc = 0;
+      int tc = 0;
+      for (int u = cluster, ui = 0; ok && u < p.n_units; u += n_clusters) {
+        GUnit un;
+        if (!global_unit<kPart>(p, u, pr, un) || un.n_tiles == 0) continue;
+        const int n_st = 2 * un.n_tiles;
+        for (int c = 0; ok && c < n_st; ++c, ++vc) {
+          const int s = vc % kNV, j = c >> 1, e = c & 1, gt = tc + j;
+          ok = __all_sync(0xffffffffu, mbar_wait(&bar.v_full[s], (vc / kNV) & 1, abort_flag, p.err, p.wait_ns));
+          if (!ok) break;
+          const int kb = un.kt0 * kTN + c * kVN;
+          // kPart: a rank's cache may hold another rank's keys, or nothing, around its range
+          const int v0 = kPart ? un.k_lo : 0;
+          const int v1 = kPart ? min(kb + kVN, un.k_hi + 1)
+                               : min(min(kb + kVN, ((un.k_hi >> 4) + 1) * kPage), un.ctx_end);
+          if (v0 > kb || v1 < kb + kVN) {
+            uint8_t* vt = base + s * kVStage;
+            for (int idx = lane; idx < kVN * 32; idx += 32) {
+              const int rr = idx >> 5, dg = idx & 31;
+              if (kb + rr < v0 || kb + rr >= v1)
+                *reinterpret_cast<uint4*>(vt + (rr >> 3) * kVKG + dg * 128 + (rr & 7) * 16) = make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async();
           }
-          fence_proxy_async();
-        }
-        __syncwarp();
-        if (!leader) {
-          if (lane == 0) mbar_arrive_remote(map_peer(smem_u32(&bar.v_ready[s]), pair_peer));
           __syncwarp();
-          continue;
-        }
-        // rank 3's half is ready; at a tile's first half, both CTAs have P_j and have applied alpha
-        ok = __all_sync(0xffffffffu, mbar_wait_cl(&bar.v_ready[s], (c / kNV) & 1, abort_flag, p.err, p.wait_ns) &&
-                                         (e == 1 || mbar_wait_cl(&bar.o_ready[j % kNP], (j / kNP) & 1, abort_flag, p.err, p.wait_ns)));
-        if (!ok) break;
-        tc_fence_after();
-        if (lane == 0) {
-          const uint32_t va = smem_u32(base + s * kVStage);
-          const uint32_t pa = smem_u32(base + kOOffP + (j % kNP) * kPSlot);
-#pragma unroll
-          for (int k = 0; k < kVN / 16; ++k) {   // 16 keys (two key groups) per step
-            const uint32_t acc = (j > 0 || e > 0 || k > 0) ? 1u : 0u;
-            const uint64_t ad = desc_tiled(pa + (4 * e + k) * 256, 128, kPRowGroup);
-            mma2_ss(tm + kTmO, ad, desc_tiled(va + k * 2 * kVKG, kVKG, 128), kIdescPV, acc);
-            mma2_ss(tm + kTmO + 256, ad, desc_tiled(va + k * 2 * kVKG + 2048, kVKG, 128), kIdescPV, acc);
+          if (!leader) {
+            if (lane == 0) mbar_arrive_remote(map_peer(smem_u32(&bar.v_ready[s]), pair_peer));
+            __syncwarp();
+            continue;
           }
-          mma2_commit_mc(&bar.v_empty[s], kOutPair);
-          if (e == 1) mma2_commit_mc(&bar.pv_done[j % kNP], kOutPair);
+          // rank 3's half is ready; at a tile's first half, both CTAs have P_j and have applied
+          // alpha; at a unit's first step, both have read the earlier unit's O out
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait_cl(&bar.v_ready[s], (vc / kNV) & 1, abort_flag, p.err, p.wait_ns) &&
+                              (e == 1 ||
+                               mbar_wait_cl(&bar.o_ready[gt % kNP], (gt / kNP) & 1, abort_flag, p.err, p.wait_ns)) &&
+                              (c > 0 || ui == 0 || mbar_wait_cl(&bar.o_free, (ui - 1) & 1, abort_flag, p.err, p.wait_ns)));
+          if (!ok) break;
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t va = smem_u32(base + s * kVStage);
+            const uint32_t pa = smem_u32(base + kOOffP + (gt % kNP) * kPSlot);
+#pragma unroll
+            for (int k = 0; k < kVN / 16; ++k) {   // 16 keys (two key groups) per step
+              const uint32_t acc = (j > 0 || e > 0 || k > 0) ? 1u : 0u;
+              const uint64_t ad = desc_tiled(pa + (4 * e + k) * 256, 128, kPRowGroup);
+              mma2_ss(tm + kTmO, ad, desc_tiled(va + k * 2 * kVKG, kVKG, 128), kIdescPV, acc);
+              mma2_ss(tm + kTmO + 256, ad, desc_tiled(va + k * 2 * kVKG + 2048, kVKG, 128), kIdescPV, acc);
+            }
+            mma2_commit_mc(&bar.v_empty[s], kOutPair);
+            if (e == 1) mma2_commit_mc(&bar.pv_done[gt % kNP], kOutPair);
+          }
+          __syncwarp();
         }
-        __syncwarp();
+        tc += un.n_tiles;
+        ++ui;
       }
     } else if (warp >= 2 && warp <= 5) {
       // ------------------------------------------------------------ alpha, O rescale, epilogue
       const int r = 32 * (warp & 3) + lane;
       const uint32_t tq = tm + tmem_lane_base(warp);
-      const int pos = kBM * t + r;
-      const bool row_ok = pos >= p_lo && pos <= p_hi;
       const uint32_t stg_free_dst = map_peer(smem_u32(&bar.stg_free), partner);
-      float l_last = 0.f;
       bool ok = true;
-      for (int j = 0; j < n_tiles; ++j) {
-        const int sb = j % kNP;
-        if (!__all_sync(0xffffffffu, mbar_wait_cl(&bar.p_full[sb], (j / kNP) & 1, abort_flag, p.err, p.wait_ns))) {
-          ok = false;
-          break;
+      int tc = 0;
+      for (int u = cluster; ok && u < p.n_units; u += n_clusters) {
+        GUnit un;
+        if (!global_unit<kPart>(p, u, pr, un)) continue;
+        const int pos = kBM * un.t + r;
+        const bool row_ok = pos >= un.p_lo && pos <= un.p_hi;
+        if (un.n_tiles == 0) {   // kPart: no key of the range: an empty partial
+          if (row_ok) {
+            float4* dst = reinterpret_cast<float4*>(p.o_part + ((size_t)(un.q_row0 + r) * p.hq + un.h) * kGD);
+            for (int i = 0; i < kGD / 4; ++i) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+          continue;
         }
-        const float2 ax = *reinterpret_cast<const float2*>(base + kOOffP + sb * kPSlot + (r >> 3) * kPRowGroup +
-                                                          16 * 128 + (r & 7) * 16);
-        if (threadIdx.x == 64) {
-          bar.p_seen[sb] = j / kNP + 1;
-          if (j + 1 < n_tiles) mbar_arrive_remote(stg_free_dst);   // the score CTA may refill its staging
-        }
-        l_last = ax.y;
-        const bool need = j > 0 && ax.x != 1.f;
-        if (__any_sync(0xffffffffu, need)) {   // O correction, after P_{j-1} V_{j-1} has landed
-          const int jp = j - 1;
-          if (!__all_sync(0xffffffffu, mbar_wait(&bar.pv_done[jp % kNP], (jp / kNP) & 1, abort_flag, p.err, p.wait_ns))) {
+        float l_last = 0.f;
+        for (int j = 0; j < un.n_tiles; ++j) {
+          const int gt = tc + j, sb = gt % kNP;
+          if (!__all_sync(0xffffffffu, mbar_wait_cl(&bar.p_full[sb], (gt / kNP) & 1, abort_flag, p.err, p.wait_ns))) {
             ok = false;
             break;
           }
-          tc_fence_after();
-          const float a = need ? ax.x : 1.f;
-#pragma unroll 1
-          for (int cc = 0; cc < kGD / 32; ++cc) {
-            uint32_t o[32];
-            tmem_ld32(tq + kTmO + 32 * cc, o);
-            tmem_ld_wait();
-#pragma unroll
-            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * a);
-            tmem_st32(tq + kTmO + 32 * cc, o);
+          const float2 ax = *reinterpret_cast<const float2*>(base + kOOffP + sb * kPSlot + (r >> 3) * kPRowGroup +
+                                                            16 * 128 + (r & 7) * 16);
+          if (threadIdx.x == 64) {
+            bar.p_seen[sb] = gt / kNP + 1;
+            mbar_arrive_remote(stg_free_dst);   // the score CTA may refill its staging
           }
-          tmem_st_wait();
+          l_last = ax.y;
+          const bool need = j > 0 && ax.x != 1.f;
+          if (__any_sync(0xffffffffu, need)) {   // O correction, after P_{j-1} V_{j-1} has landed
+            const int gp = gt - 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(&bar.pv_done[gp % kNP], (gp / kNP) & 1, abort_flag, p.err,
+                                                   p.wait_ns))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const float a = need ? ax.x : 1.f;
+#pragma unroll 1
+            for (int cc = 0; cc < kGD / 32; ++cc) {
+              uint32_t o[32];
+              tmem_ld32(tq + kTmO + 32 * cc, o);
+              tmem_ld_wait();
+#pragma unroll
+              for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * a);
+              tmem_st32(tq + kTmO + 32 * cc, o);
+            }
+            tmem_st_wait();
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) arrive_leader(&bar.o_ready[sb]);
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) arrive_leader(&bar.o_ready[sb]);
-      }
-      // Epilogue: O / l -> bf16, rows of this sequence only. A tile whose 128 rows all belong to
-      // the sequence is staged in the V ring, idle once the last P.V has completed, as the eight
-      // 128B-swizzled boxes (64 dims x 128 rows) of the output tensor map, and written by eight
-      // TMA stores; any other tile is written row by row, so that rows of other sequences and
-      // padding are never touched.
-      const int jl = n_tiles - 1;
-      const bool staged = !kPart && p_lo == kBM * t && p_hi == kBM * t + kBM - 1;
-      uint8_t* const ep = base + ((1024u - (smem_u32(base) & 1023u)) & 1023u);   // box-aligned
-      bool ok_ep = ok && __all_sync(0xffffffffu, mbar_wait(&bar.pv_done[jl % kNP], (jl / kNP) & 1, abort_flag, p.err, p.wait_ns));
-      if (ok_ep) {
+        if (!ok) break;
+        // Epilogue: O / l -> bf16 rows of this sequence only, row-contiguous stores (kPart: the
+        // un-normalised fp32 rows). Once O is in registers, the next unit's first P.V (which
+        // overwrites it) may start.
+        const int gl = tc + un.n_tiles - 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(&bar.pv_done[gl % kNP], (gl / kNP) & 1, abort_flag, p.err, p.wait_ns))) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         const float inv = (l_last > 0.f) ? __frcp_rn(l_last) : 0.f;
-        __nv_bfloat16* orow = p.out + ((size_t)(q_row0 + r) * p.hq + h) * kGD;
-        float* prow = kPart ? p.o_part + ((size_t)(q_row0 + r) * p.hq + h) * kGD : nullptr;
+        const unsigned valid = __ballot_sync(0xffffffffu, row_ok);
+        const long long wrow0 = (long long)un.q_row0 + 32 * (warp & 3);
+        float* prow = kPart ? p.o_part + ((size_t)(un.q_row0 + r) * p.hq + un.h) * kGD : nullptr;
         tmem_ld_stream64<kGD / 64>(
-            tq + kTmO, [] {},
+            tq + kTmO,
+            [&]() {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) arrive_leader(&bar.o_free);
+            },
             [&](int c, const uint32_t(&o)[64]) {
 #pragma unroll
               for (int half = 0; half < 2; ++half) {
-                if constexpr (kPart) {   // the un-normalised fp32 output of the row
+                const int d0 = o_dim(64 * c + 32 * half);   // 32 consecutive dims
+                if constexpr (kPart) {
                   if (row_ok) {
-                    float4* dst = reinterpret_cast<float4*>(prow + o_dim(64 * c + 32 * half));
+                    float4* dst = reinterpret_cast<float4*>(prow + d0);
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
                       dst[i] = make_float4(__uint_as_float(o[32 * half + 4 * i]), __uint_as_float(o[32 * half + 4 * i + 1]),
                                            __uint_as_float(o[32 * half + 4 * i + 2]),
                                            __uint_as_float(o[32 * half + 4 * i + 3]));
                   }
-                  continue;
-                }
-                uint32_t w16[16];
+                } else {
+                  uint32_t w16[16];
 #pragma unroll
-                for (int k = 0; k < 16; ++k)
-                  w16[k] = pack_bf16(__uint_as_float(o[32 * half + 2 * k]) * inv,
-                                     __uint_as_float(o[32 * half + 2 * k + 1]) * inv);
-                const int d0 = o_dim(64 * c + 32 * half);   // 32 consecutive dims: half a box
-                if (staged) {
-                  uint8_t* row = ep + (d0 >> 6) * kQChunk + r * 128;
-                  const int q0 = (d0 & 63) >> 3;
-#pragma unroll
-                  for (int i = 0; i < 4; ++i)
-                    *reinterpret_cast<uint4*>(row + (((q0 + i) ^ (r & 7)) * 16)) =
-                        make_uint4(w16[4 * i], w16[4 * i + 1], w16[4 * i + 2], w16[4 * i + 3]);
-                } else if (row_ok) {
-                  uint4* dst = reinterpret_cast<uint4*>(orow + d0);
-#pragma unroll
-                  for (int i = 0; i < 4; ++i)
-                    dst[i] = make_uint4(w16[4 * i], w16[4 * i + 1], w16[4 * i + 2], w16[4 * i + 3]);
+                  for (int k = 0; k < 16; ++k)
+                    w16[k] = pack_bf16(__uint_as_float(o[32 * half + 2 * k]) * inv,
+                                       __uint_as_float(o[32 * half + 2 * k + 1]) * inv);
+                  store_rows32<kGD>(w16, p.out, wrow0, p.hq, un.h, d0, valid, lane);
                 }
               }
             });
-      }
-      if (staged) {   // one thread stores the eight boxes once every epilogue warp has staged its rows
-        fence_proxy_async();
-        __syncwarp();
-        if (lane == 0 && ok_ep) mbar_arrive(&bar.ep_staged);
-        if (threadIdx.x == 64 && ok_ep && mbar_wait(&bar.ep_staged, 0, abort_flag, p.err, p.wait_ns)) {
-#pragma unroll
-          for (int c = 0; c < kGD / 64; ++c) tma_store_3d(&tmap_o, ep + c * kQChunk, 64 * c, h, q_row0);
-          bulk_commit_group();
-          bulk_wait_group_read0();   // the staging has been read; the writes complete on their own
-        }
-        __syncwarp();
+        tc += un.n_tiles;
       }
     } else if (warp == 6) {
       // ------------------------------------------------------------ P slot hand-back
-      // Once P.V of tile j has completed, its P slot takes tile j+2: post the bytes that tile's
-      // copies will deliver, then tell the score CTA (posting first keeps the count ahead).
+      // Once P.V of tile gt has completed, its P slot takes tile gt+2 (of this unit or a later
+      // one): post the bytes that tile's copies will deliver, then tell the score CTA (posting
+      // first keeps the count ahead).
       if (lane == 0) {
         const uint32_t pfree_dst = map_peer(smem_u32(&bar.p_free[0]), partner);
-        for (int j = 0; j < n_tiles; ++j) {
-          if (!mbar_wait(&bar.pv_done[j % kNP], (j / kNP) & 1, abort_flag, p.err, p.wait_ns)) break;
-          if (j + kNP < n_tiles) {
-            mbar_arrive_expect_tx(&bar.p_full[j % kNP], kPSendBytes);
-            mbar_arrive_remote(pfree_dst + (j % kNP) * 8);
+        for (int gt = 0; gt < total_tiles; ++gt) {
+          if (!mbar_wait(&bar.pv_done[gt % kNP], (gt / kNP) & 1, abort_flag, p.err, p.wait_ns)) break;
+          if (gt + kNP < total_tiles) {
+            mbar_arrive_expect_tx(&bar.p_full[gt % kNP], kPSendBytes);
+            mbar_arrive_remote(pfree_dst + (gt % kNP) * 8);
           }
         }
       }
@@ -708,18 +795,23 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
   // ------------------------------------------------------------ teardown
   // No CTA may free its tensor memory or leave while MMAs, copies or signals into it are in
   // flight. On an abort the flag is passed to the other three CTAs (their waits then end
-  // early), copies this CTA issued are drained (bounded), and a cluster barrier closes the unit.
+  // early), copies this CTA issued are drained (bounded), and a cluster barrier closes the cluster.
   __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (!*abort_flag && threadIdx.x == 0) {   // the last stage releases (MMA commits) have arrived
     const unsigned long long w0 = globaltimer();
-    const int n_st = is_out ? 2 * n_tiles : n_tiles, ring = is_out ? kNV : kNK;
-    uint64_t* empty = is_out ? bar.v_empty : bar.k_empty;
-    for (int s = 0; s < ring && s < n_st; ++s) {
-      const int last = s + ring * ((n_st - 1 - s) / ring);
-      while (!mbar_try_wait(smem_u32(&empty[s]), (last / ring) & 1) && globaltimer() - w0 < kWaitLimitNs) {
+    if (is_out) {
+      for (uint32_t s = 0; s < (uint32_t)kNV && s < vc_total; ++s) {
+        const uint32_t last = s + kNV * ((vc_total - 1 - s) / kNV);
+        while (!mbar_try_wait(smem_u32(&bar.v_empty[s]), (last / kNV) & 1) && globaltimer() - w0 < kWaitLimitNs) {
+        }
       }
+    } else {
+      for (int s = 0; s < kNK; ++s)
+        if (kuse[s] > 0)
+          while (!mbar_try_wait(smem_u32(&bar.k_empty[s]), (kuse[s] - 1) & 1) && globaltimer() - w0 < kWaitLimitNs) {
+          }
     }
   }
   if (*abort_flag) {
@@ -734,10 +826,12 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         }
       };
       if (!is_out) {
-        drain(&bar.q_full, 0);
-        for (int i = max(0, k_issued - kNK); i < k_issued; ++i) drain(&bar.k_full[i % kNK], (i / kNK) & 1);
+        if (bar.q_issued > 0) drain(&bar.q_full, (bar.q_issued - 1) & 1);
+        for (int s = 0; s < kNK; ++s)
+          if (kuse[s] > 0) drain(&bar.k_full[s], (kuse[s] - 1) & 1);
       } else {
-        for (int i = max(0, v_issued - kNV); i < v_issued; ++i) drain(&bar.v_full[i % kNV], (i / kNV) & 1);
+        for (uint32_t i = vc_total > (uint32_t)kNV ? vc_total - kNV : 0; i < vc_total; ++i)
+          drain(&bar.v_full[i % kNV], (i / kNV) & 1);
         for (int s = 0; s < kNP; ++s) drain(&bar.p_full[s], bar.p_seen[s] & 1);
       }
     }
@@ -875,26 +969,44 @@ cudaError_t launch_prefill_global(const SeqRows& rows, float scale_log2, const P
   // Partial calls take raw queries and no image spans.
   if (rows.span && q_raw) return cudaErrorInvalidValue;
   if (part && (!q_raw || rows.span)) return cudaErrorInvalidValue;
-  CUtensorMap mq, mo, ms, mr;   // queries (raw or staged), output rows, the cache's S and k_rot pages
+  CUtensorMap mq, ms, mr;   // queries (raw or staged), the cache's S and k_rot pages
   if (!q_map(&mq, q_raw ? q_raw : out, rows.T, cache.hq, kGD)) return cudaErrorInvalidValue;
-  if (!q_map(&mo, part ? q_raw : out, rows.T, cache.hq, kGD)) return cudaErrorInvalidValue;   // unused by partials
   if (!page_maps(&ms, &mr, cache.k, cache.krot, cache.num_pages, cache.hkv)) return cudaErrorInvalidValue;
   auto kernel = part ? prefill_global_kernel<true, true>
                      : (q_raw ? prefill_global_kernel<true, false> : prefill_global_kernel<false, false>);
   const int ki = part ? 2 : (q_raw ? 1 : 0);
   static bool attr[64][3] = {};
+  static int max_clusters[64][3] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr[dev][ki]) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGlobalSmemBytes);
     if (e != cudaSuccess) return e;
+    // clusters that fit on the device at once: the persistent grid
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(4, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kGlobalSmemBytes;
+    cudaLaunchAttribute la[1];
+    la[0].id = cudaLaunchAttributeClusterDimension;
+    la[0].val.clusterDim.x = 4;
+    la[0].val.clusterDim.y = 1;
+    la[0].val.clusterDim.z = 1;
+    cfg.attrs = la;
+    cfg.numAttrs = 1;
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
+    if (e != cudaSuccess) return e;
+    max_clusters[dev][ki] = n > 0 ? n : 1;
     attr[dev][ki] = true;
   }
   const long long slots = (long long)rows.T / kBM + 2LL * rows.B;
-  const long long blocks = slots * (cache.hq / 2) * 4;   // a cluster of four CTAs per (query tile, head pair)
-  if (blocks <= 0 || blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-  kernel<<<(unsigned)blocks, kThreads, kGlobalSmemBytes, s>>>(mq, mo, ms, mr, p);
+  const long long n_units = slots * (cache.hq / 2);   // (query tile, head pair) units
+  if (n_units <= 0 || n_units > 0x3fffffffLL) return cudaErrorInvalidValue;
+  p.n_units = (int)n_units;
+  const int n_clusters = (int)(n_units < max_clusters[dev][ki] ? n_units : max_clusters[dev][ki]);
+  kernel<<<4u * (unsigned)n_clusters, kThreads, kGlobalSmemBytes, s>>>(mq, ms, mr, p);
   return cudaGetLastError();
 }
 
