@@ -416,15 +416,21 @@ def exact_decode_times(dec, flush, reps):
 
 
 def traffic_record(kernel: str):
-    """dram bytes per launch from the committed ncu summary, if it was taken on the current source."""
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current sources
+    (the hash covers every source file the kernel is built from); None otherwise."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     rec = json.load(open(p)).get(kernel)
     if not rec:
         return None
-    src = os.path.join(ROOT, "invariant_hybrid_attention_gb300", "csrc", rec["source"])
-    if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != rec["sha256_16"]:
+    h = hashlib.sha256()
+    for name in rec["sources"]:
+        src = os.path.join(ROOT, "invariant_hybrid_attention_gb300", "csrc", name)
+        if not os.path.exists(src):
+            return None
+        h.update(open(src, "rb").read())
+    if h.hexdigest()[:16] != rec["sha256_16"]:
         return None
     return rec["dram_bytes_per_launch"]
 

@@ -9,7 +9,12 @@ packing and placement).
 Each trial batch has B ~ U[1, 128] requests with prompt lengths U[1, 16384] and the target at a
 random index. Pages are scattered by a fresh random permutation, and the cache starts as NaN.
 Odd trials use a padded layout: each sequence's rows start at the next multiple of 256, and the
-gap rows are NaN. The whole batch then decodes 64 steps together.
+gap rows are NaN. The whole batch then decodes 64 steps together. The trials cycle through four
+kinds of call: plain prefills; g4attn_prefill_vision, where the other requests carry images and
+the target's rows are text; chunked prefills, where every other request continues a history
+already in the cache (ctx_start > 0); and normed calls (per-head RMS norms on q, k and v, in the
+prefill and in every decode step), whose target is compared with its own normed run alone. The
+first three must give the target the plain run's bits.
 
 A 131072-token global prefill must also give the same bits alone and inside batches; 64 of
 its rows are checked against the fp64 oracle.
@@ -65,9 +70,20 @@ def layout_rows(lens, padded):
     return starts, max(s, 1)
 
 
-def run_request_mix(kind, target, lens, at, padded, seed):
-    """Prefill the batch (target at index `at`), then decode it DECODE_STEPS times. Returns the
-    target's prefill output rows and its decode outputs (device tensors)."""
+MODES = ("plain", "vision", "chunked", "normed")
+
+
+def stress_norms(kind):
+    """Per-head norm weights (bf16, uniform in [0.5, 1.5]) on q and k, and the unit norm on v."""
+    d = GEOM[kind]["d"]
+    g = torch.Generator().manual_seed(4242)
+    w = [(torch.rand(d, generator=g) + 0.5).to(torch.bfloat16).cuda() for _ in range(2)]
+    return w, g4.make_norms(w[0], w[1], True, 1e-6)
+
+
+def run_request_mix(kind, target, lens, at, padded, seed, mode="plain"):
+    """Prefill the batch (target at index `at`) with a call of the given mode, then decode it
+    DECODE_STEPS times. Returns the target's prefill output rows and its decode outputs."""
     layer, _ = layers(kind)
     n_kv, d = GEOM[kind]["n_kv"], GEOM[kind]["d"]
     B = len(lens)
@@ -75,6 +91,11 @@ def run_request_mix(kind, target, lens, at, padded, seed):
     lens[at] = TARGET_LEN
     starts, T = layout_rows(lens, padded)
     st = starts[at]
+    keep, norms = stress_norms(kind) if mode == "normed" else (None, None)
+    # chunked: every other request continues a history of up to 2000 keys already in the cache
+    hist = [0] * B
+    if mode == "chunked":
+        hist = [0 if b == at else h for b, h in enumerate(gi.uniform_ints(B, 1, 2000, seed + 3000))]
 
     q = device_normal((T, 32, d), seed * 7 + 1)
     k = device_normal((T, n_kv, d), seed * 7 + 2)
@@ -91,12 +112,32 @@ def run_request_mix(kind, target, lens, at, padded, seed):
             if t is not None:
                 t[~covered] = float("nan")
 
-    plan = gi.make_page_plan([L + DECODE_STEPS for L in lens], seed=seed * 7 + 4, spare_pages=7)
+    plan = gi.make_page_plan([h + L + DECODE_STEPS for h, L in zip(hist, lens)], seed=seed * 7 + 4, spare_pages=7)
     cache = PagedKV(plan.num_pages, n_kv, d, shared=(kind == "global"))   # NaN-filled
     table = plan.table.cuda()
+    if mode == "chunked":   # the histories, appended first
+        hl = gi.packed_layout(hist)
+        hk = device_normal((hl.T, n_kv, d), seed * 7 + 5)
+        hv = None if kind == "global" else device_normal((hl.T, n_kv, d), seed * 7 + 6)
+        g4.g4attn_kv_append(layer, hk, hv, device_int32(hl.q_start), device_int32(hl.q_len),
+                            device_int32([0] * B), cache.desc, table)
+        del hk, hv
     out = torch.full_like(q, float("nan"))
-    g4.g4attn_prefill(layer, q, k, v, device_int32(starts), device_int32(lens), device_int32([0] * B),
-                      cache.desc, table, out)
+    rows = (device_int32(starts), device_int32(lens), device_int32(hist))
+    if mode == "vision":   # the other requests carry one image each; the target's rows are text
+        span = torch.full((T, 2), 1 << 30, dtype=torch.int32)
+        span[:, 0] = -7   # gap rows: spans that would be refused if read
+        for b, (s0, L) in enumerate(zip(starts, lens)):
+            span[s0:s0 + L] = 0
+            if b != at and L >= 4:
+                i0, i1 = L // 4, L // 4 + max(1, min(700, L // 2))
+                span[s0 + i0:s0 + i1, 0] = i0
+                span[s0 + i0:s0 + i1, 1] = i1
+        g4.g4attn_prefill_vision(layer, None, q, k, v, *rows, span.cuda(), cache.desc, table, out)
+    elif mode == "normed":
+        g4.g4attn_prefill_normed(layer, norms, q, k, v, *rows, cache.desc, table, out)
+    else:
+        g4.g4attn_prefill(layer, q, k, v, *rows, cache.desc, table, out)
     pre = out[st:st + TARGET_LEN].clone()
     del q, k, v, out
 
@@ -112,7 +153,11 @@ def run_request_mix(kind, target, lens, at, padded, seed):
         if vn is not None:
             vn[at] = target.v[TARGET_LEN + i]
         o = torch.full_like(qd, float("nan"))
-        g4.g4attn_decode(layer, qd, kn, vn, device_int32([L + i + 1 for L in lens]), cache.desc, table, o, ws)
+        sl = device_int32([h + L + i + 1 for h, L in zip(hist, lens)])
+        if mode == "normed":
+            g4.g4attn_decode_normed(layer, norms, qd, kn, vn, sl, cache.desc, table, o, ws)
+        else:
+            g4.g4attn_decode(layer, qd, kn, vn, sl, cache.desc, table, o, ws)
         dec.append(o[at].clone())
     torch.cuda.synchronize()
     st_ = g4.g4attn_status_sync()
@@ -147,11 +192,14 @@ def test_target_request_is_bit_identical_in_20_mixed_batches(kind):
                                  None if v_h is None else v_h[:L])
         assert_close(f64(ref_dec[i]), want, f"{kind} target decode step {i}")
 
-    for seed in TRIAL_SEEDS:
+    ref_n = run_request_mix(kind, target, [TARGET_LEN], 0, False, seed=2, mode="normed")   # the normed target alone
+    for i, seed in enumerate(TRIAL_SEEDS):
         lens, at, padded = trial_shape(seed)
-        pre, dec = run_request_mix(kind, target, lens, at, padded, seed)
-        assert torch.equal(pre, ref_pre), (kind, seed, len(lens), at, padded, "prefill")
-        assert torch.equal(dec, ref_dec), (kind, seed, len(lens), at, padded, "decode")
+        mode = MODES[i % len(MODES)]
+        pre, dec = run_request_mix(kind, target, lens, at, padded, seed, mode)
+        want_pre, want_dec = ref_n if mode == "normed" else (ref_pre, ref_dec)
+        assert torch.equal(pre, want_pre), (kind, seed, mode, len(lens), at, padded, "prefill")
+        assert torch.equal(dec, want_dec), (kind, seed, mode, len(lens), at, padded, "decode")
         del pre, dec
         torch.cuda.empty_cache()
 
