@@ -613,7 +613,7 @@ __global__ void __launch_bounds__(256) append_kv_groups_kernel(const __nv_bfloat
   if (pos < cs0 || pos >= cs0 + L) return;   // outside the call's rows (the group's ragged ends)
   const int j = pos & 15;
   const size_t row = (size_t)(qs + (pos - cs0));
-#pragma unroll 1
+#pragma unroll 2   // two iterations' loads in flight at once
   for (int i = 0; i < 4; ++i) {
     const int d0 = 8 * (p + 4 * i);
     float2 cs[8];
@@ -689,6 +689,66 @@ __global__ void __launch_bounds__(256) norm_queries_kernel(const __nv_bfloat16* 
                     (SHARED && nm.wk != nullptr) ? wk : nullptr, R);
 }
 
+// The global layer's S and k_rot append by key groups (plain calls): one warp per (group of 8
+// positions aligned to 8, KV head). Lane (key kk = lane & 7, piece p = lane >> 3) copies dims
+// 8(p + 4i) .. +7 of its key's S, i = 0..15, so one warp store writes four whole core matrices of the
+// page-head block; the rotated pairs (t, t + 256), t < 64, are those of i = 0, 1 with i + 8, whose
+// p-RoPE goes to the k_rot side page with the per-row append's angles (rope_cs), rotation
+// (rope_pair) and cast, so the cache bits are the same.
+template <int D, int R>
+__global__ void __launch_bounds__(256) append_s_groups_kernel(const __nv_bfloat16* __restrict__ k, SeqRows rows,
+                                                             PagedCache c, RopeTables tb, uint32_t* err) {
+  static_assert(D == 512 && R == 64, "the group path serves the global geometry");
+  const int lane = threadIdx.x & 31;
+  const int HKV = c.hkv;
+  const int unit = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int gi = unit / HKV, g = unit % HKV;
+  int b, grp;
+  find_group(rows, gi, b, grp, err);
+  if (b < 0) return;
+  const int cs0 = rows.ctx_start[b], L = rows.q_len[b], qs = rows.q_start[b];
+  const int key0 = 8 * grp;
+  if (key0 >= kMaxPos || (key0 >> 4) >= c.max_pages) {
+    if (lane == 0) set_error(err, kErrPos);
+    return;
+  }
+  const int phys = c.page_table[(size_t)b * c.max_pages + (key0 >> 4)];
+  if (phys < 0 || phys >= c.num_pages) {
+    if (lane == 0) set_error(err, kErrPage);
+    return;
+  }
+  const int kk = lane & 7, p = lane >> 3;
+  const int pos = key0 + kk;
+  if (pos < cs0 || pos >= cs0 + L) return;   // outside the call's rows (the group's ragged ends)
+  const int j = pos & 15;
+  const __nv_bfloat16* src = k + ((size_t)(qs + (pos - cs0)) * HKV + g) * D;
+  uint4 s[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) s[i] = *reinterpret_cast<const uint4*>(src + 8 * (p + 4 * i));
+  __nv_bfloat16* sd = (__nv_bfloat16*)c.k + ((size_t)phys * HKV + g) * kPage * D;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) *reinterpret_cast<uint4*>(sd + tiled_offset(j, 8 * (p + 4 * i), D)) = s[i];
+  __nv_bfloat16* rd = (__nv_bfloat16*)c.krot + ((size_t)phys * HKV + g) * kRotPageElems;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {   // pairs t = 8 (p + 4i) + e with t + 256
+    const int t0 = 8 * (p + 4 * i);
+    uint4 lo = s[i], hi = s[i + 8];
+    uint32_t* lw = reinterpret_cast<uint32_t*>(&lo);
+    uint32_t* hw = reinterpret_cast<uint32_t*>(&hi);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      float a0 = bf16_lo(lw[w]), a1 = bf16_hi(lw[w]);
+      float b0 = bf16_lo(hw[w]), b1 = bf16_hi(hw[w]);
+      rope_pair(a0, b0, rope_cs(tb, t0 + 2 * w, pos));
+      rope_pair(a1, b1, rope_cs(tb, t0 + 2 * w + 1, pos));
+      lw[w] = pack_bf16(a0, a1);
+      hw[w] = pack_bf16(b0, b1);
+    }
+    *reinterpret_cast<uint4*>(rd + rot_offset(j, t0)) = lo;
+    *reinterpret_cast<uint4*>(rd + rot_offset(j, D / 2 + t0)) = hi;
+  }
+}
+
 cudaError_t launch_append_prefill(bool global, const void* k, const void* v, const SeqRows& rows,
                                   const PagedCache& cache, const DeviceState& st, cudaStream_t s, const void* q,
                                   void* q_out, const NormArgs& nm) {
@@ -697,12 +757,20 @@ cudaError_t launch_append_prefill(bool global, const void* k, const void* v, con
   const __nv_bfloat16 *kb = (const __nv_bfloat16*)k, *vb = (const __nv_bfloat16*)v, *qb = (const __nv_bfloat16*)q;
   __nv_bfloat16* qo = (__nv_bfloat16*)q_out;
   if (global) {
-    if (nm.any())
+    if (nm.any()) {
       append_prefill_kernel<kGlobalD, kGlobalR, true, true>
           <<<blocks, 256, 0, s>>>(kb, nullptr, qb, qo, rows, cache, st.global, st.err, nm, true);
-    else
-      append_prefill_kernel<kGlobalD, kGlobalR, true, false>
-          <<<blocks, 256, 0, s>>>(kb, nullptr, qb, qo, rows, cache, st.global, st.err, nm, true);
+    } else {
+      // S and k_rot by key groups (whole-sector writes), the staged queries (if any) by rows.
+      const long long groups = (long long)rows.T / 8 + 2LL * rows.B;   // a sequence adds at most two partial groups
+      const long long units = groups * cache.hkv;
+      if (units > 0x3fffffffLL) return cudaErrorInvalidValue;
+      append_s_groups_kernel<kGlobalD, kGlobalR>
+          <<<(unsigned)((units + 7) / 8), 256, 0, s>>>(kb, rows, cache, st.global, st.err);
+      if (qo != nullptr)
+        append_prefill_kernel<kGlobalD, kGlobalR, true, false>
+            <<<blocks, 256, 0, s>>>(kb, nullptr, qb, qo, rows, cache, st.global, st.err, nm, false);
+    }
   } else if (nm.any()) {
     append_prefill_kernel<kSlidingD, kSlidingR, false, true>
         <<<blocks, 256, 0, s>>>(kb, vb, qb, qo, rows, cache, st.sliding, st.err, nm, true);
