@@ -254,7 +254,8 @@ g4_status g4attn_decode_exact(const g4attn_layer* layer, const g4attn_norms* nor
                               const g4attn_cache* cache, const int32_t* page_table, int32_t max_pages,
                               void* out, void* workspace, size_t workspace_bytes, void* stream);
 /* Bytes of workspace g4attn_decode_exact needs for B requests (RFC section 5,
- * hybrid_kv_cache_contract: the rows of the B one-row chunks, int32 [3][B]); 0 when B <= 0. */
+ * hybrid_kv_cache_contract: the rows of the B one-row chunks and their page-table rows,
+ * int32 [4][B]); 0 when B <= 0. */
 size_t g4attn_decode_exact_workspace_bytes(int32_t B);
 
 /* Writes the K'/V (sliding) or S (global) rows of a prefill batch into the paged cache

@@ -186,10 +186,13 @@ g4_status g4attn_kv_append(const g4attn_layer* layer, const void* k, const void*
                                  stream);
 }
 
+// pt_row: optional page-table row of each sequence (the exact decode's chunks, listed from the
+// longest context down).
 static g4_status prefill_stage(const g4attn_layer* layer, const g4attn_norms* norms, const void* q, const void* k,
                                const void* v, int32_t T, const int32_t* q_start, const int32_t* q_len,
                                const int32_t* ctx_start, int32_t B, const g4attn_cache* cache,
-                               const int32_t* page_table, int32_t max_pages, void* out, void* stream) {
+                               const int32_t* page_table, int32_t max_pages, void* out, void* stream,
+                               const int32_t* pt_row = nullptr) {
   bool global = false;
   g4_status s = check_layer(layer, &global);
   if (s != G4_OK) return s;
@@ -204,7 +207,7 @@ static g4_status prefill_stage(const g4attn_layer* layer, const g4attn_norms* no
   if (device_state(&st) != cudaSuccess) return G4_ERR_CUDA;
   // Cache append, and the roped queries staged in `out`: each sequence row of `out` holds its
   // roped query until g4attn_prefill_attend overwrites it with the attention output.
-  const SeqRows rows{q_start, q_len, ctx_start, B, T};
+  const SeqRows rows{q_start, q_len, ctx_start, B, T, nullptr, pt_row, pt_row != nullptr};
   return from_cuda(launch_append_prefill(global, k, v, rows, paged(layer, cache, page_table, max_pages), st,
                                          (cudaStream_t)stream, q, out, nm));
 }
@@ -222,7 +225,7 @@ g4_status g4attn_prefill_stage(const g4attn_layer* layer, const void* q, const v
 static g4_status prefill_attend(const g4attn_layer* layer, const void* q, int32_t T, const int32_t* q_start,
                                 const int32_t* q_len, const int32_t* ctx_start, int32_t B, const int32_t* span,
                                 const g4attn_cache* cache, const int32_t* page_table, int32_t max_pages, void* out,
-                                void* stream) {
+                                void* stream, const int32_t* pt_row = nullptr) {
   bool global = false;
   g4_status s = check_layer(layer, &global);
   if (s != G4_OK) return s;
@@ -233,7 +236,7 @@ static g4_status prefill_attend(const g4attn_layer* layer, const void* q, int32_
   if (T == 0) return G4_OK;
   DeviceState st;
   if (device_state(&st) != cudaSuccess) return G4_ERR_CUDA;
-  const SeqRows rows{q_start, q_len, ctx_start, B, T, span};
+  const SeqRows rows{q_start, q_len, ctx_start, B, T, span, pt_row, pt_row != nullptr};
   return from_cuda(launch_prefill(global, rows, global ? 0 : layer->window, scale_log2(layer),
                                   paged(layer, cache, page_table, max_pages), out, st, (cudaStream_t)stream, q));
 }
@@ -384,7 +387,7 @@ g4_status g4attn_decode(const g4attn_layer* layer, const void* q, const void* k_
 }
 
 size_t g4attn_decode_exact_workspace_bytes(int32_t B) {
-  return B <= 0 ? 0 : ((size_t)B * 3 * sizeof(int32_t) + 15) / 16 * 16;
+  return B <= 0 ? 0 : ((size_t)B * 4 * sizeof(int32_t) + 15) / 16 * 16;
 }
 
 g4_status g4attn_decode_exact(const g4attn_layer* layer, const g4attn_norms* norms, const void* q, const void* k_new,
@@ -407,10 +410,10 @@ g4_status g4attn_decode_exact(const g4attn_layer* layer, const g4attn_norms* nor
   int32_t* rows = static_cast<int32_t*>(workspace);
   if (launch_decode_rows(seq_len, B, rows, st, (cudaStream_t)stream) != cudaSuccess) return G4_ERR_CUDA;
   if ((s = prefill_stage(layer, norms, q, k_new, v_new, B, rows, rows + B, rows + 2 * B, B, cache, page_table,
-                         max_pages, out, stream)) != G4_OK)
+                         max_pages, out, stream, rows + 3 * B)) != G4_OK)
     return s;
   return prefill_attend(layer, nullptr, B, rows, rows + B, rows + 2 * B, B, nullptr, cache, page_table, max_pages, out,
-                        stream);
+                        stream, rows + 3 * B);
 }
 
 g4_status g4attn_decode_static(const g4attn_layer* layer, const void* q, const void* k_new, const void* v_new,

@@ -650,20 +650,34 @@ size_t decode_workspace_bytes(bool global, int B, int max_pages, int window, int
 }
 
 // A decode step laid out as B one-row prefill chunks: request b's query is row b, at position
-// seq_len[b] - 1. A request with seq_len < 1 gets no row (and sets kErrPos).
+// seq_len[b] - 1, and it reads page-table row b. The chunks are listed from the longest context
+// down (ties by request index), so that the prefill kernels' fixed round-robin schedule gives
+// every cluster a similar share of key tiles; a chunk's arithmetic does not depend on its place in
+// the list. Steps of up to kSortedRows requests are sorted (each rank is a count over all of them);
+// larger ones keep request order. A request with seq_len < 1 gets no row (and sets kErrPos).
+constexpr int kSortedRows = 8192;
 __global__ void decode_rows_kernel(const int32_t* seq_len, int B, int32_t* q_start, int32_t* q_len,
-                                   int32_t* ctx_start, uint32_t* err) {
+                                   int32_t* ctx_start, int32_t* pt_row, uint32_t* err) {
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= B) return;
   const int n = seq_len[b];
-  q_start[b] = b;
-  q_len[b] = n >= 1 ? 1 : 0;
-  ctx_start[b] = n >= 1 ? n - 1 : 0;
+  int rank = b;
+  if (B <= kSortedRows) {
+    rank = 0;
+    for (int i = 0; i < B; ++i) {
+      const int m = __ldg(seq_len + i);
+      rank += (m > n || (m == n && i < b)) ? 1 : 0;
+    }
+  }
+  q_start[rank] = b;
+  q_len[rank] = n >= 1 ? 1 : 0;
+  ctx_start[rank] = n >= 1 ? n - 1 : 0;
+  pt_row[rank] = b;
   if (n < 1) set_error(err, kErrPos);
 }
 
 cudaError_t launch_decode_rows(const int32_t* seq_len, int B, int32_t* rows, const DeviceState& st, cudaStream_t s) {
-  decode_rows_kernel<<<(B + 127) / 128, 128, 0, s>>>(seq_len, B, rows, rows + B, rows + 2 * B, st.err);
+  decode_rows_kernel<<<(B + 127) / 128, 128, 0, s>>>(seq_len, B, rows, rows + B, rows + 2 * B, rows + 3 * B, st.err);
   return cudaGetLastError();
 }
 

@@ -35,6 +35,13 @@ struct SeqRows {
   // Optional int32 [T][2]: the image span [s0, s1) of absolute positions of each query row
   // (memory row index, like q); s1 <= s0 marks a text row. NULL: every row is text.
   const int32_t* span = nullptr;
+  // Optional int32 [B]: the page-table row of each sequence (NULL: sequence b reads row b). The
+  // exact decode lists its one-row chunks from the longest context down, for the schedule, and
+  // keeps each request's own page-table row.
+  const int32_t* pt_row = nullptr;
+  // The sequences are listed from the most expensive down: a persistent schedule then walks its
+  // rounds of units in a snake, which evens the clusters' shares.
+  bool by_cost = false;
 };
 
 // A layer's paged cache and the head counts of the call: hkv KV heads in the cache (its page-head

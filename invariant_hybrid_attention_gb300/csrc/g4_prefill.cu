@@ -143,7 +143,7 @@ __device__ __noinline__ bool sliding_unit(const PrefillParams& p, int u, uint32_
   }
   o.kt0 = o.k_lo / kSN;
   o.n_tiles = o.k_hi / kSN - o.kt0 + 1;
-  o.pt = p.page_table + (size_t)b * p.max_pages;
+  o.pt = p.page_table + (size_t)(p.rows.pt_row ? __ldg(p.rows.pt_row + b) : b) * p.max_pages;
   o.qpos = min(kQAfter, o.n_tiles);
   return true;
 }

@@ -179,8 +179,18 @@ __device__ __noinline__ bool global_unit(const PrefillParams& p, int u, uint32_t
   }
   o.kt0 = o.k_lo / kTN;
   o.n_tiles = o.k_hi >= o.k_lo ? o.k_hi / kTN - o.kt0 + 1 : 0;
-  o.pt = p.page_table + (size_t)b * p.max_pages;
+  o.pt = p.page_table + (size_t)(p.rows.pt_row ? __ldg(p.rows.pt_row + b) : b) * p.max_pages;
   return true;
+}
+
+// The k-th unit of cluster c of C: rounds of C units. When the units are listed from the most
+// expensive down (the exact decode's chunks), odd rounds are walked backwards (a snake), so that
+// the clusters' shares even out; otherwise every round is walked forwards, which keeps the clusters
+// of one KV head on neighbouring units, reading the same key tiles from L2 at about the same time
+// (the snake measured 2% slower on a causal prefill). A fixed assignment either way: which cluster
+// computes a unit changes none of its bits.
+__device__ __forceinline__ int unit_at(int k, int c, int C, bool snake) {
+  return k * C + ((snake && (k & 1)) ? C - 1 - c : c);
 }
 
 template <bool kRope, bool kPart>
@@ -205,7 +215,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
   // cluster barrier: it posts the bytes of the first two tiles' P before any copy can arrive.
   int total_tiles = 0;
   if (is_out && warp == 6) {
-    for (int u = cluster; u < p.n_units; u += n_clusters) {
+    for (int k = 0, u = unit_at(0, cluster, n_clusters, p.rows.by_cost); u < p.n_units; u = unit_at(++k, cluster, n_clusters, p.rows.by_cost)) {
       GUnit o;
       if (global_unit<kPart>(p, u, pr, o)) total_tiles += o.n_tiles;
     }
@@ -274,7 +284,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
       }
       const int pl = lane & 3;
       bool ok = true;
-      for (int u = cluster, ui = 0; ok && u < p.n_units; u += n_clusters) {
+      for (int k = 0, ui = 0, u = unit_at(0, cluster, n_clusters, p.rows.by_cost); ok && u < p.n_units; u = unit_at(++k, cluster, n_clusters, p.rows.by_cost)) {
         GUnit un;
         if (!global_unit<kPart>(p, u, pr, un) || un.n_tiles == 0) continue;
         // Lanes 0-3 copy the un-rotated dims of page `lane` of this CTA's 64 keys, lanes 4-7 its
@@ -330,7 +340,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
     } else if (warp == 1 && !leader) {
       // ------------------------------------------------------------ K relay (rank 1)
       bool ok = true;
-      for (int u = cluster; ok && u < p.n_units; u += n_clusters) {
+      for (int k = 0, u = unit_at(0, cluster, n_clusters, p.rows.by_cost); ok && u < p.n_units; u = unit_at(++k, cluster, n_clusters, p.rows.by_cost)) {
         GUnit un;
         if (!global_unit<kPart>(p, u, pr, un) || un.n_tiles == 0) continue;
         for (int j = 0; j < un.n_tiles; ++j) {
@@ -348,7 +358,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
       // ------------------------------------------------------------ QK^T issuer (rank 0)
       bool ok = true;
       int tc = 0;
-      for (int u = cluster, ui = 0; ok && u < p.n_units; u += n_clusters) {
+      for (int k = 0, ui = 0, u = unit_at(0, cluster, n_clusters, p.rows.by_cost); ok && u < p.n_units; u = unit_at(++k, cluster, n_clusters, p.rows.by_cost)) {
         GUnit un;
         if (!global_unit<kPart>(p, u, pr, un) || un.n_tiles == 0) continue;
         ok = __all_sync(0xffffffffu, mbar_wait_cl(&bar.q_pair, ui & 1, abort_flag, p.err, p.wait_ns));
@@ -394,7 +404,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
       int tc = 0;
       uint32_t kq[kNK] = {0u, 0u, 0u};   // uses of each K stage by the earlier units (thread 64)
       if (threadIdx.x == 64) prefetch_tmap(&tmap_q);
-      for (int u = cluster, ui = 0; ok && u < p.n_units; u += n_clusters) {
+      for (int k = 0, ui = 0, u = unit_at(0, cluster, n_clusters, p.rows.by_cost); ok && u < p.n_units; u = unit_at(++k, cluster, n_clusters, p.rows.by_cost)) {
         GUnit un;
         if (!global_unit<kPart>(p, u, pr, un)) continue;
         const int pos = kBM * un.t + r;
@@ -567,7 +577,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
       // ------------------------------------------------------------ V copies
       const __nv_bfloat16* sc = (const __nv_bfloat16*)p.k_cache;
       bool ok = true;
-      for (int u = cluster; ok && u < p.n_units; u += n_clusters) {
+      for (int k = 0, u = unit_at(0, cluster, n_clusters, p.rows.by_cost); ok && u < p.n_units; u = unit_at(++k, cluster, n_clusters, p.rows.by_cost)) {
         GUnit un;
         if (!global_unit<kPart>(p, u, pr, un) || un.n_tiles == 0) continue;
         // Block indices ahead of use: lane l holds page (l & 3) of stage (l >> 2) of the current
@@ -614,7 +624,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
       bool ok = true;
       uint32_t vc = 0;
       int tc = 0;
-      for (int u = cluster, ui = 0; ok && u < p.n_units; u += n_clusters) {
+      for (int k = 0, ui = 0, u = unit_at(0, cluster, n_clusters, p.rows.by_cost); ok && u < p.n_units; u = unit_at(++k, cluster, n_clusters, p.rows.by_cost)) {
         GUnit un;
         if (!global_unit<kPart>(p, u, pr, un) || un.n_tiles == 0) continue;
         const int n_st = 2 * un.n_tiles;
@@ -676,7 +686,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t stg_free_dst = map_peer(smem_u32(&bar.stg_free), partner);
       bool ok = true;
       int tc = 0;
-      for (int u = cluster; ok && u < p.n_units; u += n_clusters) {
+      for (int k = 0, u = unit_at(0, cluster, n_clusters, p.rows.by_cost); ok && u < p.n_units; u = unit_at(++k, cluster, n_clusters, p.rows.by_cost)) {
         GUnit un;
         if (!global_unit<kPart>(p, u, pr, un)) continue;
         const int pos = kBM * un.t + r;

@@ -531,7 +531,8 @@ __global__ void __launch_bounds__(256) append_prefill_kernel(const __nv_bfloat16
   }
   if (rows_kv)
     append_token_cs<D, R, SHARED, NORM>(k + (size_t)r * HKV * D, SHARED ? nullptr : v + (size_t)r * HKV * D,
-                                        owner, pos, cache, cs, err, nm, wk, 0, HKV);
+                                        rows.pt_row ? rows.pt_row[owner] : owner, pos, cache, cs, err, nm, wk, 0,
+                                        HKV);
 }
 
 // ---- the sliding K'/V append by key groups ---------------------------------------------------------
@@ -603,7 +604,7 @@ __global__ void __launch_bounds__(256) append_kv_groups_kernel(const __nv_bfloat
     if (lane == 0) set_error(err, kErrPos);
     return;
   }
-  const int phys = c.page_table[(size_t)b * c.max_pages + (key0 >> 4)];
+  const int phys = c.page_table[(size_t)(rows.pt_row ? rows.pt_row[b] : b) * c.max_pages + (key0 >> 4)];
   if (phys < 0 || phys >= c.num_pages) {
     if (lane == 0) set_error(err, kErrPage);
     return;
@@ -712,7 +713,7 @@ __global__ void __launch_bounds__(256) append_s_groups_kernel(const __nv_bfloat1
     if (lane == 0) set_error(err, kErrPos);
     return;
   }
-  const int phys = c.page_table[(size_t)b * c.max_pages + (key0 >> 4)];
+  const int phys = c.page_table[(size_t)(rows.pt_row ? rows.pt_row[b] : b) * c.max_pages + (key0 >> 4)];
   if (phys < 0 || phys >= c.num_pages) {
     if (lane == 0) set_error(err, kErrPage);
     return;
