@@ -22,13 +22,19 @@
 // tiles to absolute position; every row's arithmetic depends only on its own position and its
 // sequence's keys (section 4 rules 2, 3 and 6).
 //
-// Score CTA warps: 0 copies the Q tile (TMA) and this CTA's K half of each key tile into a
-// 3-stage ring; 1 issues QK^T (rank 0) or tells rank 0 that its ring slot has landed (rank 1);
-// 2-5 move Q into tensor memory, then run mask, online softmax and P (one thread per row).
-// Output CTA warps: 0 copies this CTA's V half of each 64-key half tile into a 4-stage ring;
-// 1 zeroes value rows that hold no key of the sequence, then issues P.V (rank 2) or tells rank
-// 2 that its half is ready (rank 3); 2-5 check alpha, rescale O when asked, and write the
-// output; 6 hands P slots back to the score CTA once P.V has read them.
+// Score CTA warps: 0 copies this CTA's K half of each key tile into a 3-stage ring; 7 copies each
+// unit's Q tile (TMA) into K stages 1-2 as soon as every QK^T of the earlier unit is done; 6 (rank 0)
+// waits for each tile's operands (the unit's Q in place, both CTAs' K halves, the S buffer read)
+// and hands the tile to the issuer; 1 issues QK^T (rank 0) or tells rank 0 that its ring slot has
+// landed (rank 1); 2-5 move Q into tensor memory, then run mask, online softmax and P (one thread
+// per row). Output CTA warps: 0 copies this CTA's V half of each 64-key half tile into a 4-stage
+// ring; 7 (rank 2) or 1 (rank 3) zeroes value rows that hold no key of the sequence, then hands the
+// step to the P.V issuer once the rest of its operands are ready (rank 2) or tells rank 2 that its
+// half is ready (rank 3); 1 (rank 2) issues P.V; 2-5 check alpha, rescale O when asked, and write
+// the output; 6 hands P slots back to the score CTA once P.V has read them. Issuing a group of MMAs
+// blocks the issuing thread for about as long as they run, so the issuers wait on one barrier each
+// (their helpers wait on the rest, three of them at cluster scope), and the next tile's MMAs follow
+// the last ones closely.
 // Queries (kRope): the Q tile is copied from the raw query rows and its 64 turning pairs (dims 0-63
 // with 256-319) are rotated in place in shared memory before the move into tensor memory: softmax
 // thread i rotates pair i % 64 of rows 64 (i / 64) .. +63 (rotate_q_pair; rows outside the sequence
@@ -56,7 +62,7 @@ constexpr int kVN = 64;             // keys per V stage
 constexpr int kNK = 3;              // K ring stages (score CTAs)
 constexpr int kNV = 4;              // V ring stages (output CTAs)
 constexpr int kNP = 2;              // S buffers (score CTAs) and P slots (output CTAs)
-constexpr int kThreads = 224;
+constexpr int kThreads = 256;
 constexpr uint16_t kScorePair = 0x3, kOutPair = 0xC;
 
 // Score-CTA K stage: this CTA's 64 keys of a tile (4 pages), all 512 dims. Each page arrives as
@@ -106,11 +112,13 @@ struct Bars {
   // score CTAs
   uint64_t k_full[kNK], k_empty[kNK], k_peer[kNK];
   uint64_t s_full[kNP], s_free[kNP], p_free[kNP];
-  uint64_t q_full, q_moved, q_pair, stg_free, q_rot;
+  uint64_t q_full, q_moved, q_pair, stg_free, q_rot, go[2];
+  uint64_t q_free;           // score CTAs: every QK^T of the unit is done (the issuer's commit, both CTAs)
   // output CTAs
   uint64_t v_full[kNV], v_empty[kNV], v_ready[kNV];
   uint64_t p_full[kNP], o_ready[kNP], pv_done[kNP];
   uint64_t o_free;           // output CTAs (rank 2): both CTAs' epilogue warps have read O out
+  uint64_t go_pv[kNV];       // output CTAs (rank 2): the helper has seen V stage s's P.V ready
   uint64_t teardown;
   uint32_t tmem_base;
   int abort_flag;
@@ -201,6 +209,11 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
   GlobalSmem& sm = *reinterpret_cast<GlobalSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   uint8_t* const base = sm.data;
   uint8_t* const q_stage = base + kKStage + ((1024u - (smem_u32(base + kKStage) & 1023u)) & 1023u);
+  // When the Q staging is clear of the P staging (the data area is 1024-byte aligned, as it is in
+  // practice), warp 7 copies each unit's Q as soon as every QK^T of the earlier unit is done;
+  // otherwise softmax thread 64 does, once the last P copy has also left the staging. The same for
+  // every CTA of the grid.
+  const bool q_sep = q_stage + 8 * kQChunk <= base + kSOffStage;
   Bars& bar = sm.bar;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
@@ -240,6 +253,10 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(&bar.q_moved, kSoftmaxThreads / 32);
     mbar_init(&bar.q_pair, 8);
     mbar_init(&bar.stg_free, 1);
+    mbar_init(&bar.q_free, 1);
+    mbar_init(&bar.go[0], 1);
+    for (int s = 0; s < kNV; ++s) mbar_init(&bar.go_pv[s], 1);
+    mbar_init(&bar.go[1], 1);
     mbar_init(&bar.q_rot, kSoftmaxThreads / 32);   // kRope: the softmax warps have rotated Q
     for (int s = 0; s < kNV; ++s) {
       mbar_init(&bar.v_full[s], 1);
@@ -361,15 +378,10 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
       for (int k = 0, ui = 0, u = unit_at(0, cluster, n_clusters, p.rows.by_cost); ok && u < p.n_units; u = unit_at(++k, cluster, n_clusters, p.rows.by_cost)) {
         GUnit un;
         if (!global_unit<kPart>(p, u, pr, un) || un.n_tiles == 0) continue;
-        ok = __all_sync(0xffffffffu, mbar_wait_cl(&bar.q_pair, ui & 1, abort_flag, p.err, p.wait_ns));
         for (int j = 0; ok && j < un.n_tiles; ++j) {
           const int s = j % kNK, gt = tc + j, sb = gt % kNP;
-          // both CTAs' halves of the tile have landed; S buffer sb was read by tile gt-2's softmax
-          ok = __all_sync(0xffffffffu,
-                          mbar_wait(&bar.k_full[s], kuse[s] & 1, abort_flag, p.err, p.wait_ns) &&
-                              mbar_wait_cl(&bar.k_peer[s], kuse[s] & 1, abort_flag, p.err, p.wait_ns) &&
-                              (gt < kNP ||
-                               mbar_wait_cl(&bar.s_free[sb], ((gt - kNP) / kNP) & 1, abort_flag, p.err, p.wait_ns)));
+          // the helper warp has seen this tile's operands ready
+          ok = __all_sync(0xffffffffu, mbar_wait(&bar.go[gt & 1], (gt >> 1) & 1, abort_flag, p.err, p.wait_ns));
           if (!ok) break;
           tc_fence_after();
           if (lane == 0) {
@@ -385,6 +397,54 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
             mma2_commit_mc(&bar.s_full[sb], kScorePair);
             mma2_commit_mc(&bar.k_empty[s], kScorePair);
           }
+          __syncwarp();
+          ++kuse[s];
+        }
+        if (!ok) break;
+        if (q_sep && lane == 0) mma2_commit_mc(&bar.q_free, kScorePair);   // the unit's QK^T are all done
+        __syncwarp();
+        tc += un.n_tiles;
+        ++ui;
+      }
+    } else if (warp == 7 && q_sep) {
+      // ------------------------------------------------------------ Q copies (each score CTA)
+      // The unit's Q goes into K stages 1-2 as soon as every QK^T of the earlier unit is done.
+      bool ok = true;
+      int ui = 0;
+      for (int k = 0, u = unit_at(0, cluster, n_clusters, p.rows.by_cost); ok && u < p.n_units; u = unit_at(++k, cluster, n_clusters, p.rows.by_cost)) {
+        GUnit un;
+        if (!global_unit<kPart>(p, u, pr, un) || un.n_tiles == 0) continue;
+        if (ui > 0) ok = __all_sync(0xffffffffu, mbar_wait(&bar.q_free, (ui - 1) & 1, abort_flag, p.err, p.wait_ns));
+        if (!ok) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bar.q_full, 8 * kQChunk);
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            tma_load_3d(q_stage + c * kQChunk, &tmap_q, 64 * c, un.h, un.q_row0, &bar.q_full);
+          bar.q_issued = ui + 1;
+        }
+        __syncwarp();
+        ++ui;
+      }
+      // the last unit's commit lands before the CTA may leave
+      if (ok && ui > 0) ok = __all_sync(0xffffffffu, mbar_wait(&bar.q_free, (ui - 1) & 1, abort_flag, p.err, p.wait_ns));
+    } else if (warp == 6 && leader) {
+      // ------------------------------------------------------------ QK^T helper (rank 0)
+      bool ok = true;
+      int tc = 0;
+      for (int k = 0, ui = 0, u = unit_at(0, cluster, n_clusters, p.rows.by_cost); ok && u < p.n_units; u = unit_at(++k, cluster, n_clusters, p.rows.by_cost)) {
+        GUnit un;
+        if (!global_unit<kPart>(p, u, pr, un) || un.n_tiles == 0) continue;
+        ok = __all_sync(0xffffffffu, mbar_wait_cl(&bar.q_pair, ui & 1, abort_flag, p.err, p.wait_ns));
+        for (int j = 0; ok && j < un.n_tiles; ++j) {
+          const int s = j % kNK, gt = tc + j, sb = gt % kNP;
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait(&bar.k_full[s], kuse[s] & 1, abort_flag, p.err, p.wait_ns) &&
+                              mbar_wait_cl(&bar.k_peer[s], kuse[s] & 1, abort_flag, p.err, p.wait_ns) &&
+                              (gt < kNP ||
+                               mbar_wait_cl(&bar.s_free[sb], ((gt - kNP) / kNP) & 1, abort_flag, p.err, p.wait_ns)));
+          if (!ok) break;
+          if (lane == 0) mbar_arrive(&bar.go[gt & 1]);
           __syncwarp();
           ++kuse[s];
         }
@@ -414,12 +474,12 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
             reinterpret_cast<float2*>(p.ml_part)[(size_t)(un.q_row0 + r) * p.hq + un.h] = make_float2(-INFINITY, 0.f);
           continue;
         }
-        // The unit's Q (8 boxes of 64 dims x 128 rows, rows outside T read as 0) goes into K stages
-        // 1-2 and the first bytes of the P staging, once the earlier units' key tiles there have
-        // been read by QK^T and the last P copy has left the staging. Thread 64 issues it: the
-        // softmax warps wait every phase of the staging barrier in order, so this wait is one
-        // phase ahead at most.
-        if (threadIdx.x == 64) {
+        // Without q_sep, the unit's Q (8 boxes of 64 dims x 128 rows, rows outside T read as 0) reaches
+        // into the first bytes of the P staging: it goes into K stages 1-2 once the earlier units' key
+        // tiles there have been read by QK^T and the last P copy has left the staging. Thread 64
+        // issues it then: the softmax warps wait every phase of the staging barrier in order, so
+        // this wait is one phase ahead at most.
+        if (threadIdx.x == 64 && !q_sep) {
           bool okq = true;
           for (int s = 1; okq && s <= 2; ++s)
             if (kq[s] > 0) okq = mbar_wait(&bar.k_empty[s], (kq[s] - 1) & 1, abort_flag, p.err, p.wait_ns);
@@ -616,8 +676,8 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
           ++vc_total;
         }
       }
-    } else if (warp == 1) {
-      // ------------------------------------------------------------ V check; P.V issuer (rank 2) or relay (rank 3)
+    } else if ((warp == 1 && !leader) || (warp == 7 && leader)) {
+      // ------------------------------------------------------------ V check; P.V helper (rank 2) or relay (rank 3)
       // Value rows of keys that hold no data of this sequence are zeroed before P.V: pages past
       // the last needed one were not copied and keep an older tile, and slots past the
       // sequence's last key may hold anything (NaN); P = 0 there does not cancel NaN.
@@ -660,6 +720,25 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                                mbar_wait_cl(&bar.o_ready[gt % kNP], (gt / kNP) & 1, abort_flag, p.err, p.wait_ns)) &&
                               (c > 0 || ui == 0 || mbar_wait_cl(&bar.o_free, (ui - 1) & 1, abort_flag, p.err, p.wait_ns)));
           if (!ok) break;
+          if (lane == 0) mbar_arrive(&bar.go_pv[s]);
+          __syncwarp();
+        }
+        tc += un.n_tiles;
+        ++ui;
+      }
+    } else if (warp == 1) {
+      // ------------------------------------------------------------ P.V issuer (rank 2)
+      bool ok = true;
+      uint32_t vc = 0;
+      int tc = 0;
+      for (int k = 0, u = unit_at(0, cluster, n_clusters, p.rows.by_cost); ok && u < p.n_units; u = unit_at(++k, cluster, n_clusters, p.rows.by_cost)) {
+        GUnit un;
+        if (!global_unit<kPart>(p, u, pr, un) || un.n_tiles == 0) continue;
+        const int n_st = 2 * un.n_tiles;
+        for (int c = 0; ok && c < n_st; ++c, ++vc) {
+          const int s = vc % kNV, j = c >> 1, e = c & 1, gt = tc + j;
+          ok = __all_sync(0xffffffffu, mbar_wait(&bar.go_pv[s], (vc / kNV) & 1, abort_flag, p.err, p.wait_ns));
+          if (!ok) break;
           tc_fence_after();
           if (lane == 0) {
             const uint32_t va = smem_u32(base + s * kVStage);
@@ -677,7 +756,6 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
           __syncwarp();
         }
         tc += un.n_tiles;
-        ++ui;
       }
     } else if (warp >= 2 && warp <= 5) {
       // ------------------------------------------------------------ alpha, O rescale, epilogue

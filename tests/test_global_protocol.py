@@ -5,15 +5,19 @@ A 4-CTA cluster computes a sequence of units (query tile, head pair), each of so
 tiles; every barrier phase continues across units. Score CTAs 0-1: warp 0 copies K tiles into 3
 stages (each unit starts at stage 0; its tile 1, and so tile 2, waits until the unit's Q, staged in
 stages 1-2, has moved into tensor memory; a unit of one tile waits for nothing of the kind, yet the
-warp never runs two phases of that barrier ahead); thread 64 copies each
-unit's Q once the earlier tiles in stages 1-2 have been read and the last P copy has left the
-staging; warp 1 issues QK^T (rank 0) or relays ring landings (rank 1); warps 2-5 move Q, run the
-softmax into one of two S buffers, write P into the staging and copy it to the output CTA of their
-head (one P slot of two). Output CTAs 2-3: warp 0 copies V (4 stages); warp 1 checks V and issues
-P.V (rank 2), a unit's first one only once both CTAs have read the earlier unit's O out; warps 2-5
-read alpha, rescale O and write the output; warp 6 hands P slots back. The model keeps the kernel's
-barriers, counts and phase arithmetic and checks at every MMA and read that the buffer holds what
-its reader expects. Planted mistakes (a wait removed) must make it fail."""
+warp never runs two phases of that barrier ahead); warp 7 copies each unit's Q once every QK^T of
+the earlier unit is done (q_free, committed by the issuer after a unit's last tile); warp 6 of rank 0
+waits for each tile's operands (the unit's Q in place, both K halves, the S buffer read) and hands
+the tile to the issuer through one of two barriers; warp 1 issues QK^T (rank 0) or relays ring
+landings (rank 1); warps 2-5 move Q, run the softmax into one of two S buffers, write P into the
+staging and copy it to the output CTA of their head (one P slot of two). Output CTAs 2-3: warp 0
+copies V (4 stages); warp 7 of rank 2 (warp 1 of rank 3) checks V and, on rank 2, waits for the
+rest of each step's operands (rank 3's half, alpha applied, a unit's first step only once both
+CTAs have read the earlier unit's O out) and hands the step to the P.V issuer (warp 1) through the
+barrier of its V stage; warps 2-5 read alpha, rescale O and write the output; warp 6 hands P slots
+back. The model keeps the kernel's barriers, counts and phase arithmetic and checks at every MMA
+and read that the buffer holds what its reader expects. Planted mistakes (a wait removed) must make
+it fail."""
 import random
 
 import pytest
@@ -41,6 +45,9 @@ def model(seed, units, mut=""):
         d["q_moved"] = Bar(f"S{X}.q_moved", 4)
         d["q_pair"] = Bar(f"S{X}.q_pair", 8)
         d["stg_free"] = Bar(f"S{X}.stg_free", 1)
+        d["q_free"] = Bar(f"S{X}.q_free", 1)
+        for b in range(2):
+            d[f"go{b}"] = Bar(f"S{X}.go{b}", 1)
         sc[X] = d
     for Y in (2, 3):
         d = {}
@@ -52,6 +59,8 @@ def model(seed, units, mut=""):
             d[f"o_ready{s}"] = Bar(f"O{Y}.o_ready{s}", 8)
             d[f"pv_done{s}"] = Bar(f"O{Y}.pv_done{s}", 1)
         d["o_free"] = Bar(f"O{Y}.o_free", 8)
+        for s in range(NV):
+            d[f"go_pv{s}"] = Bar(f"O{Y}.go_pv{s}", 1)
         oc[Y] = d
 
     # data state
@@ -61,6 +70,7 @@ def model(seed, units, mut=""):
     qmoved = {X: {} for X in (0, 1)}              # unit -> softmax warps that moved their rows
     qrows = {X: [None] * 4 for X in (0, 1)}       # unit whose Q each warp's rows hold in tensor memory
     qk_pending = {"n": 0}                         # QK^T issued and not yet complete
+    qk_done = {"unit": -1}                        # last unit whose QK^T are all complete
     sbuf = {X: [None] * NP for X in (0, 1)}
     sreads = {}
     stg_busy = {X: 0 for X in (0, 1)}             # P copies in flight from the staging
@@ -110,7 +120,7 @@ def model(seed, units, mut=""):
                 sc[0][f"k_peer{s}"].arrive(S)
                 kuse[s] += 1
 
-    def issuer():
+    def helper():
         kuse = [0] * NK
         tc = 0
         for ui, n in enumerate(units):
@@ -122,6 +132,18 @@ def model(seed, units, mut=""):
                 yield ("wait", sc[0][f"k_peer{s}"], kuse[s])
                 if gt >= NP and mut != "no_sfree":
                     yield ("wait", sc[0][f"s_free{sb}"], (gt - NP) // NP)
+                sc[0][f"go{gt % 2}"].arrive(S)
+                kuse[s] += 1
+            tc += n
+
+    def issuer():
+        tc = 0
+        for ui, n in enumerate(units):
+            for j in range(n):
+                s, gt = j % NK, tc + j
+                sb = gt % NP
+                if mut != "no_go":
+                    yield ("wait", sc[0][f"go{gt % 2}"], gt // 2)
                 qk_pending["n"] += 1
 
                 def mma(s=s, sb=sb, gt=gt, ui=ui, j=j):
@@ -136,28 +158,34 @@ def model(seed, units, mut=""):
                         sc[X][f"s_full{sb}"].arrive(S)
                         sc[X][f"k_empty{s}"].arrive(S)
                 S.later(mma, 2, 8, queue="qk")
-                kuse[s] += 1
+
+            def qfree(ui=ui):
+                qk_done["unit"] = ui
+                for X in (0, 1):
+                    sc[X]["q_free"].arrive(S)
+            S.later(qfree, 1, 3, queue="qk")   # the commit after the unit's last tile
             tc += n
+
+    def qcopier(X):
+        for ui, n in enumerate(units):
+            if ui > 0 and mut != "no_qfree":
+                yield ("wait", sc[X]["q_free"], ui - 1)
+            chk(kpend[X][1] == 0 and kpend[X][2] == 0, f"S{X} Q of unit {ui} over K tiles not yet read")
+            chk(qk_done["unit"] >= ui - 1, f"S{X} Q of unit {ui} while unit {ui - 1}'s QK^T still read stages 1-2")
+            kstage[X][1] = kstage[X][2] = "Q"
+
+            def land_q(X=X, ui=ui):
+                qland[X] = ui
+                sc[X]["q_full"].complete_tx(S, 1)
+            sc[X]["q_full"].expect_tx(S, 1)
+            S.later(land_q, 2, 10)
+        if units:
+            yield ("wait", sc[X]["q_free"], len(units) - 1)
 
     def softmax(X, w):
         kq = [0] * NK
         tc = 0
         for ui, n in enumerate(units):
-            if w == 0:   # thread 64 copies the unit's Q
-                for s in (1, 2):
-                    if kq[s] > 0 and mut != "no_kempty_q":
-                        yield ("wait", sc[X][f"k_empty{s}"], kq[s] - 1)
-                if tc > 0 and mut != "no_stgfree_q":
-                    yield ("wait", sc[X]["stg_free"], tc - 1)
-                chk(kpend[X][1] == 0 and kpend[X][2] == 0, f"S{X} Q of unit {ui} over K tiles not yet read")
-                chk(stg_busy[X] == 0, f"S{X} Q of unit {ui} over a P copy in flight")
-                kstage[X][1] = kstage[X][2] = "Q"
-
-                def land_q(X=X, ui=ui):
-                    qland[X] = ui
-                    sc[X]["q_full"].complete_tx(S, 1)
-                sc[X]["q_full"].expect_tx(S, 1)
-                S.later(land_q, 2, 10)
             for j in range(n):
                 kq[j % NK] += 1
             yield ("wait", sc[X]["q_full"], ui)
@@ -237,6 +265,19 @@ def model(seed, units, mut=""):
                 if c == 0 and ui > 0 and mut != "no_ofree":
                     yield ("wait", oc[2]["o_free"], ui - 1)
 
+                oc[2][f"go_pv{s}"].arrive(S)
+                vc += 1
+            tc += n
+
+    def pv_issuer():
+        vc, tc = 0, 0
+        for ui, n in enumerate(units):
+            for c in range(2 * n):
+                s, j, e = vc % NV, c // 2, c % 2
+                gt = tc + j
+                if mut != "no_gopv":
+                    yield ("wait", oc[2][f"go_pv{s}"], vc // NV)
+
                 def pv(s=s, vc=vc, gt=gt, e=e, c=c, ui=ui):
                     for Yy in (2, 3):
                         chk(vstage[Yy][s] == vc, f"PV {vc}: O{Yy} V stage holds {vstage[Yy][s]}")
@@ -294,6 +335,10 @@ def model(seed, units, mut=""):
             S.roles.append(Role(f"S{X}.soft{w}", softmax(X, w)))
     S.roles.append(Role("S1.relay", relay()))
     S.roles.append(Role("S0.issuer", issuer()))
+    S.roles.append(Role("S0.helper", helper()))
+    for X in (0, 1):
+        S.roles.append(Role(f"S{X}.qcopy", qcopier(X)))
+    S.roles.append(Role("O2.pv_issuer", pv_issuer()))
     for Y in (2, 3):
         S.roles.append(Role(f"O{Y}.vprod", vprod(Y)))
         S.roles.append(Role(f"O{Y}.vcheck", vcheck(Y)))
@@ -334,7 +379,7 @@ def test_runs_of_single_tile_units():
 
 
 @pytest.mark.parametrize("mut", ["no_qmoved", "no_sfree", "no_stgfree", "no_oready",
-                                 "no_pvdone_epilogue", "no_stgfree_q"])
+                                 "no_pvdone_epilogue", "no_qfree", "no_go", "no_gopv"])
 def test_global_protocol_model_catches_a_missing_wait(mut):
     """Control: each of these waits guards a hazard the model can see, so removing it fails."""
     assert run_many(150, mut)
@@ -345,10 +390,3 @@ def test_o_free_is_implied_by_the_first_o_ready():
     implied: the epilogue warps arrive on o_ready for a unit's first tile only after reading the
     earlier unit's O out, and the first P.V waits on that o_ready. So removing it is no hazard."""
     assert not run_many(150, "no_ofree")
-
-
-def test_k_empty_before_q_is_implied_by_the_last_s():
-    """Thread 64 waits for the earlier tiles in stages 1-2 to be read before copying a unit's Q; that
-    too is implied, since it copies only after reading the earlier unit's last S, and the QK^T of one
-    issuing thread complete in order. Kept as a guard; removing it is no hazard."""
-    assert not run_many(150, "no_kempty_q")
