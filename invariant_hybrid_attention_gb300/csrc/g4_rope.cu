@@ -585,9 +585,11 @@ __device__ __forceinline__ void find_group(const SeqRows& rows, int gi, int& out
 }
 
 // kGroupHeads KV heads per warp (4; 2 for a cache of 2 KV heads, the sliding layer's tensor-parallel
-// rank slice at tp = 8).
+// rank slice at tp = 8). Two blocks per SM (at most 128 registers a thread) with one iteration's
+// loads in flight per warp measured faster than one block with two (111 against 124 us for the
+// 4 x 4096 batch).
 template <int D, int R, int kGroupHeads>
-__global__ void __launch_bounds__(256) append_kv_groups_kernel(const __nv_bfloat16* __restrict__ k,
+__global__ void __launch_bounds__(256, 2) append_kv_groups_kernel(const __nv_bfloat16* __restrict__ k,
                                                                const __nv_bfloat16* __restrict__ v, SeqRows rows,
                                                                PagedCache c, RopeTables tb, uint32_t* err) {
   static_assert(D == 256 && R == 128, "the group path serves the sliding geometry");
@@ -614,7 +616,7 @@ __global__ void __launch_bounds__(256) append_kv_groups_kernel(const __nv_bfloat
   if (pos < cs0 || pos >= cs0 + L) return;   // outside the call's rows (the group's ragged ends)
   const int j = pos & 15;
   const size_t row = (size_t)(qs + (pos - cs0));
-#pragma unroll 2   // two iterations' loads in flight at once
+#pragma unroll 1
   for (int i = 0; i < 4; ++i) {
     const int d0 = 8 * (p + 4 * i);
     float2 cs[8];
@@ -696,8 +698,10 @@ __global__ void __launch_bounds__(256) norm_queries_kernel(const __nv_bfloat16* 
 // page-head block; the rotated pairs (t, t + 256), t < 64, are those of i = 0, 1 with i + 8, whose
 // p-RoPE goes to the k_rot side page with the per-row append's angles (rope_cs), rotation
 // (rope_pair) and cast, so the cache bits are the same.
+// Eight blocks per SM (32 registers a thread), so that a 2 x 8192 batch's warps are all resident at
+// once (42 against 48 us with five blocks and a second, partial wave).
 template <int D, int R>
-__global__ void __launch_bounds__(256) append_s_groups_kernel(const __nv_bfloat16* __restrict__ k, SeqRows rows,
+__global__ void __launch_bounds__(256, 8) append_s_groups_kernel(const __nv_bfloat16* __restrict__ k, SeqRows rows,
                                                              PagedCache c, RopeTables tb, uint32_t* err) {
   static_assert(D == 512 && R == 64, "the group path serves the global geometry");
   const int lane = threadIdx.x & 31;
