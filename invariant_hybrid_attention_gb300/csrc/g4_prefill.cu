@@ -23,25 +23,28 @@
 // while the current one finishes, and its roped Q tile (prefetched into L2 one unit ahead) is
 // loaded as soon as the last QK^T of the current unit has read the previous one.
 // Per CTA:
-//   warp 0     per unit: K tiles 0 and 1, then the roped Q tile (dims 0-127 into the next K
-//              ring slot, dims 128-255 into their own buffer, once the previous unit's QK^T
-//              is done), then the remaining K tiles: this CTA's K half of each key tile is four
-//              8 KB page-head blocks, into a 3-stage ring;
+//   warp 0     per unit: K tile 0, then the roped Q tile (dims 0-127 into the next K ring
+//              slot, dims 128-255 into their own buffer, once the previous unit's QK^T is
+//              done), then the remaining K tiles: this CTA's K half of each key tile is four
+//              8 KB page-head blocks, into a 2-stage ring (three stages measured the same);
 //   warp 6     this CTA's V half of each key tile (eight 4 KB copies: sliding V pages store each
-//              128-dim half of a page-head block contiguously) into a 3-stage ring;
+//              128-dim half of a page-head block contiguously) into a 2-stage ring;
 //   warp 1     even CTA: issues S = Q K^T for the pair. Odd CTA: tells the even CTA when each
 //              of its K ring slots has landed;
 //   warp 7     zeroes value rows of this CTA's V half that hold no key of the sequence; then
 //              the even CTA's issues O += P V for the pair, the odd CTA's tells the even CTA
 //              that its V half is ready;
-//   warps 2-5  one thread per query row of this CTA's head: Q dims 0-127 into tensor memory,
-//              mask, online softmax (lazy rescale, threshold 2^8), P (bf16), the O correction
-//              when needed, and the epilogue O / l -> bf16.
+//   warps 2-5, 8-11  two threads per query row of this CTA's head, one per half of the
+//              columns (warps w and w + 6 share the rows of quarter w % 4, the tensor-memory
+//              lanes they may access): Q dims 0-127 into tensor memory, mask, online softmax
+//              (lazy rescale, threshold 2^8; the halves agree on each tile's row max through a
+//              barrier of their quarter), P (bf16), the O correction when needed, and the
+//              epilogue O / l -> bf16 (the halves' sums added in a fixed order).
 // Queries (kRope): the Q tile is copied from the raw query rows and rotated in place in shared
 // memory before it moves: all 128 pairs (t, t + 128) turn, t in Q dims 0-127 (the K ring slot,
-// bound for tensor memory) and t + 128 in the shared-memory half. Softmax thread t rotates pair t
-// of every row of the tile (rotate_q_pair), the four softmax warps meet on an mbarrier, and each
-// thread then moves its row. The angles, the rotation and the bf16 cast are those of the append
+// bound for tensor memory) and t + 128 in the shared-memory half. Softmax thread i rotates pair
+// i % 128 of rows 64 (i / 128) .. +63 (rotate_q_pair), the eight softmax warps meet on an
+// mbarrier, and each thread then moves its half of its row. The angles, the rotation and the bf16 cast are those of the append
 // pass, so the roped queries, and with them every output bit, are those a staged call gives. Otherwise (the staged form: normed queries,
 // image spans, the exact decode) the append pass before this kernel wrote bf16(RoPE(q)) into the
 // sequence rows of `out`, which the Q copies read; the epilogue later overwrites exactly those
@@ -64,8 +67,8 @@ using namespace pf;
 
 constexpr int kSD = kSlidingD;                    // 256
 constexpr int kSN = 128;                          // keys per tile
-constexpr int kNK = 3, kNV = 3;                   // K and V ring stages
-constexpr int kQAfter = 2;                        // a unit's Q takes the K ring slot after its first two tiles
+constexpr int kNK = 2, kNV = 2;                   // K and V ring stages
+constexpr int kQAfter = 1;                        // a unit's Q takes the K ring slot after its first tile
 // QK^T of a unit's first tile needs its Q, so the Q slot must come while that tile's slot is still
 // held: a Q slot behind kNK or more key tiles would wait on a ring that only QK^T can free.
 static_assert(kQAfter < kNK, "the Q slot must fit in the ring beside the tiles issued before it");
@@ -75,12 +78,13 @@ constexpr int kVGroupBytes = 8 * (kSD / 2) * 2;   // V half: 8 keys x 128 dims, 
 constexpr int kVHalfPageBytes = 2 * kVGroupBytes; // V half of one page-head block: 4 KB
 constexpr int kKStage = (kSN / 2 / kPage) * kPageBytes;   // 4 pages: 32 KB
 constexpr int kVStage = (kSN / 8) * kVGroupBytes;         // 16 key groups: 32 KB
-constexpr int kThreads = 256;
+constexpr int kSmxWarps = 8;                      // softmax warps: two per row quarter, one per half of the columns
+constexpr int kThreads = 128 + 32 * kSmxWarps;    // warps 0, 1, 6, 7 have roles; 2-5 and 8-11 run the softmax
 constexpr uint32_t kTmO = 0, kTmQ = 256, kTmP = 320, kTmS = 384;
 constexpr uint32_t kIdescQK = idesc_bf16(2 * kBM, kSN, false, false);   // M 256 over the pair, N 128 keys
 constexpr uint32_t kIdescPV = idesc_bf16(2 * kBM, kSD, false, true);    // M 256, N 256 dims
 constexpr uint16_t kBoth = 0x3;
-constexpr uint32_t kPairWarps = 8;                // softmax warps of both CTAs
+constexpr uint32_t kPairWarps = 2 * kSmxWarps;   // softmax warps of both CTAs
 
 struct SlidingSmem {
   uint8_t k[kNK][kKStage];          // K halves [8 key groups][32 dim groups][8][8], or a unit's Q dims 0-127
@@ -90,6 +94,8 @@ struct SlidingSmem {
   uint64_t v_full[kNV], v_empty[kNV], v_ready[kNV];
   uint64_t s_full, s_free, p_full, pv_done;
   uint64_t q_full, q_pair, q_free, o_free, q_read, q_rot, teardown;
+  uint64_t xchg[4];                 // the two softmax warps of row quarter i have posted their halves
+  float xv[2][2][kBM];              // [exchange parity][column half][row]: a half's row max, then its sum
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -180,8 +186,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(&sm.q_pair, kPairWarps);   // even CTA: both CTAs' Q is in place
     mbar_init(&sm.q_free, 1);            // the unit's last QK^T is done: Q may be replaced
     mbar_init(&sm.o_free, kPairWarps);   // even CTA: both CTAs have read O out
-    mbar_init(&sm.q_read, kSoftmaxThreads / 32);   // this CTA's softmax warps have read the Q slot
-    mbar_init(&sm.q_rot, kSoftmaxThreads / 32);    // kRope: this CTA's softmax warps have rotated Q
+    mbar_init(&sm.q_read, kSmxWarps);    // this CTA's softmax warps have read the Q slot
+    mbar_init(&sm.q_rot, kSmxWarps);     // kRope: this CTA's softmax warps have rotated Q
+    for (int i = 0; i < 4; ++i) mbar_init(&sm.xchg[i], 2);
     mbar_init(&sm.teardown, 2);          // on an abort both issuers commit
     sm.abort_flag = 0;
     fence_mbar_init();
@@ -447,10 +454,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax / epilogue warps
+    // Two warps per row quarter: warp w (2-5, 8-11) owns rows 32 (w % 4) .. +31 (its tensor-memory
+    // lanes) and one half of the columns, hc = w / 8: keys 64 hc .. 64 hc + 63 of each S tile (P
+    // key pairs 32 hc .. +31), dims 128 hc .. 128 hc + 127 of O. The two halves of a row meet
+    // once per key tile to agree on the row max (so both scale P, l and O alike) and once per
+    // unit to add their sums; everything else a thread does is its own half's.
     const int r = 32 * (warp & 3) + lane;   // query row = tensor-memory lane
+    const int hc = warp >> 3;               // column half
+    const int sidx = 32 * (warp < 8 ? warp - 2 : warp - 4) + lane;   // softmax thread 0 .. 255
     const uint32_t tq = tm + tmem_lane_base(warp);
+    uint64_t* const xb = &sm.xchg[warp & 3];
     const float cl2 = p.scale_log2;
-    uint32_t c0 = 0, jt = 0;
+    uint32_t c0 = 0, jt = 0, xph = 0;   // xph: exchanges of this row quarter so far
     int uq = 0, u = cluster - n_clusters;
     bool ok = true;
     auto next_unit = [&](Unit& o) -> bool {   // this cluster's next unit with rows (warp-wide)
@@ -458,11 +473,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (sliding_unit<kSpan>(p, u, rank, o)) return true;
       return false;
     };
+    // Post this half's value of row r, then return the two halves' values (half 0's first). The
+    // values of one exchange sit in xv[xph & 1]: the partner reads them before it can post its
+    // next pair, and the one after that reuses the slot only once both have passed this one.
+    auto exchange = [&](float v, float& v0, float& v1) -> bool {
+      sm.xv[xph & 1][hc][r] = v;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(xb);
+      if (!__all_sync(0xffffffffu, mbar_wait_ool(xb, xph & 1, abort_flag, p.err, p.wait_ns))) return false;
+      v0 = sm.xv[xph & 1][0][r];
+      v1 = sm.xv[xph & 1][1][r];
+      ++xph;
+      return true;
+    };
     // Q dims 0-127 of unit o (the tile the producer put in K ring slot c0o + qpos, 128B swizzle)
     // into tensor memory as bf16 pairs: the A operand of half of the QK^T k-steps; with kRope the
-    // row is rotated on the way (dims 128-255 in place in shared memory). The load was issued only
+    // tile is rotated first (dims 128-255 in place in shared memory). The load was issued only
     // after the previous unit's last QK^T, so the columns and the shared-memory half are free.
-    // Once all four warps have read the slot, one thread releases it.
+    // Each warp moves dims 64 hc .. +63 of its rows. Once all eight warps have read the slot, one
+    // thread releases it.
     auto move_q = [&](const Unit& o, uint32_t c0o, int uqo) -> bool {
       const uint32_t cq = c0o + o.qpos;
       const int s = cq % kNK;
@@ -471,26 +500,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         return false;
       const uint8_t* qrow = sm.k[s] + r * 128;
       if constexpr (kRope) {
-        // thread t rotates pair t of every row of the tile
-        const int t = threadIdx.x - 64;
-        rotate_q_pair<8, kSlidingR>(sm.k[s] + (t >> 6) * kQChunk, sm.qhi + (t >> 6) * kQChunk, p.tb, t, kBM * o.t, 0);
+        // softmax thread i rotates pair i % 128 of rows 64 (i / 128) .. +63
+        const int t = sidx & 127;
+        rotate_q_pair<4, kSlidingR>(sm.k[s] + (t >> 6) * kQChunk, sm.qhi + (t >> 6) * kQChunk, p.tb, t, kBM * o.t,
+                                    64 * (sidx >> 7));
         fence_proxy_async();   // QK^T reads the rewritten half, and the ring slot is refilled, by the async proxy
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.q_rot);
         if (!__all_sync(0xffffffffu, mbar_wait_ool(&sm.q_rot, uqo & 1, abort_flag, p.err, p.wait_ns))) return false;
       }
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      {
         uint32_t w[32];
 #pragma unroll
         for (int q8 = 0; q8 < 8; ++q8) {
-          const uint4 v = *reinterpret_cast<const uint4*>(qrow + c * kQChunk + ((q8 ^ (r & 7)) * 16));
+          const uint4 v = *reinterpret_cast<const uint4*>(qrow + hc * kQChunk + ((q8 ^ (r & 7)) * 16));
           w[4 * q8] = v.x;
           w[4 * q8 + 1] = v.y;
           w[4 * q8 + 2] = v.z;
           w[4 * q8 + 3] = v.w;
         }
-        tmem_st32(tq + kTmQ + 32 * c, w);   // dims 64c .. 64c+63 -> columns 32c .. 32c+31
+        tmem_st32(tq + kTmQ + 32 * hc, w);   // dims 64hc .. 64hc+63 -> columns 32hc .. 32hc+31
       }
       tmem_st_wait();
       tc_fence_before();
@@ -513,6 +542,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     bool have = next_unit(cur);
     if (have) ok = move_q(cur, c0, uq);
     bool have_n = have && next_unit(nxt);
+    constexpr int kHN = kSN / 2;   // keys of one half
     while (ok && have) {
       const int pos = kBM * cur.t + r;
       const bool row_ok = pos >= cur.p_lo && pos <= cur.p_hi;
@@ -525,46 +555,52 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           row_hi = min(row_hi, cur.k_hi);
         }
       }
-      float m_used = -INFINITY, l_run = 0.f;
+      float m_used = -INFINITY, l_half = 0.f;
       for (int j = 0; j < cur.n_tiles; ++j, ++jt) {
-        const int kb = (cur.kt0 + j) * kSN;
+        const int kb = (cur.kt0 + j) * kSN + kHN * hc;   // this half's first key
         // Waits are made warp-uniform so that every lane leaves the loop together on an abort.
         if (!__all_sync(0xffffffffu, mbar_wait_ool(&sm.s_full, jt & 1, abort_flag, p.err, p.wait_ns))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        uint32_t sr[kSN];
+        uint32_t sr[kHN];
 #pragma unroll
-        for (int c = 0; c < kSN / 32; ++c)
-          tmem_ld32(tq + kTmS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
+        for (int c = 0; c < kHN / 32; ++c)
+          tmem_ld32(tq + kTmS + kHN * hc + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
         tmem_ld_wait();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) arrive_leader(&sm.s_free);   // S may now be overwritten by the next QK^T
 
-        float s[kSN];
+        float s[kHN];
 #pragma unroll
-        for (int c = 0; c < kSN; ++c) s[c] = __uint_as_float(sr[c]);
-        const bool full = kSpan ? row_ok && kb >= row_lo && kb + kSN - 1 <= row_hi
-                                : row_ok && kb + kSN - 1 <= pos && (W == 0 || pos - kb <= W - 1);
-        if (!full) {   // the row's visible keys in this tile are one run of columns [lo, hi]
+        for (int c = 0; c < kHN; ++c) s[c] = __uint_as_float(sr[c]);
+        const bool full = kSpan ? row_ok && kb >= row_lo && kb + kHN - 1 <= row_hi
+                                : row_ok && kb + kHN - 1 <= pos && (W == 0 || pos - kb <= W - 1);
+        if (!full) {   // the row's visible keys in this half are one run of columns [lo, hi]
           int lo = kSpan ? max(0, row_lo - kb) : (W > 0 ? max(0, pos - W + 1 - kb) : 0);
-          int hi = row_ok ? min(kSN - 1, (kSpan ? row_hi : pos) - kb) : -1;
+          int hi = row_ok ? min(kHN - 1, (kSpan ? row_hi : pos) - kb) : -1;
           if (hi < lo) lo = hi = 1 << 20;   // none
           const unsigned span = (unsigned)(hi - lo);
 #pragma unroll
-          for (int c = 0; c < kSN; ++c) s[c] = ((unsigned)(c - lo) <= span) ? s[c] : -INFINITY;
+          for (int c = 0; c < kHN; ++c) s[c] = ((unsigned)(c - lo) <= span) ? s[c] : -INFINITY;
         }
         float mx[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           mx[i] = s[i];
 #pragma unroll
-          for (int c = 1; c < kSN / 8; ++c) mx[i] = fmaxf(mx[i], s[i + 8 * c]);
+          for (int c = 1; c < kHN / 8; ++c) mx[i] = fmaxf(mx[i], s[i + 8 * c]);
         }
-        const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * cl2;
+        float m0, m1;   // the two halves' maxima of the row
+        if (!exchange(fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                            fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))),
+                      m0, m1)) {
+          ok = false;
+          break;
+        }
+        const float mt = fmaxf(m0, m1) * cl2;
         float alpha = 1.f;
         bool need_o = false;
         if (mt > m_used + kLazyRescale) {
@@ -573,17 +609,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           m_used = mt;
         }
         const float neg_m = (m_used == -INFINITY) ? 0.f : -m_used;
-        uint32_t pw[kSN / 2];
+        uint32_t pw[kHN / 2];
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int w = 0; w < kSN / 2; ++w) {
+        for (int w = 0; w < kHN / 2; ++w) {
           const float e0 = ex2(fmaf(s[2 * w], cl2, neg_m));
           const float e1 = ex2(fmaf(s[2 * w + 1], cl2, neg_m));
           ls[w & 3] += e0;
           ls[w & 3] += e1;
           pw[w] = pack_bf16(e0, e1);   // declared cast: P in bf16 for P.V
         }
-        l_run = fmaf(l_run, alpha, (ls[0] + ls[1]) + (ls[2] + ls[3]));
+        l_half = fmaf(l_half, alpha, (ls[0] + ls[1]) + (ls[2] + ls[3]));
 
         // The previous P.V has completed: the P buffer is free and O holds every earlier tile.
         if (jt > 0 && !__all_sync(0xffffffffu, mbar_wait_ool(&sm.pv_done, (jt - 1) & 1, abort_flag, p.err, p.wait_ns))) {
@@ -594,18 +630,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (__any_sync(0xffffffffu, need_o)) {   // O correction (rows whose max rose by more than 2^8)
           const float a = need_o ? alpha : 1.f;
 #pragma unroll 1
-          for (int cc = 0; cc < kSD / 32; ++cc) {
+          for (int cc = 0; cc < kSD / 64; ++cc) {
             uint32_t o[32];
-            tmem_ld32(tq + kTmO + 32 * cc, o);
+            tmem_ld32(tq + kTmO + (kSD / 2) * hc + 32 * cc, o);
             tmem_ld_wait();
 #pragma unroll
             for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * a);
-            tmem_st32(tq + kTmO + 32 * cc, o);
+            tmem_st32(tq + kTmO + (kSD / 2) * hc + 32 * cc, o);
           }
         }
-        // P_j (bf16 key pairs): the A operand of P.V.
-        tmem_st32(tq + kTmP, *reinterpret_cast<const uint32_t(*)[32]>(&pw[0]));
-        tmem_st32(tq + kTmP + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pw[32]));
+        // This half of P_j (bf16 key pairs 32 hc .. +31): the A operand of P.V.
+        tmem_st32(tq + kTmP + 32 * hc, *reinterpret_cast<const uint32_t(*)[32]>(&pw[0]));
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -621,22 +656,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         break;
       }
 
-      // Epilogue: O / l -> bf16, rows of this sequence only. Once O is in registers the even
-      // CTA may start the next unit's P.V, which overwrites it.
-      if (!__all_sync(0xffffffffu, mbar_wait_ool(&sm.pv_done, (jt - 1) & 1, abort_flag, p.err, p.wait_ns))) {
+      // Epilogue: O / l -> bf16, rows of this sequence only, this half's dims. Once O is in
+      // registers the even CTA may start the next unit's P.V, which overwrites it.
+      float l0, l1;   // the halves' sums, added in a fixed order
+      if (!exchange(l_half, l0, l1) ||
+          !__all_sync(0xffffffffu, mbar_wait_ool(&sm.pv_done, (jt - 1) & 1, abort_flag, p.err, p.wait_ns))) {
         ok = false;
         break;
       }
       tc_fence_after();
+      const float l_run = l0 + l1;
       const float inv = (l_run > 0.f) ? __frcp_rn(l_run) : 0.f;
       const unsigned valid = __ballot_sync(0xffffffffu, row_ok);
       const long long wrow0 = (long long)cur.q_row0 + 32 * (warp & 3);
 #pragma unroll 1
-      for (int cc = 0; cc < kSD / 32; ++cc) {
+      for (int cc = 0; cc < kSD / 64; ++cc) {
         uint32_t o[32];
-        tmem_ld32(tq + kTmO + 32 * cc, o);
+        tmem_ld32(tq + kTmO + (kSD / 2) * hc + 32 * cc, o);
         tmem_ld_wait();
-        if (cc == kSD / 32 - 1) {
+        if (cc == kSD / 64 - 1) {
           tc_fence_before();
           __syncwarp();
           if (lane == 0) arrive_leader(&sm.o_free);
@@ -645,7 +683,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 16; ++c)
           w16[c] = pack_bf16(__uint_as_float(o[2 * c]) * inv, __uint_as_float(o[2 * c + 1]) * inv);
-        store_rows32<kSD>(w16, p.out, wrow0, p.hq, cur.h, 32 * cc, valid, lane);
+        store_rows32<kSD>(w16, p.out, wrow0, p.hq, cur.h, (kSD / 2) * hc + 32 * cc, valid, lane);
       }
       c0 = c0n;
       ++uq;

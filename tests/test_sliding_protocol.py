@@ -1,13 +1,15 @@
 """The barrier protocol of the sliding prefill kernel (csrc/g4_prefill.cu), modelled on the CPU.
 
 A persistent 2-CTA cluster walks its units in order. Per CTA: warp 0 copies K tiles and each
-unit's roped Q (dims 0-127 into the K ring slot after the unit's first two tiles, dims 128-255
-into their own buffer, once the previous unit's last QK^T is done); warp 6 copies V; warp 1
-issues QK^T (even CTA) or relays ring landings (odd CTA); warp 7 checks V and issues P.V (even
-CTA); warps 2-5 move Q into tensor memory, run the softmax, write P and the epilogue. The model
-keeps the kernel's barriers, counts and phase arithmetic, and checks at every MMA and every
-read that the buffer holds the expected tile or unit: K slots, the Q buffers, the single S and
-P buffers in tensor memory, the V stages and O.
+unit's roped Q (dims 0-127 into the K ring slot after the unit's first tile, dims 128-255 into
+their own buffer, once the previous unit's last QK^T is done); warp 6 copies V; warp 1 issues
+QK^T (even CTA) or relays ring landings (odd CTA); warp 7 checks V and issues P.V (even CTA);
+eight softmax warps, two per row quarter (one per half of the columns), move Q into tensor
+memory, run the softmax, write P and the epilogue, and meet their row partner on a barrier of
+their quarter once per key tile (the row max) and once per unit (the sums). The model keeps the
+kernel's barriers, counts and phase arithmetic, and checks at every MMA and every read that the
+buffer holds the expected tile or unit: K slots, the Q buffers, the single S and P buffers in
+tensor memory, the V stages, O and the partner's posted half.
 
 The random unit sequences are lists of key-tile counts; a planted mistake (a wait removed) must
 make the model fail."""
@@ -17,7 +19,8 @@ import pytest
 
 from protocol_sim import Bar, Err, Role, Sim
 
-NK, NV, QAFTER = 3, 3, 2
+NK, NV, QAFTER = 2, 2, 1
+SMX = 8   # softmax warps per CTA: two per row quarter (w and w + 4 here), one per column half
 
 
 def model(seed, units, mut=""):
@@ -34,9 +37,11 @@ def model(seed, units, mut=""):
             d[f"v_full{s}"] = Bar(f"C{X}.v_full{s}", 1)
             d[f"v_empty{s}"] = Bar(f"C{X}.v_empty{s}", 1)
             d[f"v_ready{s}"] = Bar(f"C{X}.v_ready{s}", 1)
-        for nm, cnt in (("s_full", 1), ("s_free", 8), ("p_full", 8), ("pv_done", 1), ("q_full", 1),
-                        ("q_pair", 8), ("q_free", 1), ("o_free", 8), ("q_read", 4)):
+        for nm, cnt in (("s_full", 1), ("s_free", 2 * SMX), ("p_full", 2 * SMX), ("pv_done", 1), ("q_full", 1),
+                        ("q_pair", 2 * SMX), ("q_free", 1), ("o_free", 2 * SMX), ("q_read", SMX)):
             d[nm] = Bar(f"C{X}.{nm}", cnt)
+        for q in range(4):
+            d[f"xchg{q}"] = Bar(f"C{X}.xchg{q}", 2)
         B[X] = d
     qpos = [min(QAFTER, n) for n in units]
     def kslot(ui, j):
@@ -58,7 +63,8 @@ def model(seed, units, mut=""):
     vring = {X: [None] * NV for X in (0, 1)}
     o_own = {X: None for X in (0, 1)}
     o_steps = {X: 0 for X in (0, 1)}
-    o_reads = {X: 4 for X in (0, 1)}
+    o_reads = {X: SMX for X in (0, 1)}
+    xposted = {}                                   # (CTA, quarter, exchange) -> halves posted
     qk_done_unit = {"last": -1}
     def chk(c, m):
         if not c:
@@ -171,7 +177,7 @@ def model(seed, units, mut=""):
                         chk(vring[Y][s] == cv, f"PV {jt}: C{Y} V stage holds {vring[Y][s]}")
                         chk(pbuf[Y] == jt, f"PV {jt}: C{Y} P holds {pbuf[Y]}")
                         if i == 0:
-                            chk(o_reads[Y] == 4, f"PV of unit {ui} overwrites C{Y} O before it is read out")
+                            chk(o_reads[Y] == SMX, f"PV of unit {ui} overwrites C{Y} O before it is read out")
                             o_own[Y], o_steps[Y], o_reads[Y] = ui, 0, 0
                         else:
                             chk(o_own[Y] == ui, f"PV {jt} of unit {ui} into C{Y} O of {o_own[Y]}")
@@ -184,6 +190,18 @@ def model(seed, units, mut=""):
                 cv += 1
     pwrites = {}   # (CTA, tile): softmax warps that have written their rows of P
     def softmax(X, w):
+        q = w % 4
+        xn = [0]   # exchanges of this row quarter so far
+        def exchange():
+            """Post this half's value, wait for the partner's (the kernel's xchg barrier)."""
+            n = xn[0]
+            key = (X, q, n)
+            xposted[key] = xposted.get(key, 0) + 1
+            B[X][f"xchg{q}"].arrive(S)
+            if mut != "no_xchg":
+                yield ("wait", B[X][f"xchg{q}"], n)
+            chk(xposted.get(key, 0) == 2, f"C{X}.w{w} reads its row partner's half of exchange {n} before it was posted")
+            xn[0] += 1
         def move_q(ui):
             cq = c0s[ui] + qpos[ui]
             s = cq % NK
@@ -209,9 +227,10 @@ def model(seed, units, mut=""):
                 yield ("wait", B[X]["s_full"], jt)
                 chk(sbuf[X] == jt, f"C{X}.w{w} reads S holding {sbuf[X]} not {jt}")
                 sreads[X] += 1
-                if sreads[X] == 4:
+                if sreads[X] == SMX:
                     sbuf[X] = None
                 B[0]["s_free"].arrive(S)
+                yield from exchange()   # the row max
                 if jt > 0:
                     yield ("wait", B[X]["pv_done"], jt - 1)
                     if j > 0 and rng.random() < 0.5:
@@ -220,12 +239,13 @@ def model(seed, units, mut=""):
                     f"C{X}.w{w} writes P {jt} over {pbuf[X]}")
                 key = (X, jt)
                 pwrites[key] = pwrites.get(key, 0) + 1
-                if pwrites[key] == 4:
+                if pwrites[key] == SMX:
                     pbuf[X] = jt
                 B[0]["p_full"].arrive(S)
             if ui + 1 < len(units):
                 yield from move_q(ui + 1)
             jl = jt0s[ui] + n - 1
+            yield from exchange()   # the halves' sums
             yield ("wait", B[X]["pv_done"], jl)
             chk(o_own[X] == ui and o_steps[X] == n, f"C{X}.w{w} epilogue of unit {ui}: O of {o_own[X]}, {o_steps[X]} steps")
             o_reads[X] += 1
@@ -234,7 +254,7 @@ def model(seed, units, mut=""):
         S.roles.append(Role(f"C{X}.prodK", producer_k(X)))
         S.roles.append(Role(f"C{X}.prodV", producer_v(X)))
         S.roles.append(Role(f"C{X}.vpv", vpv(X)))
-        for w in range(4):
+        for w in range(SMX):
             S.roles.append(Role(f"C{X}.soft{w}", softmax(X, w)))
     S.roles.append(Role("C1.relay", relay()))
     S.roles.append(Role("C0.issuer", issuer()))
@@ -259,7 +279,7 @@ def test_sliding_protocol_has_no_deadlock_aliasing_or_hazard():
     assert not failures, failures[:3]
 
 
-@pytest.mark.parametrize("mut", ["no_qfree", "no_sfree", "no_qread"])
+@pytest.mark.parametrize("mut", ["no_qfree", "no_sfree", "no_qread", "no_xchg"])
 def test_sliding_protocol_model_catches_a_missing_wait(mut):
     """Control: each of these waits guards a hazard the model can see, so removing it fails. (The
     P.V issuer's wait for O to be read out is implied as well by its wait for the next unit's
