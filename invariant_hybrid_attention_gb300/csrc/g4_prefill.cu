@@ -20,13 +20,14 @@
 // The grid holds as many clusters as can be resident at once; cluster c computes units
 // c, c + C, c + 2C, ... (a fixed assignment: no work queue, no atomics). The K and V rings and
 // every barrier run on counters that continue across units, so the next unit's keys stream in
-// while the current one finishes, and its roped Q tile (prefetched into L2 one unit ahead) is
-// loaded as soon as the last QK^T of the current unit has read the previous one.
+// while the current one finishes; its Q tile is copied into buffers of its own while the
+// current unit runs, so that the softmax warps can turn it as soon as they are done with the
+// current unit.
 // Per CTA:
-//   warp 0     per unit: K tile 0, then the roped Q tile (dims 0-127 into the next K ring
-//              slot, dims 128-255 into their own buffer, once the previous unit's QK^T is
-//              done), then the remaining K tiles: this CTA's K half of each key tile is four
-//              8 KB page-head blocks, into a 2-stage ring (three stages measured the same);
+//   warp 0     this CTA's K half of each key tile (four 8 KB page-head blocks) into a 2-stage
+//              ring (three stages measured the same), and each unit's Q tile: dims 0-127 into a
+//              staging buffer, dims 128-255 into one of two buffers by unit parity, the next
+//              unit's after this unit's second key tile, once this unit's Q has moved on;
 //   warp 6     this CTA's V half of each key tile (eight 4 KB copies: sliding V pages store each
 //              128-dim half of a page-head block contiguously) into a 2-stage ring;
 //   warp 1     even CTA: issues S = Q K^T for the pair. Odd CTA: tells the even CTA when each
@@ -41,7 +42,7 @@
 //              barrier of their quarter), P (bf16), the O correction when needed, and the
 //              epilogue O / l -> bf16 (the halves' sums added in a fixed order).
 // Queries (kRope): the Q tile is copied from the raw query rows and rotated in place in shared
-// memory before it moves: all 128 pairs (t, t + 128) turn, t in Q dims 0-127 (the K ring slot,
+// memory before it moves: all 128 pairs (t, t + 128) turn, t in Q dims 0-127 (the staging buffer,
 // bound for tensor memory) and t + 128 in the shared-memory half. Softmax thread i rotates pair
 // i % 128 of rows 64 (i / 128) .. +63 (rotate_q_pair), the eight softmax warps meet on an
 // mbarrier, and each thread then moves its half of its row. The angles, the rotation and the bf16 cast are those of the append
@@ -68,10 +69,6 @@ using namespace pf;
 constexpr int kSD = kSlidingD;                    // 256
 constexpr int kSN = 128;                          // keys per tile
 constexpr int kNK = 2, kNV = 2;                   // K and V ring stages
-constexpr int kQAfter = 1;                        // a unit's Q takes the K ring slot after its first tile
-// QK^T of a unit's first tile needs its Q, so the Q slot must come while that tile's slot is still
-// held: a Q slot behind kNK or more key tiles would wait on a ring that only QK^T can free.
-static_assert(kQAfter < kNK, "the Q slot must fit in the ring beside the tiles issued before it");
 constexpr int kPageBytes = kPage * kSD * 2;       // one tiled page-head block: 8 KB
 constexpr int kKeyGroupBytes = 8 * kSD * 2;       // K: 8 keys x 256 dims, 4 KB
 constexpr int kVGroupBytes = 8 * (kSD / 2) * 2;   // V half: 8 keys x 128 dims, 2 KB
@@ -86,10 +83,11 @@ constexpr uint32_t kIdescPV = idesc_bf16(2 * kBM, kSD, false, true);    // M 256
 constexpr uint16_t kBoth = 0x3;
 constexpr uint32_t kPairWarps = 2 * kSmxWarps;   // softmax warps of both CTAs
 
-struct SlidingSmem {
-  uint8_t k[kNK][kKStage];          // K halves [8 key groups][32 dim groups][8][8], or a unit's Q dims 0-127
+struct alignas(1024) SlidingSmem {
+  uint8_t qlo[2 * kQChunk];         // a unit's Q dims 0-127 (128B swizzle) until they move into tensor memory
+  uint8_t qhi[2][2 * kQChunk];      // unit u's Q dims 128-255 in qhi[u & 1]: the shared-memory A operand
+  uint8_t k[kNK][kKStage];          // K halves [8 key groups][32 dim groups][8][8]
   uint8_t v[kNV][kVStage];          // V halves [16 key groups][16 dim groups][8][8]
-  uint8_t qhi[2 * kQChunk];         // Q dims 128-255 (128B swizzle), the shared-memory A operand
   uint64_t k_full[kNK], k_empty[kNK], k_peer[kNK];
   uint64_t v_full[kNV], v_empty[kNV], v_ready[kNV];
   uint64_t s_full, s_free, p_full, pv_done;
@@ -99,16 +97,13 @@ struct SlidingSmem {
   uint32_t tmem_base;
   int abort_flag;
 };
-static_assert(2 * kQChunk <= kKStage, "Q dims 0-127 must fit in one K stage");
-constexpr size_t kSlidingSmemBytes = sizeof(SlidingSmem) + 1024;
+constexpr size_t kSlidingSmemBytes = sizeof(SlidingSmem);   // the base must be 1024-aligned (checked)
 static_assert(kSlidingSmemBytes <= 232448, "sliding prefill exceeds the 227 KB shared-memory limit");
 
 // One unit as one CTA of its pair sees it.
 struct Unit {
-  int g, h, t, p_lo, p_hi, ctx_end, k_lo, k_hi, kt0, n_tiles, q_row0, qpos;
+  int g, h, t, p_lo, p_hi, ctx_end, k_lo, k_hi, kt0, n_tiles, q_row0;
   const int32_t* pt;
-  // K ring slot of key tile j, counting from the unit's first slot (its Q takes slot qpos)
-  __device__ int kslot(int j) const { return j + (j >= qpos ? 1 : 0); }
 };
 
 // Warp-wide. False when unit u holds no rows (its slot is past the last query tile) or its
@@ -150,7 +145,6 @@ __device__ __noinline__ bool sliding_unit(const PrefillParams& p, int u, uint32_
   o.kt0 = o.k_lo / kSN;
   o.n_tiles = o.k_hi / kSN - o.kt0 + 1;
   o.pt = p.page_table + (size_t)(p.rows.pt_row ? __ldg(p.rows.pt_row + b) : b) * p.max_pages;
-  o.qpos = min(kQAfter, o.n_tiles);
   return true;
 }
 
@@ -158,8 +152,14 @@ template <bool kSpan, bool kRope>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     prefill_sliding_kernel(const __grid_constant__ CUtensorMap tmap_q, PrefillParams p) {
   extern __shared__ uint8_t smem_raw[];
-  SlidingSmem& sm =
-      *reinterpret_cast<SlidingSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // The Q buffers are 128B-swizzled tiles and want 1024-byte alignment, which the dynamic shared
+  // memory of a kernel without static shared memory has; a launch without it is refused
+  // (G4_ERR_DEVICE) before any barrier exists. There is no room for an alignment pad.
+  if (smem_u32(smem_raw) & 1023u) {
+    if (threadIdx.x == 0) set_error(p.err, kErrPage | kErrPos);
+    return;
+  }
+  SlidingSmem& sm = *reinterpret_cast<SlidingSmem*>(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();   // which query head of the KV head's pair
   const uint32_t peer = rank ^ 1u;
@@ -186,7 +186,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(&sm.q_pair, kPairWarps);   // even CTA: both CTAs' Q is in place
     mbar_init(&sm.q_free, 1);            // the unit's last QK^T is done: Q may be replaced
     mbar_init(&sm.o_free, kPairWarps);   // even CTA: both CTAs have read O out
-    mbar_init(&sm.q_read, kSmxWarps);    // this CTA's softmax warps have read the Q slot
+    mbar_init(&sm.q_read, kSmxWarps);    // this CTA's softmax warps have moved Q dims 0-127 out of qlo
     mbar_init(&sm.q_rot, kSmxWarps);     // kRope: this CTA's softmax warps have rotated Q
     for (int i = 0; i < 4; ++i) mbar_init(&sm.xchg[i], 2);
     mbar_init(&sm.teardown, 2);          // on an abort both issuers commit
@@ -209,7 +209,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     else
       mbar_arrive_remote(map_peer(smem_u32(bar), 0u));
   };
-  uint32_t k_slots = 0, v_slots = 0;   // ring slots used (warp 0 keeps both for the teardown)
+  uint32_t k_slots = 0, v_slots = 0, q_units = 0;   // ring slots used, units (warp 0 keeps them for the teardown)
 
   if (warp == 0 || warp == 6) {
     // ------------------------------------------------------------ copy producers
@@ -238,6 +238,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (jt >= o.n_tiles) return kNoPage;
       return page_raw((o.kt0 + jt) * kSN + (lane & 7) * kPage, o.k_lo, o.k_hi, o.pt);
     };
+    // Q tiles (warp 0): unit u's dims 0-127 into qlo and dims 128-255 into qhi[u & 1], all four
+    // boxes of 64 dims x 128 rows (rows outside T read as 0) counted on q_full. Unit 0's goes
+    // first; unit u + 1's right after unit u's second K tile (its first, for a unit of one tile),
+    // once unit u's Q has left qlo for tensor memory (q_read). qhi[(u + 1) & 1] was last read by
+    // unit u - 1's QK^T, which are done by then: the move of unit u's Q waited for them. So the
+    // tile lands while unit u runs, and its rotation can start as soon as the softmax warps are
+    // done with unit u.
+    auto issue_q = [&](const Unit& o, int uo) {   // lane 0
+      mbar_arrive_expect_tx(&sm.q_full, 4 * kQChunk);
+#pragma unroll
+      for (int c2 = 0; c2 < kSD / 64; ++c2)
+        tma_load_3d(c2 < 2 ? sm.qlo + c2 * kQChunk : sm.qhi[uo & 1] + (c2 - 2) * kQChunk, &tmap_q, 64 * c2, o.h,
+                    o.q_row0, &sm.q_full);
+    };
     // The next unit is looked up, and the page-table entries of its first two groups of tiles
     // loaded, once the current unit's first slot is issued: at the unit boundary nothing waits
     // for memory, and the lookup does not delay the first copy.
@@ -245,6 +259,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     Unit un;
     bool have = next_valid(u, un);
     int raw0 = have ? raw_blocks(un, 0) : kNoPage, raw1 = have ? raw_blocks(un, 4) : kNoPage;
+    if (!is_v && have) {
+      if (lane == 0) issue_q(un, 0);
+      q_issued = 1;
+    }
     while (ok && have) {
       int u2 = u + n_clusters;
       Unit nx;
@@ -255,64 +273,51 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       };
       int blk_cur = page_check(raw0, p.num_pages, p.hkv, un.g, p.err);
       int blk_next = page_check(raw1, p.num_pages, p.hkv, un.g, p.err);
-      const int n_slots = is_v ? un.n_tiles : un.n_tiles + 1;
-      for (int idx = 0; idx < n_slots; ++idx, ++c) {
+      for (int j = 0; j < un.n_tiles; ++j, ++c) {   // key tile j of the unit
         const int s = c % n_st;
-        const bool is_q = !is_v && idx == un.qpos;
-        const int j = (is_v || idx < un.qpos) ? idx : idx - 1;   // key tile of a K/V slot
-        int my_blk = -1;
-        if (!is_q) {
-          if (j > 0 && (j & 3) == 0) {
-            blk_cur = blk_next;
-            blk_next = load_blocks(j + 4);
-          }
-          my_blk = __shfl_sync(0xffffffffu, blk_cur, (j & 3) * 8 + (pg & 7));
+        if (j > 0 && (j & 3) == 0) {
+          blk_cur = blk_next;
+          blk_next = load_blocks(j + 4);
         }
-        const unsigned live = __ballot_sync(0xffffffffu, !is_q && mine && my_blk >= 0);
+        const int my_blk = __shfl_sync(0xffffffffu, blk_cur, (j & 3) * 8 + (pg & 7));
+        const unsigned live = __ballot_sync(0xffffffffu, mine && my_blk >= 0);
         bool okw = true;
-        if (lane == 0) {
-          if (c >= (uint32_t)n_st) okw = mbar_wait_ool(&empty[s], ((c / n_st) - 1) & 1, abort_flag, p.err, p.wait_ns);
-          // the unit's Q replaces the previous unit's only once that unit's last QK^T is done
-          if (okw && is_q && uq > 0) okw = mbar_wait_ool(&sm.q_free, (uq - 1) & 1, abort_flag, p.err, p.wait_ns);
-        }
+        if (lane == 0 && c >= (uint32_t)n_st)
+          okw = mbar_wait_ool(&empty[s], ((c / n_st) - 1) & 1, abort_flag, p.err, p.wait_ns);
         if (!__shfl_sync(0xffffffffu, okw, 0)) {
           ok = false;
           break;
         }
-        if (is_q) {
-          if (lane == 0) {   // 4 boxes of 64 dims x 128 rows (rows outside T read as 0)
-            mbar_arrive_expect_tx(&full[s], 2 * kQChunk);
-            mbar_arrive_expect_tx(&sm.q_full, 2 * kQChunk);
-#pragma unroll
-            for (int c2 = 0; c2 < kSD / 64; ++c2)
-              tma_load_3d(c2 < 2 ? sm.k[s] + c2 * kQChunk : sm.qhi + (c2 - 2) * kQChunk, &tmap_q, 64 * c2, un.h,
-                          un.q_row0, c2 < 2 ? &full[s] : &sm.q_full);
-          }
-          ++q_issued;
-        } else {
-          if (lane == 0) mbar_arrive_expect_tx(&full[s], __popc(live) * (is_v ? kVHalfPageBytes : kPageBytes));
-          __syncwarp();
-          if (mine && my_blk >= 0) {
-            if (is_v)   // dims 128r .. 128r+127 of page pg: key groups 2pg, 2pg+1
-              bulk_g2s(sm.v[s] + pg * kVHalfPageBytes,
-                       (const __nv_bfloat16*)p.v_cache + (size_t)my_blk * kPage * kSD + rank * (kVHalfPageBytes / 2),
-                       kVHalfPageBytes, &full[s]);
-            else
-              bulk_g2s(sm.k[s] + (lane & 3) * kPageBytes,
-                       (const __nv_bfloat16*)p.k_cache + (size_t)my_blk * kPage * kSD, kPageBytes, &full[s]);
-          }
+        if (lane == 0) mbar_arrive_expect_tx(&full[s], __popc(live) * (is_v ? kVHalfPageBytes : kPageBytes));
+        __syncwarp();
+        if (mine && my_blk >= 0) {
+          if (is_v)   // dims 128r .. 128r+127 of page pg: key groups 2pg, 2pg+1
+            bulk_g2s(sm.v[s] + pg * kVHalfPageBytes,
+                     (const __nv_bfloat16*)p.v_cache + (size_t)my_blk * kPage * kSD + rank * (kVHalfPageBytes / 2),
+                     kVHalfPageBytes, &full[s]);
+          else
+            bulk_g2s(sm.k[s] + (lane & 3) * kPageBytes,
+                     (const __nv_bfloat16*)p.k_cache + (size_t)my_blk * kPage * kSD, kPageBytes, &full[s]);
         }
         __syncwarp();
-        if (idx == 0) {
+        if (j == 0) {
           have_n = next_valid(u2, nx);
-          if (!is_v && have_n && lane == 0) {   // the next unit's roped Q tile into L2, a unit ahead of its load
-#pragma unroll
-            for (int c2 = 0; c2 < kSD / 64; ++c2) tma_prefetch_l2_3d(&tmap_q, 64 * c2, nx.h, max(nx.q_row0, 0));
-          }
           if (have_n) {
             nraw0 = raw_blocks(nx, 0);
             nraw1 = raw_blocks(nx, 4);
           }
+        }
+        if (!is_v && have_n && j == min(1, un.n_tiles - 1)) {   // the next unit's Q (see issue_q)
+          bool okq = true;
+          if (lane == 0) {
+            okq = mbar_wait_ool(&sm.q_read, uq & 1, abort_flag, p.err, p.wait_ns);
+            if (okq) issue_q(nx, uq + 1);
+          }
+          if (!__shfl_sync(0xffffffffu, okq, 0)) {
+            ok = false;
+            break;
+          }
+          ++q_issued;
         }
       }
       if (!is_v) vt += un.n_tiles;
@@ -337,6 +342,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     __syncwarp();
     k_slots = c;
     v_slots = vt;
+    q_units = (uint32_t)uq;
   } else if (warp == 1 && !leader) {
     // ------------------------------------------------------------ K relay (odd CTA)
     uint32_t c = 0;
@@ -344,7 +350,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int u = cluster; ok && u < p.n_units; u += n_clusters) {
       Unit un;
       if (!sliding_unit<kSpan>(p, u, rank, un)) continue;
-      for (int idx = 0; idx <= un.n_tiles; ++idx, ++c) {   // every slot, the unit's Q included
+      for (int idx = 0; idx < un.n_tiles; ++idx, ++c) {   // every K ring slot
         const int s = c % kNK;
         ok = __all_sync(0xffffffffu, mbar_wait_ool(&sm.k_full[s], (c / kNK) & 1, abort_flag, p.err, p.wait_ns));
         if (!ok) break;
@@ -368,10 +374,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int u = cluster; ok && u < p.n_units; u += n_clusters) {
       Unit un;
       if (!sliding_unit<kSpan>(p, u, rank, un)) continue;
-      // the unit's Q: its slot has landed, and both CTAs' softmax warps have moved dims 0-127
-      ok = __all_sync(0xffffffffu, slot_ready(c0 + un.qpos) && mbar_wait_cl_ool(&sm.q_pair, uq & 1, abort_flag, p.err, p.wait_ns));
+      // the unit's Q: both CTAs' softmax warps have rotated it and moved dims 0-127
+      ok = __all_sync(0xffffffffu, mbar_wait_cl_ool(&sm.q_pair, uq & 1, abort_flag, p.err, p.wait_ns));
       for (int j = 0; ok && j < un.n_tiles; ++j, ++jt) {
-        const uint32_t c = c0 + un.kslot(j);
+        const uint32_t c = c0 + j;
         const int s = c % kNK;
         // the single S buffer: both CTAs' softmax threads have read the previous S into registers
         ok = __all_sync(0xffffffffu,
@@ -380,7 +386,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc_fence_after();
         if (lane == 0) {
           const uint32_t ka = smem_u32(sm.k[s]);
-          const uint32_t qh = smem_u32(sm.qhi);
+          const uint32_t qh = smem_u32(sm.qhi[uq & 1]);
 #pragma unroll
           for (int k = 0; k < 8; ++k)   // dims 0-127: Q from tensor memory
             mma2_ts(tm + kTmS, tm + kTmQ + 8 * k, desc_tiled(ka + k * 256, 128, kKeyGroupBytes), kIdescQK,
@@ -397,7 +403,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!ok) break;
       if (lane == 0) mma2_commit_mc(&sm.q_free, kBoth);   // done with this unit's Q once these QK^T are
       __syncwarp();
-      c0 += un.n_tiles + 1;
+      c0 += un.n_tiles;
       ++uq;
     }
   } else if (warp == 7) {
@@ -465,7 +471,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t tq = tm + tmem_lane_base(warp);
     uint64_t* const xb = &sm.xchg[warp & 3];
     const float cl2 = p.scale_log2;
-    uint32_t c0 = 0, jt = 0, xph = 0;   // xph: exchanges of this row quarter so far
+    uint32_t jt = 0, xph = 0;   // xph: exchanges of this row quarter so far
     int uq = 0, u = cluster - n_clusters;
     bool ok = true;
     auto next_unit = [&](Unit& o) -> bool {   // this cluster's next unit with rows (warp-wide)
@@ -486,29 +492,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ++xph;
       return true;
     };
-    // Q dims 0-127 of unit o (the tile the producer put in K ring slot c0o + qpos, 128B swizzle)
-    // into tensor memory as bf16 pairs: the A operand of half of the QK^T k-steps; with kRope the
-    // tile is rotated first (dims 128-255 in place in shared memory). The load was issued only
-    // after the previous unit's last QK^T, so the columns and the shared-memory half are free.
-    // Each warp moves dims 64 hc .. +63 of its rows. Once all eight warps have read the slot, one
-    // thread releases it.
-    auto move_q = [&](const Unit& o, uint32_t c0o, int uqo) -> bool {
-      const uint32_t cq = c0o + o.qpos;
-      const int s = cq % kNK;
-      if (!__all_sync(0xffffffffu, mbar_wait_ool(&sm.k_full[s], (cq / kNK) & 1, abort_flag, p.err, p.wait_ns) &&
-                                       mbar_wait_ool(&sm.q_full, uqo & 1, abort_flag, p.err, p.wait_ns)))
-        return false;
-      const uint8_t* qrow = sm.k[s] + r * 128;
+    // Unit o's Q (dims 0-127 in qlo, dims 128-255 in qhi[uqo & 1], 128B swizzle; copied while the
+    // unit before ran): with kRope rotated in place first, then dims 0-127 into tensor memory as
+    // bf16 pairs, the A operand of half of the QK^T k-steps, once the unit before's QK^T are all
+    // done with the columns. Each warp moves dims 64 hc .. +63 of its rows; q_read tells the Q
+    // copier that qlo is free again.
+    auto move_q = [&](const Unit& o, int uqo) -> bool {
+      if (!__all_sync(0xffffffffu, mbar_wait_ool(&sm.q_full, uqo & 1, abort_flag, p.err, p.wait_ns))) return false;
+      const uint8_t* qrow = sm.qlo + r * 128;
       if constexpr (kRope) {
         // softmax thread i rotates pair i % 128 of rows 64 (i / 128) .. +63
         const int t = sidx & 127;
-        rotate_q_pair<4, kSlidingR>(sm.k[s] + (t >> 6) * kQChunk, sm.qhi + (t >> 6) * kQChunk, p.tb, t, kBM * o.t,
-                                    64 * (sidx >> 7));
-        fence_proxy_async();   // QK^T reads the rewritten half, and the ring slot is refilled, by the async proxy
+        rotate_q_pair<4, kSlidingR>(sm.qlo + (t >> 6) * kQChunk, sm.qhi[uqo & 1] + (t >> 6) * kQChunk, p.tb, t,
+                                    kBM * o.t, 64 * (sidx >> 7));
+        fence_proxy_async();   // QK^T reads the rewritten dims 128-255 through the async proxy
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.q_rot);
         if (!__all_sync(0xffffffffu, mbar_wait_ool(&sm.q_rot, uqo & 1, abort_flag, p.err, p.wait_ns))) return false;
       }
+      if (uqo > 0 && !__all_sync(0xffffffffu, mbar_wait_ool(&sm.q_free, (uqo - 1) & 1, abort_flag, p.err, p.wait_ns)))
+        return false;
+      tc_fence_after();
       {
         uint32_t w[32];
 #pragma unroll
@@ -523,24 +527,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       tmem_st_wait();
       tc_fence_before();
+      fence_proxy_async();   // qlo is next written by the Q copy (async proxy), after these reads
       __syncwarp();
       if (lane == 0) {
         arrive_leader(&sm.q_pair);
         mbar_arrive(&sm.q_read);
       }
-      bool okr = true;
-      if (threadIdx.x == 64) {
-        okr = mbar_wait_ool(&sm.q_read, uqo & 1, abort_flag, p.err, p.wait_ns);
-        if (okr) mbar_arrive(&sm.k_empty[s]);
-      }
-      return __shfl_sync(0xffffffffu, okr, 0);
+      return true;
     };
 
     // The unit after the current one is looked up at the start of the current one, while the
     // softmax waits for its first scores, so that moving its Q never waits for the lookup.
     Unit cur, nxt;
     bool have = next_unit(cur);
-    if (have) ok = move_q(cur, c0, uq);
+    if (have) ok = move_q(cur, uq);
     bool have_n = have && next_unit(nxt);
     constexpr int kHN = kSN / 2;   // keys of one half
     while (ok && have) {
@@ -650,8 +650,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
       // The next unit's Q goes into tensor memory now (this unit's QK^T are all done), so that
       // its first QK^T runs while this unit's O is written out.
-      const uint32_t c0n = c0 + cur.n_tiles + 1;
-      if (have_n && !move_q(nxt, c0n, uq + 1)) {
+      if (have_n && !move_q(nxt, uq + 1)) {
         ok = false;
         break;
       }
@@ -685,7 +684,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           w16[c] = pack_bf16(__uint_as_float(o[2 * c]) * inv, __uint_as_float(o[2 * c + 1]) * inv);
         store_rows32<kSD>(w16, p.out, wrow0, p.hq, cur.h, (kSD / 2) * hc + 32 * cc, valid, lane);
       }
-      c0 = c0n;
       ++uq;
       cur = nxt;
       have = have_n;
@@ -716,7 +714,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         while (!mbar_try_wait(smem_u32(&sm.v_empty[s]), (last / kNV) & 1u) && globaltimer() - w0 < kWaitLimitNs) {
         }
       }
-      const uint32_t units = k_slots - v_slots;   // each unit takes one K ring slot more than V
+      const uint32_t units = q_units;
       if (units > 0) {
         while (!mbar_try_wait(smem_u32(&sm.q_free), (units - 1) & 1u) && globaltimer() - w0 < kWaitLimitNs) {
         }

@@ -1,15 +1,17 @@
 """The barrier protocol of the sliding prefill kernel (csrc/g4_prefill.cu), modelled on the CPU.
 
-A persistent 2-CTA cluster walks its units in order. Per CTA: warp 0 copies K tiles and each
-unit's roped Q (dims 0-127 into the K ring slot after the unit's first tile, dims 128-255 into
-their own buffer, once the previous unit's last QK^T is done); warp 6 copies V; warp 1 issues
-QK^T (even CTA) or relays ring landings (odd CTA); warp 7 checks V and issues P.V (even CTA);
-eight softmax warps, two per row quarter (one per half of the columns), move Q into tensor
-memory, run the softmax, write P and the epilogue, and meet their row partner on a barrier of
-their quarter once per key tile (the row max) and once per unit (the sums). The model keeps the
-kernel's barriers, counts and phase arithmetic, and checks at every MMA and every read that the
-buffer holds the expected tile or unit: K slots, the Q buffers, the single S and P buffers in
-tensor memory, the V stages, O and the partner's posted half.
+A persistent 2-CTA cluster walks its units in order. Per CTA: warp 0 copies K tiles into a
+two-stage ring and each unit's roped Q into its own buffers: dims 0-127 into a staging buffer,
+dims 128-255 into one of two buffers by unit parity; unit 0's at the start, unit u + 1's after
+unit u's second key tile, once unit u's Q has left the staging buffer. Warp 6 copies V; warp 1
+issues QK^T (even CTA) or relays ring landings (odd CTA); warp 7 checks V and issues P.V (even
+CTA); eight softmax warps, two per row quarter (one per half of the columns), rotate Q in shared
+memory (meeting on a barrier), move dims 0-127 into tensor memory, run the softmax, write P and
+the epilogue, and meet their row partner on a barrier of their quarter once per key tile (the
+row max) and once per unit (the sums). The model keeps the kernel's barriers, counts and phase
+arithmetic, and checks at every MMA and every read that the buffer holds the expected tile or
+unit: K slots, the Q buffers, tensor-memory Q, the single S and P buffers, the V stages, O and
+the partner's posted half.
 
 The random unit sequences are lists of key-tile counts; a planted mistake (a wait removed) must
 make the model fail."""
@@ -19,7 +21,7 @@ import pytest
 
 from protocol_sim import Bar, Err, Role, Sim
 
-NK, NV, QAFTER = 2, 2, 1
+NK, NV = 2, 2
 SMX = 8   # softmax warps per CTA: two per row quarter (w and w + 4 here), one per column half
 
 
@@ -38,25 +40,25 @@ def model(seed, units, mut=""):
             d[f"v_empty{s}"] = Bar(f"C{X}.v_empty{s}", 1)
             d[f"v_ready{s}"] = Bar(f"C{X}.v_ready{s}", 1)
         for nm, cnt in (("s_full", 1), ("s_free", 2 * SMX), ("p_full", 2 * SMX), ("pv_done", 1), ("q_full", 1),
-                        ("q_pair", 2 * SMX), ("q_free", 1), ("o_free", 2 * SMX), ("q_read", SMX)):
+                        ("q_pair", 2 * SMX), ("q_free", 1), ("o_free", 2 * SMX), ("q_read", SMX), ("q_rot", SMX)):
             d[nm] = Bar(f"C{X}.{nm}", cnt)
         for q in range(4):
             d[f"xchg{q}"] = Bar(f"C{X}.xchg{q}", 2)
         B[X] = d
-    qpos = [min(QAFTER, n) for n in units]
-    def kslot(ui, j):
-        return j + (1 if j >= qpos[ui] else 0)
     c0s = [0]
     for n in units:
-        c0s.append(c0s[-1] + n + 1)
+        c0s.append(c0s[-1] + n)
     jt0s = [0]
     for n in units:
         jt0s.append(jt0s[-1] + n)
     # data state
-    kring = {X: [None] * NK for X in (0, 1)}       # ("K", jt) or ("Q", ui) landed
+    kring = {X: [None] * NK for X in (0, 1)}       # ("K", jt) landed
     kpend = {X: [0] * NK for X in (0, 1)}          # issued, not yet released
-    qhi = {X: None for X in (0, 1)}
-    tq = {X: None for X in (0, 1)}                 # unit whose Q dims 0-127 are in tensor memory
+    qlo = {X: None for X in (0, 1)}                # unit whose Q dims 0-127 sit in the staging buffer
+    qhi = {X: [None, None] for X in (0, 1)}        # unit whose Q dims 128-255 sit in qhi[0], qhi[1]
+    qlo_read = {X: {} for X in (0, 1)}             # unit -> softmax warps that moved their share of qlo
+    rots = {X: {} for X in (0, 1)}                 # unit -> softmax warps that rotated their share
+    tq = {X: [None] * SMX for X in (0, 1)}         # unit whose Q dims 0-127 each warp's share of tensor memory holds
     sbuf = {X: None for X in (0, 1)}
     sreads = {X: 0 for X in (0, 1)}
     pbuf = {X: None for X in (0, 1)}
@@ -70,39 +72,41 @@ def model(seed, units, mut=""):
         if not c:
             raise Err(m)
     def producer_k(X):
+        def issue_q(ui):
+            chk(ui == 0 or qlo_read[X].get(ui - 1, 0) == SMX, f"C{X} Q of unit {ui} over qlo not yet moved")
+            chk(qk_done_unit["last"] >= ui - 2, f"C{X} Q of unit {ui} over qhi{ui & 1} still read by unit {ui - 2}'s QK")
+            qlo[X] = None
+            qhi[X][ui & 1] = None
+            B[X]["q_full"].expect_tx(S, 2)
+            def land_ql(X=X, ui=ui):
+                qlo[X] = ui
+                B[X]["q_full"].complete_tx(S, 1)
+            def land_qh(X=X, ui=ui):
+                qhi[X][ui & 1] = ui
+                B[X]["q_full"].complete_tx(S, 1)
+            S.later(land_ql, 2, 10)
+            S.later(land_qh, 2, 10)
+        if units:
+            issue_q(0)
         for ui, n in enumerate(units):
-            for idx in range(n + 1):
-                c = c0s[ui] + idx
+            for j in range(n):
+                c = c0s[ui] + j
                 s = c % NK
-                is_q = idx == qpos[ui]
-                j = idx if idx < qpos[ui] else idx - 1
                 if c >= NK:
                     yield ("wait", B[X][f"k_empty{s}"], c // NK - 1)
-                if is_q and ui > 0 and mut != "no_qfree":
-                    yield ("wait", B[X]["q_free"], ui - 1)
                 chk(kpend[X][s] == 0, f"C{X} slot {s} reloaded before release")
                 kpend[X][s] = 1
                 kring[X][s] = None
-                if is_q:
-                    chk(qk_done_unit["last"] >= ui - 1, f"C{X} Q of unit {ui} over qhi still read by unit {ui-1}'s QK")
-                    B[X][f"k_full{s}"].expect_tx(S, 1)
-                    B[X]["q_full"].expect_tx(S, 1)
-                    qhi[X] = None
-                    def land_ql(X=X, s=s, ui=ui):
-                        kring[X][s] = ("Q", ui)
-                        B[X][f"k_full{s}"].complete_tx(S, 1)
-                    def land_qh(X=X, ui=ui):
-                        qhi[X] = ui
-                        B[X]["q_full"].complete_tx(S, 1)
-                    S.later(land_ql, 2, 10)
-                    S.later(land_qh, 2, 10)
-                else:
-                    jt = jt0s[ui] + j
-                    B[X][f"k_full{s}"].expect_tx(S, 1)
-                    def land_k(X=X, s=s, jt=jt):
-                        kring[X][s] = ("K", jt)
-                        B[X][f"k_full{s}"].complete_tx(S, 1)
-                    S.later(land_k, 2, 10)
+                jt = jt0s[ui] + j
+                B[X][f"k_full{s}"].expect_tx(S, 1)
+                def land_k(X=X, s=s, jt=jt):
+                    kring[X][s] = ("K", jt)
+                    B[X][f"k_full{s}"].complete_tx(S, 1)
+                S.later(land_k, 2, 10)
+                if ui + 1 < len(units) and j == min(1, n - 1):   # the next unit's Q
+                    if mut != "no_qread":
+                        yield ("wait", B[X]["q_read"], ui)
+                    issue_q(ui + 1)
     def producer_v(X):
         vc = 0
         for ui, n in enumerate(units):
@@ -119,20 +123,17 @@ def model(seed, units, mut=""):
                 vc += 1
     def relay():
         for ui, n in enumerate(units):
-            for idx in range(n + 1):
+            for idx in range(n):
                 c = c0s[ui] + idx
                 s = c % NK
                 yield ("wait", B[1][f"k_full{s}"], c // NK)
                 B[0][f"k_peer{s}"].arrive(S)
     def issuer():
         for ui, n in enumerate(units):
-            cq = c0s[ui] + qpos[ui]
-            yield ("wait", B[0][f"k_full{cq % NK}"], cq // NK)
-            yield ("wait", B[0][f"k_peer{cq % NK}"], cq // NK)
             yield ("wait", B[0]["q_pair"], ui)
             for j in range(n):
                 jt = jt0s[ui] + j
-                c = c0s[ui] + kslot(ui, j)
+                c = c0s[ui] + j
                 s = c % NK
                 yield ("wait", B[0][f"k_full{s}"], c // NK)
                 yield ("wait", B[0][f"k_peer{s}"], c // NK)
@@ -141,8 +142,8 @@ def model(seed, units, mut=""):
                 def mma(s=s, jt=jt, ui=ui):
                     for X in (0, 1):
                         chk(kring[X][s] == ("K", jt), f"QK {jt}: C{X} slot {s} holds {kring[X][s]}")
-                        chk(tq[X] == ui, f"QK {jt}: C{X} TMEM Q holds unit {tq[X]}")
-                        chk(qhi[X] == ui, f"QK {jt}: C{X} qhi holds unit {qhi[X]}")
+                        chk(all(q == ui for q in tq[X]), f"QK {jt}: C{X} TMEM Q holds units {tq[X]}")
+                        chk(qhi[X][ui & 1] == ui, f"QK {jt}: C{X} qhi{ui & 1} holds unit {qhi[X][ui & 1]}")
                         chk(sbuf[X] is None, f"QK {jt}: C{X} S still holds {sbuf[X]}")
                         sbuf[X] = jt
                         sreads[X] = 0
@@ -203,21 +204,22 @@ def model(seed, units, mut=""):
             chk(xposted.get(key, 0) == 2, f"C{X}.w{w} reads its row partner's half of exchange {n} before it was posted")
             xn[0] += 1
         def move_q(ui):
-            cq = c0s[ui] + qpos[ui]
-            s = cq % NK
-            yield ("wait", B[X][f"k_full{s}"], cq // NK)
             yield ("wait", B[X]["q_full"], ui)
-            chk(kring[X][s] == ("Q", ui), f"C{X}.w{w} moves Q of unit {ui} from slot holding {kring[X][s]}")
-            tq[X] = ui
+            chk(qlo[X] == ui and qhi[X][ui & 1] == ui,
+                f"C{X}.w{w} rotates Q of unit {ui}: qlo holds {qlo[X]}, qhi{ui & 1} holds {qhi[X][ui & 1]}")
+            rots[X][ui] = rots[X].get(ui, 0) + 1
+            B[X]["q_rot"].arrive(S)
+            if mut != "no_qrot":
+                yield ("wait", B[X]["q_rot"], ui)
+            chk(rots[X].get(ui, 0) == SMX, f"C{X}.w{w} moves Q of unit {ui} before every warp rotated its share")
+            if ui > 0 and mut != "no_qfree":
+                yield ("wait", B[X]["q_free"], ui - 1)
+            chk(qk_done_unit["last"] >= ui - 1, f"C{X}.w{w} replaces tensor-memory Q while unit {ui - 1}'s QK^T read it")
+            chk(qlo[X] == ui, f"C{X}.w{w} moves Q of unit {ui}: qlo holds {qlo[X]}")
+            tq[X][w] = ui
+            qlo_read[X][ui] = qlo_read[X].get(ui, 0) + 1
             B[0]["q_pair"].arrive(S)
             B[X]["q_read"].arrive(S)
-            if w == 0:
-                if mut != "no_qread":
-                    yield ("wait", B[X]["q_read"], ui)
-                # the slot goes back to the ring only once all four warps have read it
-                chk(B[X]["q_read"].done >= ui + 1, f"C{X} Q slot released before all warps read it")
-                kpend[X][s] = 0
-                B[X][f"k_empty{s}"].arrive(S)
         if not units:
             return
         yield from move_q(0)
@@ -273,16 +275,31 @@ def run_many(n, mut="", base=5000):
 
 
 def test_sliding_protocol_has_no_deadlock_aliasing_or_hazard():
-    """300 random unit sequences (1 to 6 units of 1 to 10 key tiles, the Q slot at each position
-    it can take) run to the end with every check passing."""
+    """300 random unit sequences (1 to 6 units of 1 to 10 key tiles) run to the end with every
+    check passing."""
     failures = run_many(300)
     assert not failures, failures[:3]
 
 
-@pytest.mark.parametrize("mut", ["no_qfree", "no_sfree", "no_qread", "no_xchg"])
+def test_runs_of_single_tile_units():
+    """Units of one key tile in a row (a sequence's first query tiles): the next unit's Q copy
+    then follows the unit's only key tile."""
+    for seed in range(40):
+        model(seed, [1, 1, 1, 2, 1, 1, 3, 1])
+
+
+@pytest.mark.parametrize("mut", ["no_sfree", "no_qread", "no_xchg", "no_qrot"])
 def test_sliding_protocol_model_catches_a_missing_wait(mut):
     """Control: each of these waits guards a hazard the model can see, so removing it fails. (The
     P.V issuer's wait for O to be read out is implied as well by its wait for the next unit's
     first P: the same warps read O out before they write that P, so removing it alone cannot
     fail.)"""
     assert run_many(100, mut)
+
+
+def test_q_free_before_the_move_is_implied():
+    """The softmax warps wait for the earlier unit's QK^T to be done (q_free) before they write the
+    next unit's Q into tensor memory. The wait is kept as an explicit guard, but it is implied: the
+    same warps read the earlier unit's last S first, which lands only after its last QK^T (and the
+    QK^T of one issuer complete in order). So removing it is no hazard."""
+    assert not run_many(100, "no_qfree")
