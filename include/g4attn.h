@@ -65,6 +65,8 @@
  * outside [0, num_pages), a position >= 262144 or beyond the page table, a bad image span
  * (g4attn_prefill_vision), a bounded wait that ran out) set bits in a device error word, and the
  * affected work is skipped; read and clear the word with g4attn_status_sync. Kernels never trap.
+ * (The sliding prefill kernel also refuses, as G4_ERR_DEVICE, a launch whose dynamic shared
+ * memory does not start 1024-byte aligned; a kernel without static shared memory always does.)
  */
 #ifndef G4ATTN_H
 #define G4ATTN_H
